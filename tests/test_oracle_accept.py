@@ -1,0 +1,198 @@
+"""Pins of the oracle accept step, Philox and the own exp.
+
+* Philox4x32-10 against the Random123 known-answer vectors (golden file);
+* the own exp against math.exp within 2 ulp, with exp(0) == 1 exactly;
+* argmax ties and NaN, greedy special cases by hand;
+* the integer-mass transform against a float softmax and a brute-force top-p;
+* rejection sampling: T = 0 equals greedy, p == q accepts everything, the
+  committed-token marginals pass a chi-square test against p (the defining
+  property of Leviathan/Chen sampling) and the mean accepted length matches
+  the closed form sum_j prod_{i<j} alpha_i, alpha_i = sum_x min(p_i, q_i).
+"""
+import math
+
+import numpy as np
+import pytest
+from scipy import stats
+
+import oracle
+from conftest import golden_lines
+
+
+def test_philox_known_answers():
+    rows = list(golden_lines("philox4x32_10_kat.txt"))
+    assert len(rows) == 3
+    for r in rows:
+        v = [int(x, 16) for x in r]
+        out = oracle.philox4x32_10(v[0:4], v[4:6])
+        assert list(out) == v[6:10]
+
+
+def _ulp_err(got, ref):
+    ulp = math.ulp(np.float32(ref)) if ref != 0 else 2.0 ** -149
+    return abs(got - ref) / float(np.spacing(np.float32(ref)))
+
+
+def test_own_exp_accuracy_and_special_points():
+    assert oracle.own_exp(0.0) == 1.0
+    assert oracle.own_exp(-0.0) == 1.0
+    assert oracle.own_exp(-32.5) == 0.0
+    assert oracle.own_exp(float("nan")) == 0.0
+    g = np.random.default_rng(5)
+    xs = np.concatenate([-g.random(20000) * 32.0, -g.random(5000) * 1e-3,
+                         -np.arange(0, 32.0, 0.125)]).astype(np.float32)
+    worst = 0.0
+    for x in xs:
+        got = oracle.own_exp(float(x))
+        ref = math.exp(float(x))
+        worst = max(worst, _ulp_err(got, ref))
+    assert worst <= 2.0, worst
+    # monotone on a sorted sample
+    xs = np.sort(xs)
+    vals = [oracle.own_exp(float(x)) for x in xs]
+    assert all(a <= b for a, b in zip(vals, vals[1:]))
+
+
+def test_argmax_ties_and_nan():
+    assert oracle.argmax_f32(np.array([1, 3, 3, 2], np.float32)) == 1
+    assert oracle.argmax_f32(np.array([np.nan, 0.5, 0.5], np.float32)) == 1
+    assert oracle.argmax_f32(np.array([np.nan, np.nan], np.float32)) == 0
+    assert oracle.argmax_f32(np.array([-np.inf, np.nan, -np.inf], np.float32)) == 0
+    assert oracle.argmax_f32(np.array([-1, np.inf, np.inf], np.float32)) == 1
+
+
+def _one_hot_rows(ids, V):
+    rows = np.zeros((len(ids), V), np.float32)
+    for i, t in enumerate(ids):
+        rows[i, t] = 5.0
+    return rows
+
+
+def test_greedy_cases():
+    V = 11
+    tgt = _one_hot_rows([4, 7, 2, 9], V)[None]           # argmaxes 4, 7, 2, 9
+    # all three drafts match: len = 4, bonus = 9
+    tok, ln, bad = oracle.accept_greedy(tgt, np.array([[4, 7, 2]]))
+    assert ln[0] == 4 and list(tok[0]) == [4, 7, 2, 9] and bad == 0
+    # first mismatch at i = 1: commit draft 0 then the target's 7
+    tok, ln, _ = oracle.accept_greedy(tgt, np.array([[4, 1, 2]]))
+    assert ln[0] == 2 and list(tok[0]) == [4, 7, -1, -1]
+    # mismatch at 0
+    tok, ln, _ = oracle.accept_greedy(tgt, np.array([[0, 7, 2]]))
+    assert ln[0] == 1 and list(tok[0]) == [4, -1, -1, -1]
+    # out of range id is a rejection
+    tok, ln, bad = oracle.accept_greedy(tgt, np.array([[4, 99, 2]]))
+    assert ln[0] == 2 and list(tok[0]) == [4, 7, -1, -1] and bad == 1
+    # Kd = 0 returns the argmax
+    tok, ln, _ = oracle.accept_greedy(tgt[:, :1], np.zeros((1, 0), np.int32))
+    assert ln[0] == 1 and list(tok[0]) == [4]
+
+
+def test_row_mass_against_float_softmax_and_brute_force_top_p():
+    g = np.random.default_rng(7)
+    for trial in range(30):
+        V = int(g.integers(2, 40))
+        lg = (g.standard_normal(V) * 3).astype(np.float32)
+        T, top_p = 0.6, float(g.choice([0.5, 0.8, 0.95, 1.0]))
+        W, S = oracle.row_mass(lg, T, top_p)
+        full, Sf = oracle.row_mass(lg, T, 1.0)
+        assert int(full.max()) == 2 ** 40
+        p = np.exp((lg.astype(np.float64) - lg.max()) / T)
+        assert np.allclose(full.astype(np.float64) / 2.0 ** 40, p, rtol=2e-6, atol=2.0 ** -40)
+        # brute-force top-p on the integer masses: shortest prefix in
+        # (W desc, index asc) order with cum * 2^32 >= P * S_full
+        P = oracle.top_p_fixed(top_p)
+        order = sorted(range(V), key=lambda v: (-int(full[v]), v))
+        if P >= 2 ** 32:
+            keep = set(range(V))
+        else:
+            cum, keep = 0, set()
+            for v in order:
+                cum += int(full[v])
+                keep.add(v)
+                if cum * 2 ** 32 >= P * Sf:
+                    break
+        for v in range(V):
+            assert int(W[v]) == (int(full[v]) if v in keep else 0)
+        assert S == sum(int(full[v]) for v in keep)
+
+
+def test_rejection_t0_is_greedy():
+    g = np.random.default_rng(8)
+    B, Kd, V = 20, 4, 50
+    tgt = g.standard_normal((B, Kd + 1, V)).astype(np.float32)
+    drf = g.standard_normal((B, Kd, V)).astype(np.float32)
+    am = tgt.argmax(axis=2)
+    drafts = np.where(g.random((B, Kd)) < 0.7, am[:, :Kd], g.integers(0, V, (B, Kd))).astype(np.int32)
+    t1, l1, _ = oracle.accept_rejection(tgt, drf, drafts, 0.0, 0.95, 1, 0)
+    t2, l2, _ = oracle.accept_greedy(tgt, drafts)
+    assert np.array_equal(t1, t2) and np.array_equal(l1, l2)
+
+
+def test_rejection_p_equals_q_accepts_everything():
+    g = np.random.default_rng(9)
+    B, Kd, V = 64, 5, 30
+    tgt = (g.standard_normal((B, Kd + 1, V)) * 3).astype(np.float32)
+    drf = tgt[:, :Kd].copy()
+    drafts = oracle.sample_drafts(drf, 0.6, 0.95, 11, 1 << 32)
+    tok, ln, bad = oracle.accept_rejection(tgt, drf, drafts, 0.6, 0.95, 11, 0)
+    assert bad == 0 and np.all(ln == Kd + 1)
+    assert np.array_equal(tok[:, :Kd], drafts)
+
+
+def _dist(lg, T, top_p):
+    W, S = oracle.row_mass(lg, T, top_p)
+    return W.astype(np.float64) / S
+
+
+CHI_N = 1_000_000
+
+
+@pytest.fixture(scope="module")
+def sixteen_token_case():
+    g = np.random.default_rng(12)
+    V, Kd = 16, 3
+    tgt = (g.standard_normal((Kd + 1, V)) * 3).astype(np.float32)
+    drf = (tgt[:Kd] + g.standard_normal((Kd, V))).astype(np.float32)
+    drafts = oracle.sample_drafts(drf, 0.6, 0.95, 13, 1 << 32, broadcast_rows=True, B=CHI_N)
+    tok, ln, bad = oracle.accept_rejection(tgt, drf, drafts, 0.6, 0.95, 13, 0,
+                                           broadcast_rows=True, B=CHI_N)
+    assert bad == 0
+    return tgt, drf, drafts, tok, ln
+
+
+def _chi2_against(counts, probs):
+    nz = probs > 0
+    assert counts[~nz].sum() == 0, "a token excluded by top-p was committed"
+    exp = probs[nz] * counts.sum()
+    return stats.chisquare(counts[nz], exp).pvalue
+
+
+def test_first_token_marginal_matches_target(sixteen_token_case):
+    tgt, drf, drafts, tok, ln = sixteen_token_case
+    p0 = _dist(tgt[0], 0.6, 0.95)
+    counts = np.bincount(tok[:, 0], minlength=16)
+    assert _chi2_against(counts, p0) > 1e-4
+
+
+def test_second_token_given_first_accepted_matches_target(sixteen_token_case):
+    tgt, drf, drafts, tok, ln = sixteen_token_case
+    sel = ln >= 2                     # position 0 was accepted (token 0 == draft 0)
+    assert np.array_equal(tok[sel, 0], drafts[sel, 0])
+    p1 = _dist(tgt[1], 0.6, 0.95)
+    counts = np.bincount(tok[sel, 1], minlength=16)
+    assert _chi2_against(counts, p1) > 1e-4
+
+
+def test_mean_accepted_length_matches_closed_form(sixteen_token_case):
+    tgt, drf, drafts, tok, ln = sixteen_token_case
+    Kd = drf.shape[0]
+    alpha = [np.minimum(_dist(tgt[i], 0.6, 0.95), _dist(drf[i], 0.6, 0.95)).sum()
+             for i in range(Kd)]
+    # P(n >= j) = prod_{i<j} alpha_i
+    probs = [np.prod(alpha[:j]) for j in range(1, Kd + 1)]
+    mean = sum(probs)
+    # variance of n = sum_j P(n>=j) (2j - 1) - mean^2
+    var = sum(pr * (2 * j - 1) for j, pr in enumerate(probs, start=1)) - mean ** 2
+    got = float(np.mean(ln - 1))
+    assert abs(got - mean) <= 4 * math.sqrt(var / len(ln)), (got, mean)
