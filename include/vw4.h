@@ -1,0 +1,263 @@
+/*
+ * vw4.h -- C ABI of the GB300 (sm_103a) library for the hot path of
+ * multi-token-prediction speculative decoding verification with 4-bit
+ * weights: the skinny verify GEMM, its MoE expert-gather variant, and the
+ * on-GPU accept step (greedy longest-prefix match; rejection sampling with
+ * residual correction).
+ *
+ * Conventions for every entry point
+ *  - Pointers named *_dev are device pointers owned by the caller; nothing is
+ *    copied and nothing is freed.  The library never allocates device memory
+ *    in a call: scratch comes from the caller's workspace (sized by
+ *    vw4_workspace_bytes) or is not needed.
+ *  - `stream` is a cudaStream_t (0 = the legacy default stream).  Every call
+ *    is asynchronous on it; no call synchronizes except vw4_get_device_status.
+ *  - Argument errors are detected on the host, before anything is launched,
+ *    and returned as a vw4_status; nothing is written in that case.  A launch
+ *    failure returns VW4_ERR_CUDA (the CUDA error string is available from
+ *    vw4_last_error_string).  Conditions that only the device can see (an
+ *    out-of-range draft id, an expert id out of range, a pipeline wait that
+ *    ran out) set bits of a device status word that vw4_get_device_status
+ *    reads and clears; kernels never trap.
+ *  - Alignment: weight and scale base pointers must be 16-byte aligned (they
+ *    are read by TMA); activations and outputs need only their natural
+ *    alignment; lda and ldo are counted in elements.
+ *
+ * Formats (the pages name nvfp4 and Q4 without defining the bits; these are
+ * the standard definitions):
+ *  - nvfp4: q = u8 [N][K/2], element k of a row in byte k/2, the even element
+ *    in the LOW nibble; each nibble is FP4 E2M1 (OCP MX v1.0: s e1 e0 m).
+ *    scales = E4M3 (OCP fp8 "fn") [N][K/16], one per 16 consecutive k of a
+ *    row; tensor_scale = one fp32 factor for the whole matrix.
+ *    w[n][k] = e2m1(nibble) * e4m3(scale[n][k/16]) * tensor_scale.
+ *  - Q4_0: q = u8 [N][K/2] and scales = fp16 [N][K/32] (one per 32-element
+ *    block); in block b of a row, byte j (0..15) of the block holds element
+ *    32b+j in its low nibble and element 32b+j+16 in its high nibble.
+ *    w[n][k] = (nibble - 8) * scale[n][k/32].  tensor_scale must be 1.
+ *  - Activations are bf16 [M][lda] row-major; outputs fp32 [rows][ldo].
+ */
+#ifndef VW4_H
+#define VW4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(_WIN32)
+#define VW4_API __declspec(dllexport)
+#else
+#define VW4_API __attribute__((visibility("default")))
+#endif
+
+typedef enum { VW4_FMT_NVFP4 = 1, VW4_FMT_Q4_0 = 2 } vw4_fmt;
+
+typedef enum {
+    VW4_OK = 0,
+    VW4_ERR_INVALID_ARG = 1,   /* null pointer, size or enum out of range       */
+    VW4_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement   */
+    VW4_ERR_ALIGN = 3,         /* a pointer or leading dimension is misaligned  */
+    VW4_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed             */
+    VW4_ERR_TIMEOUT = 5,       /* reported by vw4_get_device_status bits only   */
+    VW4_ERR_WORKSPACE = 6      /* workspace missing or smaller than required    */
+} vw4_status;
+
+/* Bits of the device status word (vw4_get_device_status). */
+#define VW4_DEV_BAD_DRAFT_ID   0x1u  /* a draft id outside [0, V): treated as a rejection */
+#define VW4_DEV_BAD_EXPERT_ID  0x2u  /* an expert id outside [0, E): that pair is skipped  */
+#define VW4_DEV_WAIT_TIMEOUT   0x4u  /* a pipeline wait gave up; outputs are incomplete    */
+#define VW4_DEV_ZERO_RESIDUAL  0x8u  /* a forced rejection met p == q: drew from p instead */
+
+/* A block-quantized weight matrix [N][K] (see the format notes above). */
+typedef struct vw4_weight {
+    int32_t fmt;            /* vw4_fmt                                         */
+    int32_t N;              /* output features (rows of the stored matrix)     */
+    int32_t K;              /* reduction length (K % 16 == 0 nvfp4, % 32 Q4_0) */
+    int32_t reserved;       /* must be 0                                       */
+    const void* q_dev;      /* packed nibbles, u8 [N][K/2]                     */
+    const void* scales_dev; /* nvfp4: e4m3 [N][K/16]; Q4_0: fp16 [N][K/32]     */
+    float tensor_scale;     /* nvfp4 global factor; exactly 1.0f for Q4_0      */
+    float reserved_f;       /* must be 0                                       */
+} vw4_weight;
+
+/* Sampling parameters of the accept step. */
+typedef struct vw4_sampling {
+    float temperature;      /* 0 routes to the greedy rule (no random numbers)  */
+    float top_p;            /* (0, 1]; >= 1 keeps the whole vocabulary         */
+    int32_t top_k;          /* 0 = off (other values: VW4_ERR_UNSUPPORTED)     */
+    float min_p;            /* 0 = off (other values: VW4_ERR_UNSUPPORTED)     */
+} vw4_sampling;
+
+/* Operation ids for vw4_workspace_bytes. */
+#define VW4_OP_GEMM       1
+#define VW4_OP_MOE        2
+#define VW4_OP_REJECTION  3
+
+/*
+ * verify_gemm_w4 -- the verification pass's skinny matmul.
+ *
+ * Defined by: "Faster Gemma 4 on MLX with multi-token prediction", the
+ * paragraph on where verification time goes: a verify batch of usually 2 to 8
+ * token rows multiplied by block-quantized (nvfp4) weights, each weight block
+ * read and unpacked once and reused across the batch, with computation
+ * identical to the per-row product; and the Qiita roofline article on MTP in
+ * llama.cpp, PART 2 section 2-3 (verify turns the matrix-vector product into a
+ * thin matrix product over the same weight bytes).
+ *
+ *   out[m][n] = sum_k A[m][k] * w[n][k]       m < M, n < N        (fp32 result)
+ *
+ * W           weight descriptor (host pointer to the struct; device data).
+ * A_dev       bf16 [M][lda], lda >= K.
+ * M           1..8 verify rows.
+ * out_dev     fp32 [M][ldo], ldo >= N.
+ * row_argmax_dev  optional (NULL = skip): int32 [M]; row m receives the index
+ *             of its largest output (ties to the lowest index; NaN never
+ *             wins), computed in the same launch from the fp32 results.
+ * workspace_dev / ws_bytes  scratch of at least
+ *             vw4_workspace_bytes(VW4_OP_GEMM, M, N, K) bytes, 256-byte
+ *             aligned, reused freely between calls on the same stream.
+ * Error behaviour: VW4_ERR_INVALID_ARG for null pointers, M outside 1..8,
+ * N < 1, K not a positive multiple of the block, lda < K, ldo < N;
+ * VW4_ERR_ALIGN for misaligned pointers or leading dimensions;
+ * VW4_ERR_WORKSPACE when the workspace is too small.
+ */
+VW4_API vw4_status verify_gemm_w4(const vw4_weight* W, const void* A_dev, int M, int lda,
+                                  float* out_dev, int ldo, int32_t* row_argmax_dev,
+                                  void* workspace_dev, size_t ws_bytes, void* stream);
+
+/*
+ * verify_moe_w4 -- segmented expert-gather verify GEMM for MoE heads.
+ *
+ * Defined by: Ollama commit log for x/mlxrunner/mtp.go, paragraph on the
+ * batched head forward (the segmented gather path for MoE heads), and the
+ * Qiita article PART 3 section on expert scattering (verify rows route to
+ * different experts, so each touched expert's weights are read once for the
+ * rows that chose it).
+ *
+ * experts     weight descriptor of ALL experts stacked: N = rows per expert,
+ *             q_dev = u8 [E][N][K/2], scales_dev = [E][N][K/16] (or /32).
+ * E           number of experts.
+ * A_dev, lda  bf16 activation rows: M token rows (rows_are_pairs == 0) or
+ *             M*topk pair rows, pair p = m*topk + j (rows_are_pairs == 1).
+ * expert_ids_dev  int32 [M][topk] routed experts, distinct within a token.
+ * gates_dev   fp32 [M][topk] (read only when combine == 1).
+ * M           1..8 tokens; topk 1..8.
+ * combine     0: out[p][n] for every pair p (out has M*topk rows);
+ *             1: out[m][n] = sum_j gates[m][j] * pair(m, j)[n], j ascending.
+ * Each touched expert streams its weights once for all its pair rows.
+ * Error behaviour as verify_gemm_w4; an expert id outside [0, E) sets
+ * VW4_DEV_BAD_EXPERT_ID and that pair contributes zeros.
+ */
+VW4_API vw4_status verify_moe_w4(const vw4_weight* experts, int E, const void* A_dev, int lda,
+                                 int rows_are_pairs, const int32_t* expert_ids_dev,
+                                 const float* gates_dev, int M, int topk, int combine,
+                                 float* out_dev, int ldo, void* workspace_dev, size_t ws_bytes,
+                                 void* stream);
+
+/*
+ * accept_greedy -- longest-prefix argmax match.
+ *
+ * Defined by: "Accelerating Gemini Nano models on Pixel with frozen
+ * Multi-Token Prediction", section 3 (the longest prefix matching what the
+ * backbone itself would produce is accepted); the Qiita article PART 2
+ * section 2-4 (the target's token at the first mismatch is always committed);
+ * the mtp.go commit log paragraph "Greedy is a special case of sampled
+ * decoding" (temperature 0 is a point mass, acceptance is argmax match).
+ *
+ * target_logits_dev  fp32 [B][Kd+1][V].  May be NULL when target_argmax_dev
+ *             is given.
+ * drafts_dev  int32 [B][Kd] drafted ids.
+ * target_argmax_dev  optional int32 [B][Kd+1] precomputed argmaxes (e.g. the
+ *             row_argmax of verify_gemm_w4); NULL = computed here from the
+ *             logits (ties to the lowest index, NaN never wins).
+ * B >= 1, 0 <= Kd <= 8, V >= 1.
+ * tokens_dev  int32 [B][Kd+1]: drafts[0..n-1], then the target's token at
+ *             position n, then -1; len_dev int32 [B] = n + 1 in [1, Kd+1].
+ *             tokens_dev is also used as scratch inside the call.
+ * An out-of-range draft id never matches and sets VW4_DEV_BAD_DRAFT_ID.
+ */
+VW4_API vw4_status accept_greedy(const float* target_logits_dev, const int32_t* drafts_dev,
+                                 const int32_t* target_argmax_dev, int B, int Kd, int V,
+                                 int32_t* tokens_dev, int32_t* len_dev, void* stream);
+
+/*
+ * accept_rejection -- rejection sampling with residual correction.
+ *
+ * Defined by: "Your model may already ship a speculative decoder", section
+ * "Why it is interesting on a Mac specifically" (Leviathan and Chen rejection
+ * sampling with residual correction reproduces plain decoding at temperature
+ * 0.6, top_p 0.95); the mtp.go commit log paragraphs "Greedy is a special case
+ * of sampled decoding" and "rework the MLX sampler" (pipeline temperature /
+ * softmax -> top-p -> normalize -> categorical; acceptance, residual and bonus
+ * draws reuse the same draft and target distributions; seeded, reproducible).
+ *
+ * Exact integer form (identical on the oracle, so ids are bit-exact): each
+ * row's weights W_v = floor(exp_own((l_v - max l) * (1/T)) * 2^40); top-p
+ * keeps the shortest prefix in (W desc, index asc) order whose mass satisfies
+ * cum * 2^32 >= round(top_p * 2^32) * sum W.  Philox4x32-10 block for draft
+ * position i of sequence b: counter (i, b, offset lo, offset hi), key = seed;
+ * U = r0 >> 8 decides acceptance (U * q(x) * Sp < 2^24 * p(x) * Sq), and the
+ * 64-bit r2:r1 draws the residual max(0, p*Sq - q*Sp) at the first rejection
+ * or the bonus from p_Kd (block (Kd, b)) when all drafts are accepted.
+ *
+ * target_logits_dev  fp32 [B][Kd+1][V]; draft_logits_dev fp32 [B][Kd][V]
+ *             (may be NULL when Kd == 0); drafts_dev int32 [B][Kd].
+ * B >= 1, 0 <= Kd <= 8, 1 <= V <= 393216 (the row is held on chip by a
+ *             cluster of up to 8 CTAs; larger V returns VW4_ERR_UNSUPPORTED).
+ * params      temperature >= 0 (0 = greedy rule, no random numbers drawn),
+ *             top_p in (0, 1], top_k == 0, min_p == 0.
+ * seed, offset  Philox key and counter offset.
+ * tokens_dev, len_dev  as accept_greedy.
+ * workspace_dev / ws_bytes  at least vw4_workspace_bytes(VW4_OP_REJECTION, B, Kd, V).
+ */
+VW4_API vw4_status accept_rejection(const float* target_logits_dev, const float* draft_logits_dev,
+                                    const int32_t* drafts_dev, int B, int Kd, int V,
+                                    const vw4_sampling* params, uint64_t seed, uint64_t offset,
+                                    int32_t* tokens_dev, int32_t* len_dev, void* workspace_dev,
+                                    size_t ws_bytes, void* stream);
+
+/* Workspace bytes needed by an operation:
+ *   VW4_OP_GEMM:      (M, N, K)
+ *   VW4_OP_MOE:       (M*topk, N, K)   -- pass the number of routed pairs first
+ *   VW4_OP_REJECTION: (B, Kd, V)
+ * Returns 0 for an unknown op or invalid sizes. */
+VW4_API size_t vw4_workspace_bytes(int op, int a, int b, int c);
+
+/* Reads the device status word of the current device, ORs it into *bits and
+ * clears it.  Synchronizes `stream` first. */
+VW4_API vw4_status vw4_get_device_status(uint32_t* bits, void* stream);
+
+/* Converts Q4_0 blocks stored as 18-byte records (fp16 d, then 16 bytes of
+ * nibbles) [N][K/32] into the split layout used here (q [N][K/2], d [N][K/32]).
+ * Device pointers; asynchronous on `stream`. */
+VW4_API vw4_status vw4_q4_0_from_blocks(const void* blocks_dev, int N, int K, void* q_dev,
+                                        void* d_dev, void* stream);
+
+/* The sampler's own fp32 exp, applied elementwise: y[i] = exp(x[i]) for x in
+ * [-32, 0], 0 below -32 or for NaN.  This is the exact function the
+ * accept_rejection masses use (a Cody-Waite reduction and a degree-7 Taylor
+ * polynomial with explicit fmas), exposed so that it can be checked bit for
+ * bit against an independent implementation.  Device pointers. */
+VW4_API vw4_status vw4_own_exp(const float* x_dev, float* y_dev, int64_t n, void* stream);
+
+/* Human-readable name of a status code (static string). */
+VW4_API const char* vw4_status_str(vw4_status s);
+
+/* Text of the last CUDA error seen by this thread in a library call. */
+VW4_API const char* vw4_last_error_string(void);
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+VW4_API int vw4_version(void);
+
+/* Test hook: upper bound, in nanoseconds, of every pipeline wait inside the
+ * kernels (default 2e9).  A wait that runs out sets VW4_DEV_WAIT_TIMEOUT and
+ * the kernel returns early with its copies drained.  0 restores the default. */
+VW4_API void vw4_set_wait_limit_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VW4_H */

@@ -69,9 +69,10 @@ def _load():
         "oracle_own_exp": (f32, [f32]),
         "oracle_row_mass": (u64, [P, i64, f32, u64, P]),
         "oracle_accept_rejection": (ctypes.c_int, [P, i64, P, i64, P, ctypes.c_int, ctypes.c_int,
-                                                   i64, f32, f32, u64, u64, P, P]),
+                                                   i64, f32, f32, u64, u64, u32, P, P]),
         "oracle_sample_drafts": (None, [P, i64, ctypes.c_int, ctypes.c_int, i64, f32, f32, u64,
-                                        u64, P]),
+                                        u64, u32, P]),
+        "oracle_own_exp_array": (None, [P, P, i64]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -188,6 +189,13 @@ def own_exp(x: float) -> float:
     return float(_load().oracle_own_exp(float(x)))
 
 
+def own_exp_array(x: np.ndarray) -> np.ndarray:
+    x = _c(x, np.float32)
+    y = np.empty_like(x)
+    _load().oracle_own_exp_array(_ptr(x), _ptr(y), x.size)
+    return y
+
+
 def top_p_fixed(top_p: float) -> int:
     """P = round(top_p * 2^32), saturating at 2^32 (keep everything)."""
     pd = float(np.float32(top_p)) * 4294967296.0
@@ -204,9 +212,11 @@ def row_mass(logits, temperature: float, top_p: float):
 
 
 def accept_rejection(target, draft, drafts, temperature: float, top_p: float, seed: int,
-                     offset: int, broadcast_rows: bool = False, B: int | None = None):
+                     offset: int, broadcast_rows: bool = False, B: int | None = None,
+                     b_base: int = 0):
     """target f32 [B, Kd+1, V], draft f32 [B, Kd, V] (or one shared [Kd+1, V] / [Kd, V]
-    pair reused by every sequence when broadcast_rows=True, with B given)."""
+    pair reused by every sequence when broadcast_rows=True, with B given).  Sequence b
+    draws from Philox counter index b_base + b."""
     target = _c(target, np.float32)
     draft = _c(draft, np.float32)
     if broadcast_rows:
@@ -225,12 +235,13 @@ def accept_rejection(target, draft, drafts, temperature: float, top_p: float, se
     ln = np.empty(B, np.int32)
     bad = _load().oracle_accept_rejection(_ptr(target), ld_tb, _ptr(draft), ld_db, _ptr(drafts),
                                           B, Kd, V, float(temperature), float(top_p),
-                                          int(seed), int(offset), _ptr(tokens), _ptr(ln))
+                                          int(seed), int(offset), int(b_base), _ptr(tokens),
+                                          _ptr(ln))
     return tokens, ln, bad
 
 
 def sample_drafts(draft, temperature: float, top_p: float, seed: int, offset: int,
-                  broadcast_rows: bool = False, B: int | None = None):
+                  broadcast_rows: bool = False, B: int | None = None, b_base: int = 0):
     draft = _c(draft, np.float32)
     if broadcast_rows:
         Kd, V = draft.shape
@@ -241,5 +252,5 @@ def sample_drafts(draft, temperature: float, top_p: float, seed: int, offset: in
         ld = Kd * V
     out = np.empty((B, Kd), np.int32)
     _load().oracle_sample_drafts(_ptr(draft), ld, B, Kd, V, float(temperature), float(top_p),
-                                 int(seed), int(offset), _ptr(out))
+                                 int(seed), int(offset), int(b_base), _ptr(out))
     return out

@@ -332,6 +332,11 @@ ORACLE_API float oracle_own_exp(float x) {
     return p * two_n;
 }
 
+ORACLE_API void oracle_own_exp_array(const float* x, float* y, int64_t n) {
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) y[i] = oracle_own_exp(x[i]);
+}
+
 /* ------------------------------------------------- integer-mass sampler */
 /*
  * Temperature / softmax / top-p / normalize, made exact with integers:
@@ -424,12 +429,15 @@ static int64_t categorical_u64(const uint64_t* W, int64_t V, uint64_t total, uin
  * same block (if every r_v is 0, draw from p instead).  If all Kd are
  * accepted, draw the bonus from p_Kd with U64 of block (Kd, b).
  * temperature == 0 routes to the greedy rule and draws nothing.
+ * Sequence b of this call uses Philox counter index b_base + b (so a slice of
+ * a batch can be checked on its own).
  * Returns the number of out-of-range draft ids (counted as rejections).
  */
 ORACLE_API int oracle_accept_rejection(const float* target, int64_t ld_tb, const float* draft,
                                        int64_t ld_db, const int32_t* drafts, int B, int Kd,
                                        int64_t V, float temperature, float top_p, uint64_t seed,
-                                       uint64_t offset, int32_t* tokens, int32_t* len) {
+                                       uint64_t offset, uint32_t b_base, int32_t* tokens,
+                                       int32_t* len) {
     if (temperature == 0.0f)
         return oracle_accept_greedy(target, ld_tb, drafts, B, Kd, V, tokens, len);
     float invT = (float)(1.0 / (double)temperature);
@@ -449,7 +457,7 @@ ORACLE_API int oracle_accept_rejection(const float* target, int64_t ld_tb, const
             uint64_t Sq = oracle_row_mass(db + (int64_t)i * V, V, invT, P, Wq);
             int32_t x = drafts[(int64_t)b * Kd + i];
             uint32_t rr[4];
-            philox_at(seed, offset, (uint32_t)i, (uint32_t)b, rr);
+            philox_at(seed, offset, (uint32_t)i, b_base + (uint32_t)b, rr);
             uint64_t U = rr[0] >> 8;
             uint64_t u64 = ((uint64_t)rr[2] << 32) | rr[1];
             int ok = 0;
@@ -474,7 +482,7 @@ ORACLE_API int oracle_accept_rejection(const float* target, int64_t ld_tb, const
         if (n == Kd) {
             uint64_t Sp = oracle_row_mass(tb + (int64_t)Kd * V, V, invT, P, Wp);
             uint32_t rr[4];
-            philox_at(seed, offset, (uint32_t)Kd, (uint32_t)b, rr);
+            philox_at(seed, offset, (uint32_t)Kd, b_base + (uint32_t)b, rr);
             uint64_t u64 = ((uint64_t)rr[2] << 32) | rr[1];
             last = categorical_u64(Wp, V, Sp, u64);
         }
@@ -500,7 +508,7 @@ ORACLE_API int oracle_accept_rejection(const float* target, int64_t ld_tb, const
  */
 ORACLE_API void oracle_sample_drafts(const float* draft, int64_t ld_db, int B, int Kd, int64_t V,
                                      float temperature, float top_p, uint64_t seed,
-                                     uint64_t offset, int32_t* drafts) {
+                                     uint64_t offset, uint32_t b_base, int32_t* drafts) {
     float invT = (float)(1.0 / (double)temperature);
     double pd = (double)top_p * 4294967296.0;
     uint64_t P = (pd >= 4294967296.0) ? ((uint64_t)1 << 32) : (uint64_t)llround(pd);
@@ -509,7 +517,7 @@ ORACLE_API void oracle_sample_drafts(const float* draft, int64_t ld_db, int B, i
         for (int i = 0; i < Kd; ++i) {
             uint64_t Sq = oracle_row_mass(draft + (int64_t)b * ld_db + (int64_t)i * V, V, invT, P, Wq);
             uint32_t rr[4];
-            philox_at(seed, offset, (uint32_t)i, (uint32_t)b, rr);
+            philox_at(seed, offset, (uint32_t)i, b_base + (uint32_t)b, rr);
             uint64_t u64 = ((uint64_t)rr[2] << 32) | rr[1];
             drafts[(int64_t)b * Kd + i] = (int32_t)categorical_u64(Wq, V, Sq, u64);
         }

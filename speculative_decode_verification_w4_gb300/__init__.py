@@ -1,0 +1,277 @@
+"""speculative_decode_verification_w4_gb300 -- Python binding of the vw4 C ABI.
+
+A thin ctypes layer over ``libvw4.so`` (see ``include/vw4.h``): it marshals
+torch tensors into device pointers and sizes, and turns status codes into
+exceptions.  Every step of the computation runs in the library's CUDA kernels;
+there is no fallback.  If the library is missing or cannot be loaded, every
+call raises.
+
+Entry points (same names as the C ABI):
+  verify_gemm_w4, verify_moe_w4, accept_greedy, accept_rejection,
+  vw4_workspace_bytes, vw4_get_device_status, vw4_q4_0_from_blocks,
+  vw4_set_wait_limit_ns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libvw4.so")
+
+FMT_NVFP4 = 1
+FMT_Q4_0 = 2
+OP_GEMM = 1
+OP_MOE = 2
+OP_REJECTION = 3
+
+DEV_BAD_DRAFT_ID = 0x1
+DEV_BAD_EXPERT_ID = 0x2
+DEV_WAIT_TIMEOUT = 0x4
+DEV_ZERO_RESIDUAL = 0x8
+
+STATUS_NAMES = {0: "VW4_OK", 1: "VW4_ERR_INVALID_ARG", 2: "VW4_ERR_UNSUPPORTED",
+                3: "VW4_ERR_ALIGN", 4: "VW4_ERR_CUDA", 5: "VW4_ERR_TIMEOUT",
+                6: "VW4_ERR_WORKSPACE"}
+
+# the exported C symbols (checked against include/vw4.h by the tests)
+EXPORTS = ("verify_gemm_w4", "verify_moe_w4", "accept_greedy", "accept_rejection",
+           "vw4_workspace_bytes", "vw4_get_device_status", "vw4_q4_0_from_blocks",
+           "vw4_status_str", "vw4_last_error_string", "vw4_version", "vw4_set_wait_limit_ns",
+           "vw4_own_exp")
+
+
+class VW4Error(RuntimeError):
+    def __init__(self, code: int, where: str, detail: str = ""):
+        self.code = code
+        msg = f"{where}: {STATUS_NAMES.get(code, code)}"
+        if detail:
+            msg += f" ({detail})"
+        super().__init__(msg)
+
+
+class Weight(ctypes.Structure):
+    _fields_ = [("fmt", ctypes.c_int32), ("N", ctypes.c_int32), ("K", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("q_dev", ctypes.c_void_p),
+                ("scales_dev", ctypes.c_void_p), ("tensor_scale", ctypes.c_float),
+                ("reserved_f", ctypes.c_float)]
+
+
+class Sampling(ctypes.Structure):
+    _fields_ = [("temperature", ctypes.c_float), ("top_p", ctypes.c_float),
+                ("top_k", ctypes.c_int32), ("min_p", ctypes.c_float)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load_library(path: str = LIB_PATH):
+    """Loads libvw4.so and declares the C signatures.  Raises if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise ImportError(f"libvw4.so not built at {path}: run "
+                              "`python -m speculative_decode_verification_w4_gb300.build`")
+        lib = ctypes.CDLL(path)
+        P, I, U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64
+        sigs = {
+            "verify_gemm_w4": (I, [ctypes.POINTER(Weight), P, I, I, P, I, P, P, ctypes.c_size_t, P]),
+            "verify_moe_w4": (I, [ctypes.POINTER(Weight), I, P, I, I, P, P, I, I, I, P, I, P,
+                                  ctypes.c_size_t, P]),
+            "accept_greedy": (I, [P, P, P, I, I, I, P, P, P]),
+            "accept_rejection": (I, [P, P, P, I, I, I, ctypes.POINTER(Sampling), U64, U64, P, P,
+                                     P, ctypes.c_size_t, P]),
+            "vw4_workspace_bytes": (ctypes.c_size_t, [I, I, I, I]),
+            "vw4_get_device_status": (I, [ctypes.POINTER(ctypes.c_uint32), P]),
+            "vw4_q4_0_from_blocks": (I, [P, I, I, P, P, P]),
+            "vw4_status_str": (ctypes.c_char_p, [I]),
+            "vw4_last_error_string": (ctypes.c_char_p, []),
+            "vw4_version": (I, []),
+            "vw4_set_wait_limit_ns": (None, [U64]),
+            "vw4_own_exp": (I, [P, P, ctypes.c_int64, P]),
+        }
+        for name, (res, args) in sigs.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        detail = ""
+        if code == 4:
+            detail = load_library().vw4_last_error_string().decode(errors="replace")
+        raise VW4Error(code, where, detail)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def vw4_workspace_bytes(op: int, a: int, b: int, c: int) -> int:
+    return int(load_library().vw4_workspace_bytes(op, a, b, c))
+
+
+class Workspace:
+    """A growable device scratch buffer (256-byte aligned torch allocation)."""
+
+    def __init__(self, device=None):
+        self.device = torch.device(device or "cuda")
+        self.buf = None
+
+    def get(self, nbytes: int) -> torch.Tensor:
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+_default_ws = {}
+
+
+def _workspace(ws, nbytes, device):
+    if ws is None:
+        key = (device.index, threading.get_ident())
+        ws = _default_ws.setdefault(key, Workspace(device))
+    if isinstance(ws, Workspace):
+        return ws.get(nbytes)
+    if ws.numel() * ws.element_size() < nbytes:
+        raise VW4Error(6, "workspace", f"need {nbytes} bytes")
+    return ws
+
+
+def make_weight(fmt: int, q: torch.Tensor, scales: torch.Tensor, tensor_scale: float = 1.0,
+                N: int | None = None, K: int | None = None) -> Weight:
+    if N is None:
+        N = q.shape[-2] if q.dim() >= 2 else 1
+    if K is None:
+        K = q.shape[-1] * 2
+    return Weight(fmt, int(N), int(K), 0, q.data_ptr(), scales.data_ptr(), float(tensor_scale), 0.0)
+
+
+def verify_gemm_w4(fmt: int, q: torch.Tensor, scales: torch.Tensor, tensor_scale: float,
+                   A: torch.Tensor, out: torch.Tensor | None = None,
+                   row_argmax: torch.Tensor | None = None, workspace=None, stream=None):
+    """out[M, N] (fp32) = A[M, K] (bf16) x w[N, K]^T; q u8 [N, K/2]; see vw4.h."""
+    N, K = q.shape[0], q.shape[1] * 2
+    M = A.shape[0]
+    if A.dtype != torch.bfloat16:
+        raise ValueError("A must be bfloat16")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    W = make_weight(fmt, q, scales, tensor_scale, N, K)
+    need = vw4_workspace_bytes(OP_GEMM, M, N, K)
+    ws = _workspace(workspace, need, A.device)
+    code = load_library().verify_gemm_w4(ctypes.byref(W), _ptr(A), M, A.stride(0), _ptr(out),
+                                         out.stride(0), _ptr(row_argmax), _ptr(ws),
+                                         ws.numel(), _stream(stream))
+    _check(code, "verify_gemm_w4")
+    return out
+
+
+def verify_moe_w4(fmt: int, q: torch.Tensor, scales: torch.Tensor, tensor_scale: float, E: int,
+                  A: torch.Tensor, rows_are_pairs: int, expert_ids: torch.Tensor,
+                  gates: torch.Tensor | None, combine: int, out: torch.Tensor | None = None,
+                  workspace=None, stream=None):
+    """q u8 [E, N, K/2] (or [E*N, K/2]); expert_ids int32 [M, topk]; see vw4.h."""
+    K = q.shape[-1] * 2
+    N = q.numel() // (K // 2) // E
+    M, topk = expert_ids.shape
+    rows = M if combine else M * topk
+    if out is None:
+        out = torch.empty((rows, N), dtype=torch.float32, device=A.device)
+    W = make_weight(fmt, q, scales, tensor_scale, N, K)
+    need = vw4_workspace_bytes(OP_MOE, M * topk, N, K)
+    ws = _workspace(workspace, need, A.device)
+    code = load_library().verify_moe_w4(ctypes.byref(W), E, _ptr(A), A.stride(0), rows_are_pairs,
+                                        _ptr(expert_ids), _ptr(gates), M, topk, combine,
+                                        _ptr(out), out.stride(0), _ptr(ws), ws.numel(),
+                                        _stream(stream))
+    _check(code, "verify_moe_w4")
+    return out
+
+
+def accept_greedy(target_logits: torch.Tensor | None, drafts: torch.Tensor,
+                  target_argmax: torch.Tensor | None = None, B: int | None = None,
+                  V: int | None = None, tokens=None, length=None, stream=None):
+    """target_logits f32 [B, Kd+1, V]; drafts int32 [B, Kd] -> (tokens [B, Kd+1], len [B])."""
+    if target_logits is not None:
+        B, R, V = target_logits.shape
+    Kd = drafts.shape[1]
+    dev = drafts.device
+    if tokens is None:
+        tokens = torch.empty((B, Kd + 1), dtype=torch.int32, device=dev)
+    if length is None:
+        length = torch.empty((B,), dtype=torch.int32, device=dev)
+    code = load_library().accept_greedy(_ptr(target_logits), _ptr(drafts), _ptr(target_argmax), B,
+                                        Kd, V, _ptr(tokens), _ptr(length), _stream(stream))
+    _check(code, "accept_greedy")
+    return tokens, length
+
+
+def accept_rejection(target_logits: torch.Tensor, draft_logits: torch.Tensor | None,
+                     drafts: torch.Tensor, temperature: float, top_p: float, seed: int,
+                     offset: int = 0, top_k: int = 0, min_p: float = 0.0, tokens=None,
+                     length=None, workspace=None, stream=None):
+    """Leviathan/Chen rejection accept; returns (tokens [B, Kd+1], len [B])."""
+    B, R, V = target_logits.shape
+    Kd = R - 1
+    dev = target_logits.device
+    if tokens is None:
+        tokens = torch.empty((B, Kd + 1), dtype=torch.int32, device=dev)
+    if length is None:
+        length = torch.empty((B,), dtype=torch.int32, device=dev)
+    prm = Sampling(float(temperature), float(top_p), int(top_k), float(min_p))
+    need = vw4_workspace_bytes(OP_REJECTION, B, Kd, V)
+    ws = _workspace(workspace, need, dev)
+    code = load_library().accept_rejection(_ptr(target_logits), _ptr(draft_logits), _ptr(drafts),
+                                           B, Kd, V, ctypes.byref(prm), int(seed), int(offset),
+                                           _ptr(tokens), _ptr(length), _ptr(ws), ws.numel(),
+                                           _stream(stream))
+    _check(code, "accept_rejection")
+    return tokens, length
+
+
+def vw4_get_device_status(stream=None) -> int:
+    bits = ctypes.c_uint32(0)
+    _check(load_library().vw4_get_device_status(ctypes.byref(bits), _stream(stream)),
+           "vw4_get_device_status")
+    return int(bits.value)
+
+
+def vw4_q4_0_from_blocks(blocks: torch.Tensor, N: int, K: int, stream=None):
+    q = torch.empty((N, K // 2), dtype=torch.uint8, device=blocks.device)
+    d = torch.empty((N, K // 32), dtype=torch.float16, device=blocks.device)
+    _check(load_library().vw4_q4_0_from_blocks(_ptr(blocks), N, K, _ptr(q), _ptr(d),
+                                               _stream(stream)), "vw4_q4_0_from_blocks")
+    return q, d
+
+
+def vw4_own_exp(x: torch.Tensor, out: torch.Tensor | None = None, stream=None):
+    """The accept step's own fp32 exp, elementwise on a float32 CUDA tensor."""
+    if out is None:
+        out = torch.empty_like(x)
+    _check(load_library().vw4_own_exp(_ptr(x), _ptr(out), x.numel(), _stream(stream)),
+           "vw4_own_exp")
+    return out
+
+
+def vw4_set_wait_limit_ns(ns: int):
+    load_library().vw4_set_wait_limit_ns(int(ns))

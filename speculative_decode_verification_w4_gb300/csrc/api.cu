@@ -1,0 +1,394 @@
+// api.cu -- the C ABI declared in include/vw4.h: host-side argument checks,
+// workspace carving, TMA tensor-map encoding and kernel launches.  No call
+// allocates device memory and none synchronizes (except the status read).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "vw4.h"
+#include "vw4_internal.cuh"
+
+namespace vw4 {
+
+// One status word per device.  Kernels OR bits into it; vw4_get_device_status
+// reads and clears it.
+__device__ uint32_t g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxGrid = 608;  // upper bound of the persistent GEMM grid (workspace sizing)
+
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0;
+    int occ[3] = {0, 0, 0};  // GEMM CTAs per SM by fmt
+    uint32_t* status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+unsigned long long g_wait_ns = 2000000000ull;
+thread_local std::string g_last_error;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+vw4_status cuda_fail(cudaError_t e, const char* where) {
+    g_last_error = std::string(where) + ": " + cudaGetErrorString(e);
+    return VW4_ERR_CUDA;
+}
+
+vw4_status device_info(DeviceInfo** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return VW4_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        d.occ[1] = gemm_blocks_per_sm(1);
+        d.occ[2] = gemm_blocks_per_sm(2);
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_status_word);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+        d.status = static_cast<uint32_t*>(p);
+        if (!g_encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q{};
+            e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q);
+            if (e != cudaSuccess || fn == nullptr || q != cudaDriverEntryPointSuccess)
+                return cuda_fail(e == cudaSuccess ? cudaErrorSymbolNotFound : e,
+                                 "cuTensorMapEncodeTiled entry point");
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+        d.ready = true;
+    }
+    *out = &d;
+    return VW4_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 2-D uint8 tensor map over a row-major [rows][inner_bytes] array.
+vw4_status make_map(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t rows,
+                    uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw) {
+    cuuint64_t dims[2] = {inner_bytes, rows};
+    cuuint64_t strides[1] = {inner_bytes};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char buf[128];
+        snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+        g_last_error = buf;
+        return VW4_ERR_CUDA;
+    }
+    return VW4_OK;
+}
+
+vw4_status check_weight(const vw4_weight* W) {
+    if (!W || !W->q_dev || !W->scales_dev) return VW4_ERR_INVALID_ARG;
+    if (W->fmt != VW4_FMT_NVFP4 && W->fmt != VW4_FMT_Q4_0) return VW4_ERR_INVALID_ARG;
+    if (W->reserved != 0 || W->reserved_f != 0.0f) return VW4_ERR_INVALID_ARG;
+    if (W->N < 1 || W->K < 1) return VW4_ERR_INVALID_ARG;
+    const int blk = W->fmt == VW4_FMT_NVFP4 ? 16 : 32;
+    if (W->K % blk != 0) return VW4_ERR_INVALID_ARG;
+    if (W->fmt == VW4_FMT_Q4_0 && W->tensor_scale != 1.0f) return VW4_ERR_INVALID_ARG;
+    if (!std::isfinite(W->tensor_scale)) return VW4_ERR_INVALID_ARG;
+    if (!aligned16(W->q_dev) || !aligned16(W->scales_dev)) return VW4_ERR_ALIGN;
+    // the TMA path streams 256-wide k slices with 16-byte-multiple row pitches
+    if (W->K % kStageK != 0) return VW4_ERR_UNSUPPORTED;
+    return VW4_OK;
+}
+
+}  // namespace
+}  // namespace vw4
+
+using namespace vw4;
+
+extern "C" {
+
+VW4_API int vw4_version(void) { return 100; }
+
+VW4_API const char* vw4_status_str(vw4_status s) {
+    switch (s) {
+        case VW4_OK: return "ok";
+        case VW4_ERR_INVALID_ARG: return "invalid argument";
+        case VW4_ERR_UNSUPPORTED: return "unsupported";
+        case VW4_ERR_ALIGN: return "misaligned pointer or leading dimension";
+        case VW4_ERR_CUDA: return "CUDA error";
+        case VW4_ERR_TIMEOUT: return "device wait timed out";
+        case VW4_ERR_WORKSPACE: return "workspace too small";
+    }
+    return "unknown status";
+}
+
+VW4_API const char* vw4_last_error_string(void) { return g_last_error.c_str(); }
+
+VW4_API void vw4_set_wait_limit_ns(uint64_t ns) {
+    g_wait_ns = ns == 0 ? 2000000000ull : static_cast<unsigned long long>(ns);
+}
+
+VW4_API size_t vw4_workspace_bytes(int op, int a, int b, int c) {
+    if (op == VW4_OP_GEMM) {
+        const int M = a, N = b, K = c;
+        if (M < 1 || M > kMaxRows || N < 1 || K < kStageK || K % kStageK) return 0;
+        return gemm_workspace_layout(nullptr, 1, N, K, kMaxGrid, 0).bytes;
+    }
+    if (op == VW4_OP_MOE) {
+        const int P = a, N = b, K = c;
+        if (P < 1 || P > kMaxSeg || N < 1 || K < kStageK || K % kStageK) return 0;
+        return gemm_workspace_layout(nullptr, P, N, K, kMaxGrid, P).bytes;
+    }
+    if (op == VW4_OP_REJECTION) {
+        if (a < 1 || b < 0 || b > 8 || c < 1) return 0;
+        return rejection_workspace_bytes(a, b, c);
+    }
+    return 0;
+}
+
+VW4_API vw4_status verify_gemm_w4(const vw4_weight* W, const void* A_dev, int M, int lda,
+                                  float* out_dev, int ldo, int32_t* row_argmax_dev,
+                                  void* workspace_dev, size_t ws_bytes, void* stream) {
+    vw4_status st = check_weight(W);
+    if (st != VW4_OK) return st;
+    if (!A_dev || !out_dev) return VW4_ERR_INVALID_ARG;
+    if (M < 1 || M > kMaxRows || lda < W->K || ldo < W->N) return VW4_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(A_dev) & 1u) || (reinterpret_cast<uintptr_t>(out_dev) & 3u))
+        return VW4_ERR_ALIGN;
+    if (!workspace_dev) return VW4_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace_dev) & 255u) != 0) return VW4_ERR_ALIGN;
+    const int N = W->N, K = W->K;
+    GemmWorkspace ws = gemm_workspace_layout(workspace_dev, 1, N, K, kMaxGrid, 0);
+    if (ws.bytes > ws_bytes) return VW4_ERR_WORKSPACE;
+    DeviceInfo* d = nullptr;
+    st = device_info(&d);
+    if (st != VW4_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    CUtensorMap tmW, tmS;
+    st = make_map(&tmW, W->q_dev, static_cast<uint64_t>(K) / 2, N, kStageK / 2, kTileRows,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != VW4_OK) return st;
+    st = make_map(&tmS, W->scales_dev, static_cast<uint64_t>(K) / 16, N, 16, kTileRows,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != VW4_OK) return st;
+
+    const int T = K / kStageK;
+    const int n_tiles = (N + kTileRows - 1) / kTileRows;
+    const long long U = static_cast<long long>(n_tiles) * T;
+    long long G = static_cast<long long>(d->sms) * d->occ[W->fmt];
+    if (G > kMaxGrid) G = kMaxGrid;
+    if (G > U) G = U;
+
+    cudaError_t e = launch_prep_act(static_cast<const uint16_t*>(A_dev), lda, K, W->fmt, M, 0, 1,
+                                    1, ws, n_tiles, s);
+    if (e != cudaSuccess) return cuda_fail(e, "prep_act launch");
+    GemmParams p{};
+    p.N = N;
+    p.K = K;
+    p.T = T;
+    p.n_tiles = n_tiles;
+    p.tensor_scale = W->tensor_scale;
+    p.seg = ws.seg;
+    p.inv_scale = ws.inv_scale;
+    p.act16 = ws.act16;
+    p.out = out_dev;
+    p.ldo = ldo;
+    p.argmax_M = row_argmax_dev ? M : 0;
+    p.partials = ws.partials;
+    p.tile_cnt = ws.tile_cnt;
+    p.am_key = ws.am_key;
+    p.am_cnt = ws.am_cnt;
+    p.row_argmax = row_argmax_dev;
+    p.status = d->status;
+    p.wait_ns = g_wait_ns;
+    e = launch_gemm(W->fmt, tmW, tmS, p, static_cast<int>(G), s);
+    if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
+    return VW4_OK;
+}
+
+VW4_API vw4_status verify_moe_w4(const vw4_weight* experts, int E, const void* A_dev, int lda,
+                                 int rows_are_pairs, const int32_t* expert_ids_dev,
+                                 const float* gates_dev, int M, int topk, int combine,
+                                 float* out_dev, int ldo, void* workspace_dev, size_t ws_bytes,
+                                 void* stream) {
+    vw4_status st = check_weight(experts);
+    if (st != VW4_OK) return st;
+    if (E < 1 || !A_dev || !expert_ids_dev || !out_dev) return VW4_ERR_INVALID_ARG;
+    if (combine && !gates_dev) return VW4_ERR_INVALID_ARG;
+    if (M < 1 || M > kMaxRows || topk < 1 || topk > kMaxRows) return VW4_ERR_INVALID_ARG;
+    if ((rows_are_pairs != 0 && rows_are_pairs != 1) || (combine != 0 && combine != 1))
+        return VW4_ERR_INVALID_ARG;
+    const int N = experts->N, K = experts->K;
+    if (static_cast<long long>(E) * N > 0x7fffffffLL) return VW4_ERR_INVALID_ARG;
+    if (lda < K || ldo < N) return VW4_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(A_dev) & 1u) || (reinterpret_cast<uintptr_t>(out_dev) & 3u))
+        return VW4_ERR_ALIGN;
+    if (!workspace_dev) return VW4_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace_dev) & 255u) != 0) return VW4_ERR_ALIGN;
+    const int P = M * topk;
+    GemmWorkspace ws = gemm_workspace_layout(workspace_dev, P, N, K, kMaxGrid, P);
+    if (ws.bytes > ws_bytes) return VW4_ERR_WORKSPACE;
+    DeviceInfo* d = nullptr;
+    st = device_info(&d);
+    if (st != VW4_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    CUtensorMap tmW, tmS;
+    const uint64_t rows = static_cast<uint64_t>(E) * N;
+    st = make_map(&tmW, experts->q_dev, static_cast<uint64_t>(K) / 2, rows, kStageK / 2,
+                  kTileRows, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != VW4_OK) return st;
+    st = make_map(&tmS, experts->scales_dev, static_cast<uint64_t>(K) / 16, rows, 16, kTileRows,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != VW4_OK) return st;
+
+    const int T = K / kStageK;
+    const int n_tiles = (N + kTileRows - 1) / kTileRows;
+    long long G = static_cast<long long>(d->sms) * d->occ[experts->fmt];
+    if (G > kMaxGrid) G = kMaxGrid;
+    const long long U_max = static_cast<long long>(P) * n_tiles * T;
+    if (G > U_max) G = U_max;
+
+    cudaError_t e = launch_route(expert_ids_dev, M, topk, E, ws, d->status,
+                                 combine ? nullptr : out_dev, ldo, N, s);
+    if (e != cudaSuccess) return cuda_fail(e, "route launch");
+    e = launch_prep_act(static_cast<const uint16_t*>(A_dev), lda, K, experts->fmt, 0,
+                        rows_are_pairs, topk, P, ws, P * n_tiles, s);
+    if (e != cudaSuccess) return cuda_fail(e, "prep_act launch");
+    GemmParams p{};
+    p.N = N;
+    p.K = K;
+    p.T = T;
+    p.n_tiles = n_tiles;
+    p.tensor_scale = experts->tensor_scale;
+    p.seg = ws.seg;
+    p.inv_scale = ws.inv_scale;
+    p.act16 = ws.act16;
+    p.out = combine ? ws.pair_out : out_dev;
+    p.ldo = combine ? N : ldo;
+    p.argmax_M = 0;
+    p.partials = ws.partials;
+    p.tile_cnt = ws.tile_cnt;
+    p.am_key = ws.am_key;
+    p.am_cnt = ws.am_cnt;
+    p.row_argmax = nullptr;
+    p.status = d->status;
+    p.wait_ns = g_wait_ns;
+    e = launch_gemm(experts->fmt, tmW, tmS, p, static_cast<int>(G), s);
+    if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
+    if (combine) {
+        e = launch_combine(ws.pair_out, gates_dev, expert_ids_dev, E, M, topk, N, out_dev, ldo, s);
+        if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    }
+    return VW4_OK;
+}
+
+VW4_API vw4_status accept_greedy(const float* target_logits_dev, const int32_t* drafts_dev,
+                                 const int32_t* target_argmax_dev, int B, int Kd, int V,
+                                 int32_t* tokens_dev, int32_t* len_dev, void* stream) {
+    if (B < 1 || Kd < 0 || Kd > kMaxRows || V < 1) return VW4_ERR_INVALID_ARG;
+    if (!tokens_dev || !len_dev) return VW4_ERR_INVALID_ARG;
+    if (Kd > 0 && !drafts_dev) return VW4_ERR_INVALID_ARG;
+    if (!target_argmax_dev && !target_logits_dev) return VW4_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * (Kd + 1) * 8 > 0x7fffffffLL) return VW4_ERR_INVALID_ARG;
+    DeviceInfo* d = nullptr;
+    vw4_status st = device_info(&d);
+    if (st != VW4_OK) return st;
+    cudaError_t e = launch_accept_greedy(target_logits_dev, drafts_dev, target_argmax_dev, B, Kd,
+                                         V, tokens_dev, len_dev, d->status,
+                                         static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "accept_greedy launch");
+    return VW4_OK;
+}
+
+VW4_API vw4_status accept_rejection(const float* target_logits_dev, const float* draft_logits_dev,
+                                    const int32_t* drafts_dev, int B, int Kd, int V,
+                                    const vw4_sampling* params, uint64_t seed, uint64_t offset,
+                                    int32_t* tokens_dev, int32_t* len_dev, void* workspace_dev,
+                                    size_t ws_bytes, void* stream) {
+    if (!params || !target_logits_dev || !tokens_dev || !len_dev) return VW4_ERR_INVALID_ARG;
+    if (B < 1 || Kd < 0 || Kd > kMaxRows || V < 1 || V > (1 << 24)) return VW4_ERR_INVALID_ARG;
+    if (Kd > 0 && (!drafts_dev || !draft_logits_dev)) return VW4_ERR_INVALID_ARG;
+    const float T = params->temperature;
+    if (!(T >= 0.0f) || !std::isfinite(T)) return VW4_ERR_INVALID_ARG;
+    if (!(params->top_p > 0.0f) || !std::isfinite(params->top_p)) return VW4_ERR_INVALID_ARG;
+    if (params->top_k != 0 || params->min_p != 0.0f) return VW4_ERR_UNSUPPORTED;
+    if (T == 0.0f)  // temperature 0 is the greedy rule: no random numbers drawn
+        return accept_greedy(target_logits_dev, drafts_dev, nullptr, B, Kd, V, tokens_dev,
+                             len_dev, stream);
+    const size_t need = rejection_workspace_bytes(B, Kd, V);
+    if (!workspace_dev || ws_bytes < need) return VW4_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace_dev) & 255u) != 0) return VW4_ERR_ALIGN;
+    DeviceInfo* d = nullptr;
+    vw4_status st = device_info(&d);
+    if (st != VW4_OK) return st;
+    const float invT = static_cast<float>(1.0 / static_cast<double>(T));
+    const double pd = static_cast<double>(params->top_p) * 4294967296.0;
+    const uint64_t P = pd >= 4294967296.0 ? (1ull << 32) : static_cast<uint64_t>(std::llround(pd));
+    cudaError_t e = launch_accept_rejection(target_logits_dev, draft_logits_dev, drafts_dev, B, Kd,
+                                            V, invT, P, seed, offset, tokens_dev, len_dev,
+                                            workspace_dev, ws_bytes, d->status,
+                                            static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return VW4_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return cuda_fail(e, "accept_rejection launch");
+    return VW4_OK;
+}
+
+VW4_API vw4_status vw4_get_device_status(uint32_t* bits, void* stream) {
+    if (!bits) return VW4_ERR_INVALID_ARG;
+    DeviceInfo* d = nullptr;
+    vw4_status st = device_info(&d);
+    if (st != VW4_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t h = 0;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    e = cudaMemcpyFromSymbolAsync(&h, g_status_word, sizeof(h), 0, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(e, "read status");
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_status_word, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "clear status");
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    *bits |= h;
+    return VW4_OK;
+}
+
+VW4_API vw4_status vw4_own_exp(const float* x_dev, float* y_dev, int64_t n, void* stream) {
+    if (!x_dev || !y_dev || n < 0) return VW4_ERR_INVALID_ARG;
+    if (n == 0) return VW4_OK;
+    cudaError_t e = launch_own_exp(x_dev, y_dev, n, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "own_exp launch");
+    return VW4_OK;
+}
+
+VW4_API vw4_status vw4_q4_0_from_blocks(const void* blocks_dev, int N, int K, void* q_dev,
+                                        void* d_dev, void* stream) {
+    if (!blocks_dev || !q_dev || !d_dev || N < 1 || K < 32 || K % 32) return VW4_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(d_dev) & 1u) != 0) return VW4_ERR_ALIGN;
+    cudaError_t e = launch_q4_0_split(static_cast<const uint8_t*>(blocks_dev), N, K,
+                                      static_cast<uint8_t*>(q_dev), static_cast<__half*>(d_dev),
+                                      static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "q4_0 split launch");
+    return VW4_OK;
+}
+
+}  // extern "C"

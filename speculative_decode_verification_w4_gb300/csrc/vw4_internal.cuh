@@ -1,0 +1,97 @@
+// vw4_internal.cuh -- shapes, workspace layout and kernel parameter blocks
+// shared by the kernels and the C-ABI layer.  Not part of the public ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace vw4 {
+
+constexpr int kMaxRows = 8;        // verify rows per segment (mma n = 8)
+constexpr int kMaxSeg = 64;        // routed (token, expert) pairs per call
+constexpr int kTileRows = 128;     // weight rows per tile
+constexpr int kStageK = 256;       // k elements per pipeline stage
+constexpr int kStages = 4;         // pipeline depth
+constexpr int kConsumerWarps = 4;  // each owns 32 rows of the tile
+constexpr int kGemmThreads = (kConsumerWarps + 1) * 32;
+constexpr int kWBytes = kTileRows * (kStageK / 2);     // 16384: packed nibbles
+constexpr int kSBytes = kTileRows * 16;                // 2048: 16 B of scales per row
+constexpr int kABytes = kMaxRows * kStageK * 2;        // 4096: fp16 activations
+constexpr int kStageBytes = kWBytes + kSBytes + kABytes;  // 22528 = 22 * 1024
+constexpr int kGemmSmem = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers, flags*/;
+constexpr int kPartialFloats = kMaxRows * kTileRows;   // one partial tile: [8][128]
+
+// A "segment" is the set of verify rows that share one weight matrix: the
+// whole batch for a dense layer, or the pairs routed to one expert.
+struct SegTable {
+    int n_seg;
+    int pad[3];
+    int expert[kMaxSeg];
+    int count[kMaxSeg];
+    int dest[kMaxSeg][kMaxRows];  // output row of each segment row
+};
+
+struct GemmWorkspace {
+    SegTable* seg;
+    float* inv_scale;            // [kMaxSeg][8] 2^-s of each activation row
+    __half* act16;               // [seg][T][8][256] scaled fp16, bank-swizzled
+    float* partials;             // [2 * grid][8][128] stream-K partial tiles
+    uint32_t* tile_cnt;          // [kMaxSeg * n_tiles] arrival tickets
+    unsigned long long* am_key;  // [8] packed (value, ~index) running maxima
+    uint32_t* am_cnt;            // [1] quarter-tile tickets of the argmax
+    float* pair_out;             // [pairs][N] MoE pair rows before the combine
+    size_t bytes;
+};
+
+struct GemmParams {
+    int N, K, T, n_tiles;
+    float tensor_scale;
+    const SegTable* seg;
+    const float* inv_scale;
+    const __half* act16;
+    float* out;
+    int ldo;
+    int argmax_M;                 // 0 = no fused argmax
+    float* partials;
+    uint32_t* tile_cnt;
+    unsigned long long* am_key;
+    uint32_t* am_cnt;
+    int32_t* row_argmax;
+    uint32_t* status;
+    unsigned long long wait_ns;
+};
+
+// Lays the GEMM/MoE workspace out from `base` (nullptr: size only).
+GemmWorkspace gemm_workspace_layout(void* base, int n_seg_max, int N, int K, int grid,
+                                    int pair_rows);
+
+// Kernel launchers (gemm_w4.cu).  All asynchronous on `s`.
+cudaError_t launch_prep_act(const uint16_t* A, int lda, int K, int fmt, int dense_M,
+                            int rows_are_pairs, int topk, int n_seg_grid, const GemmWorkspace& ws,
+                            int n_counters, cudaStream_t s);
+cudaError_t launch_route(const int32_t* expert_ids, int M, int topk, int E,
+                         const GemmWorkspace& ws, uint32_t* status, float* out_zero, int ldo,
+                         int N, cudaStream_t s);
+cudaError_t launch_gemm(int fmt, const CUtensorMap& tmW, const CUtensorMap& tmS,
+                        const GemmParams& p, int grid, cudaStream_t s);
+cudaError_t launch_combine(const float* pair_out, const float* gates, const int32_t* ids,
+                           int E, int M, int topk, int N, float* out, int ldo, cudaStream_t s);
+cudaError_t launch_q4_0_split(const uint8_t* blocks, int N, int K, uint8_t* q, __half* d,
+                              cudaStream_t s);
+int gemm_blocks_per_sm(int fmt);
+
+// Accept launchers (accept.cu).
+cudaError_t launch_accept_greedy(const float* logits, const int32_t* drafts,
+                                 const int32_t* argmax_in, int B, int Kd, int V, int32_t* tokens,
+                                 int32_t* len, uint32_t* status, cudaStream_t s);
+size_t rejection_workspace_bytes(int B, int Kd, int V);
+cudaError_t launch_own_exp(const float* x, float* y, long long n, cudaStream_t s);
+cudaError_t launch_accept_rejection(const float* target, const float* draft,
+                                    const int32_t* drafts, int B, int Kd, int V, float invT,
+                                    uint64_t P, uint64_t seed, uint64_t offset, int32_t* tokens,
+                                    int32_t* len, void* ws, size_t ws_bytes, uint32_t* status,
+                                    cudaStream_t s);
+
+}  // namespace vw4

@@ -23,9 +23,6 @@ from __future__ import annotations
 
 import numpy as np
 
-E2M1_MAGS = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], np.float32)
-_E2M1_MIDS = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
-_E2M1_ODD_MIDS = np.array([0.75, 1.75, 3.5], np.float32)  # ties that round up to an even code
 
 
 def rng(seed: int) -> np.random.Generator:
@@ -49,81 +46,102 @@ def activations(g: np.random.Generator, M: int, K: int) -> np.ndarray:
     return bf16_bits(g.standard_normal((M, K), dtype=np.float32))
 
 
-def _e4m3_encode(x: np.ndarray) -> np.ndarray:
-    import torch  # the library cast is the encoder; torch is plumbing here
-    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
-    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
-
-
-def _e4m3_values(codes: np.ndarray) -> np.ndarray:
+def _e2m1_codes(y):
+    """Nearest E2M1 code of a float tensor (ties to the even code), saturating
+    at +-6.  The thresholds are the midpoints of 0, .5, 1, 1.5, 2, 3, 4, 6;
+    at a midpoint the comparison picks the even code."""
     import torch
-    t = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn)
-    return t.to(torch.float32).numpy()
+    a = y.abs()
+    code = ((a > 0.25).to(torch.uint8) + (a >= 0.75).to(torch.uint8) + (a > 1.25).to(torch.uint8)
+            + (a >= 1.75).to(torch.uint8) + (a > 2.5).to(torch.uint8)
+            + (a >= 3.5).to(torch.uint8) + (a > 5.0).to(torch.uint8))
+    sign = ((y < 0) & (code != 0)).to(torch.uint8)
+    return code | (sign << 3)
 
 
-def _e2m1_encode(y: np.ndarray) -> np.ndarray:
-    """Nearest E2M1 code (ties to the even code), saturating at +-6."""
-    a = np.abs(y)
-    code = np.searchsorted(_E2M1_MIDS, a, side="left").astype(np.uint8)
-    code += np.isin(a, _E2M1_ODD_MIDS).astype(np.uint8)
-    code = np.minimum(code, 7).astype(np.uint8)
-    sign = (np.signbit(y) & (code != 0)).astype(np.uint8) << np.uint8(3)
-    return code | sign
-
-
-def quantize_nvfp4(w: np.ndarray, rows_per_chunk: int = 4096):
-    """w fp32 [N, K] (K % 16 == 0) -> (Wq u8 [N, K/2], S u8(e4m3) [N, K/16], tensor_scale)."""
+def quantize_nvfp4(w: np.ndarray, amax: float | None = None):
+    """w fp32 [N, K] (K % 16 == 0) -> (Wq u8 [N, K/2], S u8(e4m3) [N, K/16], tensor_scale).
+    amax (the whole matrix's max |w|) may be given when w is one chunk of a larger
+    matrix.  torch CPU ops are used as multithreaded plumbing; the e4m3 encoder is
+    torch's float8_e4m3fn cast."""
+    import torch
     N, K = w.shape
     assert K % 16 == 0
-    amax = float(np.max(np.abs(w))) if w.size else 0.0
+    t = torch.from_numpy(np.ascontiguousarray(w, dtype=np.float32))
+    if amax is None:
+        amax = float(t.abs().max()) if t.numel() else 0.0
     ts = np.float32(amax / (6.0 * 448.0)) if amax > 0 else np.float32(1.0)
-    Wq = np.empty((N, K // 2), np.uint8)
-    S = np.empty((N, K // 16), np.uint8)
-    for r0 in range(0, N, rows_per_chunk):
-        blk = w[r0:r0 + rows_per_chunk].reshape(-1, K // 16, 16)
-        bamax = np.max(np.abs(blk), axis=2)
-        s_codes = _e4m3_encode(bamax / np.float32(6.0) / ts)
-        s_vals = _e4m3_values(s_codes)
-        denom = (s_vals * ts)[..., None]
-        with np.errstate(divide="ignore", invalid="ignore"):
-            y = np.where(denom > 0, blk / denom, np.float32(0.0)).astype(np.float32)
-        codes = _e2m1_encode(y).reshape(blk.shape[0], K)
-        Wq[r0:r0 + rows_per_chunk] = codes[:, 0::2] | (codes[:, 1::2] << np.uint8(4))
-        S[r0:r0 + rows_per_chunk] = s_codes
-    return Wq, S, float(ts)
+    blk = t.view(N, K // 16, 16)
+    bamax = blk.abs().amax(dim=2)
+    s8 = (bamax / 6.0 / float(ts)).to(torch.float8_e4m3fn)
+    sv = s8.to(torch.float32) * float(ts)
+    y = torch.where(sv[..., None] > 0, blk / sv[..., None].clamp_min(1e-38),
+                    torch.zeros((), dtype=torch.float32))
+    codes = _e2m1_codes(y).view(N, K)
+    Wq = (codes[:, 0::2] | (codes[:, 1::2] << 4)).numpy()
+    return np.ascontiguousarray(Wq), s8.view(torch.uint8).numpy().copy(), float(ts)
 
 
-def quantize_q4_0(w: np.ndarray, rows_per_chunk: int = 4096):
+def quantize_q4_0(w: np.ndarray):
     """w fp32 [N, K] (K % 32 == 0) -> (qs u8 [N, K/2], d f16 [N, K/32]); byte j of a
-    block holds element j (low nibble) and element j+16 (high nibble)."""
+    block holds element j (low nibble) and element j+16 (high nibble).
+    d = (the block's largest-magnitude value) / -8, q = clamp(round(w/d) + 8)."""
+    import torch
     N, K = w.shape
     assert K % 32 == 0
-    qs = np.empty((N, K // 2), np.uint8)
-    d = np.empty((N, K // 32), np.float16)
-    for r0 in range(0, N, rows_per_chunk):
-        blk = w[r0:r0 + rows_per_chunk].reshape(-1, K // 32, 32)
-        idx = np.argmax(np.abs(blk), axis=2)
-        mx = np.take_along_axis(blk, idx[..., None], axis=2)[..., 0]
-        dd = (mx / np.float32(-8.0)).astype(np.float16)
-        dv = dd.astype(np.float32)[..., None]
-        with np.errstate(divide="ignore", invalid="ignore"):
-            y = np.where(dv != 0, blk / dv, np.float32(0.0))
-        q = np.clip(np.rint(y) + 8, 0, 15).astype(np.uint8)
-        packed = q[..., :16] | (q[..., 16:] << np.uint8(4))
-        qs[r0:r0 + rows_per_chunk] = packed.reshape(-1, K // 2)
-        d[r0:r0 + rows_per_chunk] = dd
-    return qs, d
+    t = torch.from_numpy(np.ascontiguousarray(w, dtype=np.float32))
+    blk = t.view(N, K // 32, 32)
+    idx = blk.abs().argmax(dim=2, keepdim=True)
+    mx = torch.gather(blk, 2, idx)[..., 0]
+    dd = (mx / -8.0).to(torch.float16)
+    dv = dd.to(torch.float32)[..., None]
+    y = torch.where(dv != 0, blk / torch.where(dv != 0, dv, torch.ones_like(dv)),
+                    torch.zeros((), dtype=torch.float32))
+    q = (torch.round(y) + 8).clamp(0, 15).to(torch.uint8)
+    packed = q[..., :16] | (q[..., 16:] << 4)
+    return packed.reshape(N, K // 2).numpy().copy(), dd.numpy().copy()
 
 
-def linear(seed: int, N: int, K: int, fmt: str = "nvfp4", std: float = 0.02):
-    """A quantized N(0, std) linear layer [N, K] of the given format."""
-    g = rng(seed)
-    w = normal_weights(g, N, K, std)
-    if fmt == "nvfp4":
-        Wq, S, ts = quantize_nvfp4(w)
-        return Wq, S, ts
-    qs, d = quantize_q4_0(w)
-    return qs, d, 1.0
+LINEAR_CHUNK_ROWS = 2048
+
+
+def _chunk_weights(seed: int, j: int, n: int, K: int, std: float) -> np.ndarray:
+    """Rows [j*2048, j*2048 + n) of a synthetic linear: chunk j has its own
+    child stream of the seed, so chunks can be drawn in any order or in
+    parallel and the matrix is the same."""
+    return normal_weights(rng([seed, j]), n, K, std)
+
+
+def linear(seed: int, N: int, K: int, fmt: str = "nvfp4", std: float = 0.02, threads: int = 8):
+    """A quantized N(0, std) linear layer [N, K] of the given format.  Rows are
+    drawn in 2048-row chunks (a first pass finds the global max for the nvfp4
+    tensor scale), so large matrices never exist in fp32 all at once."""
+    from concurrent.futures import ThreadPoolExecutor
+    C = LINEAR_CHUNK_ROWS
+    chunks = [(j, min(C, N - j * C)) for j in range((N + C - 1) // C)]
+    with ThreadPoolExecutor(threads) as ex:
+        if fmt == "nvfp4":
+            amax = max(ex.map(lambda jc: float(np.max(np.abs(_chunk_weights(seed, jc[0], jc[1],
+                                                                              K, std)))), chunks))
+            Wq = np.empty((N, K // 2), np.uint8)
+            S = np.empty((N, K // 16), np.uint8)
+            ts = [1.0]
+
+            def quant(jc):
+                j, n = jc
+                Wq[j * C:j * C + n], S[j * C:j * C + n], ts[0] = quantize_nvfp4(
+                    _chunk_weights(seed, j, n, K, std), amax=amax)
+            list(ex.map(quant, chunks))
+            return Wq, S, ts[0]
+        qs = np.empty((N, K // 2), np.uint8)
+        d = np.empty((N, K // 32), np.float16)
+
+        def quant4(jc):
+            j, n = jc
+            qs[j * C:j * C + n], d[j * C:j * C + n] = quantize_q4_0(
+                _chunk_weights(seed, j, n, K, std))
+        list(ex.map(quant4, chunks))
+        return qs, d, 1.0
 
 
 # ----------------------------------------------------------- accept inputs

@@ -1,0 +1,92 @@
+"""The C-ABI library loads and exports every symbol include/vw4.h declares, and
+rejects bad arguments on the host before touching the GPU (no compute calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decode_verification_w4_gb300 as vw4
+from speculative_decode_verification_w4_gb300 import build as vbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    vbuild.build()
+    return vw4.load_library()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "vw4.h")).read()
+    return sorted(set(re.findall(r"VW4_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names():
+    names = declared_symbols()
+    assert set(names) == set(vw4.EXPORTS), names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(vw4.LIB_PATH)
+    for name in declared_symbols():
+        assert hasattr(raw, name), name
+
+
+def test_status_strings(lib):
+    assert lib.vw4_status_str(0) == b"ok"
+    assert lib.vw4_status_str(6) == b"workspace too small"
+    assert lib.vw4_version() >= 100
+
+
+def test_workspace_sizes(lib):
+    assert vw4.vw4_workspace_bytes(vw4.OP_GEMM, 8, 262144, 5376) > 0
+    assert vw4.vw4_workspace_bytes(vw4.OP_GEMM, 9, 1024, 1024) == 0
+    assert vw4.vw4_workspace_bytes(vw4.OP_GEMM, 4, 1024, 1000) == 0
+    assert vw4.vw4_workspace_bytes(vw4.OP_MOE, 64, 1536, 2048) > 0
+    assert vw4.vw4_workspace_bytes(99, 1, 1, 1) == 0
+
+
+def _weight(fmt=1, N=128, K=256, ts=1.0, q=0x1000, s=0x2000):
+    return vw4.Weight(fmt, N, K, 0, q, s, ts, 0.0)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(M=0), 1), (dict(M=9), 1), (dict(lda=100), 1), (dict(ldo=10), 1),
+    (dict(A=0), 1), (dict(out=0), 1), (dict(A=0x3001), 3), (dict(out=0x4002), 3),
+    (dict(ws=0), 6), (dict(ws_bytes=16), 6),
+])
+def test_gemm_argument_checks_on_host(lib, kw, code):
+    W = _weight()
+    args = dict(A=0x3000, M=2, lda=256, out=0x4000, ldo=128, am=0, ws=0x10000,
+                ws_bytes=1 << 30)
+    args.update(kw)
+    r = lib.verify_gemm_w4(ctypes.byref(W), args["A"], args["M"], args["lda"], args["out"],
+                           args["ldo"], args["am"], args["ws"], args["ws_bytes"], None)
+    assert r == code
+
+
+@pytest.mark.parametrize("W,code", [
+    (_weight(fmt=3), 1), (_weight(K=24), 1), (_weight(fmt=2, ts=2.0), 1),
+    (_weight(q=0x1001), 3), (_weight(K=272), 2), (_weight(N=0), 1),
+])
+def test_weight_checks_on_host(lib, W, code):
+    r = lib.verify_gemm_w4(ctypes.byref(W), 0x3000, 2, 512, 0x4000, 128, None, 0x10000,
+                           1 << 30, None)
+    assert r == code
+
+
+def test_accept_argument_checks_on_host(lib):
+    assert lib.accept_greedy(None, None, None, 1, 2, 10, 0x100, 0x200, None) == 1
+    assert lib.accept_greedy(0x100, 0x100, None, 0, 2, 10, 0x100, 0x200, None) == 1
+    assert lib.accept_greedy(0x100, 0x100, None, 1, 9, 10, 0x100, 0x200, None) == 1
+    prm = vw4.Sampling(0.6, 0.95, 5, 0.0)
+    assert lib.accept_rejection(0x100, 0x100, 0x100, 1, 2, 10, ctypes.byref(prm), 0, 0, 0x100,
+                                0x200, 0x1000, 1 << 20, None) == 2
+    prm = vw4.Sampling(-1.0, 0.95, 0, 0.0)
+    assert lib.accept_rejection(0x100, 0x100, 0x100, 1, 2, 10, ctypes.byref(prm), 0, 0, 0x100,
+                                0x200, 0x1000, 1 << 20, None) == 1
+    prm = vw4.Sampling(0.6, 0.0, 0, 0.0)
+    assert lib.accept_rejection(0x100, 0x100, 0x100, 1, 2, 10, ctypes.byref(prm), 0, 0, 0x100,
+                                0x200, 0x1000, 1 << 20, None) == 1

@@ -1,0 +1,96 @@
+"""GPU parity of accept_greedy against the oracle (bit-exact ids and lengths)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import speculative_decode_verification_w4_gb300 as vw4
+
+pytestmark = pytest.mark.gpu
+
+
+def run(target, drafts, argmax=None):
+    t = torch.from_numpy(np.ascontiguousarray(target)).cuda()
+    d = torch.from_numpy(np.ascontiguousarray(drafts, np.int32)).cuda()
+    am = None if argmax is None else torch.from_numpy(np.ascontiguousarray(argmax, np.int32)).cuda()
+    tok, ln = vw4.accept_greedy(None if argmax is not None else t, d, target_argmax=am,
+                                B=target.shape[0], V=target.shape[2])
+    torch.cuda.synchronize()
+    return tok.cpu().numpy(), ln.cpu().numpy()
+
+
+def test_tiny_config_greedy():
+    """Greedy accept of K=3 drafts on fp32 N(0,1) logits, vocab 1024, seed 0."""
+    g = synth.rng(0)
+    target = synth.logits(g, (1, 4, 1024), 1.0)
+    am = np.array([[oracle.argmax_f32(target[0, i]) for i in range(3)]])
+    drafts = synth.greedy_drafts(g, am, 1024)
+    tok, ln = run(target, drafts)
+    rt, rl, _ = oracle.accept_greedy(target, drafts)
+    assert np.array_equal(tok, rt) and np.array_equal(ln, rl)
+
+
+@pytest.mark.parametrize("B,Kd,V", [(1, 0, 5), (7, 1, 1000), (33, 4, 4097), (256, 8, 151936),
+                                    (3, 8, 7)])
+def test_random_cases(B, Kd, V):
+    g = synth.rng(B * 100 + Kd)
+    target = synth.logits(g, (B, Kd + 1, V), 1.0)
+    am = np.array([[oracle.argmax_f32(target[b, i]) for i in range(Kd)] for b in range(B)],
+                  np.int32).reshape(B, Kd)
+    drafts = synth.greedy_drafts(g, am, V) if Kd else np.zeros((B, 0), np.int32)
+    tok, ln = run(target, drafts)
+    rt, rl, _ = oracle.accept_greedy(target, drafts)
+    assert np.array_equal(tok, rt) and np.array_equal(ln, rl)
+
+
+def test_ties_nan_and_bad_ids():
+    V = 64
+    target = np.zeros((4, 3, V), np.float32)
+    target[0, :, 5] = 1.0
+    target[0, :, 9] = 1.0          # tie -> 5
+    target[1, :, :] = np.nan       # all NaN -> 0
+    target[2, :, 3] = np.nan
+    target[2, :, 7] = -1.0         # NaN never wins; zeros elsewhere -> 0
+    target[2, :, 0] = -2.0         # now index 1 is the first zero
+    target[3, :, 60] = np.inf
+    drafts = np.array([[5, 5], [0, 1], [1, 99], [60, -3]], np.int32)
+    vw4.vw4_get_device_status()
+    tok, ln = run(target, drafts)
+    rt, rl, bad = oracle.accept_greedy(target, drafts)
+    assert np.array_equal(tok, rt) and np.array_equal(ln, rl)
+    assert bad == 2
+    assert vw4.vw4_get_device_status() & vw4.DEV_BAD_DRAFT_ID
+
+
+def test_precomputed_argmax_path():
+    g = synth.rng(4)
+    B, Kd, V = 9, 5, 300
+    target = synth.logits(g, (B, Kd + 1, V), 1.0)
+    am = np.array([[oracle.argmax_f32(target[b, i]) for i in range(Kd + 1)] for b in range(B)],
+                  np.int32)
+    drafts = synth.greedy_drafts(g, am[:, :Kd], V)
+    tok, ln = run(target, drafts, argmax=am)
+    rt, rl, _ = oracle.accept_greedy(target, drafts)
+    assert np.array_equal(tok, rt) and np.array_equal(ln, rl)
+
+
+def test_lm_head_fused_path_end_to_end():
+    """LM-head verify + fused accept, at a reduced vocabulary: GEMM with fused
+    argmax feeding accept_greedy, against the oracle applied to the GPU logits."""
+    N, K, M = 20000, 1024, 8
+    q, s, ts = synth.linear(3, N, K, "nvfp4")
+    A = synth.activations(synth.rng(3), M, K)
+    qd = torch.from_numpy(q).cuda()
+    sd = torch.from_numpy(s).cuda()
+    Ad = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16).cuda()
+    am = torch.empty((M,), dtype=torch.int32, device="cuda")
+    logits = vw4.verify_gemm_w4(vw4.FMT_NVFP4, qd, sd, ts, Ad, row_argmax=am)
+    amh = am.cpu().numpy()
+    drafts = synth.greedy_drafts(synth.rng(31), amh[None, :M - 1], N)
+    d = torch.from_numpy(drafts).cuda()
+    tok, ln = vw4.accept_greedy(None, d, target_argmax=am.view(1, M), B=1, V=N)
+    torch.cuda.synchronize()
+    lg = logits.cpu().numpy()[None]
+    rt, rl, _ = oracle.accept_greedy(lg, drafts)
+    assert np.array_equal(tok.cpu().numpy(), rt) and np.array_equal(ln.cpu().numpy(), rl)

@@ -1,0 +1,118 @@
+"""GPU parity of accept_rejection against the oracle: committed ids and
+lengths bit-exact, on small cases, edge cases and the full-size stochastic
+sweep (vocab 151936, K = 1..8, 256 sequences; sampled sequences checked)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import speculative_decode_verification_w4_gb300 as vw4
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_accept(target, draft, drafts, T, top_p, seed, offset):
+    t = torch.from_numpy(np.ascontiguousarray(target)).cuda()
+    d = torch.from_numpy(np.ascontiguousarray(draft)).cuda() if draft.size else None
+    x = torch.from_numpy(np.ascontiguousarray(drafts, np.int32)).cuda()
+    tok, ln = vw4.accept_rejection(t, d, x, T, top_p, seed, offset)
+    torch.cuda.synchronize()
+    return tok.cpu().numpy(), ln.cpu().numpy()
+
+
+def test_own_exp_bitwise_equal_to_oracle_over_all_inputs():
+    """Every fp32 x in [-32, 0] (about 1.1e9 values), plus values below."""
+    start, stop = 0x80000000, 0xC2000000 + 1024  # -0.0 ... just below -32
+    chunk = 1 << 26
+    for lo in range(start, stop, chunk):
+        hi = min(stop, lo + chunk)
+        bits = np.arange(lo, hi, dtype=np.uint64).astype(np.uint32)
+        x = bits.view(np.float32)
+        y = vw4.vw4_own_exp(torch.from_numpy(x).cuda()).cpu().numpy()
+        ref = oracle.own_exp_array(x)
+        bad = y.view(np.uint32) != ref.view(np.uint32)
+        assert not bad.any(), (lo, x[bad][:4], y[bad][:4], ref[bad][:4])
+
+
+@pytest.mark.parametrize("B,Kd,V,top_p", [(16, 3, 16, 0.95), (64, 1, 1000, 0.95),
+                                          (32, 4, 5000, 0.8), (8, 8, 20000, 0.95),
+                                          (20, 2, 777, 1.0), (5, 0, 300, 0.95),
+                                          (12, 5, 40000, 0.5)])
+def test_small_cases_match_oracle(B, Kd, V, top_p):
+    target, draft, _ = synth.stochastic_case(B * 7 + Kd, B, Kd, V) if Kd else (
+        synth.logits(synth.rng(1), (B, 1, V), 3.0), np.zeros((B, 0, V), np.float32), None)
+    drafts = oracle.sample_drafts(draft, 0.6, top_p, 3, 1 << 32) if Kd else \
+        np.zeros((B, 0), np.int32)
+    tok, ln = gpu_accept(target, draft, drafts, 0.6, top_p, 3, 0)
+    rt, rl, _ = oracle.accept_rejection(target, draft, drafts, 0.6, top_p, 3, 0)
+    assert np.array_equal(ln, rl), (ln, rl)
+    assert np.array_equal(tok, rt)
+
+
+def test_gumbel_drafts_and_ties():
+    """Drafts from a plain float sampler (some fall outside the top-p set) and
+    logits with many exact ties (equal masses cut by index)."""
+    B, Kd, V = 24, 4, 3000
+    target, draft, drafts = synth.stochastic_case(5, B, Kd, V)
+    target[:, :, ::3] = np.round(target[:, :, ::3])  # many equal logits
+    draft[:, :, ::5] = 1.0
+    tok, ln = gpu_accept(target, draft, drafts, 0.6, 0.95, 9, 17)
+    rt, rl, _ = oracle.accept_rejection(target, draft, drafts, 0.6, 0.95, 9, 17)
+    assert np.array_equal(ln, rl) and np.array_equal(tok, rt)
+
+
+def test_flat_distribution_cut_by_index():
+    B, Kd, V = 4, 2, 4096
+    target = np.zeros((B, Kd + 1, V), np.float32)
+    draft = np.zeros((B, Kd, V), np.float32)
+    drafts = np.array([[5, 4000]] * B, np.int32)
+    tok, ln = gpu_accept(target, draft, drafts, 0.6, 0.95, 1, 0)
+    rt, rl, _ = oracle.accept_rejection(target, draft, drafts, 0.6, 0.95, 1, 0)
+    assert np.array_equal(ln, rl) and np.array_equal(tok, rt)
+
+
+def test_temperature_zero_is_greedy():
+    B, Kd, V = 9, 3, 500
+    target, draft, drafts = synth.stochastic_case(6, B, Kd, V)
+    tok, ln = gpu_accept(target, draft, drafts, 0.0, 0.95, 1, 0)
+    rt, rl, _ = oracle.accept_greedy(target, drafts)
+    assert np.array_equal(ln, rl) and np.array_equal(tok, rt)
+
+
+def test_p_equals_q_accepts_everything():
+    B, Kd, V = 32, 6, 2000
+    target = synth.logits(synth.rng(8), (B, Kd + 1, V), 3.0)
+    draft = np.ascontiguousarray(target[:, :Kd])
+    drafts = oracle.sample_drafts(draft, 0.6, 0.95, 4, 1 << 32)
+    tok, ln = gpu_accept(target, draft, drafts, 0.6, 0.95, 4, 0)
+    assert np.all(ln == Kd + 1)
+    rt, rl, _ = oracle.accept_rejection(target, draft, drafts, 0.6, 0.95, 4, 0)
+    assert np.array_equal(tok, rt)
+
+
+def test_bad_draft_ids_set_status():
+    B, Kd, V = 6, 3, 700
+    target, draft, drafts = synth.stochastic_case(7, B, Kd, V)
+    drafts[1, 0] = -1
+    drafts[3, 2] = V
+    vw4.vw4_get_device_status()
+    tok, ln = gpu_accept(target, draft, drafts, 0.6, 0.95, 2, 5)
+    rt, rl, bad = oracle.accept_rejection(target, draft, drafts, 0.6, 0.95, 2, 5)
+    assert bad >= 1
+    assert np.array_equal(ln, rl) and np.array_equal(tok, rt)
+    assert vw4.vw4_get_device_status() & vw4.DEV_BAD_DRAFT_ID
+
+
+@pytest.mark.parametrize("Kd", [1, 2, 4, 8])
+def test_stochastic_sweep_full_size_sampled(Kd):
+    """Vocab 151936, 256 sequences, fp32 N(0,3) target, draft = target + N(0,1),
+    T = 0.6, top_p = 0.95, Philox seed 4: all sequences on the GPU, a sample
+    of them through the oracle (same counter indices)."""
+    B, V = 256, 151936
+    target, draft, drafts = synth.stochastic_case(40 + Kd, B, Kd, V)
+    tok, ln = gpu_accept(target, draft, drafts, 0.6, 0.95, 4, 0)
+    for b in (0, 1, 77, 128, 200, 255):
+        rt, rl, _ = oracle.accept_rejection(target[b:b + 1], draft[b:b + 1], drafts[b:b + 1],
+                                            0.6, 0.95, 4, 0, b_base=b)
+        assert rl[0] == ln[b] and np.array_equal(rt[0], tok[b]), (b, rt, tok[b])
