@@ -1,0 +1,507 @@
+#!/usr/bin/env python
+"""Benchmark of the verify hot path on GB300.
+
+Workload (one step): the dense-27B-like layer verify -- d = 5120; q, k, v, o
+(5120 -> 6144 / 1024 / 1024, 6144 -> 5120), gate and up (5120 -> 17408) and
+down (17408 -> 5120) -- as nvfp4 weights (N(0, 0.02) quantized), with M = 8
+bf16 N(0, 1) verify rows: seven verify_gemm_w4 calls back to back on one
+stream.  The weights and scales of one step (191.7 MB) exceed the 129 MB L2,
+so every step streams them from HBM.
+
+Metric: HBM GB/s = algorithmic bytes (packed weights + scales + activations)
+per step / step time, summed over ranks (N independent replicas).  The same
+JSON line carries the per-M microseconds for M = 1, 2, 4, 8 (nvfp4 and Q4_0),
+the accept-step microseconds, the roofline of the GEMM kernel, the end-to-end
+number through the C ABI with host buffers, the CPU oracle baseline and the
+SM clocks seen during the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+LAYER = [("q", 6144, 5120), ("k", 1024, 5120), ("v", 1024, 5120), ("o", 5120, 6144),
+         ("gate", 17408, 5120), ("up", 17408, 5120), ("down", 5120, 17408)]
+HEAD_M = 8
+METRIC = "nvfp4 verify-GEMM HBM GB/s & µs/pass at M=1,2,4,8; accept µs/step"
+WORKLOAD = ("dense-27B-like layer verify: d=5120, q/k/v/o 5120->6144/1024/1024 and 6144->5120, "
+            "gate/up 5120->17408, down 17408->5120, nvfp4 (E2M1 + E4M3 per 16 + fp32 tensor "
+            "scale), bf16 activations N(0,1), M=8 verify rows; 7 linears per step")
+SPEC_HBM_GBS = 8000.0
+LAUNCHES_PER_GEMM = 2   # activation prep + the GEMM kernel
+
+
+def weight_bytes(N, K, fmt="nvfp4"):
+    return N * K // 2 + (N * K // 16 if fmt == "nvfp4" else N * K // 32 * 2)
+
+
+def step_bytes(M, fmt="nvfp4"):
+    return sum(weight_bytes(N, K, fmt) + M * K * 2 for _, N, K in LAYER)
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed loop runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.index), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"],
+                    "raw": self.lines[:2]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ inputs
+def make_layer(fmt, device):
+    import torch
+    import synth
+    layer = []
+    for i, (name, N, K) in enumerate(LAYER):
+        q, s, ts = synth.linear(100 + i, N, K, fmt)
+        qd = torch.from_numpy(q).to(device)
+        if fmt == "nvfp4":
+            sd = torch.from_numpy(s).to(device)
+        else:
+            sd = torch.from_numpy(s.view(np.uint16)).to(device).view(torch.float16)
+        layer.append((name, N, K, qd, sd, ts))
+    return layer
+
+
+def make_acts(M, device, seed=7):
+    import torch
+    import synth
+    g = synth.rng(seed)
+    acts = []
+    for _, N, K in LAYER:
+        bits = synth.activations(g, M, K)
+        acts.append(torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(device))
+    return acts
+
+
+# --------------------------------------------------------------- our arm
+def run_ours(args, rank, world, device):
+    import torch
+    import speculative_decode_verification_w4_gb300 as vw4
+
+    torch.cuda.set_device(device)
+    layers = {"nvfp4": make_layer("nvfp4", device), "q4_0": make_layer("q4_0", device)}
+    acts = {M: make_acts(M, device, seed=7 + M) for M in (1, 2, 4, 8)}
+    outs = {M: [torch.empty((M, N), dtype=torch.float32, device=device) for _, N, _ in LAYER]
+            for M in (1, 2, 4, 8)}
+    ws = vw4.Workspace(device)
+    ws.get(max(vw4.vw4_workspace_bytes(vw4.OP_GEMM, 8, N, K) for _, N, K in LAYER))
+    FMTS = {"nvfp4": vw4.FMT_NVFP4, "q4_0": vw4.FMT_Q4_0}
+
+    def one_step(fmt, M):
+        for j, (name, N, K, qd, sd, ts) in enumerate(layers[fmt]):
+            vw4.verify_gemm_w4(FMTS[fmt], qd, sd, ts, acts[M][j], out=outs[M][j], workspace=ws)
+
+    def capture(fn, warm=3):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+        return g
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    def time_graph(g, reps, warmup):
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        return e0.elapsed_time(e1)
+
+    steps, warmup = args.steps, args.warmup
+    peak, peak_kind = read_peaks()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        # headline: one step = the 7 nvfp4 linears at M = 8 (a CUDA graph of the
+        # seven C-ABI calls, replayed K times back to back)
+        g_head = capture(lambda: one_step("nvfp4", HEAD_M))
+        soak_end = time.time() + 0.4
+        while time.time() < soak_end:      # let the clock sampler see the load
+            for _ in range(20):
+                g_head.replay()
+            torch.cuda.synchronize()
+        ms = time_graph(g_head, steps, warmup)
+        ms_max = reduce_max(ms, world)
+        ms_per_step = ms_max / steps
+        value = step_bytes(HEAD_M) * steps * world / (ms_max * 1e-3) / 1e9
+
+        # per-M microseconds of the whole layer (graph of the step), both formats
+        per_m = {}
+        for fmt in ("nvfp4", "q4_0"):
+            per_m[fmt] = {}
+            for M in (1, 2, 4, 8):
+                gm = capture(lambda: one_step(fmt, M))
+                m_ms = time_graph(gm, steps, 3)
+                per_m[fmt][str(M)] = {
+                    "layer_us": round(m_ms / steps * 1e3, 2),
+                    "layer_gbs": round(step_bytes(M, fmt) / (m_ms / steps * 1e-3) / 1e9, 1),
+                    "linear_us": {}}
+                del gm
+
+        # each linear alone: a graph of R calls on R different weight copies
+        # (more than 2x L2 of weights in flight, so nothing is served from L2)
+        for fmt in ("nvfp4", "q4_0"):
+            for j, (name, N, K, qd, sd, ts) in enumerate(layers[fmt]):
+                R = max(4, int(np.ceil(320e6 / weight_bytes(N, K, fmt))))
+                copies = [(qd.clone(), sd.clone()) for _ in range(R)]
+                for M in (1, 2, 4, 8):
+                    def calls(M=M, copies=copies):
+                        for (qc, sc) in copies:
+                            vw4.verify_gemm_w4(FMTS[fmt], qc, sc, ts, acts[M][j],
+                                               out=outs[M][j], workspace=ws)
+                    gl = capture(calls, warm=1)
+                    reps = max(2, int(np.ceil(steps / 4)))
+                    l_ms = time_graph(gl, reps, 1)
+                    per_m[fmt][str(M)]["linear_us"][name] = round(l_ms / (reps * R) * 1e3, 2)
+                    del gl
+                del copies
+                torch.cuda.empty_cache()
+
+    gate = {}
+    for name in ("gate", "up", "down"):
+        t1 = per_m["nvfp4"]["1"]["linear_us"][name]
+        t8 = per_m["nvfp4"]["8"]["linear_us"][name]
+        N, K = [(n, k) for nm, n, k in LAYER if nm == name][0]
+        gbs = (weight_bytes(N, K) + 8 * K * 2) / (t8 * 1e-6) / 1e9
+        gate[name] = {"m8_over_m1": round(t8 / t1, 3), "m8_gbs": round(gbs, 1),
+                      "frac_of_8tbs": round(gbs / SPEC_HBM_GBS, 3),
+                      "frac_of_measured_copy": round(gbs / peak, 3)}
+
+    # roofline of the GEMM kernel: algorithmic bytes of the 7 linears at M = 8
+    # over their per-launch times (each timed alone, graph replay, CUDA events)
+    t_lin = per_m["nvfp4"]["8"]["linear_us"]
+    achieved = sum(weight_bytes(N, K) + HEAD_M * K * 2 for _, N, K in LAYER) / (
+        sum(t_lin[n] for n, _, _ in LAYER) * 1e-6) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "peak_kind": f"of {peak_kind} (STREAM-style copy, burst)",
+                "kernel": "vw4::gemm_w4_kernel<nvfp4> (with its activation-prep launch)",
+                "per_unit": "0.5625 B per weight (nibble + e4m3/16) + 2*M B per k of activations"}
+
+    stream = torch.cuda.current_stream()
+    accept = run_accept_timings(device, stream)
+    e2e = run_e2e(vw4, layers["nvfp4"], device, stream, steps, warmup, world)
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": steps, "warmup": warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16 x f16 -> f32 (exact nibble*scale products, fp32 accumulate)",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": HEAD_M, "fmt": "nvfp4",
+                   "bytes_per_step": step_bytes(HEAD_M),
+                   "l2": "inputs larger than L2: 191.7 MB of weights+scales per step vs 129 MB L2",
+                   "timing": "CUDA graph of the step's 7 C-ABI calls, replayed back to back",
+                   "parallelism": f"replicas x{world}"},
+        "per_m": per_m, "gate": gate, "accept_us": accept, "roofline": roofline, "e2e": e2e,
+        "gpu_launches": steps * len(LAYER) * LAUNCHES_PER_GEMM,
+        "clocks": clk.summary(),
+    }
+    return result
+
+
+def run_accept_timings(device, stream):
+    """accept_rejection on the stochastic sweep (B=256, V=151936, K=1,4,8) and
+    accept_greedy on LM-head-sized logits (B=1, 7 drafts, V=262144)."""
+    import torch
+    import speculative_decode_verification_w4_gb300 as vw4
+    out = {}
+    g = torch.Generator(device=device).manual_seed(4)
+    B, V = 256, 151936
+    for Kd in (1, 4, 8):
+        tgt = torch.randn((B, Kd + 1, V), generator=g, device=device) * 3.0
+        drf = tgt[:, :Kd] + torch.randn((B, Kd, V), generator=g, device=device)
+        probs = torch.softmax(drf.reshape(-1, V) / 0.6, dim=-1)
+        drafts = torch.multinomial(probs, 1, generator=g).reshape(B, Kd).to(torch.int32)
+        del probs
+        ws = vw4.Workspace(device)
+        for _ in range(3):
+            vw4.accept_rejection(tgt, drf, drafts, 0.6, 0.95, 4, 0, workspace=ws, stream=stream)
+        torch.cuda.synchronize()
+        reps = 10
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for r in range(reps):
+            vw4.accept_rejection(tgt, drf, drafts, 0.6, 0.95, 4, r, workspace=ws, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) / reps * 1e3
+        out[f"rejection_K{Kd}"] = {"us": round(us, 1),
+                                   "logit_gbs": round(B * (2 * Kd + 1) * V * 4 / (us * 1e-6) / 1e9, 1)}
+        del tgt, drf
+    V = 262144
+    lg = torch.randn((1, 8, V), generator=g, device=device)
+    drafts = torch.argmax(lg[:, :7], dim=-1).to(torch.int32)
+    for _ in range(3):
+        vw4.accept_greedy(lg, drafts, stream=stream)
+    torch.cuda.synchronize()
+    reps = 20
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        vw4.accept_greedy(lg, drafts, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    out["greedy_lmhead_unfused"] = {"us": round(e0.elapsed_time(e1) / reps * 1e3, 2)}
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_e2e(vw4, layer, device, stream, steps, warmup, world):
+    """Same step through the public API with pinned host inputs and outputs:
+    every step copies the activation rows in and the fp32 results out."""
+    import torch
+    M = HEAD_M
+    g = np.random.default_rng(11)
+    host_in = []
+    for _, N, K, *_ in layer:
+        import synth
+        bits = synth.activations(g, M, K)
+        host_in.append(torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).pin_memory())
+    host_out = [torch.empty((M, N), dtype=torch.float32).pin_memory() for _, N, *_ in layer]
+    dev_in = [h.to(device) for h in host_in]
+    dev_out = [torch.empty((M, N), dtype=torch.float32, device=device) for _, N, *_ in layer]
+    ws = vw4.Workspace(device)
+
+    def step():
+        for j, (name, N, K, qd, sd, ts) in enumerate(layer):
+            dev_in[j].copy_(host_in[j], non_blocking=True)
+            vw4.verify_gemm_w4(vw4.FMT_NVFP4, qd, sd, ts, dev_in[j], out=dev_out[j], workspace=ws,
+                               stream=stream)
+            host_out[j].copy_(dev_out[j], non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = reduce_max(e0.elapsed_time(e1), world)
+    h2d = sum(M * K * 2 for _, N, K in LAYER)
+    d2h = sum(M * N * 4 for _, N, K in LAYER)
+    value = step_bytes(M) * steps * world / (ms * 1e-3) / 1e9
+    return {"value": round(value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------- CPU oracle timing
+class OracleWorkload:
+    """The same layer for the CPU oracle: all seven nvfp4 linears generated
+    once; a "sample" is a random subset of output rows of every linear."""
+
+    def __init__(self):
+        import oracle
+        import synth
+        oracle.build()
+        self.lin = [synth.linear(100 + i, N, K, "nvfp4") for i, (_, N, K) in enumerate(LAYER)]
+        g = synth.rng(11)
+        self.acts = [synth.activations(g, HEAD_M, K) for _, N, K in LAYER]
+
+    def run(self, frac: float, seed: int):
+        """Returns (GB/s over the sampled algorithmic bytes, rows, seconds)."""
+        import oracle
+        g = np.random.default_rng(seed)
+        rows, secs, nbytes = 0, 0.0, 0
+        for (name, N, K), (q, s, ts), A in zip(LAYER, self.lin, self.acts):
+            n = max(1, int(round(N * frac)))
+            cols = np.sort(g.choice(N, n, replace=False)).astype(np.int32)
+            t = time.perf_counter()
+            oracle.gemm_w4(oracle.FMT_NVFP4, N, K, q, s, ts, A, cols=cols)
+            secs += time.perf_counter() - t
+            rows += n
+            nbytes += weight_bytes(n, K) + HEAD_M * K * 2
+        return nbytes / secs / 1e9, rows, secs
+
+    def frac_for(self, budget_s: float) -> float:
+        """Sample fraction whose oracle time is about budget_s (one calibration run)."""
+        _, _, secs = self.run(0.01, 1)
+        return min(1.0, 0.01 * budget_s / max(secs, 1e-6))
+
+
+def cpu_cores():
+    return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max of a per-rank float over all ranks (identity for one process)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    backend = dist.get_backend()
+    dev = torch.device("cuda", torch.cuda.current_device()) if backend == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t[0])
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle as it stands, on this machine's host cores,
+    each step a bounded sample of the same workload.  Rank 0 only."""
+    if rank != 0:
+        return None
+    wl = OracleWorkload()
+    per_step_budget = max(0.5, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
+    frac = wl.frac_for(per_step_budget)
+    for k in range(args.warmup):
+        wl.run(frac, 1000 + k)
+    vals, rows = [], 0
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        v, rows, _ = wl.run(frac, 2000 + k)
+        vals.append(v)
+    wall = time.perf_counter() - t0
+    value = statistics.mean(vals)
+    sample = (f"each step: a {frac:.4%} random subset of the output rows of all 7 linears "
+              f"({rows} rows), M=8, nvfp4; fp64 dequantize-and-dot")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(wall / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": HEAD_M, "fmt": "nvfp4"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cpu_cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+
+    import torch
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+    res = run_ours(args, rank, world, device)
+    if rank == 0:
+        wl = OracleWorkload()
+        frac = wl.frac_for(args.cpu_budget)
+        v, rows, secs = wl.run(frac, 7)
+        res["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cpu_cores(),
+                               "kind": "oracle",
+                               "sample": f"{frac:.4%} of the output rows of all 7 linears "
+                                         f"({rows} rows, {secs:.1f} s), M=8, nvfp4"}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -81,9 +81,35 @@ vw4_status device_info(DeviceInfo** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// 2-D uint8 tensor map over a row-major [rows][inner_bytes] array.
+// 2-D uint8 tensor map over a row-major [rows][inner_bytes] array.  Maps
+// depend only on (address, shape, box, swizzle), so recent ones are cached
+// to keep the per-call host cost small.
+struct MapKey {
+    const void* base;
+    uint64_t inner, rows;
+    uint32_t box_inner, box_rows, sw;
+    bool operator==(const MapKey& o) const {
+        return base == o.base && inner == o.inner && rows == o.rows &&
+               box_inner == o.box_inner && box_rows == o.box_rows && sw == o.sw;
+    }
+};
+constexpr int kMapCache = 64;
+MapKey g_map_keys[kMapCache];
+CUtensorMap g_maps[kMapCache];
+int g_map_next = 0;
+std::mutex g_map_mu;
+
 vw4_status make_map(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t rows,
                     uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw) {
+    const MapKey key{base, inner_bytes, rows, box_inner, box_rows, static_cast<uint32_t>(sw)};
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        for (int i = 0; i < kMapCache; ++i)
+            if (g_map_keys[i] == key) {
+                *map = g_maps[i];
+                return VW4_OK;
+            }
+    }
     cuuint64_t dims[2] = {inner_bytes, rows};
     cuuint64_t strides[1] = {inner_bytes};
     cuuint32_t box[2] = {box_inner, box_rows};
@@ -97,6 +123,10 @@ vw4_status make_map(CUtensorMap* map, const void* base, uint64_t inner_bytes, ui
         g_last_error = buf;
         return VW4_ERR_CUDA;
     }
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    g_map_keys[g_map_next] = key;
+    g_maps[g_map_next] = *map;
+    g_map_next = (g_map_next + 1) % kMapCache;
     return VW4_OK;
 }
 
@@ -196,7 +226,7 @@ VW4_API vw4_status verify_gemm_w4(const vw4_weight* W, const void* A_dev, int M,
     if (G > U) G = U;
 
     cudaError_t e = launch_prep_act(static_cast<const uint16_t*>(A_dev), lda, K, W->fmt, M, 0, 1,
-                                    1, ws, n_tiles, s);
+                                    1, ws, n_tiles * kConsumerWarps, s);
     if (e != cudaSuccess) return cuda_fail(e, "prep_act launch");
     GemmParams p{};
     p.N = N;
@@ -205,10 +235,10 @@ VW4_API vw4_status verify_gemm_w4(const vw4_weight* W, const void* A_dev, int M,
     p.n_tiles = n_tiles;
     p.tensor_scale = W->tensor_scale;
     p.seg = ws.seg;
-    p.inv_scale = ws.inv_scale;
-    p.act16 = ws.act16;
+    p.act = ws.act;
     p.out = out_dev;
     p.ldo = ldo;
+    p.dense_M = M;
     p.argmax_M = row_argmax_dev ? M : 0;
     p.partials = ws.partials;
     p.tile_cnt = ws.tile_cnt;
@@ -269,7 +299,7 @@ VW4_API vw4_status verify_moe_w4(const vw4_weight* experts, int E, const void* A
                                  combine ? nullptr : out_dev, ldo, N, s);
     if (e != cudaSuccess) return cuda_fail(e, "route launch");
     e = launch_prep_act(static_cast<const uint16_t*>(A_dev), lda, K, experts->fmt, 0,
-                        rows_are_pairs, topk, P, ws, P * n_tiles, s);
+                        rows_are_pairs, topk, P, ws, P * n_tiles * kConsumerWarps, s);
     if (e != cudaSuccess) return cuda_fail(e, "prep_act launch");
     GemmParams p{};
     p.N = N;
@@ -278,10 +308,10 @@ VW4_API vw4_status verify_moe_w4(const vw4_weight* experts, int E, const void* A
     p.n_tiles = n_tiles;
     p.tensor_scale = experts->tensor_scale;
     p.seg = ws.seg;
-    p.inv_scale = ws.inv_scale;
-    p.act16 = ws.act16;
+    p.act = ws.act;
     p.out = combine ? ws.pair_out : out_dev;
     p.ldo = combine ? N : ldo;
+    p.dense_M = 0;
     p.argmax_M = 0;
     p.partials = ws.partials;
     p.tile_cnt = ws.tile_cnt;

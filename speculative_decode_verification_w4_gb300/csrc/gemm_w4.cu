@@ -57,10 +57,9 @@ GemmWorkspace gemm_workspace_layout(void* base, int n_seg_max, int N, int K, int
     const int T = K / kStageK;
     const int n_tiles = (N + kTileRows - 1) / kTileRows;
     w.seg = static_cast<SegTable*>(take(sizeof(SegTable)));
-    w.inv_scale = static_cast<float*>(take(sizeof(float) * kMaxSeg * kMaxRows));
-    w.act16 = static_cast<__half*>(take((size_t)n_seg_max * T * kMaxRows * kStageK * 2));
+    w.act = static_cast<uint8_t*>(take((size_t)n_seg_max * T * kAStride));
     w.partials = static_cast<float*>(take((size_t)2 * grid * kPartialFloats * sizeof(float)));
-    w.tile_cnt = static_cast<uint32_t*>(take((size_t)n_seg_max * n_tiles * 4));
+    w.tile_cnt = static_cast<uint32_t*>(take((size_t)n_seg_max * n_tiles * kConsumerWarps * 4));
     w.am_key = static_cast<unsigned long long*>(take(sizeof(unsigned long long) * kMaxRows));
     w.am_cnt = static_cast<uint32_t*>(take(4));
     w.pair_out = pair_rows ? static_cast<float*>(take((size_t)pair_rows * N * sizeof(float)))
@@ -78,44 +77,61 @@ __device__ __forceinline__ float pow2f(int n) {  // exact 2^n, n in [-126, 127]
     return __uint_as_float(static_cast<uint32_t>(n + 127) << 23);
 }
 
-// Position, in halves, of element e (0..255) of verify row r inside one
-// stage's [8][256] fp16 block.  The order puts each consumer lane's B
-// operand of consecutive MMAs in one 16-byte chunk, and the XOR keeps the
-// eight lanes of a quarter-warp on distinct bank groups.
-__device__ __forceinline__ int act_pos(int fmt, int r, int e) {
-    if (fmt == 1) {  // nvfp4: lane c covers elements [64c, 64c+64), 8 chunks
-        const int c = e >> 6, i = (e >> 3) & 7, j = e & 7;
-        const int sw = ((r & 1) << 2) | c;
-        return r * 256 + c * 64 + ((i ^ sw) << 3) + j;
-    } else {  // Q4_0: chunk (block, lane) = elements 4c+{0,2,1,3} and 16+4c+{0,2,1,3}
-        const int beta = e >> 5, ee = e & 31, half = ee >> 4, e2 = ee & 15, c = e2 >> 2,
-                  q = e2 & 3;
-        const int perm = (q == 0) ? 0 : (q == 1) ? 2 : (q == 2) ? 1 : 3;
-        const int chunk = ((beta << 2) | c) ^ ((r & 1) << 2);
-        return r * 256 + chunk * 8 + half * 4 + perm;
+// ------------------------------------------------------------- prep kernel
+// One warp per (segment, 256-wide k stage, verify row); each lane owns one
+// 16-byte chunk of the stage's fp16 block.  The row's values in the stage are
+// multiplied by 2^s so that their max lies in [2^14, 2^15) (exact; any bf16
+// magnitude then fits fp16), and 2^-s is stored after the block for the
+// GEMM's per-stage rescale.  Dense mode (dense_M > 0) writes the one-segment
+// table itself; MoE mode reads the table written by the router.  Block 0 also
+// resets the tickets of this call.
+__device__ __forceinline__ void load8_bf16(const uint16_t* a, bool vec, float (&x)[8]) {
+    if (vec) {
+        const uint4 u = *reinterpret_cast<const uint4*>(a);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            x[2 * j] = __uint_as_float(w[j] << 16);
+            x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] = bf16_to_f32(a[j]);
     }
 }
 
-// ------------------------------------------------------------- prep kernel
-// One block per (segment, verify row).  Dense mode (dense_M > 0) writes the
-// one-segment table itself; MoE mode reads the table written by the router.
-// Also resets the tickets of this call.
-__global__ void __launch_bounds__(256) prep_act_kernel(
-    const uint16_t* __restrict__ A, int lda, int K, int fmt, int dense_M, int rows_are_pairs,
-    int topk, SegTable* seg, float* inv_scale, __half* act16, uint32_t* tile_cnt, int n_cnt,
-    unsigned long long* am_key, uint32_t* am_cnt) {
-    const int s = blockIdx.x, r = blockIdx.y, tid = threadIdx.x;
-    const int T = K / kStageK;
-    if (s == 0 && r == 0) {
-        for (int i = tid; i < n_cnt; i += blockDim.x) tile_cnt[i] = 0u;
-        if (tid < kMaxRows) am_key[tid] = 0ull;
-        if (tid == 0) *am_cnt = 0u;
+__device__ __forceinline__ void load4_bf16(const uint16_t* a, bool vec, float* x) {
+    if (vec) {
+        const uint2 u = *reinterpret_cast<const uint2*>(a);
+        x[0] = __uint_as_float(u.x << 16);
+        x[1] = __uint_as_float(u.x & 0xFFFF0000u);
+        x[2] = __uint_as_float(u.y << 16);
+        x[3] = __uint_as_float(u.y & 0xFFFF0000u);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x[j] = bf16_to_f32(a[j]);
     }
-    int n_seg, count, src_row = 0;
+}
+
+__global__ void __launch_bounds__(256) prep_act_kernel(
+    const uint16_t* __restrict__ A, int lda, int vec_ok, int K, int fmt, int dense_M,
+    int rows_are_pairs, int topk, SegTable* seg, uint8_t* act, uint32_t* tile_cnt, int n_cnt,
+    unsigned long long* am_key, uint32_t* am_cnt) {
+    // the GEMM may start streaming weights now; it waits for this grid before
+    // touching the activations or the tickets
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int T = K / kStageK;
+    const int sgi = blockIdx.x / T, st = blockIdx.x % T;
+    const int r = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (blockIdx.x == 0) {
+        for (int i = threadIdx.x; i < n_cnt; i += blockDim.x) tile_cnt[i] = 0u;
+        if (threadIdx.x < kMaxRows) am_key[threadIdx.x] = 0ull;
+        if (threadIdx.x == 0) *am_cnt = 0u;
+    }
+    int count, src_row = 0;
     if (dense_M > 0) {
-        n_seg = 1;
         count = dense_M;
-        if (s == 0 && r == 0 && tid == 0) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
             seg->n_seg = 1;
             seg->expert[0] = 0;
             seg->count[0] = dense_M;
@@ -123,60 +139,76 @@ __global__ void __launch_bounds__(256) prep_act_kernel(
         }
         src_row = r;
     } else {
-        n_seg = seg->n_seg;
-        if (s >= n_seg) return;
-        count = seg->count[s];
+        if (sgi >= seg->n_seg) return;
+        count = seg->count[sgi];
         if (r < count) {
-            const int pr = seg->dest[s][r];
+            const int pr = seg->dest[sgi][r];
             src_row = rows_are_pairs ? pr : pr / topk;
         }
     }
-    if (s >= n_seg) return;
-    __half* dst = act16 + (size_t)s * T * (kMaxRows * kStageK);
+    uint8_t* blk = act + (static_cast<size_t>(sgi) * T + st) * kAStride;
+    __half* dst = reinterpret_cast<__half*>(blk);
+    float* inv = reinterpret_cast<float*>(blk + kABytes);
+    // Where this lane's 16-byte chunk goes in the stage's [8][256] block.  The
+    // order puts a consumer lane's B operands of consecutive MMAs in one chunk
+    // and the XOR keeps a quarter-warp's reads on distinct bank groups.
+    //  nvfp4: lane holds elements 8*lane .. 8*lane+7 (consumer lane c = lane/8
+    //         covers [64c, 64c+64) of the stage);
+    //  Q4_0:  lane = 4*beta + c holds elements 4c+{0,2,1,3} and 16+4c+{0,2,1,3}
+    //         of 32-element block beta.
+    int pos;
+    if (fmt == 1) {
+        const int c = lane >> 3, i = lane & 7;
+        pos = r * 256 + c * 64 + ((i ^ (((r & 1) << 2) | c)) << 3);
+    } else {
+        pos = r * 256 + ((lane ^ ((r & 1) << 2)) << 3);
+    }
     if (r >= count) {
-        for (int k = tid; k < K; k += blockDim.x)
-            dst[(size_t)(k >> 8) * (kMaxRows * kStageK) + act_pos(fmt, r, k & 255)] =
-                __float2half_rn(0.0f);
-        if (tid == 0) inv_scale[s * kMaxRows + r] = 0.0f;
+        *reinterpret_cast<uint4*>(dst + pos) = make_uint4(0u, 0u, 0u, 0u);
+        if (lane == 0) inv[r] = 0.0f;
         return;
     }
-    const uint16_t* a = A + (size_t)src_row * lda;
+    const uint16_t* a = A + static_cast<size_t>(src_row) * lda + st * kStageK;
+    float x[8];
+    if (fmt == 1) {
+        load8_bf16(a + 8 * lane, vec_ok != 0, x);
+    } else {
+        const int beta = lane >> 2, c = lane & 3;
+        float lo4[4], hi4[4];
+        load4_bf16(a + 32 * beta + 4 * c, vec_ok != 0, lo4);
+        load4_bf16(a + 32 * beta + 16 + 4 * c, vec_ok != 0, hi4);
+        x[0] = lo4[0]; x[1] = lo4[2]; x[2] = lo4[1]; x[3] = lo4[3];
+        x[4] = hi4[0]; x[5] = hi4[2]; x[6] = hi4[1]; x[7] = hi4[3];
+    }
     float amax = 0.0f;
     int bad = 0;
-    for (int k = tid; k < K; k += blockDim.x) {
-        const float v = fabsf(bf16_to_f32(a[k]));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float v = fabsf(x[j]);
         if (!(v <= 3.4e38f)) bad = 1;
         else amax = fmaxf(amax, v);
     }
-    __shared__ float s_max[8];
-    __shared__ int s_bad[8];
+#pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         bad |= __shfl_xor_sync(0xffffffffu, bad, o);
     }
-    if ((tid & 31) == 0) {
-        s_max[tid >> 5] = amax;
-        s_bad[tid >> 5] = bad;
-    }
-    __syncthreads();
-    amax = 0.0f;
-    bad = 0;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
-        amax = fmaxf(amax, s_max[w]);
-        bad |= s_bad[w];
-    }
     int n = 0;
     if (!bad && amax > 0.0f) {
-        int e;
-        frexpf(amax, &e);  // amax in [2^(e-1), 2^e)
-        n = 15 - e;        // scaled max in [2^14, 2^15)
+        int ex;
+        frexpf(amax, &ex);  // amax in [2^(ex-1), 2^ex)
+        n = 15 - ex;        // scaled max in [2^14, 2^15)
         n = n < -125 ? -125 : (n > 125 ? 125 : n);
     }
     const float sc = pow2f(n);
-    for (int k = tid; k < K; k += blockDim.x)
-        dst[(size_t)(k >> 8) * (kMaxRows * kStageK) + act_pos(fmt, r, k & 255)] =
-            __float2half_rn(bf16_to_f32(a[k]) * sc);
-    if (tid == 0) inv_scale[s * kMaxRows + r] = pow2f(-n);
+    uint32_t h[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const __half2 v = __floats2half2_rn(x[2 * j] * sc, x[2 * j + 1] * sc);
+        h[j] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+    *reinterpret_cast<uint4*>(dst + pos) = make_uint4(h[0], h[1], h[2], h[3]);
+    if (lane == 0) inv[r] = pow2f(-n);
 }
 
 // ------------------------------------------------------------ MoE router
@@ -287,96 +319,125 @@ __device__ __forceinline__ uint32_t q4pair(uint32_t x) {
     return hsub2((x & 0x000F000Fu) | 0x64006400u, 0x64086408u);
 }
 
-// One 256-wide k slice of the warp's 32 rows, nvfp4.
-//   lane (g, c): rows g and g+8 of each 16-row half; its k range is
+// One 256-wide k slice of the warp's 16 rows.  Each stage is split into a
+// load phase, which copies everything the warp needs out of the ring slot into
+// registers (after which the slot is released to the producer), and a compute
+// phase that works on registers only.
+//
+// nvfp4 -- lane (g, c): rows g and g+8 of the warp's tile; its k range is
 //   [64c, 64c+64) of the slice, i.e. 16-byte chunks 2c and 2c+1 of a row.
 //   MMA j takes elements 64c+4j .. 64c+4j+3 from every lane: the A operand
 //   pairs (k 2c,2c+1) and (k 2c+8,2c+9) of the mma fragment are mapped to
 //   these four consecutive elements, and the B operand uses the same map, so
-//   the sum over the slice is unchanged.
-__device__ __forceinline__ void stage_nvfp4(const uint8_t* __restrict__ W,
-                                            const uint8_t* __restrict__ S,
-                                            const uint8_t* __restrict__ Ab, int warp, int lane,
-                                            float (&acc)[2][4]) {
+//   the sum over the slice is unchanged.  Even and odd MMAs accumulate into
+//   two independent chains.
+struct StageRegsNv {
+    uint4 bf[8];          // B operand: this lane's 64 activations
+    uint4 w00, w01, w10, w11;  // rows g and g+8: chunks 2c, 2c+1
+    uint32_t s0, s1;      // four e4m3 block scales of rows g and g+8
+    float2 inv;           // 2^-s of verify rows 2c, 2c+1
+};
+
+__device__ __forceinline__ void load_nvfp4(const uint8_t* __restrict__ W,
+                                           const uint8_t* __restrict__ S,
+                                           const uint8_t* __restrict__ Ab, int warp, int lane,
+                                           StageRegsNv& r) {
     const int g = lane >> 2, c = lane & 3;
-    uint4 bf[8];
     const uint8_t* ab = Ab + g * 512 + c * 128;
     const int sw = ((g & 1) << 2) | c;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) bf[i] = lds128(ab + ((i ^ sw) << 4));
+    for (int i = 0; i < 8; ++i) r.bf[i] = lds128(ab + ((i ^ sw) << 4));
+    const int r0 = warp * 16 + g;
+    const uint8_t* w0 = W + r0 * 128;
+    const uint8_t* w1 = w0 + 8 * 128;
+    const int x0 = ((2 * c) ^ g) << 4, x1 = ((2 * c + 1) ^ g) << 4;  // 128-byte swizzle
+    r.w00 = lds128(w0 + x0);
+    r.w01 = lds128(w0 + x1);
+    r.w10 = lds128(w1 + x0);
+    r.w11 = lds128(w1 + x1);
+    r.s0 = lds32(S + r0 * 16 + 4 * c);
+    r.s1 = lds32(S + (r0 + 8) * 16 + 4 * c);
+    r.inv = *reinterpret_cast<const float2*>(Ab + kABytes + 8 * c);
+}
+
+__device__ __forceinline__ void compute_nvfp4(const StageRegsNv& r, float (&acc0)[4],
+                                              float (&acc1)[4]) {
+    uint32_t sa0, sb0, sa1, sb1;
+    cvt_e4m3x4(r.s0, sa0, sb0);
+    cvt_e4m3x4(r.s1, sa1, sb1);
+    const uint32_t sc0[4] = {__byte_perm(sa0, sa0, 0x1010), __byte_perm(sa0, sa0, 0x3232),
+                             __byte_perm(sb0, sb0, 0x1010), __byte_perm(sb0, sb0, 0x3232)};
+    const uint32_t sc1[4] = {__byte_perm(sa1, sa1, 0x1010), __byte_perm(sa1, sa1, 0x3232),
+                             __byte_perm(sb1, sb1, 0x1010), __byte_perm(sb1, sb1, 0x3232)};
+    const uint32_t wr0[8] = {r.w00.x, r.w00.y, r.w00.z, r.w00.w, r.w01.x, r.w01.y, r.w01.z, r.w01.w};
+    const uint32_t wr1[8] = {r.w10.x, r.w10.y, r.w10.z, r.w10.w, r.w11.x, r.w11.y, r.w11.z, r.w11.w};
 #pragma unroll
-    for (int t2 = 0; t2 < 2; ++t2) {
-        const int r0 = warp * 32 + t2 * 16 + g;
-        const uint8_t* w0 = W + r0 * 128;
-        const uint8_t* w1 = w0 + 8 * 128;
-        const int x0 = ((2 * c) ^ g) << 4, x1 = ((2 * c + 1) ^ g) << 4;  // 128-byte swizzle
-        const uint4 p00 = lds128(w0 + x0), p01 = lds128(w0 + x1);
-        const uint4 p10 = lds128(w1 + x0), p11 = lds128(w1 + x1);
-        uint32_t sa0, sb0, sa1, sb1;
-        cvt_e4m3x4(lds32(S + r0 * 16 + 4 * c), sa0, sb0);
-        cvt_e4m3x4(lds32(S + (r0 + 8) * 16 + 4 * c), sa1, sb1);
-        const uint32_t sc0[4] = {__byte_perm(sa0, sa0, 0x1010), __byte_perm(sa0, sa0, 0x3232),
-                                 __byte_perm(sb0, sb0, 0x1010), __byte_perm(sb0, sb0, 0x3232)};
-        const uint32_t sc1[4] = {__byte_perm(sa1, sa1, 0x1010), __byte_perm(sa1, sa1, 0x3232),
-                                 __byte_perm(sb1, sb1, 0x1010), __byte_perm(sb1, sb1, 0x3232)};
-        const uint32_t wr0[8] = {p00.x, p00.y, p00.z, p00.w, p01.x, p01.y, p01.z, p01.w};
-        const uint32_t wr1[8] = {p10.x, p10.y, p10.z, p10.w, p11.x, p11.y, p11.z, p11.w};
-#pragma unroll
-        for (int wi = 0; wi < 8; ++wi) {
-            uint32_t h0, h1, h2, h3, q0, q1, q2, q3;
-            cvt_e2m1x8(wr0[wi], h0, h1, h2, h3);
-            cvt_e2m1x8(wr1[wi], q0, q1, q2, q3);
-            const uint32_t s0 = sc0[wi >> 1], s1 = sc1[wi >> 1];
-            const uint32_t* b = reinterpret_cast<const uint32_t*>(&bf[wi]);
-            mma16816(acc[t2], hmul2(h0, s0), hmul2(q0, s1), hmul2(h1, s0), hmul2(q1, s1), b[0],
-                     b[1]);
-            mma16816(acc[t2], hmul2(h2, s0), hmul2(q2, s1), hmul2(h3, s0), hmul2(q3, s1), b[2],
-                     b[3]);
-        }
+    for (int wi = 0; wi < 8; ++wi) {
+        uint32_t h0, h1, h2, h3, q0, q1, q2, q3;
+        cvt_e2m1x8(wr0[wi], h0, h1, h2, h3);
+        cvt_e2m1x8(wr1[wi], q0, q1, q2, q3);
+        const uint32_t s0 = sc0[wi >> 1], s1 = sc1[wi >> 1];
+        const uint32_t* b = reinterpret_cast<const uint32_t*>(&r.bf[wi]);
+        mma16816(acc0, hmul2(h0, s0), hmul2(q0, s1), hmul2(h1, s0), hmul2(q1, s1), b[0], b[1]);
+        mma16816(acc1, hmul2(h2, s0), hmul2(q2, s1), hmul2(h3, s0), hmul2(q3, s1), b[2], b[3]);
     }
 }
 
-// One 256-wide k slice of the warp's 32 rows, Q4_0 (eight 32-element blocks).
-//   For block beta, lane (g, c) reads bytes 4c..4c+3 of the block: low
-//   nibbles are elements 4c..4c+3, high nibbles 4c+16..4c+19.  The two MMAs
-//   of a block run on exact integers (q - 8) into a zeroed temporary, and the
-//   block's fp16 scale is applied to the fp32 result.
-__device__ __forceinline__ void stage_q4_0(const uint8_t* __restrict__ W,
-                                           const uint8_t* __restrict__ S,
-                                           const uint8_t* __restrict__ Ab, int warp, int lane,
-                                           float (&acc)[2][4]) {
-    const int g = lane >> 2, c = lane & 3;
+// Q4_0 (eight 32-element blocks per slice) -- for block beta, lane (g, c)
+//   reads bytes 4c..4c+3 of the block: low nibbles are elements 4c..4c+3,
+//   high nibbles 4c+16..4c+19.  The two MMAs of a block run on exact integers
+//   (q - 8) into a zeroed temporary, and the block's fp16 scale is applied to
+//   the fp32 result.
+struct StageRegsQ4 {
     uint4 bf[8];
+    uint32_t x0[8], x1[8];  // rows g and g+8, bytes 4c..4c+3 of each block
+    uint4 d0, d1;           // the eight fp16 scales of rows g and g+8
+    float2 inv;
+};
+
+__device__ __forceinline__ void load_q4_0(const uint8_t* __restrict__ W,
+                                          const uint8_t* __restrict__ S,
+                                          const uint8_t* __restrict__ Ab, int warp, int lane,
+                                          StageRegsQ4& r) {
+    const int g = lane >> 2, c = lane & 3;
     const uint8_t* ab = Ab + g * 512;
 #pragma unroll
     for (int beta = 0; beta < 8; ++beta)
-        bf[beta] = lds128(ab + ((((beta << 2) | c) ^ ((g & 1) << 2)) << 4));
+        r.bf[beta] = lds128(ab + ((((beta << 2) | c) ^ ((g & 1) << 2)) << 4));
+    const int r0 = warp * 16 + g;
+    const uint8_t* w0 = W + r0 * 128 + 4 * c;
+    const uint8_t* w1 = w0 + 8 * 128;
 #pragma unroll
-    for (int t2 = 0; t2 < 2; ++t2) {
-        const int r0 = warp * 32 + t2 * 16 + g;
-        const uint8_t* w0 = W + r0 * 128 + 4 * c;
-        const uint8_t* w1 = w0 + 8 * 128;
-        const uint4 d0 = lds128(S + r0 * 16), d1 = lds128(S + (r0 + 8) * 16);
-        const uint32_t dw0[4] = {d0.x, d0.y, d0.z, d0.w};
-        const uint32_t dw1[4] = {d1.x, d1.y, d1.z, d1.w};
+    for (int beta = 0; beta < 8; ++beta) {
+        r.x0[beta] = lds32(w0 + ((beta ^ g) << 4));
+        r.x1[beta] = lds32(w1 + ((beta ^ g) << 4));
+    }
+    r.d0 = lds128(S + r0 * 16);
+    r.d1 = lds128(S + (r0 + 8) * 16);
+    r.inv = *reinterpret_cast<const float2*>(Ab + kABytes + 8 * c);
+}
+
+__device__ __forceinline__ void compute_q4_0(const StageRegsQ4& r, float (&acc0)[4],
+                                             float (&acc1)[4]) {
+    const uint32_t dw0[4] = {r.d0.x, r.d0.y, r.d0.z, r.d0.w};
+    const uint32_t dw1[4] = {r.d1.x, r.d1.y, r.d1.z, r.d1.w};
 #pragma unroll
-        for (int beta = 0; beta < 8; ++beta) {
-            const uint32_t x0 = lds32(w0 + ((beta ^ g) << 4));
-            const uint32_t x1 = lds32(w1 + ((beta ^ g) << 4));
-            const uint32_t* b = reinterpret_cast<const uint32_t*>(&bf[beta]);
-            float t[4] = {0.f, 0.f, 0.f, 0.f};
-            mma16816(t, q4pair(x0), q4pair(x1), q4pair(x0 >> 8), q4pair(x1 >> 8), b[0], b[1]);
-            mma16816(t, q4pair(x0 >> 4), q4pair(x1 >> 4), q4pair(x0 >> 12), q4pair(x1 >> 12),
-                     b[2], b[3]);
-            const __half2 dh0 = *reinterpret_cast<const __half2*>(&dw0[beta >> 1]);
-            const __half2 dh1 = *reinterpret_cast<const __half2*>(&dw1[beta >> 1]);
-            const float e0 = (beta & 1) ? __high2float(dh0) : __low2float(dh0);
-            const float e1 = (beta & 1) ? __high2float(dh1) : __low2float(dh1);
-            acc[t2][0] = fmaf(e0, t[0], acc[t2][0]);
-            acc[t2][1] = fmaf(e0, t[1], acc[t2][1]);
-            acc[t2][2] = fmaf(e1, t[2], acc[t2][2]);
-            acc[t2][3] = fmaf(e1, t[3], acc[t2][3]);
-        }
+    for (int beta = 0; beta < 8; ++beta) {
+        const uint32_t x0 = r.x0[beta], x1 = r.x1[beta];
+        const uint32_t* b = reinterpret_cast<const uint32_t*>(&r.bf[beta]);
+        float t[4] = {0.f, 0.f, 0.f, 0.f};
+        mma16816(t, q4pair(x0), q4pair(x1), q4pair(x0 >> 8), q4pair(x1 >> 8), b[0], b[1]);
+        mma16816(t, q4pair(x0 >> 4), q4pair(x1 >> 4), q4pair(x0 >> 12), q4pair(x1 >> 12), b[2],
+                 b[3]);
+        const __half2 dh0 = *reinterpret_cast<const __half2*>(&dw0[beta >> 1]);
+        const __half2 dh1 = *reinterpret_cast<const __half2*>(&dw1[beta >> 1]);
+        const float e0 = (beta & 1) ? __high2float(dh0) : __low2float(dh0);
+        const float e1 = (beta & 1) ? __high2float(dh1) : __low2float(dh1);
+        float(&acc)[4] = (beta & 1) ? acc1 : acc0;
+        acc[0] = fmaf(e0, t[0], acc[0]);
+        acc[1] = fmaf(e0, t[1], acc[1]);
+        acc[2] = fmaf(e1, t[2], acc[2]);
+        acc[3] = fmaf(e1, t[3], acc[3]);
     }
 }
 
@@ -415,6 +476,14 @@ __device__ void argmax_finish(const GemmParams& p, int lane) {
     }
 }
 
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependents_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 template <int FMT>
 __global__ void __launch_bounds__(kGemmThreads, 2)
     gemm_w4_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
@@ -422,7 +491,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSmemBar);
     uint64_t* empty = full + kStages;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
 
@@ -442,7 +511,9 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     __syncthreads();
 
     const int T = p.T, n_tiles = p.n_tiles;
-    const int n_seg = p.seg->n_seg;
+    // Dense calls pass the one-segment shape directly; MoE calls read the
+    // router's table, which is complete before this grid's predecessor ran.
+    const int n_seg = p.dense_M > 0 ? 1 : p.seg->n_seg;
     // Effective grid: never more CTAs than units, so every active CTA owns at
     // least one unit (the contributor arithmetic of split tiles relies on it).
     const unsigned long long U = static_cast<unsigned long long>(n_seg) * n_tiles * T;
@@ -454,28 +525,53 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------ producer
         if (lane != 0) return;
-        const uint64_t pol_w = policy_evict_first();
-        const uint64_t pol_a = policy_evict_last();
+        const uint64_t pol_w = policy_evict_first();   // nibbles: read exactly once
+        const uint64_t pol_s = policy_evict_normal();  // scale sectors span two stages
+        const uint64_t pol_a = policy_evict_last();    // activations: reread by every tile
         uint32_t it = 0;
         bool ok = true;
-        for (unsigned long long u = u_begin; u < u_end; ++u, ++it) {
+        // The weights do not depend on the activation prep: start streaming
+        // the first kStages units before waiting for it.
+        const unsigned long long n_pre =
+            (u_end - u_begin) < static_cast<unsigned long long>(kStages) ? (u_end - u_begin)
+                                                                          : kStages;
+        for (unsigned long long u = u_begin; u < u_begin + n_pre; ++u, ++it) {
+            const unsigned long long tg = u / T;
+            const int st = static_cast<int>(u % T);
+            const int sg = static_cast<int>(tg / n_tiles), tile = static_cast<int>(tg % n_tiles);
+            const int expert = p.dense_M > 0 ? 0 : p.seg->expert[sg];
+            const int row0 = expert * p.N + tile * kTileRows;
+            mbar_arrive_expect_tx(&full[it], kStageBytes);
+            tma_load_2d(smem + it * kWBytes, &tmW, st * (kStageK / 2), row0, &full[it], pol_w);
+            tma_load_2d(smem + kSmemS + it * kSBytes, &tmS, st * 16, row0, &full[it], pol_s);
+        }
+        grid_dependency_wait();
+        for (uint32_t j = 0; j < it; ++j) {
+            const unsigned long long u = u_begin + j;
+            const unsigned long long tg = u / T;
+            const int st = static_cast<int>(u % T);
+            const int sg = static_cast<int>(tg / n_tiles);
+            bulk_load(smem + kSmemA + j * kAStride,
+                      p.act + (static_cast<size_t>(sg) * T + st) * kAStride, kAStride, &full[j],
+                      pol_a);
+        }
+        for (unsigned long long u = u_begin + n_pre; u < u_end; ++u, ++it) {
             const int s = it % kStages;
-            if (it >= (uint32_t)kStages &&
-                !mbar_wait_bounded(&empty[s], ((it / kStages) - 1) & 1, p.wait_ns, abort_flag)) {
+            if (!mbar_wait_bounded(&empty[s], ((it / kStages) - 1) & 1, p.wait_ns, abort_flag)) {
                 ok = false;
                 break;
             }
             const unsigned long long tg = u / T;
             const int st = static_cast<int>(u % T);
             const int sg = static_cast<int>(tg / n_tiles), tile = static_cast<int>(tg % n_tiles);
-            const int row0 = p.seg->expert[sg] * p.N + tile * kTileRows;
-            uint8_t* slot = smem + s * kStageBytes;
+            const int expert = p.dense_M > 0 ? 0 : p.seg->expert[sg];
+            const int row0 = expert * p.N + tile * kTileRows;
             mbar_arrive_expect_tx(&full[s], kStageBytes);
-            tma_load_2d(slot, &tmW, st * (kStageK / 2), row0, &full[s], pol_w);
-            tma_load_2d(slot + kWBytes, &tmS, st * 16, row0, &full[s], pol_w);
-            bulk_load(slot + kWBytes + kSBytes,
-                      p.act16 + (static_cast<size_t>(sg) * T + st) * (kMaxRows * kStageK),
-                      kABytes, &full[s], pol_a);
+            tma_load_2d(smem + s * kWBytes, &tmW, st * (kStageK / 2), row0, &full[s], pol_w);
+            tma_load_2d(smem + kSmemS + s * kSBytes, &tmS, st * 16, row0, &full[s], pol_s);
+            bulk_load(smem + kSmemA + s * kAStride,
+                      p.act + (static_cast<size_t>(sg) * T + st) * kAStride, kAStride, &full[s],
+                      pol_a);
         }
         if (!ok) {
             atomicOr(p.status, kStatusTimeout);
@@ -489,6 +585,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     }
 
     // ---------------------------------------------------------- consumers
+    grid_dependency_wait();  // activations, scales of this call, tickets reset
     const int g = lane >> 2, c = lane & 3;
     uint32_t it = 0;
     const unsigned long long my_first_tile = u_begin / T;
@@ -499,11 +596,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         const int st_end = (left < static_cast<unsigned long long>(T - st0))
                                ? st0 + static_cast<int>(left)
                                : T;
-        float acc[2][4];
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-            for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
+        float tot[4] = {0.f, 0.f, 0.f, 0.f};
         for (int st = st0; st < st_end; ++st, ++it) {
             const int s = it % kStages;
             if (!mbar_wait_bounded(&full[s], (it / kStages) & 1, p.wait_ns, abort_flag)) {
@@ -511,54 +604,62 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                 *abort_flag = 1;
                 return;
             }
-            const uint8_t* slot = smem + s * kStageBytes;
-            if (FMT == 1)
-                stage_nvfp4(slot, slot + kWBytes, slot + kWBytes + kSBytes, warp, lane, acc);
-            else
-                stage_q4_0(slot, slot + kWBytes, slot + kWBytes + kSBytes, warp, lane, acc);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
+            const uint8_t* Ws = smem + s * kWBytes;
+            const uint8_t* Ss = smem + kSmemS + s * kSBytes;
+            const uint8_t* As = smem + kSmemA + s * kAStride;
+            float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+            float2 inv;
+            if (FMT == 1) {
+                StageRegsNv r;
+                load_nvfp4(Ws, Ss, As, warp, lane, r);
+                __syncwarp();  // every lane's reads of the slot are done:
+                if (lane == 0) mbar_arrive(&empty[s]);  // the producer may refill it
+                compute_nvfp4(r, acc0, acc1);
+                inv = r.inv;
+            } else {
+                StageRegsQ4 r;
+                load_q4_0(Ws, Ss, As, warp, lane, r);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+                compute_q4_0(r, acc0, acc1);
+                inv = r.inv;
+            }
+            // this stage's activations were scaled by 2^s per verify row
+            tot[0] = fmaf(inv.x, acc0[0] + acc1[0], tot[0]);
+            tot[1] = fmaf(inv.y, acc0[1] + acc1[1], tot[1]);
+            tot[2] = fmaf(inv.x, acc0[2] + acc1[2], tot[2]);
+            tot[3] = fmaf(inv.y, acc0[3] + acc1[3], tot[3]);
         }
         u += static_cast<unsigned long long>(st_end - st0);
 
         // ------------------------------------------------------ epilogue
         const int sg = static_cast<int>(tg / n_tiles), tile = static_cast<int>(tg % n_tiles);
-        const int count = p.seg->count[sg];
-        const float sc0 = p.tensor_scale * p.inv_scale[sg * kMaxRows + 2 * c];
-        const float sc1 = p.tensor_scale * p.inv_scale[sg * kMaxRows + 2 * c + 1];
-        float v[2][4];
-#pragma unroll
-        for (int t2 = 0; t2 < 2; ++t2) {
-            v[t2][0] = acc[t2][0] * sc0;
-            v[t2][1] = acc[t2][1] * sc1;
-            v[t2][2] = acc[t2][2] * sc0;
-            v[t2][3] = acc[t2][3] * sc1;
-        }
+        const int count = p.dense_M > 0 ? p.dense_M : p.seg->count[sg];
+        const float v[4] = {tot[0] * p.tensor_scale, tot[1] * p.tensor_scale,
+                            tot[2] * p.tensor_scale, tot[3] * p.tensor_scale};
         const int n0 = tile * kTileRows;
         const bool whole = (st0 == 0 && st_end == T);
         if (whole) {
 #pragma unroll
-            for (int t2 = 0; t2 < 2; ++t2)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int tok = 2 * c + (q & 1);
-                    const int n = n0 + warp * 32 + t2 * 16 + g + ((q & 2) ? 8 : 0);
-                    if (tok < count && n < p.N)
-                        p.out[static_cast<size_t>(p.seg->dest[sg][tok]) * p.ldo + n] = v[t2][q];
+            for (int q = 0; q < 4; ++q) {
+                const int tok = 2 * c + (q & 1);
+                const int n = n0 + warp * 16 + g + ((q & 2) ? 8 : 0);
+                if (tok < count && n < p.N) {
+                    const int dest = p.dense_M > 0 ? tok : p.seg->dest[sg][tok];
+                    p.out[static_cast<size_t>(dest) * p.ldo + n] = v[q];
                 }
+            }
             if (p.argmax_M > 0) {
                 unsigned long long k0 = 0ull, k1 = 0ull;  // tokens 2c, 2c+1
 #pragma unroll
-                for (int t2 = 0; t2 < 2; ++t2)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int n = n0 + warp * 32 + t2 * 16 + g + ((q & 2) ? 8 : 0);
-                        if (n < p.N) {
-                            const unsigned long long k = am_key(v[t2][q], static_cast<uint32_t>(n));
-                            if (q & 1) k1 = umax64(k1, k);
-                            else k0 = umax64(k0, k);
-                        }
+                for (int q = 0; q < 4; ++q) {
+                    const int n = n0 + warp * 16 + g + ((q & 2) ? 8 : 0);
+                    if (n < p.N) {
+                        const unsigned long long k = am_key(v[q], static_cast<uint32_t>(n));
+                        if (q & 1) k1 = umax64(k1, k);
+                        else k0 = umax64(k0, k);
                     }
+                }
 #pragma unroll
                 for (int o = 4; o < 32; o <<= 1) {
                     k0 = umax64(k0, __shfl_xor_sync(0xffffffffu, k0, o));
@@ -573,11 +674,13 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                 uint32_t old = 0;
                 if (lane == 0) old = atomicAdd(p.am_cnt, 1u);
                 old = __shfl_sync(0xffffffffu, old, 0);
-                if (old + 1 == 4u * static_cast<uint32_t>(n_tiles)) argmax_finish(p, lane);
+                if (old + 1 == static_cast<uint32_t>(kConsumerWarps * n_tiles))
+                    argmax_finish(p, lane);
             }
             continue;
         }
-        // partial tile: publish my slice, then the last contributing warp sums
+        // Partial tile: publish this warp's 16-row slice; the last of the
+        // tile's contributors to arrive for this slice sums it in k order.
         const unsigned long long tile_u0 = tg * static_cast<unsigned long long>(T);
         const unsigned long long i_lo = R.owner(tile_u0), i_hi = R.owner(tile_u0 + T - 1);
         const uint32_t n_contrib = static_cast<uint32_t>(i_hi - i_lo + 1);
@@ -585,73 +688,71 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             2ull * blockIdx.x + ((my_first_tile == tg) ? 0ull : 1ull);
         float* part = p.partials + my_slot * kPartialFloats;
 #pragma unroll
-        for (int t2 = 0; t2 < 2; ++t2)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int tok = 2 * c + (q & 1);
-                const int r = warp * 32 + t2 * 16 + g + ((q & 2) ? 8 : 0);
-                __stcg(&part[tok * kTileRows + r], v[t2][q]);
-            }
+        for (int q = 0; q < 4; ++q) {
+            const int tok = 2 * c + (q & 1);
+            const int r = warp * 16 + g + ((q & 2) ? 8 : 0);
+            __stcg(&part[tok * kTileRows + r], v[q]);
+        }
         __threadfence();
         __syncwarp();
         uint32_t old = 0;
-        if (lane == 0) old = atomicAdd(&p.tile_cnt[tg], 1u);
+        if (lane == 0) old = atomicAdd(&p.tile_cnt[tg * kConsumerWarps + warp], 1u);
         old = __shfl_sync(0xffffffffu, old, 0);
-        if (old + 1 != static_cast<uint32_t>(kConsumerWarps) * n_contrib) continue;
+        if (old + 1 != n_contrib) continue;
         __threadfence();
-        // This warp sums the 8 x 128 values in contributor (= k) order.  Every
-        // contributor after the first starts inside this tile, so its slot is
-        // its "first tile" slot; only the first may end in it instead.
+        // Every contributor after the first starts inside this tile, so its
+        // slot is its "first tile" slot; only the first may end in it instead.
         const unsigned long long slot_lo =
             2ull * i_lo + ((R.start(i_lo) / T == tg) ? 0ull : 1ull);
-        float4 sum[kMaxRows];
-#pragma unroll
-        for (int tok = 0; tok < kMaxRows; ++tok) sum[tok] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (unsigned long long i = i_lo; i <= i_hi; ++i) {
-            const unsigned long long slot = (i == i_lo) ? slot_lo : 2ull * i;
-            const float4* src =
-                reinterpret_cast<const float4*>(p.partials + slot * kPartialFloats) + lane;
-            float4 x[kMaxRows];
-#pragma unroll
-            for (int tok = 0; tok < kMaxRows; ++tok) x[tok] = __ldcg(src + tok * (kTileRows / 4));
-#pragma unroll
-            for (int tok = 0; tok < kMaxRows; ++tok) {
-                sum[tok].x += x[tok].x;
-                sum[tok].y += x[tok].y;
-                sum[tok].z += x[tok].z;
-                sum[tok].w += x[tok].w;
-            }
+        const int tok = lane >> 2;
+        const int rr = warp * 16 + 4 * (lane & 3);
+        const size_t off = static_cast<size_t>(tok) * kTileRows + rr;
+        auto slot_of = [&](unsigned long long i) { return i == i_lo ? slot_lo : 2ull * i; };
+        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+        unsigned long long i = i_lo;
+        for (; i + 3 <= i_hi; i += 4) {  // four loads in flight, summed in order
+            const float4 x0 = __ldcg(reinterpret_cast<const float4*>(
+                p.partials + slot_of(i) * kPartialFloats + off));
+            const float4 x1 = __ldcg(reinterpret_cast<const float4*>(
+                p.partials + slot_of(i + 1) * kPartialFloats + off));
+            const float4 x2 = __ldcg(reinterpret_cast<const float4*>(
+                p.partials + slot_of(i + 2) * kPartialFloats + off));
+            const float4 x3 = __ldcg(reinterpret_cast<const float4*>(
+                p.partials + slot_of(i + 3) * kPartialFloats + off));
+            sum.x += x0.x; sum.y += x0.y; sum.z += x0.z; sum.w += x0.w;
+            sum.x += x1.x; sum.y += x1.y; sum.z += x1.z; sum.w += x1.w;
+            sum.x += x2.x; sum.y += x2.y; sum.z += x2.z; sum.w += x2.w;
+            sum.x += x3.x; sum.y += x3.y; sum.z += x3.z; sum.w += x3.w;
         }
-        unsigned long long kbest[kMaxRows];
-#pragma unroll
-        for (int tok = 0; tok < kMaxRows; ++tok) {
-            kbest[tok] = 0ull;
-            if (tok >= count) continue;
-            const float sv[4] = {sum[tok].x, sum[tok].y, sum[tok].z, sum[tok].w};
-            float* orow = p.out + static_cast<size_t>(p.seg->dest[sg][tok]) * p.ldo;
+        for (; i <= i_hi; ++i) {
+            const float4 x0 = __ldcg(reinterpret_cast<const float4*>(
+                p.partials + slot_of(i) * kPartialFloats + off));
+            sum.x += x0.x; sum.y += x0.y; sum.z += x0.z; sum.w += x0.w;
+        }
+        const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
+        unsigned long long kb = 0ull;
+        if (tok < count) {
+            const int dest = p.dense_M > 0 ? tok : p.seg->dest[sg][tok];
+            float* orow = p.out + static_cast<size_t>(dest) * p.ldo;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const int n = n0 + 4 * lane + j;
+                const int n = n0 + rr + j;
                 if (n < p.N) {
                     orow[n] = sv[j];
-                    kbest[tok] = umax64(kbest[tok], am_key(sv[j], static_cast<uint32_t>(n)));
+                    kb = umax64(kb, am_key(sv[j], static_cast<uint32_t>(n)));
                 }
             }
         }
         if (p.argmax_M > 0) {
-#pragma unroll
-            for (int tok = 0; tok < kMaxRows; ++tok) {
-                unsigned long long k = kbest[tok];
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) k = umax64(k, __shfl_xor_sync(0xffffffffu, k, o));
-                if (lane == 0 && tok < p.argmax_M && k) atomicMax(&p.am_key[tok], k);
-            }
+            kb = umax64(kb, __shfl_xor_sync(0xffffffffu, kb, 1));
+            kb = umax64(kb, __shfl_xor_sync(0xffffffffu, kb, 2));
+            if ((lane & 3) == 0 && tok < p.argmax_M && kb) atomicMax(&p.am_key[tok], kb);
             __threadfence();
             __syncwarp();
             uint32_t o2 = 0;
-            if (lane == 0) o2 = atomicAdd(p.am_cnt, static_cast<uint32_t>(kConsumerWarps));
+            if (lane == 0) o2 = atomicAdd(p.am_cnt, 1u);
             o2 = __shfl_sync(0xffffffffu, o2, 0);
-            if (o2 + kConsumerWarps == 4u * static_cast<uint32_t>(n_tiles)) argmax_finish(p, lane);
+            if (o2 + 1 == static_cast<uint32_t>(kConsumerWarps * n_tiles)) argmax_finish(p, lane);
         }
     }
 }
@@ -691,10 +792,11 @@ __global__ void q4_0_split_kernel(const uint8_t* __restrict__ blocks, int N, int
 cudaError_t launch_prep_act(const uint16_t* A, int lda, int K, int fmt, int dense_M,
                             int rows_are_pairs, int topk, int n_seg_grid, const GemmWorkspace& ws,
                             int n_counters, cudaStream_t s) {
-    dim3 grid(n_seg_grid, kMaxRows);
-    prep_act_kernel<<<grid, 256, 0, s>>>(A, lda, K, fmt, dense_M, rows_are_pairs, topk, ws.seg,
-                                         ws.inv_scale, ws.act16, ws.tile_cnt, n_counters,
-                                         ws.am_key, ws.am_cnt);
+    const int T = K / kStageK;
+    const int vec_ok = ((reinterpret_cast<uintptr_t>(A) & 15u) == 0 && lda % 8 == 0) ? 1 : 0;
+    prep_act_kernel<<<n_seg_grid * T, 256, 0, s>>>(A, lda, vec_ok, K, fmt, dense_M,
+                                                   rows_are_pairs, topk, ws.seg, ws.act,
+                                                   ws.tile_cnt, n_counters, ws.am_key, ws.am_cnt);
     return cudaGetLastError();
 }
 
@@ -708,8 +810,17 @@ static cudaError_t launch_gemm_t(const CUtensorMap& tmW, const CUtensorMap& tmS,
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    gemm_w4_kernel<FMT><<<grid, kGemmThreads, kGemmSmem, s>>>(tmW, tmS, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = kGemmSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_w4_kernel<FMT>, tmW, tmS, p);
 }
 
 cudaError_t launch_gemm(int fmt, const CUtensorMap& tmW, const CUtensorMap& tmS,

@@ -17,18 +17,24 @@
 //   residual  r_v = max(0, p_v * Sq - q_v * Sp), inverse CDF with a 64-bit
 //   uniform; bonus from p_Kd when every draft is accepted.
 //
-// Three kernels:
-//  1. row statistics, one thread-block cluster per logits row: the row is
-//     held in the cluster's shared memory (a slice per CTA); max and sum are
-//     combined through distributed shared memory, and the top-p cut is found
-//     by an exact radix search on W (a log-scale histogram, then 8-bit
-//     digits inside the crossing bucket), histograms merged over DSMEM.
-//     Output per row: max, threshold tau, cut index among W == tau, kept sum.
-//  2. accept decisions, one thread per sequence (Philox4x32-10 uniforms).
-//  3. the residual or bonus draw, one CTA per sequence: an exact u128 total,
-//     then an ordered scan in 4096-element tiles.
+// Kernel 1, one thread-block cluster per (sequence b, position i):
+//   * the target row (b, i) and, for i < Kd, the draft row (b, i) are loaded
+//     once into the cluster's shared memory, a slice per CTA;
+//   * per row: max and sum W over the cluster (DSMEM), a log-scale histogram
+//     of W finds the bucket where the top-p prefix ends; its members are
+//     gathered to rank 0, sorted by (W desc, index asc) and scanned, which
+//     gives the exact cut (an exact radix search over the slices is the
+//     fallback when that bucket is too crowded);
+//   * the acceptance test of draft i (Philox block (i, b)), and, only if it
+//     is rejected, the residual draw -- or, for i = Kd, the bonus draw --
+//     from the rows already on chip: an exact u128 total, then an ordered
+//     search across the cluster's slices.
+// Kernel 2, one thread per sequence: the first rejected position decides the
+// committed run.  Rows after the first rejection are evaluated in parallel
+// and discarded.
 #include <cooperative_groups.h>
 
+#include "ptx.cuh"
 #include "vw4_internal.cuh"
 
 namespace cg = cooperative_groups;
@@ -39,29 +45,27 @@ namespace {
 
 constexpr uint32_t kStatusBadDraft = 0x1u;
 constexpr uint32_t kStatusZeroResidual = 0x8u;
-constexpr int kStatThreads = 512;
-constexpr int kSampleThreads = 1024;
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
 constexpr int kLogBuckets = 16 + 37 * 8;  // exact 0..15, then 8 per binade up to 2^40
 constexpr int kLinBuckets = 256;
-constexpr int kMaxSlice = 49152;  // floats per CTA (192 KB)
+constexpr int kCandLocal = 512;   // candidates one CTA may hold per row
+constexpr int kCandTotal = 2048;  // candidates the cluster may gather per row
+constexpr int kMaxSlice = 20480;  // floats per CTA per row (two rows on chip)
 constexpr unsigned long long kKeepAll = 1ull << 32;
 
 typedef unsigned __int128 u128;
 
-struct RowStat {
+struct RowInfo {
     float mx;
     int cut;                 // largest kept index among W == tau
     unsigned long long tau;  // kept: W > tau, or W == tau and v <= cut
     unsigned long long S;    // kept sum
-    unsigned long long pad;
 };
 
-struct SeqState {
-    int mode;  // 0 residual at pos, 1 bonus from target row Kd, 2 residual forced (bad id)
-    int pos;
-    int n;
-    int pad;
-    unsigned long long u64;
+struct PairOut {
+    int accept;  // 1: draft i accepted (or the bonus row)
+    int token;   // residual draw at a rejection; bonus draw for i == Kd
 };
 
 // ------------------------------------------------------------- own exp
@@ -93,11 +97,7 @@ __device__ __forceinline__ unsigned long long mass_of(float e) {
     return __float2ull_rz(__fmul_rn(e, 1099511627776.0f));  // e * 2^40 is exact
 }
 
-__device__ __forceinline__ unsigned long long mass_at(float l, float mx, float invT) {
-    return mass_of(own_exp(scaled_x(l, mx, invT)));
-}
-
-__device__ __forceinline__ unsigned long long kept(unsigned long long W, int v, const RowStat& s) {
+__device__ __forceinline__ unsigned long long kept(unsigned long long W, int v, const RowInfo& s) {
     return (W > s.tau || (W == s.tau && v <= s.cut)) ? W : 0ull;
 }
 
@@ -129,152 +129,174 @@ __device__ __forceinline__ void philox4x32_10(uint32_t c0, uint32_t c1, uint32_t
     out[3] = c3;
 }
 
-__device__ __forceinline__ void philox_at(unsigned long long seed, unsigned long long offset,
-                                          uint32_t i, uint32_t b, uint32_t r[4]) {
-    philox4x32_10(i, b, static_cast<uint32_t>(offset), static_cast<uint32_t>(offset >> 32),
-                  static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32), r);
-}
-
-// ------------------------------------------------------- block reductions
-__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
+// --------------------------------------------------------------- helpers
 __device__ __forceinline__ u128 shfl_xor_u128(u128 v, int o) {
-    const unsigned long long lo = static_cast<unsigned long long>(v);
-    const unsigned long long hi = static_cast<unsigned long long>(v >> 64);
-    const unsigned long long l2 = __shfl_xor_sync(0xffffffffu, lo, o);
-    const unsigned long long h2 = __shfl_xor_sync(0xffffffffu, hi, o);
-    return (static_cast<u128>(h2) << 64) | l2;
+    const unsigned long long lo = __shfl_xor_sync(0xffffffffu, static_cast<unsigned long long>(v), o);
+    const unsigned long long hi =
+        __shfl_xor_sync(0xffffffffu, static_cast<unsigned long long>(v >> 64), o);
+    return (static_cast<u128>(hi) << 64) | lo;
 }
 
 __device__ __forceinline__ u128 shfl_up_u128(u128 v, int o) {
-    const unsigned long long lo = static_cast<unsigned long long>(v);
-    const unsigned long long hi = static_cast<unsigned long long>(v >> 64);
-    const unsigned long long l2 = __shfl_up_sync(0xffffffffu, lo, o);
-    const unsigned long long h2 = __shfl_up_sync(0xffffffffu, hi, o);
-    return (static_cast<u128>(h2) << 64) | l2;
+    const unsigned long long lo = __shfl_up_sync(0xffffffffu, static_cast<unsigned long long>(v), o);
+    const unsigned long long hi =
+        __shfl_up_sync(0xffffffffu, static_cast<unsigned long long>(v >> 64), o);
+    return (static_cast<u128>(hi) << 64) | lo;
 }
 
 // floor(u * R / 2^64) for a 64-bit u and a 128-bit R (< 2^120 here)
 __device__ __forceinline__ u128 scale_u64(unsigned long long u, u128 R) {
-    const unsigned long long rlo = static_cast<unsigned long long>(R);
-    const unsigned long long rhi = static_cast<unsigned long long>(R >> 64);
-    const u128 lo = static_cast<u128>(u) * rlo;
-    const u128 hi = static_cast<u128>(u) * rhi;
+    const u128 lo = static_cast<u128>(u) * static_cast<unsigned long long>(R);
+    const u128 hi = static_cast<u128>(u) * static_cast<unsigned long long>(R >> 64);
     return (lo >> 64) + hi;
 }
 
-// ------------------------------------------------------ kernel 1: row stats
-struct StatSmem {
-    unsigned int cnt[2][kLogBuckets];
-    unsigned long long mass[2][kLogBuckets];
-    unsigned int mcnt[kLogBuckets];
+struct Smem {
+    unsigned int cnt[kLogBuckets];         // this CTA's histogram (read by peers)
+    unsigned long long mass[kLogBuckets];
+    unsigned int mcnt[kLogBuckets];        // the cluster's merged histogram
     unsigned long long mmass[kLogBuckets];
-    float fred[kStatThreads / 32];
-    unsigned long long ured[kStatThreads / 32];
-    float lmax;               // this CTA's max (read by peers)
-    unsigned long long lsum;  // this CTA's sum of W (read by peers)
-    unsigned int lcnt;        // this CTA's count of W == tau (read by peers)
-    // broadcast from thread 0
-    unsigned long long lo, width, above, n_eq;
-    int wbits, done, cut_found;
+    unsigned long long cw[kCandLocal];     // this CTA's candidates (read by rank 0)
+    int ci[kCandLocal];
+    unsigned long long gw[kCandTotal];     // rank 0: gathered, sorted candidates
+    int gi[kCandTotal];
+    unsigned long long wred[kWarps];
+    unsigned long long wred2[kWarps];
+    float fred[kWarps];
+    // values peers read over DSMEM
+    float lmax;
+    unsigned long long lsum;
+    unsigned int ncand;
+    int overflow;
+    unsigned long long part_lo, part_hi;   // this CTA's u128 partial total
+    RowInfo info;                          // rank 0's result for the current row
+    int decision;
+    // broadcast inside the CTA
+    int beta, wbits;
+    unsigned long long lo, width, above, n_eq, count_eq;
+    int cut_found;
 };
 
-__global__ void __launch_bounds__(kStatThreads) row_stats_kernel(
-    const float* __restrict__ target, const float* __restrict__ draft, int Kd, int V, int slice,
-    float invT, unsigned long long P, RowStat* __restrict__ stats) {
-    cg::cluster_group cl = cg::this_cluster();
-    extern __shared__ float s_e[];
-    __shared__ StatSmem sm;
+__device__ __forceinline__ float block_max(float v, Smem& sm) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (lane == 0) sm.fred[wid] = v;
+    __syncthreads();
+    float m = -INFINITY;
+    for (int w = 0; w < kWarps; ++w) m = fmaxf(m, sm.fred[w]);
+    __syncthreads();
+    return m;
+}
+
+__device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v, Smem& sm) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) sm.wred[wid] = v;
+    __syncthreads();
+    unsigned long long t = 0;
+    for (int w = 0; w < kWarps; ++w) t += sm.wred[w];
+    __syncthreads();
+    return t;
+}
+
+__device__ __forceinline__ u128 block_sum_u128(u128 v, Smem& sm) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += shfl_xor_u128(v, o);
+    if (lane == 0) {
+        sm.wred[wid] = static_cast<unsigned long long>(v);
+        sm.wred2[wid] = static_cast<unsigned long long>(v >> 64);
+    }
+    __syncthreads();
+    u128 t = 0;
+    for (int w = 0; w < kWarps; ++w) t += (static_cast<u128>(sm.wred2[w]) << 64) | sm.wred[w];
+    __syncthreads();
+    return t;
+}
+
+// Exclusive prefix over the block of a u128 value per thread; also returns the total.
+__device__ __forceinline__ u128 block_excl_u128(u128 v, Smem& sm, u128& total) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    u128 incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const u128 y = shfl_up_u128(incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) {
+        sm.wred[wid] = static_cast<unsigned long long>(incl);
+        sm.wred2[wid] = static_cast<unsigned long long>(incl >> 64);
+    }
+    __syncthreads();
+    u128 base = 0, t = 0;
+    for (int w = 0; w < kWarps; ++w) {
+        const u128 x = (static_cast<u128>(sm.wred2[w]) << 64) | sm.wred[w];
+        if (w < wid) base += x;
+        t += x;
+    }
+    __syncthreads();
+    total = t;
+    return base + incl - v;
+}
+
+// ----------------------------------------------------------- row statistics
+// s holds this CTA's slice [lo, lo + n) of the row's logits on entry and the
+// own_exp values on exit.  Every CTA of the cluster returns the same RowInfo.
+__device__ RowInfo row_stats(cg::cluster_group& cl, float* s, int n, int lo, int V, float invT,
+                             unsigned long long P, Smem& sm) {
     const int C = static_cast<int>(cl.num_blocks());
     const int rank = static_cast<int>(cl.block_rank());
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const long long row = blockIdx.x / C;
-    const int per = 2 * Kd + 1;
-    const long long b = row / per;
-    const int i = static_cast<int>(row % per);
-    const float* src = (i <= Kd) ? target + (b * (Kd + 1) + i) * static_cast<long long>(V)
-                                 : draft + (b * Kd + (i - Kd - 1)) * static_cast<long long>(V);
-    const int lo = rank * slice;
-    const int n = (lo < V) ? ((V - lo < slice) ? V - lo : slice) : 0;
+    const int tid = threadIdx.x;
 
-    // 1. load the slice and reduce the max over the cluster
+    // 1. max over the cluster
     float lmax = -INFINITY;
-    for (int k = tid; k < n; k += kStatThreads) {
-        const float v = __ldg(src + lo + k);
-        s_e[k] = v;
-        lmax = fmaxf(lmax, v);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
-    if (lane == 0) sm.fred[wid] = lmax;
-    __syncthreads();
-    if (tid == 0) {
-        float m = -INFINITY;
-        for (int w = 0; w < kStatThreads / 32; ++w) m = fmaxf(m, sm.fred[w]);
-        sm.lmax = m;
+    for (int k = tid; k < n; k += kThreads) lmax = fmaxf(lmax, s[k]);
+    lmax = block_max(lmax, sm);
+    if (tid == 0) sm.lmax = lmax;
+    for (int t = tid; t < kLogBuckets; t += kThreads) {
+        sm.cnt[t] = 0u;
+        sm.mass[t] = 0ull;
     }
     cl.sync();
     float mx = -INFINITY;
     for (int r = 0; r < C; ++r) mx = fmaxf(mx, *cl.map_shared_rank(&sm.lmax, r));
 
-    // 2. e_v and the total mass
+    // 2. e_v, the total mass and the log-scale histogram in one pass
     unsigned long long lsum = 0;
-    for (int k = tid; k < n; k += kStatThreads) {
-        const float e = own_exp(scaled_x(s_e[k], mx, invT));
-        s_e[k] = e;
-        lsum += mass_of(e);
+    for (int k = tid; k < n; k += kThreads) {
+        const float e = own_exp(scaled_x(s[k], mx, invT));
+        s[k] = e;
+        const unsigned long long W = mass_of(e);
+        lsum += W;
+        if (W != 0ull && P < kKeepAll) {
+            const int bk = log_bucket(W);
+            atomicAdd(&sm.cnt[bk], 1u);
+            atomicAdd(&sm.mass[bk], W);
+        }
     }
-    lsum = warp_sum_u64(lsum);
-    if (lane == 0) sm.ured[wid] = lsum;
-    for (int t = tid; t < kLogBuckets; t += kStatThreads) {
-        sm.cnt[0][t] = 0u;
-        sm.mass[0][t] = 0ull;
-    }
-    __syncthreads();
-    if (tid == 0) {
-        unsigned long long s = 0;
-        for (int w = 0; w < kStatThreads / 32; ++w) s += sm.ured[w];
-        sm.lsum = s;
-    }
+    lsum = block_sum_u64(lsum, sm);
+    if (tid == 0) sm.lsum = lsum;
     cl.sync();
     unsigned long long S = 0;
     for (int r = 0; r < C; ++r) S += *cl.map_shared_rank(&sm.lsum, r);
-
-    RowStat out;
-    out.mx = mx;
-    out.pad = 0;
+    RowInfo info;
+    info.mx = mx;
     if (P >= kKeepAll) {
-        if (rank == 0 && tid == 0) {
-            out.tau = 0;
-            out.cut = V - 1;
-            out.S = S;
-            stats[row] = out;
-        }
-        cl.sync();
-        return;
+        info.cut = V - 1;
+        info.tau = 0;
+        info.S = S;
+        cl.sync();  // peers are done reading this CTA's values
+        return info;
     }
     const u128 TGT = static_cast<u128>(P) * S;
-
-    // 3. log-scale histogram of W > 0
-    for (int k = tid; k < n; k += kStatThreads) {
-        const unsigned long long W = mass_of(s_e[k]);
-        if (W == 0ull) continue;
-        const int bk = log_bucket(W);
-        atomicAdd(&sm.cnt[0][bk], 1u);
-        atomicAdd(&sm.mass[0][bk], W);
-    }
-    __syncthreads();
-    cl.sync();
-    for (int t = tid; t < kLogBuckets; t += kStatThreads) {
+    for (int t = tid; t < kLogBuckets; t += kThreads) {
         unsigned int c = 0;
         unsigned long long m = 0;
         for (int r = 0; r < C; ++r) {
-            c += cl.map_shared_rank(&sm.cnt[0][0], r)[t];
-            m += cl.map_shared_rank(&sm.mass[0][0], r)[t];
+            c += cl.map_shared_rank(&sm.cnt[0], r)[t];
+            m += cl.map_shared_rank(&sm.mass[0], r)[t];
         }
         sm.mcnt[t] = c;
         sm.mmass[t] = m;
@@ -290,7 +312,105 @@ __global__ void __launch_bounds__(kStatThreads) row_stats_kernel(
             }
             above += sm.mmass[t];
         }
+        sm.beta = beta;
         sm.above = above;
+        sm.ncand = 0;
+        sm.overflow = 0;
+    }
+    __syncthreads();
+
+    // 3. gather the members of the crossing bucket
+    const int beta = sm.beta;
+    for (int k = tid; k < n; k += kThreads) {
+        const unsigned long long W = mass_of(s[k]);
+        if (W != 0ull && log_bucket(W) == beta) {
+            const unsigned int slot = atomicAdd(&sm.ncand, 1u);
+            if (slot < static_cast<unsigned int>(kCandLocal)) {
+                sm.cw[slot] = W;
+                sm.ci[slot] = lo + k;
+            } else {
+                sm.overflow = 1;
+            }
+        }
+    }
+    __syncthreads();
+    cl.sync();
+    unsigned int total = 0;
+    int overflow = 0;
+    for (int r = 0; r < C; ++r) {
+        total += *cl.map_shared_rank(&sm.ncand, r);
+        overflow |= *cl.map_shared_rank(&sm.overflow, r);
+    }
+    if (!overflow && total <= static_cast<unsigned int>(kCandTotal)) {
+        if (rank == 0) {
+            // gather, pad to a power of two, bitonic sort by (W desc, index asc)
+            unsigned int pw = 1;
+            while (pw < total) pw <<= 1;
+            unsigned int base = 0;
+            for (int r = 0; r < C; ++r) {
+                const unsigned int cr = *cl.map_shared_rank(&sm.ncand, r);
+                const unsigned long long* rw = cl.map_shared_rank(&sm.cw[0], r);
+                const int* ri = cl.map_shared_rank(&sm.ci[0], r);
+                for (unsigned int t = tid; t < cr; t += kThreads) {
+                    sm.gw[base + t] = rw[t];
+                    sm.gi[base + t] = ri[t];
+                }
+                base += cr;
+            }
+            for (unsigned int t = total + tid; t < pw; t += kThreads) {
+                sm.gw[t] = 0ull;
+                sm.gi[t] = 0x7fffffff;
+            }
+            __syncthreads();
+            for (unsigned int kk = 2; kk <= pw; kk <<= 1) {
+                for (unsigned int j = kk >> 1; j > 0; j >>= 1) {
+                    for (unsigned int t = tid; t < pw; t += kThreads) {
+                        const unsigned int u = t ^ j;
+                        if (u > t) {
+                            const unsigned long long wa = sm.gw[t], wb = sm.gw[u];
+                            const int ia = sm.gi[t], ib = sm.gi[u];
+                            const bool a_first = wa > wb || (wa == wb && ia < ib);
+                            const bool up = (t & kk) == 0;
+                            if (up != a_first) {
+                                sm.gw[t] = wb;
+                                sm.gw[u] = wa;
+                                sm.gi[t] = ib;
+                                sm.gi[u] = ia;
+                            }
+                        }
+                    }
+                    __syncthreads();
+                }
+            }
+            // running mass down the sorted list; the first crossing is the cut
+            const unsigned int t0 = 2 * tid;
+            const unsigned long long w0 = t0 < total ? sm.gw[t0] : 0ull;
+            const unsigned long long w1 = t0 + 1 < total ? sm.gw[t0 + 1] : 0ull;
+            u128 tot;
+            const u128 ex = block_excl_u128(static_cast<u128>(w0) + w1, sm, tot);
+            const u128 above = sm.above;
+            const u128 c0 = above + ex + w0, c1 = c0 + w1;
+            if (t0 < total && (c0 << 32) >= TGT && ((above + ex) << 32) < TGT) {
+                sm.info.tau = w0;
+                sm.info.cut = sm.gi[t0];
+                sm.info.S = static_cast<unsigned long long>(c0);
+            } else if (t0 + 1 < total && (c1 << 32) >= TGT && (c0 << 32) < TGT) {
+                sm.info.tau = w1;
+                sm.info.cut = sm.gi[t0 + 1];
+                sm.info.S = static_cast<unsigned long long>(c1);
+            }
+        }
+        cl.sync();
+        const RowInfo* r0 = cl.map_shared_rank(&sm.info, 0);
+        info.tau = r0->tau;
+        info.cut = r0->cut;
+        info.S = r0->S;
+        cl.sync();  // rank 0's result stays until everyone has it
+        return info;
+    }
+
+    // 4. fallback: exact radix search over the slices inside the bucket
+    if (tid == 0) {
         if (beta < 16) {
             sm.lo = static_cast<unsigned long long>(beta);
             sm.width = 1;
@@ -305,35 +425,31 @@ __global__ void __launch_bounds__(kStatThreads) row_stats_kernel(
         }
     }
     __syncthreads();
-
-    // 4. refine inside the crossing bucket, 8 bits at a time
-    int buf = 0;
     while (sm.width > 1ull) {
-        buf ^= 1;
         const int wbits = sm.wbits;
         const int bits = wbits < 8 ? wbits : 8;
         const int shift = wbits - bits;
         const unsigned long long rlo = sm.lo, rhi = sm.lo + sm.width;
-        for (int t = tid; t < kLinBuckets; t += kStatThreads) {
-            sm.cnt[buf][t] = 0u;
-            sm.mass[buf][t] = 0ull;
+        cl.sync();  // peers finished reading this CTA's previous histogram
+        for (int t = tid; t < kLinBuckets; t += kThreads) {
+            sm.cnt[t] = 0u;
+            sm.mass[t] = 0ull;
         }
         __syncthreads();
-        for (int k = tid; k < n; k += kStatThreads) {
-            const unsigned long long W = mass_of(s_e[k]);
+        for (int k = tid; k < n; k += kThreads) {
+            const unsigned long long W = mass_of(s[k]);
             if (W < rlo || W >= rhi) continue;
             const int bk = static_cast<int>((W - rlo) >> shift);
-            atomicAdd(&sm.cnt[buf][bk], 1u);
-            atomicAdd(&sm.mass[buf][bk], W);
+            atomicAdd(&sm.cnt[bk], 1u);
+            atomicAdd(&sm.mass[bk], W);
         }
-        __syncthreads();
         cl.sync();
-        for (int t = tid; t < (1 << bits); t += kStatThreads) {
+        for (int t = tid; t < (1 << bits); t += kThreads) {
             unsigned int c = 0;
             unsigned long long m = 0;
             for (int r = 0; r < C; ++r) {
-                c += cl.map_shared_rank(&sm.cnt[buf][0], r)[t];
-                m += cl.map_shared_rank(&sm.mass[buf][0], r)[t];
+                c += cl.map_shared_rank(&sm.cnt[0], r)[t];
+                m += cl.map_shared_rank(&sm.mass[0], r)[t];
             }
             sm.mcnt[t] = c;
             sm.mmass[t] = m;
@@ -362,228 +478,234 @@ __global__ void __launch_bounds__(kStatThreads) row_stats_kernel(
     const u128 num = TGT - (static_cast<u128>(above) << 32);
     const u128 den = static_cast<u128>(tau) << 32;
     const unsigned long long jneed = static_cast<unsigned long long>((num + den - 1) / den);
-    out.tau = tau;
-    out.S = above + jneed * tau;
-    if (jneed >= n_eq) {
-        if (rank == 0 && tid == 0) {
-            out.cut = V - 1;
-            stats[row] = out;
-        }
-        cl.sync();
-        return;
-    }
-
-    // 5. the jneed-th element with W == tau in index order sets the cut
-    const int chunk = (n + kStatThreads - 1) / kStatThreads;
+    info.tau = tau;
+    info.S = above + jneed * tau;
+    info.cut = V - 1;
+    // the jneed-th element with W == tau in index order sets the cut
+    const int chunk = (n + kThreads - 1) / kThreads;
     const int k0 = tid * chunk, k1 = (k0 + chunk < n) ? k0 + chunk : n;
     unsigned int mine = 0;
-    for (int k = k0; k < k1; ++k) mine += (mass_of(s_e[k]) == tau) ? 1u : 0u;
-    // block exclusive scan of mine
-    unsigned int incl = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    if (lane == 31) sm.ured[wid] = incl;
-    __syncthreads();
+    for (int k = k0; k < k1; ++k) mine += (mass_of(s[k]) == tau) ? 1u : 0u;
+    u128 ctot;
+    const unsigned long long excl =
+        static_cast<unsigned long long>(block_excl_u128(static_cast<u128>(mine), sm, ctot));
     if (tid == 0) {
-        unsigned long long run = 0;
-        for (int w = 0; w < kStatThreads / 32; ++w) {
-            const unsigned long long x = sm.ured[w];
-            sm.ured[w] = run;
-            run += x;
-        }
-        sm.lcnt = static_cast<unsigned int>(run);
+        sm.count_eq = static_cast<unsigned long long>(ctot);
+        sm.cut_found = -1;
     }
-    __syncthreads();
-    const unsigned long long excl = sm.ured[wid] + (incl - mine);
     cl.sync();
     unsigned long long before = 0;
-    for (int r = 0; r < rank; ++r) before += *cl.map_shared_rank(&sm.lcnt, r);
-    const unsigned long long need = jneed - before;  // 1-based within this CTA
-    if (before < jneed && jneed <= before + sm.lcnt && excl < need && need <= excl + mine) {
+    for (int r = 0; r < rank; ++r) before += *cl.map_shared_rank(&sm.count_eq, r);
+    const unsigned long long need = jneed - before;  // 1-based inside this CTA
+    if (jneed < n_eq && before < jneed && jneed <= before + sm.count_eq && excl < need &&
+        need <= excl + mine) {
         unsigned long long seen = excl;
-        for (int k = k0; k < k1; ++k) {
-            if (mass_of(s_e[k]) == tau && ++seen == need) {
-                out.cut = lo + k;
-                stats[row] = out;
+        for (int k = k0; k < k1; ++k)
+            if (mass_of(s[k]) == tau && ++seen == need) {
+                sm.cut_found = lo + k;
                 break;
             }
-        }
     }
     cl.sync();
+    if (jneed < n_eq) {
+        int cut = -1;
+        for (int r = 0; r < C; ++r) {
+            const int x = *cl.map_shared_rank(&sm.cut_found, r);
+            if (x >= 0) cut = x;
+        }
+        info.cut = cut;
+    }
+    cl.sync();
+    return info;
 }
 
-// ---------------------------------------------------- kernel 2: decisions
-__global__ void decide_kernel(const float* __restrict__ target, const float* __restrict__ draft,
-                              const int32_t* __restrict__ drafts, int B, int Kd, int V,
-                              float invT, unsigned long long seed, unsigned long long offset,
-                              const RowStat* __restrict__ stats, SeqState* __restrict__ seq,
-                              int32_t* __restrict__ tokens, int32_t* __restrict__ len,
-                              uint32_t* status) {
-    const int b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= B) return;
-    const int per = 2 * Kd + 1;
-    int n = 0;
-    SeqState st;
-    st.mode = 1;
-    st.pos = Kd;
-    st.pad = 0;
-    uint32_t r[4];
-    for (int i = 0; i < Kd; ++i) {
-        const int32_t x = drafts[static_cast<long long>(b) * Kd + i];
-        philox_at(seed, offset, static_cast<uint32_t>(i), static_cast<uint32_t>(b), r);
-        const unsigned long long u64 = (static_cast<unsigned long long>(r[2]) << 32) | r[1];
-        bool ok = false;
-        if (x >= 0 && x < V) {
-            const RowStat sp = stats[static_cast<long long>(b) * per + i];
-            const RowStat sq = stats[static_cast<long long>(b) * per + Kd + 1 + i];
-            const float lp = target[(static_cast<long long>(b) * (Kd + 1) + i) * V + x];
-            const float lq = draft[(static_cast<long long>(b) * Kd + i) * V + x];
-            const unsigned long long Wp = kept(mass_at(lp, sp.mx, invT), x, sp);
-            const unsigned long long Wq = kept(mass_at(lq, sq.mx, invT), x, sq);
-            const unsigned long long U = r[0] >> 8;
-            const u128 lhs = static_cast<u128>(U * Wq) * sp.S;
-            const u128 rhs = (static_cast<u128>(Wp) * sq.S) << 24;
-            ok = lhs < rhs;
-        } else {
-            atomicOr(status, kStatusBadDraft);
-        }
-        if (ok) {
-            ++n;
-            continue;
-        }
-        st.mode = 0;
-        st.pos = i;
-        st.u64 = u64;
-        break;
+// --------------------------------------------------- ordered categorical draw
+// Weight of slice element k: the residual r_v (res) or the kept target mass.
+struct Weights {
+    const float* ep;
+    const float* eq;
+    RowInfo ip, iq;
+    bool res;
+    int lo;
+    __device__ __forceinline__ u128 at(int k) const {
+        const int v = lo + k;
+        const unsigned long long wp = kept(mass_of(ep[k]), v, ip);
+        if (!res) return static_cast<u128>(wp);
+        const unsigned long long wq = kept(mass_of(eq[k]), v, iq);
+        const u128 a = static_cast<u128>(wp) * iq.S, c = static_cast<u128>(wq) * ip.S;
+        return a > c ? a - c : static_cast<u128>(0);
     }
-    if (n == Kd) {
-        philox_at(seed, offset, static_cast<uint32_t>(Kd), static_cast<uint32_t>(b), r);
-        st.u64 = (static_cast<unsigned long long>(r[2]) << 32) | r[1];
-    }
-    st.n = n;
-    seq[b] = st;
-    for (int i = 0; i <= Kd; ++i) {
-        if (i < n) tokens[static_cast<long long>(b) * (Kd + 1) + i] = drafts[static_cast<long long>(b) * Kd + i];
-        else if (i > n) tokens[static_cast<long long>(b) * (Kd + 1) + i] = -1;
-    }
-    len[b] = n + 1;
-}
-
-// ----------------------------------------------------- kernel 3: the draw
-struct SampleSmem {
-    unsigned long long lo[kSampleThreads / 32];
-    unsigned long long hi[kSampleThreads / 32];
-    int found;
 };
 
-__device__ __forceinline__ u128 block_sum_u128(u128 v, SampleSmem& sm, int lane, int wid) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += shfl_xor_u128(v, o);
-    if (lane == 0) {
-        sm.lo[wid] = static_cast<unsigned long long>(v);
-        sm.hi[wid] = static_cast<unsigned long long>(v >> 64);
-    }
-    __syncthreads();
-    u128 t = 0;
-    for (int w = 0; w < kSampleThreads / 32; ++w)
-        t += (static_cast<u128>(sm.hi[w]) << 64) | sm.lo[w];
-    __syncthreads();
-    return t;
+// Sum of the weights of this CTA's slice (every thread gets it).
+__device__ __forceinline__ u128 slice_total(const Weights& w, int n, Smem& sm) {
+    u128 part = 0;
+    for (int k = threadIdx.x; k < n; k += kThreads) part += w.at(k);
+    return block_sum_u128(part, sm);
 }
 
-__global__ void __launch_bounds__(kSampleThreads) sample_kernel(
-    const float* __restrict__ target, const float* __restrict__ draft, int Kd, int V, float invT,
-    const RowStat* __restrict__ stats, const SeqState* __restrict__ seq,
-    int32_t* __restrict__ tokens, uint32_t* status) {
-    __shared__ SampleSmem sm;
-    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const SeqState st = seq[b];
-    const int per = 2 * Kd + 1;
-    const int pos = st.pos;
-    const RowStat sp = stats[static_cast<long long>(b) * per + pos];
-    const float* lp = target + (static_cast<long long>(b) * (Kd + 1) + pos) * V;
-    bool residual = (st.mode == 0);
-    RowStat sq{};
-    const float* lq = nullptr;
-    if (residual) {
-        sq = stats[static_cast<long long>(b) * per + Kd + 1 + pos];
-        lq = draft + (static_cast<long long>(b) * Kd + pos) * V;
+// Returns (to every CTA) the first index whose running weight sum exceeds
+// floor(u64 * total / 2^64); `mine` is this CTA's slice total.
+__device__ int ordered_draw(cg::cluster_group& cl, const Weights& w, int n, u128 mine, u128 total,
+                            unsigned long long u64, Smem& sm) {
+    const int C = static_cast<int>(cl.num_blocks());
+    const int rank = static_cast<int>(cl.block_rank());
+    const int tid = threadIdx.x;
+    const u128 t = scale_u64(u64, total);
+    if (tid == 0) {
+        sm.part_lo = static_cast<unsigned long long>(mine);
+        sm.part_hi = static_cast<unsigned long long>(mine >> 64);
+        sm.cut_found = -1;
     }
-    // weight of token v under the chosen rule
-    auto weight = [&](int v, bool res) -> u128 {
-        const unsigned long long wp = kept(mass_at(__ldg(lp + v), sp.mx, invT), v, sp);
-        if (!res) return static_cast<u128>(wp);
-        const unsigned long long wq = kept(mass_at(__ldg(lq + v), sq.mx, invT), v, sq);
-        const u128 a = static_cast<u128>(wp) * sq.S, c = static_cast<u128>(wq) * sp.S;
-        return a > c ? a - c : static_cast<u128>(0);
-    };
-    u128 total;
-    if (residual) {
-        u128 part = 0;
-        for (int v = tid; v < V; v += kSampleThreads) part += weight(v, true);
-        total = block_sum_u128(part, sm, lane, wid);
-        if (total == 0) {  // only reachable through an invalid draft id
-            residual = false;
-            if (tid == 0) atomicOr(status, kStatusZeroResidual);
-        }
-    }
-    if (!residual) total = static_cast<u128>(sp.S);
-    const u128 t = scale_u64(st.u64, total);
-    // ordered scan, 4 consecutive tokens per thread per tile
-    if (tid == 0) sm.found = -1;
-    __syncthreads();
-    u128 run = 0;
-    constexpr int kTile = 4 * kSampleThreads;
-    for (int base = 0; base < V; base += kTile) {
-        const int v0 = base + 4 * tid;
-        u128 w[4];
-        u128 mine = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            w[q] = (v0 + q < V) ? weight(v0 + q, residual) : static_cast<u128>(0);
-            mine += w[q];
-        }
-        u128 incl = mine;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const u128 y = shfl_up_u128(incl, o);
-            if (lane >= o) incl += y;
-        }
-        if (lane == 31) {
-            sm.lo[wid] = static_cast<unsigned long long>(incl);
-            sm.hi[wid] = static_cast<unsigned long long>(incl >> 64);
-        }
-        __syncthreads();
-        u128 wbase = 0, tile_total = 0;
-        for (int w2 = 0; w2 < kSampleThreads / 32; ++w2) {
-            const u128 x = (static_cast<u128>(sm.hi[w2]) << 64) | sm.lo[w2];
-            if (w2 < wid) wbase += x;
-            tile_total += x;
-        }
-        __syncthreads();
-        const u128 excl = run + wbase + (incl - mine);
-        if (excl <= t && t < excl + mine) {
-            u128 c = excl;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                c += w[q];
-                if (c > t) {
-                    sm.found = v0 + q;
+    cl.sync();
+    u128 before = 0;
+    for (int r = 0; r < rank; ++r)
+        before += (static_cast<u128>(*cl.map_shared_rank(&sm.part_hi, r)) << 64) |
+                  *cl.map_shared_rank(&sm.part_lo, r);
+    if (before <= t && t < before + mine) {  // the draw lands in this CTA's slice
+        const int chunk = (n + kThreads - 1) / kThreads;
+        const int k0 = tid * chunk, k1 = (k0 + chunk < n) ? k0 + chunk : n;
+        u128 own = 0;
+        for (int k = k0; k < k1; ++k) own += w.at(k);
+        u128 tot;
+        const u128 ex = before + block_excl_u128(own, sm, tot);
+        if (ex <= t && t < ex + own) {
+            u128 run = ex;
+            for (int k = k0; k < k1; ++k) {
+                run += w.at(k);
+                if (run > t) {
+                    sm.cut_found = w.lo + k;
                     break;
                 }
             }
         }
-        __syncthreads();
-        if (sm.found >= 0) break;
-        run += tile_total;
     }
-    if (tid == 0) {
-        const int tok = sm.found >= 0 ? sm.found : V - 1;
-        tokens[static_cast<long long>(b) * (Kd + 1) + st.n] = tok;
+    cl.sync();
+    int tok = -1;
+    for (int r = 0; r < C; ++r) {
+        const int x = *cl.map_shared_rank(&sm.cut_found, r);
+        if (x >= 0) tok = x;
     }
+    cl.sync();
+    return tok;
+}
+
+__device__ __forceinline__ void load_slice(float* dst, const float* src, int n, bool vec) {
+    if (vec) {
+        const int n4 = n >> 2;
+        const float4* s4 = reinterpret_cast<const float4*>(src);
+        float4* d4 = reinterpret_cast<float4*>(dst);
+        for (int k = threadIdx.x; k < n4; k += kThreads) d4[k] = __ldg(s4 + k);
+        for (int k = 4 * n4 + threadIdx.x; k < n; k += kThreads) dst[k] = __ldg(src + k);
+    } else {
+        for (int k = threadIdx.x; k < n; k += kThreads) dst[k] = __ldg(src + k);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) pair_kernel(
+    const float* __restrict__ target, const float* __restrict__ draft,
+    const int32_t* __restrict__ drafts, int Kd, int V, int slice, int vec_ok, float invT,
+    unsigned long long P, unsigned long long seed, unsigned long long offset,
+    PairOut* __restrict__ out, uint32_t* status) {
+    cg::cluster_group cl = cg::this_cluster();
+    extern __shared__ float4 dyn[];
+    __shared__ Smem sm;
+    float* sp = reinterpret_cast<float*>(dyn);
+    float* sq = sp + slice;
+    const int C = static_cast<int>(cl.num_blocks());
+    const int rank = static_cast<int>(cl.block_rank());
+    const long long pid = blockIdx.x / C;
+    const long long b = pid / (Kd + 1);
+    const int i = static_cast<int>(pid % (Kd + 1));
+    const bool has_q = i < Kd;
+    const int lo = rank * slice;
+    const int n = (lo < V) ? ((V - lo < slice) ? V - lo : slice) : 0;
+    const float* lp = target + (b * (Kd + 1) + i) * static_cast<long long>(V);
+    const float* lq = has_q ? draft + (b * Kd + i) * static_cast<long long>(V) : nullptr;
+    const bool vec = vec_ok != 0;  // rows start on 16-byte boundaries
+    load_slice(sp, lp + lo, n, vec);
+    if (has_q) load_slice(sq, lq + lo, n, vec);
+    __syncthreads();
+
+    const RowInfo ip = row_stats(cl, sp, n, lo, V, invT, P, sm);
+    RowInfo iq{};
+    if (has_q) iq = row_stats(cl, sq, n, lo, V, invT, P, sm);
+
+    uint32_t rr[4];
+    philox4x32_10(static_cast<uint32_t>(i), static_cast<uint32_t>(b),
+                  static_cast<uint32_t>(offset), static_cast<uint32_t>(offset >> 32),
+                  static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32), rr);
+    const unsigned long long u64 = (static_cast<unsigned long long>(rr[2]) << 32) | rr[1];
+
+    Weights w{sp, sq, ip, iq, false, lo};
+    if (!has_q) {  // the bonus row
+        const u128 mine = slice_total(w, n, sm);
+        const int tok = ordered_draw(cl, w, n, mine, static_cast<u128>(ip.S), u64, sm);
+        if (rank == 0 && threadIdx.x == 0) out[pid] = PairOut{1, tok};
+        return;
+    }
+    // the acceptance test of draft i
+    if (rank == 0 && threadIdx.x == 0) {
+        const int32_t x = drafts[b * Kd + i];
+        int ok = 0;
+        if (x >= 0 && x < V) {
+            const unsigned long long Wp = kept(mass_of(own_exp(scaled_x(lp[x], ip.mx, invT))), x, ip);
+            const unsigned long long Wq = kept(mass_of(own_exp(scaled_x(lq[x], iq.mx, invT))), x, iq);
+            const unsigned long long U = rr[0] >> 8;
+            const u128 lhs = static_cast<u128>(U * Wq) * ip.S;
+            const u128 rhs = (static_cast<u128>(Wp) * iq.S) << 24;
+            ok = lhs < rhs ? 1 : 0;
+        } else {
+            atomicOr(status, kStatusBadDraft);
+        }
+        sm.decision = ok;
+    }
+    cl.sync();
+    const int ok = *cl.map_shared_rank(&sm.decision, 0);
+    if (ok) {
+        cl.sync();
+        if (rank == 0 && threadIdx.x == 0) out[pid] = PairOut{1, -1};
+        return;
+    }
+    // rejected: residual max(0, p*Sq - q*Sp) from the rows on chip
+    w.res = true;
+    u128 mine = slice_total(w, n, sm);
+    if (threadIdx.x == 0) {
+        sm.part_lo = static_cast<unsigned long long>(mine);
+        sm.part_hi = static_cast<unsigned long long>(mine >> 64);
+    }
+    cl.sync();
+    u128 R = 0;
+    for (int r = 0; r < C; ++r)
+        R += (static_cast<u128>(*cl.map_shared_rank(&sm.part_hi, r)) << 64) |
+             *cl.map_shared_rank(&sm.part_lo, r);
+    cl.sync();
+    if (R == 0) {  // only reachable through an invalid draft id: draw from p
+        if (rank == 0 && threadIdx.x == 0) atomicOr(status, kStatusZeroResidual);
+        w.res = false;
+        mine = slice_total(w, n, sm);
+        R = static_cast<u128>(ip.S);
+    }
+    const int tok = ordered_draw(cl, w, n, mine, R, u64, sm);
+    if (rank == 0 && threadIdx.x == 0) out[pid] = PairOut{0, tok};
+}
+
+// One thread per sequence: the first rejection decides the committed run.
+__global__ void commit_kernel(const int32_t* __restrict__ drafts, const PairOut* __restrict__ pairs,
+                              int B, int Kd, int32_t* __restrict__ tokens,
+                              int32_t* __restrict__ len) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    const PairOut* pr = pairs + static_cast<long long>(b) * (Kd + 1);
+    int n = 0;
+    while (n < Kd && pr[n].accept) ++n;
+    for (int i = 0; i <= Kd; ++i) {
+        int32_t t = -1;
+        if (i < n) t = drafts[static_cast<long long>(b) * Kd + i];
+        else if (i == n) t = pr[n].token;
+        tokens[static_cast<long long>(b) * (Kd + 1) + i] = t;
+    }
+    len[b] = n + 1;
 }
 
 __global__ void own_exp_kernel(const float* __restrict__ x, float* __restrict__ y, long long n) {
@@ -609,8 +731,8 @@ cudaError_t launch_own_exp(const float* x, float* y, long long n, cudaStream_t s
 
 size_t rejection_workspace_bytes(int B, int Kd, int V) {
     (void)V;
-    const size_t rows = static_cast<size_t>(B) * (2 * Kd + 1);
-    return ((rows * sizeof(RowStat) + 255) / 256) * 256 + ((B * sizeof(SeqState) + 255) / 256) * 256;
+    const size_t pairs = static_cast<size_t>(B) * (Kd + 1);
+    return ((pairs * sizeof(PairOut) + 255) / 256) * 256;
 }
 
 cudaError_t launch_accept_rejection(const float* target, const float* draft,
@@ -622,21 +744,18 @@ cudaError_t launch_accept_rejection(const float* target, const float* draft,
     int slice = (V + C - 1) / C;
     slice = (slice + 3) & ~3;
     if (slice > kMaxSlice) return cudaErrorNotSupported;
-    const size_t rows = static_cast<size_t>(B) * (2 * Kd + 1);
-    if (rows * C > 0x7fffffffull) return cudaErrorNotSupported;
-    char* base = static_cast<char*>(ws);
-    RowStat* stats = reinterpret_cast<RowStat*>(base);
-    SeqState* seq = reinterpret_cast<SeqState*>(base + ((rows * sizeof(RowStat) + 255) / 256) * 256);
+    const size_t pairs = static_cast<size_t>(B) * (Kd + 1);
+    if (pairs * C > 0x7fffffffull) return cudaErrorNotSupported;
     if (rejection_workspace_bytes(B, Kd, V) > ws_bytes) return cudaErrorInvalidValue;
+    PairOut* out = static_cast<PairOut*>(ws);
 
-    const size_t smem = static_cast<size_t>(slice) * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(row_stats_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const size_t smem = static_cast<size_t>(2) * slice * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(static_cast<unsigned>(rows * C));
-    cfg.blockDim = dim3(kStatThreads);
+    cfg.gridDim = dim3(static_cast<unsigned>(pairs * C));
+    cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -646,15 +765,15 @@ cudaError_t launch_accept_rejection(const float* target, const float* draft,
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, row_stats_kernel, target, draft, Kd, V, slice, invT,
-                           static_cast<unsigned long long>(P), stats);
+    const int vec_ok = (V % 4 == 0 && (reinterpret_cast<uintptr_t>(target) & 15u) == 0 &&
+                        (reinterpret_cast<uintptr_t>(draft) & 15u) == 0)
+                           ? 1
+                           : 0;
+    e = cudaLaunchKernelEx(&cfg, pair_kernel, target, draft, drafts, Kd, V, slice, vec_ok, invT,
+                           static_cast<unsigned long long>(P), static_cast<unsigned long long>(seed),
+                           static_cast<unsigned long long>(offset), out, status);
     if (e != cudaSuccess) return e;
-    decide_kernel<<<(B + 127) / 128, 128, 0, s>>>(target, draft, drafts, B, Kd, V, invT, seed,
-                                                   offset, stats, seq, tokens, len, status);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    sample_kernel<<<B, kSampleThreads, 0, s>>>(target, draft, Kd, V, invT, stats, seq, tokens,
-                                               status);
+    commit_kernel<<<(B + 127) / 128, 128, 0, s>>>(drafts, out, B, Kd, tokens, len);
     return cudaGetLastError();
 }
 

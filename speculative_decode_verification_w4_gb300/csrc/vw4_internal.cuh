@@ -14,13 +14,19 @@ constexpr int kMaxSeg = 64;        // routed (token, expert) pairs per call
 constexpr int kTileRows = 128;     // weight rows per tile
 constexpr int kStageK = 256;       // k elements per pipeline stage
 constexpr int kStages = 4;         // pipeline depth
-constexpr int kConsumerWarps = 4;  // each owns 32 rows of the tile
+constexpr int kConsumerWarps = 8;  // each owns 16 rows of the tile
 constexpr int kGemmThreads = (kConsumerWarps + 1) * 32;
 constexpr int kWBytes = kTileRows * (kStageK / 2);     // 16384: packed nibbles
 constexpr int kSBytes = kTileRows * 16;                // 2048: 16 B of scales per row
 constexpr int kABytes = kMaxRows * kStageK * 2;        // 4096: fp16 activations
-constexpr int kStageBytes = kWBytes + kSBytes + kABytes;  // 22528 = 22 * 1024
-constexpr int kGemmSmem = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers, flags*/;
+constexpr int kAStride = kABytes + kMaxRows * 4;       // + the 8 rows' 2^-s: 4128
+constexpr int kStageBytes = kWBytes + kSBytes + kAStride;  // bytes streamed per unit
+// shared memory: [W x kStages][S x kStages][A x kStages][barriers]; every W slot
+// is 1024-byte aligned (128-byte swizzle)
+constexpr int kSmemS = kStages * kWBytes;
+constexpr int kSmemA = kSmemS + kStages * kSBytes;
+constexpr int kSmemBar = kSmemA + kStages * kAStride;
+constexpr int kGemmSmem = kSmemBar + 256 /*barriers, flags*/ + 1024 /*align*/;
 constexpr int kPartialFloats = kMaxRows * kTileRows;   // one partial tile: [8][128]
 
 // A "segment" is the set of verify rows that share one weight matrix: the
@@ -35,10 +41,10 @@ struct SegTable {
 
 struct GemmWorkspace {
     SegTable* seg;
-    float* inv_scale;            // [kMaxSeg][8] 2^-s of each activation row
-    __half* act16;               // [seg][T][8][256] scaled fp16, bank-swizzled
+    uint8_t* act;                // [seg][T] blocks of kAStride bytes: fp16 [8][256]
+                                 // (scaled, bank-swizzled) then float 2^-s [8]
     float* partials;             // [2 * grid][8][128] stream-K partial tiles
-    uint32_t* tile_cnt;          // [kMaxSeg * n_tiles] arrival tickets
+    uint32_t* tile_cnt;          // [seg * n_tiles * kConsumerWarps] slice arrival tickets
     unsigned long long* am_key;  // [8] packed (value, ~index) running maxima
     uint32_t* am_cnt;            // [1] quarter-tile tickets of the argmax
     float* pair_out;             // [pairs][N] MoE pair rows before the combine
@@ -49,10 +55,10 @@ struct GemmParams {
     int N, K, T, n_tiles;
     float tensor_scale;
     const SegTable* seg;
-    const float* inv_scale;
-    const __half* act16;
+    const uint8_t* act;
     float* out;
     int ldo;
+    int dense_M;                  // > 0: one dense segment of dense_M rows (no table reads)
     int argmax_M;                 // 0 = no fused argmax
     float* partials;
     uint32_t* tile_cnt;
