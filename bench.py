@@ -351,13 +351,13 @@ def run_e2e(vw4, layer, device, stream, steps, warmup, world):
     host_out = [torch.empty((M, N), dtype=torch.float32).pin_memory() for _, N, *_ in layer]
     dev_in = [h.to(device) for h in host_in]
     dev_out = [torch.empty((M, N), dtype=torch.float32, device=device) for _, N, *_ in layer]
-    ws = vw4.Workspace(device)
+    gemms = [vw4.PreparedGemm(vw4.FMT_NVFP4, qd, sd, ts, M, stream=stream)
+             for (name, N, K, qd, sd, ts) in layer]
 
     def step():
-        for j, (name, N, K, qd, sd, ts) in enumerate(layer):
+        for j in range(len(layer)):
             dev_in[j].copy_(host_in[j], non_blocking=True)
-            vw4.verify_gemm_w4(vw4.FMT_NVFP4, qd, sd, ts, dev_in[j], out=dev_out[j], workspace=ws,
-                               stream=stream)
+            gemms[j](dev_in[j], dev_out[j])
             host_out[j].copy_(dev_out[j], non_blocking=True)
 
     for _ in range(warmup):

@@ -186,6 +186,33 @@ def verify_gemm_w4(fmt: int, q: torch.Tensor, scales: torch.Tensor, tensor_scale
     return out
 
 
+class PreparedGemm:
+    """One weight matrix bound to the C ABI once: the vw4_weight descriptor,
+    a workspace sized for up to M_max verify rows and the stream handle are
+    kept, so every call is a single ctypes call with integer pointers.  The
+    computation is verify_gemm_w4 (same entry point, same kernels)."""
+
+    def __init__(self, fmt: int, q: torch.Tensor, scales: torch.Tensor, tensor_scale: float,
+                 M_max: int = 8, stream=None):
+        self._keep = (q, scales)
+        self.N, self.K = q.shape[0], q.shape[1] * 2
+        self.W = make_weight(fmt, q, scales, tensor_scale, self.N, self.K)
+        need = vw4_workspace_bytes(OP_GEMM, M_max, self.N, self.K)
+        self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+        self.ws_ptr, self.ws_bytes = self.ws.data_ptr(), self.ws.numel()
+        self.stream = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+        self._fn = load_library().verify_gemm_w4
+        self._Wref = ctypes.byref(self.W)
+
+    def __call__(self, A: torch.Tensor, out: torch.Tensor, row_argmax: torch.Tensor | None = None):
+        code = self._fn(self._Wref, A.data_ptr(), A.shape[0], A.stride(0), out.data_ptr(),
+                        out.stride(0), None if row_argmax is None else row_argmax.data_ptr(),
+                        self.ws_ptr, self.ws_bytes, self.stream)
+        if code:
+            _check(code, "verify_gemm_w4")
+        return out
+
+
 def verify_moe_w4(fmt: int, q: torch.Tensor, scales: torch.Tensor, tensor_scale: float, E: int,
                   A: torch.Tensor, rows_are_pairs: int, expert_ids: torch.Tensor,
                   gates: torch.Tensor | None, combine: int, out: torch.Tensor | None = None,

@@ -211,10 +211,11 @@ VW4_API vw4_status verify_gemm_w4(const vw4_weight* W, const void* A_dev, int M,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     CUtensorMap tmW, tmS;
+    const int sgroup = K / kStageK < kScaleGroup ? K / kStageK : kScaleGroup;
     st = make_map(&tmW, W->q_dev, static_cast<uint64_t>(K) / 2, N, kStageK / 2, kTileRows,
                   CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != VW4_OK) return st;
-    st = make_map(&tmS, W->scales_dev, static_cast<uint64_t>(K) / 16, N, 16, kTileRows,
+    st = make_map(&tmS, W->scales_dev, static_cast<uint64_t>(K) / 16, N, 16 * sgroup, kTileRows,
                   CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != VW4_OK) return st;
 
@@ -233,6 +234,7 @@ VW4_API vw4_status verify_gemm_w4(const vw4_weight* W, const void* A_dev, int M,
     p.K = K;
     p.T = T;
     p.n_tiles = n_tiles;
+    p.sgroup = sgroup;
     p.tensor_scale = W->tensor_scale;
     p.seg = ws.seg;
     p.act = ws.act;
@@ -281,10 +283,11 @@ VW4_API vw4_status verify_moe_w4(const vw4_weight* experts, int E, const void* A
 
     CUtensorMap tmW, tmS;
     const uint64_t rows = static_cast<uint64_t>(E) * N;
+    const int sgroup = K / kStageK < kScaleGroup ? K / kStageK : kScaleGroup;
     st = make_map(&tmW, experts->q_dev, static_cast<uint64_t>(K) / 2, rows, kStageK / 2,
                   kTileRows, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != VW4_OK) return st;
-    st = make_map(&tmS, experts->scales_dev, static_cast<uint64_t>(K) / 16, rows, 16, kTileRows,
+    st = make_map(&tmS, experts->scales_dev, static_cast<uint64_t>(K) / 16, rows, 16 * sgroup, kTileRows,
                   CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != VW4_OK) return st;
 
@@ -306,6 +309,7 @@ VW4_API vw4_status verify_moe_w4(const vw4_weight* experts, int E, const void* A
     p.K = K;
     p.T = T;
     p.n_tiles = n_tiles;
+    p.sgroup = sgroup;
     p.tensor_scale = experts->tensor_scale;
     p.seg = ws.seg;
     p.act = ws.act;

@@ -338,10 +338,12 @@ struct StageRegsNv {
     float2 inv;           // 2^-s of verify rows 2c, 2c+1
 };
 
+// S points at this stage's 16 bytes inside row 0 of the scale slot (rows are
+// spitch bytes apart: the box width).
 __device__ __forceinline__ void load_nvfp4(const uint8_t* __restrict__ W,
                                            const uint8_t* __restrict__ S,
-                                           const uint8_t* __restrict__ Ab, int warp, int lane,
-                                           StageRegsNv& r) {
+                                           const uint8_t* __restrict__ Ab, int spitch, int warp,
+                                           int lane, StageRegsNv& r) {
     const int g = lane >> 2, c = lane & 3;
     const uint8_t* ab = Ab + g * 512 + c * 128;
     const int sw = ((g & 1) << 2) | c;
@@ -355,8 +357,8 @@ __device__ __forceinline__ void load_nvfp4(const uint8_t* __restrict__ W,
     r.w01 = lds128(w0 + x1);
     r.w10 = lds128(w1 + x0);
     r.w11 = lds128(w1 + x1);
-    r.s0 = lds32(S + r0 * 16 + 4 * c);
-    r.s1 = lds32(S + (r0 + 8) * 16 + 4 * c);
+    r.s0 = lds32(S + r0 * spitch + 4 * c);
+    r.s1 = lds32(S + (r0 + 8) * spitch + 4 * c);
     r.inv = *reinterpret_cast<const float2*>(Ab + kABytes + 8 * c);
 }
 
@@ -397,8 +399,8 @@ struct StageRegsQ4 {
 
 __device__ __forceinline__ void load_q4_0(const uint8_t* __restrict__ W,
                                           const uint8_t* __restrict__ S,
-                                          const uint8_t* __restrict__ Ab, int warp, int lane,
-                                          StageRegsQ4& r) {
+                                          const uint8_t* __restrict__ Ab, int spitch, int warp,
+                                          int lane, StageRegsQ4& r) {
     const int g = lane >> 2, c = lane & 3;
     const uint8_t* ab = Ab + g * 512;
 #pragma unroll
@@ -412,8 +414,8 @@ __device__ __forceinline__ void load_q4_0(const uint8_t* __restrict__ W,
         r.x0[beta] = lds32(w0 + ((beta ^ g) << 4));
         r.x1[beta] = lds32(w1 + ((beta ^ g) << 4));
     }
-    r.d0 = lds128(S + r0 * 16);
-    r.d1 = lds128(S + (r0 + 8) * 16);
+    r.d0 = lds128(S + r0 * spitch);
+    r.d1 = lds128(S + (r0 + 8) * spitch);
     r.inv = *reinterpret_cast<const float2*>(Ab + kABytes + 8 * c);
 }
 
@@ -530,20 +532,62 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         const uint64_t pol_a = policy_evict_last();    // activations: reread by every tile
         uint32_t it = 0;
         bool ok = true;
-        // The weights do not depend on the activation prep: start streaming
-        // the first kStages units before waiting for it.
-        const unsigned long long n_pre =
-            (u_end - u_begin) < static_cast<unsigned long long>(kStages) ? (u_end - u_begin)
-                                                                          : kStages;
-        for (unsigned long long u = u_begin; u < u_begin + n_pre; ++u, ++it) {
+        // Scale boxes: a unit that starts a group of kScaleGroup stages (or
+        // this CTA's range) loads one box into the next scale slot.  Before
+        // reusing a slot, every stage that read the previous box must have
+        // been released; the stage ring implies it unless that was less than
+        // kStages units ago, in which case wait for that release explicitly.
+        uint32_t n_sbox = 0;
+        uint32_t slot_last[kSSlots] = {0xffffffffu, 0xffffffffu};
+        // Returns 1 when issued, 0 when a wait ran out, -1 when the unit would
+        // have to wait but may not (then nothing was changed).
+        auto issue = [&](unsigned long long u, uint32_t it_u, bool with_act, bool may_wait) -> int {
+            const int s = it_u % kStages;
             const unsigned long long tg = u / T;
             const int st = static_cast<int>(u % T);
             const int sg = static_cast<int>(tg / n_tiles), tile = static_cast<int>(tg % n_tiles);
             const int expert = p.dense_M > 0 ? 0 : p.seg->expert[sg];
             const int row0 = expert * p.N + tile * kTileRows;
-            mbar_arrive_expect_tx(&full[it], kStageBytes);
-            tma_load_2d(smem + it * kWBytes, &tmW, st * (kStageK / 2), row0, &full[it], pol_w);
-            tma_load_2d(smem + kSmemS + it * kSBytes, &tmS, st * 16, row0, &full[it], pol_s);
+            const int sg_n = p.sgroup;
+            const bool new_box = (u == u_begin) || (st % sg_n == 0);
+            // the activation copy of a unit issued before the prep wait is
+            // added later, but its bytes are expected here already
+            uint32_t bytes = kWBytes + kAStride;
+            int sslot = (n_sbox + kSSlots - 1) % kSSlots;
+            if (new_box) {
+                sslot = n_sbox % kSSlots;
+                const uint32_t last = slot_last[sslot];
+                if (last != 0xffffffffu && it_u - last < static_cast<uint32_t>(kStages)) {
+                    if (!may_wait) return -1;
+                    if (!mbar_wait_bounded(&empty[last % kStages], (last / kStages) & 1, p.wait_ns,
+                                           abort_flag))
+                        return 0;
+                }
+                bytes += kTileRows * 16 * sg_n;
+                ++n_sbox;
+            }
+            slot_last[sslot] = it_u;
+            mbar_arrive_expect_tx(&full[s], bytes);
+            tma_load_2d(smem + s * kWBytes, &tmW, st * (kStageK / 2), row0, &full[s], pol_w);
+            if (new_box) {  // box start: this stage, moved back to fit inside the row
+                const int st_box = st < T - sg_n ? st : T - sg_n;
+                tma_load_2d(smem + kSmemS + sslot * kSSlotBytes, &tmS, st_box * 16, row0, &full[s],
+                            pol_s);
+            }
+            if (with_act)
+                bulk_load(smem + kSmemA + s * kAStride,
+                          p.act + (static_cast<size_t>(sg) * T + st) * kAStride, kAStride,
+                          &full[s], pol_a);
+            return 1;
+        };
+        // The weights and scales do not depend on the activation prep: start
+        // streaming up to kStages units before waiting for it (stopping early
+        // rather than waiting on consumers, who need the activations first).
+        unsigned long long n_pre = 0;
+        for (unsigned long long u = u_begin; u < u_end && n_pre < kStages; ++u) {
+            if (issue(u, it, false, false) != 1) break;
+            ++it;
+            ++n_pre;
         }
         grid_dependency_wait();
         for (uint32_t j = 0; j < it; ++j) {
@@ -557,21 +601,12 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         }
         for (unsigned long long u = u_begin + n_pre; u < u_end; ++u, ++it) {
             const int s = it % kStages;
-            if (!mbar_wait_bounded(&empty[s], ((it / kStages) - 1) & 1, p.wait_ns, abort_flag)) {
+            if ((it >= static_cast<uint32_t>(kStages) &&
+                 !mbar_wait_bounded(&empty[s], ((it / kStages) - 1) & 1, p.wait_ns, abort_flag)) ||
+                issue(u, it, true, true) != 1) {
                 ok = false;
                 break;
             }
-            const unsigned long long tg = u / T;
-            const int st = static_cast<int>(u % T);
-            const int sg = static_cast<int>(tg / n_tiles), tile = static_cast<int>(tg % n_tiles);
-            const int expert = p.dense_M > 0 ? 0 : p.seg->expert[sg];
-            const int row0 = expert * p.N + tile * kTileRows;
-            mbar_arrive_expect_tx(&full[s], kStageBytes);
-            tma_load_2d(smem + s * kWBytes, &tmW, st * (kStageK / 2), row0, &full[s], pol_w);
-            tma_load_2d(smem + kSmemS + s * kSBytes, &tmS, st * 16, row0, &full[s], pol_s);
-            bulk_load(smem + kSmemA + s * kAStride,
-                      p.act + (static_cast<size_t>(sg) * T + st) * kAStride, kAStride, &full[s],
-                      pol_a);
         }
         if (!ok) {
             atomicOr(p.status, kStatusTimeout);
@@ -588,6 +623,8 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     grid_dependency_wait();  // activations, scales of this call, tickets reset
     const int g = lane >> 2, c = lane & 3;
     uint32_t it = 0;
+    uint32_t n_sbox = 0;  // scale boxes seen, in the producer's order
+    int sbox_st = 0;      // first stage covered by the current scale box
     const unsigned long long my_first_tile = u_begin / T;
     for (unsigned long long u = u_begin; u < u_end;) {
         const unsigned long long tg = u / T;
@@ -604,21 +641,26 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                 *abort_flag = 1;
                 return;
             }
+            if ((u == u_begin && st == st0) || st % p.sgroup == 0) {
+                ++n_sbox;
+                sbox_st = st < T - p.sgroup ? st : T - p.sgroup;
+            }
             const uint8_t* Ws = smem + s * kWBytes;
-            const uint8_t* Ss = smem + kSmemS + s * kSBytes;
+            const uint8_t* Ss = smem + kSmemS + ((n_sbox - 1) % kSSlots) * kSSlotBytes +
+                                (st - sbox_st) * 16;
             const uint8_t* As = smem + kSmemA + s * kAStride;
             float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
             float2 inv;
             if (FMT == 1) {
                 StageRegsNv r;
-                load_nvfp4(Ws, Ss, As, warp, lane, r);
+                load_nvfp4(Ws, Ss, As, 16 * p.sgroup, warp, lane, r);
                 __syncwarp();  // every lane's reads of the slot are done:
                 if (lane == 0) mbar_arrive(&empty[s]);  // the producer may refill it
                 compute_nvfp4(r, acc0, acc1);
                 inv = r.inv;
             } else {
                 StageRegsQ4 r;
-                load_q4_0(Ws, Ss, As, warp, lane, r);
+                load_q4_0(Ws, Ss, As, 16 * p.sgroup, warp, lane, r);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
                 compute_q4_0(r, acc0, acc1);

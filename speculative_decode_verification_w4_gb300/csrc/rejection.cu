@@ -270,11 +270,7 @@ __device__ RowInfo row_stats(cg::cluster_group& cl, float* s, int n, int lo, int
         s[k] = e;
         const unsigned long long W = mass_of(e);
         lsum += W;
-        if (W != 0ull && P < kKeepAll) {
-            const int bk = log_bucket(W);
-            atomicAdd(&sm.cnt[bk], 1u);
-            atomicAdd(&sm.mass[bk], W);
-        }
+        if (W != 0ull && P < kKeepAll) atomicAdd(&sm.mass[log_bucket(W)], W);
     }
     lsum = block_sum_u64(lsum, sm);
     if (tid == 0) sm.lsum = lsum;
@@ -291,40 +287,40 @@ __device__ RowInfo row_stats(cg::cluster_group& cl, float* s, int n, int lo, int
         return info;
     }
     const u128 TGT = static_cast<u128>(P) * S;
-    for (int t = tid; t < kLogBuckets; t += kThreads) {
-        unsigned int c = 0;
-        unsigned long long m = 0;
-        for (int r = 0; r < C; ++r) {
-            c += cl.map_shared_rank(&sm.cnt[0], r)[t];
-            m += cl.map_shared_rank(&sm.mass[0], r)[t];
-        }
-        sm.mcnt[t] = c;
-        sm.mmass[t] = m;
+    // merged bucket masses, then a block-wide suffix sum: the crossing bucket
+    // beta is the highest bucket whose suffix mass reaches the target
+    unsigned long long m = 0;
+    const int tb = kLogBuckets - 1 - tid;  // thread tid holds bucket 311 - tid
+    if (tb >= 1) {
+        for (int r = 0; r < C; ++r) m += cl.map_shared_rank(&sm.mass[0], r)[tb];
+        sm.mmass[tb] = m;
     }
-    __syncthreads();
+    u128 tot_unused;
+    const u128 incl = block_excl_u128(static_cast<u128>(m), sm, tot_unused) + m;  // mass of >= tb
     if (tid == 0) {
-        unsigned long long above = 0;
-        int beta = 1;
-        for (int t = kLogBuckets - 1; t >= 1; --t) {
-            if ((static_cast<u128>(above + sm.mmass[t]) << 32) >= TGT) {
-                beta = t;
-                break;
-            }
-            above += sm.mmass[t];
-        }
-        sm.beta = beta;
-        sm.above = above;
         sm.ncand = 0;
         sm.overflow = 0;
+    }
+    if (tb >= 1 && (incl << 32) >= TGT && ((incl - m) << 32) < TGT) {
+        sm.beta = tb;
+        sm.above = static_cast<unsigned long long>(incl - m);
     }
     __syncthreads();
 
     // 3. gather the members of the crossing bucket
     const int beta = sm.beta;
-    for (int k = tid; k < n; k += kThreads) {
-        const unsigned long long W = mass_of(s[k]);
-        if (W != 0ull && log_bucket(W) == beta) {
-            const unsigned int slot = atomicAdd(&sm.ncand, 1u);
+    const int lane = tid & 31;
+    for (int k0 = tid - lane; k0 < n; k0 += kThreads) {  // warp-uniform trip count
+        const int k = k0 + lane;
+        const unsigned long long W = k < n ? mass_of(s[k]) : 0ull;
+        const bool hit = W != 0ull && log_bucket(W) == beta;
+        const unsigned int ball = __ballot_sync(0xffffffffu, hit);
+        if (ball == 0u) continue;
+        unsigned int base = 0;
+        if (lane == 0) base = atomicAdd(&sm.ncand, static_cast<unsigned int>(__popc(ball)));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if (hit) {
+            const unsigned int slot = base + __popc(ball & ((1u << lane) - 1u));
             if (slot < static_cast<unsigned int>(kCandLocal)) {
                 sm.cw[slot] = W;
                 sm.ci[slot] = lo + k;
@@ -415,7 +411,7 @@ __device__ RowInfo row_stats(cg::cluster_group& cl, float* s, int n, int lo, int
             sm.lo = static_cast<unsigned long long>(beta);
             sm.width = 1;
             sm.wbits = 0;
-            sm.n_eq = sm.mcnt[beta];
+            sm.n_eq = total;  // every member of an exact bucket has W == beta
         } else {
             const int msb = 4 + (beta - 16) / 8, j = (beta - 16) % 8;
             sm.wbits = msb - 3;
@@ -455,23 +451,27 @@ __device__ RowInfo row_stats(cg::cluster_group& cl, float* s, int n, int lo, int
             sm.mmass[t] = m;
         }
         __syncthreads();
-        if (tid == 0) {
-            unsigned long long above = sm.above;
-            int sb = 0;
-            for (int t = (1 << bits) - 1; t >= 0; --t) {
-                if ((static_cast<u128>(above + sm.mmass[t]) << 32) >= TGT) {
-                    sb = t;
-                    break;
-                }
-                above += sm.mmass[t];
+        {
+            const int nb = 1 << bits;
+            const int t = nb - 1 - tid;  // thread tid holds sub-bucket nb - 1 - tid
+            const unsigned long long mt = t >= 0 ? sm.mmass[t] : 0ull;
+            u128 tot2;
+            const u128 inc = block_excl_u128(static_cast<u128>(mt), sm, tot2) + mt;
+            const u128 ab = static_cast<u128>(sm.above);
+            if (t >= 0 && ((ab + inc) << 32) >= TGT && ((ab + inc - mt) << 32) < TGT) {
+                sm.beta = t;
+                sm.lo = rlo + (static_cast<unsigned long long>(t) << shift);
+                sm.n_eq = sm.mcnt[t];
+                sm.count_eq = static_cast<unsigned long long>(ab + inc - mt);
             }
-            sm.above = above;
-            sm.lo = rlo + (static_cast<unsigned long long>(sb) << shift);
-            sm.width = 1ull << shift;
-            sm.wbits = shift;
-            if (shift == 0) sm.n_eq = sm.mcnt[sb];
+            __syncthreads();
+            if (tid == 0) {
+                sm.above = sm.count_eq;
+                sm.width = 1ull << shift;
+                sm.wbits = shift;
+            }
+            __syncthreads();
         }
-        __syncthreads();
     }
     const unsigned long long tau = sm.lo, above = sm.above, n_eq = sm.n_eq;
     // smallest j >= 1 with (above + j*tau) * 2^32 >= P*S

@@ -17,14 +17,21 @@ constexpr int kStages = 4;         // pipeline depth
 constexpr int kConsumerWarps = 8;  // each owns 16 rows of the tile
 constexpr int kGemmThreads = (kConsumerWarps + 1) * 32;
 constexpr int kWBytes = kTileRows * (kStageK / 2);     // 16384: packed nibbles
-constexpr int kSBytes = kTileRows * 16;                // 2048: 16 B of scales per row
 constexpr int kABytes = kMaxRows * kStageK * 2;        // 4096: fp16 activations
 constexpr int kAStride = kABytes + kMaxRows * 4;       // + the 8 rows' 2^-s: 4128
-constexpr int kStageBytes = kWBytes + kSBytes + kAStride;  // bytes streamed per unit
-// shared memory: [W x kStages][S x kStages][A x kStages][barriers]; every W slot
-// is 1024-byte aligned (128-byte swizzle)
+// Scales travel in boxes of 128 rows x (16 * g) bytes that cover g = min(4, T)
+// consecutive stages (16 bytes per row per stage), into a ring of 2 slots: one
+// request of two full sectors per row instead of four half-sector requests.
+// Every box lies inside the row: the last one of a row is moved back to end
+// at the row's end.
+constexpr int kScaleGroup = 4;
+constexpr int kSBoxBytes = 16 * kScaleGroup;           // 64 (slot row pitch)
+constexpr int kSSlotBytes = kTileRows * kSBoxBytes;    // 8192
+constexpr int kSSlots = 2;
+// shared memory: [W x kStages][S x kSSlots][A x kStages][barriers]; every W
+// slot is 1024-byte aligned (128-byte swizzle)
 constexpr int kSmemS = kStages * kWBytes;
-constexpr int kSmemA = kSmemS + kStages * kSBytes;
+constexpr int kSmemA = kSmemS + kSSlots * kSSlotBytes;
 constexpr int kSmemBar = kSmemA + kStages * kAStride;
 constexpr int kGemmSmem = kSmemBar + 256 /*barriers, flags*/ + 1024 /*align*/;
 constexpr int kPartialFloats = kMaxRows * kTileRows;   // one partial tile: [8][128]
@@ -53,6 +60,7 @@ struct GemmWorkspace {
 
 struct GemmParams {
     int N, K, T, n_tiles;
+    int sgroup;                   // stages per scale box, min(kScaleGroup, T)
     float tensor_scale;
     const SegTable* seg;
     const uint8_t* act;

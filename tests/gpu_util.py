@@ -44,6 +44,8 @@ def gemm_gpu(fmt, q, s, ts, A_bits, out=None, row_argmax=None, lda_pad=0, ldo_pa
         out = torch.full((M, N + ldo_pad), float("nan"), dtype=torch.float32, device="cuda")[:, :N]
     o = vw4.verify_gemm_w4(FMT[fmt], qd, sd, ts, Ad, out=out, row_argmax=row_argmax)
     torch.cuda.synchronize()
+    st = vw4.vw4_get_device_status()
+    assert st == 0, f"device status {st:#x} after verify_gemm_w4"
     return o
 
 

@@ -50,6 +50,19 @@ def test_small_shapes_elementwise(fmt, N, K, M):
 
 
 @pytest.mark.parametrize("fmt", ["nvfp4", "q4_0"])
+@pytest.mark.parametrize("N,K,M", [(5000, 5376, 8), (20000, 5376, 1), (3000, 1792, 3),
+                                   (9000, 3328, 2)])
+def test_stage_counts_not_multiple_of_scale_group(fmt, N, K, M):
+    """K/256 = 21, 7, 13: the last group of scale stages in a row is short, and
+    with many tiles the stream-K ranges start at every stage offset."""
+    q, s, ts, A = _case(fmt, N + K + M, N, K, M)
+    gpu = gemm_gpu(fmt, q, s, ts, A).cpu().numpy()
+    cols = np.unique(np.concatenate([np.arange(0, N, 7), [N - 1]])).astype(np.int32)
+    ref, bnd = oracle.gemm_w4(ORACLE_FMT[fmt], N, K, q, s, ts, A, cols=cols)
+    assert_gemm_close(gpu[:, cols], ref, bnd, f"{fmt} N={N} K={K} M={M}")
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "q4_0"])
 def test_strided_activations_and_outputs(fmt):
     N, K, M = 333, 1024, 5
     q, s, ts, A = _case(fmt, 99, N, K, M)
@@ -152,6 +165,19 @@ def test_lm_head_full_size_sampled_and_fused_argmax():
             k = int(np.searchsorted(cols, am[m]))
             gap = ref[m, j] - ref[m, k]
             assert gap <= 2e-3 * max(bnd[m, j], bnd[m, k]), (m, cols[j], am[m], gap)
+
+
+def test_prepared_gemm_matches_plain_call():
+    N, K, M = 900, 1536, 6
+    q, s, ts, A = _case("nvfp4", 12, N, K, M)
+    qd, sd = upload_weight(q, s, "nvfp4")
+    Ad = bf16_dev(A)
+    plain = vw4.verify_gemm_w4(vw4.FMT_NVFP4, qd, sd, ts, Ad)
+    prep = vw4.PreparedGemm(vw4.FMT_NVFP4, qd, sd, ts, M_max=8)
+    out = torch.empty_like(plain)
+    prep(Ad, out)
+    torch.cuda.synchronize()
+    assert torch.equal(plain, out)
 
 
 def test_q4_0_from_blocks_matches_split_layout():
