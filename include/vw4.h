@@ -218,6 +218,32 @@ VW4_API vw4_status accept_rejection(const float* target_logits_dev, const float*
                                     int32_t* tokens_dev, int32_t* len_dev, void* workspace_dev,
                                     size_t ws_bytes, void* stream);
 
+/*
+ * verify_gemm_w4_noalloc -- verify_gemm_w4 for callers that cannot allocate.
+ *
+ * No counterpart in the source material: this is a deployment convenience.
+ * Some callers have no way to provide a workspace: a plugin that is handed
+ * only its input and output pointers, code living in another framework's
+ * memory pool that must not allocate outside it, or a path where calling
+ * cudaMalloc would synchronize the device.  This entry point takes no
+ * workspace and allocates nothing; it uses one fixed 8 MiB scratch array in
+ * device memory that the library reserves on every GPU it is loaded on, for
+ * as long as the process lives.
+ *
+ * Arguments, result and errors are those of verify_gemm_w4, plus:
+ * VW4_ERR_WORKSPACE (with a message from vw4_last_error_string) when the
+ * shape needs more scratch than the fixed array holds -- every verify shape of
+ * the dense layer and LM-head configurations fits.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress); make that
+ * first call before any stream capture.  Each GPU has its own array, and each
+ * call resets the parts of it that must start at zero, but all calls on one
+ * GPU share it: calls that can overlap there (on different streams, from
+ * different threads) race on it, so serialize them.
+ */
+VW4_API vw4_status verify_gemm_w4_noalloc(const vw4_weight* W, const void* A_dev, int M, int lda,
+                                          float* out_dev, int ldo, int32_t* row_argmax_dev,
+                                          void* stream);
+
 /* Workspace bytes needed by an operation:
  *   VW4_OP_GEMM:      (M, N, K)
  *   VW4_OP_MOE:       (M*topk, N, K)   -- pass the number of routed pairs first

@@ -41,7 +41,7 @@ STATUS_NAMES = {0: "VW4_OK", 1: "VW4_ERR_INVALID_ARG", 2: "VW4_ERR_UNSUPPORTED",
 EXPORTS = ("verify_gemm_w4", "verify_moe_w4", "accept_greedy", "accept_rejection",
            "vw4_workspace_bytes", "vw4_get_device_status", "vw4_q4_0_from_blocks",
            "vw4_status_str", "vw4_last_error_string", "vw4_version", "vw4_set_wait_limit_ns",
-           "vw4_own_exp")
+           "vw4_own_exp", "verify_gemm_w4_noalloc")
 
 
 class VW4Error(RuntimeError):
@@ -95,6 +95,7 @@ def load_library(path: str = LIB_PATH):
             "vw4_version": (I, []),
             "vw4_set_wait_limit_ns": (None, [U64]),
             "vw4_own_exp": (I, [P, P, ctypes.c_int64, P]),
+            "verify_gemm_w4_noalloc": (I, [ctypes.POINTER(Weight), P, I, I, P, I, P, P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -211,6 +212,26 @@ class PreparedGemm:
         if code:
             _check(code, "verify_gemm_w4")
         return out
+
+
+def verify_gemm_w4_noalloc(fmt: int, q: torch.Tensor, scales: torch.Tensor, tensor_scale: float,
+                           A: torch.Tensor, out: torch.Tensor | None = None,
+                           row_argmax: torch.Tensor | None = None, stream=None):
+    """verify_gemm_w4 without a workspace: for callers that cannot allocate
+    device memory.  The library's fixed device scratch array is used instead;
+    calls that may overlap on the GPU must be serialized by the caller."""
+    N, K = q.shape[0], q.shape[1] * 2
+    M = A.shape[0]
+    if A.dtype != torch.bfloat16:
+        raise ValueError("A must be bfloat16")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    W = make_weight(fmt, q, scales, tensor_scale, N, K)
+    code = load_library().verify_gemm_w4_noalloc(ctypes.byref(W), _ptr(A), M, A.stride(0),
+                                                 _ptr(out), out.stride(0), _ptr(row_argmax),
+                                                 _stream(stream))
+    _check(code, "verify_gemm_w4_noalloc")
+    return out
 
 
 def verify_moe_w4(fmt: int, q: torch.Tensor, scales: torch.Tensor, tensor_scale: float, E: int,

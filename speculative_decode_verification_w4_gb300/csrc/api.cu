@@ -406,6 +406,66 @@ VW4_API vw4_status vw4_get_device_status(uint32_t* bits, void* stream) {
     return VW4_OK;
 }
 
+}  // extern "C"
+
+// ------------------------------------------------------------------------
+// Allocation-free variant of verify_gemm_w4.
+//
+// Some callers cannot allocate device memory at the point where they need
+// the verify GEMM: code running inside another framework's memory pool that
+// forbids foreign allocations, a plugin handed only input and output
+// pointers, or a path that must not call cudaMalloc because it would
+// synchronize the device or fail under a capture.  For them this file keeps
+// one fixed scratch array in device memory, reserved on every GPU that loads
+// the library until the process exits.  The host only ever passes the
+// array's device address, obtained once per device with
+// cudaGetSymbolAddress while that device is current (the symbol itself is a
+// host-side stand-in, not a device address).
+// Every GPU has its own copy of the array.  Its size bounds the shapes this
+// entry point accepts (the workspace of verify_gemm_w4 for that shape).
+static constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_ptr[kMaxDevices] = {};
+
+extern "C" {
+
+VW4_API vw4_status verify_gemm_w4_noalloc(const vw4_weight* W, const void* A_dev, int M, int lda,
+                                          float* out_dev, int ldo, int32_t* row_argmax_dev,
+                                          void* stream) {
+    if (W && W->N >= 1 && W->K >= kStageK && W->K % kStageK == 0) {
+        const size_t need = gemm_workspace_layout(nullptr, 1, W->N, W->K, kMaxGrid, 0).bytes;
+        if (need > kNoAllocScratchBytes) {
+            char buf[160];
+            snprintf(buf, sizeof buf,
+                     "verify_gemm_w4_noalloc: N=%d K=%d needs %zu scratch bytes, above the "
+                     "fixed %zu",
+                     W->N, W->K, need, kNoAllocScratchBytes);
+            g_last_error = buf;
+            return VW4_ERR_WORKSPACE;
+        }
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return VW4_ERR_UNSUPPORTED;
+    void* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_noalloc_mu);
+        if (g_noalloc_ptr[dev] == nullptr) {  // first call on this device
+            void* p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+            if (e != cudaSuccess || p == nullptr)
+                return cuda_fail(e == cudaSuccess ? cudaErrorInvalidSymbol : e,
+                                 "cudaGetSymbolAddress(noalloc scratch)");
+            g_noalloc_ptr[dev] = p;
+        }
+        scratch = g_noalloc_ptr[dev];
+    }
+    return verify_gemm_w4(W, A_dev, M, lda, out_dev, ldo, row_argmax_dev, scratch,
+                          kNoAllocScratchBytes, stream);
+}
+
 VW4_API vw4_status vw4_own_exp(const float* x_dev, float* y_dev, int64_t n, void* stream) {
     if (!x_dev || !y_dev || n < 0) return VW4_ERR_INVALID_ARG;
     if (n == 0) return VW4_OK;
