@@ -319,51 +319,60 @@ __device__ __forceinline__ uint32_t q4pair(uint32_t x) {
     return hsub2((x & 0x000F000Fu) | 0x64006400u, 0x64086408u);
 }
 
-// One 256-wide k slice of the warp's 16 rows.  Each stage is split into a
-// load phase, which copies everything the warp needs out of the ring slot into
-// registers (after which the slot is released to the producer), and a compute
-// phase that works on registers only.
+// One 256-wide k slice of the warp's 32 rows, as two 16-row MMA blocks that
+// share the activation fragments.  Each stage is split into a load phase,
+// which copies everything the warp needs out of the ring slot into registers
+// (after which the slot is released to the producer), and a compute phase
+// that works on registers only.  Row block rb of warp w covers tile rows
+// 32w + 16rb + [0, 16); lane (g, c) holds rows g and g+8 of the block.  The
+// 128-byte swizzle XORs the 16-byte chunk index with the row mod 8, which is
+// g for every row a lane touches.
 //
-// nvfp4 -- lane (g, c): rows g and g+8 of the warp's tile; its k range is
-//   [64c, 64c+64) of the slice, i.e. 16-byte chunks 2c and 2c+1 of a row.
-//   MMA j takes elements 64c+4j .. 64c+4j+3 from every lane: the A operand
-//   pairs (k 2c,2c+1) and (k 2c+8,2c+9) of the mma fragment are mapped to
-//   these four consecutive elements, and the B operand uses the same map, so
-//   the sum over the slice is unchanged.  Even and odd MMAs accumulate into
-//   two independent chains.
-struct StageRegsNv {
-    uint4 bf[8];          // B operand: this lane's 64 activations
-    uint4 w00, w01, w10, w11;  // rows g and g+8: chunks 2c, 2c+1
-    uint32_t s0, s1;      // four e4m3 block scales of rows g and g+8
-    float2 inv;           // 2^-s of verify rows 2c, 2c+1
+// nvfp4 -- lane c's k range is [64c, 64c+64) of the slice, i.e. 16-byte
+//   chunks 2c and 2c+1 of a row.  MMA j takes elements 64c+4j .. 64c+4j+3
+//   from every lane: the A operand pairs (k 2c,2c+1) and (k 2c+8,2c+9) of the
+//   mma fragment are mapped to these four consecutive elements, and the B
+//   operand uses the same map, so the sum over the slice is unchanged.  Even
+//   and odd MMAs accumulate into two independent chains.
+struct ActRegs {
+    uint4 bf[8];  // B operand: this lane's 64 activations
+    float2 inv;   // 2^-s of verify rows 2c, 2c+1
 };
 
-// S points at this stage's 16 bytes inside row 0 of the scale slot (rows are
-// spitch bytes apart: the box width).
-__device__ __forceinline__ void load_nvfp4(const uint8_t* __restrict__ W,
-                                           const uint8_t* __restrict__ S,
-                                           const uint8_t* __restrict__ Ab, int spitch, int warp,
-                                           int lane, StageRegsNv& r) {
+struct WRegsNv {
+    uint4 w00, w01, w10, w11;  // rows g and g+8: chunks 2c, 2c+1
+    uint32_t s0, s1;           // four e4m3 block scales of rows g and g+8
+};
+
+__device__ __forceinline__ void load_act_nvfp4(const uint8_t* __restrict__ Ab, int lane,
+                                               ActRegs& a) {
     const int g = lane >> 2, c = lane & 3;
     const uint8_t* ab = Ab + g * 512 + c * 128;
     const int sw = ((g & 1) << 2) | c;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) r.bf[i] = lds128(ab + ((i ^ sw) << 4));
-    const int r0 = warp * 16 + g;
+    for (int i = 0; i < 8; ++i) a.bf[i] = lds128(ab + ((i ^ sw) << 4));
+    a.inv = *reinterpret_cast<const float2*>(Ab + kABytes + 8 * c);
+}
+
+// W: the stage's weight slot; Sr: this stage's 16 bytes inside the scale
+// slot row of tile row r0 (rows are spitch bytes apart: the box width).
+__device__ __forceinline__ void load_w_nvfp4(const uint8_t* __restrict__ W,
+                                             const uint8_t* __restrict__ Sr, int spitch, int r0,
+                                             int lane, WRegsNv& r) {
+    const int g = lane >> 2, c = lane & 3;
     const uint8_t* w0 = W + r0 * 128;
     const uint8_t* w1 = w0 + 8 * 128;
-    const int x0 = ((2 * c) ^ g) << 4, x1 = ((2 * c + 1) ^ g) << 4;  // 128-byte swizzle
+    const int x0 = ((2 * c) ^ g) << 4, x1 = ((2 * c + 1) ^ g) << 4;
     r.w00 = lds128(w0 + x0);
     r.w01 = lds128(w0 + x1);
     r.w10 = lds128(w1 + x0);
     r.w11 = lds128(w1 + x1);
-    r.s0 = lds32(S + r0 * spitch + 4 * c);
-    r.s1 = lds32(S + (r0 + 8) * spitch + 4 * c);
-    r.inv = *reinterpret_cast<const float2*>(Ab + kABytes + 8 * c);
+    r.s0 = lds32(Sr + 4 * c);
+    r.s1 = lds32(Sr + 8 * spitch + 4 * c);
 }
 
-__device__ __forceinline__ void compute_nvfp4(const StageRegsNv& r, float (&acc0)[4],
-                                              float (&acc1)[4]) {
+__device__ __forceinline__ void compute_nvfp4(const ActRegs& a, const WRegsNv& r,
+                                              float (&acc0)[4], float (&acc1)[4]) {
     uint32_t sa0, sb0, sa1, sb1;
     cvt_e4m3x4(r.s0, sa0, sb0);
     cvt_e4m3x4(r.s1, sa1, sb1);
@@ -379,9 +388,9 @@ __device__ __forceinline__ void compute_nvfp4(const StageRegsNv& r, float (&acc0
         cvt_e2m1x8(wr0[wi], h0, h1, h2, h3);
         cvt_e2m1x8(wr1[wi], q0, q1, q2, q3);
         const uint32_t s0 = sc0[wi >> 1], s1 = sc1[wi >> 1];
-        const uint32_t* b = reinterpret_cast<const uint32_t*>(&r.bf[wi]);
-        mma16816(acc0, hmul2(h0, s0), hmul2(q0, s1), hmul2(h1, s0), hmul2(q1, s1), b[0], b[1]);
-        mma16816(acc1, hmul2(h2, s0), hmul2(q2, s1), hmul2(h3, s0), hmul2(q3, s1), b[2], b[3]);
+        const uint4& b = a.bf[wi];
+        mma16816(acc0, hmul2(h0, s0), hmul2(q0, s1), hmul2(h1, s0), hmul2(q1, s1), b.x, b.y);
+        mma16816(acc1, hmul2(h2, s0), hmul2(q2, s1), hmul2(h3, s0), hmul2(q3, s1), b.z, b.w);
     }
 }
 
@@ -390,23 +399,25 @@ __device__ __forceinline__ void compute_nvfp4(const StageRegsNv& r, float (&acc0
 //   high nibbles 4c+16..4c+19.  The two MMAs of a block run on exact integers
 //   (q - 8) into a zeroed temporary, and the block's fp16 scale is applied to
 //   the fp32 result.
-struct StageRegsQ4 {
-    uint4 bf[8];
+struct WRegsQ4 {
     uint32_t x0[8], x1[8];  // rows g and g+8, bytes 4c..4c+3 of each block
     uint4 d0, d1;           // the eight fp16 scales of rows g and g+8
-    float2 inv;
 };
 
-__device__ __forceinline__ void load_q4_0(const uint8_t* __restrict__ W,
-                                          const uint8_t* __restrict__ S,
-                                          const uint8_t* __restrict__ Ab, int spitch, int warp,
-                                          int lane, StageRegsQ4& r) {
+__device__ __forceinline__ void load_act_q4_0(const uint8_t* __restrict__ Ab, int lane,
+                                              ActRegs& a) {
     const int g = lane >> 2, c = lane & 3;
     const uint8_t* ab = Ab + g * 512;
 #pragma unroll
     for (int beta = 0; beta < 8; ++beta)
-        r.bf[beta] = lds128(ab + ((((beta << 2) | c) ^ ((g & 1) << 2)) << 4));
-    const int r0 = warp * 16 + g;
+        a.bf[beta] = lds128(ab + ((((beta << 2) | c) ^ ((g & 1) << 2)) << 4));
+    a.inv = *reinterpret_cast<const float2*>(Ab + kABytes + 8 * c);
+}
+
+__device__ __forceinline__ void load_w_q4_0(const uint8_t* __restrict__ W,
+                                            const uint8_t* __restrict__ Sr, int spitch, int r0,
+                                            int lane, WRegsQ4& r) {
+    const int g = lane >> 2, c = lane & 3;
     const uint8_t* w0 = W + r0 * 128 + 4 * c;
     const uint8_t* w1 = w0 + 8 * 128;
 #pragma unroll
@@ -414,23 +425,22 @@ __device__ __forceinline__ void load_q4_0(const uint8_t* __restrict__ W,
         r.x0[beta] = lds32(w0 + ((beta ^ g) << 4));
         r.x1[beta] = lds32(w1 + ((beta ^ g) << 4));
     }
-    r.d0 = lds128(S + r0 * spitch);
-    r.d1 = lds128(S + (r0 + 8) * spitch);
-    r.inv = *reinterpret_cast<const float2*>(Ab + kABytes + 8 * c);
+    r.d0 = lds128(Sr);
+    r.d1 = lds128(Sr + 8 * spitch);
 }
 
-__device__ __forceinline__ void compute_q4_0(const StageRegsQ4& r, float (&acc0)[4],
-                                             float (&acc1)[4]) {
+__device__ __forceinline__ void compute_q4_0(const ActRegs& a, const WRegsQ4& r,
+                                             float (&acc0)[4], float (&acc1)[4]) {
     const uint32_t dw0[4] = {r.d0.x, r.d0.y, r.d0.z, r.d0.w};
     const uint32_t dw1[4] = {r.d1.x, r.d1.y, r.d1.z, r.d1.w};
 #pragma unroll
     for (int beta = 0; beta < 8; ++beta) {
         const uint32_t x0 = r.x0[beta], x1 = r.x1[beta];
-        const uint32_t* b = reinterpret_cast<const uint32_t*>(&r.bf[beta]);
+        const uint4& b = a.bf[beta];
         float t[4] = {0.f, 0.f, 0.f, 0.f};
-        mma16816(t, q4pair(x0), q4pair(x1), q4pair(x0 >> 8), q4pair(x1 >> 8), b[0], b[1]);
-        mma16816(t, q4pair(x0 >> 4), q4pair(x1 >> 4), q4pair(x0 >> 12), q4pair(x1 >> 12), b[2],
-                 b[3]);
+        mma16816(t, q4pair(x0), q4pair(x1), q4pair(x0 >> 8), q4pair(x1 >> 8), b.x, b.y);
+        mma16816(t, q4pair(x0 >> 4), q4pair(x1 >> 4), q4pair(x0 >> 12), q4pair(x1 >> 12), b.z,
+                 b.w);
         const __half2 dh0 = *reinterpret_cast<const __half2*>(&dw0[beta >> 1]);
         const __half2 dh1 = *reinterpret_cast<const __half2*>(&dw1[beta >> 1]);
         const float e0 = (beta & 1) ? __high2float(dh0) : __low2float(dh0);
@@ -538,25 +548,48 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         // been released; the stage ring implies it unless that was less than
         // kStages units ago, in which case wait for that release explicitly.
         uint32_t n_sbox = 0;
-        uint32_t slot_last[kSSlots] = {0xffffffffu, 0xffffffffu};
+        static_assert(kSSlots == 2, "two scale slots");
+        uint32_t slot_last0 = 0xffffffffu, slot_last1 = 0xffffffffu;  // last unit per slot
+        const int sg_n = p.sgroup;
+        const int smask = sg_n == kScaleGroup ? kScaleGroup - 1 : 0x7fffffff;
+        // Position of a unit: k stage, row tile, segment; advanced one unit at
+        // a time so that the loop does no division.
+        struct Cursor {
+            int st, tile, sg, row0;
+        };
+        auto cursor_at = [&](unsigned long long u) {
+            const unsigned long long tg = u / T;
+            Cursor c{static_cast<int>(u % T), static_cast<int>(tg % n_tiles),
+                     static_cast<int>(tg / n_tiles), 0};
+            const int expert = p.dense_M > 0 ? 0 : p.seg->expert[c.sg];
+            c.row0 = expert * p.N + c.tile * kTileRows;
+            return c;
+        };
+        auto advance = [&](Cursor& c) {
+            if (++c.st < T) return;
+            c.st = 0;
+            c.row0 += kTileRows;
+            if (++c.tile < n_tiles) return;
+            c.tile = 0;
+            ++c.sg;
+            if (c.sg < n_seg) {
+                const int expert = p.dense_M > 0 ? 0 : p.seg->expert[c.sg];
+                c.row0 = expert * p.N;
+            }
+        };
         // Returns 1 when issued, 0 when a wait ran out, -1 when the unit would
         // have to wait but may not (then nothing was changed).
-        auto issue = [&](unsigned long long u, uint32_t it_u, bool with_act, bool may_wait) -> int {
+        auto issue = [&](const Cursor& c, bool first, uint32_t it_u, bool with_act,
+                         bool may_wait) -> int {
             const int s = it_u % kStages;
-            const unsigned long long tg = u / T;
-            const int st = static_cast<int>(u % T);
-            const int sg = static_cast<int>(tg / n_tiles), tile = static_cast<int>(tg % n_tiles);
-            const int expert = p.dense_M > 0 ? 0 : p.seg->expert[sg];
-            const int row0 = expert * p.N + tile * kTileRows;
-            const int sg_n = p.sgroup;
-            const bool new_box = (u == u_begin) || (st % sg_n == 0);
+            const bool new_box = first || (c.st & smask) == 0;
             // the activation copy of a unit issued before the prep wait is
             // added later, but its bytes are expected here already
             uint32_t bytes = kWBytes + kAStride;
             int sslot = (n_sbox + kSSlots - 1) % kSSlots;
             if (new_box) {
                 sslot = n_sbox % kSSlots;
-                const uint32_t last = slot_last[sslot];
+                const uint32_t last = sslot ? slot_last1 : slot_last0;
                 if (last != 0xffffffffu && it_u - last < static_cast<uint32_t>(kStages)) {
                     if (!may_wait) return -1;
                     if (!mbar_wait_bounded(&empty[last % kStages], (last / kStages) & 1, p.wait_ns,
@@ -566,44 +599,46 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                 bytes += kTileRows * 16 * sg_n;
                 ++n_sbox;
             }
-            slot_last[sslot] = it_u;
+            if (sslot) slot_last1 = it_u;
+            else slot_last0 = it_u;
             mbar_arrive_expect_tx(&full[s], bytes);
-            tma_load_2d(smem + s * kWBytes, &tmW, st * (kStageK / 2), row0, &full[s], pol_w);
+            tma_load_2d(smem + s * kWBytes, &tmW, c.st * (kStageK / 2), c.row0, &full[s], pol_w);
             if (new_box) {  // box start: this stage, moved back to fit inside the row
-                const int st_box = st < T - sg_n ? st : T - sg_n;
-                tma_load_2d(smem + kSmemS + sslot * kSSlotBytes, &tmS, st_box * 16, row0, &full[s],
-                            pol_s);
+                const int st_box = c.st < T - sg_n ? c.st : T - sg_n;
+                tma_load_2d(smem + kSmemS + sslot * kSSlotBytes, &tmS, st_box * 16, c.row0,
+                            &full[s], pol_s);
             }
             if (with_act)
                 bulk_load(smem + kSmemA + s * kAStride,
-                          p.act + (static_cast<size_t>(sg) * T + st) * kAStride, kAStride,
+                          p.act + (static_cast<size_t>(c.sg) * T + c.st) * kAStride, kAStride,
                           &full[s], pol_a);
             return 1;
         };
         // The weights and scales do not depend on the activation prep: start
         // streaming up to kStages units before waiting for it (stopping early
         // rather than waiting on consumers, who need the activations first).
-        unsigned long long n_pre = 0;
-        for (unsigned long long u = u_begin; u < u_end && n_pre < kStages; ++u) {
-            if (issue(u, it, false, false) != 1) break;
+        const Cursor c0 = cursor_at(u_begin);
+        Cursor cur = c0;
+        const unsigned long long n_units = u_end - u_begin;
+        while (it < n_units && it < static_cast<uint32_t>(kStages)) {
+            if (issue(cur, it == 0, it, false, false) != 1) break;
             ++it;
-            ++n_pre;
+            advance(cur);
         }
+        const uint32_t n_pre = it;
         grid_dependency_wait();
-        for (uint32_t j = 0; j < it; ++j) {
-            const unsigned long long u = u_begin + j;
-            const unsigned long long tg = u / T;
-            const int st = static_cast<int>(u % T);
-            const int sg = static_cast<int>(tg / n_tiles);
-            bulk_load(smem + kSmemA + j * kAStride,
-                      p.act + (static_cast<size_t>(sg) * T + st) * kAStride, kAStride, &full[j],
-                      pol_a);
+        {
+            Cursor a = c0;
+            for (uint32_t j = 0; j < n_pre; ++j, advance(a))
+                bulk_load(smem + kSmemA + j * kAStride,
+                          p.act + (static_cast<size_t>(a.sg) * T + a.st) * kAStride, kAStride,
+                          &full[j], pol_a);
         }
-        for (unsigned long long u = u_begin + n_pre; u < u_end; ++u, ++it) {
+        for (; it < n_units; ++it, advance(cur)) {
             const int s = it % kStages;
             if ((it >= static_cast<uint32_t>(kStages) &&
                  !mbar_wait_bounded(&empty[s], ((it / kStages) - 1) & 1, p.wait_ns, abort_flag)) ||
-                issue(u, it, true, true) != 1) {
+                issue(cur, it == 0, it, true, true) != 1) {
                 ok = false;
                 break;
             }
@@ -622,9 +657,14 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     // ---------------------------------------------------------- consumers
     grid_dependency_wait();  // activations, scales of this call, tickets reset
     const int g = lane >> 2, c = lane & 3;
+    const int wrow = warp * kWarpRows;  // first tile row of this warp
     uint32_t it = 0;
     uint32_t n_sbox = 0;  // scale boxes seen, in the producer's order
-    int sbox_st = 0;      // first stage covered by the current scale box
+    // scale slot of the current box, offset back by the box's first stage
+    const uint8_t* s_base = smem + kSmemS;
+    const int sg_n = p.sgroup;
+    const int spitch = 16 * sg_n;
+    const int smask = sg_n == kScaleGroup ? kScaleGroup - 1 : 0x7fffffff;
     const unsigned long long my_first_tile = u_begin / T;
     for (unsigned long long u = u_begin; u < u_end;) {
         const unsigned long long tg = u / T;
@@ -633,7 +673,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         const int st_end = (left < static_cast<unsigned long long>(T - st0))
                                ? st0 + static_cast<int>(left)
                                : T;
-        float tot[4] = {0.f, 0.f, 0.f, 0.f};
+        float tot[kRowBlocks][4] = {};
         for (int st = st0; st < st_end; ++st, ++it) {
             const int s = it % kStages;
             if (!mbar_wait_bounded(&full[s], (it / kStages) & 1, p.wait_ns, abort_flag)) {
@@ -641,67 +681,84 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                 *abort_flag = 1;
                 return;
             }
-            if ((u == u_begin && st == st0) || st % p.sgroup == 0) {
+            if (it == 0 || (st & smask) == 0) {
                 ++n_sbox;
-                sbox_st = st < T - p.sgroup ? st : T - p.sgroup;
+                const int sbox_st = st < T - sg_n ? st : T - sg_n;
+                s_base = smem + kSmemS + ((n_sbox - 1) % kSSlots) * kSSlotBytes - sbox_st * 16;
             }
             const uint8_t* Ws = smem + s * kWBytes;
-            const uint8_t* Ss = smem + kSmemS + ((n_sbox - 1) % kSSlots) * kSSlotBytes +
-                                (st - sbox_st) * 16;
+            const uint8_t* Ss = s_base + st * 16 + (wrow + g) * spitch;
             const uint8_t* As = smem + kSmemA + s * kAStride;
-            float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
-            float2 inv;
+            float acc[kRowBlocks][2][4] = {};
+            ActRegs ar;
             if (FMT == 1) {
-                StageRegsNv r;
-                load_nvfp4(Ws, Ss, As, 16 * p.sgroup, warp, lane, r);
+                WRegsNv wr[kRowBlocks];
+                load_act_nvfp4(As, lane, ar);
+#pragma unroll
+                for (int rb = 0; rb < kRowBlocks; ++rb)
+                    load_w_nvfp4(Ws, Ss + rb * 16 * spitch, spitch, wrow + rb * 16 + g, lane,
+                                 wr[rb]);
                 __syncwarp();  // every lane's reads of the slot are done:
                 if (lane == 0) mbar_arrive(&empty[s]);  // the producer may refill it
-                compute_nvfp4(r, acc0, acc1);
-                inv = r.inv;
+#pragma unroll
+                for (int rb = 0; rb < kRowBlocks; ++rb)
+                    compute_nvfp4(ar, wr[rb], acc[rb][0], acc[rb][1]);
             } else {
-                StageRegsQ4 r;
-                load_q4_0(Ws, Ss, As, 16 * p.sgroup, warp, lane, r);
+                WRegsQ4 wr[kRowBlocks];
+                load_act_q4_0(As, lane, ar);
+#pragma unroll
+                for (int rb = 0; rb < kRowBlocks; ++rb)
+                    load_w_q4_0(Ws, Ss + rb * 16 * spitch, spitch, wrow + rb * 16 + g, lane,
+                                wr[rb]);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
-                compute_q4_0(r, acc0, acc1);
-                inv = r.inv;
+#pragma unroll
+                for (int rb = 0; rb < kRowBlocks; ++rb)
+                    compute_q4_0(ar, wr[rb], acc[rb][0], acc[rb][1]);
             }
             // this stage's activations were scaled by 2^s per verify row
-            tot[0] = fmaf(inv.x, acc0[0] + acc1[0], tot[0]);
-            tot[1] = fmaf(inv.y, acc0[1] + acc1[1], tot[1]);
-            tot[2] = fmaf(inv.x, acc0[2] + acc1[2], tot[2]);
-            tot[3] = fmaf(inv.y, acc0[3] + acc1[3], tot[3]);
+#pragma unroll
+            for (int rb = 0; rb < kRowBlocks; ++rb) {
+                tot[rb][0] = fmaf(ar.inv.x, acc[rb][0][0] + acc[rb][1][0], tot[rb][0]);
+                tot[rb][1] = fmaf(ar.inv.y, acc[rb][0][1] + acc[rb][1][1], tot[rb][1]);
+                tot[rb][2] = fmaf(ar.inv.x, acc[rb][0][2] + acc[rb][1][2], tot[rb][2]);
+                tot[rb][3] = fmaf(ar.inv.y, acc[rb][0][3] + acc[rb][1][3], tot[rb][3]);
+            }
         }
         u += static_cast<unsigned long long>(st_end - st0);
 
         // ------------------------------------------------------ epilogue
+        // Lane (g, c) holds, per row block rb, rows r = wrow + 16rb + g (+8
+        // for q & 2) and verify rows 2c + (q & 1).
         const int sg = static_cast<int>(tg / n_tiles), tile = static_cast<int>(tg % n_tiles);
         const int count = p.dense_M > 0 ? p.dense_M : p.seg->count[sg];
-        const float v[4] = {tot[0] * p.tensor_scale, tot[1] * p.tensor_scale,
-                            tot[2] * p.tensor_scale, tot[3] * p.tensor_scale};
+        float v[kRowBlocks][4];
+#pragma unroll
+        for (int rb = 0; rb < kRowBlocks; ++rb)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) v[rb][q] = tot[rb][q] * p.tensor_scale;
         const int n0 = tile * kTileRows;
         const bool whole = (st0 == 0 && st_end == T);
         if (whole) {
+            unsigned long long k0 = 0ull, k1 = 0ull;  // argmax keys of tokens 2c, 2c+1
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int tok = 2 * c + (q & 1);
-                const int n = n0 + warp * 16 + g + ((q & 2) ? 8 : 0);
-                if (tok < count && n < p.N) {
-                    const int dest = p.dense_M > 0 ? tok : p.seg->dest[sg][tok];
-                    p.out[static_cast<size_t>(dest) * p.ldo + n] = v[q];
-                }
-            }
-            if (p.argmax_M > 0) {
-                unsigned long long k0 = 0ull, k1 = 0ull;  // tokens 2c, 2c+1
+            for (int rb = 0; rb < kRowBlocks; ++rb) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const int n = n0 + warp * 16 + g + ((q & 2) ? 8 : 0);
+                    const int tok = 2 * c + (q & 1);
+                    const int n = n0 + wrow + rb * 16 + g + ((q & 2) ? 8 : 0);
                     if (n < p.N) {
-                        const unsigned long long k = am_key(v[q], static_cast<uint32_t>(n));
+                        if (tok < count) {
+                            const int dest = p.dense_M > 0 ? tok : p.seg->dest[sg][tok];
+                            p.out[static_cast<size_t>(dest) * p.ldo + n] = v[rb][q];
+                        }
+                        const unsigned long long k = am_key(v[rb][q], static_cast<uint32_t>(n));
                         if (q & 1) k1 = umax64(k1, k);
                         else k0 = umax64(k0, k);
                     }
                 }
+            }
+            if (p.argmax_M > 0) {
 #pragma unroll
                 for (int o = 4; o < 32; o <<= 1) {
                     k0 = umax64(k0, __shfl_xor_sync(0xffffffffu, k0, o));
@@ -721,7 +778,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             }
             continue;
         }
-        // Partial tile: publish this warp's 16-row slice; the last of the
+        // Partial tile: publish this warp's 32-row slice; the last of the
         // tile's contributors to arrive for this slice sums it in k order.
         const unsigned long long tile_u0 = tg * static_cast<unsigned long long>(T);
         const unsigned long long i_lo = R.owner(tile_u0), i_hi = R.owner(tile_u0 + T - 1);
@@ -730,11 +787,13 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             2ull * blockIdx.x + ((my_first_tile == tg) ? 0ull : 1ull);
         float* part = p.partials + my_slot * kPartialFloats;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int tok = 2 * c + (q & 1);
-            const int r = warp * 16 + g + ((q & 2) ? 8 : 0);
-            __stcg(&part[tok * kTileRows + r], v[q]);
-        }
+        for (int rb = 0; rb < kRowBlocks; ++rb)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int tok = 2 * c + (q & 1);
+                const int r = wrow + rb * 16 + g + ((q & 2) ? 8 : 0);
+                __stcg(&part[tok * kTileRows + r], v[rb][q]);
+            }
         __threadfence();
         __syncwarp();
         uint32_t old = 0;
@@ -746,39 +805,37 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         // slot is its "first tile" slot; only the first may end in it instead.
         const unsigned long long slot_lo =
             2ull * i_lo + ((R.start(i_lo) / T == tg) ? 0ull : 1ull);
+        // lane: verify row tok, rows rr .. rr+3 and rr+16 .. rr+19 of the slice
         const int tok = lane >> 2;
-        const int rr = warp * 16 + 4 * (lane & 3);
+        const int rr = wrow + 4 * (lane & 3);
         const size_t off = static_cast<size_t>(tok) * kTileRows + rr;
         auto slot_of = [&](unsigned long long i) { return i == i_lo ? slot_lo : 2ull * i; };
-        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+        auto ld4 = [&](unsigned long long i, int h) {
+            return __ldcg(reinterpret_cast<const float4*>(p.partials + slot_of(i) * kPartialFloats +
+                                                          off + 16 * h));
+        };
+        float4 sa = make_float4(0.f, 0.f, 0.f, 0.f), sb = sa;
         unsigned long long i = i_lo;
-        for (; i + 3 <= i_hi; i += 4) {  // four loads in flight, summed in order
-            const float4 x0 = __ldcg(reinterpret_cast<const float4*>(
-                p.partials + slot_of(i) * kPartialFloats + off));
-            const float4 x1 = __ldcg(reinterpret_cast<const float4*>(
-                p.partials + slot_of(i + 1) * kPartialFloats + off));
-            const float4 x2 = __ldcg(reinterpret_cast<const float4*>(
-                p.partials + slot_of(i + 2) * kPartialFloats + off));
-            const float4 x3 = __ldcg(reinterpret_cast<const float4*>(
-                p.partials + slot_of(i + 3) * kPartialFloats + off));
-            sum.x += x0.x; sum.y += x0.y; sum.z += x0.z; sum.w += x0.w;
-            sum.x += x1.x; sum.y += x1.y; sum.z += x1.z; sum.w += x1.w;
-            sum.x += x2.x; sum.y += x2.y; sum.z += x2.z; sum.w += x2.w;
-            sum.x += x3.x; sum.y += x3.y; sum.z += x3.z; sum.w += x3.w;
+        for (; i + 1 <= i_hi; i += 2) {  // four loads in flight, summed in order
+            const float4 a0 = ld4(i, 0), b0 = ld4(i, 1), a1 = ld4(i + 1, 0), b1 = ld4(i + 1, 1);
+            sa.x += a0.x; sa.y += a0.y; sa.z += a0.z; sa.w += a0.w;
+            sb.x += b0.x; sb.y += b0.y; sb.z += b0.z; sb.w += b0.w;
+            sa.x += a1.x; sa.y += a1.y; sa.z += a1.z; sa.w += a1.w;
+            sb.x += b1.x; sb.y += b1.y; sb.z += b1.z; sb.w += b1.w;
         }
-        for (; i <= i_hi; ++i) {
-            const float4 x0 = __ldcg(reinterpret_cast<const float4*>(
-                p.partials + slot_of(i) * kPartialFloats + off));
-            sum.x += x0.x; sum.y += x0.y; sum.z += x0.z; sum.w += x0.w;
+        if (i <= i_hi) {
+            const float4 a0 = ld4(i, 0), b0 = ld4(i, 1);
+            sa.x += a0.x; sa.y += a0.y; sa.z += a0.z; sa.w += a0.w;
+            sb.x += b0.x; sb.y += b0.y; sb.z += b0.z; sb.w += b0.w;
         }
-        const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
+        const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
         unsigned long long kb = 0ull;
         if (tok < count) {
             const int dest = p.dense_M > 0 ? tok : p.seg->dest[sg][tok];
             float* orow = p.out + static_cast<size_t>(dest) * p.ldo;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int n = n0 + rr + j;
+            for (int j = 0; j < 8; ++j) {
+                const int n = n0 + rr + (j & 3) + ((j & 4) ? 16 : 0);
                 if (n < p.N) {
                     orow[n] = sv[j];
                     kb = umax64(kb, am_key(sv[j], static_cast<uint32_t>(n)));

@@ -14,8 +14,11 @@ constexpr int kMaxSeg = 64;        // routed (token, expert) pairs per call
 constexpr int kTileRows = 128;     // weight rows per tile
 constexpr int kStageK = 256;       // k elements per pipeline stage
 constexpr int kStages = 4;         // pipeline depth
-constexpr int kConsumerWarps = 8;  // each owns 16 rows of the tile
+constexpr int kConsumerWarps = 4;  // each owns 32 rows of the tile
+constexpr int kWarpRows = kTileRows / kConsumerWarps;  // 32
+constexpr int kRowBlocks = kWarpRows / 16;             // 16-row MMA blocks per warp
 constexpr int kGemmThreads = (kConsumerWarps + 1) * 32;
+static_assert(kRowBlocks == 2, "the split-tile finish assumes two row blocks per warp");
 constexpr int kWBytes = kTileRows * (kStageK / 2);     // 16384: packed nibbles
 constexpr int kABytes = kMaxRows * kStageK * 2;        // 4096: fp16 activations
 constexpr int kAStride = kABytes + kMaxRows * 4;       // + the 8 rows' 2^-s: 4128
@@ -25,6 +28,7 @@ constexpr int kAStride = kABytes + kMaxRows * 4;       // + the 8 rows' 2^-s: 41
 // Every box lies inside the row: the last one of a row is moved back to end
 // at the row's end.
 constexpr int kScaleGroup = 4;
+static_assert((kScaleGroup & (kScaleGroup - 1)) == 0, "scale group must be a power of two");
 constexpr int kSBoxBytes = 16 * kScaleGroup;           // 64 (slot row pitch)
 constexpr int kSSlotBytes = kTileRows * kSBoxBytes;    // 8192
 constexpr int kSSlots = 2;
