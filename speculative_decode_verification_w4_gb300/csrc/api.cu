@@ -224,6 +224,19 @@ VW4_API vw4_status verify_gemm_w4(const vw4_weight* W, const void* A_dev, int M,
     const long long U = static_cast<long long>(n_tiles) * T;
     long long G = static_cast<long long>(d->sms) * d->occ[W->fmt];
     if (G > kMaxGrid) G = kMaxGrid;
+    // When every tile fits in one wave, split each tile's stages into S
+    // nearly equal parts, one CTA each (no CTA spans two tiles, and a part has
+    // at least kMinUnitsPerCta stages so that few partials are combined).
+    // Otherwise stream-K over all units balances the work exactly.
+    int split = 0;
+    if (n_tiles <= G) {
+        long long S = G / n_tiles;
+        long long S_cap = T / kMinUnitsPerCta;
+        if (S_cap < 1) S_cap = 1;
+        if (S > S_cap) S = S_cap;
+        split = static_cast<int>(S);
+        G = n_tiles * S;
+    }
     if (G > U) G = U;
 
     cudaError_t e = launch_prep_act(static_cast<const uint16_t*>(A_dev), lda, K, W->fmt, M, 0, 1,
@@ -235,6 +248,7 @@ VW4_API vw4_status verify_gemm_w4(const vw4_weight* W, const void* A_dev, int M,
     p.T = T;
     p.n_tiles = n_tiles;
     p.sgroup = sgroup;
+    p.split = split;
     p.tensor_scale = W->tensor_scale;
     p.seg = ws.seg;
     p.act = ws.act;

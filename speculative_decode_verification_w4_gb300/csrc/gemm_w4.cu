@@ -117,9 +117,12 @@ __global__ void __launch_bounds__(256) prep_act_kernel(
     const uint16_t* __restrict__ A, int lda, int vec_ok, int K, int fmt, int dense_M,
     int rows_are_pairs, int topk, SegTable* seg, uint8_t* act, uint32_t* tile_cnt, int n_cnt,
     unsigned long long* am_key, uint32_t* am_cnt) {
-    // the GEMM may start streaming weights now; it waits for this grid before
-    // touching the activations or the tickets
+    // The GEMM may start streaming weights now; it waits for this grid before
+    // touching the activations or the tickets.  This grid itself may have
+    // been launched while its predecessor (the previous GEMM, or the router)
+    // still runs: nothing is read or written before that grid has finished.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int T = K / kStageK;
     const int sgi = blockIdx.x / T, st = blockIdx.x % T;
     const int r = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -463,18 +466,42 @@ __device__ __forceinline__ unsigned long long am_key(float v, uint32_t idx) {
     return (static_cast<unsigned long long>(ord) << 32) | (0xFFFFFFFFu - idx);
 }
 
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(p), "r"(v)
+                 : "memory");
+    return old;
+}
+
+constexpr int kFinishBatch = 8;
+
 __device__ __forceinline__ unsigned long long umax64(unsigned long long a,
                                                      unsigned long long b) {
     return a > b ? a : b;
 }
 
+// The unit range of each CTA.  Stream-K (S == 0): CTA i owns units
+// [iU/G, (i+1)U/G) of the (tile, stage) order, whatever the tile boundaries.
+// Tile-aligned split-K (S > 0, G = tiles * S): CTA tS + p owns stages
+// [pT/S, (p+1)T/S) of tile t, so no CTA spans two tiles.
 struct Range {
     unsigned long long U, G;
+    int T, S;
     __device__ __forceinline__ unsigned long long start(unsigned long long i) const {
+        if (S > 0) {
+            const unsigned long long t = i / S, q = i % S;
+            return t * T + q * T / S;
+        }
         return i * U / G;
     }
     // the CTA whose range holds unit u
     __device__ __forceinline__ unsigned long long owner(unsigned long long u) const {
+        if (S > 0) {
+            const unsigned long long t = u / T, st = u % T;
+            return t * S + ((st + 1) * S - 1) / T;
+        }
         return ((u + 1) * G + U - 1) / U - 1;
     }
 };
@@ -508,6 +535,9 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // The next call's kernels may become resident now: they touch nothing
+    // this grid uses before it has finished, and prefetch only weights.
+    grid_dependents_launch();
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
@@ -531,7 +561,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     const unsigned long long U = static_cast<unsigned long long>(n_seg) * n_tiles * T;
     const unsigned long long G = U < gridDim.x ? U : gridDim.x;
     if (blockIdx.x >= G) return;
-    const Range R{U, G};
+    const Range R{U, G, T, p.split};
     const unsigned long long u_begin = R.start(blockIdx.x), u_end = R.start(blockIdx.x + 1);
 
     if (warp == kConsumerWarps) {
@@ -768,10 +798,9 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                     if (2 * c < p.argmax_M && k0) atomicMax(&p.am_key[2 * c], k0);
                     if (2 * c + 1 < p.argmax_M && k1) atomicMax(&p.am_key[2 * c + 1], k1);
                 }
-                __threadfence();
                 __syncwarp();
                 uint32_t old = 0;
-                if (lane == 0) old = atomicAdd(p.am_cnt, 1u);
+                if (lane == 0) old = atom_add_acq_rel_gpu(p.am_cnt, 1u);
                 old = __shfl_sync(0xffffffffu, old, 0);
                 if (old + 1 == static_cast<uint32_t>(kConsumerWarps * n_tiles))
                     argmax_finish(p, lane);
@@ -794,13 +823,13 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                 const int r = wrow + rb * 16 + g + ((q & 2) ? 8 : 0);
                 __stcg(&part[tok * kTileRows + r], v[rb][q]);
             }
-        __threadfence();
+        // The warp barrier orders every lane's partial stores before lane 0's
+        // release; the last arriver's acquire orders the reads after them.
         __syncwarp();
         uint32_t old = 0;
-        if (lane == 0) old = atomicAdd(&p.tile_cnt[tg * kConsumerWarps + warp], 1u);
+        if (lane == 0) old = atom_add_acq_rel_gpu(&p.tile_cnt[tg * kConsumerWarps + warp], 1u);
         old = __shfl_sync(0xffffffffu, old, 0);
         if (old + 1 != n_contrib) continue;
-        __threadfence();
         // Every contributor after the first starts inside this tile, so its
         // slot is its "first tile" slot; only the first may end in it instead.
         const unsigned long long slot_lo =
@@ -815,18 +844,22 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                                                           off + 16 * h));
         };
         float4 sa = make_float4(0.f, 0.f, 0.f, 0.f), sb = sa;
-        unsigned long long i = i_lo;
-        for (; i + 1 <= i_hi; i += 2) {  // four loads in flight, summed in order
-            const float4 a0 = ld4(i, 0), b0 = ld4(i, 1), a1 = ld4(i + 1, 0), b1 = ld4(i + 1, 1);
-            sa.x += a0.x; sa.y += a0.y; sa.z += a0.z; sa.w += a0.w;
-            sb.x += b0.x; sb.y += b0.y; sb.z += b0.z; sb.w += b0.w;
-            sa.x += a1.x; sa.y += a1.y; sa.z += a1.z; sa.w += a1.w;
-            sb.x += b1.x; sb.y += b1.y; sb.z += b1.z; sb.w += b1.w;
-        }
-        if (i <= i_hi) {
-            const float4 a0 = ld4(i, 0), b0 = ld4(i, 1);
-            sa.x += a0.x; sa.y += a0.y; sa.z += a0.z; sa.w += a0.w;
-            sb.x += b0.x; sb.y += b0.y; sb.z += b0.z; sb.w += b0.w;
+        // up to kFinishBatch contributors' loads in flight, then summed in order
+        for (unsigned long long i0 = i_lo; i0 <= i_hi; i0 += kFinishBatch) {
+            float4 xa[kFinishBatch], xb[kFinishBatch];
+#pragma unroll
+            for (int j = 0; j < kFinishBatch; ++j) {  // past the end: reload the last
+                const unsigned long long ij = i0 + j <= i_hi ? i0 + j : i_hi;
+                xa[j] = ld4(ij, 0);
+                xb[j] = ld4(ij, 1);
+            }
+#pragma unroll
+            for (int j = 0; j < kFinishBatch; ++j) {
+                if (i0 + j <= i_hi) {
+                    sa.x += xa[j].x; sa.y += xa[j].y; sa.z += xa[j].z; sa.w += xa[j].w;
+                    sb.x += xb[j].x; sb.y += xb[j].y; sb.z += xb[j].z; sb.w += xb[j].w;
+                }
+            }
         }
         const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
         unsigned long long kb = 0ull;
@@ -846,10 +879,9 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             kb = umax64(kb, __shfl_xor_sync(0xffffffffu, kb, 1));
             kb = umax64(kb, __shfl_xor_sync(0xffffffffu, kb, 2));
             if ((lane & 3) == 0 && tok < p.argmax_M && kb) atomicMax(&p.am_key[tok], kb);
-            __threadfence();
             __syncwarp();
             uint32_t o2 = 0;
-            if (lane == 0) o2 = atomicAdd(p.am_cnt, 1u);
+            if (lane == 0) o2 = atom_add_acq_rel_gpu(p.am_cnt, 1u);
             o2 = __shfl_sync(0xffffffffu, o2, 0);
             if (o2 + 1 == static_cast<uint32_t>(kConsumerWarps * n_tiles)) argmax_finish(p, lane);
         }
@@ -893,10 +925,20 @@ cudaError_t launch_prep_act(const uint16_t* A, int lda, int K, int fmt, int dens
                             int n_counters, cudaStream_t s) {
     const int T = K / kStageK;
     const int vec_ok = ((reinterpret_cast<uintptr_t>(A) & 15u) == 0 && lda % 8 == 0) ? 1 : 0;
-    prep_act_kernel<<<n_seg_grid * T, 256, 0, s>>>(A, lda, vec_ok, K, fmt, dense_M,
-                                                   rows_are_pairs, topk, ws.seg, ws.act,
-                                                   ws.tile_cnt, n_counters, ws.am_key, ws.am_cnt);
-    return cudaGetLastError();
+    // a programmatic dependent of whatever kernel precedes it on the stream
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(n_seg_grid * T);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prep_act_kernel, A, lda, vec_ok, K, fmt, dense_M,
+                              rows_are_pairs, topk, ws.seg, ws.act, ws.tile_cnt, n_counters,
+                              ws.am_key, ws.am_cnt);
 }
 
 template <int FMT>

@@ -14,6 +14,7 @@ constexpr int kMaxSeg = 64;        // routed (token, expert) pairs per call
 constexpr int kTileRows = 128;     // weight rows per tile
 constexpr int kStageK = 256;       // k elements per pipeline stage
 constexpr int kStages = 4;         // pipeline depth
+constexpr int kMinUnitsPerCta = 4; // tile-aligned split-K: at least this many stages per part
 constexpr int kConsumerWarps = 4;  // each owns 32 rows of the tile
 constexpr int kWarpRows = kTileRows / kConsumerWarps;  // 32
 constexpr int kRowBlocks = kWarpRows / 16;             // 16-row MMA blocks per warp
@@ -65,6 +66,7 @@ struct GemmWorkspace {
 struct GemmParams {
     int N, K, T, n_tiles;
     int sgroup;                   // stages per scale box, min(kScaleGroup, T)
+    int split;                    // > 0: tile-aligned split-K into this many parts; 0: stream-K
     float tensor_scale;
     const SegTable* seg;
     const uint8_t* act;
