@@ -53,6 +53,34 @@ def step_bytes(M, fmt="nvfp4"):
     return sum(weight_bytes(N, K, fmt) + M * K * 2 for _, N, K in LAYER)
 
 
+KERNEL_SOURCES = ["speculative_decode_verification_w4_gb300/csrc/" + f
+                  for f in ("gemm_w4.cu", "vw4_internal.cuh", "ptx.cuh", "api.cu")]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_w4_dense_layer_m8_traffic.json")
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic():
+    """DRAM bytes (read + write) of the GEMM kernel per layer step (its 7
+    launches), from the committed ncu summary -- null when the kernel sources
+    changed since those counters were taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_step")
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -263,7 +291,8 @@ def run_ours(args, rank, world, device):
     achieved = sum(weight_bytes(N, K) + HEAD_M * K * 2 for _, N, K in LAYER) / (
         sum(t_lin[n] for n, _, _ in LAYER) * 1e-6) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": None,
+                "frac": round(achieved / peak, 4), "traffic": measured_traffic(),
+                "per": "layer step: the 7 GEMM calls at M = 8 (bytes, time, traffic)",
                 "peak_kind": f"of {peak_kind} (STREAM-style copy, burst)",
                 "kernel": "vw4::gemm_w4_kernel<nvfp4> (with its activation-prep launch)",
                 "per_unit": "0.5625 B per weight (nibble + e4m3/16) + 2*M B per k of activations"}
@@ -408,9 +437,24 @@ class OracleWorkload:
         return nbytes / secs / 1e9, rows, secs
 
     def frac_for(self, budget_s: float) -> float:
-        """Sample fraction whose oracle time is about budget_s (one calibration run)."""
+        """Sample fraction whose oracle time is about budget_s (one calibration
+        run); above 1.0 the whole layer is run that many times."""
         _, _, secs = self.run(0.01, 1)
-        return min(1.0, 0.01 * budget_s / max(secs, 1e-6))
+        return 0.01 * budget_s / max(secs, 1e-6)
+
+    def run_budget(self, frac: float, seed: int):
+        """run() over a fraction of the rows, or the whole layer repeated when
+        frac > 1; returns (GB/s, rows, seconds)."""
+        if frac <= 1.0:
+            return self.run(frac, seed)
+        reps = max(1, int(round(frac)))
+        tot_rows, tot_s, gbs = 0, 0.0, []
+        for r in range(reps):
+            v, rows, secs = self.run(1.0, seed + r)
+            gbs.append(v)
+            tot_rows += rows
+            tot_s += secs
+        return len(gbs) / sum(1.0 / v for v in gbs), tot_rows, tot_s
 
 
 def cpu_cores():
@@ -439,16 +483,17 @@ def run_reference(args, rank, world):
     per_step_budget = max(0.5, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
     frac = wl.frac_for(per_step_budget)
     for k in range(args.warmup):
-        wl.run(frac, 1000 + k)
+        wl.run_budget(frac, 1000 + k)
     vals, rows = [], 0
     t0 = time.perf_counter()
     for k in range(args.steps):
-        v, rows, _ = wl.run(frac, 2000 + k)
+        v, rows, _ = wl.run_budget(frac, 2000 + k)
         vals.append(v)
     wall = time.perf_counter() - t0
     value = statistics.mean(vals)
-    sample = (f"each step: a {frac:.4%} random subset of the output rows of all 7 linears "
-              f"({rows} rows), M=8, nvfp4; fp64 dequantize-and-dot")
+    what = (f"a {frac:.4%} random subset of the output rows of all 7 linears" if frac <= 1.0
+            else f"all 7 linears, {int(round(frac))} times")
+    sample = f"each step: {what} ({rows} rows), M=8, nvfp4; fp64 dequantize-and-dot"
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -462,6 +507,36 @@ def run_reference(args, rank, world):
     }
 
 
+def run_case(case: str, device):
+    """Profiling helper: a few calls of the GEMM on a fixed case, nothing timed
+    or printed but a one-line summary.  'dense' = the 7 nvfp4 linears of the
+    layer at M = 8 (3 warm-up passes, then 1); 'N,K,M' = one nvfp4 GEMM of that
+    shape (3 warm-up calls, then 1)."""
+    import torch
+    import speculative_decode_verification_w4_gb300 as vw4
+    torch.cuda.set_device(device)
+    ws = vw4.Workspace(device)
+    if case == "dense":
+        layer = make_layer("nvfp4", device)
+        acts = make_acts(HEAD_M, device, seed=7 + HEAD_M)
+        jobs = [(qd, sd, ts, acts[j], N) for j, (name, N, K, qd, sd, ts) in enumerate(layer)]
+    else:
+        import synth
+        N, K, M = (int(x) for x in case.split(","))
+        q, sc, ts = synth.linear(1, N, K, "nvfp4")
+        bits = synth.activations(synth.rng(2), M, K)
+        A = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(device)
+        jobs = [(torch.from_numpy(q).to(device), torch.from_numpy(sc).to(device), ts, A, N)]
+    outs = [torch.empty((a.shape[0], N), dtype=torch.float32, device=device)
+            for (_, _, _, a, N) in jobs]
+    for _ in range(4):
+        for (qd, sd, ts, a, N), o in zip(jobs, outs):
+            vw4.verify_gemm_w4(vw4.FMT_NVFP4, qd, sd, ts, a, out=o, workspace=ws)
+    torch.cuda.synchronize()
+    print(f"case {case}: {len(jobs)} GEMM(s) x 4 calls, device status "
+          f"{vw4.vw4_get_device_status()}", flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -469,6 +544,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--case", default=None,
+                    help="profiling helper: 'dense' or 'N,K,M' (see run_case); no JSON line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -489,15 +566,20 @@ def main():
     device = torch.device("cuda", local)
     import __graft_entry__
     __graft_entry__.build()
+    if args.case:
+        run_case(args.case, device)
+        return
     res = run_ours(args, rank, world, device)
     if rank == 0:
         wl = OracleWorkload()
         frac = wl.frac_for(args.cpu_budget)
-        v, rows, secs = wl.run(frac, 7)
+        v, rows, secs = wl.run_budget(frac, 7)
+        what = (f"{frac:.4%} of the output rows of all 7 linears" if frac <= 1.0
+                else f"all 7 linears, {int(round(frac))} times")
         res["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cpu_cores(),
                                "kind": "oracle",
-                               "sample": f"{frac:.4%} of the output rows of all 7 linears "
-                                         f"({rows} rows, {secs:.1f} s), M=8, nvfp4"}
+                               "sample": f"{what} ({rows} rows, {secs:.1f} s), M=8, nvfp4, "
+                                         f"fp64 dequantize-and-dot"}
         print(json.dumps(res), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
