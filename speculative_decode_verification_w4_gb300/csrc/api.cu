@@ -388,10 +388,11 @@ VW4_API vw4_status accept_rejection(const float* target_logits_dev, const float*
     if (st != VW4_OK) return st;
     const float invT = static_cast<float>(1.0 / static_cast<double>(T));
     const double pd = static_cast<double>(params->top_p) * 4294967296.0;
-    const uint64_t P = pd >= 4294967296.0 ? (1ull << 32) : static_cast<uint64_t>(std::llround(pd));
+    uint64_t P = pd >= 4294967296.0 ? (1ull << 32) : static_cast<uint64_t>(std::llround(pd));
+    if (P == 0) P = 1;  // keeps the top entry alone, exactly as P = 0 does
     cudaError_t e = launch_accept_rejection(target_logits_dev, draft_logits_dev, drafts_dev, B, Kd,
                                             V, invT, P, seed, offset, tokens_dev, len_dev,
-                                            workspace_dev, ws_bytes, d->status,
+                                            workspace_dev, ws_bytes, d->status, g_wait_ns,
                                             static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return VW4_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return cuda_fail(e, "accept_rejection launch");

@@ -17,22 +17,27 @@
 //   residual  r_v = max(0, p_v * Sq - q_v * Sp), inverse CDF with a 64-bit
 //   uniform; bonus from p_Kd when every draft is accepted.
 //
-// Kernel 1, one thread-block cluster per (sequence b, position i):
-//   * the target row (b, i) and, for i < Kd, the draft row (b, i) are loaded
-//     once into the cluster's shared memory, a slice per CTA;
-//   * per row: max and sum W over the cluster (DSMEM), a log-scale histogram
-//     of W finds the bucket where the top-p prefix ends; its members are
-//     gathered to rank 0, sorted by (W desc, index asc) and scanned, which
-//     gives the exact cut (an exact radix search over the slices is the
-//     fallback when that bucket is too crowded);
-//   * the acceptance test of draft i (Philox block (i, b)), and, only if it
-//     is rejected, the residual draw -- or, for i = Kd, the bonus draw --
-//     from the rows already on chip: an exact u128 total, then an ordered
-//     search across the cluster's slices.
-// Kernel 2, one thread per sequence: the first rejected position decides the
-// committed run.  Rows after the first rejection are evaluated in parallel
-// and discarded.
+// Kernel 1 (row_kernel), one thread-block cluster per logits row -- every
+// target row (b, i <= Kd) and every draft row (b, i < Kd) independently:
+//   * the row is read once from HBM into the cluster's shared memory, a
+//     slice per CTA; max and sum W over the cluster (DSMEM);
+//   * the top-p cut: a log-scale histogram of the mass of the entries at or
+//     above c = floor((2^32 - P) * S / (V * 2^32)) -- every entry below c lies
+//     in the dropped tail, because all of them together weigh less than
+//     (1 - P/2^32) * S -- finds the bucket where the kept prefix ends; its
+//     members are sorted by (W desc, index asc) and scanned, which gives the
+//     exact cut (an exact radix search over the slices is the fallback when
+//     that bucket is too crowded);
+//   * (max, tau, cut, kept sum) of the row go to the workspace.
+// Kernel 2 (seq_kernel), one CTA per sequence: the acceptance tests in
+// order (Philox block (i, b)), then one ordered draw over the row it needs --
+// the residual at the first rejection, or the bonus from p_Kd -- and the
+// committed run.  The draw skips, with two flops, every entry whose logit is
+// too small to be kept (a bound below the cut with a 1e-3 margin in the
+// exponent), so it streams the row once at memory speed.
 #include <cooperative_groups.h>
+
+#include <cmath>
 
 #include "ptx.cuh"
 #include "vw4_internal.cuh"
@@ -44,15 +49,21 @@ namespace vw4 {
 namespace {
 
 constexpr uint32_t kStatusBadDraft = 0x1u;
+constexpr uint32_t kStatusTimeout = 0x4u;
 constexpr uint32_t kStatusZeroResidual = 0x8u;
-constexpr int kThreads = 1024;
+constexpr int kThreads = 512;  // both kernels
 constexpr int kWarps = kThreads / 32;
 constexpr int kLogBuckets = 16 + 37 * 8;  // exact 0..15, then 8 per binade up to 2^40
 constexpr int kLinBuckets = 256;
-constexpr int kCandLocal = 512;   // candidates one CTA may hold per row
-constexpr int kCandTotal = 2048;  // candidates the cluster may gather per row
-constexpr int kMaxSlice = 20480;  // floats per CTA per row (two rows on chip)
+constexpr int kCandLocal = 512;    // candidates one CTA may hold per row
+constexpr int kCandTotal = 1024;   // candidates the cluster may gather per row
+constexpr int kRankSortMax = 128;  // up to this many: sort by counting ranks
+constexpr int kListCap = 4096;     // entries >= c0 one CTA lists; more: scan the slice
+constexpr int kExpBatch = 8;       // entries per thread per step of the exp pass
+constexpr int kMaxSlice = 20480;   // floats per CTA (one row on chip)
 constexpr unsigned long long kKeepAll = 1ull << 32;
+static_assert(kThreads >= kLogBuckets, "one thread per log bucket in the suffix scan");
+static_assert(kThreads >= kLinBuckets, "one thread per radix bucket");
 
 typedef unsigned __int128 u128;
 
@@ -61,11 +72,6 @@ struct RowInfo {
     int cut;                 // largest kept index among W == tau
     unsigned long long tau;  // kept: W > tau, or W == tau and v <= cut
     unsigned long long S;    // kept sum
-};
-
-struct PairOut {
-    int accept;  // 1: draft i accepted (or the bonus row)
-    int token;   // residual draw at a rejection; bonus draw for i == Kd
 };
 
 // ------------------------------------------------------------- own exp
@@ -85,7 +91,9 @@ __device__ __forceinline__ float own_exp(float x) {
     p = __fmaf_rn(p, r, 0.5f);
     p = __fmaf_rn(p, r, 1.0f);
     p = __fmaf_rn(p, r, 1.0f);
-    const int ni = static_cast<int>(n);
+    // n is an integer in [-47, 1]: adding 1.5 * 2^23 puts it in the low
+    // mantissa bits (exact), which avoids a float-to-int conversion
+    const int ni = __float_as_int(__fadd_rn(n, 12582912.0f)) - 0x4B400000;
     return __fmul_rn(p, __uint_as_float(static_cast<uint32_t>(ni + 127) << 23));
 }
 
@@ -93,8 +101,26 @@ __device__ __forceinline__ float scaled_x(float l, float mx, float invT) {
     return __fmul_rn(__fsub_rn(l, mx), invT);
 }
 
+// floor(e * 2^40) for 0 <= e <= 1 with 32-bit float operations only: f =
+// e * 2^40 is exact; fh = floor(f / 2^20) < 2^21 and d = f - fh * 2^20 in
+// [0, 2^20) are exact in fp32 (d is a multiple of ulp(f)); each integer part
+// is read from the mantissa after adding 2^23.
+__device__ __forceinline__ void mass_parts(float e, uint32_t& hi, uint32_t& lo) {
+    const float f = __fmul_rn(e, 1099511627776.0f);
+    const float fh = floorf(__fmul_rn(e, 1048576.0f));  // = floor(f / 2^20)
+    const float dl = floorf(__fmaf_rn(-fh, 1048576.0f, f));
+    hi = __float_as_uint(__fadd_rn(fh, 8388608.0f)) - 0x4B000000u;
+    lo = __float_as_uint(__fadd_rn(dl, 8388608.0f)) - 0x4B000000u;
+}
+
 __device__ __forceinline__ unsigned long long mass_of(float e) {
-    return __float2ull_rz(__fmul_rn(e, 1099511627776.0f));  // e * 2^40 is exact
+    const float f = __fmul_rn(e, 1099511627776.0f);
+    const float fh = floorf(__fmul_rn(f, 9.5367431640625e-07f));
+    const float d = __fmaf_rn(-fh, 1048576.0f, f);
+    const float dl = floorf(d);
+    const uint32_t hi = __float_as_uint(__fadd_rn(fh, 8388608.0f)) - 0x4B000000u;
+    const uint32_t lo = __float_as_uint(__fadd_rn(dl, 8388608.0f)) - 0x4B000000u;
+    return (static_cast<unsigned long long>(hi) << 20) | lo;
 }
 
 __device__ __forceinline__ unsigned long long kept(unsigned long long W, int v, const RowInfo& s) {
@@ -106,6 +132,32 @@ __device__ __forceinline__ int log_bucket(unsigned long long W) {
     if (W < 16ull) return static_cast<int>(W);
     const int msb = 63 - __clzll(static_cast<long long>(W));
     return 16 + (msb - 4) * 8 + static_cast<int>((W >> (msb - 3)) & 7ull);
+}
+
+// log_bucket(floor(f)) for f = e * 2^40 >= 1, from the float's bits: every
+// bucket edge at or above 16 is an integer, so floor() never crosses one.
+__device__ __forceinline__ int log_bucket_e(float e) {
+    const float f = __fmul_rn(e, 1099511627776.0f);
+    if (f < 16.0f) return static_cast<int>(f);
+    const uint32_t bits = __float_as_uint(f);
+    const int msb = static_cast<int>((bits >> 23) & 0xFFu) - 127;
+    return 16 + (msb - 4) * 8 + static_cast<int>((bits >> 20) & 7u);
+}
+
+// The e range [lo, hi) of log bucket beta (exact: the edges have at most 4
+// significant bits, and the 2^-40 scaling is exact).
+__device__ __forceinline__ void bucket_e_range(int beta, float& lo, float& hi) {
+    unsigned long long a, b;
+    if (beta < 16) {
+        a = static_cast<unsigned long long>(beta);
+        b = a + 1ull;
+    } else {
+        const int msb = 4 + (beta - 16) / 8, j = (beta - 16) % 8;
+        a = static_cast<unsigned long long>(8 + j) << (msb - 3);
+        b = static_cast<unsigned long long>(9 + j) << (msb - 3);
+    }
+    lo = __fmul_rn(__ull2float_rn(a), 9.094947017729282379e-13f);  // * 2^-40
+    hi = __fmul_rn(__ull2float_rn(b), 9.094947017729282379e-13f);
 }
 
 // ------------------------------------------------------------- Philox
@@ -144,6 +196,12 @@ __device__ __forceinline__ u128 shfl_up_u128(u128 v, int o) {
     return (static_cast<u128>(hi) << 64) | lo;
 }
 
+__device__ __forceinline__ u128 warp_sum_u128(u128 v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += shfl_xor_u128(v, o);
+    return v;
+}
+
 // floor(u * R / 2^64) for a 64-bit u and a 128-bit R (< 2^120 here)
 __device__ __forceinline__ u128 scale_u64(unsigned long long u, u128 R) {
     const u128 lo = static_cast<u128>(u) * static_cast<unsigned long long>(R);
@@ -151,73 +209,39 @@ __device__ __forceinline__ u128 scale_u64(unsigned long long u, u128 R) {
     return (lo >> 64) + hi;
 }
 
-struct Smem {
-    unsigned int cnt[kLogBuckets];         // this CTA's histogram (read by peers)
-    unsigned long long mass[kLogBuckets];
-    unsigned int mcnt[kLogBuckets];        // the cluster's merged histogram
-    unsigned long long mmass[kLogBuckets];
-    unsigned long long cw[kCandLocal];     // this CTA's candidates (read by rank 0)
-    int ci[kCandLocal];
-    unsigned long long gw[kCandTotal];     // rank 0: gathered, sorted candidates
-    int gi[kCandTotal];
-    unsigned long long wred[kWarps];
-    unsigned long long wred2[kWarps];
-    float fred[kWarps];
-    // values peers read over DSMEM
-    float lmax;
-    unsigned long long lsum;
-    unsigned int ncand;
-    int overflow;
-    unsigned long long part_lo, part_hi;   // this CTA's u128 partial total
-    RowInfo info;                          // rank 0's result for the current row
-    int decision;
-    // broadcast inside the CTA
-    int beta, wbits;
-    unsigned long long lo, width, above, n_eq, count_eq;
-    int cut_found;
+// Scratch of the block-wide reductions.
+struct Red {
+    unsigned long long w[kWarps];
+    unsigned long long w2[kWarps];
+    float f[kWarps];
 };
 
-__device__ __forceinline__ float block_max(float v, Smem& sm) {
+__device__ __forceinline__ float block_max(float v, Red& sm) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    if (lane == 0) sm.fred[wid] = v;
+    if (lane == 0) sm.f[wid] = v;
     __syncthreads();
     float m = -INFINITY;
-    for (int w = 0; w < kWarps; ++w) m = fmaxf(m, sm.fred[w]);
+    for (int w = 0; w < kWarps; ++w) m = fmaxf(m, sm.f[w]);
     __syncthreads();
     return m;
 }
 
-__device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v, Smem& sm) {
+__device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v, Red& sm) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) sm.wred[wid] = v;
+    if (lane == 0) sm.w[wid] = v;
     __syncthreads();
     unsigned long long t = 0;
-    for (int w = 0; w < kWarps; ++w) t += sm.wred[w];
-    __syncthreads();
-    return t;
-}
-
-__device__ __forceinline__ u128 block_sum_u128(u128 v, Smem& sm) {
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += shfl_xor_u128(v, o);
-    if (lane == 0) {
-        sm.wred[wid] = static_cast<unsigned long long>(v);
-        sm.wred2[wid] = static_cast<unsigned long long>(v >> 64);
-    }
-    __syncthreads();
-    u128 t = 0;
-    for (int w = 0; w < kWarps; ++w) t += (static_cast<u128>(sm.wred2[w]) << 64) | sm.wred[w];
+    for (int w = 0; w < kWarps; ++w) t += sm.w[w];
     __syncthreads();
     return t;
 }
 
 // Exclusive prefix over the block of a u128 value per thread; also returns the total.
-__device__ __forceinline__ u128 block_excl_u128(u128 v, Smem& sm, u128& total) {
+__device__ __forceinline__ u128 block_excl_u128(u128 v, Red& sm, u128& total) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     u128 incl = v;
 #pragma unroll
@@ -226,13 +250,13 @@ __device__ __forceinline__ u128 block_excl_u128(u128 v, Smem& sm, u128& total) {
         if (lane >= o) incl += y;
     }
     if (lane == 31) {
-        sm.wred[wid] = static_cast<unsigned long long>(incl);
-        sm.wred2[wid] = static_cast<unsigned long long>(incl >> 64);
+        sm.w[wid] = static_cast<unsigned long long>(incl);
+        sm.w2[wid] = static_cast<unsigned long long>(incl >> 64);
     }
     __syncthreads();
     u128 base = 0, t = 0;
     for (int w = 0; w < kWarps; ++w) {
-        const u128 x = (static_cast<u128>(sm.wred2[w]) << 64) | sm.wred[w];
+        const u128 x = (static_cast<u128>(sm.w2[w]) << 64) | sm.w[w];
         if (w < wid) base += x;
         t += x;
     }
@@ -242,44 +266,174 @@ __device__ __forceinline__ u128 block_excl_u128(u128 v, Smem& sm, u128& total) {
 }
 
 // ----------------------------------------------------------- row statistics
+// Exact 64-bit add into shared memory with two native 32-bit atomics: the
+// low word's carry goes to the high word (the value reads back as one u64).
+__device__ __forceinline__ void atomic_add_u64_split(unsigned long long* a, unsigned long long v) {
+    uint32_t* w = reinterpret_cast<uint32_t*>(a);  // little endian: w[0] low, w[1] high
+    const uint32_t lo = static_cast<uint32_t>(v);
+    const uint32_t hi = static_cast<uint32_t>(v >> 32);
+    const uint32_t old = atomicAdd(&w[0], lo);
+    const uint32_t carry = (old + lo < old) ? 1u : 0u;
+    if (hi + carry) atomicAdd(&w[1], hi + carry);
+}
+
+// Adds, for every member lane (in), W to mass[bk] (and 1 to cnt[bk] unless
+// cnt is null).  Lanes of one bucket add their sum once: a row whose entries
+// share few buckets would otherwise serialise on a handful of addresses.
+// Called by all 32 lanes.
+__device__ __forceinline__ void warp_bucket_add(bool in, int bk, unsigned long long W, int lane,
+                                                unsigned int* cnt, unsigned long long* mass) {
+    const int key = in ? bk : -1 - lane;  // non-members: groups of one
+    const unsigned int peers = __match_any_sync(0xffffffffu, key);
+    unsigned int m = in ? peers : 0u;
+    unsigned long long sum = 0;
+    while (__any_sync(0xffffffffu, m != 0u)) {
+        const int src = m ? __ffs(m) - 1 : lane;
+        const unsigned long long x = __shfl_sync(0xffffffffu, W, src);
+        if (m) {
+            sum += x;
+            m &= m - 1u;
+        }
+    }
+    if (in && lane == __ffs(peers) - 1) {
+        atomic_add_u64_split(&mass[bk], sum);
+        if (cnt) atomicAdd(&cnt[bk], static_cast<unsigned int>(__popc(peers)));
+    }
+}
+
+struct RowSmem {
+    Red red;
+    unsigned int cnt[kLinBuckets];        // radix fallback: this CTA's counts (read by peers)
+    unsigned long long mass[kLogBuckets]; // this CTA's histogram (read by peers)
+    unsigned int mcnt[kLinBuckets];       // the cluster's merged histogram
+    unsigned long long mmass[kLogBuckets];
+    unsigned long long cw[kCandLocal];    // this CTA's candidates (read by rank 0)
+    int ci[kCandLocal];
+    union {
+        struct {
+            unsigned long long w[kCandTotal];  // rank 0: gathered, sorted candidates
+            int i[kCandTotal];
+        } g;
+        struct {
+            int k[kListCap];  // slice indices of this CTA's entries with W >= c0
+        } l;
+    } u;
+    unsigned int nlist;
+    // values peers read over DSMEM
+    float lmax;
+    unsigned long long lsum;
+    unsigned int ncand;
+    int overflow;
+    RowInfo info;  // rank 0's result
+    // broadcast inside the CTA
+    int beta, wbits;
+    unsigned long long lo, width, above, n_eq, count_eq;
+    int cut_found;
+};
+
 // s holds this CTA's slice [lo, lo + n) of the row's logits on entry and the
-// own_exp values on exit.  Every CTA of the cluster returns the same RowInfo.
+// own_exp values on exit.  The RowInfo returned by rank 0 is the row's; the
+// other CTAs may return before the cut is known.
 __device__ RowInfo row_stats(cg::cluster_group& cl, float* s, int n, int lo, int V, float invT,
-                             unsigned long long P, Smem& sm) {
+                             unsigned long long P, RowSmem& sm) {
     const int C = static_cast<int>(cl.num_blocks());
     const int rank = static_cast<int>(cl.block_rank());
     const int tid = threadIdx.x;
+    const int lane = tid & 31;
 
     // 1. max over the cluster
     float lmax = -INFINITY;
     for (int k = tid; k < n; k += kThreads) lmax = fmaxf(lmax, s[k]);
-    lmax = block_max(lmax, sm);
+    lmax = block_max(lmax, sm.red);
     if (tid == 0) sm.lmax = lmax;
-    for (int t = tid; t < kLogBuckets; t += kThreads) {
-        sm.cnt[t] = 0u;
-        sm.mass[t] = 0ull;
-    }
+    for (int t = tid; t < kLogBuckets; t += kThreads) sm.mass[t] = 0ull;
+    if (tid == 0) sm.nlist = 0u;
     cl.sync();
     float mx = -INFINITY;
     for (int r = 0; r < C; ++r) mx = fmaxf(mx, *cl.map_shared_rank(&sm.lmax, r));
 
-    // 2. e_v, the total mass and the log-scale histogram in one pass
-    unsigned long long lsum = 0;
-    for (int k = tid; k < n; k += kThreads) {
-        const float e = own_exp(scaled_x(s[k], mx, invT));
-        s[k] = e;
-        const unsigned long long W = mass_of(e);
-        lsum += W;
-        if (W != 0ull && P < kKeepAll) atomicAdd(&sm.mass[log_bucket(W)], W);
+    // 2. e_v, the total mass, and the log-scale mass histogram of the entries
+    //    at or above c0.  Together the entries below c <= (1 - P/2^32) S / V
+    //    weigh less than (1 - P/2^32) S, so they all lie in the dropped tail
+    //    and the cut is at or above c; c0 uses 2^40 (the top entry's mass,
+    //    a lower bound of S) in place of S, so c0 <= c and the histogram of
+    //    the entries >= c0 holds every bucket the cut can be in, exactly.
+    const bool want_hist = P < kKeepAll;
+    const unsigned long long c0 =
+        want_hist ? ((kKeepAll - P) << 8) / static_cast<unsigned long long>(V) : 0ull;
+    const unsigned long long cmin = c0 > 1ull ? c0 : 1ull;
+    // e < e_lo proves W < cmin with one compare (e_lo rounds cmin * 2^-40 down)
+    const float e_lo = want_hist ? __fmul_rn(__ull2float_rd(cmin), 9.094947017729282379e-13f)
+                                 : INFINITY;
+    // Batches of kExpBatch entries per thread: the own_exp chains of a batch
+    // are independent, and the warp reserves list slots once per batch.  The
+    // list takes every entry with e >= e_lo (a superset of W >= c0; the exact
+    // test is made on the listed entries).  sum W is kept per thread as the
+    // sums of the two exact 20-bit halves of each W (each fits in 32 bits).
+    uint32_t sum_hi = 0u, sum_lo = 0u;
+    for (int kb = tid - lane; kb < n; kb += kThreads * kExpBatch) {  // warp-uniform trip count
+        unsigned int ball[kExpBatch];
+        unsigned int tot = 0;
+#pragma unroll
+        for (int j = 0; j < kExpBatch; ++j) {
+            const int k = kb + j * kThreads + lane;
+            float e = 0.0f;
+            if (k < n) {
+                e = own_exp(scaled_x(s[k], mx, invT));
+                s[k] = e;
+            }
+            uint32_t hi, lo;
+            mass_parts(e, hi, lo);
+            sum_hi += hi;
+            sum_lo += lo;
+            ball[j] = __ballot_sync(0xffffffffu, e >= e_lo);
+            tot += __popc(ball[j]);
+        }
+        if (tot == 0u) continue;
+        unsigned int base = 0;
+        if (lane == 0) base = atomicAdd(&sm.nlist, tot);
+        base = __shfl_sync(0xffffffffu, base, 0);
+        const unsigned int below = (1u << lane) - 1u;
+#pragma unroll
+        for (int j = 0; j < kExpBatch; ++j) {
+            if ((ball[j] >> lane) & 1u) {
+                const unsigned int slot = base + __popc(ball[j] & below);
+                if (slot < static_cast<unsigned int>(kListCap))
+                    sm.u.l.k[slot] = kb + j * kThreads + lane;
+            }
+            base += __popc(ball[j]);
+        }
     }
-    lsum = block_sum_u64(lsum, sm);
+    unsigned long long lsum = (static_cast<unsigned long long>(sum_hi) << 20) + sum_lo;
+    __syncthreads();
+    const unsigned int nl = sm.nlist;
+    const bool listed = nl <= static_cast<unsigned int>(kListCap);
+    if (listed) {  // the histogram of the listed entries (they crowd a few buckets)
+        for (int t0 = tid - lane; t0 < static_cast<int>(nl); t0 += kThreads) {  // warp-uniform
+            const int t = t0 + lane;
+            const float e = t < static_cast<int>(nl) ? s[sm.u.l.k[t]] : 0.0f;
+            const unsigned long long W = mass_of(e);
+            const bool in = t < static_cast<int>(nl) && W >= cmin;
+            warp_bucket_add(in, in ? log_bucket_e(e) : 0, W, lane, nullptr, sm.mass);
+        }
+    } else {  // too many: scan the slice again, adding per bucket once per warp
+        for (int k0 = tid - lane; k0 < n; k0 += kThreads) {  // warp-uniform trip count
+            const int k = k0 + lane;
+            const float e = k < n ? s[k] : 0.0f;
+            const unsigned long long W = mass_of(e);
+            const bool in = e >= e_lo && W >= cmin;
+            if (__ballot_sync(0xffffffffu, in) == 0u) continue;
+            warp_bucket_add(in, in ? log_bucket_e(e) : 0, W, lane, nullptr, sm.mass);
+        }
+    }
+    lsum = block_sum_u64(lsum, sm.red);
     if (tid == 0) sm.lsum = lsum;
     cl.sync();
     unsigned long long S = 0;
     for (int r = 0; r < C; ++r) S += *cl.map_shared_rank(&sm.lsum, r);
     RowInfo info;
     info.mx = mx;
-    if (P >= kKeepAll) {
+    if (!want_hist) {
         info.cut = V - 1;
         info.tau = 0;
         info.S = S;
@@ -296,7 +450,7 @@ __device__ RowInfo row_stats(cg::cluster_group& cl, float* s, int n, int lo, int
         sm.mmass[tb] = m;
     }
     u128 tot_unused;
-    const u128 incl = block_excl_u128(static_cast<u128>(m), sm, tot_unused) + m;  // mass of >= tb
+    const u128 incl = block_excl_u128(static_cast<u128>(m), sm.red, tot_unused) + m;
     if (tid == 0) {
         sm.ncand = 0;
         sm.overflow = 0;
@@ -307,15 +461,25 @@ __device__ RowInfo row_stats(cg::cluster_group& cl, float* s, int n, int lo, int
     }
     __syncthreads();
 
-    // 3. gather the members of the crossing bucket
+    // 4. gather the members of the crossing bucket
     const int beta = sm.beta;
-    const int lane = tid & 31;
-    for (int k0 = tid - lane; k0 < n; k0 += kThreads) {  // warp-uniform trip count
-        const int k = k0 + lane;
-        const unsigned long long W = k < n ? mass_of(s[k]) : 0ull;
-        const bool hit = W != 0ull && log_bucket(W) == beta;
+    float b_lo, b_hi;  // members of bucket beta: b_lo <= e < b_hi
+    bucket_e_range(beta, b_lo, b_hi);
+    // Entries of bucket beta below c0 are not listed; they are below the cut
+    // (c0 <= tau) and sort after it, so the scan below never reaches them.
+    const int n_scan = listed ? static_cast<int>(nl) : n;
+    for (int k0 = tid - lane; k0 < n_scan; k0 += kThreads) {  // warp-uniform trip count
+        const int j = k0 + lane;
+        float e = 0.0f;
+        int k = 0;
+        if (j < n_scan) {
+            k = listed ? sm.u.l.k[j] : j;
+            e = s[k];
+        }
+        const bool hit = j < n_scan && e >= b_lo && e < b_hi;
         const unsigned int ball = __ballot_sync(0xffffffffu, hit);
         if (ball == 0u) continue;
+        const unsigned long long W = mass_of(e);
         unsigned int base = 0;
         if (lane == 0) base = atomicAdd(&sm.ncand, static_cast<unsigned int>(__popc(ball)));
         base = __shfl_sync(0xffffffffu, base, 0);
@@ -338,24 +502,48 @@ __device__ RowInfo row_stats(cg::cluster_group& cl, float* s, int n, int lo, int
         overflow |= *cl.map_shared_rank(&sm.overflow, r);
     }
     if (!overflow && total <= static_cast<unsigned int>(kCandTotal)) {
-        if (rank == 0) {
-            // gather, pad to a power of two, bitonic sort by (W desc, index asc)
-            unsigned int pw = 1;
-            while (pw < total) pw <<= 1;
+        if (rank == 0) {  // gather the candidates in rank order
             unsigned int base = 0;
             for (int r = 0; r < C; ++r) {
                 const unsigned int cr = *cl.map_shared_rank(&sm.ncand, r);
                 const unsigned long long* rw = cl.map_shared_rank(&sm.cw[0], r);
                 const int* ri = cl.map_shared_rank(&sm.ci[0], r);
                 for (unsigned int t = tid; t < cr; t += kThreads) {
-                    sm.gw[base + t] = rw[t];
-                    sm.gi[base + t] = ri[t];
+                    sm.u.g.w[base + t] = rw[t];
+                    sm.u.g.i[base + t] = ri[t];
                 }
                 base += cr;
             }
+        }
+        cl.sync();  // the peers' candidates are copied: only rank 0 goes on
+        if (rank != 0) return info;
+        if (total <= static_cast<unsigned int>(kRankSortMax)) {
+            // few: each candidate's place is the number that precede it
+            unsigned long long wt = 0ull;
+            int it = 0x7fffffff;
+            unsigned int place = 0;
+            if (static_cast<unsigned int>(tid) < total) {
+                wt = sm.u.g.w[tid];
+                it = sm.u.g.i[tid];
+                for (unsigned int u = 0; u < total; ++u) {
+                    const unsigned long long wu = sm.u.g.w[u];
+                    const int iu = sm.u.g.i[u];
+                    place += (wu > wt || (wu == wt && iu < it)) ? 1u : 0u;
+                }
+            }
+            __syncthreads();
+            if (static_cast<unsigned int>(tid) < total) {
+                sm.u.g.w[place] = wt;
+                sm.u.g.i[place] = it;
+            }
+            __syncthreads();
+        } else {
+            // pad to a power of two, bitonic sort by (W desc, index asc)
+            unsigned int pw = 1;
+            while (pw < total) pw <<= 1;
             for (unsigned int t = total + tid; t < pw; t += kThreads) {
-                sm.gw[t] = 0ull;
-                sm.gi[t] = 0x7fffffff;
+                sm.u.g.w[t] = 0ull;
+                sm.u.g.i[t] = 0x7fffffff;
             }
             __syncthreads();
             for (unsigned int kk = 2; kk <= pw; kk <<= 1) {
@@ -363,49 +551,47 @@ __device__ RowInfo row_stats(cg::cluster_group& cl, float* s, int n, int lo, int
                     for (unsigned int t = tid; t < pw; t += kThreads) {
                         const unsigned int u = t ^ j;
                         if (u > t) {
-                            const unsigned long long wa = sm.gw[t], wb = sm.gw[u];
-                            const int ia = sm.gi[t], ib = sm.gi[u];
+                            const unsigned long long wa = sm.u.g.w[t], wb = sm.u.g.w[u];
+                            const int ia = sm.u.g.i[t], ib = sm.u.g.i[u];
                             const bool a_first = wa > wb || (wa == wb && ia < ib);
                             const bool up = (t & kk) == 0;
                             if (up != a_first) {
-                                sm.gw[t] = wb;
-                                sm.gw[u] = wa;
-                                sm.gi[t] = ib;
-                                sm.gi[u] = ia;
+                                sm.u.g.w[t] = wb;
+                                sm.u.g.w[u] = wa;
+                                sm.u.g.i[t] = ib;
+                                sm.u.g.i[u] = ia;
                             }
                         }
                     }
                     __syncthreads();
                 }
             }
-            // running mass down the sorted list; the first crossing is the cut
-            const unsigned int t0 = 2 * tid;
-            const unsigned long long w0 = t0 < total ? sm.gw[t0] : 0ull;
-            const unsigned long long w1 = t0 + 1 < total ? sm.gw[t0 + 1] : 0ull;
-            u128 tot;
-            const u128 ex = block_excl_u128(static_cast<u128>(w0) + w1, sm, tot);
-            const u128 above = sm.above;
-            const u128 c0 = above + ex + w0, c1 = c0 + w1;
-            if (t0 < total && (c0 << 32) >= TGT && ((above + ex) << 32) < TGT) {
-                sm.info.tau = w0;
-                sm.info.cut = sm.gi[t0];
-                sm.info.S = static_cast<unsigned long long>(c0);
-            } else if (t0 + 1 < total && (c1 << 32) >= TGT && (c0 << 32) < TGT) {
-                sm.info.tau = w1;
-                sm.info.cut = sm.gi[t0 + 1];
-                sm.info.S = static_cast<unsigned long long>(c1);
-            }
         }
-        cl.sync();
-        const RowInfo* r0 = cl.map_shared_rank(&sm.info, 0);
-        info.tau = r0->tau;
-        info.cut = r0->cut;
-        info.S = r0->S;
-        cl.sync();  // rank 0's result stays until everyone has it
-        return info;
+        // running mass down the sorted list; the first crossing is the cut
+        const unsigned int t0 = 2 * tid;
+        const unsigned long long w0 = t0 < total ? sm.u.g.w[t0] : 0ull;
+        const unsigned long long w1 = t0 + 1 < total ? sm.u.g.w[t0 + 1] : 0ull;
+        u128 tot;
+        const u128 ex = block_excl_u128(static_cast<u128>(w0) + w1, sm.red, tot);
+        const u128 above = sm.above;
+        const u128 c0s = above + ex + w0, c1s = c0s + w1;
+        if (t0 < total && (c0s << 32) >= TGT && ((above + ex) << 32) < TGT) {
+            sm.info.tau = w0;
+            sm.info.cut = sm.u.g.i[t0];
+            sm.info.S = static_cast<unsigned long long>(c0s);
+        } else if (t0 + 1 < total && (c1s << 32) >= TGT && (c0s << 32) < TGT) {
+            sm.info.tau = w1;
+            sm.info.cut = sm.u.g.i[t0 + 1];
+            sm.info.S = static_cast<unsigned long long>(c1s);
+        }
+        __syncthreads();
+        info.tau = sm.info.tau;
+        info.cut = sm.info.cut;
+        info.S = sm.info.S;
+        return info;  // rank 0 only: the peers have returned
     }
 
-    // 4. fallback: exact radix search over the slices inside the bucket
+    // 5. fallback: exact radix search over the slices inside the bucket
     if (tid == 0) {
         if (beta < 16) {
             sm.lo = static_cast<unsigned long long>(beta);
@@ -432,12 +618,13 @@ __device__ RowInfo row_stats(cg::cluster_group& cl, float* s, int n, int lo, int
             sm.mass[t] = 0ull;
         }
         __syncthreads();
-        for (int k = tid; k < n; k += kThreads) {
-            const unsigned long long W = mass_of(s[k]);
-            if (W < rlo || W >= rhi) continue;
-            const int bk = static_cast<int>((W - rlo) >> shift);
-            atomicAdd(&sm.cnt[bk], 1u);
-            atomicAdd(&sm.mass[bk], W);
+        for (int k0 = tid - lane; k0 < n; k0 += kThreads) {  // warp-uniform trip count
+            const int k = k0 + lane;
+            const unsigned long long W = k < n ? mass_of(s[k]) : 0ull;
+            const bool in = k < n && W >= rlo && W < rhi;
+            if (__ballot_sync(0xffffffffu, in) == 0u) continue;
+            warp_bucket_add(in, in ? static_cast<int>((W - rlo) >> shift) : 0, W, lane, sm.cnt,
+                            sm.mass);
         }
         cl.sync();
         for (int t = tid; t < (1 << bits); t += kThreads) {
@@ -456,7 +643,7 @@ __device__ RowInfo row_stats(cg::cluster_group& cl, float* s, int n, int lo, int
             const int t = nb - 1 - tid;  // thread tid holds sub-bucket nb - 1 - tid
             const unsigned long long mt = t >= 0 ? sm.mmass[t] : 0ull;
             u128 tot2;
-            const u128 inc = block_excl_u128(static_cast<u128>(mt), sm, tot2) + mt;
+            const u128 inc = block_excl_u128(static_cast<u128>(mt), sm.red, tot2) + mt;
             const u128 ab = static_cast<u128>(sm.above);
             if (t >= 0 && ((ab + inc) << 32) >= TGT && ((ab + inc - mt) << 32) < TGT) {
                 sm.beta = t;
@@ -488,7 +675,7 @@ __device__ RowInfo row_stats(cg::cluster_group& cl, float* s, int n, int lo, int
     for (int k = k0; k < k1; ++k) mine += (mass_of(s[k]) == tau) ? 1u : 0u;
     u128 ctot;
     const unsigned long long excl =
-        static_cast<unsigned long long>(block_excl_u128(static_cast<u128>(mine), sm, ctot));
+        static_cast<unsigned long long>(block_excl_u128(static_cast<u128>(mine), sm.red, ctot));
     if (tid == 0) {
         sm.count_eq = static_cast<unsigned long long>(ctot);
         sm.cut_found = -1;
@@ -519,77 +706,7 @@ __device__ RowInfo row_stats(cg::cluster_group& cl, float* s, int n, int lo, int
     return info;
 }
 
-// --------------------------------------------------- ordered categorical draw
-// Weight of slice element k: the residual r_v (res) or the kept target mass.
-struct Weights {
-    const float* ep;
-    const float* eq;
-    RowInfo ip, iq;
-    bool res;
-    int lo;
-    __device__ __forceinline__ u128 at(int k) const {
-        const int v = lo + k;
-        const unsigned long long wp = kept(mass_of(ep[k]), v, ip);
-        if (!res) return static_cast<u128>(wp);
-        const unsigned long long wq = kept(mass_of(eq[k]), v, iq);
-        const u128 a = static_cast<u128>(wp) * iq.S, c = static_cast<u128>(wq) * ip.S;
-        return a > c ? a - c : static_cast<u128>(0);
-    }
-};
-
-// Sum of the weights of this CTA's slice (every thread gets it).
-__device__ __forceinline__ u128 slice_total(const Weights& w, int n, Smem& sm) {
-    u128 part = 0;
-    for (int k = threadIdx.x; k < n; k += kThreads) part += w.at(k);
-    return block_sum_u128(part, sm);
-}
-
-// Returns (to every CTA) the first index whose running weight sum exceeds
-// floor(u64 * total / 2^64); `mine` is this CTA's slice total.
-__device__ int ordered_draw(cg::cluster_group& cl, const Weights& w, int n, u128 mine, u128 total,
-                            unsigned long long u64, Smem& sm) {
-    const int C = static_cast<int>(cl.num_blocks());
-    const int rank = static_cast<int>(cl.block_rank());
-    const int tid = threadIdx.x;
-    const u128 t = scale_u64(u64, total);
-    if (tid == 0) {
-        sm.part_lo = static_cast<unsigned long long>(mine);
-        sm.part_hi = static_cast<unsigned long long>(mine >> 64);
-        sm.cut_found = -1;
-    }
-    cl.sync();
-    u128 before = 0;
-    for (int r = 0; r < rank; ++r)
-        before += (static_cast<u128>(*cl.map_shared_rank(&sm.part_hi, r)) << 64) |
-                  *cl.map_shared_rank(&sm.part_lo, r);
-    if (before <= t && t < before + mine) {  // the draw lands in this CTA's slice
-        const int chunk = (n + kThreads - 1) / kThreads;
-        const int k0 = tid * chunk, k1 = (k0 + chunk < n) ? k0 + chunk : n;
-        u128 own = 0;
-        for (int k = k0; k < k1; ++k) own += w.at(k);
-        u128 tot;
-        const u128 ex = before + block_excl_u128(own, sm, tot);
-        if (ex <= t && t < ex + own) {
-            u128 run = ex;
-            for (int k = k0; k < k1; ++k) {
-                run += w.at(k);
-                if (run > t) {
-                    sm.cut_found = w.lo + k;
-                    break;
-                }
-            }
-        }
-    }
-    cl.sync();
-    int tok = -1;
-    for (int r = 0; r < C; ++r) {
-        const int x = *cl.map_shared_rank(&sm.cut_found, r);
-        if (x >= 0) tok = x;
-    }
-    cl.sync();
-    return tok;
-}
-
+// ------------------------------------------------------------- row kernel
 __device__ __forceinline__ void load_slice(float* dst, const float* src, int n, bool vec) {
     if (vec) {
         const int n4 = n >> 2;
@@ -602,110 +719,294 @@ __device__ __forceinline__ void load_slice(float* dst, const float* src, int n, 
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) pair_kernel(
-    const float* __restrict__ target, const float* __restrict__ draft,
-    const int32_t* __restrict__ drafts, int Kd, int V, int slice, int vec_ok, float invT,
-    unsigned long long P, unsigned long long seed, unsigned long long offset,
-    PairOut* __restrict__ out, uint32_t* status) {
+// Rows 0 .. B(Kd+1)-1 are the target rows (b, i) in order, then the B*Kd
+// draft rows (b, i).
+__global__ void __launch_bounds__(kThreads, 2) row_kernel(
+    const float* __restrict__ target, const float* __restrict__ draft, long long n_target_rows,
+    int V, int slice, int vec_ok, float invT, unsigned long long P, RowInfo* __restrict__ info,
+    uint32_t* status, unsigned long long wait_ns) {
     cg::cluster_group cl = cg::this_cluster();
     extern __shared__ float4 dyn[];
-    __shared__ Smem sm;
-    float* sp = reinterpret_cast<float*>(dyn);
-    float* sq = sp + slice;
+    __shared__ RowSmem sm;
+    float* s = reinterpret_cast<float*>(dyn);
     const int C = static_cast<int>(cl.num_blocks());
     const int rank = static_cast<int>(cl.block_rank());
-    const long long pid = blockIdx.x / C;
-    const long long b = pid / (Kd + 1);
-    const int i = static_cast<int>(pid % (Kd + 1));
-    const bool has_q = i < Kd;
+    const long long row = blockIdx.x / C;
+    const float* src = row < n_target_rows
+                           ? target + row * static_cast<long long>(V)
+                           : draft + (row - n_target_rows) * static_cast<long long>(V);
     const int lo = rank * slice;
     const int n = (lo < V) ? ((V - lo < slice) ? V - lo : slice) : 0;
-    const float* lp = target + (b * (Kd + 1) + i) * static_cast<long long>(V);
-    const float* lq = has_q ? draft + (b * Kd + i) * static_cast<long long>(V) : nullptr;
-    const bool vec = vec_ok != 0;  // rows start on 16-byte boundaries
-    load_slice(sp, lp + lo, n, vec);
-    if (has_q) load_slice(sq, lq + lo, n, vec);
-    __syncthreads();
-
-    const RowInfo ip = row_stats(cl, sp, n, lo, V, invT, P, sm);
-    RowInfo iq{};
-    if (has_q) iq = row_stats(cl, sq, n, lo, V, invT, P, sm);
-
-    uint32_t rr[4];
-    philox4x32_10(static_cast<uint32_t>(i), static_cast<uint32_t>(b),
-                  static_cast<uint32_t>(offset), static_cast<uint32_t>(offset >> 32),
-                  static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32), rr);
-    const unsigned long long u64 = (static_cast<unsigned long long>(rr[2]) << 32) | rr[1];
-
-    Weights w{sp, sq, ip, iq, false, lo};
-    if (!has_q) {  // the bonus row
-        const u128 mine = slice_total(w, n, sm);
-        const int tok = ordered_draw(cl, w, n, mine, static_cast<u128>(ip.S), u64, sm);
-        if (rank == 0 && threadIdx.x == 0) out[pid] = PairOut{1, tok};
-        return;
-    }
-    // the acceptance test of draft i
-    if (rank == 0 && threadIdx.x == 0) {
-        const int32_t x = drafts[b * Kd + i];
-        int ok = 0;
-        if (x >= 0 && x < V) {
-            const unsigned long long Wp = kept(mass_of(own_exp(scaled_x(lp[x], ip.mx, invT))), x, ip);
-            const unsigned long long Wq = kept(mass_of(own_exp(scaled_x(lq[x], iq.mx, invT))), x, iq);
-            const unsigned long long U = rr[0] >> 8;
-            const u128 lhs = static_cast<u128>(U * Wq) * ip.S;
-            const u128 rhs = (static_cast<u128>(Wp) * iq.S) << 24;
-            ok = lhs < rhs ? 1 : 0;
-        } else {
-            atomicOr(status, kStatusBadDraft);
+    if (vec_ok && n > 0) {
+        // one bulk copy of the whole slice (16-byte aligned, a multiple of 16 bytes)
+        __shared__ __align__(8) uint64_t bar;
+        if (threadIdx.x == 0) {
+            mbar_init(&bar, 1);
+            fence_barrier_init();
+            mbar_arrive_expect_tx(&bar, static_cast<uint32_t>(n) * 4u);
+            bulk_load(s, src + lo, static_cast<uint32_t>(n) * 4u, &bar, policy_evict_first());
         }
-        sm.decision = ok;
+        if (threadIdx.x < 32) {  // one warp polls; the others sleep in the barrier below
+            __syncwarp();        // the barrier is initialised before any lane polls it
+            if (!mbar_wait_bounded(&bar, 0, wait_ns, nullptr) && threadIdx.x == 0)
+                atomicOr(status, kStatusTimeout);
+        }
+    } else {
+        load_slice(s, src + lo, n, false);
     }
-    cl.sync();
-    const int ok = *cl.map_shared_rank(&sm.decision, 0);
-    if (ok) {
-        cl.sync();
-        if (rank == 0 && threadIdx.x == 0) out[pid] = PairOut{1, -1};
-        return;
-    }
-    // rejected: residual max(0, p*Sq - q*Sp) from the rows on chip
-    w.res = true;
-    u128 mine = slice_total(w, n, sm);
-    if (threadIdx.x == 0) {
-        sm.part_lo = static_cast<unsigned long long>(mine);
-        sm.part_hi = static_cast<unsigned long long>(mine >> 64);
-    }
-    cl.sync();
-    u128 R = 0;
-    for (int r = 0; r < C; ++r)
-        R += (static_cast<u128>(*cl.map_shared_rank(&sm.part_hi, r)) << 64) |
-             *cl.map_shared_rank(&sm.part_lo, r);
-    cl.sync();
-    if (R == 0) {  // only reachable through an invalid draft id: draw from p
-        if (rank == 0 && threadIdx.x == 0) atomicOr(status, kStatusZeroResidual);
-        w.res = false;
-        mine = slice_total(w, n, sm);
-        R = static_cast<u128>(ip.S);
-    }
-    const int tok = ordered_draw(cl, w, n, mine, R, u64, sm);
-    if (rank == 0 && threadIdx.x == 0) out[pid] = PairOut{0, tok};
+    __syncthreads();
+    const RowInfo r = row_stats(cl, s, n, lo, V, invT, P, sm);
+    if (rank == 0 && threadIdx.x == 0) info[row] = r;
 }
 
-// One thread per sequence: the first rejection decides the committed run.
-__global__ void commit_kernel(const int32_t* __restrict__ drafts, const PairOut* __restrict__ pairs,
-                              int B, int Kd, int32_t* __restrict__ tokens,
-                              int32_t* __restrict__ len) {
-    const int b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= B) return;
-    const PairOut* pr = pairs + static_cast<long long>(b) * (Kd + 1);
-    int n = 0;
-    while (n < Kd && pr[n].accept) ++n;
-    for (int i = 0; i <= Kd; ++i) {
-        int32_t t = -1;
-        if (i < n) t = drafts[static_cast<long long>(b) * Kd + i];
-        else if (i == n) t = pr[n].token;
-        tokens[static_cast<long long>(b) * (Kd + 1) + i] = t;
+// --------------------------------------------------------- sequence kernel
+// Weight of entry v in the draw: the kept target mass (p), or the residual
+// max(0, p_v * Sq - q_v * Sp).  Entries whose scaled logit is below xth have
+// a kept target mass of 0 (own_exp is monotone and within 2 ulp of exp, and
+// xth sits 1e-3 below log(max(tau, 1) / 2^40)), so they cost two flops.
+struct DrawRow {
+    const float* lp;
+    const float* lq;  // null: draw from p
+    RowInfo ip, iq;
+    float invT, xth;
+    __device__ __forceinline__ u128 at(int v) const {
+        const float xp = scaled_x(__ldg(lp + v), ip.mx, invT);
+        if (xp < xth) return 0;
+        const unsigned long long wp = kept(mass_of(own_exp(xp)), v, ip);
+        if (lq == nullptr || wp == 0ull) return static_cast<u128>(wp);
+        const unsigned long long wq =
+            kept(mass_of(own_exp(scaled_x(__ldg(lq + v), iq.mx, invT))), v, iq);
+        const u128 a = static_cast<u128>(wp) * iq.S, c = static_cast<u128>(wq) * ip.S;
+        return a > c ? a - c : static_cast<u128>(0);
     }
-    len[b] = n + 1;
+    __device__ __forceinline__ float4 ld4(int v) const {  // v % 4 == 0, rows 16-byte aligned
+        return __ldg(reinterpret_cast<const float4*>(lp + v));
+    }
+    __device__ __forceinline__ u128 at4(int v) const { return at4(v, ld4(v)); }
+    __device__ __forceinline__ u128 at4(int v, float4 l) const {  // l = lp[v .. v+3]
+        const float x0 = scaled_x(l.x, ip.mx, invT), x1 = scaled_x(l.y, ip.mx, invT);
+        const float x2 = scaled_x(l.z, ip.mx, invT), x3 = scaled_x(l.w, ip.mx, invT);
+        if (x0 < xth && x1 < xth && x2 < xth && x3 < xth) return 0;
+        return at(v) + at(v + 1) + at(v + 2) + at(v + 3);
+    }
+};
+
+struct SeqSmem {
+    Red red;
+    unsigned long long tot_lo[kWarps], tot_hi[kWarps];
+    unsigned long long u64s[kMaxRows + 1];
+    int ok[kMaxRows + 1];
+    int n_acc, rowp, rowq, sel, token;
+    unsigned long long u64;
+    unsigned long long t_lo, t_hi;
+};
+
+// Sum of the weights of [a, b) by one warp (every lane gets it).
+__device__ __forceinline__ u128 warp_range_sum(const DrawRow& w, int a, int b, bool vec, int lane) {
+    u128 acc = 0;
+    if (vec) {
+        const int a4 = (a + 3) & ~3, b4 = b & ~3;
+        if (a4 <= b4) {
+            int v = a4 + 4 * lane;
+            for (; v + 3 * 128 < b4; v += 4 * 128) {  // four float4 loads in flight
+                const float4 l0 = w.ld4(v), l1 = w.ld4(v + 128), l2 = w.ld4(v + 256),
+                             l3 = w.ld4(v + 384);
+                acc += w.at4(v, l0) + w.at4(v + 128, l1) + w.at4(v + 256, l2) +
+                       w.at4(v + 384, l3);
+            }
+            for (; v < b4; v += 128) acc += w.at4(v);
+            if (lane < a4 - a) acc += w.at(a + lane);
+            if (lane < b - b4) acc += w.at(b4 + lane);
+            return warp_sum_u128(acc);
+        }
+    }
+    for (int v = a + lane; v < b; v += 32) acc += w.at(v);
+    return warp_sum_u128(acc);
+}
+
+// One CTA per sequence: acceptance tests in order, then one ordered draw and
+// the committed run.
+__global__ void __launch_bounds__(kThreads) seq_kernel(
+    const float* __restrict__ target, const float* __restrict__ draft,
+    const int32_t* __restrict__ drafts, int Kd, int V, int vec_ok, float invT,
+    unsigned long long seed, unsigned long long offset, long long n_target_rows,
+    const RowInfo* __restrict__ info, int32_t* __restrict__ tokens, int32_t* __restrict__ len,
+    uint32_t* status) {
+    __shared__ SeqSmem sm;
+    const int b = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    // the Kd acceptance tests are independent: thread i takes draft i
+    if (tid <= Kd) {
+        const int i = tid;
+        uint32_t rr[4];
+        philox4x32_10(static_cast<uint32_t>(i), static_cast<uint32_t>(b),
+                      static_cast<uint32_t>(offset), static_cast<uint32_t>(offset >> 32),
+                      static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32), rr);
+        sm.u64s[i] = (static_cast<unsigned long long>(rr[2]) << 32) | rr[1];
+        int ok = 1;  // position Kd: the bonus
+        if (i < Kd) {
+            const long long rp = static_cast<long long>(b) * (Kd + 1) + i;
+            const long long rq = n_target_rows + static_cast<long long>(b) * Kd + i;
+            const RowInfo ip = info[rp], iq = info[rq];
+            const int32_t x = drafts[static_cast<long long>(b) * Kd + i];
+            ok = 0;
+            if (x >= 0 && x < V) {
+                const float lpx = target[rp * V + x];
+                const float lqx = draft[(rq - n_target_rows) * V + x];
+                const unsigned long long Wp =
+                    kept(mass_of(own_exp(scaled_x(lpx, ip.mx, invT))), x, ip);
+                const unsigned long long Wq =
+                    kept(mass_of(own_exp(scaled_x(lqx, iq.mx, invT))), x, iq);
+                const unsigned long long U = rr[0] >> 8;
+                const u128 lhs = static_cast<u128>(U * Wq) * ip.S;
+                const u128 rhs = (static_cast<u128>(Wp) * iq.S) << 24;
+                ok = lhs < rhs ? 1 : 0;
+            } else {
+                atomicOr(status, kStatusBadDraft);
+            }
+        }
+        sm.ok[i] = ok;
+    }
+    __syncthreads();
+    if (tid == 0) {  // the first rejection decides the run
+        int n = 0;
+        while (n < Kd && sm.ok[n]) ++n;
+        sm.n_acc = n;
+        sm.rowp = b * (Kd + 1) + n;
+        sm.rowq = n < Kd ? static_cast<int>(n_target_rows + static_cast<long long>(b) * Kd + n) : -1;
+        sm.u64 = sm.u64s[n];
+        sm.token = -1;
+    }
+    __syncthreads();
+    const int rowp = sm.rowp, rowq = sm.rowq;
+    DrawRow w;
+    w.ip = info[rowp];
+    w.lp = target + static_cast<long long>(rowp) * V;
+    w.lq = nullptr;
+    if (rowq >= 0) {
+        w.iq = info[rowq];
+        w.lq = draft + (rowq - n_target_rows) * static_cast<long long>(V);
+    }
+    w.invT = invT;
+    {
+        const unsigned long long tm = w.ip.tau > 1ull ? w.ip.tau : 1ull;
+        w.xth = static_cast<float>(log(static_cast<double>(tm)) - 40.0 * 0.69314718055994530942 -
+                                   1e-3);
+    }
+    const bool vec = vec_ok != 0;
+
+    // level 1: each warp totals a contiguous range of the row
+    const int L1 = (((V + kWarps - 1) / kWarps) + 3) & ~3;
+    int a1 = wid * L1, b1 = a1 + L1;
+    if (a1 > V) a1 = V;
+    if (b1 > V) b1 = V;
+    u128 wt = warp_range_sum(w, a1, b1, vec, lane);
+    if (lane == 0) {
+        sm.tot_lo[wid] = static_cast<unsigned long long>(wt);
+        sm.tot_hi[wid] = static_cast<unsigned long long>(wt >> 64);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        u128 R = 0;
+        for (int k = 0; k < kWarps; ++k) R += (static_cast<u128>(sm.tot_hi[k]) << 64) | sm.tot_lo[k];
+        sm.sel = 0;
+        if (rowq >= 0 && R == 0) {  // only reachable through an invalid draft id
+            atomicOr(status, kStatusZeroResidual);
+            sm.sel = 1;
+        }
+        const u128 total = rowq >= 0 && R != 0 ? R : static_cast<u128>(w.ip.S);
+        const u128 t = scale_u64(sm.u64, total);
+        sm.t_lo = static_cast<unsigned long long>(t);
+        sm.t_hi = static_cast<unsigned long long>(t >> 64);
+    }
+    __syncthreads();
+    if (sm.sel) {  // the residual is empty: draw from p, with fresh level-1 totals
+        w.lq = nullptr;
+        wt = warp_range_sum(w, a1, b1, vec, lane);
+        __syncthreads();
+        if (lane == 0) {
+            sm.tot_lo[wid] = static_cast<unsigned long long>(wt);
+            sm.tot_hi[wid] = static_cast<unsigned long long>(wt >> 64);
+        }
+        __syncthreads();
+    }
+    // which warp range holds t
+    u128 t = (static_cast<u128>(sm.t_hi) << 64) | sm.t_lo;
+    int sel = kWarps - 1;
+    {
+        u128 run = 0;
+        for (int k = 0; k < kWarps; ++k) {
+            const u128 x = (static_cast<u128>(sm.tot_hi[k]) << 64) | sm.tot_lo[k];
+            if (t < run + x) {
+                sel = k;
+                break;
+            }
+            run += x;
+        }
+        t -= run;
+    }
+    __syncthreads();
+    // level 2: the warps split that range again
+    const int A = sel * L1 < V ? sel * L1 : V;
+    const int Bnd = A + L1 < V ? A + L1 : V;
+    const int L2 = ((((Bnd - A) + kWarps - 1) / kWarps) + 3) & ~3;
+    int a2 = A + wid * L2, b2 = a2 + L2;
+    if (a2 > Bnd) a2 = Bnd;
+    if (b2 > Bnd) b2 = Bnd;
+    wt = warp_range_sum(w, a2, b2, vec, lane);
+    if (lane == 0) {
+        sm.tot_lo[wid] = static_cast<unsigned long long>(wt);
+        sm.tot_hi[wid] = static_cast<unsigned long long>(wt >> 64);
+    }
+    __syncthreads();
+    int sel2 = kWarps - 1;
+    {
+        u128 run = 0;
+        for (int k = 0; k < kWarps; ++k) {
+            const u128 x = (static_cast<u128>(sm.tot_hi[k]) << 64) | sm.tot_lo[k];
+            if (t < run + x) {
+                sel2 = k;
+                break;
+            }
+            run += x;
+        }
+        t -= run;
+    }
+    // level 3: warp 0 scans that sub-range in index order
+    if (wid == 0) {
+        int a3 = A + sel2 * L2, b3 = a3 + L2;
+        if (a3 > Bnd) a3 = Bnd;
+        if (b3 > Bnd) b3 = Bnd;
+        u128 run = 0;
+        int tok = -1;
+        for (int base = a3; base < b3 && tok < 0; base += 32) {
+            const int v = base + lane;
+            const u128 x = v < b3 ? w.at(v) : static_cast<u128>(0);
+            u128 incl = x;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const u128 y = shfl_up_u128(incl, o);
+                if (lane >= o) incl += y;
+            }
+            const unsigned int hit = __ballot_sync(0xffffffffu, run + incl > t);
+            if (hit) tok = base + __ffs(hit) - 1;
+            const unsigned long long hlo =
+                __shfl_sync(0xffffffffu, static_cast<unsigned long long>(incl), 31);
+            const unsigned long long hhi =
+                __shfl_sync(0xffffffffu, static_cast<unsigned long long>(incl >> 64), 31);
+            run += (static_cast<u128>(hhi) << 64) | hlo;
+        }
+        if (lane == 0) sm.token = tok >= 0 ? tok : V - 1;
+    }
+    __syncthreads();
+    if (tid <= Kd) {
+        const int n = sm.n_acc;
+        int32_t tk = -1;
+        if (tid < n) tk = drafts[static_cast<long long>(b) * Kd + tid];
+        else if (tid == n) tk = sm.token;
+        tokens[static_cast<long long>(b) * (Kd + 1) + tid] = tk;
+    }
+    if (tid == 0) len[b] = sm.n_acc + 1;
 }
 
 __global__ void own_exp_kernel(const float* __restrict__ x, float* __restrict__ y, long long n) {
@@ -731,30 +1032,31 @@ cudaError_t launch_own_exp(const float* x, float* y, long long n, cudaStream_t s
 
 size_t rejection_workspace_bytes(int B, int Kd, int V) {
     (void)V;
-    const size_t pairs = static_cast<size_t>(B) * (Kd + 1);
-    return ((pairs * sizeof(PairOut) + 255) / 256) * 256;
+    const size_t rows = static_cast<size_t>(B) * (2 * static_cast<size_t>(Kd) + 1);
+    return ((rows * sizeof(RowInfo) + 255) / 256) * 256;
 }
 
 cudaError_t launch_accept_rejection(const float* target, const float* draft,
                                     const int32_t* drafts, int B, int Kd, int V, float invT,
                                     uint64_t P, uint64_t seed, uint64_t offset, int32_t* tokens,
                                     int32_t* len, void* ws, size_t ws_bytes, uint32_t* status,
-                                    cudaStream_t s) {
+                                    unsigned long long wait_ns, cudaStream_t s) {
     const int C = cluster_for(V);
     int slice = (V + C - 1) / C;
     slice = (slice + 3) & ~3;
     if (slice > kMaxSlice) return cudaErrorNotSupported;
-    const size_t pairs = static_cast<size_t>(B) * (Kd + 1);
-    if (pairs * C > 0x7fffffffull) return cudaErrorNotSupported;
+    const long long n_target_rows = static_cast<long long>(B) * (Kd + 1);
+    const long long rows = n_target_rows + static_cast<long long>(B) * Kd;
+    if (rows * C > 0x7fffffffll || rows > 0x7fffffffll) return cudaErrorNotSupported;
     if (rejection_workspace_bytes(B, Kd, V) > ws_bytes) return cudaErrorInvalidValue;
-    PairOut* out = static_cast<PairOut*>(ws);
+    RowInfo* info = static_cast<RowInfo*>(ws);
 
-    const size_t smem = static_cast<size_t>(2) * slice * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const size_t smem = static_cast<size_t>(slice) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(static_cast<unsigned>(pairs * C));
+    cfg.gridDim = dim3(static_cast<unsigned>(rows * C));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -769,11 +1071,14 @@ cudaError_t launch_accept_rejection(const float* target, const float* draft,
                         (reinterpret_cast<uintptr_t>(draft) & 15u) == 0)
                            ? 1
                            : 0;
-    e = cudaLaunchKernelEx(&cfg, pair_kernel, target, draft, drafts, Kd, V, slice, vec_ok, invT,
-                           static_cast<unsigned long long>(P), static_cast<unsigned long long>(seed),
-                           static_cast<unsigned long long>(offset), out, status);
+    e = cudaLaunchKernelEx(&cfg, row_kernel, target, draft, n_target_rows, V, slice, vec_ok, invT,
+                           static_cast<unsigned long long>(P), info, status,
+                           static_cast<unsigned long long>(wait_ns));
     if (e != cudaSuccess) return e;
-    commit_kernel<<<(B + 127) / 128, 128, 0, s>>>(drafts, out, B, Kd, tokens, len);
+    seq_kernel<<<B, kThreads, 0, s>>>(target, draft, drafts, Kd, V, vec_ok, invT,
+                                      static_cast<unsigned long long>(seed),
+                                      static_cast<unsigned long long>(offset), n_target_rows,
+                                      info, tokens, len, status);
     return cudaGetLastError();
 }
 

@@ -112,6 +112,6 @@ cudaError_t launch_accept_rejection(const float* target, const float* draft,
                                     const int32_t* drafts, int B, int Kd, int V, float invT,
                                     uint64_t P, uint64_t seed, uint64_t offset, int32_t* tokens,
                                     int32_t* len, void* ws, size_t ws_bytes, uint32_t* status,
-                                    cudaStream_t s);
+                                    unsigned long long wait_ns, cudaStream_t s);
 
 }  // namespace vw4
