@@ -234,10 +234,14 @@ VW4_API vw4_status verify_gemm_w4(const vw4_weight* W, const void* A_dev, int M,
         long long S_cap = T / kMinUnitsPerCta;
         if (S_cap < 1) S_cap = 1;
         if (S > S_cap) S = S_cap;
+        if (S > kMaxSplit) S = kMaxSplit;
         split = static_cast<int>(S);
         G = n_tiles * S;
     }
     if (G > U) G = U;
+    // Up to kMaxClusterSplit parts (and no fused argmax): the parts of a tile
+    // form one cluster and combine over distributed shared memory.
+    const bool clustered = split > 1 && split <= kMaxClusterSplit && row_argmax_dev == nullptr;
 
     cudaError_t e = launch_prep_act(static_cast<const uint16_t*>(A_dev), lda, K, W->fmt, M, 0, 1,
                                     1, ws, n_tiles * kConsumerWarps, s);
@@ -263,7 +267,8 @@ VW4_API vw4_status verify_gemm_w4(const vw4_weight* W, const void* A_dev, int M,
     p.row_argmax = row_argmax_dev;
     p.status = d->status;
     p.wait_ns = g_wait_ns;
-    e = launch_gemm(W->fmt, tmW, tmS, p, static_cast<int>(G), s);
+    p.cluster = clustered ? 1 : 0;
+    e = launch_gemm(W->fmt, tmW, tmS, p, static_cast<int>(G), clustered ? split : 1, s);
     if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
     return VW4_OK;
 }
@@ -338,7 +343,7 @@ VW4_API vw4_status verify_moe_w4(const vw4_weight* experts, int E, const void* A
     p.row_argmax = nullptr;
     p.status = d->status;
     p.wait_ns = g_wait_ns;
-    e = launch_gemm(experts->fmt, tmW, tmS, p, static_cast<int>(G), s);
+    e = launch_gemm(experts->fmt, tmW, tmS, p, static_cast<int>(G), 1, s);
     if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
     if (combine) {
         e = launch_combine(ws.pair_out, gates_dev, expert_ids_dev, E, M, topk, N, out_dev, ldo, s);

@@ -32,10 +32,13 @@
 //    index, NaN never wins) via 64-bit atomic max on (ordered value, ~index).
 // Every wait is bounded (global timer); a wait that runs out sets a status
 // bit, the producer drains its in-flight copies, and the kernel returns.
+#include <cooperative_groups.h>
 #include <cuda_fp16.h>
 
 #include "ptx.cuh"
 #include "vw4_internal.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace vw4 {
 
@@ -563,10 +566,18 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     if (blockIdx.x >= G) return;
     const Range R{U, G, T, p.split};
     const unsigned long long u_begin = R.start(blockIdx.x), u_end = R.start(blockIdx.x + 1);
+    // The split parts of a tile form one cluster and combine over DSMEM.
+    // Every thread of such a CTA must reach both cluster barriers at the end,
+    // so nothing below returns early in this mode (all waits are bounded).
+    const bool cluster_mode = p.cluster != 0 && p.split > 1;
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------ producer
-        if (lane != 0) return;
+        // Lane 0 issues the copies and waits on the ring.
+        if (lane != 0) {
+            if (!cluster_mode) return;
+            goto combine;
+        }
         const uint64_t pol_w = policy_evict_first();   // nibbles: read exactly once
         const uint64_t pol_s = policy_evict_normal();  // scale sectors span two stages
         const uint64_t pol_a = policy_evict_last();    // activations: reread by every tile
@@ -609,6 +620,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         };
         // Returns 1 when issued, 0 when a wait ran out, -1 when the unit would
         // have to wait but may not (then nothing was changed).
+        // with_act: also copy the stage's activation block now (it is ready).
         auto issue = [&](const Cursor& c, bool first, uint32_t it_u, bool with_act,
                          bool may_wait) -> int {
             const int s = it_u % kStages;
@@ -667,7 +679,8 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         for (; it < n_units; ++it, advance(cur)) {
             const int s = it % kStages;
             if ((it >= static_cast<uint32_t>(kStages) &&
-                 !mbar_wait_bounded(&empty[s], ((it / kStages) - 1) & 1, p.wait_ns, abort_flag)) ||
+                 !mbar_wait_bounded(&empty[s], ((it / kStages) - 1) & 1, p.wait_ns,
+                                    abort_flag)) ||
                 issue(cur, it == 0, it, true, true) != 1) {
                 ok = false;
                 break;
@@ -681,10 +694,12 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         const uint64_t drain_ns = p.wait_ns > 2000000000ull ? p.wait_ns : 2000000000ull;
         for (uint32_t j = (it > (uint32_t)kStages ? it - kStages : 0u); j < it; ++j)
             mbar_wait_bounded(&full[j % kStages], (j / kStages) & 1, drain_ns, nullptr);
-        return;
+        if (!cluster_mode) return;
+        goto combine;
     }
 
     // ---------------------------------------------------------- consumers
+    {
     grid_dependency_wait();  // activations, scales of this call, tickets reset
     const int g = lane >> 2, c = lane & 3;
     const int wrow = warp * kWarpRows;  // first tile row of this warp
@@ -709,6 +724,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             if (!mbar_wait_bounded(&full[s], (it / kStages) & 1, p.wait_ns, abort_flag)) {
                 if (lane == 0) atomicOr(p.status, kStatusTimeout);
                 *abort_flag = 1;
+                if (cluster_mode) goto combine;
                 return;
             }
             if (it == 0 || (st & smask) == 0) {
@@ -807,6 +823,18 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             }
             continue;
         }
+        if (cluster_mode) {  // leave this part's slice in shared memory
+            float* part = reinterpret_cast<float*>(smem + kSmemPart);
+#pragma unroll
+            for (int rb = 0; rb < kRowBlocks; ++rb)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int tok = 2 * c + (q & 1);
+                    const int r = wrow + rb * 16 + g + ((q & 2) ? 8 : 0);
+                    part[tok * kTileRows + r] = v[rb][q];
+                }
+            continue;
+        }
         // Partial tile: publish this warp's 32-row slice; the last of the
         // tile's contributors to arrive for this slice sums it in k order.
         const unsigned long long tile_u0 = tg * static_cast<unsigned long long>(T);
@@ -886,6 +914,40 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             if (o2 + 1 == static_cast<uint32_t>(kConsumerWarps * n_tiles)) argmax_finish(p, lane);
         }
     }
+    }
+    if (!cluster_mode) return;
+combine:
+    {
+        // Fused split-K: the parts' partial tiles (rank order = k order) are
+        // summed by rank 0's consumers; the second barrier keeps every part's
+        // shared memory alive until rank 0 has read it.
+        cg::cluster_group cl = cg::this_cluster();
+        cl.sync();
+        const int S = static_cast<int>(cl.num_blocks());
+        if (cl.block_rank() == 0 && warp < kConsumerWarps) {
+            int aborted = 0;
+            for (int r = 0; r < S; ++r) aborted |= *cl.map_shared_rank(const_cast<int*>(abort_flag), r);
+            const int t = threadIdx.x;         // 0 .. 127
+            const int tok = t >> 4;            // verify row
+            const int r0 = (t & 15) * 8;       // eight tile rows
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int r = 0; r < S; ++r) {
+                const float* part = cl.map_shared_rank(reinterpret_cast<float*>(smem + kSmemPart), r);
+                const float4 a = *reinterpret_cast<const float4*>(part + tok * kTileRows + r0);
+                const float4 b = *reinterpret_cast<const float4*>(part + tok * kTileRows + r0 + 4);
+                acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+                acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+            }
+            const int n0 = static_cast<int>(blockIdx.x / S) * kTileRows;
+            if (!aborted && tok < p.dense_M) {
+                float* orow = p.out + static_cast<size_t>(tok) * p.ldo;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (n0 + r0 + j < p.N) orow[n0 + r0 + j] = acc[j];
+            }
+        }
+        cl.sync();
+    }
 }
 
 // ------------------------------------------------------------ MoE combine
@@ -943,7 +1005,7 @@ cudaError_t launch_prep_act(const uint16_t* A, int lda, int K, int fmt, int dens
 
 template <int FMT>
 static cudaError_t launch_gemm_t(const CUtensorMap& tmW, const CUtensorMap& tmS,
-                                 const GemmParams& p, int grid, cudaStream_t s) {
+                                 const GemmParams& p, int grid, int cluster, cudaStream_t s) {
     static bool attr_done = false;
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(gemm_w4_kernel<FMT>,
@@ -956,17 +1018,25 @@ static cudaError_t launch_gemm_t(const CUtensorMap& tmW, const CUtensorMap& tmS,
     cfg.blockDim = dim3(kGemmThreads);
     cfg.dynamicSmemBytes = kGemmSmem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (cluster > 1) {  // the split parts of a tile: one cluster
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = cluster;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
     return cudaLaunchKernelEx(&cfg, gemm_w4_kernel<FMT>, tmW, tmS, p);
 }
 
 cudaError_t launch_gemm(int fmt, const CUtensorMap& tmW, const CUtensorMap& tmS,
-                        const GemmParams& p, int grid, cudaStream_t s) {
-    return fmt == 1 ? launch_gemm_t<1>(tmW, tmS, p, grid, s) : launch_gemm_t<2>(tmW, tmS, p, grid, s);
+                        const GemmParams& p, int grid, int cluster, cudaStream_t s) {
+    return fmt == 1 ? launch_gemm_t<1>(tmW, tmS, p, grid, cluster, s)
+                    : launch_gemm_t<2>(tmW, tmS, p, grid, cluster, s);
 }
 
 int gemm_blocks_per_sm(int fmt) {

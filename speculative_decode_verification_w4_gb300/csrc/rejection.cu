@@ -127,15 +127,10 @@ __device__ __forceinline__ unsigned long long kept(unsigned long long W, int v, 
     return (W > s.tau || (W == s.tau && v <= s.cut)) ? W : 0ull;
 }
 
-// Log-scale bucket of W > 0: exact below 16, then the binade and 3 more bits.
-__device__ __forceinline__ int log_bucket(unsigned long long W) {
-    if (W < 16ull) return static_cast<int>(W);
-    const int msb = 63 - __clzll(static_cast<long long>(W));
-    return 16 + (msb - 4) * 8 + static_cast<int>((W >> (msb - 3)) & 7ull);
-}
-
-// log_bucket(floor(f)) for f = e * 2^40 >= 1, from the float's bits: every
-// bucket edge at or above 16 is an integer, so floor() never crosses one.
+// Log-scale bucket of W = floor(f) >= 1, f = e * 2^40: W itself below 16,
+// then 16 + 8 * (binade - 4) + the 3 bits after the leading one.  Computed
+// from the float's bits: every bucket edge at or above 16 is an integer, so
+// floor() never crosses one.
 __device__ __forceinline__ int log_bucket_e(float e) {
     const float f = __fmul_rn(e, 1099511627776.0f);
     if (f < 16.0f) return static_cast<int>(f);

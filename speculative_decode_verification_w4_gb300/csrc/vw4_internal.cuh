@@ -15,6 +15,8 @@ constexpr int kTileRows = 128;     // weight rows per tile
 constexpr int kStageK = 256;       // k elements per pipeline stage
 constexpr int kStages = 4;         // pipeline depth
 constexpr int kMinUnitsPerCta = 4; // tile-aligned split-K: at least this many stages per part
+constexpr int kMaxSplit = 8;       // tile-aligned split-K: at most this many parts
+constexpr int kMaxClusterSplit = 6; // parts combined as one cluster (larger ones place poorly)
 constexpr int kConsumerWarps = 4;  // each owns 32 rows of the tile
 constexpr int kWarpRows = kTileRows / kConsumerWarps;  // 32
 constexpr int kRowBlocks = kWarpRows / 16;             // 16-row MMA blocks per warp
@@ -38,7 +40,8 @@ constexpr int kSSlots = 2;
 constexpr int kSmemS = kStages * kWBytes;
 constexpr int kSmemA = kSmemS + kSSlots * kSSlotBytes;
 constexpr int kSmemBar = kSmemA + kStages * kAStride;
-constexpr int kGemmSmem = kSmemBar + 256 /*barriers, flags*/ + 1024 /*align*/;
+constexpr int kSmemPart = kSmemBar + 256;                // cluster mode: this CTA's partial tile
+constexpr int kGemmSmem = kSmemPart + kMaxRows * kTileRows * 4 + 1024 /*align*/;
 constexpr int kPartialFloats = kMaxRows * kTileRows;   // one partial tile: [8][128]
 
 // A "segment" is the set of verify rows that share one weight matrix: the
@@ -81,6 +84,10 @@ struct GemmParams {
     int32_t* row_argmax;
     uint32_t* status;
     unsigned long long wait_ns;
+    // cluster != 0 (tile-aligned split-K without the fused argmax): the split
+    // parts of a tile are launched as one cluster and combine their partial
+    // tiles over distributed shared memory instead of tickets in L2.
+    int cluster;
 };
 
 // Lays the GEMM/MoE workspace out from `base` (nullptr: size only).
@@ -95,7 +102,7 @@ cudaError_t launch_route(const int32_t* expert_ids, int M, int topk, int E,
                          const GemmWorkspace& ws, uint32_t* status, float* out_zero, int ldo,
                          int N, cudaStream_t s);
 cudaError_t launch_gemm(int fmt, const CUtensorMap& tmW, const CUtensorMap& tmS,
-                        const GemmParams& p, int grid, cudaStream_t s);
+                        const GemmParams& p, int grid, int cluster, cudaStream_t s);
 cudaError_t launch_combine(const float* pair_out, const float* gates, const int32_t* ids,
                            int E, int M, int topk, int N, float* out, int ldo, cudaStream_t s);
 cudaError_t launch_q4_0_split(const uint8_t* blocks, int N, int K, uint8_t* q, __half* d,
