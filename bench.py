@@ -4,16 +4,19 @@
 Workload (one step): the dense-27B-like layer verify -- d = 5120; q, k, v, o
 (5120 -> 6144 / 1024 / 1024, 6144 -> 5120), gate and up (5120 -> 17408) and
 down (17408 -> 5120) -- as nvfp4 weights (N(0, 0.02) quantized), with M = 8
-bf16 N(0, 1) verify rows: seven verify_gemm_w4 calls back to back on one
-stream.  The weights and scales of one step (191.7 MB) exceed the 129 MB L2,
-so every step streams them from HBM.
+bf16 N(0, 1) verify rows.  q/k/v and gate/up read the same input and are
+stored concatenated along N, as inference engines store them, so the step is
+four verify_gemm_w4 calls back to back on one stream (qkv 5120 -> 8192, o,
+gate_up 5120 -> 34816, down).  The weights and scales of one step (191.7 MB)
+exceed the 129 MB L2, so every step streams them from HBM.
 
 Metric: HBM GB/s = algorithmic bytes (packed weights + scales + activations)
 per step / step time, summed over ranks (N independent replicas).  The same
 JSON line carries the per-M microseconds for M = 1, 2, 4, 8 (nvfp4 and Q4_0),
-the accept-step microseconds, the roofline of the GEMM kernel, the end-to-end
-number through the C ABI with host buffers, the CPU oracle baseline and the
-SM clocks seen during the timed region.
+the seven-call (unpacked) layer for comparison, the accept-step
+microseconds, the roofline of the GEMM kernel, the end-to-end number through
+the C ABI with host buffers, the CPU oracle baseline and the SM clocks seen
+during the timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
@@ -34,13 +37,19 @@ if ROOT not in sys.path:
 
 import numpy as np  # noqa: E402
 
+# The seven linears of the layer, and the step as an inference engine stores
+# them: q/k/v and gate/up each read the same input, so their weights sit
+# concatenated along N (one packed matrix, one call each).  The packed step
+# streams the same weight bytes with 4 calls instead of 7.
 LAYER = [("q", 6144, 5120), ("k", 1024, 5120), ("v", 1024, 5120), ("o", 5120, 6144),
          ("gate", 17408, 5120), ("up", 17408, 5120), ("down", 5120, 17408)]
+STEP = [("qkv", 8192, 5120), ("o", 5120, 6144), ("gate_up", 34816, 5120), ("down", 5120, 17408)]
 HEAD_M = 8
 METRIC = "nvfp4 verify-GEMM HBM GB/s & µs/pass at M=1,2,4,8; accept µs/step"
 WORKLOAD = ("dense-27B-like layer verify: d=5120, q/k/v/o 5120->6144/1024/1024 and 6144->5120, "
             "gate/up 5120->17408, down 17408->5120, nvfp4 (E2M1 + E4M3 per 16 + fp32 tensor "
-            "scale), bf16 activations N(0,1), M=8 verify rows; 7 linears per step")
+            "scale), bf16 activations N(0,1), M=8 verify rows; q/k/v and gate/up packed along "
+            "N (qkv 5120->8192, gate_up 5120->34816): 4 verify_gemm_w4 calls per step")
 SPEC_HBM_GBS = 8000.0
 LAUNCHES_PER_GEMM = 2   # activation prep + the GEMM kernel
 
@@ -49,8 +58,8 @@ def weight_bytes(N, K, fmt="nvfp4"):
     return N * K // 2 + (N * K // 16 if fmt == "nvfp4" else N * K // 32 * 2)
 
 
-def step_bytes(M, fmt="nvfp4"):
-    return sum(weight_bytes(N, K, fmt) + M * K * 2 for _, N, K in LAYER)
+def step_bytes(M, fmt="nvfp4", spec=None):
+    return sum(weight_bytes(N, K, fmt) + M * K * 2 for _, N, K in (spec or STEP))
 
 
 KERNEL_SOURCES = ["speculative_decode_verification_w4_gb300/csrc/" + f
@@ -153,11 +162,11 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ inputs
-def make_layer(fmt, device):
+def make_layer(fmt, device, spec=None):
     import torch
     import synth
     layer = []
-    for i, (name, N, K) in enumerate(LAYER):
+    for i, (name, N, K) in enumerate(spec or STEP):
         q, s, ts = synth.linear(100 + i, N, K, fmt)
         qd = torch.from_numpy(q).to(device)
         if fmt == "nvfp4":
@@ -168,12 +177,12 @@ def make_layer(fmt, device):
     return layer
 
 
-def make_acts(M, device, seed=7):
+def make_acts(M, device, seed=7, spec=None):
     import torch
     import synth
     g = synth.rng(seed)
     acts = []
-    for _, N, K in LAYER:
+    for _, N, K in (spec or STEP):
         bits = synth.activations(g, M, K)
         acts.append(torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(device))
     return acts
@@ -187,10 +196,10 @@ def run_ours(args, rank, world, device):
     torch.cuda.set_device(device)
     layers = {"nvfp4": make_layer("nvfp4", device), "q4_0": make_layer("q4_0", device)}
     acts = {M: make_acts(M, device, seed=7 + M) for M in (1, 2, 4, 8)}
-    outs = {M: [torch.empty((M, N), dtype=torch.float32, device=device) for _, N, _ in LAYER]
+    outs = {M: [torch.empty((M, N), dtype=torch.float32, device=device) for _, N, _ in STEP]
             for M in (1, 2, 4, 8)}
     ws = vw4.Workspace(device)
-    ws.get(max(vw4.vw4_workspace_bytes(vw4.OP_GEMM, 8, N, K) for _, N, K in LAYER))
+    ws.get(max(vw4.vw4_workspace_bytes(vw4.OP_GEMM, 8, N, K) for _, N, K in STEP + LAYER))
     FMTS = {"nvfp4": vw4.FMT_NVFP4, "q4_0": vw4.FMT_Q4_0}
 
     def one_step(fmt, M):
@@ -227,11 +236,27 @@ def run_ours(args, rank, world, device):
         barrier()
         return e0.elapsed_time(e1)
 
+    def time_alone(fmt, name, N, K, qd, sd, ts, A, out, steps):
+        """One call timed alone: a graph of R calls on R different weight copies
+        (more than 2x L2 of weights in flight, so nothing is served from L2)."""
+        R = max(4, int(np.ceil(320e6 / weight_bytes(N, K, fmt))))
+        copies = [(qd.clone(), sd.clone()) for _ in range(R)]
+
+        def calls():
+            for (qc, sc) in copies:
+                vw4.verify_gemm_w4(FMTS[fmt], qc, sc, ts, A, out=out, workspace=ws)
+        gl = capture(calls, warm=1)
+        reps = max(2, int(np.ceil(steps / 4)))
+        us = time_graph(gl, reps, 1) / (reps * R) * 1e3
+        del gl, copies
+        torch.cuda.empty_cache()
+        return round(us, 2)
+
     steps, warmup = args.steps, args.warmup
     peak, peak_kind = read_peaks()
     with ClockSampler(torch.cuda.current_device()) as clk:
-        # headline: one step = the 7 nvfp4 linears at M = 8 (a CUDA graph of the
-        # seven C-ABI calls, replayed K times back to back)
+        # headline: one step = the packed layer at M = 8 (a CUDA graph of the
+        # four C-ABI calls, replayed K times back to back)
         g_head = capture(lambda: one_step("nvfp4", HEAD_M))
         soak_end = time.time() + 0.4
         while time.time() < soak_end:      # let the clock sampler see the load
@@ -243,7 +268,8 @@ def run_ours(args, rank, world, device):
         ms_per_step = ms_max / steps
         value = step_bytes(HEAD_M) * steps * world / (ms_max * 1e-3) / 1e9
 
-        # per-M microseconds of the whole layer (graph of the step), both formats
+        # per-M microseconds of the packed layer (graph of the step), both
+        # formats, and of each of its calls alone
         per_m = {}
         for fmt in ("nvfp4", "q4_0"):
             per_m[fmt] = {}
@@ -253,46 +279,51 @@ def run_ours(args, rank, world, device):
                 per_m[fmt][str(M)] = {
                     "layer_us": round(m_ms / steps * 1e3, 2),
                     "layer_gbs": round(step_bytes(M, fmt) / (m_ms / steps * 1e-3) / 1e9, 1),
-                    "linear_us": {}}
+                    "call_us": {}}
                 del gm
-
-        # each linear alone: a graph of R calls on R different weight copies
-        # (more than 2x L2 of weights in flight, so nothing is served from L2)
-        for fmt in ("nvfp4", "q4_0"):
             for j, (name, N, K, qd, sd, ts) in enumerate(layers[fmt]):
-                R = max(4, int(np.ceil(320e6 / weight_bytes(N, K, fmt))))
-                copies = [(qd.clone(), sd.clone()) for _ in range(R)]
                 for M in (1, 2, 4, 8):
-                    def calls(M=M, copies=copies):
-                        for (qc, sc) in copies:
-                            vw4.verify_gemm_w4(FMTS[fmt], qc, sc, ts, acts[M][j],
-                                               out=outs[M][j], workspace=ws)
-                    gl = capture(calls, warm=1)
-                    reps = max(2, int(np.ceil(steps / 4)))
-                    l_ms = time_graph(gl, reps, 1)
-                    per_m[fmt][str(M)]["linear_us"][name] = round(l_ms / (reps * R) * 1e3, 2)
-                    del gl
-                del copies
-                torch.cuda.empty_cache()
+                    per_m[fmt][str(M)]["call_us"][name] = time_alone(
+                        fmt, name, N, K, qd, sd, ts, acts[M][j], outs[M][j], steps)
+
+        # the same layer as seven separate calls (no packing), nvfp4
+        unpacked = {}
+        lay7 = make_layer("nvfp4", device, LAYER)
+        for M in (1, 8):
+            a7 = make_acts(M, device, seed=17 + M, spec=LAYER)
+            o7 = [torch.empty((M, N), dtype=torch.float32, device=device) for _, N, _ in LAYER]
+
+            def step7(a7=a7, o7=o7):
+                for j, (name, N, K, qd, sd, ts) in enumerate(lay7):
+                    vw4.verify_gemm_w4(vw4.FMT_NVFP4, qd, sd, ts, a7[j], out=o7[j], workspace=ws)
+            g7 = capture(step7)
+            m7 = time_graph(g7, steps, 3)
+            del g7
+            unpacked[str(M)] = {
+                "layer_us": round(m7 / steps * 1e3, 2),
+                "layer_gbs": round(step_bytes(M, "nvfp4", LAYER) / (m7 / steps * 1e-3) / 1e9, 1),
+                "linear_us": {name: time_alone("nvfp4", name, N, K, qd, sd, ts, a7[j], o7[j], steps)
+                              for j, (name, N, K, qd, sd, ts) in enumerate(lay7)}}
+        del lay7
+        torch.cuda.empty_cache()
 
     gate = {}
-    for name in ("gate", "up", "down"):
-        t1 = per_m["nvfp4"]["1"]["linear_us"][name]
-        t8 = per_m["nvfp4"]["8"]["linear_us"][name]
-        N, K = [(n, k) for nm, n, k in LAYER if nm == name][0]
+    for name in ("qkv", "o", "gate_up", "down"):
+        t1 = per_m["nvfp4"]["1"]["call_us"][name]
+        t8 = per_m["nvfp4"]["8"]["call_us"][name]
+        N, K = [(n, k) for nm, n, k in STEP if nm == name][0]
         gbs = (weight_bytes(N, K) + 8 * K * 2) / (t8 * 1e-6) / 1e9
         gate[name] = {"m8_over_m1": round(t8 / t1, 3), "m8_gbs": round(gbs, 1),
                       "frac_of_8tbs": round(gbs / SPEC_HBM_GBS, 3),
                       "frac_of_measured_copy": round(gbs / peak, 3)}
 
-    # roofline of the GEMM kernel: algorithmic bytes of the 7 linears at M = 8
-    # over their per-launch times (each timed alone, graph replay, CUDA events)
-    t_lin = per_m["nvfp4"]["8"]["linear_us"]
-    achieved = sum(weight_bytes(N, K) + HEAD_M * K * 2 for _, N, K in LAYER) / (
-        sum(t_lin[n] for n, _, _ in LAYER) * 1e-6) / 1e9
+    # roofline of the GEMM: algorithmic bytes of the step's calls at M = 8 over
+    # their times, each call timed alone (graph replay, CUDA events)
+    t_call = per_m["nvfp4"]["8"]["call_us"]
+    achieved = step_bytes(HEAD_M) / (sum(t_call[n] for n, _, _ in STEP) * 1e-6) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": measured_traffic(),
-                "per": "layer step: the 7 GEMM calls at M = 8 (bytes, time, traffic)",
+                "per": "layer step: the 4 GEMM calls at M = 8 (bytes, time, traffic)",
                 "peak_kind": f"of {peak_kind} (STREAM-style copy, burst)",
                 "kernel": "vw4::gemm_w4_kernel<nvfp4> (with its activation-prep launch)",
                 "per_unit": "0.5625 B per weight (nibble + e4m3/16) + 2*M B per k of activations"}
@@ -310,10 +341,11 @@ def run_ours(args, rank, world, device):
         "config": {"workload": WORKLOAD, "M": HEAD_M, "fmt": "nvfp4",
                    "bytes_per_step": step_bytes(HEAD_M),
                    "l2": "inputs larger than L2: 191.7 MB of weights+scales per step vs 129 MB L2",
-                   "timing": "CUDA graph of the step's 7 C-ABI calls, replayed back to back",
+                   "timing": "CUDA graph of the step's 4 C-ABI calls, replayed back to back",
                    "parallelism": f"replicas x{world}"},
-        "per_m": per_m, "gate": gate, "accept_us": accept, "roofline": roofline, "e2e": e2e,
-        "gpu_launches": steps * len(LAYER) * LAUNCHES_PER_GEMM,
+        "per_m": per_m, "unpacked_7_calls": unpacked, "gate": gate, "accept_us": accept,
+        "roofline": roofline, "e2e": e2e,
+        "gpu_launches": steps * len(STEP) * LAUNCHES_PER_GEMM,
         "clocks": clk.summary(),
     }
     return result
@@ -401,8 +433,8 @@ def run_e2e(vw4, layer, device, stream, steps, warmup, world):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = reduce_max(e0.elapsed_time(e1), world)
-    h2d = sum(M * K * 2 for _, N, K in LAYER)
-    d2h = sum(M * N * 4 for _, N, K in LAYER)
+    h2d = sum(M * K * 2 for _, N, K in STEP)
+    d2h = sum(M * N * 4 for _, N, K in STEP)
     value = step_bytes(M) * steps * world / (ms * 1e-3) / 1e9
     return {"value": round(value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h}
@@ -410,23 +442,23 @@ def run_e2e(vw4, layer, device, stream, steps, warmup, world):
 
 # ------------------------------------------------------- CPU oracle timing
 class OracleWorkload:
-    """The same layer for the CPU oracle: all seven nvfp4 linears generated
+    """The same packed layer for the CPU oracle: its four nvfp4 matrices generated
     once; a "sample" is a random subset of output rows of every linear."""
 
     def __init__(self):
         import oracle
         import synth
         oracle.build()
-        self.lin = [synth.linear(100 + i, N, K, "nvfp4") for i, (_, N, K) in enumerate(LAYER)]
+        self.lin = [synth.linear(100 + i, N, K, "nvfp4") for i, (_, N, K) in enumerate(STEP)]
         g = synth.rng(11)
-        self.acts = [synth.activations(g, HEAD_M, K) for _, N, K in LAYER]
+        self.acts = [synth.activations(g, HEAD_M, K) for _, N, K in STEP]
 
     def run(self, frac: float, seed: int):
         """Returns (GB/s over the sampled algorithmic bytes, rows, seconds)."""
         import oracle
         g = np.random.default_rng(seed)
         rows, secs, nbytes = 0, 0.0, 0
-        for (name, N, K), (q, s, ts), A in zip(LAYER, self.lin, self.acts):
+        for (name, N, K), (q, s, ts), A in zip(STEP, self.lin, self.acts):
             n = max(1, int(round(N * frac)))
             cols = np.sort(g.choice(N, n, replace=False)).astype(np.int32)
             t = time.perf_counter()
@@ -491,8 +523,8 @@ def run_reference(args, rank, world):
         vals.append(v)
     wall = time.perf_counter() - t0
     value = statistics.mean(vals)
-    what = (f"a {frac:.4%} random subset of the output rows of all 7 linears" if frac <= 1.0
-            else f"all 7 linears, {int(round(frac))} times")
+    what = (f"a {frac:.4%} random subset of the output rows of the layer's 4 packed matrices" if frac <= 1.0
+            else f"the whole packed layer, {int(round(frac))} times")
     sample = f"each step: {what} ({rows} rows), M=8, nvfp4; fp64 dequantize-and-dot"
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
@@ -509,9 +541,9 @@ def run_reference(args, rank, world):
 
 def run_case(case: str, device):
     """Profiling helper: a few calls of the GEMM on a fixed case, nothing timed
-    or printed but a one-line summary.  'dense' = the 7 nvfp4 linears of the
-    layer at M = 8 (3 warm-up passes, then 1); 'N,K,M' = one nvfp4 GEMM of that
-    shape (3 warm-up calls, then 1)."""
+    or printed but a one-line summary.  'dense' = the 4 nvfp4 calls of the
+    packed layer step at M = 8 (3 warm-up passes, then 1); 'N,K,M' = one nvfp4
+    GEMM of that shape (3 warm-up calls, then 1)."""
     import torch
     import speculative_decode_verification_w4_gb300 as vw4
     torch.cuda.set_device(device)
@@ -574,8 +606,8 @@ def main():
         wl = OracleWorkload()
         frac = wl.frac_for(args.cpu_budget)
         v, rows, secs = wl.run_budget(frac, 7)
-        what = (f"{frac:.4%} of the output rows of all 7 linears" if frac <= 1.0
-                else f"all 7 linears, {int(round(frac))} times")
+        what = (f"{frac:.4%} of the output rows of the layer's 4 packed matrices" if frac <= 1.0
+                else f"the whole packed layer, {int(round(frac))} times")
         res["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cpu_cores(),
                                "kind": "oracle",
                                "sample": f"{what} ({rows} rows, {secs:.1f} s), M=8, nvfp4, "

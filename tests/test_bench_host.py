@@ -52,6 +52,12 @@ def test_step_bytes_counts_weights_scales_and_activations():
     # q: 6144 x 5120 nvfp4 = 0.5625 B per weight, plus M*K*2 activation bytes
     assert bench.weight_bytes(6144, 5120) == 6144 * 5120 * 9 // 16
     assert bench.weight_bytes(6144, 5120, "q4_0") == 6144 * 5120 * 9 // 16
-    total = sum(n * k * 9 // 16 + 8 * k * 2 for _, n, k in bench.LAYER)
+    total = sum(n * k * 9 // 16 + 8 * k * 2 for _, n, k in bench.STEP)
     assert bench.step_bytes(8) == total
-    assert abs(bench.step_bytes(8) / 1e6 - 192.5) < 0.1
+    assert abs(bench.step_bytes(8) / 1e6 - 192.2) < 0.1
+    # the packed step holds exactly the seven linears' weights; the shared
+    # inputs of q/k/v and gate/up are read once instead of three and two times
+    w7 = sum(n * k * 9 // 16 for _, n, k in bench.LAYER)
+    w4 = sum(n * k * 9 // 16 for _, n, k in bench.STEP)
+    assert w7 == w4
+    assert bench.step_bytes(8, spec=bench.LAYER) - total == 8 * 5120 * 2 * 3
