@@ -330,6 +330,7 @@ def run_ours(args, rank, world, device):
 
     stream = torch.cuda.current_stream()
     accept = run_accept_timings(device, stream)
+    heads = run_head_timings(device, stream)
     e2e = run_e2e(vw4, layers["nvfp4"], device, stream, steps, warmup, world)
 
     result = {
@@ -344,6 +345,7 @@ def run_ours(args, rank, world, device):
                    "timing": "CUDA graph of the step's 4 C-ABI calls, replayed back to back",
                    "parallelism": f"replicas x{world}"},
         "per_m": per_m, "unpacked_7_calls": unpacked, "gate": gate, "accept_us": accept,
+        "heads": heads,
         "roofline": roofline, "e2e": e2e,
         "gpu_launches": steps * len(STEP) * LAUNCHES_PER_GEMM,
         "clocks": clk.summary(),
@@ -394,6 +396,104 @@ def run_accept_timings(device, stream):
     e1.record(stream)
     torch.cuda.synchronize()
     out["greedy_lmhead_unfused"] = {"us": round(e0.elapsed_time(e1) / reps * 1e3, 2)}
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_head_timings(device, stream):
+    """The two other verify configurations, timed with CUDA events:
+    * MoE head: 128 experts, top-8, d = 2048, expert gate/up 2048 -> 768 each
+      (stacked) and down 768 -> 2048, nvfp4, M = 8 tokens with seeded top-8
+      routing: the pair GEMM and the down GEMM with the gate combine (the
+      silu(gate) * up between them is harness work, made once);
+    * LM head 5376 -> 262144 nvfp4, M = 8, with the fused argmax, and the
+      greedy accept of 7 drafts from that argmax.
+    Two weight copies alternate, so that nothing is served from L2."""
+    import torch
+    import synth
+    import speculative_decode_verification_w4_gb300 as vw4
+    out = {}
+    stream = torch.cuda.Stream(device)  # graphs are captured off the default stream
+    torch.cuda.synchronize()
+    E, d, f, M, topk = 128, 2048, 768, 8, 8
+    gu = [synth.linear(200 + c, E * 2 * f, d, "nvfp4") for c in range(2)]
+    dn = [synth.linear(210 + c, E * d, f, "nvfp4") for c in range(2)]
+    gu = [(torch.from_numpy(q).to(device), torch.from_numpy(sc).to(device), ts) for q, sc, ts in gu]
+    dn = [(torch.from_numpy(q).to(device), torch.from_numpy(sc).to(device), ts) for q, sc, ts in dn]
+    ids, gates = synth.routing(300, M, E, topk)
+    ids_d = torch.from_numpy(np.ascontiguousarray(ids, np.int32)).to(device)
+    gates_d = torch.from_numpy(np.ascontiguousarray(gates, np.float32)).to(device)
+    A = torch.from_numpy(synth.activations(synth.rng(301), M, d).view(np.int16)).view(
+        torch.bfloat16).to(device)
+    pair = torch.empty((M * topk, 2 * f), dtype=torch.float32, device=device)
+    res = torch.empty((M, d), dtype=torch.float32, device=device)
+    g0, u0 = pair[:, :f], pair[:, f:]
+    ws = vw4.Workspace(device)
+    vw4.verify_moe_w4(vw4.FMT_NVFP4, *gu[0], E, A, 0, ids_d, gates_d, 0, out=pair, workspace=ws,
+                      stream=stream)
+    h = (torch.nn.functional.silu(g0) * u0).to(torch.bfloat16).contiguous()
+
+    def moe(c):
+        vw4.verify_moe_w4(vw4.FMT_NVFP4, *gu[c], E, A, 0, ids_d, gates_d, 0, out=pair,
+                          workspace=ws, stream=stream)
+        vw4.verify_moe_w4(vw4.FMT_NVFP4, *dn[c], E, h, 1, ids_d, gates_d, 1, out=res,
+                          workspace=ws, stream=stream)
+
+    def timed(fn, reps):
+        """Microseconds per fn call: a CUDA graph of fn(0), fn(1) (the two
+        weight copies), replayed reps times (no host work in the timed loop)."""
+        for c in range(4):
+            fn(c % 2)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn(0)
+            fn(1)
+        with torch.cuda.stream(stream):  # replays and events on one stream
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / (2 * reps) * 1e3
+
+    us = timed(moe, 20)
+    n_exp = len(set(int(x) for x in ids.reshape(-1)))
+    moe_bytes = n_exp * (2 * f * d + d * f) * 9 // 16 + (M * d + M * topk * f) * 2
+    out["moe_head_m8"] = {"us": round(us, 2), "distinct_experts": n_exp,
+                          "gbs": round(moe_bytes / (us * 1e-6) / 1e9, 1)}
+    del gu, dn, pair, res, h
+    torch.cuda.empty_cache()
+
+    V, K = 262144, 5376
+    heads = [synth.linear(220 + c, V, K, "nvfp4") for c in range(2)]
+    heads = [(torch.from_numpy(q).to(device), torch.from_numpy(sc).to(device), ts)
+             for q, sc, ts in heads]
+    Ah = torch.from_numpy(synth.activations(synth.rng(222), 8, K).view(np.int16)).view(
+        torch.bfloat16).to(device)
+    logits = torch.empty((8, V), dtype=torch.float32, device=device)
+    am = torch.empty((8,), dtype=torch.int32, device=device)
+    vw4.verify_gemm_w4(vw4.FMT_NVFP4, *heads[0], Ah, out=logits, row_argmax=am, workspace=ws,
+                       stream=stream)
+    torch.cuda.synchronize()
+    drafts = am[:7].clone().reshape(1, 7)   # every draft agrees: the whole run commits
+    tokens = torch.empty((1, 8), dtype=torch.int32, device=device)
+    length = torch.empty((1,), dtype=torch.int32, device=device)
+
+    def head(c):
+        vw4.verify_gemm_w4(vw4.FMT_NVFP4, *heads[c], Ah, out=logits, row_argmax=am,
+                           workspace=ws, stream=stream)
+        vw4.accept_greedy(None, drafts, target_argmax=am, B=1, V=V, tokens=tokens,
+                          length=length, stream=stream)
+
+    us = timed(head, 10)
+    hb = weight_bytes(V, K) + 8 * K * 2
+    out["lmhead_fused_greedy_m8"] = {"us": round(us, 2), "gbs": round(hb / (us * 1e-6) / 1e9, 1)}
+    del heads, logits
     torch.cuda.empty_cache()
     return out
 

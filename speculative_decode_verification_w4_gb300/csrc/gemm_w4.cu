@@ -219,49 +219,59 @@ __global__ void __launch_bounds__(256) prep_act_kernel(
 
 // ------------------------------------------------------------ MoE router
 // Stable counting sort of the routed pairs by expert into segments of at
-// most 8 rows (one thread; at most 64 pairs).  Pairs with an invalid expert
-// are dropped, flagged, and their direct output rows zeroed.
+// most 8 rows, one thread per pair (at most 64): a pair's segment is the
+// number of segments of the smaller expert ids plus its rank among the pairs
+// of its own expert, divided by 8.  Segments come out ordered by expert id,
+// and inside an expert by pair index.  Pairs with an invalid expert are
+// dropped, flagged, and their direct output rows zeroed.
 __global__ void route_kernel(const int32_t* __restrict__ ids, int P, int E, SegTable* seg,
                              uint32_t* status, float* out_zero, int ldo, int N) {
     __shared__ int s_ids[kMaxSeg];
+    __shared__ int s_cnt[kMaxSeg];    // pairs of this pair's expert
+    __shared__ int s_first[kMaxSeg];  // this pair is its expert's first
     __shared__ int s_bad[kMaxSeg];
-    __shared__ int s_nbad;
+    __shared__ int s_nbad, s_nseg;
     const int tid = threadIdx.x;
+    if (tid == 0) {
+        s_nbad = 0;
+        s_nseg = 0;
+    }
     if (tid < P) s_ids[tid] = ids[tid];
     __syncthreads();
-    if (tid == 0) {
-        int order[kMaxSeg];
-        int cnt = 0, nbad = 0;
-        for (int p = 0; p < P; ++p) {
-            const int e = s_ids[p];
-            if (e < 0 || e >= E) {
-                s_bad[nbad++] = p;
-                continue;
-            }
-            int j = cnt++;
-            while (j > 0 && s_ids[order[j - 1]] > e) {  // stable insertion
-                order[j] = order[j - 1];
-                --j;
-            }
-            order[j] = p;
+    int e = -1, rank = 0, valid = 0;
+    if (tid < P) {
+        e = s_ids[tid];
+        valid = (e >= 0 && e < E) ? 1 : 0;
+        int cnt = 0;
+        for (int q = 0; q < P; ++q) {
+            const int same = s_ids[q] == e ? 1 : 0;
+            cnt += same;
+            rank += (same && q < tid) ? 1 : 0;
         }
-        int ns = 0;
-        for (int i = 0; i < cnt;) {
-            const int e = s_ids[order[i]];
-            int c = 0;
-            while (i < cnt && s_ids[order[i]] == e && c < kMaxRows) {
-                seg->dest[ns][c++] = order[i++];
-            }
-            for (int j = c; j < kMaxRows; ++j) seg->dest[ns][j] = 0;
-            seg->expert[ns] = e;
-            seg->count[ns] = c;
-            ++ns;
-        }
-        seg->n_seg = ns;
-        s_nbad = nbad;
-        if (nbad) atomicOr(status, kStatusBadExpert);
+        s_cnt[tid] = cnt;
+        s_first[tid] = (valid && rank == 0) ? 1 : 0;
+        if (!valid) s_bad[atomicAdd(&s_nbad, 1)] = tid;
     }
     __syncthreads();
+    if (tid < P && valid) {
+        int base = 0;  // segments of the smaller expert ids
+        for (int q = 0; q < P; ++q)
+            if (s_first[q] && s_ids[q] < e) base += (s_cnt[q] + kMaxRows - 1) / kMaxRows;
+        const int sgi = base + rank / kMaxRows, slot = rank % kMaxRows;
+        seg->dest[sgi][slot] = tid;
+        if (slot == 0) {
+            const int c = min(kMaxRows, s_cnt[tid] - rank);
+            seg->expert[sgi] = e;
+            seg->count[sgi] = c;
+            for (int j = c; j < kMaxRows; ++j) seg->dest[sgi][j] = 0;
+        }
+        if (s_first[tid]) atomicAdd(&s_nseg, (s_cnt[tid] + kMaxRows - 1) / kMaxRows);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        seg->n_seg = s_nseg;
+        if (s_nbad) atomicOr(status, kStatusBadExpert);
+    }
     if (out_zero != nullptr) {
         for (int b = 0; b < s_nbad; ++b) {
             float* row = out_zero + (size_t)s_bad[b] * ldo;
