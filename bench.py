@@ -643,11 +643,27 @@ def run_case(case: str, device):
     """Profiling helper: a few calls of the GEMM on a fixed case, nothing timed
     or printed but a one-line summary.  'dense' = the 4 nvfp4 calls of the
     packed layer step at M = 8 (3 warm-up passes, then 1); 'N,K,M' = one nvfp4
-    GEMM of that shape (3 warm-up calls, then 1)."""
+    GEMM of that shape (3 warm-up calls, then 1); 'rejection:K' = the
+    rejection accept of the stochastic sweep (B = 256, V = 151936, K drafts),
+    4 calls."""
     import torch
     import speculative_decode_verification_w4_gb300 as vw4
     torch.cuda.set_device(device)
     ws = vw4.Workspace(device)
+    if case.startswith("rejection:"):  # the stochastic sweep's accept step, K drafts
+        Kd, B, V = int(case.split(":")[1]), 256, 151936
+        g = torch.Generator(device=device).manual_seed(4)
+        tgt = torch.randn((B, Kd + 1, V), generator=g, device=device) * 3.0
+        drf = tgt[:, :Kd] + torch.randn((B, Kd, V), generator=g, device=device)
+        probs = torch.softmax(drf.reshape(-1, V) / 0.6, dim=-1)
+        drafts = torch.multinomial(probs, 1, generator=g).reshape(B, Kd).to(torch.int32)
+        del probs
+        for r in range(4):
+            tok, ln = vw4.accept_rejection(tgt, drf, drafts, 0.6, 0.95, 4, r, workspace=ws)
+        torch.cuda.synchronize()
+        print(f"case {case}: 4 calls, mean run {ln.float().mean().item():.3f}, device status "
+              f"{vw4.vw4_get_device_status()}", flush=True)
+        return
     if case == "dense":
         layer = make_layer("nvfp4", device)
         acts = make_acts(HEAD_M, device, seed=7 + HEAD_M)
@@ -677,7 +693,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--case", default=None,
-                    help="profiling helper: 'dense' or 'N,K,M' (see run_case); no JSON line")
+                    help="profiling helper: 'dense', 'N,K,M' or 'rejection:K' (see run_case); "
+                         "no JSON line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
