@@ -17,17 +17,19 @@
 //   residual  r_v = max(0, p_v * Sq - q_v * Sp), inverse CDF with a 64-bit
 //   uniform; bonus from p_Kd when every draft is accepted.
 //
-// Kernel 1 (row_kernel), one thread-block cluster per logits row -- every
-// target row (b, i <= Kd) and every draft row (b, i < Kd) independently:
-//   * the row is read once from HBM into the cluster's shared memory, a
-//     slice per CTA; max and sum W over the cluster (DSMEM);
-//   * the top-p cut: a log-scale histogram of the mass of the entries at or
-//     above c = floor((2^32 - P) * S / (V * 2^32)) -- every entry below c lies
-//     in the dropped tail, because all of them together weigh less than
-//     (1 - P/2^32) * S -- finds the bucket where the kept prefix ends; its
-//     members are sorted by (W desc, index asc) and scanned, which gives the
-//     exact cut (an exact radix search over the slices is the fallback when
-//     that bucket is too crowded);
+// Kernel 1 (row_kernel), one CTA per logits row -- every target row
+// (b, i <= Kd) and every draft row (b, i < Kd) independently; the row is
+// streamed three times (the second and third mostly from L2):
+//   * the max;
+//   * own_exp, sum W, and a log-scale histogram of the mass of the entries
+//     at or above c0 = floor((2^32 - P) * 2^40 / (V * 2^32)) -- every entry
+//     below it lies in the dropped tail, because all of them together weigh
+//     less than (1 - P/2^32) * S (S >= 2^40, the top entry's own mass) -- in
+//     one private copy per warp; the merged suffix sums give the bucket where
+//     the kept prefix ends;
+//   * that bucket's members (a scaled-logit window, then the exact test),
+//     sorted by (W desc, index asc) and scanned, which gives the exact cut
+//     (an exact radix search is the fallback when the bucket is crowded);
 //   * (max, tau, cut, kept sum) of the row go to the workspace.
 // Kernel 2 (seq_kernel), one CTA per sequence: the acceptance tests in
 // order (Philox block (i, b)), then one ordered draw over the row it needs --
@@ -35,35 +37,25 @@
 // committed run.  The draw skips, with two flops, every entry whose logit is
 // too small to be kept (a bound below the cut with a 1e-3 margin in the
 // exponent), so it streams the row once at memory speed.
-#include <cooperative_groups.h>
-
 #include <cmath>
 
 #include "ptx.cuh"
 #include "vw4_internal.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace vw4 {
 
 namespace {
 
 constexpr uint32_t kStatusBadDraft = 0x1u;
-constexpr uint32_t kStatusTimeout = 0x4u;
 constexpr uint32_t kStatusZeroResidual = 0x8u;
 constexpr int kThreads = 512;  // both kernels
 constexpr int kWarps = kThreads / 32;
 constexpr int kLogBuckets = 16 + 37 * 8;  // exact 0..15, then 8 per binade up to 2^40
 constexpr int kLinBuckets = 256;
-constexpr int kCandLocal = 512;    // candidates one CTA may hold per row
-constexpr int kCandTotal = 1024;   // candidates the cluster may gather per row
+constexpr int kCandTotal = 1024;   // crossing-bucket members a row may gather
 constexpr int kRankSortMax = 128;  // up to this many: sort by counting ranks
-constexpr int kListCap = 4096;     // entries >= c0 one CTA lists; more: scan the slice
-constexpr int kExpBatch = 8;       // entries per thread per step of the exp pass
-constexpr int kMaxSlice = 20480;   // floats per CTA (one row on chip)
 constexpr unsigned long long kKeepAll = 1ull << 32;
-static_assert(kThreads >= kLogBuckets, "one thread per log bucket in the suffix scan");
-static_assert(kThreads >= kLinBuckets, "one thread per radix bucket");
+static_assert(kThreads >= kMaxRows + 1, "one thread per acceptance test");
 
 typedef unsigned __int128 u128;
 
@@ -204,11 +196,12 @@ __device__ __forceinline__ u128 scale_u64(unsigned long long u, u128 R) {
     return (lo >> 64) + hi;
 }
 
-// Scratch of the block-wide reductions.
+// Scratch of the block-wide reductions (up to 32 warps; loops use the
+// block's own warp count).
 struct Red {
-    unsigned long long w[kWarps];
-    unsigned long long w2[kWarps];
-    float f[kWarps];
+    unsigned long long w[32];
+    unsigned long long w2[32];
+    float f[32];
 };
 
 __device__ __forceinline__ float block_max(float v, Red& sm) {
@@ -218,7 +211,7 @@ __device__ __forceinline__ float block_max(float v, Red& sm) {
     if (lane == 0) sm.f[wid] = v;
     __syncthreads();
     float m = -INFINITY;
-    for (int w = 0; w < kWarps; ++w) m = fmaxf(m, sm.f[w]);
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) m = fmaxf(m, sm.f[w]);
     __syncthreads();
     return m;
 }
@@ -230,7 +223,7 @@ __device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v
     if (lane == 0) sm.w[wid] = v;
     __syncthreads();
     unsigned long long t = 0;
-    for (int w = 0; w < kWarps; ++w) t += sm.w[w];
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t += sm.w[w];
     __syncthreads();
     return t;
 }
@@ -250,7 +243,7 @@ __device__ __forceinline__ u128 block_excl_u128(u128 v, Red& sm, u128& total) {
     }
     __syncthreads();
     u128 base = 0, t = 0;
-    for (int w = 0; w < kWarps; ++w) {
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) {
         const u128 x = (static_cast<u128>(sm.w2[w]) << 64) | sm.w[w];
         if (w < wid) base += x;
         t += x;
@@ -272,87 +265,79 @@ __device__ __forceinline__ void atomic_add_u64_split(unsigned long long* a, unsi
     if (hi + carry) atomicAdd(&w[1], hi + carry);
 }
 
-// Adds, for every member lane (in), W to mass[bk] (and 1 to cnt[bk] unless
-// cnt is null).  Lanes of one bucket add their sum once: a row whose entries
-// share few buckets would otherwise serialise on a handful of addresses.
-// Called by all 32 lanes.
-__device__ __forceinline__ void warp_bucket_add(bool in, int bk, unsigned long long W, int lane,
-                                                unsigned int* cnt, unsigned long long* mass) {
-    const int key = in ? bk : -1 - lane;  // non-members: groups of one
-    const unsigned int peers = __match_any_sync(0xffffffffu, key);
-    unsigned int m = in ? peers : 0u;
-    unsigned long long sum = 0;
-    while (__any_sync(0xffffffffu, m != 0u)) {
-        const int src = m ? __ffs(m) - 1 : lane;
-        const unsigned long long x = __shfl_sync(0xffffffffu, W, src);
-        if (m) {
-            sum += x;
-            m &= m - 1u;
-        }
-    }
-    if (in && lane == __ffs(peers) - 1) {
-        atomic_add_u64_split(&mass[bk], sum);
-        if (cnt) atomicAdd(&cnt[bk], static_cast<unsigned int>(__popc(peers)));
-    }
-}
+// One CTA per logits row.  The row is streamed three times (the second and
+// third from L2): the max; own_exp, sum W and the mass histogram of the
+// entries >= c0; the members of the crossing bucket.
+constexpr int kRowThreads = 1024;
+constexpr int kRowWarps = kRowThreads / 32;
+static_assert(kRowThreads >= kLogBuckets, "one thread per log bucket in the suffix scan");
 
 struct RowSmem {
     Red red;
-    unsigned int cnt[kLinBuckets];        // radix fallback: this CTA's counts (read by peers)
-    unsigned long long mass[kLogBuckets]; // this CTA's histogram (read by peers)
-    unsigned int mcnt[kLinBuckets];       // the cluster's merged histogram
-    unsigned long long mmass[kLogBuckets];
-    unsigned long long cw[kCandLocal];    // this CTA's candidates (read by rank 0)
-    int ci[kCandLocal];
-    union {
-        struct {
-            unsigned long long w[kCandTotal];  // rank 0: gathered, sorted candidates
-            int i[kCandTotal];
-        } g;
-        struct {
-            int k[kListCap];  // slice indices of this CTA's entries with W >= c0
-        } l;
-    } u;
-    unsigned int nlist;
-    // values peers read over DSMEM
-    float lmax;
-    unsigned long long lsum;
+    unsigned long long whist[kRowWarps][kLogBuckets];  // per-warp mass histograms
+    unsigned long long mass[kLogBuckets];             // merged
+    unsigned int cnt[kLinBuckets];                    // radix fallback: counts
+    unsigned long long lmass[kLinBuckets];            //                 masses
+    unsigned long long cw[kCandTotal];                // crossing-bucket members
+    int ci[kCandTotal];
     unsigned int ncand;
-    int overflow;
-    RowInfo info;  // rank 0's result
-    // broadcast inside the CTA
-    int beta, wbits;
-    unsigned long long lo, width, above, n_eq, count_eq;
-    int cut_found;
+    int beta, wbits, cut_found;
+    unsigned long long above, lo, width, n_eq, count_eq;
+    RowInfo info;
 };
 
-// s holds this CTA's slice [lo, lo + n) of the row's logits on entry and the
-// own_exp values on exit.  The RowInfo returned by rank 0 is the row's; the
-// other CTAs may return before the cut is known.
-__device__ RowInfo row_stats(cg::cluster_group& cl, float* s, int n, int lo, int V, float invT,
-                             unsigned long long P, RowSmem& sm) {
-    const int C = static_cast<int>(cl.num_blocks());
-    const int rank = static_cast<int>(cl.block_rank());
+// f(k, l) for every entry of the row, each thread taking entries in
+// coalesced float4 groups (four loads in flight).
+template <class F>
+__device__ __forceinline__ void stream_row(const float* __restrict__ row, int V, bool vec, F&& f) {
     const int tid = threadIdx.x;
-    const int lane = tid & 31;
+    if (vec) {
+        const float4* r4 = reinterpret_cast<const float4*>(row);
+        const int V4 = V >> 2;
+        int i = tid;
+        for (; i + 3 * kRowThreads < V4; i += 4 * kRowThreads) {
+            const float4 a = __ldg(r4 + i), b = __ldg(r4 + i + kRowThreads),
+                         c = __ldg(r4 + i + 2 * kRowThreads), d = __ldg(r4 + i + 3 * kRowThreads);
+            f(4 * i, a.x); f(4 * i + 1, a.y); f(4 * i + 2, a.z); f(4 * i + 3, a.w);
+            const int j = i + kRowThreads, m = i + 2 * kRowThreads, q = i + 3 * kRowThreads;
+            f(4 * j, b.x); f(4 * j + 1, b.y); f(4 * j + 2, b.z); f(4 * j + 3, b.w);
+            f(4 * m, c.x); f(4 * m + 1, c.y); f(4 * m + 2, c.z); f(4 * m + 3, c.w);
+            f(4 * q, d.x); f(4 * q + 1, d.y); f(4 * q + 2, d.z); f(4 * q + 3, d.w);
+        }
+        for (; i < V4; i += kRowThreads) {
+            const float4 a = __ldg(r4 + i);
+            f(4 * i, a.x); f(4 * i + 1, a.y); f(4 * i + 2, a.z); f(4 * i + 3, a.w);
+        }
+    } else {
+        for (int k = tid; k < V; k += kRowThreads) f(k, __ldg(row + k));
+    }
+}
 
-    // 1. max over the cluster
+// The scaled-logit window [xa, xb) that holds every entry with wlo <= W <
+// whi (1 <= wlo): own_exp is monotone and within 2 ulp of exp, so a margin of
+// 1e-3 in the exponent is far wider than any rounding.
+__device__ __forceinline__ void x_window(unsigned long long wlo, unsigned long long whi, float& xa,
+                                         float& xb) {
+    const float ln2_40 = 27.725887222397812f;
+    xa = __logf(static_cast<float>(wlo)) - ln2_40 - 1e-3f;
+    xb = __logf(static_cast<float>(whi)) - ln2_40 + 1e-3f;
+}
+
+// The row's (max, tau, cut, kept sum); valid in every thread.
+__device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, float invT,
+                             unsigned long long P, RowSmem& sm) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+
+    // 1. max
     float lmax = -INFINITY;
-    for (int k = tid; k < n; k += kThreads) lmax = fmaxf(lmax, s[k]);
-    lmax = block_max(lmax, sm.red);
-    if (tid == 0) sm.lmax = lmax;
-    for (int t = tid; t < kLogBuckets; t += kThreads) sm.mass[t] = 0ull;
-    if (tid == 0) sm.nlist = 0u;
-    cl.sync();
-    float mx = -INFINITY;
-    for (int r = 0; r < C; ++r) mx = fmaxf(mx, *cl.map_shared_rank(&sm.lmax, r));
+    stream_row(row, V, vec, [&](int, float l) { lmax = fmaxf(lmax, l); });
+    const float mx = block_max(lmax, sm.red);
 
-    // 2. e_v, the total mass, and the log-scale mass histogram of the entries
-    //    at or above c0.  Together the entries below c <= (1 - P/2^32) S / V
-    //    weigh less than (1 - P/2^32) S, so they all lie in the dropped tail
-    //    and the cut is at or above c; c0 uses 2^40 (the top entry's mass,
-    //    a lower bound of S) in place of S, so c0 <= c and the histogram of
-    //    the entries >= c0 holds every bucket the cut can be in, exactly.
+    // 2. sum W, and the mass histogram of the entries with W >= c0 (each warp
+    //    its own copy).  The entries below c <= (1 - P/2^32) S / V weigh less
+    //    than (1 - P/2^32) S together, so they all lie in the dropped tail;
+    //    c0 uses 2^40 (the top entry's mass, a lower bound of S) in place of
+    //    S, so c0 <= c and the histogram holds every bucket the cut can be in.
     const bool want_hist = P < kKeepAll;
     const unsigned long long c0 =
         want_hist ? ((kKeepAll - P) << 8) / static_cast<unsigned long long>(V) : 0ull;
@@ -360,201 +345,125 @@ __device__ RowInfo row_stats(cg::cluster_group& cl, float* s, int n, int lo, int
     // e < e_lo proves W < cmin with one compare (e_lo rounds cmin * 2^-40 down)
     const float e_lo = want_hist ? __fmul_rn(__ull2float_rd(cmin), 9.094947017729282379e-13f)
                                  : INFINITY;
-    // Batches of kExpBatch entries per thread: the own_exp chains of a batch
-    // are independent, and the warp reserves list slots once per batch.  The
-    // list takes every entry with e >= e_lo (a superset of W >= c0; the exact
-    // test is made on the listed entries).  sum W is kept per thread as the
-    // sums of the two exact 20-bit halves of each W (each fits in 32 bits).
-    uint32_t sum_hi = 0u, sum_lo = 0u;
-    for (int kb = tid - lane; kb < n; kb += kThreads * kExpBatch) {  // warp-uniform trip count
-        unsigned int ball[kExpBatch];
-        unsigned int tot = 0;
-#pragma unroll
-        for (int j = 0; j < kExpBatch; ++j) {
-            const int k = kb + j * kThreads + lane;
-            float e = 0.0f;
-            if (k < n) {
-                e = own_exp(scaled_x(s[k], mx, invT));
-                s[k] = e;
-            }
-            uint32_t hi, lo;
-            mass_parts(e, hi, lo);
-            sum_hi += hi;
-            sum_lo += lo;
-            ball[j] = __ballot_sync(0xffffffffu, e >= e_lo);
-            tot += __popc(ball[j]);
+    unsigned long long* hist = sm.whist[wid];
+    for (int t = lane; t < kLogBuckets; t += 32) hist[t] = 0ull;
+    __syncwarp();
+    uint32_t sum_hi = 0u, sum_lo = 0u;  // the two exact 20-bit halves of each W
+    stream_row(row, V, vec, [&](int, float l) {
+        const float e = own_exp(scaled_x(l, mx, invT));
+        uint32_t hi, lo;
+        mass_parts(e, hi, lo);
+        sum_hi += hi;
+        sum_lo += lo;
+        if (e >= e_lo) {
+            const unsigned long long W = (static_cast<unsigned long long>(hi) << 20) | lo;
+            if (W >= cmin) atomic_add_u64_split(&hist[log_bucket_e(e)], W);
         }
-        if (tot == 0u) continue;
-        unsigned int base = 0;
-        if (lane == 0) base = atomicAdd(&sm.nlist, tot);
-        base = __shfl_sync(0xffffffffu, base, 0);
-        const unsigned int below = (1u << lane) - 1u;
-#pragma unroll
-        for (int j = 0; j < kExpBatch; ++j) {
-            if ((ball[j] >> lane) & 1u) {
-                const unsigned int slot = base + __popc(ball[j] & below);
-                if (slot < static_cast<unsigned int>(kListCap))
-                    sm.u.l.k[slot] = kb + j * kThreads + lane;
-            }
-            base += __popc(ball[j]);
-        }
-    }
-    unsigned long long lsum = (static_cast<unsigned long long>(sum_hi) << 20) + sum_lo;
-    __syncthreads();
-    const unsigned int nl = sm.nlist;
-    const bool listed = nl <= static_cast<unsigned int>(kListCap);
-    if (listed) {  // the histogram of the listed entries (they crowd a few buckets)
-        for (int t0 = tid - lane; t0 < static_cast<int>(nl); t0 += kThreads) {  // warp-uniform
-            const int t = t0 + lane;
-            const float e = t < static_cast<int>(nl) ? s[sm.u.l.k[t]] : 0.0f;
-            const unsigned long long W = mass_of(e);
-            const bool in = t < static_cast<int>(nl) && W >= cmin;
-            warp_bucket_add(in, in ? log_bucket_e(e) : 0, W, lane, nullptr, sm.mass);
-        }
-    } else {  // too many: scan the slice again, adding per bucket once per warp
-        for (int k0 = tid - lane; k0 < n; k0 += kThreads) {  // warp-uniform trip count
-            const int k = k0 + lane;
-            const float e = k < n ? s[k] : 0.0f;
-            const unsigned long long W = mass_of(e);
-            const bool in = e >= e_lo && W >= cmin;
-            if (__ballot_sync(0xffffffffu, in) == 0u) continue;
-            warp_bucket_add(in, in ? log_bucket_e(e) : 0, W, lane, nullptr, sm.mass);
-        }
-    }
-    lsum = block_sum_u64(lsum, sm.red);
-    if (tid == 0) sm.lsum = lsum;
-    cl.sync();
-    unsigned long long S = 0;
-    for (int r = 0; r < C; ++r) S += *cl.map_shared_rank(&sm.lsum, r);
+    });
+    const unsigned long long S =
+        block_sum_u64((static_cast<unsigned long long>(sum_hi) << 20) + sum_lo, sm.red);
     RowInfo info;
     info.mx = mx;
     if (!want_hist) {
         info.cut = V - 1;
         info.tau = 0;
         info.S = S;
-        cl.sync();  // peers are done reading this CTA's values
         return info;
     }
     const u128 TGT = static_cast<u128>(P) * S;
     // merged bucket masses, then a block-wide suffix sum: the crossing bucket
     // beta is the highest bucket whose suffix mass reaches the target
-    unsigned long long m = 0;
     const int tb = kLogBuckets - 1 - tid;  // thread tid holds bucket 311 - tid
-    if (tb >= 1) {
-        for (int r = 0; r < C; ++r) m += cl.map_shared_rank(&sm.mass[0], r)[tb];
-        sm.mmass[tb] = m;
-    }
+    unsigned long long m = 0;
+    if (tb >= 1)
+        for (int w = 0; w < kRowWarps; ++w) m += sm.whist[w][tb];
     u128 tot_unused;
     const u128 incl = block_excl_u128(static_cast<u128>(m), sm.red, tot_unused) + m;
-    if (tid == 0) {
-        sm.ncand = 0;
-        sm.overflow = 0;
-    }
+    if (tid == 0) sm.ncand = 0;
     if (tb >= 1 && (incl << 32) >= TGT && ((incl - m) << 32) < TGT) {
         sm.beta = tb;
         sm.above = static_cast<unsigned long long>(incl - m);
     }
     __syncthreads();
 
-    // 4. gather the members of the crossing bucket
+    // 3. the members of the crossing bucket.  Members below c0 are not in the
+    //    histogram but are gathered too; they are below the cut and sort
+    //    after it, so the scan below never reaches them.
     const int beta = sm.beta;
     float b_lo, b_hi;  // members of bucket beta: b_lo <= e < b_hi
     bucket_e_range(beta, b_lo, b_hi);
-    // Entries of bucket beta below c0 are not listed; they are below the cut
-    // (c0 <= tau) and sort after it, so the scan below never reaches them.
-    const int n_scan = listed ? static_cast<int>(nl) : n;
-    for (int k0 = tid - lane; k0 < n_scan; k0 += kThreads) {  // warp-uniform trip count
-        const int j = k0 + lane;
-        float e = 0.0f;
-        int k = 0;
-        if (j < n_scan) {
-            k = listed ? sm.u.l.k[j] : j;
-            e = s[k];
+    {
+        unsigned long long wlo, whi;
+        if (beta < 16) {
+            wlo = static_cast<unsigned long long>(beta);
+            whi = wlo + 1ull;
+        } else {
+            const int msb = 4 + (beta - 16) / 8, j = (beta - 16) % 8;
+            wlo = static_cast<unsigned long long>(8 + j) << (msb - 3);
+            whi = static_cast<unsigned long long>(9 + j) << (msb - 3);
         }
-        const bool hit = j < n_scan && e >= b_lo && e < b_hi;
-        const unsigned int ball = __ballot_sync(0xffffffffu, hit);
-        if (ball == 0u) continue;
-        const unsigned long long W = mass_of(e);
-        unsigned int base = 0;
-        if (lane == 0) base = atomicAdd(&sm.ncand, static_cast<unsigned int>(__popc(ball)));
-        base = __shfl_sync(0xffffffffu, base, 0);
-        if (hit) {
-            const unsigned int slot = base + __popc(ball & ((1u << lane) - 1u));
-            if (slot < static_cast<unsigned int>(kCandLocal)) {
-                sm.cw[slot] = W;
-                sm.ci[slot] = lo + k;
-            } else {
-                sm.overflow = 1;
+        float xa, xb;
+        x_window(wlo, whi, xa, xb);
+        stream_row(row, V, vec, [&](int k, float l) {
+            const float x = scaled_x(l, mx, invT);
+            if (x >= xa && x < xb) {
+                const float e = own_exp(x);
+                if (e >= b_lo && e < b_hi) {
+                    const unsigned int slot = atomicAdd(&sm.ncand, 1u);
+                    if (slot < static_cast<unsigned int>(kCandTotal)) {
+                        sm.cw[slot] = mass_of(e);
+                        sm.ci[slot] = k;
+                    }
+                }
             }
-        }
+        });
     }
     __syncthreads();
-    cl.sync();
-    unsigned int total = 0;
-    int overflow = 0;
-    for (int r = 0; r < C; ++r) {
-        total += *cl.map_shared_rank(&sm.ncand, r);
-        overflow |= *cl.map_shared_rank(&sm.overflow, r);
-    }
-    if (!overflow && total <= static_cast<unsigned int>(kCandTotal)) {
-        if (rank == 0) {  // gather the candidates in rank order
-            unsigned int base = 0;
-            for (int r = 0; r < C; ++r) {
-                const unsigned int cr = *cl.map_shared_rank(&sm.ncand, r);
-                const unsigned long long* rw = cl.map_shared_rank(&sm.cw[0], r);
-                const int* ri = cl.map_shared_rank(&sm.ci[0], r);
-                for (unsigned int t = tid; t < cr; t += kThreads) {
-                    sm.u.g.w[base + t] = rw[t];
-                    sm.u.g.i[base + t] = ri[t];
-                }
-                base += cr;
-            }
-        }
-        cl.sync();  // the peers' candidates are copied: only rank 0 goes on
-        if (rank != 0) return info;
+    const unsigned int total = sm.ncand;
+    if (total <= static_cast<unsigned int>(kCandTotal)) {
         if (total <= static_cast<unsigned int>(kRankSortMax)) {
             // few: each candidate's place is the number that precede it
             unsigned long long wt = 0ull;
             int it = 0x7fffffff;
             unsigned int place = 0;
             if (static_cast<unsigned int>(tid) < total) {
-                wt = sm.u.g.w[tid];
-                it = sm.u.g.i[tid];
+                wt = sm.cw[tid];
+                it = sm.ci[tid];
                 for (unsigned int u = 0; u < total; ++u) {
-                    const unsigned long long wu = sm.u.g.w[u];
-                    const int iu = sm.u.g.i[u];
+                    const unsigned long long wu = sm.cw[u];
+                    const int iu = sm.ci[u];
                     place += (wu > wt || (wu == wt && iu < it)) ? 1u : 0u;
                 }
             }
             __syncthreads();
             if (static_cast<unsigned int>(tid) < total) {
-                sm.u.g.w[place] = wt;
-                sm.u.g.i[place] = it;
+                sm.cw[place] = wt;
+                sm.ci[place] = it;
             }
             __syncthreads();
         } else {
             // pad to a power of two, bitonic sort by (W desc, index asc)
             unsigned int pw = 1;
             while (pw < total) pw <<= 1;
-            for (unsigned int t = total + tid; t < pw; t += kThreads) {
-                sm.u.g.w[t] = 0ull;
-                sm.u.g.i[t] = 0x7fffffff;
+            for (unsigned int t = total + tid; t < pw; t += kRowThreads) {
+                sm.cw[t] = 0ull;
+                sm.ci[t] = 0x7fffffff;
             }
             __syncthreads();
             for (unsigned int kk = 2; kk <= pw; kk <<= 1) {
                 for (unsigned int j = kk >> 1; j > 0; j >>= 1) {
-                    for (unsigned int t = tid; t < pw; t += kThreads) {
+                    for (unsigned int t = tid; t < pw; t += kRowThreads) {
                         const unsigned int u = t ^ j;
                         if (u > t) {
-                            const unsigned long long wa = sm.u.g.w[t], wb = sm.u.g.w[u];
-                            const int ia = sm.u.g.i[t], ib = sm.u.g.i[u];
+                            const unsigned long long wa = sm.cw[t], wb = sm.cw[u];
+                            const int ia = sm.ci[t], ib = sm.ci[u];
                             const bool a_first = wa > wb || (wa == wb && ia < ib);
                             const bool up = (t & kk) == 0;
                             if (up != a_first) {
-                                sm.u.g.w[t] = wb;
-                                sm.u.g.w[u] = wa;
-                                sm.u.g.i[t] = ib;
-                                sm.u.g.i[u] = ia;
+                                sm.cw[t] = wb;
+                                sm.cw[u] = wa;
+                                sm.ci[t] = ib;
+                                sm.ci[u] = ia;
                             }
                         }
                     }
@@ -564,29 +473,29 @@ __device__ RowInfo row_stats(cg::cluster_group& cl, float* s, int n, int lo, int
         }
         // running mass down the sorted list; the first crossing is the cut
         const unsigned int t0 = 2 * tid;
-        const unsigned long long w0 = t0 < total ? sm.u.g.w[t0] : 0ull;
-        const unsigned long long w1 = t0 + 1 < total ? sm.u.g.w[t0 + 1] : 0ull;
+        const unsigned long long w0 = t0 < total ? sm.cw[t0] : 0ull;
+        const unsigned long long w1 = t0 + 1 < total ? sm.cw[t0 + 1] : 0ull;
         u128 tot;
         const u128 ex = block_excl_u128(static_cast<u128>(w0) + w1, sm.red, tot);
         const u128 above = sm.above;
         const u128 c0s = above + ex + w0, c1s = c0s + w1;
         if (t0 < total && (c0s << 32) >= TGT && ((above + ex) << 32) < TGT) {
             sm.info.tau = w0;
-            sm.info.cut = sm.u.g.i[t0];
+            sm.info.cut = sm.ci[t0];
             sm.info.S = static_cast<unsigned long long>(c0s);
         } else if (t0 + 1 < total && (c1s << 32) >= TGT && (c0s << 32) < TGT) {
             sm.info.tau = w1;
-            sm.info.cut = sm.u.g.i[t0 + 1];
+            sm.info.cut = sm.ci[t0 + 1];
             sm.info.S = static_cast<unsigned long long>(c1s);
         }
         __syncthreads();
         info.tau = sm.info.tau;
         info.cut = sm.info.cut;
         info.S = sm.info.S;
-        return info;  // rank 0 only: the peers have returned
+        return info;
     }
 
-    // 5. fallback: exact radix search over the slices inside the bucket
+    // 4. fallback (a crowded bucket): exact radix search inside the bucket
     if (tid == 0) {
         if (beta < 16) {
             sm.lo = static_cast<unsigned long long>(beta);
@@ -607,43 +516,36 @@ __device__ RowInfo row_stats(cg::cluster_group& cl, float* s, int n, int lo, int
         const int bits = wbits < 8 ? wbits : 8;
         const int shift = wbits - bits;
         const unsigned long long rlo = sm.lo, rhi = sm.lo + sm.width;
-        cl.sync();  // peers finished reading this CTA's previous histogram
-        for (int t = tid; t < kLinBuckets; t += kThreads) {
+        for (int t = tid; t < kLinBuckets; t += kRowThreads) {
             sm.cnt[t] = 0u;
-            sm.mass[t] = 0ull;
+            sm.lmass[t] = 0ull;
         }
         __syncthreads();
-        for (int k0 = tid - lane; k0 < n; k0 += kThreads) {  // warp-uniform trip count
-            const int k = k0 + lane;
-            const unsigned long long W = k < n ? mass_of(s[k]) : 0ull;
-            const bool in = k < n && W >= rlo && W < rhi;
-            if (__ballot_sync(0xffffffffu, in) == 0u) continue;
-            warp_bucket_add(in, in ? static_cast<int>((W - rlo) >> shift) : 0, W, lane, sm.cnt,
-                            sm.mass);
-        }
-        cl.sync();
-        for (int t = tid; t < (1 << bits); t += kThreads) {
-            unsigned int c = 0;
-            unsigned long long m = 0;
-            for (int r = 0; r < C; ++r) {
-                c += cl.map_shared_rank(&sm.cnt[0], r)[t];
-                m += cl.map_shared_rank(&sm.mass[0], r)[t];
+        float xa, xb;
+        x_window(rlo, rhi, xa, xb);
+        stream_row(row, V, vec, [&](int, float l) {
+            const float x = scaled_x(l, mx, invT);
+            if (x >= xa && x < xb) {
+                const unsigned long long W = mass_of(own_exp(x));
+                if (W >= rlo && W < rhi) {
+                    const int bk = static_cast<int>((W - rlo) >> shift);
+                    atomicAdd(&sm.cnt[bk], 1u);
+                    atomic_add_u64_split(&sm.lmass[bk], W);
+                }
             }
-            sm.mcnt[t] = c;
-            sm.mmass[t] = m;
-        }
+        });
         __syncthreads();
         {
             const int nb = 1 << bits;
             const int t = nb - 1 - tid;  // thread tid holds sub-bucket nb - 1 - tid
-            const unsigned long long mt = t >= 0 ? sm.mmass[t] : 0ull;
+            const unsigned long long mt = t >= 0 ? sm.lmass[t] : 0ull;
             u128 tot2;
             const u128 inc = block_excl_u128(static_cast<u128>(mt), sm.red, tot2) + mt;
             const u128 ab = static_cast<u128>(sm.above);
             if (t >= 0 && ((ab + inc) << 32) >= TGT && ((ab + inc - mt) << 32) < TGT) {
                 sm.beta = t;
                 sm.lo = rlo + (static_cast<unsigned long long>(t) << shift);
-                sm.n_eq = sm.mcnt[t];
+                sm.n_eq = sm.cnt[t];
                 sm.count_eq = static_cast<unsigned long long>(ab + inc - mt);
             }
             __syncthreads();
@@ -663,95 +565,52 @@ __device__ RowInfo row_stats(cg::cluster_group& cl, float* s, int n, int lo, int
     info.tau = tau;
     info.S = above + jneed * tau;
     info.cut = V - 1;
-    // the jneed-th element with W == tau in index order sets the cut
-    const int chunk = (n + kThreads - 1) / kThreads;
-    const int k0 = tid * chunk, k1 = (k0 + chunk < n) ? k0 + chunk : n;
-    unsigned int mine = 0;
-    for (int k = k0; k < k1; ++k) mine += (mass_of(s[k]) == tau) ? 1u : 0u;
-    u128 ctot;
-    const unsigned long long excl =
-        static_cast<unsigned long long>(block_excl_u128(static_cast<u128>(mine), sm.red, ctot));
-    if (tid == 0) {
-        sm.count_eq = static_cast<unsigned long long>(ctot);
-        sm.cut_found = -1;
-    }
-    cl.sync();
-    unsigned long long before = 0;
-    for (int r = 0; r < rank; ++r) before += *cl.map_shared_rank(&sm.count_eq, r);
-    const unsigned long long need = jneed - before;  // 1-based inside this CTA
-    if (jneed < n_eq && before < jneed && jneed <= before + sm.count_eq && excl < need &&
-        need <= excl + mine) {
-        unsigned long long seen = excl;
-        for (int k = k0; k < k1; ++k)
-            if (mass_of(s[k]) == tau && ++seen == need) {
-                sm.cut_found = lo + k;
-                break;
-            }
-    }
-    cl.sync();
     if (jneed < n_eq) {
-        int cut = -1;
-        for (int r = 0; r < C; ++r) {
-            const int x = *cl.map_shared_rank(&sm.cut_found, r);
-            if (x >= 0) cut = x;
+        // the jneed-th entry with W == tau in index order sets the cut: each
+        // thread counts its contiguous chunk, a block scan orders the chunks
+        const int chunk = (V + kRowThreads - 1) / kRowThreads;
+        const int k0 = tid * chunk, k1 = (k0 + chunk < V) ? k0 + chunk : V;
+        float xa, xb;
+        x_window(tau, tau + 1ull, xa, xb);
+        auto is_tau = [&](int k) {
+            const float x = scaled_x(__ldg(row + k), mx, invT);
+            return x >= xa && x < xb && mass_of(own_exp(x)) == tau;
+        };
+        unsigned int mine = 0;
+        for (int k = k0; k < k1; ++k) mine += is_tau(k) ? 1u : 0u;
+        u128 ctot;
+        const unsigned long long excl = static_cast<unsigned long long>(
+            block_excl_u128(static_cast<u128>(mine), sm.red, ctot));
+        if (tid == 0) sm.cut_found = -1;
+        __syncthreads();
+        if (excl < jneed && jneed <= excl + mine) {
+            unsigned long long seen = excl;
+            for (int k = k0; k < k1; ++k)
+                if (is_tau(k) && ++seen == jneed) {
+                    sm.cut_found = k;
+                    break;
+                }
         }
-        info.cut = cut;
+        __syncthreads();
+        info.cut = sm.cut_found;
     }
-    cl.sync();
     return info;
 }
 
 // ------------------------------------------------------------- row kernel
-__device__ __forceinline__ void load_slice(float* dst, const float* src, int n, bool vec) {
-    if (vec) {
-        const int n4 = n >> 2;
-        const float4* s4 = reinterpret_cast<const float4*>(src);
-        float4* d4 = reinterpret_cast<float4*>(dst);
-        for (int k = threadIdx.x; k < n4; k += kThreads) d4[k] = __ldg(s4 + k);
-        for (int k = 4 * n4 + threadIdx.x; k < n; k += kThreads) dst[k] = __ldg(src + k);
-    } else {
-        for (int k = threadIdx.x; k < n; k += kThreads) dst[k] = __ldg(src + k);
-    }
-}
-
 // Rows 0 .. B(Kd+1)-1 are the target rows (b, i) in order, then the B*Kd
 // draft rows (b, i).
-__global__ void __launch_bounds__(kThreads, 2) row_kernel(
+__global__ void __launch_bounds__(kRowThreads, 1) row_kernel(
     const float* __restrict__ target, const float* __restrict__ draft, long long n_target_rows,
-    int V, int slice, int vec_ok, float invT, unsigned long long P, RowInfo* __restrict__ info,
-    uint32_t* status, unsigned long long wait_ns) {
-    cg::cluster_group cl = cg::this_cluster();
+    int V, int vec_ok, float invT, unsigned long long P, RowInfo* __restrict__ info) {
     extern __shared__ float4 dyn[];
-    __shared__ RowSmem sm;
-    float* s = reinterpret_cast<float*>(dyn);
-    const int C = static_cast<int>(cl.num_blocks());
-    const int rank = static_cast<int>(cl.block_rank());
-    const long long row = blockIdx.x / C;
+    RowSmem& sm = *reinterpret_cast<RowSmem*>(dyn);
+    const long long row = blockIdx.x;
     const float* src = row < n_target_rows
                            ? target + row * static_cast<long long>(V)
                            : draft + (row - n_target_rows) * static_cast<long long>(V);
-    const int lo = rank * slice;
-    const int n = (lo < V) ? ((V - lo < slice) ? V - lo : slice) : 0;
-    if (vec_ok && n > 0) {
-        // one bulk copy of the whole slice (16-byte aligned, a multiple of 16 bytes)
-        __shared__ __align__(8) uint64_t bar;
-        if (threadIdx.x == 0) {
-            mbar_init(&bar, 1);
-            fence_barrier_init();
-            mbar_arrive_expect_tx(&bar, static_cast<uint32_t>(n) * 4u);
-            bulk_load(s, src + lo, static_cast<uint32_t>(n) * 4u, &bar, policy_evict_first());
-        }
-        if (threadIdx.x < 32) {  // one warp polls; the others sleep in the barrier below
-            __syncwarp();        // the barrier is initialised before any lane polls it
-            if (!mbar_wait_bounded(&bar, 0, wait_ns, nullptr) && threadIdx.x == 0)
-                atomicOr(status, kStatusTimeout);
-        }
-    } else {
-        load_slice(s, src + lo, n, false);
-    }
-    __syncthreads();
-    const RowInfo r = row_stats(cl, s, n, lo, V, invT, P, sm);
-    if (rank == 0 && threadIdx.x == 0) info[row] = r;
+    const RowInfo r = row_stats(src, V, vec_ok != 0, invT, P, sm);
+    if (threadIdx.x == 0) info[row] = r;
 }
 
 // --------------------------------------------------------- sequence kernel
@@ -1010,10 +869,6 @@ __global__ void own_exp_kernel(const float* __restrict__ x, float* __restrict__ 
         y[i] = own_exp(x[i]);
 }
 
-int cluster_for(int V) {
-    int c = (V + 16383) / 16384;
-    return c < 1 ? 1 : (c > 8 ? 8 : c);
-}
 
 }  // namespace
 
@@ -1036,39 +891,24 @@ cudaError_t launch_accept_rejection(const float* target, const float* draft,
                                     uint64_t P, uint64_t seed, uint64_t offset, int32_t* tokens,
                                     int32_t* len, void* ws, size_t ws_bytes, uint32_t* status,
                                     unsigned long long wait_ns, cudaStream_t s) {
-    const int C = cluster_for(V);
-    int slice = (V + C - 1) / C;
-    slice = (slice + 3) & ~3;
-    if (slice > kMaxSlice) return cudaErrorNotSupported;
     const long long n_target_rows = static_cast<long long>(B) * (Kd + 1);
     const long long rows = n_target_rows + static_cast<long long>(B) * Kd;
-    if (rows * C > 0x7fffffffll || rows > 0x7fffffffll) return cudaErrorNotSupported;
+    if (rows > 0x7fffffffll) return cudaErrorNotSupported;
     if (rejection_workspace_bytes(B, Kd, V) > ws_bytes) return cudaErrorInvalidValue;
     RowInfo* info = static_cast<RowInfo*>(ws);
+    (void)wait_ns;
 
-    const size_t smem = static_cast<size_t>(slice) * sizeof(float);
+    const size_t smem = sizeof(RowSmem);
     cudaError_t e = cudaFuncSetAttribute(row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(static_cast<unsigned>(rows * C));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = C;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     const int vec_ok = (V % 4 == 0 && (reinterpret_cast<uintptr_t>(target) & 15u) == 0 &&
                         (reinterpret_cast<uintptr_t>(draft) & 15u) == 0)
                            ? 1
                            : 0;
-    e = cudaLaunchKernelEx(&cfg, row_kernel, target, draft, n_target_rows, V, slice, vec_ok, invT,
-                           static_cast<unsigned long long>(P), info, status,
-                           static_cast<unsigned long long>(wait_ns));
+    row_kernel<<<static_cast<unsigned>(rows), kRowThreads, smem, s>>>(
+        target, draft, n_target_rows, V, vec_ok, invT, static_cast<unsigned long long>(P), info);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     seq_kernel<<<B, kThreads, 0, s>>>(target, draft, drafts, Kd, V, vec_ok, invT,
                                       static_cast<unsigned long long>(seed),
