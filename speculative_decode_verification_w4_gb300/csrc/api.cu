@@ -336,6 +336,9 @@ VW4_API vw4_status verify_moe_w4(const vw4_weight* experts, int E, const void* A
     p.ldo = combine ? N : ldo;
     p.dense_M = 0;
     p.argmax_M = 0;
+    // whole tiles per CTA: a segment's tiles are short (an expert's rows),
+    // and splitting them across CTAs costs more than the imbalance
+    p.split = -1;
     p.partials = ws.partials;
     p.tile_cnt = ws.tile_cnt;
     p.am_key = ws.am_key;

@@ -498,7 +498,8 @@ __device__ __forceinline__ unsigned long long umax64(unsigned long long a,
 // The unit range of each CTA.  Stream-K (S == 0): CTA i owns units
 // [iU/G, (i+1)U/G) of the (tile, stage) order, whatever the tile boundaries.
 // Tile-aligned split-K (S > 0, G = tiles * S): CTA tS + p owns stages
-// [pT/S, (p+1)T/S) of tile t, so no CTA spans two tiles.
+// [pT/S, (p+1)T/S) of tile t, so no CTA spans two tiles.  Whole tiles
+// (S < 0): CTA i owns tiles [i TT/G, (i+1) TT/G) of the TT = U / T tiles.
 struct Range {
     unsigned long long U, G;
     int T, S;
@@ -507,6 +508,7 @@ struct Range {
             const unsigned long long t = i / S, q = i % S;
             return t * T + q * T / S;
         }
+        if (S < 0) return i * (U / T) / G * T;
         return i * U / G;
     }
     // the CTA whose range holds unit u
@@ -514,6 +516,10 @@ struct Range {
         if (S > 0) {
             const unsigned long long t = u / T, st = u % T;
             return t * S + ((st + 1) * S - 1) / T;
+        }
+        if (S < 0) {
+            const unsigned long long TT = U / T;
+            return ((u / T + 1) * G + TT - 1) / TT - 1;
         }
         return ((u + 1) * G + U - 1) / U - 1;
     }
@@ -572,7 +578,9 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     // Effective grid: never more CTAs than units, so every active CTA owns at
     // least one unit (the contributor arithmetic of split tiles relies on it).
     const unsigned long long U = static_cast<unsigned long long>(n_seg) * n_tiles * T;
-    const unsigned long long G = U < gridDim.x ? U : gridDim.x;
+    // (whole-tile mode: never more CTAs than tiles)
+    const unsigned long long n_items = p.split < 0 ? U / T : U;
+    const unsigned long long G = n_items < gridDim.x ? n_items : gridDim.x;
     if (blockIdx.x >= G) return;
     const Range R{U, G, T, p.split};
     const unsigned long long u_begin = R.start(blockIdx.x), u_end = R.start(blockIdx.x + 1);
