@@ -89,6 +89,44 @@ __device__ __forceinline__ float own_exp(float x) {
     return __fmul_rn(p, __uint_as_float(static_cast<uint32_t>(ni + 127) << 23));
 }
 
+// own_exp(x) * 2^40 as the row statistics need it: the same reduction and
+// polynomial, with the final power of two taken as 2^(n + 40).  The value is
+// __fmul_rn(own_exp(x), 2^40) exactly wherever own_exp(x) > 0 (both are
+// p * 2^(n + 40), in the normal range).  Below -32 (and for NaN) x is clamped
+// to -32, where own_exp is 0 and this gives less than 1: the integer mass
+// floor() of either is 0.
+__device__ __forceinline__ float own_exp_2_40(float x) {
+    x = fmaxf(x, -32.0f);
+    const float t = __fmul_rn(x, 1.44269504088896340736f);
+    const float n = rintf(t);
+    float r = __fmaf_rn(-n, 0.693145751953125f, x);
+    r = __fmaf_rn(-n, 1.42860682030941723212e-6f, r);
+    float p = 1.0f / 5040.0f;
+    p = __fmaf_rn(p, r, 1.0f / 720.0f);
+    p = __fmaf_rn(p, r, 1.0f / 120.0f);
+    p = __fmaf_rn(p, r, 1.0f / 24.0f);
+    p = __fmaf_rn(p, r, 1.0f / 6.0f);
+    p = __fmaf_rn(p, r, 0.5f);
+    p = __fmaf_rn(p, r, 1.0f);
+    p = __fmaf_rn(p, r, 1.0f);
+    // the bits of n + 1.5 * 2^23 are 0x4B400000 + n; the exponent field of
+    // 2^(n + 40) is n + 167
+    const uint32_t nb = __float_as_uint(__fadd_rn(n, 12582912.0f));
+    return __fmul_rn(p, __uint_as_float((nb - (0x4B400000u - 167u)) << 23));
+}
+
+// The two exact 20-bit halves of W = floor(f), 0 <= f <= 2^40, as the bit
+// patterns of 2^23 + hi and 2^23 + lo (a sum of them loses the 2^23 terms
+// once, at the end): adding 2^23 rounding down is floor() below 2^23, and
+// f - hi * 2^20 is exact (a multiple of ulp(f) below 2^20).
+__device__ __forceinline__ void mass_bits(float f, uint32_t& hib, uint32_t& lob) {
+    const float t1 = __fadd_rd(__fmul_rn(f, 9.5367431640625e-07f), 8388608.0f);
+    const float fh = __fsub_rn(t1, 8388608.0f);
+    const float t2 = __fadd_rd(__fmaf_rn(-fh, 1048576.0f, f), 8388608.0f);
+    hib = __float_as_uint(t1);
+    lob = __float_as_uint(t2);
+}
+
 __device__ __forceinline__ float scaled_x(float l, float mx, float invT) {
     return __fmul_rn(__fsub_rn(l, mx), invT);
 }
@@ -97,14 +135,6 @@ __device__ __forceinline__ float scaled_x(float l, float mx, float invT) {
 // e * 2^40 is exact; fh = floor(f / 2^20) < 2^21 and d = f - fh * 2^20 in
 // [0, 2^20) are exact in fp32 (d is a multiple of ulp(f)); each integer part
 // is read from the mantissa after adding 2^23.
-__device__ __forceinline__ void mass_parts(float e, uint32_t& hi, uint32_t& lo) {
-    const float f = __fmul_rn(e, 1099511627776.0f);
-    const float fh = floorf(__fmul_rn(e, 1048576.0f));  // = floor(f / 2^20)
-    const float dl = floorf(__fmaf_rn(-fh, 1048576.0f, f));
-    hi = __float_as_uint(__fadd_rn(fh, 8388608.0f)) - 0x4B000000u;
-    lo = __float_as_uint(__fadd_rn(dl, 8388608.0f)) - 0x4B000000u;
-}
-
 __device__ __forceinline__ unsigned long long mass_of(float e) {
     const float f = __fmul_rn(e, 1099511627776.0f);
     const float fh = floorf(__fmul_rn(f, 9.5367431640625e-07f));
@@ -123,8 +153,7 @@ __device__ __forceinline__ unsigned long long kept(unsigned long long W, int v, 
 // then 16 + 8 * (binade - 4) + the 3 bits after the leading one.  Computed
 // from the float's bits: every bucket edge at or above 16 is an integer, so
 // floor() never crosses one.
-__device__ __forceinline__ int log_bucket_e(float e) {
-    const float f = __fmul_rn(e, 1099511627776.0f);
+__device__ __forceinline__ int log_bucket_f(float f) {
     if (f < 16.0f) return static_cast<int>(f);
     const uint32_t bits = __float_as_uint(f);
     const int msb = static_cast<int>((bits >> 23) & 0xFFu) - 127;
@@ -313,6 +342,16 @@ __device__ __forceinline__ void stream_row(const float* __restrict__ row, int V,
     }
 }
 
+// How many entries stream_row hands to this thread.
+__device__ __forceinline__ uint32_t stream_count(int V, bool vec) {
+    const int tid = threadIdx.x;
+    if (vec) {
+        const int V4 = V >> 2;
+        return tid < V4 ? 4u * static_cast<uint32_t>((V4 - 1 - tid) / kRowThreads + 1) : 0u;
+    }
+    return tid < V ? static_cast<uint32_t>((V - 1 - tid) / kRowThreads + 1) : 0u;
+}
+
 // The scaled-logit window [xa, xb) that holds every entry with wlo <= W <
 // whi (1 <= wlo): own_exp is monotone and within 2 ulp of exp, so a margin of
 // 1e-3 in the exponent is far wider than any rounding.
@@ -343,25 +382,29 @@ __device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, flo
         want_hist ? ((kKeepAll - P) << 8) / static_cast<unsigned long long>(V) : 0ull;
     const unsigned long long cmin = c0 > 1ull ? c0 : 1ull;
     // e < e_lo proves W < cmin with one compare (e_lo rounds cmin * 2^-40 down)
-    const float e_lo = want_hist ? __fmul_rn(__ull2float_rd(cmin), 9.094947017729282379e-13f)
-                                 : INFINITY;
+    // f < f_lo proves W < cmin with one compare (f_lo is cmin rounded down)
+    const float f_lo = want_hist ? __ull2float_rd(cmin) : INFINITY;
     unsigned long long* hist = sm.whist[wid];
     for (int t = lane; t < kLogBuckets; t += 32) hist[t] = 0ull;
     __syncwarp();
-    uint32_t sum_hi = 0u, sum_lo = 0u;  // the two exact 20-bit halves of each W
+    // the two exact 20-bit halves of each W, summed as 2^23-biased bit
+    // patterns (mod 2^32; the true sums stay below 2^32)
+    uint32_t sum_hib = 0u, sum_lob = 0u;
     stream_row(row, V, vec, [&](int, float l) {
-        const float e = own_exp(scaled_x(l, mx, invT));
-        uint32_t hi, lo;
-        mass_parts(e, hi, lo);
-        sum_hi += hi;
-        sum_lo += lo;
-        if (e >= e_lo) {
-            const unsigned long long W = (static_cast<unsigned long long>(hi) << 20) | lo;
-            if (W >= cmin) atomic_add_u64_split(&hist[log_bucket_e(e)], W);
+        const float f = own_exp_2_40(scaled_x(l, mx, invT));
+        uint32_t hib, lob;
+        mass_bits(f, hib, lob);
+        sum_hib += hib;
+        sum_lob += lob;
+        if (f >= f_lo) {
+            const unsigned long long W =
+                (static_cast<unsigned long long>(hib - 0x4B000000u) << 20) | (lob - 0x4B000000u);
+            if (W >= cmin) atomic_add_u64_split(&hist[log_bucket_f(f)], W);
         }
     });
-    const unsigned long long S =
-        block_sum_u64((static_cast<unsigned long long>(sum_hi) << 20) + sum_lo, sm.red);
+    const uint32_t bias = stream_count(V, vec) * 0x4B000000u;
+    const unsigned long long S = block_sum_u64(
+        (static_cast<unsigned long long>(sum_hib - bias) << 20) + (sum_lob - bias), sm.red);
     RowInfo info;
     info.mx = mx;
     if (!want_hist) {
