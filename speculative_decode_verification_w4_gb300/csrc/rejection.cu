@@ -17,26 +17,29 @@
 //   residual  r_v = max(0, p_v * Sq - q_v * Sp), inverse CDF with a 64-bit
 //   uniform; bonus from p_Kd when every draft is accepted.
 //
-// Kernel 1 (row_kernel), one CTA per logits row -- every target row
-// (b, i <= Kd) and every draft row (b, i < Kd) independently; the row is
-// streamed three times (the second and third mostly from L2):
-//   * the max;
+// Kernel 1 (row_kernel), one 512-thread CTA per logits row (two per SM) --
+// every target row (b, i <= Kd) and every draft row (b, i < Kd)
+// independently; the row is streamed three times:
+//   * the max, and the max of every 128-entry segment (to the workspace);
 //   * own_exp, sum W, and a log-scale histogram of the mass of the entries
 //     at or above c0 = floor((2^32 - P) * 2^40 / (V * 2^32)) -- every entry
 //     below it lies in the dropped tail, because all of them together weigh
 //     less than (1 - P/2^32) * S (S >= 2^40, the top entry's own mass) -- in
 //     one private copy per warp; the merged suffix sums give the bucket where
 //     the kept prefix ends;
-//   * that bucket's members (a scaled-logit window, then the exact test),
-//     sorted by (W desc, index asc) and scanned, which gives the exact cut
-//     (an exact radix search is the fallback when the bucket is crowded);
+//   * that bucket's members (a scaled-logit window, then the exact test;
+//     only the segments whose max reaches the window are read), sorted by
+//     (W desc, index asc) and scanned, which gives the exact cut (an exact
+//     radix search is the fallback when the bucket is crowded);
 //   * (max, tau, cut, kept sum) of the row go to the workspace.
 // Kernel 2 (seq_kernel), one CTA per sequence: the acceptance tests in
 // order (Philox block (i, b)), then one ordered draw over the row it needs --
 // the residual at the first rejection, or the bonus from p_Kd -- and the
-// committed run.  The draw skips, with two flops, every entry whose logit is
-// too small to be kept (a bound below the cut with a 1e-3 margin in the
-// exponent), so it streams the row once at memory speed.
+// committed run.  Every entry whose scaled logit lies below a bound under the
+// cut (a 1e-3 margin in the exponent) weighs 0, and so does every segment
+// whose max does: the draw reads only the other segments, sums each of them
+// (to the workspace), finds the segment that holds the draw point by a block
+// scan of those sums and rescans that one segment.
 #include <cmath>
 
 #include "ptx.cuh"
@@ -113,6 +116,31 @@ __device__ __forceinline__ float own_exp_2_40(float x) {
     // 2^(n + 40) is n + 167
     const uint32_t nb = __float_as_uint(__fadd_rn(n, 12582912.0f));
     return __fmul_rn(p, __uint_as_float((nb - (0x4B400000u - 167u)) << 23));
+}
+
+// own_exp_2_40 of two scaled logits with packed fp32-pair operations: each
+// half is the same IEEE operation, rounding included, as in own_exp_2_40
+// (x - n c equals x + n (-c); rint(t) is read from t + 1.5 * 2^23, which
+// rounds to the nearest even integer just as rint does, |t| < 2^22).
+__device__ __forceinline__ float2 own_exp_2_40_x2(float2 x) {
+    x.x = fmaxf(x.x, -32.0f);
+    x.y = fmaxf(x.y, -32.0f);
+    const float2 t = __fmul2_rn(x, make_float2(1.44269504088896340736f, 1.44269504088896340736f));
+    const float2 m = __fadd2_rn(t, make_float2(12582912.0f, 12582912.0f));
+    const float2 n = __fadd2_rn(m, make_float2(-12582912.0f, -12582912.0f));
+    float2 r = __ffma2_rn(n, make_float2(-0.693145751953125f, -0.693145751953125f), x);
+    r = __ffma2_rn(n, make_float2(-1.42860682030941723212e-6f, -1.42860682030941723212e-6f), r);
+    float2 p = make_float2(1.0f / 5040.0f, 1.0f / 5040.0f);
+    p = __ffma2_rn(p, r, make_float2(1.0f / 720.0f, 1.0f / 720.0f));
+    p = __ffma2_rn(p, r, make_float2(1.0f / 120.0f, 1.0f / 120.0f));
+    p = __ffma2_rn(p, r, make_float2(1.0f / 24.0f, 1.0f / 24.0f));
+    p = __ffma2_rn(p, r, make_float2(1.0f / 6.0f, 1.0f / 6.0f));
+    p = __ffma2_rn(p, r, make_float2(0.5f, 0.5f));
+    p = __ffma2_rn(p, r, make_float2(1.0f, 1.0f));
+    p = __ffma2_rn(p, r, make_float2(1.0f, 1.0f));
+    const uint32_t bx = __float_as_uint(m.x), by = __float_as_uint(m.y);
+    return __fmul2_rn(p, make_float2(__uint_as_float((bx - (0x4B400000u - 167u)) << 23),
+                                     __uint_as_float((by - (0x4B400000u - 167u)) << 23)));
 }
 
 // The two exact 20-bit halves of W = floor(f), 0 <= f <= 2^40, as the bit
@@ -297,7 +325,7 @@ __device__ __forceinline__ void atomic_add_u64_split(unsigned long long* a, unsi
 // One CTA per logits row.  The row is streamed three times (the second and
 // third from L2): the max; own_exp, sum W and the mass histogram of the
 // entries >= c0; the members of the crossing bucket.
-constexpr int kRowThreads = 1024;
+constexpr int kRowThreads = 512;
 constexpr int kRowWarps = kRowThreads / 32;
 static_assert(kRowThreads >= kLogBuckets, "one thread per log bucket in the suffix scan");
 
@@ -342,6 +370,53 @@ __device__ __forceinline__ void stream_row(const float* __restrict__ row, int V,
     }
 }
 
+// Segments: the row's entries in runs of kSegLen = 128 (one warp's float4
+// group).  The max pass records each segment's largest logit; a later pass
+// that only wants entries with scaled logit >= xa skips every segment whose
+// max falls below (scaled_x is monotone, so no entry of it can qualify; an
+// entry that is NaN never qualifies either, and fmaxf passes it over).
+constexpr int kSegLen = 128;
+
+__device__ __forceinline__ int n_segments(int V) { return (V + kSegLen - 1) / kSegLen; }
+
+// Order-preserving int key of a float (for a warp max by integer reduction).
+__device__ __forceinline__ int float_key(float x) {
+    const int k = __float_as_int(x);
+    return k ^ ((k >> 31) & 0x7fffffff);
+}
+
+// f(k, l) for every entry of the segments whose max passes the window test
+// (vec rows with a segment table; otherwise every entry, as stream_row).
+// seg[] was written by this CTA in its max pass: read through L2.
+template <class F>
+__device__ __forceinline__ void stream_window(const float* __restrict__ row, int V, bool vec,
+                                              const float* seg, float mx, float invT, float xa,
+                                              F&& f) {
+    if (seg == nullptr) {
+        stream_row(row, V, vec, f);
+        return;
+    }
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+    const int V4 = V >> 2, nk = (V4 + kRowThreads - 1) / kRowThreads, nseg = n_segments(V);
+    for (int k0 = 0; k0 < nk; k0 += 32) {
+        // lane j tests the segment of step k0 + j that this warp streams
+        const int k = k0 + lane, sg = k * kRowWarps + wid;
+        bool need = false;
+        if (k < nk && sg < nseg) need = !(scaled_x(__ldcg(seg + sg), mx, invT) < xa);
+        unsigned int m = __ballot_sync(0xffffffffu, need);
+        while (m) {
+            const int j = __ffs(m) - 1;
+            m &= m - 1;
+            const int i = (k0 + j) * kRowThreads + tid;
+            if (i < V4) {
+                const float4 a = __ldg(r4 + i);
+                f(4 * i, a.x); f(4 * i + 1, a.y); f(4 * i + 2, a.z); f(4 * i + 3, a.w);
+            }
+        }
+    }
+}
+
 // How many entries stream_row hands to this thread.
 __device__ __forceinline__ uint32_t stream_count(int V, bool vec) {
     const int tid = threadIdx.x;
@@ -363,13 +438,38 @@ __device__ __forceinline__ void x_window(unsigned long long wlo, unsigned long l
 }
 
 // The row's (max, tau, cut, kept sum); valid in every thread.
+// seg: this row's segment maxima (vec rows), or null.
 __device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, float invT,
-                             unsigned long long P, RowSmem& sm) {
+                             unsigned long long P, float* seg, RowSmem& sm) {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
 
-    // 1. max
+    // 1. max, and the segment maxima: at step k warp w streams float4 groups
+    //    kRowThreads k + 32 w + lane, i.e. segment kRowWarps k + w
     float lmax = -INFINITY;
-    stream_row(row, V, vec, [&](int, float l) { lmax = fmaxf(lmax, l); });
+    if (seg != nullptr) {
+        const float4* r4 = reinterpret_cast<const float4*>(row);
+        const int V4 = V >> 2, nk = (V4 + kRowThreads - 1) / kRowThreads, nseg = n_segments(V);
+        const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        for (int k0 = 0; k0 < nk; k0 += 4) {
+            float4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = (k0 + j) * kRowThreads + tid;
+                v[j] = (k0 + j < nk && i < V4) ? __ldg(r4 + i) : ninf;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (k0 + j >= nk) break;  // the same for the whole warp
+                const float m = fmaxf(fmaxf(v[j].x, v[j].y), fmaxf(v[j].z, v[j].w));
+                lmax = fmaxf(lmax, m);
+                const int key = __reduce_max_sync(0xffffffffu, float_key(m));
+                const int sg = (k0 + j) * kRowWarps + wid;
+                if (lane == 0 && sg < nseg) seg[sg] = __int_as_float(key ^ ((key >> 31) & 0x7fffffff));
+            }
+        }
+    } else {
+        stream_row(row, V, vec, [&](int, float l) { lmax = fmaxf(lmax, l); });
+    }
     const float mx = block_max(lmax, sm.red);
 
     // 2. sum W, and the mass histogram of the entries with W >= c0 (each warp
@@ -381,7 +481,6 @@ __device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, flo
     const unsigned long long c0 =
         want_hist ? ((kKeepAll - P) << 8) / static_cast<unsigned long long>(V) : 0ull;
     const unsigned long long cmin = c0 > 1ull ? c0 : 1ull;
-    // e < e_lo proves W < cmin with one compare (e_lo rounds cmin * 2^-40 down)
     // f < f_lo proves W < cmin with one compare (f_lo is cmin rounded down)
     const float f_lo = want_hist ? __ull2float_rd(cmin) : INFINITY;
     unsigned long long* hist = sm.whist[wid];
@@ -390,18 +489,53 @@ __device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, flo
     // the two exact 20-bit halves of each W, summed as 2^23-biased bit
     // patterns (mod 2^32; the true sums stay below 2^32)
     uint32_t sum_hib = 0u, sum_lob = 0u;
-    stream_row(row, V, vec, [&](int, float l) {
-        const float f = own_exp_2_40(scaled_x(l, mx, invT));
-        uint32_t hib, lob;
-        mass_bits(f, hib, lob);
-        sum_hib += hib;
-        sum_lob += lob;
-        if (f >= f_lo) {
-            const unsigned long long W =
-                (static_cast<unsigned long long>(hib - 0x4B000000u) << 20) | (lob - 0x4B000000u);
-            if (W >= cmin) atomic_add_u64_split(&hist[log_bucket_f(f)], W);
+    auto to_hist = [&](float f, uint32_t hib, uint32_t lob) {
+        const unsigned long long W =
+            (static_cast<unsigned long long>(hib - 0x4B000000u) << 20) | (lob - 0x4B000000u);
+        if (W >= cmin) atomic_add_u64_split(&hist[log_bucket_f(f)], W);
+    };
+    if (vec) {
+        // two entries per packed operation (mass_bits on pairs)
+        const float2 nmx = make_float2(-mx, -mx), it2 = make_float2(invT, invT);
+        const float2 k20 = make_float2(9.5367431640625e-07f, 9.5367431640625e-07f);
+        const float2 m20 = make_float2(-1048576.0f, -1048576.0f);
+        const float2 b23 = make_float2(8388608.0f, 8388608.0f), nb23 = make_float2(-8388608.0f, -8388608.0f);
+        auto pair = [&](float la, float lb) {
+            const float2 f = own_exp_2_40_x2(__fmul2_rn(__fadd2_rn(make_float2(la, lb), nmx), it2));
+            const float2 t1 = __fadd2_rd(__fmul2_rn(f, k20), b23);
+            const float2 t2 = __fadd2_rd(__ffma2_rn(__fadd2_rn(t1, nb23), m20, f), b23);
+            const uint32_t h0 = __float_as_uint(t1.x), h1 = __float_as_uint(t1.y);
+            const uint32_t l0 = __float_as_uint(t2.x), l1 = __float_as_uint(t2.y);
+            sum_hib += h0 + h1;
+            sum_lob += l0 + l1;
+            if (fmaxf(f.x, f.y) >= f_lo) {
+                if (f.x >= f_lo) to_hist(f.x, h0, l0);
+                if (f.y >= f_lo) to_hist(f.y, h1, l1);
+            }
+        };
+        const float4* r4 = reinterpret_cast<const float4*>(row);
+        const int V4 = V >> 2;
+        int i = tid;
+        for (; i + 3 * kRowThreads < V4; i += 4 * kRowThreads) {
+            const float4 a = __ldg(r4 + i), b = __ldg(r4 + i + kRowThreads),
+                         c = __ldg(r4 + i + 2 * kRowThreads), d = __ldg(r4 + i + 3 * kRowThreads);
+            pair(a.x, a.y); pair(a.z, a.w); pair(b.x, b.y); pair(b.z, b.w);
+            pair(c.x, c.y); pair(c.z, c.w); pair(d.x, d.y); pair(d.z, d.w);
         }
-    });
+        for (; i < V4; i += kRowThreads) {
+            const float4 a = __ldg(r4 + i);
+            pair(a.x, a.y); pair(a.z, a.w);
+        }
+    } else {
+        stream_row(row, V, vec, [&](int, float l) {
+            const float f = own_exp_2_40(scaled_x(l, mx, invT));
+            uint32_t hib, lob;
+            mass_bits(f, hib, lob);
+            sum_hib += hib;
+            sum_lob += lob;
+            if (f >= f_lo) to_hist(f, hib, lob);
+        });
+    }
     const uint32_t bias = stream_count(V, vec) * 0x4B000000u;
     const unsigned long long S = block_sum_u64(
         (static_cast<unsigned long long>(sum_hib - bias) << 20) + (sum_lob - bias), sm.red);
@@ -447,7 +581,7 @@ __device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, flo
         }
         float xa, xb;
         x_window(wlo, whi, xa, xb);
-        stream_row(row, V, vec, [&](int k, float l) {
+        stream_window(row, V, vec, seg, mx, invT, xa, [&](int k, float l) {
             const float x = scaled_x(l, mx, invT);
             if (x >= xa && x < xb) {
                 const float e = own_exp(x);
@@ -566,7 +700,7 @@ __device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, flo
         __syncthreads();
         float xa, xb;
         x_window(rlo, rhi, xa, xb);
-        stream_row(row, V, vec, [&](int, float l) {
+        stream_window(row, V, vec, seg, mx, invT, xa, [&](int, float l) {
             const float x = scaled_x(l, mx, invT);
             if (x >= xa && x < xb) {
                 const unsigned long long W = mass_of(own_exp(x));
@@ -643,16 +777,18 @@ __device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, flo
 // ------------------------------------------------------------- row kernel
 // Rows 0 .. B(Kd+1)-1 are the target rows (b, i) in order, then the B*Kd
 // draft rows (b, i).
-__global__ void __launch_bounds__(kRowThreads, 1) row_kernel(
+__global__ void __launch_bounds__(kRowThreads, 2) row_kernel(
     const float* __restrict__ target, const float* __restrict__ draft, long long n_target_rows,
-    int V, int vec_ok, float invT, unsigned long long P, RowInfo* __restrict__ info) {
+    int V, int vec_ok, float invT, unsigned long long P, RowInfo* __restrict__ info,
+    float* __restrict__ segmax) {
     extern __shared__ float4 dyn[];
     RowSmem& sm = *reinterpret_cast<RowSmem*>(dyn);
     const long long row = blockIdx.x;
     const float* src = row < n_target_rows
                            ? target + row * static_cast<long long>(V)
                            : draft + (row - n_target_rows) * static_cast<long long>(V);
-    const RowInfo r = row_stats(src, V, vec_ok != 0, invT, P, sm);
+    float* seg = vec_ok ? segmax + row * static_cast<long long>(n_segments(V)) : nullptr;
+    const RowInfo r = row_stats(src, V, vec_ok != 0, invT, P, seg, sm);
     if (threadIdx.x == 0) info[row] = r;
 }
 
@@ -664,71 +800,187 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(
 struct DrawRow {
     const float* lp;
     const float* lq;  // null: draw from p
+    const float* sp;  // segment maxima of the p row (vec rows), or null
     RowInfo ip, iq;
     float invT, xth;
-    __device__ __forceinline__ u128 at(int v) const {
-        const float xp = scaled_x(__ldg(lp + v), ip.mx, invT);
+    int V;
+    bool vec;
+    __device__ __forceinline__ u128 weight(int v, float lpv, float lqv) const {
+        const float xp = scaled_x(lpv, ip.mx, invT);
         if (xp < xth) return 0;
         const unsigned long long wp = kept(mass_of(own_exp(xp)), v, ip);
         if (lq == nullptr || wp == 0ull) return static_cast<u128>(wp);
-        const unsigned long long wq =
-            kept(mass_of(own_exp(scaled_x(__ldg(lq + v), iq.mx, invT))), v, iq);
+        const unsigned long long wq = kept(mass_of(own_exp(scaled_x(lqv, iq.mx, invT))), v, iq);
         const u128 a = static_cast<u128>(wp) * iq.S, c = static_cast<u128>(wq) * ip.S;
         return a > c ? a - c : static_cast<u128>(0);
     }
-    __device__ __forceinline__ float4 ld4(int v) const {  // v % 4 == 0, rows 16-byte aligned
-        return __ldg(reinterpret_cast<const float4*>(lp + v));
+    // The logits of entries v .. v+3 (v % 4 == 0; entries >= V read as -inf,
+    // which weighs 0).
+    __device__ __forceinline__ void load4(int v, float4& p, float4& q) const {
+        const float ninf = -INFINITY;
+        q = make_float4(ninf, ninf, ninf, ninf);
+        if (vec) {  // V % 4 == 0 and 16-byte aligned rows
+            p = v < V ? __ldg(reinterpret_cast<const float4*>(lp + v)) : q;
+            if (lq != nullptr && v < V) q = __ldg(reinterpret_cast<const float4*>(lq + v));
+            return;
+        }
+        p = make_float4(v < V ? __ldg(lp + v) : ninf, v + 1 < V ? __ldg(lp + v + 1) : ninf,
+                        v + 2 < V ? __ldg(lp + v + 2) : ninf, v + 3 < V ? __ldg(lp + v + 3) : ninf);
+        if (lq != nullptr)
+            q = make_float4(v < V ? __ldg(lq + v) : ninf, v + 1 < V ? __ldg(lq + v + 1) : ninf,
+                            v + 2 < V ? __ldg(lq + v + 2) : ninf,
+                            v + 3 < V ? __ldg(lq + v + 3) : ninf);
     }
-    __device__ __forceinline__ u128 at4(int v) const { return at4(v, ld4(v)); }
-    __device__ __forceinline__ u128 at4(int v, float4 l) const {  // l = lp[v .. v+3]
-        const float x0 = scaled_x(l.x, ip.mx, invT), x1 = scaled_x(l.y, ip.mx, invT);
-        const float x2 = scaled_x(l.z, ip.mx, invT), x3 = scaled_x(l.w, ip.mx, invT);
-        if (x0 < xth && x1 < xth && x2 < xth && x3 < xth) return 0;
-        return at(v) + at(v + 1) + at(v + 2) + at(v + 3);
+    __device__ __forceinline__ void weights4(int v, const float4& p, const float4& q,
+                                             u128 w[4]) const {
+        w[0] = weight(v, p.x, q.x);
+        w[1] = weight(v + 1, p.y, q.y);
+        w[2] = weight(v + 2, p.z, q.z);
+        w[3] = weight(v + 3, p.w, q.w);
+    }
+    // false: every entry of segment s weighs 0 (its max is below xth)
+    __device__ __forceinline__ bool may_weigh(int s) const {
+        return sp == nullptr || !(scaled_x(__ldg(sp + s), ip.mx, invT) < xth);
     }
 };
 
+// A warp's queue of the entries of one batch of segments that may weigh
+// (scaled logit >= xth): a few per batch, so their weights are computed one
+// per lane instead of in divergent per-slot passes.
+constexpr int kQueue = 64;
+struct WarpQueue {
+    int v[kQueue];
+    float lp[kQueue], lq[kQueue];
+    unsigned char slot[kQueue];
+    unsigned long long acc[4][2];  // the batch's segment sums (lo, hi)
+};
+
 struct SeqSmem {
+    WarpQueue q[kWarps];
     Red red;
     unsigned long long tot_lo[kWarps], tot_hi[kWarps];
     unsigned long long u64s[kMaxRows + 1];
     int ok[kMaxRows + 1];
-    int n_acc, rowp, rowq, sel, token;
+    int n_acc, rowp, rowq, sel, token, seg;
     unsigned long long u64;
-    unsigned long long t_lo, t_hi;
+    unsigned long long t_lo, t_hi;  // the draw point, then its offset inside segment seg
 };
 
-// Sum of the weights of [a, b) by one warp (every lane gets it).
-__device__ __forceinline__ u128 warp_range_sum(const DrawRow& w, int a, int b, bool vec, int lane) {
-    u128 acc = 0;
-    if (vec) {
-        const int a4 = (a + 3) & ~3, b4 = b & ~3;
-        if (a4 <= b4) {
-            int v = a4 + 4 * lane;
-            for (; v + 3 * 128 < b4; v += 4 * 128) {  // four float4 loads in flight
-                const float4 l0 = w.ld4(v), l1 = w.ld4(v + 128), l2 = w.ld4(v + 256),
-                             l3 = w.ld4(v + 384);
-                acc += w.at4(v, l0) + w.at4(v + 128, l1) + w.at4(v + 256, l2) +
-                       w.at4(v + 384, l3);
+// Exact 128-bit add into shared memory: 64-bit atomics, the low word's carry
+// to the high word.
+__device__ __forceinline__ void atomic_add_u128(unsigned long long* a, u128 x) {
+    const unsigned long long lo = static_cast<unsigned long long>(x);
+    const unsigned long long hi = static_cast<unsigned long long>(x >> 64);
+    const unsigned long long old = atomicAdd(&a[0], lo);
+    const unsigned long long h = hi + (old + lo < old ? 1ull : 0ull);
+    if (h) atomicAdd(&a[1], h);
+}
+
+// Level 1 of the draw: warp wid sums the weights of each segment of its run
+// of segments into ssum[] (zero for the segments that cannot weigh) and
+// returns the run's total (in lane 0).
+__device__ __forceinline__ u128 segment_sums(const DrawRow& w, ulonglong2* ssum, WarpQueue& wq,
+                                             int wid, int lane) {
+    const int nseg = n_segments(w.V);
+    const int s_lo = static_cast<int>(static_cast<long long>(wid) * nseg / kWarps);
+    const int s_hi = static_cast<int>(static_cast<long long>(wid + 1) * nseg / kWarps);
+    u128 tot = 0;
+    for (int s0 = s_lo; s0 < s_hi; s0 += 32) {
+        const int s = s0 + lane;
+        const bool need = s < s_hi && w.may_weigh(s);
+        if (s < s_hi && !need) __stcg(ssum + s, make_ulonglong2(0ull, 0ull));
+        unsigned int m = __ballot_sync(0xffffffffu, need);
+        while (m) {
+            // up to four marked segments at a time, their loads first
+            const int n = __popc(m) < 4 ? __popc(m) : 4;
+            int sj[4];
+            float4 p[4], q[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                sj[j] = s0 + static_cast<int>(__fns(m, 0, j < n ? j + 1 : 1));
+                w.load4(sj[j] * kSegLen + 4 * lane, p[j], q[j]);
             }
-            for (; v < b4; v += 128) acc += w.at4(v);
-            if (lane < a4 - a) acc += w.at(a + lane);
-            if (lane < b - b4) acc += w.at(b4 + lane);
-            return warp_sum_u128(acc);
+            // the entries that may weigh: bit 4 j + e of fl for entry e of segment j
+            uint32_t fl = 0u;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (j < n) {
+                    fl |= (scaled_x(p[j].x, w.ip.mx, w.invT) < w.xth ? 0u : 1u) << (4 * j);
+                    fl |= (scaled_x(p[j].y, w.ip.mx, w.invT) < w.xth ? 0u : 2u) << (4 * j);
+                    fl |= (scaled_x(p[j].z, w.ip.mx, w.invT) < w.xth ? 0u : 4u) << (4 * j);
+                    fl |= (scaled_x(p[j].w, w.ip.mx, w.invT) < w.xth ? 0u : 8u) << (4 * j);
+                }
+            }
+            const int c = __popc(fl);
+            int incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const int K = __shfl_sync(0xffffffffu, incl, 31);
+            if (K <= kQueue) {
+                int pos = incl - c;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float pv[4] = {p[j].x, p[j].y, p[j].z, p[j].w};
+                    const float qv[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if ((fl >> (4 * j + e)) & 1u) {
+                            wq.v[pos] = sj[j] * kSegLen + 4 * lane + e;
+                            wq.lp[pos] = pv[e];
+                            wq.lq[pos] = qv[e];
+                            wq.slot[pos] = static_cast<unsigned char>(j);
+                            ++pos;
+                        }
+                    }
+                }
+                if (lane < 8) (&wq.acc[0][0])[lane] = 0ull;
+                __syncwarp();
+                for (int r = lane; r < K; r += 32)
+                    atomic_add_u128(wq.acc[wq.slot[r]], w.weight(wq.v[r], wq.lp[r], wq.lq[r]));
+                __syncwarp();
+            } else {
+                // a crowded batch: every entry through the slot-by-slot path
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (j >= n) break;
+                    u128 e[4];
+                    w.weights4(sj[j] * kSegLen + 4 * lane, p[j], q[j], e);
+                    const u128 seg = warp_sum_u128(e[0] + e[1] + e[2] + e[3]);
+                    if (lane == 0) {
+                        wq.acc[j][0] = static_cast<unsigned long long>(seg);
+                        wq.acc[j][1] = static_cast<unsigned long long>(seg >> 64);
+                    }
+                }
+                __syncwarp();
+            }
+            if (lane == 0) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (j >= n) break;
+                    const unsigned long long lo = wq.acc[j][0], hi = wq.acc[j][1];
+                    __stcg(ssum + sj[j], make_ulonglong2(lo, hi));
+                    tot += (static_cast<u128>(hi) << 64) | lo;
+                }
+            }
+            __syncwarp();
+            for (int j = 0; j < n; ++j) m &= m - 1;
         }
     }
-    for (int v = a + lane; v < b; v += 32) acc += w.at(v);
-    return warp_sum_u128(acc);
+    return tot;
 }
 
 // One CTA per sequence: acceptance tests in order, then one ordered draw and
 // the committed run.
-__global__ void __launch_bounds__(kThreads) seq_kernel(
+// (Two CTAs per SM: 256 sequences fit one wave.)
+__global__ void __launch_bounds__(kThreads, 2) seq_kernel(
     const float* __restrict__ target, const float* __restrict__ draft,
     const int32_t* __restrict__ drafts, int Kd, int V, int vec_ok, float invT,
     unsigned long long seed, unsigned long long offset, long long n_target_rows,
-    const RowInfo* __restrict__ info, int32_t* __restrict__ tokens, int32_t* __restrict__ len,
-    uint32_t* status) {
+    const RowInfo* __restrict__ info, const float* __restrict__ segmax, ulonglong2* segsum,
+    int32_t* __restrict__ tokens, int32_t* __restrict__ len, uint32_t* status) {
     __shared__ SeqSmem sm;
     const int b = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -773,31 +1025,32 @@ __global__ void __launch_bounds__(kThreads) seq_kernel(
         sm.rowq = n < Kd ? static_cast<int>(n_target_rows + static_cast<long long>(b) * Kd + n) : -1;
         sm.u64 = sm.u64s[n];
         sm.token = -1;
+        sm.seg = -1;
     }
     __syncthreads();
     const int rowp = sm.rowp, rowq = sm.rowq;
+    const int nseg = n_segments(V);
     DrawRow w;
     w.ip = info[rowp];
     w.lp = target + static_cast<long long>(rowp) * V;
+    w.sp = vec_ok ? segmax + static_cast<long long>(rowp) * nseg : nullptr;
     w.lq = nullptr;
     if (rowq >= 0) {
         w.iq = info[rowq];
         w.lq = draft + (rowq - n_target_rows) * static_cast<long long>(V);
     }
     w.invT = invT;
+    w.V = V;
+    w.vec = vec_ok != 0;
     {
         const unsigned long long tm = w.ip.tau > 1ull ? w.ip.tau : 1ull;
         w.xth = static_cast<float>(log(static_cast<double>(tm)) - 40.0 * 0.69314718055994530942 -
                                    1e-3);
     }
-    const bool vec = vec_ok != 0;
+    ulonglong2* ssum = segsum + static_cast<long long>(b) * nseg;
 
-    // level 1: each warp totals a contiguous range of the row
-    const int L1 = (((V + kWarps - 1) / kWarps) + 3) & ~3;
-    int a1 = wid * L1, b1 = a1 + L1;
-    if (a1 > V) a1 = V;
-    if (b1 > V) b1 = V;
-    u128 wt = warp_range_sum(w, a1, b1, vec, lane);
+    // level 1: the weight of every segment, and the total
+    u128 wt = segment_sums(w, ssum, sm.q[wid], wid, lane);
     if (lane == 0) {
         sm.tot_lo[wid] = static_cast<unsigned long long>(wt);
         sm.tot_hi[wid] = static_cast<unsigned long long>(wt >> 64);
@@ -817,81 +1070,74 @@ __global__ void __launch_bounds__(kThreads) seq_kernel(
         sm.t_hi = static_cast<unsigned long long>(t >> 64);
     }
     __syncthreads();
-    if (sm.sel) {  // the residual is empty: draw from p, with fresh level-1 totals
+    if (sm.sel) {  // the residual is empty: draw from p
         w.lq = nullptr;
-        wt = warp_range_sum(w, a1, b1, vec, lane);
-        __syncthreads();
-        if (lane == 0) {
-            sm.tot_lo[wid] = static_cast<unsigned long long>(wt);
-            sm.tot_hi[wid] = static_cast<unsigned long long>(wt >> 64);
-        }
+        segment_sums(w, ssum, sm.q[wid], wid, lane);
         __syncthreads();
     }
-    // which warp range holds t
-    u128 t = (static_cast<u128>(sm.t_hi) << 64) | sm.t_lo;
-    int sel = kWarps - 1;
+    // level 2: the segment whose inclusive prefix first exceeds t (each
+    // thread sums a run of consecutive segments; a block scan orders the runs)
+    const u128 t = (static_cast<u128>(sm.t_hi) << 64) | sm.t_lo;
     {
+        const int c = (nseg + kThreads - 1) / kThreads;
+        const int a = tid * c < nseg ? tid * c : nseg, e = a + c < nseg ? a + c : nseg;
         u128 run = 0;
-        for (int k = 0; k < kWarps; ++k) {
-            const u128 x = (static_cast<u128>(sm.tot_hi[k]) << 64) | sm.tot_lo[k];
-            if (t < run + x) {
-                sel = k;
-                break;
-            }
-            run += x;
+        for (int s = a; s < e; ++s) {
+            const ulonglong2 x = __ldcg(ssum + s);
+            run += (static_cast<u128>(x.y) << 64) | x.x;
         }
-        t -= run;
+        u128 all;
+        const u128 excl = block_excl_u128(run, sm.red, all);
+        if (excl <= t && t < excl + run) {
+            u128 acc = excl;
+            for (int s = a; s < e; ++s) {
+                const ulonglong2 x = __ldcg(ssum + s);
+                const u128 xs = (static_cast<u128>(x.y) << 64) | x.x;
+                if (t < acc + xs) {
+                    sm.seg = s;
+                    const u128 rem = t - acc;
+                    sm.t_lo = static_cast<unsigned long long>(rem);
+                    sm.t_hi = static_cast<unsigned long long>(rem >> 64);
+                    break;
+                }
+                acc += xs;
+            }
+        }
     }
     __syncthreads();
-    // level 2: the warps split that range again
-    const int A = sel * L1 < V ? sel * L1 : V;
-    const int Bnd = A + L1 < V ? A + L1 : V;
-    const int L2 = ((((Bnd - A) + kWarps - 1) / kWarps) + 3) & ~3;
-    int a2 = A + wid * L2, b2 = a2 + L2;
-    if (a2 > Bnd) a2 = Bnd;
-    if (b2 > Bnd) b2 = Bnd;
-    wt = warp_range_sum(w, a2, b2, vec, lane);
-    if (lane == 0) {
-        sm.tot_lo[wid] = static_cast<unsigned long long>(wt);
-        sm.tot_hi[wid] = static_cast<unsigned long long>(wt >> 64);
-    }
-    __syncthreads();
-    int sel2 = kWarps - 1;
-    {
-        u128 run = 0;
-        for (int k = 0; k < kWarps; ++k) {
-            const u128 x = (static_cast<u128>(sm.tot_hi[k]) << 64) | sm.tot_lo[k];
-            if (t < run + x) {
-                sel2 = k;
-                break;
-            }
-            run += x;
-        }
-        t -= run;
-    }
-    // level 3: warp 0 scans that sub-range in index order
+    // level 3: warp 0 rescans that segment in index order
     if (wid == 0) {
-        int a3 = A + sel2 * L2, b3 = a3 + L2;
-        if (a3 > Bnd) a3 = Bnd;
-        if (b3 > Bnd) b3 = Bnd;
-        u128 run = 0;
+        const int s = sm.seg;
         int tok = -1;
-        for (int base = a3; base < b3 && tok < 0; base += 32) {
-            const int v = base + lane;
-            const u128 x = v < b3 ? w.at(v) : static_cast<u128>(0);
-            u128 incl = x;
+        if (s >= 0) {
+            const u128 tt = (static_cast<u128>(sm.t_hi) << 64) | sm.t_lo;
+            const int v = s * kSegLen + 4 * lane;
+            float4 p, q;
+            w.load4(v, p, q);
+            u128 e[4];
+            w.weights4(v, p, q, e);
+            const u128 mine = e[0] + e[1] + e[2] + e[3];
+            u128 incl = mine;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const u128 y = shfl_up_u128(incl, o);
                 if (lane >= o) incl += y;
             }
-            const unsigned int hit = __ballot_sync(0xffffffffu, run + incl > t);
-            if (hit) tok = base + __ffs(hit) - 1;
-            const unsigned long long hlo =
-                __shfl_sync(0xffffffffu, static_cast<unsigned long long>(incl), 31);
-            const unsigned long long hhi =
-                __shfl_sync(0xffffffffu, static_cast<unsigned long long>(incl >> 64), 31);
-            run += (static_cast<u128>(hhi) << 64) | hlo;
+            const unsigned int hit = __ballot_sync(0xffffffffu, incl > tt);
+            if (hit) {
+                const int L = __ffs(hit) - 1;
+                if (lane == L) {
+                    u128 cum = incl - mine;
+                    for (int j = 0; j < 4; ++j) {
+                        cum += e[j];
+                        if (cum > tt) {
+                            tok = v + j;
+                            break;
+                        }
+                    }
+                }
+                tok = __shfl_sync(0xffffffffu, tok, L);
+            }
         }
         if (lane == 0) sm.token = tok >= 0 ? tok : V - 1;
     }
@@ -923,10 +1169,19 @@ cudaError_t launch_own_exp(const float* x, float* y, long long n, cudaStream_t s
     return cudaGetLastError();
 }
 
+// [rows] RowInfo, then [rows][segments] float segment maxima.
+static size_t info_bytes(size_t rows) { return ((rows * sizeof(RowInfo) + 255) / 256) * 256; }
+
+// ... then [B][segments] 128-bit segment weights of the draw.
+static size_t segmax_bytes(size_t rows, int V) {
+    const size_t seg = rows * static_cast<size_t>((V + kSegLen - 1) / kSegLen) * sizeof(float);
+    return ((seg + 255) / 256) * 256;
+}
+
 size_t rejection_workspace_bytes(int B, int Kd, int V) {
-    (void)V;
     const size_t rows = static_cast<size_t>(B) * (2 * static_cast<size_t>(Kd) + 1);
-    return ((rows * sizeof(RowInfo) + 255) / 256) * 256;
+    const size_t draw = static_cast<size_t>(B) * ((V + kSegLen - 1) / kSegLen) * 16;
+    return info_bytes(rows) + segmax_bytes(rows, V) + draw;
 }
 
 cudaError_t launch_accept_rejection(const float* target, const float* draft,
@@ -939,6 +1194,9 @@ cudaError_t launch_accept_rejection(const float* target, const float* draft,
     if (rows > 0x7fffffffll) return cudaErrorNotSupported;
     if (rejection_workspace_bytes(B, Kd, V) > ws_bytes) return cudaErrorInvalidValue;
     RowInfo* info = static_cast<RowInfo*>(ws);
+    float* segmax = reinterpret_cast<float*>(static_cast<char*>(ws) + info_bytes(rows));
+    ulonglong2* segsum = reinterpret_cast<ulonglong2*>(static_cast<char*>(ws) + info_bytes(rows) +
+                                                       segmax_bytes(rows, V));
     (void)wait_ns;
 
     const size_t smem = sizeof(RowSmem);
@@ -950,13 +1208,14 @@ cudaError_t launch_accept_rejection(const float* target, const float* draft,
                            ? 1
                            : 0;
     row_kernel<<<static_cast<unsigned>(rows), kRowThreads, smem, s>>>(
-        target, draft, n_target_rows, V, vec_ok, invT, static_cast<unsigned long long>(P), info);
+        target, draft, n_target_rows, V, vec_ok, invT, static_cast<unsigned long long>(P), info,
+        segmax);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     seq_kernel<<<B, kThreads, 0, s>>>(target, draft, drafts, Kd, V, vec_ok, invT,
                                       static_cast<unsigned long long>(seed),
                                       static_cast<unsigned long long>(offset), n_target_rows,
-                                      info, tokens, len, status);
+                                      info, segmax, segsum, tokens, len, status);
     return cudaGetLastError();
 }
 
