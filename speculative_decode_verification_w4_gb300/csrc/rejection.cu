@@ -513,16 +513,19 @@ __device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, flo
                 if (f.y >= f_lo) to_hist(f.y, h1, l1);
             }
         };
+        // last groups first: they left L2 least long ago in the max pass
         const float4* r4 = reinterpret_cast<const float4*>(row);
         const int V4 = V >> 2;
-        int i = tid;
-        for (; i + 3 * kRowThreads < V4; i += 4 * kRowThreads) {
-            const float4 a = __ldg(r4 + i), b = __ldg(r4 + i + kRowThreads),
-                         c = __ldg(r4 + i + 2 * kRowThreads), d = __ldg(r4 + i + 3 * kRowThreads);
+        const int nk = (V4 + kRowThreads - 1) / kRowThreads;
+        int i = (nk - 1) * kRowThreads + tid;
+        if (i >= V4) i -= kRowThreads;
+        for (; i - 3 * kRowThreads >= 0; i -= 4 * kRowThreads) {
+            const float4 a = __ldg(r4 + i), b = __ldg(r4 + i - kRowThreads),
+                         c = __ldg(r4 + i - 2 * kRowThreads), d = __ldg(r4 + i - 3 * kRowThreads);
             pair(a.x, a.y); pair(a.z, a.w); pair(b.x, b.y); pair(b.z, b.w);
             pair(c.x, c.y); pair(c.z, c.w); pair(d.x, d.y); pair(d.z, d.w);
         }
-        for (; i < V4; i += kRowThreads) {
+        for (; i >= 0; i -= kRowThreads) {
             const float4 a = __ldg(r4 + i);
             pair(a.x, a.y); pair(a.z, a.w);
         }
