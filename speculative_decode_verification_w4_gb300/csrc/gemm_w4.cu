@@ -937,31 +937,45 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
 combine:
     {
         // Fused split-K: the parts' partial tiles (rank order = k order) are
-        // summed by rank 0's consumers; the second barrier keeps every part's
-        // shared memory alive until rank 0 has read it.
+        // summed by the consumers of all the parts, each part taking its
+        // share of the tile's elements (every partial of an element loaded
+        // before the first add); the second barrier keeps every part's
+        // shared memory alive until all have read it.
         cg::cluster_group cl = cg::this_cluster();
         cl.sync();
         const int S = static_cast<int>(cl.num_blocks());
-        if (cl.block_rank() == 0 && warp < kConsumerWarps) {
+        if (warp < kConsumerWarps) {
             int aborted = 0;
-            for (int r = 0; r < S; ++r) aborted |= *cl.map_shared_rank(const_cast<int*>(abort_flag), r);
-            const int t = threadIdx.x;         // 0 .. 127
-            const int tok = t >> 4;            // verify row
-            const int r0 = (t & 15) * 8;       // eight tile rows
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int r = 0; r < S; ++r) {
-                const float* part = cl.map_shared_rank(reinterpret_cast<float*>(smem + kSmemPart), r);
-                const float4 a = *reinterpret_cast<const float4*>(part + tok * kTileRows + r0);
-                const float4 b = *reinterpret_cast<const float4*>(part + tok * kTileRows + r0 + 4);
-                acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-                acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+            const float* parts[kMaxClusterSplit];
+#pragma unroll
+            for (int r = 0; r < kMaxClusterSplit; ++r) {
+                parts[r] = nullptr;
+                if (r < S) {
+                    aborted |= *cl.map_shared_rank(const_cast<int*>(abort_flag), r);
+                    parts[r] = cl.map_shared_rank(reinterpret_cast<float*>(smem + kSmemPart), r);
+                }
             }
             const int n0 = static_cast<int>(blockIdx.x / S) * kTileRows;
-            if (!aborted && tok < p.dense_M) {
-                float* orow = p.out + static_cast<size_t>(tok) * p.ldo;
+            constexpr int kPairs = kMaxRows * kTileRows / 2;  // the tile as float2
+            for (int e = static_cast<int>(cl.block_rank()) * kGemmConsumers + threadIdx.x;
+                 e < kPairs; e += S * kGemmConsumers) {
+                const int tok = e / (kTileRows / 2), r0 = (e % (kTileRows / 2)) * 2;
+                float2 v[kMaxClusterSplit];
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (n0 + r0 + j < p.N) orow[n0 + r0 + j] = acc[j];
+                for (int r = 0; r < kMaxClusterSplit; ++r)
+                    if (r < S) v[r] = *reinterpret_cast<const float2*>(parts[r] + tok * kTileRows + r0);
+                float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int r = 0; r < kMaxClusterSplit; ++r)
+                    if (r < S) {
+                        acc.x += v[r].x;
+                        acc.y += v[r].y;
+                    }
+                if (!aborted && tok < p.dense_M) {
+                    float* orow = p.out + static_cast<size_t>(tok) * p.ldo;
+                    if (n0 + r0 < p.N) orow[n0 + r0] = acc.x;
+                    if (n0 + r0 + 1 < p.N) orow[n0 + r0 + 1] = acc.y;
+                }
             }
         }
         cl.sync();

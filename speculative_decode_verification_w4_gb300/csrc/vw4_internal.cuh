@@ -21,6 +21,7 @@ constexpr int kConsumerWarps = 4;  // each owns 32 rows of the tile
 constexpr int kWarpRows = kTileRows / kConsumerWarps;  // 32
 constexpr int kRowBlocks = kWarpRows / 16;             // 16-row MMA blocks per warp
 constexpr int kGemmThreads = (kConsumerWarps + 1) * 32;
+constexpr int kGemmConsumers = kConsumerWarps * 32;
 static_assert(kRowBlocks == 2, "the split-tile finish assumes two row blocks per warp");
 constexpr int kWBytes = kTileRows * (kStageK / 2);     // 16384: packed nibbles
 constexpr int kABytes = kMaxRows * kStageK * 2;        // 4096: fp16 activations
