@@ -15,7 +15,7 @@ constexpr int kTileRows = 128;     // weight rows per tile
 constexpr int kStageK = 256;       // k elements per pipeline stage
 constexpr int kStages = 4;         // pipeline depth
 constexpr int kMinUnitsPerCta = 4; // tile-aligned split-K: at least this many stages per part
-constexpr int kMaxSplit = 8;       // tile-aligned split-K: at most this many parts
+constexpr int kMaxSplit = 6;       // tile-aligned split-K: at most this many parts
 constexpr int kMaxClusterSplit = 6; // parts combined as one cluster (larger ones place poorly)
 constexpr int kConsumerWarps = 4;  // each owns 32 rows of the tile
 constexpr int kWarpRows = kTileRows / kConsumerWarps;  // 32
