@@ -550,6 +550,15 @@ __device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, flo
         info.S = S;
         return info;
     }
+    if (S == 0ull) {
+        // every W is 0 (the row's max is not finite: all -inf, or a +inf):
+        // the kept prefix is the first entry in (W desc, index asc) order,
+        // with mass 0
+        info.cut = 0;
+        info.tau = 0;
+        info.S = 0;
+        return info;
+    }
     const u128 TGT = static_cast<u128>(P) * S;
     // merged bucket masses, then a block-wide suffix sum: the crossing bucket
     // beta is the highest bucket whose suffix mass reaches the target
@@ -559,7 +568,11 @@ __device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, flo
         for (int w = 0; w < kRowWarps; ++w) m += sm.whist[w][tb];
     u128 tot_unused;
     const u128 incl = block_excl_u128(static_cast<u128>(m), sm.red, tot_unused) + m;
-    if (tid == 0) sm.ncand = 0;
+    if (tid == 0) {
+        sm.ncand = 0;
+        sm.beta = -1;
+    }
+    __syncthreads();
     if (tb >= 1 && (incl << 32) >= TGT && ((incl - m) << 32) < TGT) {
         sm.beta = tb;
         sm.above = static_cast<unsigned long long>(incl - m);
@@ -570,6 +583,12 @@ __device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, flo
     //    histogram but are gathered too; they are below the cut and sort
     //    after it, so the scan below never reaches them.
     const int beta = sm.beta;
+    if (beta < 0) {  // not reached: the entries >= c0 hold at least P/2^32 of S
+        info.cut = V - 1;
+        info.tau = 0;
+        info.S = S;
+        return info;
+    }
     float b_lo, b_hi;  // members of bucket beta: b_lo <= e < b_hi
     bucket_e_range(beta, b_lo, b_hi);
     {

@@ -72,6 +72,30 @@ def test_flat_distribution_cut_by_index():
     assert np.array_equal(ln, rl) and np.array_equal(tok, rt)
 
 
+@pytest.mark.parametrize("V", [3000, 2999])  # float4 rows, scalar rows
+def test_masked_vocabulary_and_degenerate_rows(V):
+    """-inf logits (a masked vocabulary), one-hot rows, a fully masked target
+    row and a target row holding +inf: in the last two every W is 0, so the
+    draw from them has total mass 0 and returns V - 1, as in the oracle."""
+    B, Kd = 12, 3
+    target, draft, _ = synth.stochastic_case(11 + V, B, Kd, V)
+    mask = synth.rng(V).random((B, Kd + 1, V)) < 0.3
+    target[mask] = -np.inf
+    draft[mask[:, :Kd]] = -np.inf
+    target[1, 0, :] = -np.inf
+    target[1, 0, 7] = 2.0
+    target[2, 1, :] = -np.inf
+    target[3, 0, 100] = np.inf
+    draft[4, 0, :] = -np.inf
+    draft[4, 0, 5] = 0.0
+    drafts = oracle.sample_drafts(draft, 0.6, 0.95, 3, 1 << 32)
+    tok, ln = gpu_accept(target, draft, drafts, 0.6, 0.95, 3, 0)
+    rt, rl, _ = oracle.accept_rejection(target, draft, drafts, 0.6, 0.95, 3, 0)
+    vw4.vw4_get_device_status()  # an empty residual sets a status bit: clear it
+    assert np.array_equal(ln, rl), (ln, rl)
+    assert np.array_equal(tok, rt)
+
+
 def test_temperature_zero_is_greedy():
     B, Kd, V = 9, 3, 500
     target, draft, drafts = synth.stochastic_case(6, B, Kd, V)
