@@ -317,11 +317,11 @@ VW4_API vw4_status verify_moe_w4(const vw4_weight* experts, int E, const void* A
     const long long U_max = static_cast<long long>(P) * n_tiles * T;
     if (G > U_max) G = U_max;
 
-    cudaError_t e = launch_route(expert_ids_dev, M, topk, E, ws, d->status,
-                                 combine ? nullptr : out_dev, ldo, N, s);
-    if (e != cudaSuccess) return cuda_fail(e, "route launch");
-    e = launch_prep_act(static_cast<const uint16_t*>(A_dev), lda, K, experts->fmt, 0,
-                        rows_are_pairs, topk, P, ws, P * n_tiles * kConsumerWarps, s);
+    // the prep launch routes the pairs as well
+    cudaError_t e = launch_prep_act(static_cast<const uint16_t*>(A_dev), lda, K, experts->fmt, 0,
+                                    rows_are_pairs, topk, P, ws, P * n_tiles * kConsumerWarps, s,
+                                    expert_ids_dev, E, d->status, combine ? nullptr : out_dev, ldo,
+                                    N);
     if (e != cudaSuccess) return cuda_fail(e, "prep_act launch");
     GemmParams p{};
     p.N = N;

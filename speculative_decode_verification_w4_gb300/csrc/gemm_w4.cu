@@ -116,10 +116,76 @@ __device__ __forceinline__ void load4_bf16(const uint16_t* a, bool vec, float* x
     }
 }
 
+// ------------------------------------------------------------ MoE router
+// Stable counting sort of the routed pairs by expert into segments of at
+// most 8 rows, one thread per pair (at most 64): a pair's segment is the
+// number of segments of the smaller expert ids plus its rank among the pairs
+// of its own expert, divided by 8.  Segments come out ordered by expert id,
+// and inside an expert by pair index.  Computed by threads 0 .. P-1 of a
+// block into a table in its shared memory; pairs with an invalid expert id
+// join no segment and are listed in bad[0 .. nbad).
+struct RouteScratch {
+    int ids[kMaxSeg];
+    int cnt[kMaxSeg];    // pairs of this pair's expert
+    int first[kMaxSeg];  // this pair is its expert's first
+    int bad[kMaxSeg];
+    int nbad, nseg;
+};
+
+__device__ void route_pairs(const int32_t* __restrict__ ids, int P, int E, SegTable& seg,
+                            RouteScratch& rs) {
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        rs.nbad = 0;
+        rs.nseg = 0;
+    }
+    if (tid < P) rs.ids[tid] = ids[tid];
+    __syncthreads();
+    int e = -1, rank = 0, valid = 0;
+    if (tid < P) {
+        e = rs.ids[tid];
+        valid = (e >= 0 && e < E) ? 1 : 0;
+        int cnt = 0;
+        for (int q = 0; q < P; ++q) {
+            const int same = rs.ids[q] == e ? 1 : 0;
+            cnt += same;
+            rank += (same && q < tid) ? 1 : 0;
+        }
+        rs.cnt[tid] = cnt;
+        rs.first[tid] = (valid && rank == 0) ? 1 : 0;
+        if (!valid) rs.bad[atomicAdd(&rs.nbad, 1)] = tid;
+    }
+    __syncthreads();
+    if (tid < P && valid) {
+        int base = 0;  // segments of the smaller expert ids
+        for (int q = 0; q < P; ++q)
+            if (rs.first[q] && rs.ids[q] < e) base += (rs.cnt[q] + kMaxRows - 1) / kMaxRows;
+        const int sgi = base + rank / kMaxRows, slot = rank % kMaxRows;
+        seg.dest[sgi][slot] = tid;
+        if (slot == 0) {
+            const int c = min(kMaxRows, rs.cnt[tid] - rank);
+            seg.expert[sgi] = e;
+            seg.count[sgi] = c;
+            for (int j = c; j < kMaxRows; ++j) seg.dest[sgi][j] = 0;
+        }
+        if (rs.first[tid]) atomicAdd(&rs.nseg, (rs.cnt[tid] + kMaxRows - 1) / kMaxRows);
+    }
+    __syncthreads();
+    if (tid == 0) seg.n_seg = rs.nseg;
+    __syncthreads();
+}
+
+// MoE calls (dense_M == 0) route the pairs here too: every block computes the
+// (tiny) routing into its own shared memory and block 0 publishes it for the
+// GEMM, marks invalid expert ids in the status word and zeroes their output
+// rows (out_zero, when the pair rows are the output).
 __global__ void __launch_bounds__(256) prep_act_kernel(
     const uint16_t* __restrict__ A, int lda, int vec_ok, int K, int fmt, int dense_M,
     int rows_are_pairs, int topk, SegTable* seg, uint8_t* act, uint32_t* tile_cnt, int n_cnt,
-    unsigned long long* am_key, uint32_t* am_cnt) {
+    unsigned long long* am_key, uint32_t* am_cnt, const int32_t* __restrict__ ids, int P, int E,
+    uint32_t* status, float* out_zero, int ldo, int N) {
+    __shared__ SegTable lt;
+    __shared__ RouteScratch rs;
     // The GEMM may start streaming weights now; it waits for this grid before
     // touching the activations or the tickets.  This grid itself may have
     // been launched while its predecessor (the previous GEMM, or the router)
@@ -145,10 +211,21 @@ __global__ void __launch_bounds__(256) prep_act_kernel(
         }
         src_row = r;
     } else {
-        if (sgi >= seg->n_seg) return;
-        count = seg->count[sgi];
+        route_pairs(ids, P, E, lt, rs);
+        if (blockIdx.x == 0) {
+            for (int i = threadIdx.x; i < static_cast<int>(sizeof(SegTable) / 4); i += blockDim.x)
+                reinterpret_cast<int*>(seg)[i] = reinterpret_cast<const int*>(&lt)[i];
+            if (threadIdx.x == 0 && rs.nbad) atomicOr(status, kStatusBadExpert);
+            if (out_zero != nullptr)
+                for (int bq = 0; bq < rs.nbad; ++bq) {
+                    float* row = out_zero + static_cast<size_t>(rs.bad[bq]) * ldo;
+                    for (int n = threadIdx.x; n < N; n += blockDim.x) row[n] = 0.0f;
+                }
+        }
+        if (sgi >= lt.n_seg) return;
+        count = lt.count[sgi];
         if (r < count) {
-            const int pr = seg->dest[sgi][r];
+            const int pr = lt.dest[sgi][r];
             src_row = rows_are_pairs ? pr : pr / topk;
         }
     }
@@ -215,69 +292,6 @@ __global__ void __launch_bounds__(256) prep_act_kernel(
     }
     *reinterpret_cast<uint4*>(dst + pos) = make_uint4(h[0], h[1], h[2], h[3]);
     if (lane == 0) inv[r] = pow2f(-n);
-}
-
-// ------------------------------------------------------------ MoE router
-// Stable counting sort of the routed pairs by expert into segments of at
-// most 8 rows, one thread per pair (at most 64): a pair's segment is the
-// number of segments of the smaller expert ids plus its rank among the pairs
-// of its own expert, divided by 8.  Segments come out ordered by expert id,
-// and inside an expert by pair index.  Pairs with an invalid expert are
-// dropped, flagged, and their direct output rows zeroed.
-__global__ void route_kernel(const int32_t* __restrict__ ids, int P, int E, SegTable* seg,
-                             uint32_t* status, float* out_zero, int ldo, int N) {
-    __shared__ int s_ids[kMaxSeg];
-    __shared__ int s_cnt[kMaxSeg];    // pairs of this pair's expert
-    __shared__ int s_first[kMaxSeg];  // this pair is its expert's first
-    __shared__ int s_bad[kMaxSeg];
-    __shared__ int s_nbad, s_nseg;
-    const int tid = threadIdx.x;
-    if (tid == 0) {
-        s_nbad = 0;
-        s_nseg = 0;
-    }
-    if (tid < P) s_ids[tid] = ids[tid];
-    __syncthreads();
-    int e = -1, rank = 0, valid = 0;
-    if (tid < P) {
-        e = s_ids[tid];
-        valid = (e >= 0 && e < E) ? 1 : 0;
-        int cnt = 0;
-        for (int q = 0; q < P; ++q) {
-            const int same = s_ids[q] == e ? 1 : 0;
-            cnt += same;
-            rank += (same && q < tid) ? 1 : 0;
-        }
-        s_cnt[tid] = cnt;
-        s_first[tid] = (valid && rank == 0) ? 1 : 0;
-        if (!valid) s_bad[atomicAdd(&s_nbad, 1)] = tid;
-    }
-    __syncthreads();
-    if (tid < P && valid) {
-        int base = 0;  // segments of the smaller expert ids
-        for (int q = 0; q < P; ++q)
-            if (s_first[q] && s_ids[q] < e) base += (s_cnt[q] + kMaxRows - 1) / kMaxRows;
-        const int sgi = base + rank / kMaxRows, slot = rank % kMaxRows;
-        seg->dest[sgi][slot] = tid;
-        if (slot == 0) {
-            const int c = min(kMaxRows, s_cnt[tid] - rank);
-            seg->expert[sgi] = e;
-            seg->count[sgi] = c;
-            for (int j = c; j < kMaxRows; ++j) seg->dest[sgi][j] = 0;
-        }
-        if (s_first[tid]) atomicAdd(&s_nseg, (s_cnt[tid] + kMaxRows - 1) / kMaxRows);
-    }
-    __syncthreads();
-    if (tid == 0) {
-        seg->n_seg = s_nseg;
-        if (s_nbad) atomicOr(status, kStatusBadExpert);
-    }
-    if (out_zero != nullptr) {
-        for (int b = 0; b < s_nbad; ++b) {
-            float* row = out_zero + (size_t)s_bad[b] * ldo;
-            for (int n = tid; n < N; n += blockDim.x) row[n] = 0.0f;
-        }
-    }
 }
 
 // ------------------------------------------------------------ GEMM pieces
@@ -986,6 +1000,9 @@ combine:
 __global__ void combine_kernel(const float* __restrict__ pair_out, const float* __restrict__ gates,
                                const int32_t* __restrict__ ids, int E, int M, int topk, int N,
                                float* __restrict__ out, int ldo) {
+    // launched early behind the GEMM; reads nothing before that grid is done
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int m = blockIdx.y;
     for (int n = blockIdx.x * blockDim.x + threadIdx.x; n < N; n += gridDim.x * blockDim.x) {
         float s = 0.0f;
@@ -1016,7 +1033,8 @@ __global__ void q4_0_split_kernel(const uint8_t* __restrict__ blocks, int N, int
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_prep_act(const uint16_t* A, int lda, int K, int fmt, int dense_M,
                             int rows_are_pairs, int topk, int n_seg_grid, const GemmWorkspace& ws,
-                            int n_counters, cudaStream_t s) {
+                            int n_counters, cudaStream_t s, const int32_t* ids, int E,
+                            uint32_t* status, float* out_zero, int ldo, int N) {
     const int T = K / kStageK;
     const int vec_ok = ((reinterpret_cast<uintptr_t>(A) & 15u) == 0 && lda % 8 == 0) ? 1 : 0;
     // a programmatic dependent of whatever kernel precedes it on the stream
@@ -1032,7 +1050,8 @@ cudaError_t launch_prep_act(const uint16_t* A, int lda, int K, int fmt, int dens
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, prep_act_kernel, A, lda, vec_ok, K, fmt, dense_M,
                               rows_are_pairs, topk, ws.seg, ws.act, ws.tile_cnt, n_counters,
-                              ws.am_key, ws.am_cnt);
+                              ws.am_key, ws.am_cnt, ids, dense_M > 0 ? 0 : n_seg_grid, E, status,
+                              out_zero, ldo, N);
 }
 
 template <int FMT>
@@ -1087,16 +1106,16 @@ int gemm_blocks_per_sm(int fmt) {
 
 cudaError_t launch_combine(const float* pair_out, const float* gates, const int32_t* ids,
                                int E, int M, int topk, int N, float* out, int ldo, cudaStream_t s) {
-    dim3 grid((N + 255) / 256, M);
-    combine_kernel<<<grid, 256, 0, s>>>(pair_out, gates, ids, E, M, topk, N, out, ldo);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_route(const int32_t* expert_ids, int M, int topk, int E,
-                              const GemmWorkspace& ws, uint32_t* status, float* out_zero, int ldo,
-                              int N, cudaStream_t s) {
-    route_kernel<<<1, 64, 0, s>>>(expert_ids, M * topk, E, ws.seg, status, out_zero, ldo, N);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((N + 255) / 256, M);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, combine_kernel, pair_out, gates, ids, E, M, topk, N, out, ldo);
 }
 
 cudaError_t launch_q4_0_split(const uint8_t* blocks, int N, int K, uint8_t* q, __half* d,

@@ -98,10 +98,9 @@ GemmWorkspace gemm_workspace_layout(void* base, int n_seg_max, int N, int K, int
 // Kernel launchers (gemm_w4.cu).  All asynchronous on `s`.
 cudaError_t launch_prep_act(const uint16_t* A, int lda, int K, int fmt, int dense_M,
                             int rows_are_pairs, int topk, int n_seg_grid, const GemmWorkspace& ws,
-                            int n_counters, cudaStream_t s);
-cudaError_t launch_route(const int32_t* expert_ids, int M, int topk, int E,
-                         const GemmWorkspace& ws, uint32_t* status, float* out_zero, int ldo,
-                         int N, cudaStream_t s);
+                            int n_counters, cudaStream_t s, const int32_t* ids = nullptr, int E = 0,
+                            uint32_t* status = nullptr, float* out_zero = nullptr, int ldo = 0,
+                            int N = 0);
 cudaError_t launch_gemm(int fmt, const CUtensorMap& tmW, const CUtensorMap& tmS,
                         const GemmParams& p, int grid, int cluster, cudaStream_t s);
 cudaError_t launch_combine(const float* pair_out, const float* gates, const int32_t* ids,
