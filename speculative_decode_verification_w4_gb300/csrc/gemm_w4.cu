@@ -743,6 +743,9 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     const int spitch = 16 * sg_n;
     const int smask = sg_n == kScaleGroup ? kScaleGroup - 1 : 0x7fffffff;
     const unsigned long long my_first_tile = u_begin / T;
+    // fused argmax: this warp's running key of verify row lane / 4 (held in
+    // the lanes with lane % 4 == 0), published once when the warp is done
+    unsigned long long am_run = 0ull;
     for (unsigned long long u = u_begin; u < u_end;) {
         const unsigned long long tg = u / T;
         const int st0 = static_cast<int>(u % T);
@@ -842,16 +845,11 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                     k0 = umax64(k0, __shfl_xor_sync(0xffffffffu, k0, o));
                     k1 = umax64(k1, __shfl_xor_sync(0xffffffffu, k1, o));
                 }
-                if (g == 0) {
-                    if (2 * c < p.argmax_M && k0) atomicMax(&p.am_key[2 * c], k0);
-                    if (2 * c + 1 < p.argmax_M && k1) atomicMax(&p.am_key[2 * c + 1], k1);
-                }
-                __syncwarp();
-                uint32_t old = 0;
-                if (lane == 0) old = atom_add_acq_rel_gpu(p.am_cnt, 1u);
-                old = __shfl_sync(0xffffffffu, old, 0);
-                if (old + 1 == static_cast<uint32_t>(kConsumerWarps * n_tiles))
-                    argmax_finish(p, lane);
+                // lane c (< 4) holds rows 2c and 2c + 1; row t goes to lane 4t
+                const int t = lane >> 2;
+                const unsigned long long a = __shfl_sync(0xffffffffu, k0, t >> 1);
+                const unsigned long long b = __shfl_sync(0xffffffffu, k1, t >> 1);
+                am_run = umax64(am_run, (t & 1) ? b : a);
             }
             continue;
         }
@@ -938,13 +936,19 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         if (p.argmax_M > 0) {
             kb = umax64(kb, __shfl_xor_sync(0xffffffffu, kb, 1));
             kb = umax64(kb, __shfl_xor_sync(0xffffffffu, kb, 2));
-            if ((lane & 3) == 0 && tok < p.argmax_M && kb) atomicMax(&p.am_key[tok], kb);
-            __syncwarp();
-            uint32_t o2 = 0;
-            if (lane == 0) o2 = atom_add_acq_rel_gpu(p.am_cnt, 1u);
-            o2 = __shfl_sync(0xffffffffu, o2, 0);
-            if (o2 + 1 == static_cast<uint32_t>(kConsumerWarps * n_tiles)) argmax_finish(p, lane);
+            am_run = umax64(am_run, kb);  // lane 4 tok holds row tok
         }
+    }
+    if (p.argmax_M > 0) {
+        // one 64-bit max per verify row and warp, then a ticket: the last of
+        // the grid's consumer warps reads the maxima out
+        const int t = lane >> 2;
+        if ((lane & 3) == 0 && t < p.argmax_M && am_run) atomicMax(&p.am_key[t], am_run);
+        __syncwarp();
+        uint32_t o2 = 0;
+        if (lane == 0) o2 = atom_add_acq_rel_gpu(p.am_cnt, 1u);
+        o2 = __shfl_sync(0xffffffffu, o2, 0);
+        if (o2 + 1 == static_cast<uint32_t>(kConsumerWarps * G)) argmax_finish(p, lane);
     }
     }
     if (!cluster_mode) return;
