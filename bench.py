@@ -382,20 +382,37 @@ def run_accept_timings(device, stream):
         out[f"rejection_K{Kd}"] = {"us": round(us, 1),
                                    "logit_gbs": round(B * (2 * Kd + 1) * V * 4 / (us * 1e-6) / 1e9, 1)}
         del tgt, drf
-    V = 262144
-    lg = torch.randn((1, 8, V), generator=g, device=device)
-    drafts = torch.argmax(lg[:, :7], dim=-1).to(torch.int32)
-    for _ in range(3):
-        vw4.accept_greedy(lg, drafts, stream=stream)
+    # greedy accept of 7 drafts from 8 fp32 logits rows of the LM head (V =
+    # 262144): a CUDA graph over 20 logits copies (160 MB, more than L2), so
+    # that neither host launch work nor L2 residency enters the number
+    V, n_copy = 262144, 20
+    lgs = [torch.randn((1, 8, V), generator=g, device=device) for _ in range(n_copy)]
+    drafts = torch.argmax(lgs[0][:, :7], dim=-1).to(torch.int32)
+    tk = torch.empty((1, 8), dtype=torch.int32, device=device)
+    ln = torch.empty((1,), dtype=torch.int32, device=device)
+    gs = torch.cuda.Stream(device)
+    for lg in lgs:
+        vw4.accept_greedy(lg, drafts, tokens=tk, length=ln, stream=gs)
     torch.cuda.synchronize()
-    reps = 20
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(reps):
-        vw4.accept_greedy(lg, drafts, stream=stream)
-    e1.record(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=gs):
+        for lg in lgs:
+            vw4.accept_greedy(lg, drafts, tokens=tk, length=ln, stream=gs)
+    reps = 10
+    with torch.cuda.stream(gs):
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(gs)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(gs)
     torch.cuda.synchronize()
-    out["greedy_lmhead_unfused"] = {"us": round(e0.elapsed_time(e1) / reps * 1e3, 2)}
+    us = e0.elapsed_time(e1) / (reps * n_copy) * 1e3
+    out["greedy_lmhead_unfused"] = {"us": round(us, 2),
+                                    "logit_gbs": round(8 * V * 4 / (us * 1e-6) / 1e9, 1)}
+    del lgs
     torch.cuda.empty_cache()
     return out
 

@@ -36,27 +36,55 @@ __device__ __forceinline__ unsigned long long kmax(unsigned long long a, unsigne
 }
 
 __global__ void __cluster_dims__(kArgCluster, 1, 1) __launch_bounds__(kArgThreads)
-    row_argmax_kernel(const float* __restrict__ logits, long long V, int32_t* __restrict__ out) {
+    row_argmax_kernel(const float* __restrict__ logits, long long V, int vec,
+                      int32_t* __restrict__ out) {
     cg::cluster_group cluster = cg::this_cluster();
     __shared__ unsigned long long s_warp[kArgThreads / 32];
     __shared__ unsigned long long s_key;
     const int rank = static_cast<int>(cluster.block_rank());
     const long long row = blockIdx.x / kArgCluster;
     const float* x = logits + row * V;
-    const long long chunk = (V + kArgCluster - 1) / kArgCluster;
-    const long long lo = rank * chunk;
-    const long long hi = (lo + chunk < V) ? lo + chunk : V;
     unsigned long long best = 0ull;
-    long long v = lo + threadIdx.x;
-    for (; v + 3 * kArgThreads < hi; v += 4 * kArgThreads) {
-        const float a0 = __ldg(x + v), a1 = __ldg(x + v + kArgThreads);
-        const float a2 = __ldg(x + v + 2 * kArgThreads), a3 = __ldg(x + v + 3 * kArgThreads);
-        best = kmax(best, greedy_key(a0, static_cast<uint32_t>(v)));
-        best = kmax(best, greedy_key(a1, static_cast<uint32_t>(v + kArgThreads)));
-        best = kmax(best, greedy_key(a2, static_cast<uint32_t>(v + 2 * kArgThreads)));
-        best = kmax(best, greedy_key(a3, static_cast<uint32_t>(v + 3 * kArgThreads)));
+    if (vec) {
+        // 16-byte rows: float4 groups, eight loads in flight per thread; the
+        // CTA's slice is a whole number of groups
+        const long long V4 = V >> 2;
+        const long long chunk = (V4 + kArgCluster - 1) / kArgCluster;
+        const long long lo = rank * chunk;
+        const long long hi = (lo + chunk < V4) ? lo + chunk : V4;
+        const float4* x4 = reinterpret_cast<const float4*>(x);
+        for (long long g0 = lo + threadIdx.x; g0 < hi; g0 += 8 * kArgThreads) {
+            float4 a[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const long long g = g0 + static_cast<long long>(j) * kArgThreads;
+                a[j] = g < hi ? __ldg(x4 + g) : make_float4(NAN, NAN, NAN, NAN);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t v = static_cast<uint32_t>(4 * (g0 + static_cast<long long>(j) * kArgThreads));
+                best = kmax(best, greedy_key(a[j].x, v));
+                best = kmax(best, greedy_key(a[j].y, v + 1));
+                best = kmax(best, greedy_key(a[j].z, v + 2));
+                best = kmax(best, greedy_key(a[j].w, v + 3));
+            }
+        }
+    } else {
+        const long long chunk = (V + kArgCluster - 1) / kArgCluster;
+        const long long lo = rank * chunk;
+        const long long hi = (lo + chunk < V) ? lo + chunk : V;
+        long long v = lo + threadIdx.x;
+        for (; v + 3 * kArgThreads < hi; v += 4 * kArgThreads) {
+            const float a0 = __ldg(x + v), a1 = __ldg(x + v + kArgThreads);
+            const float a2 = __ldg(x + v + 2 * kArgThreads), a3 = __ldg(x + v + 3 * kArgThreads);
+            best = kmax(best, greedy_key(a0, static_cast<uint32_t>(v)));
+            best = kmax(best, greedy_key(a1, static_cast<uint32_t>(v + kArgThreads)));
+            best = kmax(best, greedy_key(a2, static_cast<uint32_t>(v + 2 * kArgThreads)));
+            best = kmax(best, greedy_key(a3, static_cast<uint32_t>(v + 3 * kArgThreads)));
+        }
+        for (; v < hi; v += kArgThreads)
+            best = kmax(best, greedy_key(__ldg(x + v), static_cast<uint32_t>(v)));
     }
-    for (; v < hi; v += kArgThreads) best = kmax(best, greedy_key(__ldg(x + v), static_cast<uint32_t>(v)));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) best = kmax(best, __shfl_xor_sync(0xffffffffu, best, o));
     if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = best;
@@ -81,6 +109,9 @@ __global__ void greedy_finish_kernel(const int32_t* __restrict__ drafts,
                                      const int32_t* argmax /* [B][Kd+1], may alias tokens */,
                                      int B, int Kd, int V, int32_t* tokens, int32_t* len,
                                      uint32_t* status) {
+    // launched early behind the argmax (or whatever precedes it); reads
+    // nothing before that grid is done
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= B) return;
     int32_t g[9];
@@ -112,14 +143,23 @@ cudaError_t launch_accept_greedy(const float* logits, const int32_t* drafts,
     const int32_t* am = argmax_in;
     if (am == nullptr) {
         const long long rows = static_cast<long long>(B) * (Kd + 1);
+        const int vec = (V % 4 == 0 && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0) ? 1 : 0;
         row_argmax_kernel<<<static_cast<unsigned>(rows * kArgCluster), kArgThreads, 0, s>>>(
-            logits, V, tokens);
+            logits, V, vec, tokens);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         am = tokens;
     }
-    greedy_finish_kernel<<<(B + 127) / 128, 128, 0, s>>>(drafts, am, B, Kd, V, tokens, len, status);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((B + 127) / 128);
+    cfg.blockDim = dim3(128);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, greedy_finish_kernel, drafts, am, B, Kd, V, tokens, len, status);
 }
 
 }  // namespace vw4
