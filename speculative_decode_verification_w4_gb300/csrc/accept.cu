@@ -7,8 +7,8 @@
 // the target's token at the first mismatch (or the bonus token) is always
 // committed.  Argmax ties go to the lowest index; NaN never wins.
 //
-// Row argmax: one thread-block cluster of 8 CTAs per logits row, each CTA
-// scanning one eighth of the vocabulary; the eight partial maxima are combined
+// Row argmax: one thread-block cluster of 16 CTAs per logits row, each CTA
+// scanning one sixteenth of the vocabulary; the partial maxima are combined
 // through distributed shared memory, so no global scratch is needed.
 #include <cooperative_groups.h>
 
@@ -19,7 +19,7 @@ namespace cg = cooperative_groups;
 namespace vw4 {
 
 constexpr uint32_t kStatusBadDraft = 0x1u;
-constexpr int kArgCluster = 8;
+constexpr int kArgCluster = 16;  // a non-portable cluster size, opted into at launch
 constexpr int kArgThreads = 512;
 
 // (ordered value, ~index): larger key = larger value, then smaller index.
@@ -144,6 +144,13 @@ cudaError_t launch_accept_greedy(const float* logits, const int32_t* drafts,
     if (am == nullptr) {
         const long long rows = static_cast<long long>(B) * (Kd + 1);
         const int vec = (V % 4 == 0 && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0) ? 1 : 0;
+        static bool attr_done = false;
+        if (!attr_done) {
+            cudaError_t e = cudaFuncSetAttribute(
+                row_argmax_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+            attr_done = true;
+        }
         row_argmax_kernel<<<static_cast<unsigned>(rows * kArgCluster), kArgThreads, 0, s>>>(
             logits, V, vec, tokens);
         cudaError_t e = cudaGetLastError();
