@@ -344,9 +344,21 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Q4_0 nibble pairs -> f16x2 of (q - 8): 0x6400|q is 1024 + q exactly.
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Q4_0 nibble pairs -> f16x2 of (q - 8).  Nibbles at bits 0..3 and 16..19:
+// 0x6400 | q is 1024 + q exactly, minus 1032.  Nibbles at bits 4..7 and
+// 20..23 (no shift needed): 0x6400 | q << 4 is 1024 + 16 q exactly, and one
+// fma with 1/16 and -72 gives q - 8 exactly.
 __device__ __forceinline__ uint32_t q4pair(uint32_t x) {
     return hsub2((x & 0x000F000Fu) | 0x64006400u, 0x64086408u);
+}
+__device__ __forceinline__ uint32_t q4pair_hi(uint32_t x) {
+    return hfma2((x & 0x00F000F0u) | 0x64006400u, 0x2C002C00u, 0xD480D480u);
 }
 
 // One 256-wide k slice of the warp's 32 rows, as two 16-row MMA blocks that
@@ -468,9 +480,9 @@ __device__ __forceinline__ void compute_q4_0(const ActRegs& a, const WRegsQ4& r,
         const uint32_t x0 = r.x0[beta], x1 = r.x1[beta];
         const uint4& b = a.bf[beta];
         float t[4] = {0.f, 0.f, 0.f, 0.f};
-        mma16816(t, q4pair(x0), q4pair(x1), q4pair(x0 >> 8), q4pair(x1 >> 8), b.x, b.y);
-        mma16816(t, q4pair(x0 >> 4), q4pair(x1 >> 4), q4pair(x0 >> 12), q4pair(x1 >> 12), b.z,
-                 b.w);
+        const uint32_t y0 = x0 >> 8, y1 = x1 >> 8;
+        mma16816(t, q4pair(x0), q4pair(x1), q4pair(y0), q4pair(y1), b.x, b.y);
+        mma16816(t, q4pair_hi(x0), q4pair_hi(x1), q4pair_hi(y0), q4pair_hi(y1), b.z, b.w);
         const __half2 dh0 = *reinterpret_cast<const __half2*>(&dw0[beta >> 1]);
         const __half2 dh1 = *reinterpret_cast<const __half2*>(&dw1[beta >> 1]);
         const float e0 = (beta & 1) ? __high2float(dh0) : __low2float(dh0);
