@@ -22,8 +22,8 @@ def gpu_accept(target, draft, drafts, T, top_p, seed, offset):
 
 
 def test_own_exp_bitwise_equal_to_oracle_over_all_inputs():
-    """Every fp32 x in [-32, 0] (about 1.1e9 values), plus values below."""
-    start, stop = 0x80000000, 0xC2000000 + 1024  # -0.0 ... just below -32
+    """Every fp32 x in [-104, 0] (about 1.1e9 values; below -32 both give 0)."""
+    start, stop = 0x80000000, 0xC2D00000 + 1  # -0.0 ... -104.0
     chunk = 1 << 26
     for lo in range(start, stop, chunk):
         hi = min(stop, lo + chunk)
@@ -33,6 +33,10 @@ def test_own_exp_bitwise_equal_to_oracle_over_all_inputs():
         ref = oracle.own_exp_array(x)
         bad = y.view(np.uint32) != ref.view(np.uint32)
         assert not bad.any(), (lo, x[bad][:4], y[bad][:4], ref[bad][:4])
+    # the special values: -inf and NaN give 0 on both sides
+    sp = np.array([-np.inf, np.nan, -1e30, 0.0], np.float32)
+    y = vw4.vw4_own_exp(torch.from_numpy(sp).cuda()).cpu().numpy()
+    assert np.array_equal(y.view(np.uint32), oracle.own_exp_array(sp).view(np.uint32))
 
 
 @pytest.mark.parametrize("B,Kd,V,top_p", [(16, 3, 16, 0.95), (64, 1, 1000, 0.95),
