@@ -51,7 +51,7 @@ namespace {
 
 constexpr uint32_t kStatusBadDraft = 0x1u;
 constexpr uint32_t kStatusZeroResidual = 0x8u;
-constexpr int kThreads = 512;  // both kernels
+constexpr int kThreads = 512;  // the sequence kernel
 constexpr int kWarps = kThreads / 32;
 constexpr int kLogBuckets = 16 + 37 * 8;  // exact 0..15, then 8 per binade up to 2^40
 constexpr int kLinBuckets = 256;
@@ -322,9 +322,10 @@ __device__ __forceinline__ void atomic_add_u64_split(unsigned long long* a, unsi
     if (hi + carry) atomicAdd(&w[1], hi + carry);
 }
 
-// One CTA per logits row.  The row is streamed three times (the second and
-// third from L2): the max; own_exp, sum W and the mass histogram of the
-// entries >= c0; the members of the crossing bucket.
+// One 512-thread CTA per logits row, two per SM.  The row is streamed three
+// times (the second and third partly from L2): the max and the segment
+// maxima; own_exp, sum W and the mass histogram of the entries >= c0; the
+// members of the crossing bucket, in the segments that can hold them.
 constexpr int kRowThreads = 512;
 constexpr int kRowWarps = kRowThreads / 32;
 static_assert(kRowThreads >= kLogBuckets, "one thread per log bucket in the suffix scan");
