@@ -507,9 +507,19 @@ def run_head_timings(device, stream):
         vw4.accept_greedy(None, drafts, target_argmax=am, B=1, V=V, tokens=tokens,
                           length=length, stream=stream)
 
-    us = timed(head, 10)
     hb = weight_bytes(V, K) + 8 * K * 2
-    out["lmhead_fused_greedy_m8"] = {"us": round(us, 2), "gbs": round(hb / (us * 1e-6) / 1e9, 1)}
+    us = timed(head, 10)
+    out["lmhead_fused_greedy_m8_two_launches"] = {
+        "us": round(us, 2), "gbs": round(hb / (us * 1e-6) / 1e9, 1),
+        "what": "verify_gemm_w4 (logits + fused argmax) then accept_greedy"}
+
+    def head1(c):  # GEMM, argmax and accept in one launch, no logits written
+        vw4.verify_greedy_w4(vw4.FMT_NVFP4, *heads[c], Ah, drafts, tokens=tokens, length=length,
+                             workspace=ws, stream=stream)
+
+    us = timed(head1, 10)
+    out["lmhead_fused_greedy_m8"] = {"us": round(us, 2), "gbs": round(hb / (us * 1e-6) / 1e9, 1),
+                                     "what": "verify_greedy_w4: one launch, no logits written"}
     del heads, logits
     torch.cuda.empty_cache()
     return out

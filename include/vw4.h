@@ -128,6 +128,38 @@ VW4_API vw4_status verify_gemm_w4(const vw4_weight* W, const void* A_dev, int M,
                                   void* workspace_dev, size_t ws_bytes, void* stream);
 
 /*
+ * verify_greedy_w4 -- the verify GEMM, its row argmax and the greedy accept
+ * in one launch.
+ *
+ * Defined by: "Accelerating Gemini Nano models on Pixel with frozen
+ * Multi-Token Prediction", section 3 (verify the drafted tokens in one pass,
+ * keep the longest prefix the target agrees with, plus the target's own token
+ * at the first disagreement) with the argmax taken over the verify GEMM's
+ * fp32 outputs as verify_gemm_w4's row_argmax does, and Ollama's mtp.go
+ * commit log paragraph "Greedy is a special case of sampled decoding".
+ *
+ * The GEMM runs over M = B * (Kd + 1) rows: row b (Kd + 1) + i of A is
+ * sequence b's hidden state at verify position i.  The last warp of the
+ * launch turns the row argmaxes into the committed run, exactly as
+ * accept_greedy does with them: tokens[b][i] = drafts[b][i] for i < n, the
+ * argmax of position n at i == n, -1 after; len[b] = n + 1, n the length of
+ * the agreeing prefix.
+ *
+ * W, A_dev, lda   as verify_gemm_w4; B * (Kd + 1) must be 1..8.
+ * drafts_dev      int32 [B][Kd] (may be NULL when Kd == 0).
+ * tokens_dev      int32 [B][Kd + 1]; len_dev int32 [B].
+ * out_dev, ldo    optional fp32 [M][ldo] logits; NULL = not written.
+ * workspace_dev / ws_bytes  as verify_gemm_w4 for M rows.
+ * Errors: as verify_gemm_w4, and VW4_ERR_INVALID_ARG for B < 1, Kd < 0,
+ * B * (Kd + 1) > 8 or null outputs.  A draft id outside [0, N) ends the
+ * prefix and sets VW4_DEV_BAD_DRAFT_ID in the device status word.
+ */
+VW4_API vw4_status verify_greedy_w4(const vw4_weight* W, const void* A_dev, int lda,
+                                    const int32_t* drafts_dev, int B, int Kd, int32_t* tokens_dev,
+                                    int32_t* len_dev, float* out_dev, int ldo,
+                                    void* workspace_dev, size_t ws_bytes, void* stream);
+
+/*
  * verify_moe_w4 -- segmented expert-gather verify GEMM for MoE heads.
  *
  * Defined by: Ollama commit log for x/mlxrunner/mtp.go, paragraph on the

@@ -41,7 +41,7 @@ STATUS_NAMES = {0: "VW4_OK", 1: "VW4_ERR_INVALID_ARG", 2: "VW4_ERR_UNSUPPORTED",
 EXPORTS = ("verify_gemm_w4", "verify_moe_w4", "accept_greedy", "accept_rejection",
            "vw4_workspace_bytes", "vw4_get_device_status", "vw4_q4_0_from_blocks",
            "vw4_status_str", "vw4_last_error_string", "vw4_version", "vw4_set_wait_limit_ns",
-           "vw4_own_exp", "verify_gemm_w4_noalloc")
+           "vw4_own_exp", "verify_gemm_w4_noalloc", "verify_greedy_w4")
 
 
 class VW4Error(RuntimeError):
@@ -96,6 +96,8 @@ def load_library(path: str = LIB_PATH):
             "vw4_set_wait_limit_ns": (None, [U64]),
             "vw4_own_exp": (I, [P, P, ctypes.c_int64, P]),
             "verify_gemm_w4_noalloc": (I, [ctypes.POINTER(Weight), P, I, I, P, I, P, P]),
+            "verify_greedy_w4": (I, [ctypes.POINTER(Weight), P, I, P, I, I, P, P, P, I, P,
+                                     ctypes.c_size_t, P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -185,6 +187,31 @@ def verify_gemm_w4(fmt: int, q: torch.Tensor, scales: torch.Tensor, tensor_scale
                                          ws.numel(), _stream(stream))
     _check(code, "verify_gemm_w4")
     return out
+
+
+def verify_greedy_w4(fmt: int, q: torch.Tensor, scales: torch.Tensor, tensor_scale: float,
+                     A: torch.Tensor, drafts: torch.Tensor, out: torch.Tensor | None = None,
+                     tokens=None, length=None, workspace=None, stream=None):
+    """The verify GEMM over A [B*(Kd+1), K] (sequence b's rows together), its
+    row argmax and the greedy accept of drafts int32 [B, Kd], in one launch ->
+    (tokens [B, Kd+1], len [B]).  out: optional fp32 [B*(Kd+1), N] logits (not
+    written when None); see vw4.h."""
+    N, K = q.shape[0], q.shape[1] * 2
+    B, Kd = drafts.shape
+    M = B * (Kd + 1)
+    if A.dtype != torch.bfloat16 or A.shape[0] != M:
+        raise ValueError("A must be bfloat16 [B*(Kd+1), K]")
+    if tokens is None:
+        tokens = torch.empty((B, Kd + 1), dtype=torch.int32, device=A.device)
+    if length is None:
+        length = torch.empty((B,), dtype=torch.int32, device=A.device)
+    W = make_weight(fmt, q, scales, tensor_scale, N, K)
+    ws = _workspace(workspace, vw4_workspace_bytes(OP_GEMM, M, N, K), A.device)
+    code = load_library().verify_greedy_w4(
+        ctypes.byref(W), _ptr(A), A.stride(0), _ptr(drafts), B, Kd, _ptr(tokens), _ptr(length),
+        _ptr(out), out.stride(0) if out is not None else 0, _ptr(ws), ws.numel(), _stream(stream))
+    _check(code, "verify_greedy_w4")
+    return tokens, length
 
 
 class PreparedGemm:

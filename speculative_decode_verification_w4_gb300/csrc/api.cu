@@ -191,13 +191,25 @@ VW4_API size_t vw4_workspace_bytes(int op, int a, int b, int c) {
     return 0;
 }
 
-VW4_API vw4_status verify_gemm_w4(const vw4_weight* W, const void* A_dev, int M, int lda,
-                                  float* out_dev, int ldo, int32_t* row_argmax_dev,
-                                  void* workspace_dev, size_t ws_bytes, void* stream) {
+// The verify GEMM launch behind verify_gemm_w4 and verify_greedy_w4 (greedy
+// non-null: the fused argmax feeds the greedy accept in the same launch, and
+// out_dev may be null).
+struct GreedyArgs {
+    const int32_t* drafts;
+    int B, Kd;
+    int32_t* tokens;
+    int32_t* len;
+};
+
+static vw4_status gemm_entry(const vw4_weight* W, const void* A_dev, int M, int lda,
+                             float* out_dev, int ldo, int32_t* row_argmax_dev,
+                             const GreedyArgs* greedy, void* workspace_dev, size_t ws_bytes,
+                             void* stream) {
     vw4_status st = check_weight(W);
     if (st != VW4_OK) return st;
-    if (!A_dev || !out_dev) return VW4_ERR_INVALID_ARG;
-    if (M < 1 || M > kMaxRows || lda < W->K || ldo < W->N) return VW4_ERR_INVALID_ARG;
+    if (!A_dev || (!out_dev && !greedy)) return VW4_ERR_INVALID_ARG;
+    if (M < 1 || M > kMaxRows || lda < W->K || (out_dev && ldo < W->N))
+        return VW4_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(A_dev) & 1u) || (reinterpret_cast<uintptr_t>(out_dev) & 3u))
         return VW4_ERR_ALIGN;
     if (!workspace_dev) return VW4_ERR_WORKSPACE;
@@ -241,7 +253,8 @@ VW4_API vw4_status verify_gemm_w4(const vw4_weight* W, const void* A_dev, int M,
     if (G > U) G = U;
     // Up to kMaxClusterSplit parts (and no fused argmax): the parts of a tile
     // form one cluster and combine over distributed shared memory.
-    const bool clustered = split > 1 && split <= kMaxClusterSplit && row_argmax_dev == nullptr;
+    const bool fused_argmax = row_argmax_dev != nullptr || greedy != nullptr;
+    const bool clustered = split > 1 && split <= kMaxClusterSplit && !fused_argmax;
 
     cudaError_t e = launch_prep_act(static_cast<const uint16_t*>(A_dev), lda, K, W->fmt, M, 0, 1,
                                     1, ws, n_tiles * kConsumerWarps, s);
@@ -259,7 +272,7 @@ VW4_API vw4_status verify_gemm_w4(const vw4_weight* W, const void* A_dev, int M,
     p.out = out_dev;
     p.ldo = ldo;
     p.dense_M = M;
-    p.argmax_M = row_argmax_dev ? M : 0;
+    p.argmax_M = fused_argmax ? M : 0;
     p.partials = ws.partials;
     p.tile_cnt = ws.tile_cnt;
     p.am_key = ws.am_key;
@@ -268,9 +281,34 @@ VW4_API vw4_status verify_gemm_w4(const vw4_weight* W, const void* A_dev, int M,
     p.status = d->status;
     p.wait_ns = g_wait_ns;
     p.cluster = clustered ? 1 : 0;
+    if (greedy) {
+        p.greedy_B = greedy->B;
+        p.greedy_Kd = greedy->Kd;
+        p.drafts = greedy->drafts;
+        p.tokens = greedy->tokens;
+        p.len = greedy->len;
+    }
     e = launch_gemm(W->fmt, tmW, tmS, p, static_cast<int>(G), clustered ? split : 1, s);
     if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
     return VW4_OK;
+}
+
+VW4_API vw4_status verify_gemm_w4(const vw4_weight* W, const void* A_dev, int M, int lda,
+                                  float* out_dev, int ldo, int32_t* row_argmax_dev,
+                                  void* workspace_dev, size_t ws_bytes, void* stream) {
+    return gemm_entry(W, A_dev, M, lda, out_dev, ldo, row_argmax_dev, nullptr, workspace_dev,
+                      ws_bytes, stream);
+}
+
+VW4_API vw4_status verify_greedy_w4(const vw4_weight* W, const void* A_dev, int lda,
+                                    const int32_t* drafts_dev, int B, int Kd, int32_t* tokens_dev,
+                                    int32_t* len_dev, float* out_dev, int ldo,
+                                    void* workspace_dev, size_t ws_bytes, void* stream) {
+    if (B < 1 || Kd < 0 || B * (Kd + 1) > kMaxRows) return VW4_ERR_INVALID_ARG;
+    if (!tokens_dev || !len_dev || (Kd > 0 && !drafts_dev)) return VW4_ERR_INVALID_ARG;
+    const GreedyArgs g{drafts_dev, B, Kd, tokens_dev, len_dev};
+    return gemm_entry(W, A_dev, B * (Kd + 1), lda, out_dev, ldo, nullptr, &g, workspace_dev,
+                      ws_bytes, stream);
 }
 
 VW4_API vw4_status verify_moe_w4(const vw4_weight* experts, int E, const void* A_dev, int lda,

@@ -43,6 +43,7 @@ namespace cg = cooperative_groups;
 namespace vw4 {
 
 constexpr uint32_t kStatusTimeout = 0x4u;
+constexpr uint32_t kStatusBadDraft = 0x1u;
 constexpr uint32_t kStatusBadExpert = 0x2u;
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -552,11 +553,42 @@ struct Range {
 };
 
 // Called by the warp that completes the fused argmax bookkeeping.
+// The last warp of the grid: each verify row's argmax out of its key, then,
+// with greedy_B > 0, the greedy accept of every sequence (the longest draft
+// prefix equal to the row argmaxes, then the argmax at the first mismatch or
+// the bonus; a draft id outside [0, N) stops the prefix and is flagged).
 __device__ void argmax_finish(const GemmParams& p, int lane) {
     __threadfence();
+    int32_t am = 0;
     if (lane < p.argmax_M) {
         const unsigned long long k = atomicAdd(&p.am_key[lane], 0ull);
-        p.row_argmax[lane] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(k));
+        am = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(k));
+        if (p.row_argmax != nullptr) p.row_argmax[lane] = am;
+    }
+    if (p.greedy_B > 0) {
+        int32_t g[kMaxRows];
+#pragma unroll
+        for (int i = 0; i < kMaxRows; ++i) g[i] = __shfl_sync(0xffffffffu, am, i);
+        const int Kd = p.greedy_Kd, b = lane;
+        if (b < p.greedy_B) {
+            const int32_t* d = p.drafts + b * Kd;
+            const int r0 = b * (Kd + 1);
+            int n = 0;
+            bool bad = false;
+            for (int i = 0; i < Kd; ++i) {
+                const int32_t x = d[i];
+                if (x < 0 || x >= p.N) {
+                    bad = true;
+                    break;
+                }
+                if (x != g[r0 + i]) break;
+                ++n;
+            }
+            for (int i = 0; i <= Kd; ++i)
+                p.tokens[r0 + i] = i < n ? d[i] : (i == n ? g[r0 + n] : -1);
+            p.len[b] = n + 1;
+            if (bad) atomicOr(p.status, kStatusBadDraft);
+        }
     }
 }
 
@@ -841,7 +873,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                     const int tok = 2 * c + (q & 1);
                     const int n = n0 + wrow + rb * 16 + g + ((q & 2) ? 8 : 0);
                     if (n < p.N) {
-                        if (tok < count) {
+                        if (tok < count && p.out != nullptr) {
                             const int dest = p.dense_M > 0 ? tok : p.seg->dest[sg][tok];
                             p.out[static_cast<size_t>(dest) * p.ldo + n] = v[rb][q];
                         }
@@ -935,12 +967,12 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         unsigned long long kb = 0ull;
         if (tok < count) {
             const int dest = p.dense_M > 0 ? tok : p.seg->dest[sg][tok];
-            float* orow = p.out + static_cast<size_t>(dest) * p.ldo;
+            float* orow = p.out != nullptr ? p.out + static_cast<size_t>(dest) * p.ldo : nullptr;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int n = n0 + rr + (j & 3) + ((j & 4) ? 16 : 0);
                 if (n < p.N) {
-                    orow[n] = sv[j];
+                    if (p.out != nullptr) orow[n] = sv[j];
                     kb = umax64(kb, am_key(sv[j], static_cast<uint32_t>(n)));
                 }
             }

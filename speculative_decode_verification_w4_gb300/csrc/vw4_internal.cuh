@@ -89,6 +89,13 @@ struct GemmParams {
     // parts of a tile are launched as one cluster and combine their partial
     // tiles over distributed shared memory instead of tickets in L2.
     int cluster;
+    // greedy accept in the same launch (greedy_B > 0, with the fused argmax
+    // over M = greedy_B * (greedy_Kd + 1) rows): sequence b's target rows are
+    // b (Kd + 1) .. b (Kd + 1) + Kd; out may then be null (no logits written)
+    int greedy_B, greedy_Kd;
+    const int32_t* drafts;
+    int32_t* tokens;
+    int32_t* len;
 };
 
 // Lays the GEMM/MoE workspace out from `base` (nullptr: size only).

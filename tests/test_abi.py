@@ -90,3 +90,18 @@ def test_accept_argument_checks_on_host(lib):
     prm = vw4.Sampling(0.6, 0.0, 0, 0.0)
     assert lib.accept_rejection(0x100, 0x100, 0x100, 1, 2, 10, ctypes.byref(prm), 0, 0, 0x100,
                                 0x200, 0x1000, 1 << 20, None) == 1
+
+
+def test_verify_greedy_argument_checks_on_host(lib):
+    W = _weight()
+    # B * (Kd + 1) above 8, B < 1, Kd < 0, null tokens / lengths, null drafts with Kd > 0
+    assert lib.verify_greedy_w4(ctypes.byref(W), 0x3000, 512, 0x100, 2, 4, 0x200, 0x300, None, 0,
+                                0x10000, 1 << 30, None) == 1
+    assert lib.verify_greedy_w4(ctypes.byref(W), 0x3000, 512, 0x100, 0, 3, 0x200, 0x300, None, 0,
+                                0x10000, 1 << 30, None) == 1
+    assert lib.verify_greedy_w4(ctypes.byref(W), 0x3000, 512, 0x100, 1, -1, 0x200, 0x300, None,
+                                0, 0x10000, 1 << 30, None) == 1
+    assert lib.verify_greedy_w4(ctypes.byref(W), 0x3000, 512, 0x100, 1, 3, None, 0x300, None, 0,
+                                0x10000, 1 << 30, None) == 1
+    assert lib.verify_greedy_w4(ctypes.byref(W), 0x3000, 512, None, 1, 3, 0x200, 0x300, None, 0,
+                                0x10000, 1 << 30, None) == 1

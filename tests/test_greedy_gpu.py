@@ -94,3 +94,57 @@ def test_lm_head_fused_path_end_to_end():
     lg = logits.cpu().numpy()[None]
     rt, rl, _ = oracle.accept_greedy(lg, drafts)
     assert np.array_equal(tok.cpu().numpy(), rt) and np.array_equal(ln.cpu().numpy(), rl)
+
+
+@pytest.mark.parametrize("N,K,B,Kd", [(20000, 1024, 1, 7), (20000, 1024, 2, 3), (5000, 2048, 4, 1),
+                                      (3000, 512, 3, 0), (70000, 768, 1, 7)])
+def test_verify_greedy_one_launch(N, K, B, Kd):
+    """GEMM, row argmax and greedy accept in one launch: the committed run
+    equals the oracle's greedy accept over the GPU's own fp32 logits (which
+    the same call writes when asked), and the call without logits commits the
+    same run."""
+    M = B * (Kd + 1)
+    q, s, ts = synth.linear(N + K, N, K, "nvfp4")
+    A = synth.activations(synth.rng(K), M, K)
+    qd, sd = torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda()
+    Ad = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16).cuda()
+    am = torch.empty((M,), dtype=torch.int32, device="cuda")
+    vw4.verify_gemm_w4(vw4.FMT_NVFP4, qd, sd, ts, Ad, row_argmax=am)
+    amh = am.cpu().numpy().reshape(B, Kd + 1)
+    drafts = synth.greedy_drafts(synth.rng(N), amh[:, :Kd], N) if Kd else \
+        np.zeros((B, 0), np.int32)
+    d = torch.from_numpy(np.ascontiguousarray(drafts, np.int32)).cuda()
+    logits = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    tok, ln = vw4.verify_greedy_w4(vw4.FMT_NVFP4, qd, sd, ts, Ad, d, out=logits)
+    tok2, ln2 = vw4.verify_greedy_w4(vw4.FMT_NVFP4, qd, sd, ts, Ad, d)
+    torch.cuda.synchronize()
+    assert vw4.vw4_get_device_status() == 0
+    lg = logits.cpu().numpy().reshape(B, Kd + 1, N)
+    rt, rl, _ = oracle.accept_greedy(lg, drafts)
+    assert np.array_equal(tok.cpu().numpy(), rt) and np.array_equal(ln.cpu().numpy(), rl)
+    assert np.array_equal(tok2.cpu().numpy(), rt) and np.array_equal(ln2.cpu().numpy(), rl)
+    # the logits it wrote are the verify GEMM's
+    ref, bnd = oracle.gemm_w4(oracle.FMT_NVFP4, N, K, q, s, ts, A,
+                              cols=np.arange(0, N, 97, dtype=np.int32))
+    assert np.all(np.abs(lg.reshape(M, N)[:, ::97] - ref) <= 1e-3 * bnd)
+
+
+def test_verify_greedy_bad_draft_ids():
+    N, K, B, Kd = 4000, 512, 2, 3
+    q, s, ts = synth.linear(9, N, K, "nvfp4")
+    A = synth.activations(synth.rng(9), B * (Kd + 1), K)
+    qd, sd = torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda()
+    Ad = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16).cuda()
+    logits = vw4.verify_gemm_w4(vw4.FMT_NVFP4, qd, sd, ts, Ad)
+    lg = logits.cpu().numpy().reshape(B, Kd + 1, N)
+    am = lg.argmax(axis=-1).astype(np.int32)
+    drafts = am[:, :Kd].copy()
+    drafts[0, 1] = N          # out of range after one agreeing position
+    drafts[1, 0] = -5
+    vw4.vw4_get_device_status()
+    tok, ln = vw4.verify_greedy_w4(vw4.FMT_NVFP4, qd, sd, ts, Ad,
+                                   torch.from_numpy(drafts).cuda())
+    torch.cuda.synchronize()
+    assert vw4.vw4_get_device_status() & vw4.DEV_BAD_DRAFT_ID
+    rt, rl, _ = oracle.accept_greedy(lg, drafts)
+    assert np.array_equal(tok.cpu().numpy(), rt) and np.array_equal(ln.cpu().numpy(), rl)
