@@ -328,6 +328,22 @@ def run_ours(args, rank, world, device):
                 "kernel": "vw4::gemm_w4_kernel<nvfp4> (with its activation-prep launch)",
                 "per_unit": "0.5625 B per weight (nibble + e4m3/16) + 2*M B per k of activations"}
 
+    # the draft-depth controller on the measured verify cost of each width
+    # (the layer step at M = 1, 2, 4, 8; linear in between), a synthetic
+    # acceptance of 0.8 at every position and, as an assumption, a draft
+    # costing a tenth of a one-row verify step per token
+    mus = {int(m): per_m["nvfp4"][m]["layer_us"] for m in per_m["nvfp4"]}
+    pts = sorted(mus)
+    verify_us = {w: float(np.interp(w, pts, [mus[p] for p in pts])) for w in range(1, 9)}
+    ctl = vw4.DepthController(k_max=7, decay=1.0, verify_us=verify_us,
+                              draft_us_per_token=0.1 * verify_us[1])
+    for i in range(8):      # counts giving (acc + 1) / (att + 2) ~ 0.8 at every position
+        ctl.state.att[i], ctl.state.acc[i] = 10000.0, 8000.0
+    rates = {k: round(ctl.expected(k)[0] / ctl.expected(k)[1] * 1e3, 3) for k in range(8)}
+    depth = {"acceptance": 0.8, "draft_us_per_token": round(0.1 * verify_us[1], 2),
+             "verify_us": {w: round(v, 2) for w, v in verify_us.items()},
+             "committed_tokens_per_ms": rates, "chosen_depth": ctl.choose()}
+
     stream = torch.cuda.current_stream()
     accept = run_accept_timings(device, stream)
     heads = run_head_timings(device, stream)
@@ -345,6 +361,7 @@ def run_ours(args, rank, world, device):
                    "timing": "CUDA graph of the step's 4 C-ABI calls, replayed back to back",
                    "parallelism": f"replicas x{world}"},
         "per_m": per_m, "unpacked_7_calls": unpacked, "gate": gate, "accept_us": accept,
+        "depth_controller": depth,
         "heads": heads,
         "roofline": roofline, "e2e": e2e,
         "gpu_launches": steps * len(STEP) * LAUNCHES_PER_GEMM,

@@ -300,6 +300,53 @@ VW4_API vw4_status vw4_q4_0_from_blocks(const void* blocks_dev, int N, int K, vo
  * bit against an independent implementation.  Device pointers. */
 VW4_API vw4_status vw4_own_exp(const float* x_dev, float* y_dev, int64_t n, void* stream);
 
+/*
+ * Draft-depth controller (host only, no GPU work).
+ *
+ * Defined by: the Ollama commit log for x/mlxrunner/mtp.go, the paragraph that
+ * replaces the heuristic draft schedule by an engine-level controller drafting
+ * the depth that maximizes committed tokens per wall-clock time from live
+ * per-position acceptance and the persisted forward cost of each verify width;
+ * and "Faster Gemma 4 on MLX with multi-token prediction" (draft length tuned
+ * at runtime from acceptance rates and verification pass times, falling back
+ * when drafting does not pay).
+ *
+ * State (caller-owned, zero it or call vw4_depth_ctl_init):
+ *   att[i], acc[i]  decayed counts of drafts attempted / accepted at position
+ *                   i, given drafts 0..i-1 were accepted (i < 8);
+ *   verify_us[w]    the cost of a verify pass over w = K + 1 rows (1..8);
+ *   draft_us_fixed, draft_us_per_token   the cost of drafting K > 0 tokens,
+ *                   fixed + K * per_token;
+ *   k_max           the deepest draft considered (0..7: M = K + 1 <= 8);
+ *   decay           weight kept by old observations at each new one (0..1].
+ * The acceptance estimate of position i is (acc[i] + 1) / (att[i] + 2).  The
+ * expected committed run of depth K is sum_{j=0..K} prod_{i<j} alpha_i (the
+ * target's own token always commits), its cost verify_us[K + 1] plus the
+ * drafting cost (none at K = 0, plain decoding).
+ */
+typedef struct vw4_depth_ctl {
+    double att[8], acc[8];
+    float verify_us[9];
+    float draft_us_fixed, draft_us_per_token;
+    int k_max;
+    float decay;
+} vw4_depth_ctl;
+
+/* Resets the counts and sets the limits; verify costs default to 1 us each. */
+VW4_API vw4_status vw4_depth_ctl_init(vw4_depth_ctl* c, int k_max, float decay);
+
+/* Records one verify step: `depth` drafts were verified and the first
+ * `accepted` of them were accepted (0 <= accepted <= depth <= k_max). */
+VW4_API vw4_status vw4_depth_ctl_observe(vw4_depth_ctl* c, int depth, int accepted);
+
+/* Expected committed tokens of a run at `depth` and its cost in us. */
+VW4_API vw4_status vw4_depth_ctl_expected(const vw4_depth_ctl* c, int depth, double* tokens,
+                                          double* us);
+
+/* The depth in 0..k_max with the most expected committed tokens per us (ties
+ * to the shallower depth); -1 for an invalid state. */
+VW4_API int vw4_depth_ctl_choose(const vw4_depth_ctl* c);
+
 /* Human-readable name of a status code (static string). */
 VW4_API const char* vw4_status_str(vw4_status s);
 

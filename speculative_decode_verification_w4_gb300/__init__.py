@@ -41,7 +41,8 @@ STATUS_NAMES = {0: "VW4_OK", 1: "VW4_ERR_INVALID_ARG", 2: "VW4_ERR_UNSUPPORTED",
 EXPORTS = ("verify_gemm_w4", "verify_moe_w4", "accept_greedy", "accept_rejection",
            "vw4_workspace_bytes", "vw4_get_device_status", "vw4_q4_0_from_blocks",
            "vw4_status_str", "vw4_last_error_string", "vw4_version", "vw4_set_wait_limit_ns",
-           "vw4_own_exp", "verify_gemm_w4_noalloc", "verify_greedy_w4")
+           "vw4_own_exp", "verify_gemm_w4_noalloc", "verify_greedy_w4", "vw4_depth_ctl_init",
+           "vw4_depth_ctl_observe", "vw4_depth_ctl_expected", "vw4_depth_ctl_choose")
 
 
 class VW4Error(RuntimeError):
@@ -51,6 +52,14 @@ class VW4Error(RuntimeError):
         if detail:
             msg += f" ({detail})"
         super().__init__(msg)
+
+
+class DepthCtl(ctypes.Structure):
+    """vw4_depth_ctl (see vw4.h): the draft-depth controller's state."""
+    _fields_ = [("att", ctypes.c_double * 8), ("acc", ctypes.c_double * 8),
+                ("verify_us", ctypes.c_float * 9), ("draft_us_fixed", ctypes.c_float),
+                ("draft_us_per_token", ctypes.c_float), ("k_max", ctypes.c_int32),
+                ("decay", ctypes.c_float)]
 
 
 class Weight(ctypes.Structure):
@@ -96,6 +105,12 @@ def load_library(path: str = LIB_PATH):
             "vw4_set_wait_limit_ns": (None, [U64]),
             "vw4_own_exp": (I, [P, P, ctypes.c_int64, P]),
             "verify_gemm_w4_noalloc": (I, [ctypes.POINTER(Weight), P, I, I, P, I, P, P]),
+            "vw4_depth_ctl_init": (I, [ctypes.POINTER(DepthCtl), I, ctypes.c_float]),
+            "vw4_depth_ctl_observe": (I, [ctypes.POINTER(DepthCtl), I, I]),
+            "vw4_depth_ctl_expected": (I, [ctypes.POINTER(DepthCtl), I,
+                                           ctypes.POINTER(ctypes.c_double),
+                                           ctypes.POINTER(ctypes.c_double)]),
+            "vw4_depth_ctl_choose": (I, [ctypes.POINTER(DepthCtl)]),
             "verify_greedy_w4": (I, [ctypes.POINTER(Weight), P, I, P, I, I, P, P, P, I, P,
                                      ctypes.c_size_t, P]),
         }
@@ -212,6 +227,40 @@ def verify_greedy_w4(fmt: int, q: torch.Tensor, scales: torch.Tensor, tensor_sca
         _ptr(out), out.stride(0) if out is not None else 0, _ptr(ws), ws.numel(), _stream(stream))
     _check(code, "verify_greedy_w4")
     return tokens, length
+
+
+class DepthController:
+    """The draft-depth controller of vw4.h on a caller-owned state: verify
+    costs per width (us, for 1..k_max+1 rows), the drafting cost, live
+    per-position acceptance from observed verify steps."""
+
+    def __init__(self, k_max: int = 7, decay: float = 0.98, verify_us=None,
+                 draft_us_fixed: float = 0.0, draft_us_per_token: float = 0.0):
+        self.state = DepthCtl()
+        _check(load_library().vw4_depth_ctl_init(ctypes.byref(self.state), k_max, decay),
+               "vw4_depth_ctl_init")
+        if verify_us is not None:
+            for w, us in verify_us.items():
+                self.state.verify_us[w] = us
+        self.state.draft_us_fixed = draft_us_fixed
+        self.state.draft_us_per_token = draft_us_per_token
+
+    def observe(self, depth: int, accepted: int) -> None:
+        _check(load_library().vw4_depth_ctl_observe(ctypes.byref(self.state), depth, accepted),
+               "vw4_depth_ctl_observe")
+
+    def expected(self, depth: int):
+        t, us = ctypes.c_double(), ctypes.c_double()
+        _check(load_library().vw4_depth_ctl_expected(ctypes.byref(self.state), depth,
+                                                     ctypes.byref(t), ctypes.byref(us)),
+               "vw4_depth_ctl_expected")
+        return t.value, us.value
+
+    def choose(self) -> int:
+        k = load_library().vw4_depth_ctl_choose(ctypes.byref(self.state))
+        if k < 0:
+            raise VW4Error(1, "vw4_depth_ctl_choose", "invalid controller state")
+        return k
 
 
 class PreparedGemm:

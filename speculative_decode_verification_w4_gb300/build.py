@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libvw4.so")
-SOURCES = ["api.cu", "gemm_w4.cu", "accept.cu", "rejection.cu"]
+SOURCES = ["api.cu", "gemm_w4.cu", "accept.cu", "rejection.cu", "controller.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler",
          "-fvisibility=hidden", "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
@@ -46,7 +46,7 @@ def build(force: bool = False, verbose: bool = False, extra=None) -> str:
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
         if force or _stale(o, [s] + headers):
             jobs.append([cc, *ARCH, *FLAGS, *extra, "-c", s, "-o", o])
     def run(cmd):
@@ -60,7 +60,7 @@ def build(force: bool = False, verbose: bool = False, extra=None) -> str:
         for msg in ex.map(run, jobs):
             if verbose and msg:
                 print(msg, file=sys.stderr)
-    objs = [os.path.join(BUILD, s.replace(".cu", ".o")) for s in SOURCES]
+    objs = [os.path.join(BUILD, os.path.splitext(s)[0] + ".o") for s in SOURCES]
     if force or jobs or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
         run([cc, *ARCH, "-shared", "-o", tmp, *objs])
