@@ -73,6 +73,12 @@ def _load():
         "oracle_sample_drafts": (None, [P, i64, ctypes.c_int, ctypes.c_int, i64, f32, f32, u64,
                                         u64, u32, P]),
         "oracle_own_exp_array": (None, [P, P, i64]),
+        "oracle_row_mass_ex": (u64, [P, i64, f32, u64, i64, u64, P]),
+        "oracle_accept_rejection_ex": (ctypes.c_int, [P, i64, P, i64, P, ctypes.c_int,
+                                                      ctypes.c_int, i64, f32, f32, i64, f32, u64,
+                                                      u64, u32, P, P]),
+        "oracle_sample_drafts_ex": (None, [P, i64, ctypes.c_int, ctypes.c_int, i64, f32, f32,
+                                           i64, f32, u64, u64, u32, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -202,18 +208,21 @@ def top_p_fixed(top_p: float) -> int:
     return (1 << 32) if pd >= 4294967296.0 else int(np.floor(pd + 0.5))
 
 
-def row_mass(logits, temperature: float, top_p: float):
-    """Integer masses W (uint64 [V]) after temperature/softmax/top-p, and their sum."""
+def row_mass(logits, temperature: float, top_p: float, top_k: int = 0, min_p: float = 0.0):
+    """Integer masses W (uint64 [V]) after top-k / temperature+softmax / top-p /
+    min-p, and their kept sum."""
     logits = _c(logits, np.float32)
     invT = float(np.float32(1.0 / float(np.float32(temperature))))
     W = np.empty(logits.size, np.uint64)
-    S = _load().oracle_row_mass(_ptr(logits), logits.size, invT, top_p_fixed(top_p), _ptr(W))
+    mp = top_p_fixed(min_p) if min_p > 0 else 0
+    S = _load().oracle_row_mass_ex(_ptr(logits), logits.size, invT, top_p_fixed(top_p),
+                                   int(top_k), mp, _ptr(W))
     return W, int(S)
 
 
 def accept_rejection(target, draft, drafts, temperature: float, top_p: float, seed: int,
                      offset: int, broadcast_rows: bool = False, B: int | None = None,
-                     b_base: int = 0):
+                     b_base: int = 0, top_k: int = 0, min_p: float = 0.0):
     """target f32 [B, Kd+1, V], draft f32 [B, Kd, V] (or one shared [Kd+1, V] / [Kd, V]
     pair reused by every sequence when broadcast_rows=True, with B given).  Sequence b
     draws from Philox counter index b_base + b."""
@@ -233,15 +242,16 @@ def accept_rejection(target, draft, drafts, temperature: float, top_p: float, se
         draft = np.zeros(1, np.float32)
     tokens = np.empty((B, Kd + 1), np.int32)
     ln = np.empty(B, np.int32)
-    bad = _load().oracle_accept_rejection(_ptr(target), ld_tb, _ptr(draft), ld_db, _ptr(drafts),
-                                          B, Kd, V, float(temperature), float(top_p),
-                                          int(seed), int(offset), int(b_base), _ptr(tokens),
-                                          _ptr(ln))
+    bad = _load().oracle_accept_rejection_ex(_ptr(target), ld_tb, _ptr(draft), ld_db,
+                                             _ptr(drafts), B, Kd, V, float(temperature),
+                                             float(top_p), int(top_k), float(min_p), int(seed),
+                                             int(offset), int(b_base), _ptr(tokens), _ptr(ln))
     return tokens, ln, bad
 
 
 def sample_drafts(draft, temperature: float, top_p: float, seed: int, offset: int,
-                  broadcast_rows: bool = False, B: int | None = None, b_base: int = 0):
+                  broadcast_rows: bool = False, B: int | None = None, b_base: int = 0,
+                  top_k: int = 0, min_p: float = 0.0):
     draft = _c(draft, np.float32)
     if broadcast_rows:
         Kd, V = draft.shape
@@ -251,6 +261,7 @@ def sample_drafts(draft, temperature: float, top_p: float, seed: int, offset: in
         B, Kd, V = draft.shape
         ld = Kd * V
     out = np.empty((B, Kd), np.int32)
-    _load().oracle_sample_drafts(_ptr(draft), ld, B, Kd, V, float(temperature), float(top_p),
-                                 int(seed), int(offset), int(b_base), _ptr(out))
+    _load().oracle_sample_drafts_ex(_ptr(draft), ld, B, Kd, V, float(temperature),
+                                    float(top_p), int(top_k), float(min_p), int(seed),
+                                    int(offset), int(b_base), _ptr(out))
     return out

@@ -21,8 +21,9 @@
  *    own token at the first mismatch is always committed.
  *  - Ollama commit log for x/mlxrunner/mtp.go, "Greedy is a special case of
  *    sampled decoding" and "rework the MLX sampler": greedy is the temperature-0
- *    point mass; the distribution pipeline order is temperature/softmax ->
- *    top-p -> normalize -> categorical; acceptance, residual and bonus draws
+ *    point mass; the distribution pipeline order is top-k -> temperature/
+ *    softmax -> top-p -> min-p -> normalize -> categorical (penalties, the
+ *    first stage there, are left to the caller); acceptance, residual and bonus draws
  *    reuse the same draft/target distributions; the seed makes it reproducible.
  *  - "Your model may already ship a speculative decoder", section "Why it is
  *    interesting on a Mac specifically": Leviathan/Chen rejection sampling with
@@ -360,13 +361,49 @@ static int cmp_wdesc_iasc(const void* a, const void* b) {
     return (x->idx < y->idx) ? -1 : (x->idx > y->idx);
 }
 
-ORACLE_API uint64_t oracle_row_mass(const float* logits, int64_t V, float invT, uint64_t P,
-                                    uint64_t* W) {
+/* Order of the top-k stage: logit descending (NaN as -infinity, -0 equal to
+ * +0, as in the argmax), then index ascending. */
+typedef struct { float l; int64_t idx; } li_t;
+
+static int cmp_ldesc_iasc(const void* a, const void* b) {
+    const li_t* x = (const li_t*)a;
+    const li_t* y = (const li_t*)b;
+    if (x->l != y->l) return (x->l > y->l) ? -1 : 1;
+    return (x->idx < y->idx) ? -1 : (x->idx > y->idx);
+}
+
+/*
+ * The whole pipeline of "rework the MLX sampler" (penalties are not part of
+ * it here): top-k on the logits, temperature/softmax as the integer masses W,
+ * top-p, min-p, normalize.
+ *   top_k:  0 or >= V = off; else only the top_k first entries in (logit
+ *           desc, index asc) order keep a mass, every other W is 0.
+ *   P:      top-p as above, over the masses left by top-k.
+ *   MP:     min-p, MP = round(min_p * 2^32), 0 = off: of the entries top-p
+ *           keeps, those with W * 2^32 < MP * W_top are dropped too, W_top the
+ *           largest mass.  (Both stages keep a prefix of the (W desc, index
+ *           asc) order, so the result is the shorter of the two prefixes.)
+ * Returns the kept sum.
+ */
+ORACLE_API uint64_t oracle_row_mass_ex(const float* logits, int64_t V, float invT, uint64_t P,
+                                       int64_t top_k, uint64_t MP, uint64_t* W) {
     float mx = logits[0];
     for (int64_t v = 1; v < V; ++v)
         if (logits[v] > mx) mx = logits[v];
+    unsigned char* in_k = (unsigned char*)malloc((size_t)V);
+    memset(in_k, 1, (size_t)V);
+    if (top_k > 0 && top_k < V) {
+        li_t* o = (li_t*)malloc(sizeof(li_t) * (size_t)V);
+        for (int64_t v = 0; v < V; ++v) { o[v].l = nan_low(logits[v]); o[v].idx = v; }
+        qsort(o, (size_t)V, sizeof(li_t), cmp_ldesc_iasc);
+        memset(in_k, 0, (size_t)V);
+        for (int64_t j = 0; j < top_k; ++j) in_k[o[j].idx] = 1;
+        free(o);
+    }
     uint64_t S = 0;
     for (int64_t v = 0; v < V; ++v) {
+        W[v] = 0;
+        if (!in_k[v]) continue;
         float d = logits[v] - mx;
         float x = d * invT;
         float e = oracle_own_exp(x);
@@ -374,20 +411,38 @@ ORACLE_API uint64_t oracle_row_mass(const float* logits, int64_t V, float invT, 
         W[v] = (uint64_t)scaled;
         S += W[v];
     }
-    if (P >= ((uint64_t)1 << 32)) return S;
+    free(in_k);
+    if (P >= ((uint64_t)1 << 32) && MP == 0) return S;
     wi_t* srt = (wi_t*)malloc(sizeof(wi_t) * (size_t)V);
     for (int64_t v = 0; v < V; ++v) { srt[v].w = W[v]; srt[v].idx = v; }
     qsort(srt, (size_t)V, sizeof(wi_t), cmp_wdesc_iasc);
-    u128 target = (u128)P * (u128)S;
-    uint64_t cum = 0;
     int64_t keep = V;
-    for (int64_t j = 0; j < V; ++j) {
-        cum += srt[j].w;
-        if (((u128)cum << 32) >= target) { keep = j + 1; break; }
+    if (P < ((uint64_t)1 << 32)) {
+        u128 target = (u128)P * (u128)S;
+        uint64_t cum = 0;
+        for (int64_t j = 0; j < V; ++j) {
+            cum += srt[j].w;
+            if (((u128)cum << 32) >= target) { keep = j + 1; break; }
+        }
     }
-    for (int64_t j = keep; j < V; ++j) W[srt[j].idx] = 0;
+    if (MP > 0) {
+        const uint64_t Wtop = srt[0].w;
+        int64_t j = 0;
+        while (j < keep && ((u128)srt[j].w << 32) >= (u128)MP * Wtop) ++j;
+        keep = j;
+    }
+    uint64_t kept = 0;
+    for (int64_t j = 0; j < V; ++j) {
+        if (j < keep) kept += srt[j].w;
+        else W[srt[j].idx] = 0;
+    }
     free(srt);
-    return cum;
+    return kept;
+}
+
+ORACLE_API uint64_t oracle_row_mass(const float* logits, int64_t V, float invT, uint64_t P,
+                                    uint64_t* W) {
+    return oracle_row_mass_ex(logits, V, invT, P, 0, 0, W);
 }
 
 /* Inverse CDF: first v (ascending) whose running sum of weights exceeds
@@ -433,16 +488,26 @@ static int64_t categorical_u64(const uint64_t* W, int64_t V, uint64_t total, uin
  * a batch can be checked on its own).
  * Returns the number of out-of-range draft ids (counted as rejections).
  */
-ORACLE_API int oracle_accept_rejection(const float* target, int64_t ld_tb, const float* draft,
-                                       int64_t ld_db, const int32_t* drafts, int B, int Kd,
-                                       int64_t V, float temperature, float top_p, uint64_t seed,
-                                       uint64_t offset, uint32_t b_base, int32_t* tokens,
-                                       int32_t* len) {
+/* P = round(p * 2^32) of a probability threshold, saturating at 2^32. */
+static uint64_t fixed32(float p) {
+    double pd = (double)p * 4294967296.0;
+    return (pd >= 4294967296.0) ? ((uint64_t)1 << 32) : (uint64_t)llround(pd);
+}
+
+/* With top_k and min_p (the rest of the sampler pipeline, oracle_row_mass_ex)
+ * applied to the target and the draft rows alike; top_k = 0 and min_p = 0 is
+ * oracle_accept_rejection. */
+ORACLE_API int oracle_accept_rejection_ex(const float* target, int64_t ld_tb, const float* draft,
+                                          int64_t ld_db, const int32_t* drafts, int B, int Kd,
+                                          int64_t V, float temperature, float top_p,
+                                          int64_t top_k, float min_p, uint64_t seed,
+                                          uint64_t offset, uint32_t b_base, int32_t* tokens,
+                                          int32_t* len) {
     if (temperature == 0.0f)
         return oracle_accept_greedy(target, ld_tb, drafts, B, Kd, V, tokens, len);
     float invT = (float)(1.0 / (double)temperature);
-    double pd = (double)top_p * 4294967296.0;
-    uint64_t P = (pd >= 4294967296.0) ? ((uint64_t)1 << 32) : (uint64_t)llround(pd);
+    const uint64_t P = fixed32(top_p);
+    const uint64_t MP = min_p > 0.0f ? fixed32(min_p) : 0;
     int bad = 0;
     uint64_t* Wp = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)V);
     uint64_t* Wq = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)V);
@@ -453,8 +518,8 @@ ORACLE_API int oracle_accept_rejection(const float* target, int64_t ld_tb, const
         int n = 0;
         int64_t last = -1;
         for (int i = 0; i < Kd; ++i) {
-            uint64_t Sp = oracle_row_mass(tb + (int64_t)i * V, V, invT, P, Wp);
-            uint64_t Sq = oracle_row_mass(db + (int64_t)i * V, V, invT, P, Wq);
+            uint64_t Sp = oracle_row_mass_ex(tb + (int64_t)i * V, V, invT, P, top_k, MP, Wp);
+            uint64_t Sq = oracle_row_mass_ex(db + (int64_t)i * V, V, invT, P, top_k, MP, Wq);
             int32_t x = drafts[(int64_t)b * Kd + i];
             uint32_t rr[4];
             philox_at(seed, offset, (uint32_t)i, b_base + (uint32_t)b, rr);
@@ -480,7 +545,7 @@ ORACLE_API int oracle_accept_rejection(const float* target, int64_t ld_tb, const
             break;
         }
         if (n == Kd) {
-            uint64_t Sp = oracle_row_mass(tb + (int64_t)Kd * V, V, invT, P, Wp);
+            uint64_t Sp = oracle_row_mass_ex(tb + (int64_t)Kd * V, V, invT, P, top_k, MP, Wp);
             uint32_t rr[4];
             philox_at(seed, offset, (uint32_t)Kd, b_base + (uint32_t)b, rr);
             uint64_t u64 = ((uint64_t)rr[2] << 32) | rr[1];
@@ -500,26 +565,44 @@ ORACLE_API int oracle_accept_rejection(const float* target, int64_t ld_tb, const
     return bad;
 }
 
+ORACLE_API int oracle_accept_rejection(const float* target, int64_t ld_tb, const float* draft,
+                                       int64_t ld_db, const int32_t* drafts, int B, int Kd,
+                                       int64_t V, float temperature, float top_p, uint64_t seed,
+                                       uint64_t offset, uint32_t b_base, int32_t* tokens,
+                                       int32_t* len) {
+    return oracle_accept_rejection_ex(target, ld_tb, draft, ld_db, drafts, B, Kd, V, temperature,
+                                      top_p, 0, 0.0f, seed, offset, b_base, tokens, len);
+}
+
 /*
  * Draws x_i ~ q_i for every sequence and draft position with the same
  * transform and inverse-CDF rule, using Philox blocks (i, b, offset) -- the
  * caller passes an offset disjoint from the acceptance offset (e.g. +2^32).
  * Used only to make test inputs whose drafts really come from q.
  */
-ORACLE_API void oracle_sample_drafts(const float* draft, int64_t ld_db, int B, int Kd, int64_t V,
-                                     float temperature, float top_p, uint64_t seed,
-                                     uint64_t offset, uint32_t b_base, int32_t* drafts) {
+ORACLE_API void oracle_sample_drafts_ex(const float* draft, int64_t ld_db, int B, int Kd,
+                                        int64_t V, float temperature, float top_p, int64_t top_k,
+                                        float min_p, uint64_t seed, uint64_t offset,
+                                        uint32_t b_base, int32_t* drafts) {
     float invT = (float)(1.0 / (double)temperature);
-    double pd = (double)top_p * 4294967296.0;
-    uint64_t P = (pd >= 4294967296.0) ? ((uint64_t)1 << 32) : (uint64_t)llround(pd);
+    const uint64_t P = fixed32(top_p);
+    const uint64_t MP = min_p > 0.0f ? fixed32(min_p) : 0;
     uint64_t* Wq = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)V);
     for (int b = 0; b < B; ++b)
         for (int i = 0; i < Kd; ++i) {
-            uint64_t Sq = oracle_row_mass(draft + (int64_t)b * ld_db + (int64_t)i * V, V, invT, P, Wq);
+            uint64_t Sq = oracle_row_mass_ex(draft + (int64_t)b * ld_db + (int64_t)i * V, V, invT,
+                                             P, top_k, MP, Wq);
             uint32_t rr[4];
             philox_at(seed, offset, (uint32_t)i, b_base + (uint32_t)b, rr);
             uint64_t u64 = ((uint64_t)rr[2] << 32) | rr[1];
             drafts[(int64_t)b * Kd + i] = (int32_t)categorical_u64(Wq, V, Sq, u64);
         }
     free(Wq);
+}
+
+ORACLE_API void oracle_sample_drafts(const float* draft, int64_t ld_db, int B, int Kd, int64_t V,
+                                     float temperature, float top_p, uint64_t seed,
+                                     uint64_t offset, uint32_t b_base, int32_t* drafts) {
+    oracle_sample_drafts_ex(draft, ld_db, B, Kd, V, temperature, top_p, 0, 0.0f, seed, offset,
+                            b_base, drafts);
 }

@@ -196,3 +196,96 @@ def test_mean_accepted_length_matches_closed_form(sixteen_token_case):
     var = sum(pr * (2 * j - 1) for j, pr in enumerate(probs, start=1)) - mean ** 2
     got = float(np.mean(ln - 1))
     assert abs(got - mean) <= 4 * math.sqrt(var / len(ln)), (got, mean)
+
+
+def test_row_mass_top_k_and_min_p_against_float_definitions():
+    """top-k keeps the k largest logits (ties to the lower index) with their
+    unchanged masses; min-p keeps the entries whose probability is at least
+    min_p times the largest (checked against float64 away from the edge);
+    with top-p as well the kept set is the shorter of the two prefixes."""
+    g = np.random.default_rng(21)
+    for trial in range(40):
+        V = int(g.integers(3, 60))
+        lg = (g.standard_normal(V) * 3).astype(np.float32)
+        if trial % 5 == 0:
+            lg[g.integers(0, V, 3)] = lg[0]          # some exact ties
+        T = 0.6
+        full, Sf = oracle.row_mass(lg, T, 1.0)
+        k = int(g.integers(1, V))
+        W, S = oracle.row_mass(lg, T, 1.0, top_k=k)
+        order = np.lexsort((np.arange(V), -lg.astype(np.float64)))   # logit desc, index asc
+        top = set(int(v) for v in order[:k])
+        assert set(np.nonzero(W)[0].tolist()) <= top
+        for v in range(V):
+            assert int(W[v]) == (int(full[v]) if v in top else 0)
+        assert S == sum(int(full[v]) for v in top)
+        # min-p alone
+        mp = float(g.choice([0.01, 0.05, 0.2, 0.5]))
+        Wm, Sm = oracle.row_mass(lg, T, 1.0, min_p=mp)
+        ratio = np.exp((lg.astype(np.float64) - lg.max()) / T)      # p_v / p_max
+        for v in range(V):
+            if ratio[v] > mp * (1 + 1e-5):
+                assert int(Wm[v]) == int(full[v])
+            elif ratio[v] < mp * (1 - 1e-5):
+                assert int(Wm[v]) == 0
+        # top-p and min-p: the shorter prefix of the (W desc, index asc) order
+        top_p = float(g.choice([0.5, 0.8, 0.95]))
+        Wb, Sb = oracle.row_mass(lg, T, top_p, min_p=mp)
+        Wp, _ = oracle.row_mass(lg, T, top_p)
+        for v in range(V):
+            assert int(Wb[v]) == (int(full[v]) if (Wp[v] > 0 and Wm[v] > 0) else 0)
+        assert Sb == int(Wb.sum())
+
+
+def test_top_k_one_commits_the_argmax():
+    g = np.random.default_rng(22)
+    B, Kd, V = 200, 2, 40
+    tgt = (g.standard_normal((B, Kd + 1, V)) * 3).astype(np.float32)
+    drf = (tgt[:, :Kd] + g.standard_normal((B, Kd, V))).astype(np.float32)
+    drafts = oracle.sample_drafts(drf, 0.6, 0.95, 5, 1 << 32, top_k=1)
+    assert np.array_equal(drafts, drf.argmax(axis=2))
+    tok, ln, bad = oracle.accept_rejection(tgt, drf, drafts, 0.6, 0.95, 5, 0, top_k=1)
+    am = tgt.argmax(axis=2)
+    for b in range(B):
+        n = ln[b] - 1
+        assert np.array_equal(tok[b, :n], drafts[b, :n])
+        assert np.all(tok[b, :n] == am[b, :n])         # accepted drafts are the argmax
+        assert tok[b, n] == am[b, n]                     # the committed token too
+
+
+def _float_pipeline(lg, T, top_k, top_p, min_p):
+    """The sampler pipeline in float64: top-k on the logits, softmax at T,
+    top-p (shortest prefix by probability reaching top_p), min-p, normalize."""
+    lg = lg.astype(np.float64)
+    V = lg.size
+    keep = np.zeros(V, bool)
+    keep[np.lexsort((np.arange(V), -lg))[:top_k if top_k else V]] = True
+    p = np.where(keep, np.exp((lg - lg.max()) / T), 0.0)
+    p /= p.sum()
+    order = np.lexsort((np.arange(V), -p))
+    cum = np.cumsum(p[order])
+    n = int(np.searchsorted(cum, top_p - 1e-12) + 1) if top_p < 1 else V
+    kp = np.zeros(V, bool)
+    kp[order[:n]] = True
+    kp &= p >= min_p * p.max()
+    q = np.where(kp, p, 0.0)
+    return q / q.sum()
+
+
+def test_first_token_marginal_with_top_k_and_min_p():
+    """Chi-square of the first committed token, with the whole pipeline on
+    (top-k 6, top-p 0.9, min-p 0.05), against its float64 definition."""
+    g = np.random.default_rng(23)
+    V, Kd = 16, 2
+    tgt = (g.standard_normal((Kd + 1, V)) * 2).astype(np.float32)
+    drf = (tgt[:Kd] + g.standard_normal((Kd, V))).astype(np.float32)
+    kw = dict(top_k=6, min_p=0.05)
+    drafts = oracle.sample_drafts(drf, 0.6, 0.9, 31, 1 << 32, broadcast_rows=True, B=CHI_N, **kw)
+    tok, ln, bad = oracle.accept_rejection(tgt, drf, drafts, 0.6, 0.9, 31, 0,
+                                           broadcast_rows=True, B=CHI_N, **kw)
+    assert bad == 0
+    p0 = _float_pipeline(tgt[0], 0.6, 6, 0.9, 0.05)
+    W0, S0 = oracle.row_mass(tgt[0], 0.6, 0.9, **kw)
+    assert np.array_equal(W0 > 0, p0 > 0)           # the same kept set as the float pipeline
+    counts = np.bincount(tok[:, 0], minlength=V)
+    assert _chi2_against(counts, p0) > 1e-4
