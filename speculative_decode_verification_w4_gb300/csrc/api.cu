@@ -422,7 +422,8 @@ VW4_API vw4_status accept_rejection(const float* target_logits_dev, const float*
     const float T = params->temperature;
     if (!(T >= 0.0f) || !std::isfinite(T)) return VW4_ERR_INVALID_ARG;
     if (!(params->top_p > 0.0f) || !std::isfinite(params->top_p)) return VW4_ERR_INVALID_ARG;
-    if (params->top_k != 0 || params->min_p != 0.0f) return VW4_ERR_UNSUPPORTED;
+    if (params->top_k < 0) return VW4_ERR_INVALID_ARG;
+    if (!(params->min_p >= 0.0f && params->min_p <= 1.0f)) return VW4_ERR_INVALID_ARG;
     if (T == 0.0f)  // temperature 0 is the greedy rule: no random numbers drawn
         return accept_greedy(target_logits_dev, drafts_dev, nullptr, B, Kd, V, tokens_dev,
                              len_dev, stream);
@@ -436,8 +437,15 @@ VW4_API vw4_status accept_rejection(const float* target_logits_dev, const float*
     const double pd = static_cast<double>(params->top_p) * 4294967296.0;
     uint64_t P = pd >= 4294967296.0 ? (1ull << 32) : static_cast<uint64_t>(std::llround(pd));
     if (P == 0) P = 1;  // keeps the top entry alone, exactly as P = 0 does
+    // min-p in the same fixed point, 0 = off
+    const double md = static_cast<double>(params->min_p) * 4294967296.0;
+    const uint64_t MP = params->min_p > 0.0f
+                            ? (md >= 4294967296.0 ? (1ull << 32)
+                                                  : static_cast<uint64_t>(std::llround(md)))
+                            : 0ull;
     cudaError_t e = launch_accept_rejection(target_logits_dev, draft_logits_dev, drafts_dev, B, Kd,
-                                            V, invT, P, seed, offset, tokens_dev, len_dev,
+                                            V, invT, P, params->top_k, MP, seed, offset,
+                                            tokens_dev, len_dev,
                                             workspace_dev, ws_bytes, d->status, g_wait_ns,
                                             static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return VW4_ERR_UNSUPPORTED;

@@ -67,7 +67,18 @@ struct RowInfo {
     int cut;                 // largest kept index among W == tau
     unsigned long long tau;  // kept: W > tau, or W == tau and v <= cut
     unsigned long long S;    // kept sum
+    uint32_t tk_key;         // top-k: an entry takes part iff its logit key > tk_key,
+    int tk_idx;              //   or == tk_key and its index <= tk_idx (off: 0, max int)
 };
+
+// The top-k order of a logit (the argmax's): NaN as -infinity, -0 as +0,
+// then an order-preserving unsigned key.
+__device__ __forceinline__ uint32_t logit_key(float l) {
+    if (l != l) l = -INFINITY;
+    if (l == 0.0f) l = 0.0f;
+    const uint32_t b = __float_as_uint(l);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
 
 // ------------------------------------------------------------- own exp
 // Cody-Waite reduction + degree-7 Taylor polynomial in fp32 with explicit
@@ -173,8 +184,15 @@ __device__ __forceinline__ unsigned long long mass_of(float e) {
     return (static_cast<unsigned long long>(hi) << 20) | lo;
 }
 
-__device__ __forceinline__ unsigned long long kept(unsigned long long W, int v, const RowInfo& s) {
-    return (W > s.tau || (W == s.tau && v <= s.cut)) ? W : 0ull;
+__device__ __forceinline__ bool in_top_k(float l, int v, const RowInfo& s) {
+    const uint32_t k = logit_key(l);
+    return k > s.tk_key || (k == s.tk_key && v <= s.tk_idx);
+}
+
+// The kept mass of entry v (logit l, mass W) of a row.
+__device__ __forceinline__ unsigned long long kept(unsigned long long W, float l, int v,
+                                                   const RowInfo& s) {
+    return ((W > s.tau || (W == s.tau && v <= s.cut)) && in_top_k(l, v, s)) ? W : 0ull;
 }
 
 // Log-scale bucket of W = floor(f) >= 1, f = e * 2^40: W itself below 16,
@@ -389,10 +407,10 @@ __device__ __forceinline__ int float_key(float x) {
 // f(k, l) for every entry of the segments whose max passes the window test
 // (vec rows with a segment table; otherwise every entry, as stream_row).
 // seg[] was written by this CTA in its max pass: read through L2.
-template <class F>
-__device__ __forceinline__ void stream_window(const float* __restrict__ row, int V, bool vec,
-                                              const float* seg, float mx, float invT, float xa,
-                                              F&& f) {
+// (need(m): whether a segment whose largest logit is m can hold a wanted entry)
+template <class N, class F>
+__device__ __forceinline__ void stream_segments(const float* __restrict__ row, int V, bool vec,
+                                                const float* seg, N&& need_of, F&& f) {
     if (seg == nullptr) {
         stream_row(row, V, vec, f);
         return;
@@ -404,7 +422,7 @@ __device__ __forceinline__ void stream_window(const float* __restrict__ row, int
         // lane j tests the segment of step k0 + j that this warp streams
         const int k = k0 + lane, sg = k * kRowWarps + wid;
         bool need = false;
-        if (k < nk && sg < nseg) need = !(scaled_x(__ldcg(seg + sg), mx, invT) < xa);
+        if (k < nk && sg < nseg) need = need_of(__ldcg(seg + sg));
         unsigned int m = __ballot_sync(0xffffffffu, need);
         while (m) {
             const int j = __ffs(m) - 1;
@@ -416,6 +434,14 @@ __device__ __forceinline__ void stream_window(const float* __restrict__ row, int
             }
         }
     }
+}
+
+template <class F>
+__device__ __forceinline__ void stream_window(const float* __restrict__ row, int V, bool vec,
+                                              const float* seg, float mx, float invT, float xa,
+                                              F&& f) {
+    stream_segments(row, V, vec, seg,
+                    [&](float m) { return !(scaled_x(m, mx, invT) < xa); }, f);
 }
 
 // How many entries stream_row hands to this thread.
@@ -438,10 +464,9 @@ __device__ __forceinline__ void x_window(unsigned long long wlo, unsigned long l
     xb = __logf(static_cast<float>(whi)) - ln2_40 + 1e-3f;
 }
 
-// The row's (max, tau, cut, kept sum); valid in every thread.
-// seg: this row's segment maxima (vec rows), or null.
-__device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, float invT,
-                             unsigned long long P, float* seg, RowSmem& sm) {
+// The row's max (valid in every thread), and its segment maxima into seg
+// (vec rows), or null.
+__device__ float row_max(const float* __restrict__ row, int V, bool vec, float* seg, RowSmem& sm) {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
 
     // 1. max, and the segment maxima: at step k warp w streams float4 groups
@@ -471,7 +496,94 @@ __device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, flo
     } else {
         stream_row(row, V, vec, [&](int, float l) { lmax = fmaxf(lmax, l); });
     }
-    const float mx = block_max(lmax, sm.red);
+    return block_max(lmax, sm.red);
+}
+
+// The top-k cut of a row: the key K and index I of its top_k-th entry in
+// (logit key desc, index asc) order, so that an entry is among the first
+// top_k iff its key > K, or == K and its index <= I.  A radix select on the
+// 32-bit keys, eight bits a level: each level counts the entries whose higher
+// bits match so far (warp-aggregated counts into per-warp histograms),
+// skipping the segments whose largest logit lies below the level's range;
+// then, when K is shared by more entries than the cut takes, the index cut
+// among them in index order.
+__device__ void top_k_cut(const float* __restrict__ row, int V, bool vec, const float* seg,
+                          int top_k, RowSmem& sm, uint32_t& K, int& I) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    uint32_t* hist = reinterpret_cast<uint32_t*>(&sm.whist[0][0]);  // [kRowWarps][256]
+    uint32_t prefix = 0u;
+    unsigned long long need = static_cast<unsigned long long>(top_k);
+    unsigned long long n_at = 0ull;  // entries with the final key
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        const uint32_t hmask = shift == 24 ? 0u : (0xFFFFFFFFu << (shift + 8));
+        const uint32_t lo_key = prefix & hmask;  // the smallest key of this level's range
+        for (int t = tid; t < kRowWarps * 256; t += kRowThreads) hist[t] = 0u;
+        __syncthreads();
+        uint32_t* h = hist + wid * 256;
+        stream_segments(row, V, vec, seg, [&](float m) { return logit_key(m) >= lo_key; },
+                        [&](int, float l) {
+                            const uint32_t k = logit_key(l);
+                            const bool in = (k & hmask) == lo_key;
+                            const unsigned int d = in ? ((k >> shift) & 255u) : 256u;
+                            const unsigned int peers = __match_any_sync(__activemask(), d);
+                            if (in && __ffs(peers) - 1 == lane) atomicAdd(&h[d], __popc(peers));
+                        });
+        __syncthreads();
+        // thread t holds digit 255 - t: the digit where the count from the
+        // top first reaches `need`
+        const int dg = 255 - tid;
+        unsigned long long c = 0ull;
+        if (dg >= 0)
+            for (int w = 0; w < kRowWarps; ++w) c += hist[w * 256 + dg];
+        u128 tot_unused;
+        const u128 incl = block_excl_u128(static_cast<u128>(c), sm.red, tot_unused) + c;
+        if (dg >= 0 && incl >= need && incl - c < need) {
+            sm.beta = dg;
+            sm.above = static_cast<unsigned long long>(incl - c);
+            sm.count_eq = c;
+        }
+        __syncthreads();
+        prefix |= static_cast<uint32_t>(sm.beta) << shift;
+        need -= sm.above;
+        n_at = sm.count_eq;
+        __syncthreads();
+    }
+    K = prefix;
+    I = 0x7fffffff;
+    if (need < n_at) {
+        // the need-th entry with key K in index order: each thread counts its
+        // contiguous chunk, a block scan orders the chunks
+        const int chunk = (V + kRowThreads - 1) / kRowThreads;
+        const int k0 = tid * chunk < V ? tid * chunk : V, k1 = k0 + chunk < V ? k0 + chunk : V;
+        unsigned int mine = 0u;
+        for (int k = k0; k < k1; ++k) mine += logit_key(__ldg(row + k)) == prefix ? 1u : 0u;
+        u128 ctot;
+        const unsigned long long excl = static_cast<unsigned long long>(
+            block_excl_u128(static_cast<u128>(mine), sm.red, ctot));
+        if (tid == 0) sm.cut_found = V - 1;
+        __syncthreads();
+        if (excl < need && need <= excl + mine) {
+            unsigned long long seen = excl;
+            for (int k = k0; k < k1; ++k)
+                if (logit_key(__ldg(row + k)) == prefix && ++seen == need) {
+                    sm.cut_found = k;
+                    break;
+                }
+        }
+        __syncthreads();
+        I = sm.cut_found;
+        __syncthreads();
+    }
+}
+
+// The row's (tau, cut, kept sum) after top-p, over the entries the top-k
+// stage of info keeps (n_keep of them); valid in every thread.
+__device__ RowInfo row_cut(const float* __restrict__ row, int V, bool vec, float invT,
+                           unsigned long long P, const float* seg, RowInfo info, int n_keep,
+                           RowSmem& sm) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const float mx = info.mx;
+    const bool topk = n_keep < V;
 
     // 2. sum W, and the mass histogram of the entries with W >= c0 (each warp
     //    its own copy).  The entries below c <= (1 - P/2^32) S / V weigh less
@@ -480,7 +592,7 @@ __device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, flo
     //    S, so c0 <= c and the histogram holds every bucket the cut can be in.
     const bool want_hist = P < kKeepAll;
     const unsigned long long c0 =
-        want_hist ? ((kKeepAll - P) << 8) / static_cast<unsigned long long>(V) : 0ull;
+        want_hist ? ((kKeepAll - P) << 8) / static_cast<unsigned long long>(n_keep) : 0ull;
     const unsigned long long cmin = c0 > 1ull ? c0 : 1ull;
     // f < f_lo proves W < cmin with one compare (f_lo is cmin rounded down)
     const float f_lo = want_hist ? __ull2float_rd(cmin) : INFINITY;
@@ -495,7 +607,22 @@ __device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, flo
             (static_cast<unsigned long long>(hib - 0x4B000000u) << 20) | (lob - 0x4B000000u);
         if (W >= cmin) atomic_add_u64_split(&hist[log_bucket_f(f)], W);
     };
-    if (vec) {
+    uint32_t n_mine = 0u;  // entries this thread summed (the top-k path)
+    if (topk) {
+        // only the top-k entries carry mass: the segments that can hold one
+        stream_segments(row, V, vec, seg,
+                        [&](float m) { return logit_key(m) >= info.tk_key; },
+                        [&](int k, float l) {
+                            if (!in_top_k(l, k, info)) return;
+                            const float f = own_exp_2_40(scaled_x(l, mx, invT));
+                            uint32_t hib, lob;
+                            mass_bits(f, hib, lob);
+                            sum_hib += hib;
+                            sum_lob += lob;
+                            ++n_mine;
+                            if (f >= f_lo) to_hist(f, hib, lob);
+                        });
+    } else if (vec) {
         // two entries per packed operation (mass_bits on pairs)
         const float2 nmx = make_float2(-mx, -mx), it2 = make_float2(invT, invT);
         const float2 k20 = make_float2(9.5367431640625e-07f, 9.5367431640625e-07f);
@@ -540,11 +667,9 @@ __device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, flo
             if (f >= f_lo) to_hist(f, hib, lob);
         });
     }
-    const uint32_t bias = stream_count(V, vec) * 0x4B000000u;
+    const uint32_t bias = (topk ? n_mine : stream_count(V, vec)) * 0x4B000000u;
     const unsigned long long S = block_sum_u64(
         (static_cast<unsigned long long>(sum_hib - bias) << 20) + (sum_lob - bias), sm.red);
-    RowInfo info;
-    info.mx = mx;
     if (!want_hist) {
         info.cut = V - 1;
         info.tau = 0;
@@ -606,7 +731,7 @@ __device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, flo
         x_window(wlo, whi, xa, xb);
         stream_window(row, V, vec, seg, mx, invT, xa, [&](int k, float l) {
             const float x = scaled_x(l, mx, invT);
-            if (x >= xa && x < xb) {
+            if (x >= xa && x < xb && in_top_k(l, k, info)) {
                 const float e = own_exp(x);
                 if (e >= b_lo && e < b_hi) {
                     const unsigned int slot = atomicAdd(&sm.ncand, 1u);
@@ -723,9 +848,9 @@ __device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, flo
         __syncthreads();
         float xa, xb;
         x_window(rlo, rhi, xa, xb);
-        stream_window(row, V, vec, seg, mx, invT, xa, [&](int, float l) {
+        stream_window(row, V, vec, seg, mx, invT, xa, [&](int k, float l) {
             const float x = scaled_x(l, mx, invT);
-            if (x >= xa && x < xb) {
+            if (x >= xa && x < xb && in_top_k(l, k, info)) {
                 const unsigned long long W = mass_of(own_exp(x));
                 if (W >= rlo && W < rhi) {
                     const int bk = static_cast<int>((W - rlo) >> shift);
@@ -773,8 +898,9 @@ __device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, flo
         float xa, xb;
         x_window(tau, tau + 1ull, xa, xb);
         auto is_tau = [&](int k) {
-            const float x = scaled_x(__ldg(row + k), mx, invT);
-            return x >= xa && x < xb && mass_of(own_exp(x)) == tau;
+            const float l = __ldg(row + k);
+            const float x = scaled_x(l, mx, invT);
+            return x >= xa && x < xb && mass_of(own_exp(x)) == tau && in_top_k(l, k, info);
         };
         unsigned int mine = 0;
         for (int k = k0; k < k1; ++k) mine += is_tau(k) ? 1u : 0u;
@@ -797,13 +923,55 @@ __device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, flo
     return info;
 }
 
+// The row's RowInfo through the whole pipeline: max, top-k (0 or >= V: off),
+// the integer masses, top-p, min-p (MP = round(min_p 2^32), 0: off);
+// valid in every thread.  seg: this row's segment maxima (vec rows), or null.
+__device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, float invT,
+                             unsigned long long P, int top_k, unsigned long long MP, float* seg,
+                             RowSmem& sm) {
+    RowInfo info;
+    info.mx = row_max(row, V, vec, seg, sm);
+    info.tk_key = 0u;
+    info.tk_idx = 0x7fffffff;
+    info.tau = 0ull;
+    info.cut = V - 1;
+    info.S = 0ull;
+    const bool topk = top_k > 0 && top_k < V;
+    if (topk) top_k_cut(row, V, vec, seg, top_k, sm, info.tk_key, info.tk_idx);
+    RowInfo r = row_cut(row, V, vec, invT, P, seg, info, topk ? top_k : V, sm);
+    // min-p: of what top-p keeps, only W * 2^32 >= MP * W_top, W_top = 2^40
+    // (the max entry's own mass), i.e. W >= MP * 2^8.  Both keep a prefix of
+    // the (W desc, index asc) order: when min-p's is the shorter, it is every
+    // entry with W >= MP 2^8, ties included.
+    if (MP > 0ull && r.S > 0ull) {
+        const unsigned long long Wmin = MP << 8;
+        if (Wmin > r.tau) {
+            float xa, xb;
+            x_window(Wmin, Wmin + 1ull, xa, xb);
+            const float mx = r.mx;
+            unsigned long long part = 0ull;
+            stream_window(row, V, vec, seg, mx, invT, xa, [&](int k, float l) {
+                const float x = scaled_x(l, mx, invT);
+                if (x >= xa && in_top_k(l, k, r)) {
+                    const unsigned long long W = mass_of(own_exp(x));
+                    if (W >= Wmin) part += W;
+                }
+            });
+            r.S = block_sum_u64(part, sm.red);
+            r.tau = Wmin;
+            r.cut = V - 1;
+        }
+    }
+    return r;
+}
+
 // ------------------------------------------------------------- row kernel
 // Rows 0 .. B(Kd+1)-1 are the target rows (b, i) in order, then the B*Kd
 // draft rows (b, i).
 __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(
     const float* __restrict__ target, const float* __restrict__ draft, long long n_target_rows,
-    int V, int vec_ok, float invT, unsigned long long P, RowInfo* __restrict__ info,
-    float* __restrict__ segmax) {
+    int V, int vec_ok, float invT, unsigned long long P, int top_k, unsigned long long MP,
+    RowInfo* __restrict__ info, float* __restrict__ segmax) {
     extern __shared__ float4 dyn[];
     RowSmem& sm = *reinterpret_cast<RowSmem*>(dyn);
     const long long row = blockIdx.x;
@@ -811,7 +979,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(
                            ? target + row * static_cast<long long>(V)
                            : draft + (row - n_target_rows) * static_cast<long long>(V);
     float* seg = vec_ok ? segmax + row * static_cast<long long>(n_segments(V)) : nullptr;
-    const RowInfo r = row_stats(src, V, vec_ok != 0, invT, P, seg, sm);
+    const RowInfo r = row_stats(src, V, vec_ok != 0, invT, P, top_k, MP, seg, sm);
     if (threadIdx.x == 0) info[row] = r;
 }
 
@@ -831,9 +999,10 @@ struct DrawRow {
     __device__ __forceinline__ u128 weight(int v, float lpv, float lqv) const {
         const float xp = scaled_x(lpv, ip.mx, invT);
         if (xp < xth) return 0;
-        const unsigned long long wp = kept(mass_of(own_exp(xp)), v, ip);
+        const unsigned long long wp = kept(mass_of(own_exp(xp)), lpv, v, ip);
         if (lq == nullptr || wp == 0ull) return static_cast<u128>(wp);
-        const unsigned long long wq = kept(mass_of(own_exp(scaled_x(lqv, iq.mx, invT))), v, iq);
+        const unsigned long long wq =
+            kept(mass_of(own_exp(scaled_x(lqv, iq.mx, invT))), lqv, v, iq);
         const u128 a = static_cast<u128>(wp) * iq.S, c = static_cast<u128>(wq) * ip.S;
         return a > c ? a - c : static_cast<u128>(0);
     }
@@ -1026,9 +1195,9 @@ __global__ void __launch_bounds__(kThreads, 2) seq_kernel(
                 const float lpx = target[rp * V + x];
                 const float lqx = draft[(rq - n_target_rows) * V + x];
                 const unsigned long long Wp =
-                    kept(mass_of(own_exp(scaled_x(lpx, ip.mx, invT))), x, ip);
+                    kept(mass_of(own_exp(scaled_x(lpx, ip.mx, invT))), lpx, x, ip);
                 const unsigned long long Wq =
-                    kept(mass_of(own_exp(scaled_x(lqx, iq.mx, invT))), x, iq);
+                    kept(mass_of(own_exp(scaled_x(lqx, iq.mx, invT))), lqx, x, iq);
                 const unsigned long long U = rr[0] >> 8;
                 const u128 lhs = static_cast<u128>(U * Wq) * ip.S;
                 const u128 rhs = (static_cast<u128>(Wp) * iq.S) << 24;
@@ -1209,7 +1378,8 @@ size_t rejection_workspace_bytes(int B, int Kd, int V) {
 
 cudaError_t launch_accept_rejection(const float* target, const float* draft,
                                     const int32_t* drafts, int B, int Kd, int V, float invT,
-                                    uint64_t P, uint64_t seed, uint64_t offset, int32_t* tokens,
+                                    uint64_t P, int top_k, uint64_t MP, uint64_t seed,
+                                    uint64_t offset, int32_t* tokens,
                                     int32_t* len, void* ws, size_t ws_bytes, uint32_t* status,
                                     unsigned long long wait_ns, cudaStream_t s) {
     const long long n_target_rows = static_cast<long long>(B) * (Kd + 1);
@@ -1231,7 +1401,8 @@ cudaError_t launch_accept_rejection(const float* target, const float* draft,
                            ? 1
                            : 0;
     row_kernel<<<static_cast<unsigned>(rows), kRowThreads, smem, s>>>(
-        target, draft, n_target_rows, V, vec_ok, invT, static_cast<unsigned long long>(P), info,
+        target, draft, n_target_rows, V, vec_ok, invT, static_cast<unsigned long long>(P), top_k,
+        static_cast<unsigned long long>(MP), info,
         segmax);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

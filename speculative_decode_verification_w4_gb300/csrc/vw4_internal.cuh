@@ -124,7 +124,8 @@ size_t rejection_workspace_bytes(int B, int Kd, int V);
 cudaError_t launch_own_exp(const float* x, float* y, long long n, cudaStream_t s);
 cudaError_t launch_accept_rejection(const float* target, const float* draft,
                                     const int32_t* drafts, int B, int Kd, int V, float invT,
-                                    uint64_t P, uint64_t seed, uint64_t offset, int32_t* tokens,
+                                    uint64_t P, int top_k, uint64_t MP, uint64_t seed,
+                                    uint64_t offset, int32_t* tokens,
                                     int32_t* len, void* ws, size_t ws_bytes, uint32_t* status,
                                     unsigned long long wait_ns, cudaStream_t s);
 

@@ -81,9 +81,10 @@ def test_accept_argument_checks_on_host(lib):
     assert lib.accept_greedy(None, None, None, 1, 2, 10, 0x100, 0x200, None) == 1
     assert lib.accept_greedy(0x100, 0x100, None, 0, 2, 10, 0x100, 0x200, None) == 1
     assert lib.accept_greedy(0x100, 0x100, None, 1, 9, 10, 0x100, 0x200, None) == 1
-    prm = vw4.Sampling(0.6, 0.95, 5, 0.0)
-    assert lib.accept_rejection(0x100, 0x100, 0x100, 1, 2, 10, ctypes.byref(prm), 0, 0, 0x100,
-                                0x200, 0x1000, 1 << 20, None) == 2
+    for bad in (vw4.Sampling(0.6, 0.95, -1, 0.0), vw4.Sampling(0.6, 0.95, 5, 1.5),
+                vw4.Sampling(0.6, 0.95, 5, float("nan"))):
+        assert lib.accept_rejection(0x100, 0x100, 0x100, 1, 2, 10, ctypes.byref(bad), 0, 0,
+                                    0x100, 0x200, 0x1000, 1 << 20, None) == 1
     prm = vw4.Sampling(-1.0, 0.95, 0, 0.0)
     assert lib.accept_rejection(0x100, 0x100, 0x100, 1, 2, 10, ctypes.byref(prm), 0, 0, 0x100,
                                 0x200, 0x1000, 1 << 20, None) == 1

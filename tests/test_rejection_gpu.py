@@ -12,11 +12,11 @@ import speculative_decode_verification_w4_gb300 as vw4
 pytestmark = pytest.mark.gpu
 
 
-def gpu_accept(target, draft, drafts, T, top_p, seed, offset):
+def gpu_accept(target, draft, drafts, T, top_p, seed, offset, top_k=0, min_p=0.0):
     t = torch.from_numpy(np.ascontiguousarray(target)).cuda()
     d = torch.from_numpy(np.ascontiguousarray(draft)).cuda() if draft.size else None
     x = torch.from_numpy(np.ascontiguousarray(drafts, np.int32)).cuda()
-    tok, ln = vw4.accept_rejection(t, d, x, T, top_p, seed, offset)
+    tok, ln = vw4.accept_rejection(t, d, x, T, top_p, seed, offset, top_k=top_k, min_p=min_p)
     torch.cuda.synchronize()
     return tok.cpu().numpy(), ln.cpu().numpy()
 
@@ -144,3 +144,38 @@ def test_stochastic_sweep_full_size_sampled(Kd):
         rt, rl, _ = oracle.accept_rejection(target[b:b + 1], draft[b:b + 1], drafts[b:b + 1],
                                             0.6, 0.95, 4, 0, b_base=b)
         assert rl[0] == ln[b] and np.array_equal(rt[0], tok[b]), (b, rt, tok[b])
+
+
+@pytest.mark.parametrize("B,Kd,V,top_p,top_k,min_p", [
+    (16, 3, 16, 0.95, 5, 0.0), (32, 2, 1000, 0.95, 40, 0.0), (24, 4, 5000, 0.9, 40, 0.05),
+    (8, 3, 20000, 1.0, 100, 0.1), (12, 2, 777, 0.95, 1, 0.0), (10, 3, 3000, 0.95, 0, 0.2),
+    (6, 2, 2000, 0.8, 5000, 0.0), (9, 5, 40000, 0.95, 1000, 1.0), (20, 1, 151936, 0.95, 50, 0.05),
+])
+def test_top_k_and_min_p_match_oracle(B, Kd, V, top_p, top_k, min_p):
+    """The sampler's top-k and min-p stages (top-k above V is off; min-p 1
+    keeps the entries as likely as the top one)."""
+    target, draft, _ = synth.stochastic_case(B * 3 + V, B, Kd, V)
+    kw = dict(top_k=top_k, min_p=min_p)
+    drafts = oracle.sample_drafts(draft, 0.6, top_p, 3, 1 << 32, **kw)
+    tok, ln = gpu_accept(target, draft, drafts, 0.6, top_p, 3, 0, **kw)
+    rt, rl, _ = oracle.accept_rejection(target, draft, drafts, 0.6, top_p, 3, 0, **kw)
+    assert np.array_equal(ln, rl), (ln, rl)
+    assert np.array_equal(tok, rt)
+
+
+@pytest.mark.parametrize("V", [4096, 4095])
+def test_top_k_cut_inside_ties(V):
+    """Many equal logits: the top-k cut falls inside a run of equal keys and is
+    taken by index; rounded logits also tie in mass under top-p and min-p."""
+    B, Kd = 6, 3
+    target, draft, _ = synth.stochastic_case(77, B, Kd, V)
+    target = np.round(target)                       # long runs of equal logits
+    draft = np.round(draft * 2) / 2
+    target[2] = 0.0                                   # a flat position: every key equal
+    for top_k, min_p in ((30, 0.0), (200, 0.1), (V // 2, 0.0), (7, 0.5)):
+        drafts = oracle.sample_drafts(draft, 0.6, 0.95, 5, 1 << 32, top_k=top_k, min_p=min_p)
+        tok, ln = gpu_accept(target, draft, drafts, 0.6, 0.95, 5, 1, top_k=top_k, min_p=min_p)
+        rt, rl, _ = oracle.accept_rejection(target, draft, drafts, 0.6, 0.95, 5, 1, top_k=top_k,
+                                            min_p=min_p)
+        assert np.array_equal(ln, rl), (top_k, min_p, ln, rl)
+        assert np.array_equal(tok, rt), (top_k, min_p)
