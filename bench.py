@@ -398,6 +398,18 @@ def run_accept_timings(device, stream):
         us = e0.elapsed_time(e1) / reps * 1e3
         out[f"rejection_K{Kd}"] = {"us": round(us, 1),
                                    "logit_gbs": round(B * (2 * Kd + 1) * V * 4 / (us * 1e-6) / 1e9, 1)}
+        if Kd in (1, 8):
+            # the same step with the sampler's top-k (50) and min-p (0.05) stages on
+            e0.record(stream)
+            for r in range(reps):
+                vw4.accept_rejection(tgt, drf, drafts, 0.6, 0.95, 4, r, top_k=50, min_p=0.05,
+                                     workspace=ws, stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) / reps * 1e3
+            out[f"rejection_K{Kd}_topk50_minp0.05"] = {
+                "us": round(us, 1),
+                "logit_gbs": round(B * (2 * Kd + 1) * V * 4 / (us * 1e-6) / 1e9, 1)}
         del tgt, drf
     # greedy accept of 7 drafts from 8 fp32 logits rows of the LM head (V =
     # 262144): a CUDA graph over 20 logits copies (160 MB, more than L2), so
