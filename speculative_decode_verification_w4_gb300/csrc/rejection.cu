@@ -499,6 +499,74 @@ __device__ float row_max(const float* __restrict__ row, int V, bool vec, float* 
     return block_max(lmax, sm.red);
 }
 
+// Sorts a[0 .. n) in descending order (n a power of two; the whole block).
+template <class T>
+__device__ void block_sort_desc(T* a, unsigned int n) {
+    for (unsigned int k = 2; k <= n; k <<= 1) {
+        for (unsigned int j = k >> 1; j > 0; j >>= 1) {
+            for (unsigned int t = threadIdx.x; t < n; t += blockDim.x) {
+                const unsigned int u = t ^ j;
+                if (u > t) {
+                    const T x = a[t], y = a[u];
+                    if ((t & k) == 0 ? (x < y) : (x > y)) {
+                        a[t] = y;
+                        a[u] = x;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// The top-k cut from the segment maxima: the k-th largest segment max L is
+// a lower bound of the k-th largest entry (the k largest maxima are k
+// distinct entries >= L), so every top-k entry has a key >= L and lies in a
+// segment whose max reaches L.  Those entries are gathered (each as the
+// packed key (logit key, ~index)), sorted, and the k-th is the cut.  Returns
+// false -- nothing decided -- when the row has too many segments, k is
+// larger than the gather can hold, or too many entries reach L.
+__device__ bool top_k_cut_segments(const float* __restrict__ row, int V, const float* seg,
+                                   int top_k, RowSmem& sm, uint32_t& K, int& I) {
+    constexpr int kMaxSegSort = 2048;
+    const int nseg = n_segments(V);
+    if (nseg > kMaxSegSort || nseg < top_k || top_k > kCandTotal) return false;
+    const int tid = threadIdx.x;
+    uint32_t* sk = reinterpret_cast<uint32_t*>(&sm.whist[0][0]);  // [kMaxSegSort]
+    unsigned int pw = 1;
+    while (pw < static_cast<unsigned int>(nseg)) pw <<= 1;
+    for (unsigned int t = tid; t < pw; t += kRowThreads)
+        sk[t] = t < static_cast<unsigned int>(nseg) ? logit_key(__ldcg(seg + t)) : 0u;
+    __syncthreads();
+    block_sort_desc(sk, pw);
+    const uint32_t L = sk[top_k - 1];
+    if (tid == 0) sm.ncand = 0;
+    __syncthreads();
+    stream_segments(row, V, true, seg, [&](float m) { return logit_key(m) >= L; },
+                    [&](int k, float l) {
+                        const uint32_t key = logit_key(l);
+                        if (key >= L) {
+                            const unsigned int slot = atomicAdd(&sm.ncand, 1u);
+                            if (slot < static_cast<unsigned int>(kCandTotal))
+                                sm.cw[slot] = (static_cast<unsigned long long>(key) << 32) |
+                                              (0xFFFFFFFFu - static_cast<uint32_t>(k));
+                        }
+                    });
+    __syncthreads();
+    const unsigned int C = sm.ncand;
+    if (C > static_cast<unsigned int>(kCandTotal)) return false;  // the same in every thread
+    unsigned int pc = 1;
+    while (pc < C) pc <<= 1;
+    for (unsigned int t = C + tid; t < pc; t += kRowThreads) sm.cw[t] = 0ull;
+    __syncthreads();
+    block_sort_desc(sm.cw, pc);
+    const unsigned long long kk = sm.cw[top_k - 1];
+    K = static_cast<uint32_t>(kk >> 32);
+    I = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(kk));
+    __syncthreads();
+    return true;
+}
+
 // The top-k cut of a row: the key K and index I of its top_k-th entry in
 // (logit key desc, index asc) order, so that an entry is among the first
 // top_k iff its key > K, or == K and its index <= I.  A radix select on the
@@ -509,6 +577,7 @@ __device__ float row_max(const float* __restrict__ row, int V, bool vec, float* 
 // among them in index order.
 __device__ void top_k_cut(const float* __restrict__ row, int V, bool vec, const float* seg,
                           int top_k, RowSmem& sm, uint32_t& K, int& I) {
+    if (seg != nullptr && top_k_cut_segments(row, V, seg, top_k, sm, K, I)) return;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     uint32_t* hist = reinterpret_cast<uint32_t*>(&sm.whist[0][0]);  // [kRowWarps][256]
     uint32_t prefix = 0u;
