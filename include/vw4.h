@@ -86,8 +86,8 @@ typedef struct vw4_weight {
 typedef struct vw4_sampling {
     float temperature;      /* 0 routes to the greedy rule (no random numbers)  */
     float top_p;            /* (0, 1]; >= 1 keeps the whole vocabulary         */
-    int32_t top_k;          /* 0 = off (other values: VW4_ERR_UNSUPPORTED)     */
-    float min_p;            /* 0 = off (other values: VW4_ERR_UNSUPPORTED)     */
+    int32_t top_k;          /* 0 = off; >= V keeps everything; < 0 invalid      */
+    float min_p;            /* 0 = off; in [0, 1]                               */
 } vw4_sampling;
 
 /* Operation ids for vw4_workspace_bytes. */
@@ -221,25 +221,30 @@ VW4_API vw4_status accept_greedy(const float* target_logits_dev, const int32_t* 
  * "Why it is interesting on a Mac specifically" (Leviathan and Chen rejection
  * sampling with residual correction reproduces plain decoding at temperature
  * 0.6, top_p 0.95); the mtp.go commit log paragraphs "Greedy is a special case
- * of sampled decoding" and "rework the MLX sampler" (pipeline temperature /
- * softmax -> top-p -> normalize -> categorical; acceptance, residual and bonus
- * draws reuse the same draft and target distributions; seeded, reproducible).
+ * of sampled decoding" and "rework the MLX sampler" (pipeline
+ * top-k -> temperature / softmax -> top-p -> min-p -> normalize -> categorical;
+ * acceptance, residual and bonus draws reuse the same draft and target
+ * distributions; seeded, reproducible).
  *
  * Exact integer form (identical on the oracle, so ids are bit-exact): each
- * row's weights W_v = floor(exp_own((l_v - max l) * (1/T)) * 2^40); top-p
- * keeps the shortest prefix in (W desc, index asc) order whose mass satisfies
- * cum * 2^32 >= round(top_p * 2^32) * sum W.  Philox4x32-10 block for draft
- * position i of sequence b: counter (i, b, offset lo, offset hi), key = seed;
- * U = r0 >> 8 decides acceptance (U * q(x) * Sp < 2^24 * p(x) * Sq), and the
- * 64-bit r2:r1 draws the residual max(0, p*Sq - q*Sp) at the first rejection
- * or the bonus from p_Kd (block (Kd, b)) when all drafts are accepted.
+ * row's weights W_v = floor(exp_own((l_v - max l) * (1/T)) * 2^40).  Top-k
+ * keeps the first top_k entries in (logit desc, index asc) order (NaN reads
+ * as -inf, -0 as +0); top-p then keeps the shortest prefix of the kept
+ * entries in (W desc, index asc) order whose mass satisfies
+ * cum * 2^32 >= round(top_p * 2^32) * sum W; min-p then keeps the entries with
+ * W >= round(min_p * 2^32) * 2^8 (the top entry's W is 2^40).  Philox4x32-10
+ * block for draft position i of sequence b: counter (i, b, offset lo,
+ * offset hi), key = seed; U = r0 >> 8 decides acceptance
+ * (U * q(x) * Sp < 2^24 * p(x) * Sq), and the 64-bit r2:r1 draws the residual
+ * max(0, p*Sq - q*Sp) at the first rejection or the bonus from p_Kd
+ * (block (Kd, b)) when all drafts are accepted.
  *
  * target_logits_dev  fp32 [B][Kd+1][V]; draft_logits_dev fp32 [B][Kd][V]
  *             (may be NULL when Kd == 0); drafts_dev int32 [B][Kd].
- * B >= 1, 0 <= Kd <= 8, 1 <= V <= 393216 (the row is held on chip by a
- *             cluster of up to 8 CTAs; larger V returns VW4_ERR_UNSUPPORTED).
+ * B >= 1, 0 <= Kd <= 8, 1 <= V <= 2^24 (rows are streamed from memory).
  * params      temperature >= 0 (0 = greedy rule, no random numbers drawn),
- *             top_p in (0, 1], top_k == 0, min_p == 0.
+ *             top_p in (0, 1] (finite, values above 1 act as 1), top_k >= 0,
+ *             min_p in [0, 1]; anything else is VW4_ERR_INVALID_ARG.
  * seed, offset  Philox key and counter offset.
  * tokens_dev, len_dev  as accept_greedy.
  * workspace_dev / ws_bytes  at least vw4_workspace_bytes(VW4_OP_REJECTION, B, Kd, V).

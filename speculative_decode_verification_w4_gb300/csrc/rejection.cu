@@ -499,47 +499,70 @@ __device__ float row_max(const float* __restrict__ row, int V, bool vec, float* 
     return block_max(lmax, sm.red);
 }
 
-// Sorts a[0 .. n) in descending order (n a power of two; the whole block).
-template <class T>
-__device__ void block_sort_desc(T* a, unsigned int n) {
-    for (unsigned int k = 2; k <= n; k <<= 1) {
-        for (unsigned int j = k >> 1; j > 0; j >>= 1) {
-            for (unsigned int t = threadIdx.x; t < n; t += blockDim.x) {
-                const unsigned int u = t ^ j;
-                if (u > t) {
-                    const T x = a[t], y = a[u];
-                    if ((t & k) == 0 ? (x < y) : (x > y)) {
-                        a[t] = y;
-                        a[u] = x;
-                    }
-                }
-            }
-            __syncthreads();
-        }
-    }
-}
-
-// The top-k cut from the segment maxima: the k-th largest segment max L is
-// a lower bound of the k-th largest entry (the k largest maxima are k
-// distinct entries >= L), so every top-k entry has a key >= L and lies in a
-// segment whose max reaches L.  Those entries are gathered (each as the
-// packed key (logit key, ~index)), sorted, and the k-th is the cut.  Returns
-// false -- nothing decided -- when the row has too many segments, k is
-// larger than the gather can hold, or too many entries reach L.
+// The top-k cut from the segment maxima.  Any L at or below the k-th largest
+// segment max bounds the k-th largest entry from below (the k largest maxima
+// are k distinct entries >= L), so every top-k entry has a key >= L and lies
+// in a segment whose max reaches L.  L is the lower edge of the 16-bit key
+// bucket holding the k-th largest maximum (two 256-bucket histograms of the
+// maxima); the entries >= L are gathered (each as the packed key (logit key,
+// ~index), all distinct) and the k-th of them found by counting ranks.
+// Returns false -- nothing decided -- when the row has too many segments, k
+// is larger than the gather holds, or too many entries reach L.
 __device__ bool top_k_cut_segments(const float* __restrict__ row, int V, const float* seg,
                                    int top_k, RowSmem& sm, uint32_t& K, int& I) {
-    constexpr int kMaxSegSort = 2048;
+    constexpr int kMaxSegs = 2048;
     const int nseg = n_segments(V);
-    if (nseg > kMaxSegSort || nseg < top_k || top_k > kCandTotal) return false;
-    const int tid = threadIdx.x;
-    uint32_t* sk = reinterpret_cast<uint32_t*>(&sm.whist[0][0]);  // [kMaxSegSort]
-    unsigned int pw = 1;
-    while (pw < static_cast<unsigned int>(nseg)) pw <<= 1;
-    for (unsigned int t = tid; t < pw; t += kRowThreads)
-        sk[t] = t < static_cast<unsigned int>(nseg) ? logit_key(__ldcg(seg + t)) : 0u;
-    __syncthreads();
-    block_sort_desc(sk, pw);
-    const uint32_t L = sk[top_k - 1];
+    if (nseg > kMaxSegs || nseg < top_k || top_k > kCandTotal) return false;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    uint32_t* sk = reinterpret_cast<uint32_t*>(&sm.whist[0][0]);  // [kMaxSegs] maxima keys
+    uint32_t* hist = sk + kMaxSegs;                                // [256]
+    for (int t = tid; t < nseg; t += kRowThreads) sk[t] = logit_key(__ldcg(seg + t));
+    uint32_t prefix = 0u;
+    unsigned int need = static_cast<unsigned int>(top_k);
+    for (int shift = 24; shift >= 16; shift -= 8) {
+        const uint32_t hmask = shift == 24 ? 0u : 0xFF000000u;
+        if (tid < 256) hist[tid] = 0u;
+        __syncthreads();
+        for (int t0 = 0; t0 < nseg; t0 += kRowThreads) {  // the whole warp in step
+            const int t = t0 + tid;
+            const bool in = t < nseg && (sk[t] & hmask) == prefix;
+            const unsigned int d = in ? ((sk[t] >> shift) & 255u) : 256u;
+            const unsigned int peers = __match_any_sync(0xffffffffu, d);
+            if (in && __ffs(peers) - 1 == lane) atomicAdd(&hist[d], __popc(peers));
+        }
+        __syncthreads();
+        if (wid == 0) {
+            // lane j holds buckets 255 - 8j .. 248 - 8j, counted from the top
+            unsigned int c8[8], sum = 0u;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                c8[i] = hist[255 - 8 * lane - i];
+                sum += c8[i];
+            }
+            unsigned int incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            unsigned int run = incl - sum;
+            if (run < need && need <= incl) {
+                for (int i = 0; i < 8; ++i) {
+                    if (run + c8[i] >= need) {
+                        sm.beta = 255 - 8 * lane - i;
+                        sm.above = run;
+                        break;
+                    }
+                    run += c8[i];
+                }
+            }
+        }
+        __syncthreads();
+        prefix |= static_cast<uint32_t>(sm.beta) << shift;
+        need -= static_cast<unsigned int>(sm.above);
+        __syncthreads();
+    }
+    const uint32_t L = prefix;  // the 16-bit bucket's lower edge
     if (tid == 0) sm.ncand = 0;
     __syncthreads();
     stream_segments(row, V, true, seg, [&](float m) { return logit_key(m) >= L; },
@@ -555,12 +578,15 @@ __device__ bool top_k_cut_segments(const float* __restrict__ row, int V, const f
     __syncthreads();
     const unsigned int C = sm.ncand;
     if (C > static_cast<unsigned int>(kCandTotal)) return false;  // the same in every thread
-    unsigned int pc = 1;
-    while (pc < C) pc <<= 1;
-    for (unsigned int t = C + tid; t < pc; t += kRowThreads) sm.cw[t] = 0ull;
+    // the candidate with exactly top_k - 1 larger ones
+    for (unsigned int i = tid; i < C; i += kRowThreads) {
+        const unsigned long long ki = sm.cw[i];
+        unsigned int rank = 0u;
+        for (unsigned int j = 0; j < C; ++j) rank += sm.cw[j] > ki ? 1u : 0u;
+        if (rank == static_cast<unsigned int>(top_k - 1)) sm.lo = ki;
+    }
     __syncthreads();
-    block_sort_desc(sm.cw, pc);
-    const unsigned long long kk = sm.cw[top_k - 1];
+    const unsigned long long kk = sm.lo;
     K = static_cast<uint32_t>(kk >> 32);
     I = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(kk));
     __syncthreads();
