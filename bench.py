@@ -45,6 +45,8 @@ LAYER = [("q", 6144, 5120), ("k", 1024, 5120), ("v", 1024, 5120), ("o", 5120, 61
          ("gate", 17408, 5120), ("up", 17408, 5120), ("down", 5120, 17408)]
 STEP = [("qkv", 8192, 5120), ("o", 5120, 6144), ("gate_up", 34816, 5120), ("down", 5120, 17408)]
 HEAD_M = 8
+# verify widths timed per M (9..16 rows take the two-n-tile kernel)
+PER_M = (1, 2, 4, 8, 16)
 METRIC = "nvfp4 verify-GEMM HBM GB/s & µs/pass at M=1,2,4,8; accept µs/step"
 WORKLOAD = ("dense-27B-like layer verify: d=5120, q/k/v/o 5120->6144/1024/1024 and 6144->5120, "
             "gate/up 5120->17408, down 17408->5120, nvfp4 (E2M1 + E4M3 per 16 + fp32 tensor "
@@ -195,11 +197,12 @@ def run_ours(args, rank, world, device):
 
     torch.cuda.set_device(device)
     layers = {"nvfp4": make_layer("nvfp4", device), "q4_0": make_layer("q4_0", device)}
-    acts = {M: make_acts(M, device, seed=7 + M) for M in (1, 2, 4, 8)}
+    acts = {M: make_acts(M, device, seed=7 + M) for M in PER_M}
     outs = {M: [torch.empty((M, N), dtype=torch.float32, device=device) for _, N, _ in STEP]
-            for M in (1, 2, 4, 8)}
+            for M in PER_M}
     ws = vw4.Workspace(device)
-    ws.get(max(vw4.vw4_workspace_bytes(vw4.OP_GEMM, 8, N, K) for _, N, K in STEP + LAYER))
+    ws.get(max(vw4.vw4_workspace_bytes(vw4.OP_GEMM, max(PER_M), N, K)
+               for _, N, K in STEP + LAYER))
     FMTS = {"nvfp4": vw4.FMT_NVFP4, "q4_0": vw4.FMT_Q4_0}
 
     def one_step(fmt, M):
@@ -273,7 +276,7 @@ def run_ours(args, rank, world, device):
         per_m = {}
         for fmt in ("nvfp4", "q4_0"):
             per_m[fmt] = {}
-            for M in (1, 2, 4, 8):
+            for M in PER_M:
                 gm = capture(lambda: one_step(fmt, M))
                 m_ms = time_graph(gm, steps, 3)
                 per_m[fmt][str(M)] = {
@@ -282,7 +285,7 @@ def run_ours(args, rank, world, device):
                     "call_us": {}}
                 del gm
             for j, (name, N, K, qd, sd, ts) in enumerate(layers[fmt]):
-                for M in (1, 2, 4, 8):
+                for M in PER_M:
                     per_m[fmt][str(M)]["call_us"][name] = time_alone(
                         fmt, name, N, K, qd, sd, ts, acts[M][j], outs[M][j], steps)
 

@@ -110,7 +110,11 @@ typedef struct vw4_sampling {
  *
  * W           weight descriptor (host pointer to the struct; device data).
  * A_dev       bf16 [M][lda], lda >= K.
- * M           1..8 verify rows.
+ * M           1..16 verify rows.  Up to 8 rows take one mma n-tile; 9..16
+ *             take two that share every unpacked weight fragment (wider
+ *             batches, as in the batched head forward of Ollama's mtp.go
+ *             commit log, where per-token cost falls as the batch grows):
+ *             each weight block is still read and unpacked once per call.
  * out_dev     fp32 [M][ldo], ldo >= N.
  * row_argmax_dev  optional (NULL = skip): int32 [M]; row m receives the index
  *             of its largest output (ties to the lowest index; NaN never
@@ -118,7 +122,7 @@ typedef struct vw4_sampling {
  * workspace_dev / ws_bytes  scratch of at least
  *             vw4_workspace_bytes(VW4_OP_GEMM, M, N, K) bytes, 256-byte
  *             aligned, reused freely between calls on the same stream.
- * Error behaviour: VW4_ERR_INVALID_ARG for null pointers, M outside 1..8,
+ * Error behaviour: VW4_ERR_INVALID_ARG for null pointers, M outside 1..16,
  * N < 1, K not a positive multiple of the block, lda < K, ldo < N;
  * VW4_ERR_ALIGN for misaligned pointers or leading dimensions;
  * VW4_ERR_WORKSPACE when the workspace is too small.
@@ -145,13 +149,13 @@ VW4_API vw4_status verify_gemm_w4(const vw4_weight* W, const void* A_dev, int M,
  * argmax of position n at i == n, -1 after; len[b] = n + 1, n the length of
  * the agreeing prefix.
  *
- * W, A_dev, lda   as verify_gemm_w4; B * (Kd + 1) must be 1..8.
+ * W, A_dev, lda   as verify_gemm_w4; B * (Kd + 1) must be 1..16.
  * drafts_dev      int32 [B][Kd] (may be NULL when Kd == 0).
  * tokens_dev      int32 [B][Kd + 1]; len_dev int32 [B].
  * out_dev, ldo    optional fp32 [M][ldo] logits; NULL = not written.
  * workspace_dev / ws_bytes  as verify_gemm_w4 for M rows.
  * Errors: as verify_gemm_w4, and VW4_ERR_INVALID_ARG for B < 1, Kd < 0,
- * B * (Kd + 1) > 8 or null outputs.  A draft id outside [0, N) ends the
+ * B * (Kd + 1) > 16 or null outputs.  A draft id outside [0, N) ends the
  * prefix and sets VW4_DEV_BAD_DRAFT_ID in the device status word.
  */
 VW4_API vw4_status verify_greedy_w4(const vw4_weight* W, const void* A_dev, int lda,
@@ -263,7 +267,7 @@ VW4_API vw4_status accept_rejection(const float* target_logits_dev, const float*
  * only its input and output pointers, code living in another framework's
  * memory pool that must not allocate outside it, or a path where calling
  * cudaMalloc would synchronize the device.  This entry point takes no
- * workspace and allocates nothing; it uses one fixed 8 MiB scratch array in
+ * workspace and allocates nothing; it uses one fixed 16 MiB scratch array in
  * device memory that the library reserves on every GPU it is loaded on, for
  * as long as the process lives.
  *

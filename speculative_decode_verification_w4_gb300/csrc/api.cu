@@ -27,7 +27,7 @@ constexpr int kMaxGrid = 608;  // upper bound of the persistent GEMM grid (works
 struct DeviceInfo {
     bool ready = false;
     int sms = 0;
-    int occ[3] = {0, 0, 0};  // GEMM CTAs per SM by fmt
+    int occ[3][2] = {};  // GEMM CTAs per SM by fmt and row block (8, 16 rows)
     uint32_t* status = nullptr;
 };
 
@@ -57,8 +57,10 @@ vw4_status device_info(DeviceInfo** out) {
     if (!d.ready) {
         e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-        d.occ[1] = gemm_blocks_per_sm(1);
-        d.occ[2] = gemm_blocks_per_sm(2);
+        for (int f = 1; f <= 2; ++f) {
+            d.occ[f][0] = gemm_blocks_per_sm(f, 8);
+            d.occ[f][1] = gemm_blocks_per_sm(f, 16);
+        }
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_status_word);
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
@@ -176,13 +178,13 @@ VW4_API void vw4_set_wait_limit_ns(uint64_t ns) {
 VW4_API size_t vw4_workspace_bytes(int op, int a, int b, int c) {
     if (op == VW4_OP_GEMM) {
         const int M = a, N = b, K = c;
-        if (M < 1 || M > kMaxRows || N < 1 || K < kStageK || K % kStageK) return 0;
-        return gemm_workspace_layout(nullptr, 1, N, K, kMaxGrid, 0).bytes;
+        if (M < 1 || M > kMaxVerifyRows || N < 1 || K < kStageK || K % kStageK) return 0;
+        return gemm_workspace_layout(nullptr, 1, N, K, kMaxGrid, 0, gemm_rows_for(M)).bytes;
     }
     if (op == VW4_OP_MOE) {
         const int P = a, N = b, K = c;
         if (P < 1 || P > kMaxSeg || N < 1 || K < kStageK || K % kStageK) return 0;
-        return gemm_workspace_layout(nullptr, P, N, K, kMaxGrid, P).bytes;
+        return gemm_workspace_layout(nullptr, P, N, K, kMaxGrid, P, 8).bytes;
     }
     if (op == VW4_OP_REJECTION) {
         if (a < 1 || b < 0 || b > 8 || c < 1) return 0;
@@ -208,14 +210,16 @@ static vw4_status gemm_entry(const vw4_weight* W, const void* A_dev, int M, int 
     vw4_status st = check_weight(W);
     if (st != VW4_OK) return st;
     if (!A_dev || (!out_dev && !greedy)) return VW4_ERR_INVALID_ARG;
-    if (M < 1 || M > kMaxRows || lda < W->K || (out_dev && ldo < W->N))
+    if (M < 1 || M > kMaxVerifyRows || lda < W->K || (out_dev && ldo < W->N))
         return VW4_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(A_dev) & 1u) || (reinterpret_cast<uintptr_t>(out_dev) & 3u))
         return VW4_ERR_ALIGN;
     if (!workspace_dev) return VW4_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace_dev) & 255u) != 0) return VW4_ERR_ALIGN;
     const int N = W->N, K = W->K;
-    GemmWorkspace ws = gemm_workspace_layout(workspace_dev, 1, N, K, kMaxGrid, 0);
+    // 1..8 rows: one mma n-tile; 9..16: two n-tiles over the same weights
+    const int nr = gemm_rows_for(M);
+    GemmWorkspace ws = gemm_workspace_layout(workspace_dev, 1, N, K, kMaxGrid, 0, nr);
     if (ws.bytes > ws_bytes) return VW4_ERR_WORKSPACE;
     DeviceInfo* d = nullptr;
     st = device_info(&d);
@@ -234,7 +238,7 @@ static vw4_status gemm_entry(const vw4_weight* W, const void* A_dev, int M, int 
     const int T = K / kStageK;
     const int n_tiles = (N + kTileRows - 1) / kTileRows;
     const long long U = static_cast<long long>(n_tiles) * T;
-    long long G = static_cast<long long>(d->sms) * d->occ[W->fmt];
+    long long G = static_cast<long long>(d->sms) * d->occ[W->fmt][nr == 16 ? 1 : 0];
     if (G > kMaxGrid) G = kMaxGrid;
     // When every tile fits in one wave, split each tile's stages into S
     // nearly equal parts, one CTA each (no CTA spans two tiles, and a part has
@@ -257,7 +261,7 @@ static vw4_status gemm_entry(const vw4_weight* W, const void* A_dev, int M, int 
     const bool clustered = split > 1 && split <= kMaxClusterSplit && !fused_argmax;
 
     cudaError_t e = launch_prep_act(static_cast<const uint16_t*>(A_dev), lda, K, W->fmt, M, 0, 1,
-                                    1, ws, n_tiles * kConsumerWarps, s);
+                                    1, ws, n_tiles * kConsumerWarps, s, nr);
     if (e != cudaSuccess) return cuda_fail(e, "prep_act launch");
     GemmParams p{};
     p.N = N;
@@ -288,7 +292,7 @@ static vw4_status gemm_entry(const vw4_weight* W, const void* A_dev, int M, int 
         p.tokens = greedy->tokens;
         p.len = greedy->len;
     }
-    e = launch_gemm(W->fmt, tmW, tmS, p, static_cast<int>(G), clustered ? split : 1, s);
+    e = launch_gemm(W->fmt, nr, tmW, tmS, p, static_cast<int>(G), clustered ? split : 1, s);
     if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
     return VW4_OK;
 }
@@ -304,7 +308,7 @@ VW4_API vw4_status verify_greedy_w4(const vw4_weight* W, const void* A_dev, int 
                                     const int32_t* drafts_dev, int B, int Kd, int32_t* tokens_dev,
                                     int32_t* len_dev, float* out_dev, int ldo,
                                     void* workspace_dev, size_t ws_bytes, void* stream) {
-    if (B < 1 || Kd < 0 || B * (Kd + 1) > kMaxRows) return VW4_ERR_INVALID_ARG;
+    if (B < 1 || Kd < 0 || B * (Kd + 1) > kMaxVerifyRows) return VW4_ERR_INVALID_ARG;
     if (!tokens_dev || !len_dev || (Kd > 0 && !drafts_dev)) return VW4_ERR_INVALID_ARG;
     const GreedyArgs g{drafts_dev, B, Kd, tokens_dev, len_dev};
     return gemm_entry(W, A_dev, B * (Kd + 1), lda, out_dev, ldo, nullptr, &g, workspace_dev,
@@ -331,7 +335,7 @@ VW4_API vw4_status verify_moe_w4(const vw4_weight* experts, int E, const void* A
     if (!workspace_dev) return VW4_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace_dev) & 255u) != 0) return VW4_ERR_ALIGN;
     const int P = M * topk;
-    GemmWorkspace ws = gemm_workspace_layout(workspace_dev, P, N, K, kMaxGrid, P);
+    GemmWorkspace ws = gemm_workspace_layout(workspace_dev, P, N, K, kMaxGrid, P, 8);
     if (ws.bytes > ws_bytes) return VW4_ERR_WORKSPACE;
     DeviceInfo* d = nullptr;
     st = device_info(&d);
@@ -350,7 +354,7 @@ VW4_API vw4_status verify_moe_w4(const vw4_weight* experts, int E, const void* A
 
     const int T = K / kStageK;
     const int n_tiles = (N + kTileRows - 1) / kTileRows;
-    long long G = static_cast<long long>(d->sms) * d->occ[experts->fmt];
+    long long G = static_cast<long long>(d->sms) * d->occ[experts->fmt][0];
     if (G > kMaxGrid) G = kMaxGrid;
     const long long U_max = static_cast<long long>(P) * n_tiles * T;
     if (G > U_max) G = U_max;
@@ -358,7 +362,7 @@ VW4_API vw4_status verify_moe_w4(const vw4_weight* experts, int E, const void* A
     // the prep launch routes the pairs as well
     cudaError_t e = launch_prep_act(static_cast<const uint16_t*>(A_dev), lda, K, experts->fmt, 0,
                                     rows_are_pairs, topk, P, ws, P * n_tiles * kConsumerWarps, s,
-                                    expert_ids_dev, E, d->status, combine ? nullptr : out_dev, ldo,
+                                    8, expert_ids_dev, E, d->status, combine ? nullptr : out_dev, ldo,
                                     N);
     if (e != cudaSuccess) return cuda_fail(e, "prep_act launch");
     GemmParams p{};
@@ -384,7 +388,7 @@ VW4_API vw4_status verify_moe_w4(const vw4_weight* experts, int E, const void* A
     p.row_argmax = nullptr;
     p.status = d->status;
     p.wait_ns = g_wait_ns;
-    e = launch_gemm(experts->fmt, tmW, tmS, p, static_cast<int>(G), 1, s);
+    e = launch_gemm(experts->fmt, 8, tmW, tmS, p, static_cast<int>(G), 1, s);
     if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
     if (combine) {
         e = launch_combine(ws.pair_out, gates_dev, expert_ids_dev, E, M, topk, N, out_dev, ldo, s);
@@ -492,7 +496,7 @@ VW4_API vw4_status vw4_get_device_status(uint32_t* bits, void* stream) {
 // host-side stand-in, not a device address).
 // Every GPU has its own copy of the array.  Its size bounds the shapes this
 // entry point accepts (the workspace of verify_gemm_w4 for that shape).
-static constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+static constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 static std::mutex g_noalloc_mu;
 static void* g_noalloc_ptr[kMaxDevices] = {};
@@ -502,14 +506,16 @@ extern "C" {
 VW4_API vw4_status verify_gemm_w4_noalloc(const vw4_weight* W, const void* A_dev, int M, int lda,
                                           float* out_dev, int ldo, int32_t* row_argmax_dev,
                                           void* stream) {
-    if (W && W->N >= 1 && W->K >= kStageK && W->K % kStageK == 0) {
-        const size_t need = gemm_workspace_layout(nullptr, 1, W->N, W->K, kMaxGrid, 0).bytes;
+    if (W && W->N >= 1 && W->K >= kStageK && W->K % kStageK == 0 && M >= 1 &&
+        M <= kMaxVerifyRows) {
+        const size_t need =
+            gemm_workspace_layout(nullptr, 1, W->N, W->K, kMaxGrid, 0, gemm_rows_for(M)).bytes;
         if (need > kNoAllocScratchBytes) {
             char buf[160];
             snprintf(buf, sizeof buf,
-                     "verify_gemm_w4_noalloc: N=%d K=%d needs %zu scratch bytes, above the "
+                     "verify_gemm_w4_noalloc: M=%d N=%d K=%d needs %zu scratch bytes, above the "
                      "fixed %zu",
-                     W->N, W->K, need, kNoAllocScratchBytes);
+                     M, W->N, W->K, need, kNoAllocScratchBytes);
             g_last_error = buf;
             return VW4_ERR_WORKSPACE;
         }

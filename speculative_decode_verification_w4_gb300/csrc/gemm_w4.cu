@@ -49,7 +49,7 @@ constexpr uint32_t kStatusBadExpert = 0x2u;
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 GemmWorkspace gemm_workspace_layout(void* base, int n_seg_max, int N, int K, int grid,
-                                    int pair_rows) {
+                                    int pair_rows, int nr) {
     GemmWorkspace w{};
     char* b = static_cast<char*>(base);
     size_t off = 0;
@@ -61,10 +61,10 @@ GemmWorkspace gemm_workspace_layout(void* base, int n_seg_max, int N, int K, int
     const int T = K / kStageK;
     const int n_tiles = (N + kTileRows - 1) / kTileRows;
     w.seg = static_cast<SegTable*>(take(sizeof(SegTable)));
-    w.act = static_cast<uint8_t*>(take((size_t)n_seg_max * T * kAStride));
-    w.partials = static_cast<float*>(take((size_t)2 * grid * kPartialFloats * sizeof(float)));
+    w.act = static_cast<uint8_t*>(take((size_t)n_seg_max * T * act_stride(nr)));
+    w.partials = static_cast<float*>(take((size_t)2 * grid * nr * kTileRows * sizeof(float)));
     w.tile_cnt = static_cast<uint32_t*>(take((size_t)n_seg_max * n_tiles * kConsumerWarps * 4));
-    w.am_key = static_cast<unsigned long long*>(take(sizeof(unsigned long long) * kMaxRows));
+    w.am_key = static_cast<unsigned long long*>(take(sizeof(unsigned long long) * kMaxVerifyRows));
     w.am_cnt = static_cast<uint32_t*>(take(4));
     w.pair_out = pair_rows ? static_cast<float*>(take((size_t)pair_rows * N * sizeof(float)))
                            : nullptr;
@@ -180,8 +180,9 @@ __device__ void route_pairs(const int32_t* __restrict__ ids, int P, int E, SegTa
 // (tiny) routing into its own shared memory and block 0 publishes it for the
 // GEMM, marks invalid expert ids in the status word and zeroes their output
 // rows (out_zero, when the pair rows are the output).
-__global__ void __launch_bounds__(256) prep_act_kernel(
-    const uint16_t* __restrict__ A, int lda, int vec_ok, int K, int fmt, int dense_M,
+// One warp per verify row: 256 threads (8 rows) or 512 (16 rows, dense only).
+__global__ void __launch_bounds__(512) prep_act_kernel(
+    const uint16_t* __restrict__ A, int lda, int vec_ok, int K, int fmt, int nr, int dense_M,
     int rows_are_pairs, int topk, SegTable* seg, uint8_t* act, uint32_t* tile_cnt, int n_cnt,
     unsigned long long* am_key, uint32_t* am_cnt, const int32_t* __restrict__ ids, int P, int E,
     uint32_t* status, float* out_zero, int ldo, int N) {
@@ -198,7 +199,7 @@ __global__ void __launch_bounds__(256) prep_act_kernel(
     const int r = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (blockIdx.x == 0) {
         for (int i = threadIdx.x; i < n_cnt; i += blockDim.x) tile_cnt[i] = 0u;
-        if (threadIdx.x < kMaxRows) am_key[threadIdx.x] = 0ull;
+        if (threadIdx.x < kMaxVerifyRows) am_key[threadIdx.x] = 0ull;
         if (threadIdx.x == 0) *am_cnt = 0u;
     }
     int count, src_row = 0;
@@ -230,10 +231,11 @@ __global__ void __launch_bounds__(256) prep_act_kernel(
             src_row = rows_are_pairs ? pr : pr / topk;
         }
     }
-    uint8_t* blk = act + (static_cast<size_t>(sgi) * T + st) * kAStride;
+    uint8_t* blk = act + (static_cast<size_t>(sgi) * T + st) * act_stride(nr);
     __half* dst = reinterpret_cast<__half*>(blk);
-    float* inv = reinterpret_cast<float*>(blk + kABytes);
-    // Where this lane's 16-byte chunk goes in the stage's [8][256] block.  The
+    float* inv = reinterpret_cast<float*>(blk + act_bytes(nr));
+    // Where this lane's 16-byte chunk goes in the stage's [nr][256] block (16
+    // rows: two [8][256] halves, one per mma n-tile, laid out alike).  The
     // order puts a consumer lane's B operands of consecutive MMAs in one chunk
     // and the XOR keeps a quarter-warp's reads on distinct bank groups.
     //  nvfp4: lane holds elements 8*lane .. 8*lane+7 (consumer lane c = lane/8
@@ -387,14 +389,16 @@ struct WRegsNv {
     uint32_t s0, s1;           // four e4m3 block scales of rows g and g+8
 };
 
-__device__ __forceinline__ void load_act_nvfp4(const uint8_t* __restrict__ Ab, int lane,
+// Ab: the n-tile's [8][256] activation block; Ai: its eight 2^-s factors.
+__device__ __forceinline__ void load_act_nvfp4(const uint8_t* __restrict__ Ab,
+                                               const uint8_t* __restrict__ Ai, int lane,
                                                ActRegs& a) {
     const int g = lane >> 2, c = lane & 3;
     const uint8_t* ab = Ab + g * 512 + c * 128;
     const int sw = ((g & 1) << 2) | c;
 #pragma unroll
     for (int i = 0; i < 8; ++i) a.bf[i] = lds128(ab + ((i ^ sw) << 4));
-    a.inv = *reinterpret_cast<const float2*>(Ab + kABytes + 8 * c);
+    a.inv = *reinterpret_cast<const float2*>(Ai + 8 * c);
 }
 
 // W: the stage's weight slot; Sr: this stage's 16 bytes inside the scale
@@ -414,8 +418,18 @@ __device__ __forceinline__ void load_w_nvfp4(const uint8_t* __restrict__ W,
     r.s1 = lds32(Sr + 8 * spitch + 4 * c);
 }
 
-__device__ __forceinline__ void compute_nvfp4(const ActRegs& a, const WRegsNv& r,
-                                              float (&acc0)[4], float (&acc1)[4]) {
+// NT n-tiles (8 verify rows each) share every unpacked weight fragment.
+// Accumulator chains per n-tile: two (even and odd MMAs) for one n-tile; one
+// for two n-tiles, whose chains are already independent of each other.
+template <int NT>
+struct Chains {
+    static constexpr int kN = NT == 1 ? 2 : 1;
+};
+
+template <int NT>
+__device__ __forceinline__ void compute_nvfp4(const ActRegs (&a)[NT], const WRegsNv& r,
+                                              float (&acc)[NT][Chains<NT>::kN][4]) {
+    constexpr int C1 = Chains<NT>::kN - 1;
     uint32_t sa0, sb0, sa1, sb1;
     cvt_e4m3x4(r.s0, sa0, sb0);
     cvt_e4m3x4(r.s1, sa1, sb1);
@@ -431,9 +445,16 @@ __device__ __forceinline__ void compute_nvfp4(const ActRegs& a, const WRegsNv& r
         cvt_e2m1x8(wr0[wi], h0, h1, h2, h3);
         cvt_e2m1x8(wr1[wi], q0, q1, q2, q3);
         const uint32_t s0 = sc0[wi >> 1], s1 = sc1[wi >> 1];
-        const uint4& b = a.bf[wi];
-        mma16816(acc0, hmul2(h0, s0), hmul2(q0, s1), hmul2(h1, s0), hmul2(q1, s1), b.x, b.y);
-        mma16816(acc1, hmul2(h2, s0), hmul2(q2, s1), hmul2(h3, s0), hmul2(q3, s1), b.z, b.w);
+        const uint32_t e0 = hmul2(h0, s0), e1 = hmul2(q0, s1), e2 = hmul2(h1, s0),
+                       e3 = hmul2(q1, s1);
+        const uint32_t o0 = hmul2(h2, s0), o1 = hmul2(q2, s1), o2 = hmul2(h3, s0),
+                       o3 = hmul2(q3, s1);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const uint4& b = a[nt].bf[wi];
+            mma16816(acc[nt][0], e0, e1, e2, e3, b.x, b.y);
+            mma16816(acc[nt][C1], o0, o1, o2, o3, b.z, b.w);
+        }
     }
 }
 
@@ -447,14 +468,15 @@ struct WRegsQ4 {
     uint4 d0, d1;           // the eight fp16 scales of rows g and g+8
 };
 
-__device__ __forceinline__ void load_act_q4_0(const uint8_t* __restrict__ Ab, int lane,
+__device__ __forceinline__ void load_act_q4_0(const uint8_t* __restrict__ Ab,
+                                              const uint8_t* __restrict__ Ai, int lane,
                                               ActRegs& a) {
     const int g = lane >> 2, c = lane & 3;
     const uint8_t* ab = Ab + g * 512;
 #pragma unroll
     for (int beta = 0; beta < 8; ++beta)
         a.bf[beta] = lds128(ab + ((((beta << 2) | c) ^ ((g & 1) << 2)) << 4));
-    a.inv = *reinterpret_cast<const float2*>(Ab + kABytes + 8 * c);
+    a.inv = *reinterpret_cast<const float2*>(Ai + 8 * c);
 }
 
 __device__ __forceinline__ void load_w_q4_0(const uint8_t* __restrict__ W,
@@ -472,27 +494,35 @@ __device__ __forceinline__ void load_w_q4_0(const uint8_t* __restrict__ W,
     r.d1 = lds128(Sr + 8 * spitch);
 }
 
-__device__ __forceinline__ void compute_q4_0(const ActRegs& a, const WRegsQ4& r,
-                                             float (&acc0)[4], float (&acc1)[4]) {
+template <int NT>
+__device__ __forceinline__ void compute_q4_0(const ActRegs (&a)[NT], const WRegsQ4& r,
+                                             float (&acc)[NT][Chains<NT>::kN][4]) {
+    constexpr int C1 = Chains<NT>::kN - 1;
     const uint32_t dw0[4] = {r.d0.x, r.d0.y, r.d0.z, r.d0.w};
     const uint32_t dw1[4] = {r.d1.x, r.d1.y, r.d1.z, r.d1.w};
 #pragma unroll
     for (int beta = 0; beta < 8; ++beta) {
         const uint32_t x0 = r.x0[beta], x1 = r.x1[beta];
-        const uint4& b = a.bf[beta];
-        float t[4] = {0.f, 0.f, 0.f, 0.f};
         const uint32_t y0 = x0 >> 8, y1 = x1 >> 8;
-        mma16816(t, q4pair(x0), q4pair(x1), q4pair(y0), q4pair(y1), b.x, b.y);
-        mma16816(t, q4pair_hi(x0), q4pair_hi(x1), q4pair_hi(y0), q4pair_hi(y1), b.z, b.w);
+        const uint32_t l0 = q4pair(x0), l1 = q4pair(x1), l2 = q4pair(y0), l3 = q4pair(y1);
+        const uint32_t u0 = q4pair_hi(x0), u1 = q4pair_hi(x1), u2 = q4pair_hi(y0),
+                       u3 = q4pair_hi(y1);
         const __half2 dh0 = *reinterpret_cast<const __half2*>(&dw0[beta >> 1]);
         const __half2 dh1 = *reinterpret_cast<const __half2*>(&dw1[beta >> 1]);
         const float e0 = (beta & 1) ? __high2float(dh0) : __low2float(dh0);
         const float e1 = (beta & 1) ? __high2float(dh1) : __low2float(dh1);
-        float(&acc)[4] = (beta & 1) ? acc1 : acc0;
-        acc[0] = fmaf(e0, t[0], acc[0]);
-        acc[1] = fmaf(e0, t[1], acc[1]);
-        acc[2] = fmaf(e1, t[2], acc[2]);
-        acc[3] = fmaf(e1, t[3], acc[3]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const uint4& b = a[nt].bf[beta];
+            float t[4] = {0.f, 0.f, 0.f, 0.f};
+            mma16816(t, l0, l1, l2, l3, b.x, b.y);
+            mma16816(t, u0, u1, u2, u3, b.z, b.w);
+            float(&ac)[4] = (beta & 1) ? acc[nt][C1] : acc[nt][0];
+            ac[0] = fmaf(e0, t[0], ac[0]);
+            ac[1] = fmaf(e0, t[1], ac[1]);
+            ac[2] = fmaf(e1, t[2], ac[2]);
+            ac[3] = fmaf(e1, t[3], ac[3]);
+        }
     }
 }
 
@@ -566,9 +596,9 @@ __device__ void argmax_finish(const GemmParams& p, int lane) {
         if (p.row_argmax != nullptr) p.row_argmax[lane] = am;
     }
     if (p.greedy_B > 0) {
-        int32_t g[kMaxRows];
+        int32_t g[kMaxVerifyRows];
 #pragma unroll
-        for (int i = 0; i < kMaxRows; ++i) g[i] = __shfl_sync(0xffffffffu, am, i);
+        for (int i = 0; i < kMaxVerifyRows; ++i) g[i] = __shfl_sync(0xffffffffu, am, i);
         const int Kd = p.greedy_Kd, b = lane;
         if (b < p.greedy_B) {
             const int32_t* d = p.drafts + b * Kd;
@@ -600,23 +630,27 @@ __device__ __forceinline__ void grid_dependents_launch() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-template <int FMT>
+// NR verify rows per activation block: 8 (one mma n-tile; dense or MoE) or
+// 16 (two n-tiles over the same unpacked weights; dense calls of 9..16 rows).
+template <int FMT, int NR>
 __global__ void __launch_bounds__(kGemmThreads, 2)
     gemm_w4_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
                    const GemmParams p) {
+    using Sh = GemmShape<NR>;
+    constexpr int NT = Sh::kNT;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSmemBar);
-    uint64_t* empty = full + kStages;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Sh::kSmemBar);
+    uint64_t* empty = full + Sh::kStages;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + Sh::kStages);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // The next call's kernels may become resident now: they touch nothing
     // this grid uses before it has finished, and prefetch only weights.
     grid_dependents_launch();
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < Sh::kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps);
         }
@@ -663,7 +697,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         // this CTA's range) loads one box into the next scale slot.  Before
         // reusing a slot, every stage that read the previous box must have
         // been released; the stage ring implies it unless that was less than
-        // kStages units ago, in which case wait for that release explicitly.
+        // Sh::kStages units ago, in which case wait for that release explicitly.
         uint32_t n_sbox = 0;
         static_assert(kSSlots == 2, "two scale slots");
         uint32_t slot_last0 = 0xffffffffu, slot_last1 = 0xffffffffu;  // last unit per slot
@@ -699,18 +733,18 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         // with_act: also copy the stage's activation block now (it is ready).
         auto issue = [&](const Cursor& c, bool first, uint32_t it_u, bool with_act,
                          bool may_wait) -> int {
-            const int s = it_u % kStages;
+            const int s = it_u % Sh::kStages;
             const bool new_box = first || (c.st & smask) == 0;
             // the activation copy of a unit issued before the prep wait is
             // added later, but its bytes are expected here already
-            uint32_t bytes = kWBytes + kAStride;
+            uint32_t bytes = kWBytes + Sh::kAStride;
             int sslot = (n_sbox + kSSlots - 1) % kSSlots;
             if (new_box) {
                 sslot = n_sbox % kSSlots;
                 const uint32_t last = sslot ? slot_last1 : slot_last0;
-                if (last != 0xffffffffu && it_u - last < static_cast<uint32_t>(kStages)) {
+                if (last != 0xffffffffu && it_u - last < static_cast<uint32_t>(Sh::kStages)) {
                     if (!may_wait) return -1;
-                    if (!mbar_wait_bounded(&empty[last % kStages], (last / kStages) & 1, p.wait_ns,
+                    if (!mbar_wait_bounded(&empty[last % Sh::kStages], (last / Sh::kStages) & 1, p.wait_ns,
                                            abort_flag))
                         return 0;
                 }
@@ -723,22 +757,22 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             tma_load_2d(smem + s * kWBytes, &tmW, c.st * (kStageK / 2), c.row0, &full[s], pol_w);
             if (new_box) {  // box start: this stage, moved back to fit inside the row
                 const int st_box = c.st < T - sg_n ? c.st : T - sg_n;
-                tma_load_2d(smem + kSmemS + sslot * kSSlotBytes, &tmS, st_box * 16, c.row0,
+                tma_load_2d(smem + Sh::kSmemS + sslot * kSSlotBytes, &tmS, st_box * 16, c.row0,
                             &full[s], pol_s);
             }
             if (with_act)
-                bulk_load(smem + kSmemA + s * kAStride,
-                          p.act + (static_cast<size_t>(c.sg) * T + c.st) * kAStride, kAStride,
+                bulk_load(smem + Sh::kSmemA + s * Sh::kAStride,
+                          p.act + (static_cast<size_t>(c.sg) * T + c.st) * Sh::kAStride, Sh::kAStride,
                           &full[s], pol_a);
             return 1;
         };
         // The weights and scales do not depend on the activation prep: start
-        // streaming up to kStages units before waiting for it (stopping early
+        // streaming up to Sh::kStages units before waiting for it (stopping early
         // rather than waiting on consumers, who need the activations first).
         const Cursor c0 = cursor_at(u_begin);
         Cursor cur = c0;
         const unsigned long long n_units = u_end - u_begin;
-        while (it < n_units && it < static_cast<uint32_t>(kStages)) {
+        while (it < n_units && it < static_cast<uint32_t>(Sh::kStages)) {
             if (issue(cur, it == 0, it, false, false) != 1) break;
             ++it;
             advance(cur);
@@ -748,14 +782,14 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         {
             Cursor a = c0;
             for (uint32_t j = 0; j < n_pre; ++j, advance(a))
-                bulk_load(smem + kSmemA + j * kAStride,
-                          p.act + (static_cast<size_t>(a.sg) * T + a.st) * kAStride, kAStride,
+                bulk_load(smem + Sh::kSmemA + j * Sh::kAStride,
+                          p.act + (static_cast<size_t>(a.sg) * T + a.st) * Sh::kAStride, Sh::kAStride,
                           &full[j], pol_a);
         }
         for (; it < n_units; ++it, advance(cur)) {
-            const int s = it % kStages;
-            if ((it >= static_cast<uint32_t>(kStages) &&
-                 !mbar_wait_bounded(&empty[s], ((it / kStages) - 1) & 1, p.wait_ns,
+            const int s = it % Sh::kStages;
+            if ((it >= static_cast<uint32_t>(Sh::kStages) &&
+                 !mbar_wait_bounded(&empty[s], ((it / Sh::kStages) - 1) & 1, p.wait_ns,
                                     abort_flag)) ||
                 issue(cur, it == 0, it, true, true) != 1) {
                 ok = false;
@@ -768,8 +802,8 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         }
         // Drain: every issued copy must land before this CTA may exit.
         const uint64_t drain_ns = p.wait_ns > 2000000000ull ? p.wait_ns : 2000000000ull;
-        for (uint32_t j = (it > (uint32_t)kStages ? it - kStages : 0u); j < it; ++j)
-            mbar_wait_bounded(&full[j % kStages], (j / kStages) & 1, drain_ns, nullptr);
+        for (uint32_t j = (it > (uint32_t)Sh::kStages ? it - Sh::kStages : 0u); j < it; ++j)
+            mbar_wait_bounded(&full[j % Sh::kStages], (j / Sh::kStages) & 1, drain_ns, nullptr);
         if (!cluster_mode) return;
         goto combine;
     }
@@ -782,14 +816,14 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     uint32_t it = 0;
     uint32_t n_sbox = 0;  // scale boxes seen, in the producer's order
     // scale slot of the current box, offset back by the box's first stage
-    const uint8_t* s_base = smem + kSmemS;
+    const uint8_t* s_base = smem + Sh::kSmemS;
     const int sg_n = p.sgroup;
     const int spitch = 16 * sg_n;
     const int smask = sg_n == kScaleGroup ? kScaleGroup - 1 : 0x7fffffff;
     const unsigned long long my_first_tile = u_begin / T;
     // fused argmax: this warp's running key of verify row lane / 4 (held in
     // the lanes with lane % 4 == 0), published once when the warp is done
-    unsigned long long am_run = 0ull;
+    unsigned long long am_run[NT] = {};
     for (unsigned long long u = u_begin; u < u_end;) {
         const unsigned long long tg = u / T;
         const int st0 = static_cast<int>(u % T);
@@ -797,10 +831,10 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         const int st_end = (left < static_cast<unsigned long long>(T - st0))
                                ? st0 + static_cast<int>(left)
                                : T;
-        float tot[kRowBlocks][4] = {};
+        float tot[kRowBlocks][NT][4] = {};
         for (int st = st0; st < st_end; ++st, ++it) {
-            const int s = it % kStages;
-            if (!mbar_wait_bounded(&full[s], (it / kStages) & 1, p.wait_ns, abort_flag)) {
+            const int s = it % Sh::kStages;
+            if (!mbar_wait_bounded(&full[s], (it / Sh::kStages) & 1, p.wait_ns, abort_flag)) {
                 if (lane == 0) atomicOr(p.status, kStatusTimeout);
                 *abort_flag = 1;
                 if (cluster_mode) goto combine;
@@ -809,16 +843,19 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             if (it == 0 || (st & smask) == 0) {
                 ++n_sbox;
                 const int sbox_st = st < T - sg_n ? st : T - sg_n;
-                s_base = smem + kSmemS + ((n_sbox - 1) % kSSlots) * kSSlotBytes - sbox_st * 16;
+                s_base = smem + Sh::kSmemS + ((n_sbox - 1) % kSSlots) * kSSlotBytes - sbox_st * 16;
             }
             const uint8_t* Ws = smem + s * kWBytes;
             const uint8_t* Ss = s_base + st * 16 + (wrow + g) * spitch;
-            const uint8_t* As = smem + kSmemA + s * kAStride;
-            float acc[kRowBlocks][2][4] = {};
-            ActRegs ar;
+            const uint8_t* As = smem + Sh::kSmemA + s * Sh::kAStride;
+            constexpr int NC = Chains<NT>::kN;
+            float acc[kRowBlocks][NT][NC][4] = {};
+            ActRegs ar[NT];
             if (FMT == 1) {
                 WRegsNv wr[kRowBlocks];
-                load_act_nvfp4(As, lane, ar);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    load_act_nvfp4(As + nt * act_bytes(8), As + Sh::kABytes + nt * 32, lane, ar[nt]);
 #pragma unroll
                 for (int rb = 0; rb < kRowBlocks; ++rb)
                     load_w_nvfp4(Ws, Ss + rb * 16 * spitch, spitch, wrow + rb * 16 + g, lane,
@@ -827,10 +864,12 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                 if (lane == 0) mbar_arrive(&empty[s]);  // the producer may refill it
 #pragma unroll
                 for (int rb = 0; rb < kRowBlocks; ++rb)
-                    compute_nvfp4(ar, wr[rb], acc[rb][0], acc[rb][1]);
+                    compute_nvfp4<NT>(ar, wr[rb], acc[rb]);
             } else {
                 WRegsQ4 wr[kRowBlocks];
-                load_act_q4_0(As, lane, ar);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    load_act_q4_0(As + nt * act_bytes(8), As + Sh::kABytes + nt * 32, lane, ar[nt]);
 #pragma unroll
                 for (int rb = 0; rb < kRowBlocks; ++rb)
                     load_w_q4_0(Ws, Ss + rb * 16 * spitch, spitch, wrow + rb * 16 + g, lane,
@@ -839,74 +878,99 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                 if (lane == 0) mbar_arrive(&empty[s]);
 #pragma unroll
                 for (int rb = 0; rb < kRowBlocks; ++rb)
-                    compute_q4_0(ar, wr[rb], acc[rb][0], acc[rb][1]);
+                    compute_q4_0<NT>(ar, wr[rb], acc[rb]);
             }
             // this stage's activations were scaled by 2^s per verify row
 #pragma unroll
-            for (int rb = 0; rb < kRowBlocks; ++rb) {
-                tot[rb][0] = fmaf(ar.inv.x, acc[rb][0][0] + acc[rb][1][0], tot[rb][0]);
-                tot[rb][1] = fmaf(ar.inv.y, acc[rb][0][1] + acc[rb][1][1], tot[rb][1]);
-                tot[rb][2] = fmaf(ar.inv.x, acc[rb][0][2] + acc[rb][1][2], tot[rb][2]);
-                tot[rb][3] = fmaf(ar.inv.y, acc[rb][0][3] + acc[rb][1][3], tot[rb][3]);
-            }
+            for (int rb = 0; rb < kRowBlocks; ++rb)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const float2 iv = ar[nt].inv;
+                    float(&t)[4] = tot[rb][nt];
+                    const float(&a0)[4] = acc[rb][nt][0];
+                    const float(&a1)[4] = acc[rb][nt][NC - 1];
+                    if (NC == 2) {
+                        t[0] = fmaf(iv.x, a0[0] + a1[0], t[0]);
+                        t[1] = fmaf(iv.y, a0[1] + a1[1], t[1]);
+                        t[2] = fmaf(iv.x, a0[2] + a1[2], t[2]);
+                        t[3] = fmaf(iv.y, a0[3] + a1[3], t[3]);
+                    } else {
+                        t[0] = fmaf(iv.x, a0[0], t[0]);
+                        t[1] = fmaf(iv.y, a0[1], t[1]);
+                        t[2] = fmaf(iv.x, a0[2], t[2]);
+                        t[3] = fmaf(iv.y, a0[3], t[3]);
+                    }
+                }
         }
         u += static_cast<unsigned long long>(st_end - st0);
 
         // ------------------------------------------------------ epilogue
-        // Lane (g, c) holds, per row block rb, rows r = wrow + 16rb + g (+8
-        // for q & 2) and verify rows 2c + (q & 1).
+        // Lane (g, c) holds, per row block rb and n-tile nt, rows
+        // r = wrow + 16rb + g (+8 for q & 2) and verify rows 8nt + 2c + (q & 1).
         const int sg = static_cast<int>(tg / n_tiles), tile = static_cast<int>(tg % n_tiles);
         const int count = p.dense_M > 0 ? p.dense_M : p.seg->count[sg];
-        float v[kRowBlocks][4];
+        // output row of verify row tok (16-row blocks are dense-only)
+        auto dest_of = [&](int tok) {
+            return (NR > kMaxRows || p.dense_M > 0) ? tok : p.seg->dest[sg][tok];
+        };
+        float v[kRowBlocks][NT][4];
 #pragma unroll
         for (int rb = 0; rb < kRowBlocks; ++rb)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) v[rb][q] = tot[rb][q] * p.tensor_scale;
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) v[rb][nt][q] = tot[rb][nt][q] * p.tensor_scale;
         const int n0 = tile * kTileRows;
         const bool whole = (st0 == 0 && st_end == T);
         if (whole) {
-            unsigned long long k0 = 0ull, k1 = 0ull;  // argmax keys of tokens 2c, 2c+1
 #pragma unroll
-            for (int rb = 0; rb < kRowBlocks; ++rb) {
+            for (int nt = 0; nt < NT; ++nt) {
+                // argmax keys of verify rows 8nt + 2c and 8nt + 2c + 1
+                unsigned long long k0 = 0ull, k1 = 0ull;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int tok = 2 * c + (q & 1);
-                    const int n = n0 + wrow + rb * 16 + g + ((q & 2) ? 8 : 0);
-                    if (n < p.N) {
-                        if (tok < count && p.out != nullptr) {
-                            const int dest = p.dense_M > 0 ? tok : p.seg->dest[sg][tok];
-                            p.out[static_cast<size_t>(dest) * p.ldo + n] = v[rb][q];
+                for (int rb = 0; rb < kRowBlocks; ++rb) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int tok = 8 * nt + 2 * c + (q & 1);
+                        const int n = n0 + wrow + rb * 16 + g + ((q & 2) ? 8 : 0);
+                        if (n < p.N) {
+                            if (tok < count && p.out != nullptr)
+                                p.out[static_cast<size_t>(dest_of(tok)) * p.ldo + n] = v[rb][nt][q];
+                            const unsigned long long k =
+                                am_key(v[rb][nt][q], static_cast<uint32_t>(n));
+                            if (q & 1) k1 = umax64(k1, k);
+                            else k0 = umax64(k0, k);
                         }
-                        const unsigned long long k = am_key(v[rb][q], static_cast<uint32_t>(n));
-                        if (q & 1) k1 = umax64(k1, k);
-                        else k0 = umax64(k0, k);
                     }
                 }
-            }
-            if (p.argmax_M > 0) {
+                if (p.argmax_M > 0) {
 #pragma unroll
-                for (int o = 4; o < 32; o <<= 1) {
-                    k0 = umax64(k0, __shfl_xor_sync(0xffffffffu, k0, o));
-                    k1 = umax64(k1, __shfl_xor_sync(0xffffffffu, k1, o));
+                    for (int o = 4; o < 32; o <<= 1) {
+                        k0 = umax64(k0, __shfl_xor_sync(0xffffffffu, k0, o));
+                        k1 = umax64(k1, __shfl_xor_sync(0xffffffffu, k1, o));
+                    }
+                    // lane c (< 4) holds rows 2c and 2c + 1 of the n-tile;
+                    // row t goes to lanes 4t .. 4t + 3
+                    const int t = lane >> 2;
+                    const unsigned long long a = __shfl_sync(0xffffffffu, k0, t >> 1);
+                    const unsigned long long b = __shfl_sync(0xffffffffu, k1, t >> 1);
+                    am_run[nt] = umax64(am_run[nt], (t & 1) ? b : a);
                 }
-                // lane c (< 4) holds rows 2c and 2c + 1; row t goes to lane 4t
-                const int t = lane >> 2;
-                const unsigned long long a = __shfl_sync(0xffffffffu, k0, t >> 1);
-                const unsigned long long b = __shfl_sync(0xffffffffu, k1, t >> 1);
-                am_run = umax64(am_run, (t & 1) ? b : a);
             }
             continue;
         }
         if (cluster_mode) {  // leave this part's slice in shared memory
-            float* part = reinterpret_cast<float*>(smem + kSmemPart);
+            float* part = reinterpret_cast<float*>(smem + Sh::kSmemPart);
 #pragma unroll
             for (int rb = 0; rb < kRowBlocks; ++rb)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int tok = 2 * c + (q & 1);
-                    const int r = wrow + rb * 16 + g + ((q & 2) ? 8 : 0);
-                    part[tok * kTileRows + r] = v[rb][q];
-                }
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int tok = 8 * nt + 2 * c + (q & 1);
+                        const int r = wrow + rb * 16 + g + ((q & 2) ? 8 : 0);
+                        part[tok * kTileRows + r] = v[rb][nt][q];
+                    }
             continue;
         }
         // Partial tile: publish this warp's 32-row slice; the last of the
@@ -916,15 +980,17 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         const uint32_t n_contrib = static_cast<uint32_t>(i_hi - i_lo + 1);
         const unsigned long long my_slot =
             2ull * blockIdx.x + ((my_first_tile == tg) ? 0ull : 1ull);
-        float* part = p.partials + my_slot * kPartialFloats;
+        float* part = p.partials + my_slot * Sh::kPartialFloats;
 #pragma unroll
         for (int rb = 0; rb < kRowBlocks; ++rb)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int tok = 2 * c + (q & 1);
-                const int r = wrow + rb * 16 + g + ((q & 2) ? 8 : 0);
-                __stcg(&part[tok * kTileRows + r], v[rb][q]);
-            }
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int tok = 8 * nt + 2 * c + (q & 1);
+                    const int r = wrow + rb * 16 + g + ((q & 2) ? 8 : 0);
+                    __stcg(&part[tok * kTileRows + r], v[rb][nt][q]);
+                }
         // The warp barrier orders every lane's partial stores before lane 0's
         // release; the last arriver's acquire orders the reads after them.
         __syncwarp();
@@ -936,58 +1002,67 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         // slot is its "first tile" slot; only the first may end in it instead.
         const unsigned long long slot_lo =
             2ull * i_lo + ((R.start(i_lo) / T == tg) ? 0ull : 1ull);
-        // lane: verify row tok, rows rr .. rr+3 and rr+16 .. rr+19 of the slice
-        const int tok = lane >> 2;
+        // lane: verify row 8nt + tok of each n-tile, rows rr .. rr+3 and
+        // rr+16 .. rr+19 of the slice
         const int rr = wrow + 4 * (lane & 3);
-        const size_t off = static_cast<size_t>(tok) * kTileRows + rr;
         auto slot_of = [&](unsigned long long i) { return i == i_lo ? slot_lo : 2ull * i; };
-        auto ld4 = [&](unsigned long long i, int h) {
-            return __ldcg(reinterpret_cast<const float4*>(p.partials + slot_of(i) * kPartialFloats +
-                                                          off + 16 * h));
-        };
-        float4 sa = make_float4(0.f, 0.f, 0.f, 0.f), sb = sa;
-        // up to kFinishBatch contributors' loads in flight, then summed in order
-        for (unsigned long long i0 = i_lo; i0 <= i_hi; i0 += kFinishBatch) {
-            float4 xa[kFinishBatch], xb[kFinishBatch];
 #pragma unroll
-            for (int j = 0; j < kFinishBatch; ++j) {  // past the end: reload the last
-                const unsigned long long ij = i0 + j <= i_hi ? i0 + j : i_hi;
-                xa[j] = ld4(ij, 0);
-                xb[j] = ld4(ij, 1);
-            }
+        for (int nt = 0; nt < NT; ++nt) {
+            const int tok = 8 * nt + (lane >> 2);
+            const size_t off = static_cast<size_t>(tok) * kTileRows + rr;
+            auto ld4 = [&](unsigned long long i, int h) {
+                return __ldcg(reinterpret_cast<const float4*>(
+                    p.partials + slot_of(i) * Sh::kPartialFloats + off + 16 * h));
+            };
+            float4 sa = make_float4(0.f, 0.f, 0.f, 0.f), sb = sa;
+            // up to kFinishBatch contributors' loads in flight, then summed in order
+            for (unsigned long long i0 = i_lo; i0 <= i_hi; i0 += kFinishBatch) {
+                float4 xa[kFinishBatch], xb[kFinishBatch];
 #pragma unroll
-            for (int j = 0; j < kFinishBatch; ++j) {
-                if (i0 + j <= i_hi) {
-                    sa.x += xa[j].x; sa.y += xa[j].y; sa.z += xa[j].z; sa.w += xa[j].w;
-                    sb.x += xb[j].x; sb.y += xb[j].y; sb.z += xb[j].z; sb.w += xb[j].w;
+                for (int j = 0; j < kFinishBatch; ++j) {  // past the end: reload the last
+                    const unsigned long long ij = i0 + j <= i_hi ? i0 + j : i_hi;
+                    xa[j] = ld4(ij, 0);
+                    xb[j] = ld4(ij, 1);
+                }
+#pragma unroll
+                for (int j = 0; j < kFinishBatch; ++j) {
+                    if (i0 + j <= i_hi) {
+                        sa.x += xa[j].x; sa.y += xa[j].y; sa.z += xa[j].z; sa.w += xa[j].w;
+                        sb.x += xb[j].x; sb.y += xb[j].y; sb.z += xb[j].z; sb.w += xb[j].w;
+                    }
                 }
             }
-        }
-        const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
-        unsigned long long kb = 0ull;
-        if (tok < count) {
-            const int dest = p.dense_M > 0 ? tok : p.seg->dest[sg][tok];
-            float* orow = p.out != nullptr ? p.out + static_cast<size_t>(dest) * p.ldo : nullptr;
+            const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+            unsigned long long kb = 0ull;
+            if (tok < count) {
+                float* orow =
+                    p.out != nullptr ? p.out + static_cast<size_t>(dest_of(tok)) * p.ldo : nullptr;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int n = n0 + rr + (j & 3) + ((j & 4) ? 16 : 0);
-                if (n < p.N) {
-                    if (p.out != nullptr) orow[n] = sv[j];
-                    kb = umax64(kb, am_key(sv[j], static_cast<uint32_t>(n)));
+                for (int j = 0; j < 8; ++j) {
+                    const int n = n0 + rr + (j & 3) + ((j & 4) ? 16 : 0);
+                    if (n < p.N) {
+                        if (p.out != nullptr) orow[n] = sv[j];
+                        kb = umax64(kb, am_key(sv[j], static_cast<uint32_t>(n)));
+                    }
                 }
             }
-        }
-        if (p.argmax_M > 0) {
-            kb = umax64(kb, __shfl_xor_sync(0xffffffffu, kb, 1));
-            kb = umax64(kb, __shfl_xor_sync(0xffffffffu, kb, 2));
-            am_run = umax64(am_run, kb);  // lane 4 tok holds row tok
+            if (p.argmax_M > 0) {
+                kb = umax64(kb, __shfl_xor_sync(0xffffffffu, kb, 1));
+                kb = umax64(kb, __shfl_xor_sync(0xffffffffu, kb, 2));
+                am_run[nt] = umax64(am_run[nt], kb);  // lanes 4t .. 4t+3 hold row 8nt + t
+            }
         }
     }
     if (p.argmax_M > 0) {
         // one 64-bit max per verify row and warp, then a ticket: the last of
         // the grid's consumer warps reads the maxima out
         const int t = lane >> 2;
-        if ((lane & 3) == 0 && t < p.argmax_M && am_run) atomicMax(&p.am_key[t], am_run);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int row = 8 * nt + t;
+            if ((lane & 3) == 0 && row < p.argmax_M && am_run[nt])
+                atomicMax(&p.am_key[row], am_run[nt]);
+        }
         __syncwarp();
         uint32_t o2 = 0;
         if (lane == 0) o2 = atom_add_acq_rel_gpu(p.am_cnt, 1u);
@@ -1014,11 +1089,11 @@ combine:
                 parts[r] = nullptr;
                 if (r < S) {
                     aborted |= *cl.map_shared_rank(const_cast<int*>(abort_flag), r);
-                    parts[r] = cl.map_shared_rank(reinterpret_cast<float*>(smem + kSmemPart), r);
+                    parts[r] = cl.map_shared_rank(reinterpret_cast<float*>(smem + Sh::kSmemPart), r);
                 }
             }
             const int n0 = static_cast<int>(blockIdx.x / S) * kTileRows;
-            constexpr int kPairs = kMaxRows * kTileRows / 2;  // the tile as float2
+            constexpr int kPairs = NR * kTileRows / 2;  // the tile as float2
             for (int e = static_cast<int>(cl.block_rank()) * kGemmConsumers + threadIdx.x;
                  e < kPairs; e += S * kGemmConsumers) {
                 const int tok = e / (kTileRows / 2), r0 = (e % (kTileRows / 2)) * 2;
@@ -1081,14 +1156,15 @@ __global__ void q4_0_split_kernel(const uint8_t* __restrict__ blocks, int N, int
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_prep_act(const uint16_t* A, int lda, int K, int fmt, int dense_M,
                             int rows_are_pairs, int topk, int n_seg_grid, const GemmWorkspace& ws,
-                            int n_counters, cudaStream_t s, const int32_t* ids, int E,
+                            int n_counters, cudaStream_t s, int nr, const int32_t* ids, int E,
                             uint32_t* status, float* out_zero, int ldo, int N) {
+    if ((nr != 8 && nr != 16) || (nr == 16 && dense_M <= 0)) return cudaErrorInvalidValue;
     const int T = K / kStageK;
     const int vec_ok = ((reinterpret_cast<uintptr_t>(A) & 15u) == 0 && lda % 8 == 0) ? 1 : 0;
     // a programmatic dependent of whatever kernel precedes it on the stream
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(n_seg_grid * T);
-    cfg.blockDim = dim3(256);
+    cfg.blockDim = dim3(32 * nr);  // one warp per verify row
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -1096,26 +1172,27 @@ cudaError_t launch_prep_act(const uint16_t* A, int lda, int K, int fmt, int dens
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prep_act_kernel, A, lda, vec_ok, K, fmt, dense_M,
+    return cudaLaunchKernelEx(&cfg, prep_act_kernel, A, lda, vec_ok, K, fmt, nr, dense_M,
                               rows_are_pairs, topk, ws.seg, ws.act, ws.tile_cnt, n_counters,
                               ws.am_key, ws.am_cnt, ids, dense_M > 0 ? 0 : n_seg_grid, E, status,
                               out_zero, ldo, N);
 }
 
-template <int FMT>
+template <int FMT, int NR>
 static cudaError_t launch_gemm_t(const CUtensorMap& tmW, const CUtensorMap& tmS,
                                  const GemmParams& p, int grid, int cluster, cudaStream_t s) {
+    constexpr int kSmem = GemmShape<NR>::kSmem;
     static bool attr_done = false;
     if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_w4_kernel<FMT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+        cudaError_t e = cudaFuncSetAttribute(gemm_w4_kernel<FMT, NR>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kGemmThreads);
-    cfg.dynamicSmemBytes = kGemmSmem;
+    cfg.dynamicSmemBytes = kSmem;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1129,27 +1206,33 @@ static cudaError_t launch_gemm_t(const CUtensorMap& tmW, const CUtensorMap& tmS,
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
     }
-    return cudaLaunchKernelEx(&cfg, gemm_w4_kernel<FMT>, tmW, tmS, p);
+    return cudaLaunchKernelEx(&cfg, gemm_w4_kernel<FMT, NR>, tmW, tmS, p);
 }
 
-cudaError_t launch_gemm(int fmt, const CUtensorMap& tmW, const CUtensorMap& tmS,
+cudaError_t launch_gemm(int fmt, int nr, const CUtensorMap& tmW, const CUtensorMap& tmS,
                         const GemmParams& p, int grid, int cluster, cudaStream_t s) {
-    return fmt == 1 ? launch_gemm_t<1>(tmW, tmS, p, grid, cluster, s)
-                    : launch_gemm_t<2>(tmW, tmS, p, grid, cluster, s);
+    if (nr == 16) {
+        if (p.dense_M <= 0) return cudaErrorInvalidValue;  // 16-row blocks are dense-only
+        return fmt == 1 ? launch_gemm_t<1, 16>(tmW, tmS, p, grid, cluster, s)
+                        : launch_gemm_t<2, 16>(tmW, tmS, p, grid, cluster, s);
+    }
+    return fmt == 1 ? launch_gemm_t<1, 8>(tmW, tmS, p, grid, cluster, s)
+                    : launch_gemm_t<2, 8>(tmW, tmS, p, grid, cluster, s);
 }
 
-int gemm_blocks_per_sm(int fmt) {
+template <int FMT, int NR>
+static int blocks_per_sm_t() {
+    constexpr int kSmem = GemmShape<NR>::kSmem;
     int n = 0;
-    if (fmt == 1) {
-        cudaFuncSetAttribute(gemm_w4_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kGemmSmem);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemm_w4_kernel<1>, kGemmThreads, kGemmSmem);
-    } else {
-        cudaFuncSetAttribute(gemm_w4_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kGemmSmem);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemm_w4_kernel<2>, kGemmThreads, kGemmSmem);
-    }
+    cudaFuncSetAttribute(gemm_w4_kernel<FMT, NR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         kSmem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemm_w4_kernel<FMT, NR>, kGemmThreads, kSmem);
     return n > 0 ? n : 1;
+}
+
+int gemm_blocks_per_sm(int fmt, int nr) {
+    if (nr == 16) return fmt == 1 ? blocks_per_sm_t<1, 16>() : blocks_per_sm_t<2, 16>();
+    return fmt == 1 ? blocks_per_sm_t<1, 8>() : blocks_per_sm_t<2, 8>();
 }
 
 cudaError_t launch_combine(const float* pair_out, const float* gates, const int32_t* ids,

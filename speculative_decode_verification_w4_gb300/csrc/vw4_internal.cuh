@@ -9,11 +9,11 @@
 
 namespace vw4 {
 
-constexpr int kMaxRows = 8;        // verify rows per segment (mma n = 8)
+constexpr int kMaxRows = 8;        // rows of one mma n-tile; verify rows per MoE segment
+constexpr int kMaxVerifyRows = 16; // dense verify rows per call: two n-tiles
 constexpr int kMaxSeg = 64;        // routed (token, expert) pairs per call
 constexpr int kTileRows = 128;     // weight rows per tile
 constexpr int kStageK = 256;       // k elements per pipeline stage
-constexpr int kStages = 4;         // pipeline depth
 constexpr int kMinUnitsPerCta = 4; // tile-aligned split-K: at least this many stages per part
 constexpr int kMaxSplit = 6;       // tile-aligned split-K: at most this many parts
 constexpr int kMaxClusterSplit = 6; // parts combined as one cluster (larger ones place poorly)
@@ -24,8 +24,6 @@ constexpr int kGemmThreads = (kConsumerWarps + 1) * 32;
 constexpr int kGemmConsumers = kConsumerWarps * 32;
 static_assert(kRowBlocks == 2, "the split-tile finish assumes two row blocks per warp");
 constexpr int kWBytes = kTileRows * (kStageK / 2);     // 16384: packed nibbles
-constexpr int kABytes = kMaxRows * kStageK * 2;        // 4096: fp16 activations
-constexpr int kAStride = kABytes + kMaxRows * 4;       // + the 8 rows' 2^-s: 4128
 // Scales travel in boxes of 128 rows x (16 * g) bytes that cover g = min(4, T)
 // consecutive stages (16 bytes per row per stage), into a ring of 2 slots: one
 // request of two full sectors per row instead of four half-sector requests.
@@ -36,14 +34,36 @@ static_assert((kScaleGroup & (kScaleGroup - 1)) == 0, "scale group must be a pow
 constexpr int kSBoxBytes = 16 * kScaleGroup;           // 64 (slot row pitch)
 constexpr int kSSlotBytes = kTileRows * kSBoxBytes;    // 8192
 constexpr int kSSlots = 2;
-// shared memory: [W x kStages][S x kSSlots][A x kStages][barriers]; every W
-// slot is 1024-byte aligned (128-byte swizzle)
-constexpr int kSmemS = kStages * kWBytes;
-constexpr int kSmemA = kSmemS + kSSlots * kSSlotBytes;
-constexpr int kSmemBar = kSmemA + kStages * kAStride;
-constexpr int kSmemPart = kSmemBar + 256;                // cluster mode: this CTA's partial tile
-constexpr int kGemmSmem = kSmemPart + kMaxRows * kTileRows * 4 + 1024 /*align*/;
-constexpr int kPartialFloats = kMaxRows * kTileRows;   // one partial tile: [8][128]
+
+// Activation block of one (segment, stage) for NR verify rows: fp16 [NR][256]
+// (scaled, bank-swizzled), then float 2^-s [NR].
+__host__ __device__ constexpr int act_bytes(int nr) { return nr * kStageK * 2; }
+__host__ __device__ constexpr int act_stride(int nr) { return act_bytes(nr) + nr * 4; }
+
+// The GEMM's shapes for NR verify rows (8: one mma n-tile; 16: two n-tiles
+// sharing every unpacked weight fragment).  Shared memory:
+// [W x kStages][S x kSSlots][A x kStages][barriers][partial tile]; every W slot
+// is 1024-byte aligned (128-byte swizzle).  Sixteen rows double the
+// activation slots and the partial tile, so that ring is one stage shorter
+// to keep two CTAs per SM.
+template <int NR>
+struct GemmShape {
+    static_assert(NR == 8 || NR == 16, "8 or 16 verify rows");
+    static constexpr int kNT = NR / 8;
+    static constexpr int kStages = NR == 8 ? 4 : 3;
+    static constexpr int kABytes = act_bytes(NR);     // 4096 / 8192
+    static constexpr int kAStride = act_stride(NR);   // 4128 / 8256
+    static constexpr int kSmemS = kStages * kWBytes;
+    static constexpr int kSmemA = kSmemS + kSSlots * kSSlotBytes;
+    static constexpr int kSmemBar = kSmemA + kStages * kAStride;
+    static constexpr int kSmemPart = kSmemBar + 256;  // cluster mode: this CTA's partial tile
+    static constexpr int kPartialFloats = NR * kTileRows;
+    static constexpr int kSmem = kSmemPart + kPartialFloats * 4 + 1024 /*align*/;
+    static_assert(kAStride % 16 == 0 && kSmemA % 16 == 0, "bulk copies need 16-byte alignment");
+    static_assert(kSmemBar % 8 == 0 && kSmemPart % 16 == 0, "barrier / partial alignment");
+    static_assert(kSmem <= 113 * 1024, "two CTAs per SM");
+};
+inline int gemm_rows_for(int M) { return M <= kMaxRows ? 8 : 16; }
 
 // A "segment" is the set of verify rows that share one weight matrix: the
 // whole batch for a dense layer, or the pairs routed to one expert.
@@ -57,11 +77,10 @@ struct SegTable {
 
 struct GemmWorkspace {
     SegTable* seg;
-    uint8_t* act;                // [seg][T] blocks of kAStride bytes: fp16 [8][256]
-                                 // (scaled, bank-swizzled) then float 2^-s [8]
-    float* partials;             // [2 * grid][8][128] stream-K partial tiles
+    uint8_t* act;                // [seg][T] blocks of act_stride(nr) bytes
+    float* partials;             // [2 * grid][nr][128] stream-K partial tiles
     uint32_t* tile_cnt;          // [seg * n_tiles * kConsumerWarps] slice arrival tickets
-    unsigned long long* am_key;  // [8] packed (value, ~index) running maxima
+    unsigned long long* am_key;  // [16] packed (value, ~index) running maxima
     uint32_t* am_cnt;            // [1] quarter-tile tickets of the argmax
     float* pair_out;             // [pairs][N] MoE pair rows before the combine
     size_t bytes;
@@ -98,23 +117,25 @@ struct GemmParams {
     int32_t* len;
 };
 
-// Lays the GEMM/MoE workspace out from `base` (nullptr: size only).
+// Lays the GEMM/MoE workspace out from `base` (nullptr: size only) for
+// blocks of nr (8 or 16) verify rows.
 GemmWorkspace gemm_workspace_layout(void* base, int n_seg_max, int N, int K, int grid,
-                                    int pair_rows);
+                                    int pair_rows, int nr);
 
 // Kernel launchers (gemm_w4.cu).  All asynchronous on `s`.
+// nr: rows per activation block (8, or 16 for a dense call of 9..16 rows)
 cudaError_t launch_prep_act(const uint16_t* A, int lda, int K, int fmt, int dense_M,
                             int rows_are_pairs, int topk, int n_seg_grid, const GemmWorkspace& ws,
-                            int n_counters, cudaStream_t s, const int32_t* ids = nullptr, int E = 0,
-                            uint32_t* status = nullptr, float* out_zero = nullptr, int ldo = 0,
-                            int N = 0);
-cudaError_t launch_gemm(int fmt, const CUtensorMap& tmW, const CUtensorMap& tmS,
+                            int n_counters, cudaStream_t s, int nr, const int32_t* ids = nullptr,
+                            int E = 0, uint32_t* status = nullptr, float* out_zero = nullptr,
+                            int ldo = 0, int N = 0);
+cudaError_t launch_gemm(int fmt, int nr, const CUtensorMap& tmW, const CUtensorMap& tmS,
                         const GemmParams& p, int grid, int cluster, cudaStream_t s);
 cudaError_t launch_combine(const float* pair_out, const float* gates, const int32_t* ids,
                            int E, int M, int topk, int N, float* out, int ldo, cudaStream_t s);
 cudaError_t launch_q4_0_split(const uint8_t* blocks, int N, int K, uint8_t* q, __half* d,
                               cudaStream_t s);
-int gemm_blocks_per_sm(int fmt);
+int gemm_blocks_per_sm(int fmt, int nr);
 
 // Accept launchers (accept.cu).
 cudaError_t launch_accept_greedy(const float* logits, const int32_t* drafts,

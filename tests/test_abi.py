@@ -42,7 +42,12 @@ def test_status_strings(lib):
 
 def test_workspace_sizes(lib):
     assert vw4.vw4_workspace_bytes(vw4.OP_GEMM, 8, 262144, 5376) > 0
-    assert vw4.vw4_workspace_bytes(vw4.OP_GEMM, 9, 1024, 1024) == 0
+    # 9..16 rows take 16-row activation blocks and partial tiles: more bytes
+    w8 = vw4.vw4_workspace_bytes(vw4.OP_GEMM, 8, 262144, 5376)
+    assert vw4.vw4_workspace_bytes(vw4.OP_GEMM, 9, 262144, 5376) > w8
+    assert vw4.vw4_workspace_bytes(vw4.OP_GEMM, 16, 262144, 5376) == \
+        vw4.vw4_workspace_bytes(vw4.OP_GEMM, 9, 262144, 5376)
+    assert vw4.vw4_workspace_bytes(vw4.OP_GEMM, 17, 1024, 1024) == 0
     assert vw4.vw4_workspace_bytes(vw4.OP_GEMM, 4, 1024, 1000) == 0
     assert vw4.vw4_workspace_bytes(vw4.OP_MOE, 64, 1536, 2048) > 0
     assert vw4.vw4_workspace_bytes(99, 1, 1, 1) == 0
@@ -53,7 +58,7 @@ def _weight(fmt=1, N=128, K=256, ts=1.0, q=0x1000, s=0x2000):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(M=0), 1), (dict(M=9), 1), (dict(lda=100), 1), (dict(ldo=10), 1),
+    (dict(M=0), 1), (dict(M=17), 1), (dict(lda=100), 1), (dict(ldo=10), 1),
     (dict(A=0), 1), (dict(out=0), 1), (dict(A=0x3001), 3), (dict(out=0x4002), 3),
     (dict(ws=0), 6), (dict(ws_bytes=16), 6),
 ])
@@ -95,8 +100,8 @@ def test_accept_argument_checks_on_host(lib):
 
 def test_verify_greedy_argument_checks_on_host(lib):
     W = _weight()
-    # B * (Kd + 1) above 8, B < 1, Kd < 0, null tokens / lengths, null drafts with Kd > 0
-    assert lib.verify_greedy_w4(ctypes.byref(W), 0x3000, 512, 0x100, 2, 4, 0x200, 0x300, None, 0,
+    # B * (Kd + 1) above 16, B < 1, Kd < 0, null tokens / lengths, null drafts with Kd > 0
+    assert lib.verify_greedy_w4(ctypes.byref(W), 0x3000, 512, 0x100, 3, 5, 0x200, 0x300, None, 0,
                                 0x10000, 1 << 30, None) == 1
     assert lib.verify_greedy_w4(ctypes.byref(W), 0x3000, 512, 0x100, 0, 3, 0x200, 0x300, None, 0,
                                 0x10000, 1 << 30, None) == 1

@@ -198,7 +198,7 @@ def test_argument_errors_are_synchronous():
     qd, sd = upload_weight(q, s, "nvfp4")
     Ad = bf16_dev(A)
     with pytest.raises(vw4.VW4Error) as e:
-        vw4.verify_gemm_w4(vw4.FMT_NVFP4, qd, sd, ts, torch.cat([Ad] * 5))  # M = 10
+        vw4.verify_gemm_w4(vw4.FMT_NVFP4, qd, sd, ts, torch.cat([Ad] * 9))  # M = 18
     assert e.value.code == 1
     with pytest.raises(vw4.VW4Error) as e:
         vw4.verify_gemm_w4(vw4.FMT_Q4_0, qd, sd, 2.0, Ad)  # Q4_0 needs tensor_scale 1

@@ -97,7 +97,10 @@ def test_lm_head_fused_path_end_to_end():
 
 
 @pytest.mark.parametrize("N,K,B,Kd", [(20000, 1024, 1, 7), (20000, 1024, 2, 3), (5000, 2048, 4, 1),
-                                      (3000, 512, 3, 0), (70000, 768, 1, 7)])
+                                      (3000, 512, 3, 0), (70000, 768, 1, 7),
+                                      # 9..16 verify rows: two n-tiles per weight fragment
+                                      (20000, 1024, 2, 7), (5000, 2048, 4, 3), (70000, 768, 8, 1),
+                                      (3000, 512, 5, 2)])
 def test_verify_greedy_one_launch(N, K, B, Kd):
     """GEMM, row argmax and greedy accept in one launch: the committed run
     equals the oracle's greedy accept over the GPU's own fp32 logits (which

@@ -30,7 +30,8 @@ def _call_noalloc(W, A, out, row_argmax=None):
 
 
 @pytest.mark.parametrize("fmt,N,K,M", [("nvfp4", 1000, 2304, 8), ("q4_0", 2049, 512, 3),
-                                       ("nvfp4", 17408, 5120, 8)])
+                                       ("nvfp4", 17408, 5120, 8), ("nvfp4", 40000, 512, 16),
+                                       ("q4_0", 1000, 2304, 12)])
 def test_noalloc_matches_workspace_entry_point_twice(fmt, N, K, M):
     q, s, ts = synth.linear(300 + N, N, K, fmt)
     qd = torch.from_numpy(q).cuda()
