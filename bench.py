@@ -413,6 +413,32 @@ def run_accept_timings(device, stream):
             out[f"rejection_K{Kd}_topk50_minp0.05"] = {
                 "us": round(us, 1),
                 "logit_gbs": round(B * (2 * Kd + 1) * V * 4 / (us * 1e-6) / 1e9, 1)}
+            # the rows handed on as top-64 lists (ids and logits; taken here
+            # with torch.topk, outside the timed region) to accept_rejection_topk,
+            # with drafts drawn from the draft lists; the lists (2.2 MB at K = 8)
+            # stay in L2 across the repetitions
+            Kt = 64
+            tv, ti = torch.topk(tgt, Kt, dim=-1)
+            dv, di = torch.topk(drf, Kt, dim=-1)
+            ti, di = ti.to(torch.int32).contiguous(), di.to(torch.int32).contiguous()
+            tv, dv = tv.contiguous(), dv.contiguous()
+            pick = torch.multinomial(torch.softmax(dv.reshape(-1, Kt) / 0.6, dim=-1), 1,
+                                     generator=g).reshape(B, Kd, 1)
+            ldrafts = torch.gather(di, 2, pick).reshape(B, Kd).contiguous()
+            for _ in range(3):
+                vw4.accept_rejection_topk(ti, tv, di, dv, ldrafts, V, 0.6, 0.95, 4, 0,
+                                          workspace=ws, stream=stream)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for r in range(reps):
+                vw4.accept_rejection_topk(ti, tv, di, dv, ldrafts, V, 0.6, 0.95, 4, r,
+                                          workspace=ws, stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) / reps * 1e3
+            out[f"rejection_topk_lists_K{Kd}_kt{Kt}"] = {
+                "us": round(us, 1), "list_bytes": B * (2 * Kd + 1) * Kt * 8}
+            del tv, ti, dv, di
         del tgt, drf
     # greedy accept of 7 drafts from 8 fp32 logits rows of the LM head (V =
     # 262144): a CUDA graph over 20 logits copies (160 MB, more than L2), so

@@ -69,6 +69,7 @@ typedef enum {
 #define VW4_DEV_BAD_EXPERT_ID  0x2u  /* an expert id outside [0, E): that pair is skipped  */
 #define VW4_DEV_WAIT_TIMEOUT   0x4u  /* a pipeline wait gave up; outputs are incomplete    */
 #define VW4_DEV_ZERO_RESIDUAL  0x8u  /* a forced rejection met p == q: drew from p instead */
+#define VW4_DEV_BAD_LIST_ID    0x10u /* a top-k list id outside [0, V): entry dropped      */
 
 /* A block-quantized weight matrix [N][K] (see the format notes above). */
 typedef struct vw4_weight {
@@ -94,6 +95,7 @@ typedef struct vw4_sampling {
 #define VW4_OP_GEMM       1
 #define VW4_OP_MOE        2
 #define VW4_OP_REJECTION  3
+#define VW4_OP_REJECTION_TOPK 4
 
 /*
  * verify_gemm_w4 -- the verification pass's skinny matmul.
@@ -260,6 +262,42 @@ VW4_API vw4_status accept_rejection(const float* target_logits_dev, const float*
                                     size_t ws_bytes, void* stream);
 
 /*
+ * accept_rejection_topk -- accept_rejection over rows kept as top-k lists.
+ *
+ * Defined by: Ollama's mtp.go commit log, paragraph "rework the MLX sampler"
+ * (the top-k stage keeps [B, K] ids and probabilities on the device, and the
+ * acceptance, bonus and residual draws reuse them), with the rule of
+ * accept_rejection above.
+ *
+ * Each row is given as Kt (id, logit) pairs, in any order; every id not
+ * listed reads as a logit of -infinity.  The committed ids and lengths are
+ * exactly those of accept_rejection on dense rows holding the listed logits
+ * and -infinity elsewhere, with the same params (params->top_k may cut the
+ * lists further).  The accept reads Kt * 8 bytes per row instead of V * 4.
+ *
+ * target_ids_dev / target_vals_dev  int32 / fp32 [B][Kd+1][Kt].
+ * draft_ids_dev / draft_vals_dev    int32 / fp32 [B][Kd][Kt] (NULL when Kd == 0).
+ * drafts_dev  int32 [B][Kd].
+ * B >= 1, 0 <= Kd <= 8, 1 <= V <= 2^24, 1 <= Kt <= 1024 (larger Kt:
+ *             VW4_ERR_UNSUPPORTED).  The ids of a row must be distinct; an id
+ *             outside [0, V) is dropped (read as -infinity) and sets
+ *             VW4_DEV_BAD_LIST_ID.
+ * params      as accept_rejection, except that temperature 0 returns
+ *             VW4_ERR_UNSUPPORTED (the greedy rule needs no distribution:
+ *             accept_greedy takes the argmax of each row, its first entry).
+ * seed, offset, tokens_dev, len_dev  as accept_rejection.
+ * workspace_dev / ws_bytes  at least
+ *             vw4_workspace_bytes(VW4_OP_REJECTION_TOPK, B, Kd, Kt).
+ */
+VW4_API vw4_status accept_rejection_topk(const int32_t* target_ids_dev,
+                                         const float* target_vals_dev,
+                                         const int32_t* draft_ids_dev, const float* draft_vals_dev,
+                                         const int32_t* drafts_dev, int B, int Kd, int Kt, int V,
+                                         const vw4_sampling* params, uint64_t seed,
+                                         uint64_t offset, int32_t* tokens_dev, int32_t* len_dev,
+                                         void* workspace_dev, size_t ws_bytes, void* stream);
+
+/*
  * verify_gemm_w4_noalloc -- verify_gemm_w4 for callers that cannot allocate.
  *
  * No counterpart in the source material: this is a deployment convenience.
@@ -289,6 +327,7 @@ VW4_API vw4_status verify_gemm_w4_noalloc(const vw4_weight* W, const void* A_dev
  *   VW4_OP_GEMM:      (M, N, K)
  *   VW4_OP_MOE:       (M*topk, N, K)   -- pass the number of routed pairs first
  *   VW4_OP_REJECTION: (B, Kd, V)
+ *   VW4_OP_REJECTION_TOPK: (B, Kd, Kt)
  * Returns 0 for an unknown op or invalid sizes. */
 VW4_API size_t vw4_workspace_bytes(int op, int a, int b, int c);
 

@@ -249,6 +249,38 @@ def accept_rejection(target, draft, drafts, temperature: float, top_p: float, se
     return tokens, ln, bad
 
 
+def lists_to_rows(ids, vals, V: int):
+    """Dense rows [B, R, V] of top-k lists ids / logits [B, R, Kt]: each listed
+    logit at its id, -inf at every id not listed (ids outside [0, V) are
+    dropped).  The reading of the sampler's sparse [B, K] representation in
+    Ollama's mtp.go commit log ("rework the MLX sampler"): the entries a
+    top-k stage did not keep have no probability."""
+    ids = np.asarray(ids, np.int64)
+    vals = np.asarray(vals, np.float32)
+    B, R, Kt = ids.shape
+    rows = np.full((B, R, V), -np.inf, np.float32)
+    for b in range(B):
+        for r in range(R):
+            for t in range(Kt):
+                v = ids[b, r, t]
+                if 0 <= v < V:
+                    rows[b, r, v] = vals[b, r, t]
+    return rows
+
+
+def accept_rejection_topk(t_ids, t_vals, d_ids, d_vals, drafts, V: int, temperature: float,
+                          top_p: float, seed: int, offset: int, b_base: int = 0,
+                          top_k: int = 0, min_p: float = 0.0):
+    """The accept over top-k lists, by its definition: accept_rejection on the
+    dense rows of the lists (lists_to_rows)."""
+    target = lists_to_rows(t_ids, t_vals, V)
+    B, R, _ = target.shape
+    Kd = R - 1
+    draft = lists_to_rows(d_ids, d_vals, V) if Kd else np.zeros((B, 0, V), np.float32)
+    return accept_rejection(target, draft, drafts, temperature, top_p, seed, offset,
+                            b_base=b_base, top_k=top_k, min_p=min_p)
+
+
 def sample_drafts(draft, temperature: float, top_p: float, seed: int, offset: int,
                   broadcast_rows: bool = False, B: int | None = None, b_base: int = 0,
                   top_k: int = 0, min_p: float = 0.0):

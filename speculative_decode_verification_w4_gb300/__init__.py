@@ -8,6 +8,7 @@ call raises.
 
 Entry points (same names as the C ABI):
   verify_gemm_w4, verify_moe_w4, accept_greedy, accept_rejection,
+  accept_rejection_topk,
   vw4_workspace_bytes, vw4_get_device_status, vw4_q4_0_from_blocks,
   vw4_set_wait_limit_ns.
 """
@@ -27,11 +28,13 @@ FMT_Q4_0 = 2
 OP_GEMM = 1
 OP_MOE = 2
 OP_REJECTION = 3
+OP_REJECTION_TOPK = 4
 
 DEV_BAD_DRAFT_ID = 0x1
 DEV_BAD_EXPERT_ID = 0x2
 DEV_WAIT_TIMEOUT = 0x4
 DEV_ZERO_RESIDUAL = 0x8
+DEV_BAD_LIST_ID = 0x10
 
 STATUS_NAMES = {0: "VW4_OK", 1: "VW4_ERR_INVALID_ARG", 2: "VW4_ERR_UNSUPPORTED",
                 3: "VW4_ERR_ALIGN", 4: "VW4_ERR_CUDA", 5: "VW4_ERR_TIMEOUT",
@@ -42,7 +45,8 @@ EXPORTS = ("verify_gemm_w4", "verify_moe_w4", "accept_greedy", "accept_rejection
            "vw4_workspace_bytes", "vw4_get_device_status", "vw4_q4_0_from_blocks",
            "vw4_status_str", "vw4_last_error_string", "vw4_version", "vw4_set_wait_limit_ns",
            "vw4_own_exp", "verify_gemm_w4_noalloc", "verify_greedy_w4", "vw4_depth_ctl_init",
-           "vw4_depth_ctl_observe", "vw4_depth_ctl_expected", "vw4_depth_ctl_choose")
+           "vw4_depth_ctl_observe", "vw4_depth_ctl_expected", "vw4_depth_ctl_choose",
+           "accept_rejection_topk")
 
 
 class VW4Error(RuntimeError):
@@ -96,6 +100,8 @@ def load_library(path: str = LIB_PATH):
             "accept_greedy": (I, [P, P, P, I, I, I, P, P, P]),
             "accept_rejection": (I, [P, P, P, I, I, I, ctypes.POINTER(Sampling), U64, U64, P, P,
                                      P, ctypes.c_size_t, P]),
+            "accept_rejection_topk": (I, [P, P, P, P, P, I, I, I, I, ctypes.POINTER(Sampling),
+                                          U64, U64, P, P, P, ctypes.c_size_t, P]),
             "vw4_workspace_bytes": (ctypes.c_size_t, [I, I, I, I]),
             "vw4_get_device_status": (I, [ctypes.POINTER(ctypes.c_uint32), P]),
             "vw4_q4_0_from_blocks": (I, [P, I, I, P, P, P]),
@@ -370,6 +376,32 @@ def accept_rejection(target_logits: torch.Tensor, draft_logits: torch.Tensor | N
                                            _ptr(tokens), _ptr(length), _ptr(ws), ws.numel(),
                                            _stream(stream))
     _check(code, "accept_rejection")
+    return tokens, length
+
+
+def accept_rejection_topk(target_ids: torch.Tensor, target_vals: torch.Tensor,
+                          draft_ids: torch.Tensor | None, draft_vals: torch.Tensor | None,
+                          drafts: torch.Tensor, V: int, temperature: float, top_p: float,
+                          seed: int, offset: int = 0, top_k: int = 0, min_p: float = 0.0,
+                          tokens=None, length=None, workspace=None, stream=None):
+    """accept_rejection over rows given as top-k lists: target ids/logits
+    int32/fp32 [B, Kd+1, Kt], draft ids/logits [B, Kd, Kt], vocabulary size V;
+    returns (tokens [B, Kd+1], len [B])."""
+    B, R, Kt = target_ids.shape
+    Kd = R - 1
+    dev = target_ids.device
+    if tokens is None:
+        tokens = torch.empty((B, Kd + 1), dtype=torch.int32, device=dev)
+    if length is None:
+        length = torch.empty((B,), dtype=torch.int32, device=dev)
+    prm = Sampling(float(temperature), float(top_p), int(top_k), float(min_p))
+    need = vw4_workspace_bytes(OP_REJECTION_TOPK, B, Kd, Kt)
+    ws = _workspace(workspace, need, dev)
+    code = load_library().accept_rejection_topk(
+        _ptr(target_ids), _ptr(target_vals), _ptr(draft_ids), _ptr(draft_vals), _ptr(drafts), B,
+        Kd, Kt, int(V), ctypes.byref(prm), int(seed), int(offset), _ptr(tokens), _ptr(length),
+        _ptr(ws), ws.numel(), _stream(stream))
+    _check(code, "accept_rejection_topk")
     return tokens, length
 
 

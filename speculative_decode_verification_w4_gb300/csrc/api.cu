@@ -190,6 +190,10 @@ VW4_API size_t vw4_workspace_bytes(int op, int a, int b, int c) {
         if (a < 1 || b < 0 || b > 8 || c < 1) return 0;
         return rejection_workspace_bytes(a, b, c);
     }
+    if (op == VW4_OP_REJECTION_TOPK) {
+        if (a < 1 || b < 0 || b > 8 || c < 1 || c > 1024) return 0;
+        return rejection_topk_workspace_bytes(a, b, c);
+    }
     return 0;
 }
 
@@ -454,6 +458,48 @@ VW4_API vw4_status accept_rejection(const float* target_logits_dev, const float*
                                             static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return VW4_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return cuda_fail(e, "accept_rejection launch");
+    return VW4_OK;
+}
+
+VW4_API vw4_status accept_rejection_topk(const int32_t* target_ids_dev,
+                                         const float* target_vals_dev,
+                                         const int32_t* draft_ids_dev, const float* draft_vals_dev,
+                                         const int32_t* drafts_dev, int B, int Kd, int Kt, int V,
+                                         const vw4_sampling* params, uint64_t seed,
+                                         uint64_t offset, int32_t* tokens_dev, int32_t* len_dev,
+                                         void* workspace_dev, size_t ws_bytes, void* stream) {
+    if (!params || !target_ids_dev || !target_vals_dev || !tokens_dev || !len_dev)
+        return VW4_ERR_INVALID_ARG;
+    if (B < 1 || Kd < 0 || Kd > kMaxRows || V < 1 || V > (1 << 24) || Kt < 1)
+        return VW4_ERR_INVALID_ARG;
+    if (Kd > 0 && (!drafts_dev || !draft_ids_dev || !draft_vals_dev)) return VW4_ERR_INVALID_ARG;
+    const float T = params->temperature;
+    if (!(T >= 0.0f) || !std::isfinite(T)) return VW4_ERR_INVALID_ARG;
+    if (!(params->top_p > 0.0f) || !std::isfinite(params->top_p)) return VW4_ERR_INVALID_ARG;
+    if (params->top_k < 0) return VW4_ERR_INVALID_ARG;
+    if (!(params->min_p >= 0.0f && params->min_p <= 1.0f)) return VW4_ERR_INVALID_ARG;
+    if (T == 0.0f || Kt > 1024) return VW4_ERR_UNSUPPORTED;
+    const size_t need = rejection_topk_workspace_bytes(B, Kd, Kt);
+    if (!workspace_dev || ws_bytes < need) return VW4_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace_dev) & 255u) != 0) return VW4_ERR_ALIGN;
+    DeviceInfo* d = nullptr;
+    vw4_status st = device_info(&d);
+    if (st != VW4_OK) return st;
+    const float invT = static_cast<float>(1.0 / static_cast<double>(T));
+    const double pd = static_cast<double>(params->top_p) * 4294967296.0;
+    uint64_t P = pd >= 4294967296.0 ? (1ull << 32) : static_cast<uint64_t>(std::llround(pd));
+    if (P == 0) P = 1;
+    const double md = static_cast<double>(params->min_p) * 4294967296.0;
+    const uint64_t MP = params->min_p > 0.0f
+                            ? (md >= 4294967296.0 ? (1ull << 32)
+                                                  : static_cast<uint64_t>(std::llround(md)))
+                            : 0ull;
+    cudaError_t e = launch_accept_rejection_topk(
+        target_ids_dev, target_vals_dev, draft_ids_dev, draft_vals_dev, drafts_dev, B, Kd, Kt, V,
+        invT, P, params->top_k, MP, seed, offset, tokens_dev, len_dev, workspace_dev, ws_bytes,
+        d->status, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return VW4_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return cuda_fail(e, "accept_rejection_topk launch");
     return VW4_OK;
 }
 

@@ -51,6 +51,7 @@ namespace {
 
 constexpr uint32_t kStatusBadDraft = 0x1u;
 constexpr uint32_t kStatusZeroResidual = 0x8u;
+constexpr uint32_t kStatusBadListId = 0x10u;
 constexpr int kThreads = 512;  // the sequence kernel
 constexpr int kWarps = kThreads / 32;
 constexpr int kLogBuckets = 16 + 37 * 8;  // exact 0..15, then 8 per binade up to 2^40
@@ -1439,6 +1440,335 @@ __global__ void __launch_bounds__(kThreads, 2) seq_kernel(
     if (tid == 0) len[b] = sm.n_acc + 1;
 }
 
+// ------------------------------------------------------ top-k lists
+// The accept over sparse rows: every row is given as Kt (id, logit) pairs,
+// the entries a top-k stage kept, in any order; every other entry of the
+// vocabulary reads as -infinity.  The kept masses are those of the dense
+// pipeline on that row, so the committed ids equal the dense accept's on
+// rows holding the listed logits and -infinity elsewhere.
+constexpr int kListMax = 1024;     // longest list
+constexpr int kListThreads = 256;  // row kernel
+constexpr int kListPer = kListMax / kListThreads;
+
+struct ListSmem {
+    unsigned long long key[kListMax];
+    unsigned long long W[kListMax];
+    int id[kListMax];
+    float l[kListMax];
+    Red red;
+    int nan0, cut_p, cut_mp;
+};
+
+// Sorts a[0 .. n) (n a power of two, at most kListMax) in descending order
+// across the block.
+__device__ void list_sort_desc(unsigned long long* a, int n) {
+    for (int k = 2; k <= n; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int t = threadIdx.x; t < n; t += blockDim.x) {
+                const int u = t ^ j;
+                if (u > t) {
+                    const unsigned long long x = a[t], y = a[u];
+                    if ((t & k) == 0 ? (x < y) : (x > y)) {
+                        a[t] = y;
+                        a[u] = x;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// Inclusive prefix over the block of one u64 per thread (the block's
+// threads in order).
+__device__ __forceinline__ unsigned long long block_incl_u64(unsigned long long v, Red& sm) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    unsigned long long incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) sm.w[wid] = incl;
+    __syncthreads();
+    unsigned long long base = 0;
+    for (int w = 0; w < wid; ++w) base += sm.w[w];
+    __syncthreads();
+    return base + incl;
+}
+
+// One CTA per list row: rows (b, j) for j = 0..Kd are target rows, j =
+// Kd+1..2Kd draft rows.  Writes the row's entries sorted by id with their
+// kept masses (0 for the dropped ones) and the kept sum.
+__global__ void __launch_bounds__(kListThreads) list_row_kernel(
+    const int32_t* __restrict__ t_ids, const float* __restrict__ t_vals,
+    const int32_t* __restrict__ d_ids, const float* __restrict__ d_vals, int Kd, int Kt, int V,
+    float invT, unsigned long long P, int top_k, unsigned long long MP, int32_t* __restrict__ o_ids,
+    unsigned long long* __restrict__ o_W, unsigned long long* __restrict__ o_S, uint32_t* status) {
+    __shared__ ListSmem sm;
+    const int tid = threadIdx.x;
+    const long long r = blockIdx.x;
+    const int per_seq = 2 * Kd + 1;
+    const long long b = r / per_seq;
+    const int j = static_cast<int>(r % per_seq);
+    const long long src = j <= Kd ? (b * (Kd + 1) + j) * Kt : (b * Kd + (j - Kd - 1)) * Kt;
+    const int32_t* ids = j <= Kd ? t_ids : d_ids;
+    const float* vals = j <= Kd ? t_vals : d_vals;
+    int n = 1;
+    while (n < Kt) n <<= 1;
+
+    // (1) load; an id outside [0, V) is dropped (its logit read as -inf)
+    if (tid == 0) sm.nan0 = 0;
+    __syncthreads();
+    float m = -INFINITY;
+    int bad = 0;
+    for (int t = tid; t < Kt; t += kListThreads) {
+        int id = __ldg(ids + src + t);
+        float l = __ldg(vals + src + t);
+        if (id < 0 || id >= V) {
+            bad = 1;
+            id = V + t;  // past every real id: sorts last, never looked up
+            l = -INFINITY;
+        }
+        if (id == 0 && l != l) sm.nan0 = 1;
+        m = fmaxf(m, l);  // NaN never raises the max
+        sm.id[t] = id;
+        sm.l[t] = l;
+    }
+    if (bad) atomicOr(status, kStatusBadListId);
+    // The dense row's max is taken from index 0 upwards with ">": a NaN at
+    // index 0 makes it NaN (then every mass is 0); elsewhere NaN is skipped.
+    m = block_max(m, sm.red);
+    const float mx = sm.nan0 ? __int_as_float(0x7fc00000) : m;
+
+    // (2) top-k: the first top_k entries in (logit desc, id asc) order take
+    // part; -inf and NaN entries weigh 0 whether they take part or not
+    const bool tk_on = top_k > 0 && top_k < V && top_k < Kt;
+    unsigned long long tk_cut = 0ull;
+    if (tk_on) {
+        for (int t = tid; t < n; t += kListThreads)
+            sm.key[t] = t < Kt ? (static_cast<unsigned long long>(logit_key(sm.l[t])) << 32) |
+                                     (0xFFFFFFFFu - static_cast<uint32_t>(sm.id[t]))
+                               : 0ull;
+        __syncthreads();
+        list_sort_desc(sm.key, n);
+        tk_cut = sm.key[top_k - 1];
+        __syncthreads();
+    }
+    // (3) masses
+    unsigned long long part = 0ull;
+    for (int t = tid; t < Kt; t += kListThreads) {
+        const float l = sm.l[t];
+        bool in = true;
+        if (tk_on)
+            in = ((static_cast<unsigned long long>(logit_key(l)) << 32) |
+                  (0xFFFFFFFFu - static_cast<uint32_t>(sm.id[t]))) >= tk_cut;
+        const unsigned long long W = in ? mass_of(own_exp(scaled_x(l, mx, invT))) : 0ull;
+        sm.W[t] = W;
+        part += W;
+    }
+    const unsigned long long S = block_sum_u64(part, sm.red);
+
+    // (4) top-p and min-p: both keep a prefix of the (W desc, id asc) order.
+    // Key: W (2^40 read as 2^40 - 1: no other mass lies above 2^40 - 2^16),
+    // then the low 24 bits of ~id (ids below 2^24; only dropped ids collide,
+    // and they weigh 0).
+    if (P < kKeepAll || MP > 0) {
+        for (int t = tid; t < n; t += kListThreads) {
+            unsigned long long key = 0ull;
+            if (t < Kt) {
+                const unsigned long long W = sm.W[t];
+                const unsigned long long w40 = W >= (1ull << 40) ? (1ull << 40) - 1ull : W;
+                key = (w40 << 24) | (0xFFFFFFull - (static_cast<uint32_t>(sm.id[t]) & 0xFFFFFFu));
+            }
+            sm.key[t] = key;
+        }
+        if (tid == 0) {
+            sm.cut_p = Kt;
+            sm.cut_mp = Kt;
+        }
+        __syncthreads();
+        list_sort_desc(sm.key, n);
+        // each thread takes kListPer consecutive sorted positions
+        const int p0 = tid * kListPer;
+        unsigned long long w[kListPer], run = 0ull;
+#pragma unroll
+        for (int q = 0; q < kListPer; ++q) {
+            const int p = p0 + q;
+            unsigned long long W = 0ull;
+            if (p < Kt) {
+                W = sm.key[p] >> 24;
+                if (W == (1ull << 40) - 1ull) W = 1ull << 40;
+            }
+            w[q] = W;
+            run += W;
+        }
+        const unsigned long long incl = block_incl_u64(run, sm.red);
+        const unsigned long long w_top = sm.key[0] >> 24 == (1ull << 40) - 1ull
+                                             ? (1ull << 40)
+                                             : sm.key[0] >> 24;
+        unsigned long long cum = incl - run;
+        const u128 target = static_cast<u128>(P) * S;
+#pragma unroll
+        for (int q = 0; q < kListPer; ++q) {
+            const int p = p0 + q;
+            if (p >= Kt) break;
+            cum += w[q];
+            if (P < kKeepAll && (static_cast<u128>(cum) << 32) >= target)
+                atomicMin(&sm.cut_p, p + 1);  // the shortest prefix reaching P
+            if (MP > 0 && (static_cast<u128>(w[q]) << 32) < static_cast<u128>(MP) * w_top)
+                atomicMin(&sm.cut_mp, p);     // the first entry below min-p
+        }
+        __syncthreads();
+        const int keep = min(sm.cut_p, sm.cut_mp);
+        // the kept entries are the sorted positions below keep; keep >= 1
+        // unless min-p drops the top entry itself (then nothing is kept)
+        const unsigned long long kcut = keep > 0 ? sm.key[keep - 1] : ~0ull;
+        __syncthreads();
+        for (int t = tid; t < Kt; t += kListThreads) {
+            const unsigned long long W = sm.W[t];
+            const unsigned long long w40 = W >= (1ull << 40) ? (1ull << 40) - 1ull : W;
+            const unsigned long long key =
+                (w40 << 24) | (0xFFFFFFull - (static_cast<uint32_t>(sm.id[t]) & 0xFFFFFFu));
+            if (keep == 0 || key < kcut) sm.W[t] = 0ull;
+        }
+        __syncthreads();
+    }
+    unsigned long long kpart = 0ull;
+    for (int t = tid; t < Kt; t += kListThreads) kpart += sm.W[t];
+    const unsigned long long S_kept = block_sum_u64(kpart, sm.red);
+
+    // (5) the row sorted by id (ascending), with its kept masses
+    for (int t = tid; t < n; t += kListThreads)
+        sm.key[t] = t < Kt ? ((static_cast<unsigned long long>(0x7FFFFFFF - sm.id[t]) << 32) |
+                              static_cast<uint32_t>(t))
+                           : 0ull;
+    __syncthreads();
+    list_sort_desc(sm.key, n);  // descending in 0x7FFFFFFF - id: ascending in id
+    for (int p = tid; p < Kt; p += kListThreads) {
+        const int t = static_cast<int>(sm.key[p] & 0xFFFFFFFFu);
+        o_ids[r * Kt + p] = sm.id[t];
+        o_W[r * Kt + p] = sm.W[t];
+    }
+    if (tid == 0) o_S[r] = S_kept;
+}
+
+// The kept mass of id x in a row sorted by id (0 when absent).
+__device__ __forceinline__ unsigned long long list_mass(const int32_t* ids,
+                                                        const unsigned long long* W, int Kt,
+                                                        int x) {
+    int lo = 0, hi = Kt;  // first position with id >= x
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(ids + mid) < x) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo < Kt && __ldg(ids + lo) == x ? __ldg(W + lo) : 0ull;
+}
+
+// One warp per sequence: the acceptance tests in order, then one ordered
+// draw over the rejected position's list (the residual against the draft's
+// list, or p itself), or the bonus from the last target list.
+constexpr int kListSeqWarps = 4;
+
+__global__ void __launch_bounds__(kListSeqWarps * 32) list_seq_kernel(
+    const int32_t* __restrict__ drafts, int B, int Kd, int Kt, int V, unsigned long long seed,
+    unsigned long long offset, const int32_t* __restrict__ l_ids,
+    const unsigned long long* __restrict__ l_W, const unsigned long long* __restrict__ l_S,
+    int32_t* __restrict__ tokens, int32_t* __restrict__ len, uint32_t* status) {
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.x * kListSeqWarps + (threadIdx.x >> 5);
+    if (b >= B) return;
+    const long long per_seq = 2 * Kd + 1;
+    auto row = [&](int j) { return static_cast<long long>(b) * per_seq + j; };  // list row
+    int n = 0;
+    unsigned long long u64 = 0ull;
+    for (; n <= Kd; ++n) {
+        uint32_t rr[4];
+        philox4x32_10(static_cast<uint32_t>(n), static_cast<uint32_t>(b),
+                      static_cast<uint32_t>(offset), static_cast<uint32_t>(offset >> 32),
+                      static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32), rr);
+        u64 = (static_cast<unsigned long long>(rr[2]) << 32) | rr[1];
+        if (n == Kd) break;  // every draft accepted: the bonus
+        const int32_t x = drafts[static_cast<long long>(b) * Kd + n];
+        bool ok = false;
+        if (x >= 0 && x < V) {
+            const long long rp = row(n), rq = row(Kd + 1 + n);
+            const unsigned long long Wp = list_mass(l_ids + rp * Kt, l_W + rp * Kt, Kt, x);
+            const unsigned long long Wq = list_mass(l_ids + rq * Kt, l_W + rq * Kt, Kt, x);
+            const unsigned long long U = rr[0] >> 8;
+            const u128 lhs = static_cast<u128>(U * Wq) * l_S[rp];
+            const u128 rhs = (static_cast<u128>(Wp) * l_S[rq]) << 24;
+            ok = lhs < rhs;
+        } else if (lane == 0) {
+            atomicOr(status, kStatusBadDraft);
+        }
+        if (!ok) break;
+    }
+    // the draw: over target list n in id order, weights the residual
+    // max(0, Wp Sq - Wq Sp) at a rejection, else (the bonus, or an empty
+    // residual) Wp itself
+    const long long rp = row(n);
+    const int32_t* pid = l_ids + rp * Kt;
+    const unsigned long long* pW = l_W + rp * Kt;
+    const unsigned long long Sp = l_S[rp];
+    const bool rejected = n < Kd;
+    const long long rq = rejected ? row(Kd + 1 + n) : -1;
+    const unsigned long long Sq = rejected ? l_S[rq] : 0ull;
+    const int c = (Kt + 31) / 32;
+    const int a = min(lane * c, Kt), e = min(a + c, Kt);
+    auto weight = [&](int p, bool resid) -> u128 {
+        const unsigned long long Wp = __ldg(pW + p);
+        if (!resid) return Wp;
+        const unsigned long long Wq =
+            Wp ? list_mass(l_ids + rq * Kt, l_W + rq * Kt, Kt, __ldg(pid + p)) : 0ull;
+        const u128 x = static_cast<u128>(Wp) * Sq, y = static_cast<u128>(Wq) * Sp;
+        return x > y ? x - y : 0;
+    };
+    bool resid = rejected;
+    u128 mine = 0;
+    for (int p = a; p < e; ++p) mine += weight(p, resid);
+    u128 R = warp_sum_u128(mine);
+    if (resid && R == 0) {  // only reachable through an invalid draft id
+        if (lane == 0) atomicOr(status, kStatusZeroResidual);
+        resid = false;
+        mine = 0;
+        for (int p = a; p < e; ++p) mine += weight(p, false);
+        R = warp_sum_u128(mine);
+    }
+    int tok = V - 1;  // an empty row: as the dense draw
+    if (R > 0) {
+        const u128 t = scale_u64(u64, R);
+        u128 incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const u128 y = shfl_up_u128(incl, o);
+            if (lane >= o) incl += y;
+        }
+        const unsigned int hit = __ballot_sync(0xffffffffu, incl > t);
+        const int L = __ffs(hit) - 1;  // R > t, so some lane's prefix exceeds t
+        int found = -1;
+        if (lane == L) {
+            u128 cum = incl - mine;
+            for (int p = a; p < e; ++p) {
+                cum += weight(p, resid);
+                if (cum > t) {
+                    found = __ldg(pid + p);
+                    break;
+                }
+            }
+        }
+        tok = __shfl_sync(0xffffffffu, found, L);
+    }
+    for (int i = lane; i <= Kd; i += 32) {
+        int32_t tk = -1;
+        if (i < n) tk = drafts[static_cast<long long>(b) * Kd + i];
+        else if (i == n) tk = tok;
+        tokens[static_cast<long long>(b) * (Kd + 1) + i] = tk;
+    }
+    if (lane == 0) len[b] = n + 1;
+}
+
 __global__ void own_exp_kernel(const float* __restrict__ x, float* __restrict__ y, long long n) {
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<long long>(gridDim.x) * blockDim.x)
@@ -1505,6 +1835,41 @@ cudaError_t launch_accept_rejection(const float* target, const float* draft,
                                       static_cast<unsigned long long>(seed),
                                       static_cast<unsigned long long>(offset), n_target_rows,
                                       info, segmax, segsum, tokens, len, status);
+    return cudaGetLastError();
+}
+
+static size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+size_t rejection_topk_workspace_bytes(int B, int Kd, int Kt) {
+    const size_t rows = static_cast<size_t>(B) * (2 * static_cast<size_t>(Kd) + 1);
+    return round256(rows * Kt * 4) + round256(rows * Kt * 8) + round256(rows * 8);
+}
+
+cudaError_t launch_accept_rejection_topk(const int32_t* t_ids, const float* t_vals,
+                                         const int32_t* d_ids, const float* d_vals,
+                                         const int32_t* drafts, int B, int Kd, int Kt, int V,
+                                         float invT, uint64_t P, int top_k, uint64_t MP,
+                                         uint64_t seed, uint64_t offset, int32_t* tokens,
+                                         int32_t* len, void* ws, size_t ws_bytes,
+                                         uint32_t* status, cudaStream_t s) {
+    if (Kt < 1 || Kt > kListMax) return cudaErrorNotSupported;
+    const long long rows = static_cast<long long>(B) * (2 * Kd + 1);
+    if (rows > 0x7fffffffll) return cudaErrorNotSupported;
+    if (rejection_topk_workspace_bytes(B, Kd, Kt) > ws_bytes) return cudaErrorInvalidValue;
+    char* w = static_cast<char*>(ws);
+    int32_t* l_ids = reinterpret_cast<int32_t*>(w);
+    w += round256(static_cast<size_t>(rows) * Kt * 4);
+    unsigned long long* l_W = reinterpret_cast<unsigned long long*>(w);
+    w += round256(static_cast<size_t>(rows) * Kt * 8);
+    unsigned long long* l_S = reinterpret_cast<unsigned long long*>(w);
+    list_row_kernel<<<static_cast<unsigned>(rows), kListThreads, 0, s>>>(
+        t_ids, t_vals, d_ids, d_vals, Kd, Kt, V, invT, static_cast<unsigned long long>(P), top_k,
+        static_cast<unsigned long long>(MP), l_ids, l_W, l_S, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    list_seq_kernel<<<(B + kListSeqWarps - 1) / kListSeqWarps, kListSeqWarps * 32, 0, s>>>(
+        drafts, B, Kd, Kt, V, static_cast<unsigned long long>(seed),
+        static_cast<unsigned long long>(offset), l_ids, l_W, l_S, tokens, len, status);
     return cudaGetLastError();
 }
 

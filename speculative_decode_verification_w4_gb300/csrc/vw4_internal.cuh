@@ -150,4 +150,13 @@ cudaError_t launch_accept_rejection(const float* target, const float* draft,
                                     int32_t* len, void* ws, size_t ws_bytes, uint32_t* status,
                                     unsigned long long wait_ns, cudaStream_t s);
 
+size_t rejection_topk_workspace_bytes(int B, int Kd, int Kt);
+cudaError_t launch_accept_rejection_topk(const int32_t* t_ids, const float* t_vals,
+                                         const int32_t* d_ids, const float* d_vals,
+                                         const int32_t* drafts, int B, int Kd, int Kt, int V,
+                                         float invT, uint64_t P, int top_k, uint64_t MP,
+                                         uint64_t seed, uint64_t offset, int32_t* tokens,
+                                         int32_t* len, void* ws, size_t ws_bytes,
+                                         uint32_t* status, cudaStream_t s);
+
 }  // namespace vw4

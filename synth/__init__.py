@@ -182,3 +182,36 @@ def routing(seed: int, M: int, E: int, topk: int):
     gp = np.take_along_axis(p, order, axis=1)
     gates = (gp / gp.sum(axis=1, keepdims=True)).astype(np.float32)
     return order.astype(np.int32), gates
+
+
+def topk_lists_case(seed: int, B: int, Kd: int, Kt: int, V: int, temperature: float = 0.6,
+                    target_std: float = 3.0, noise_std: float = 1.0, swap: float = 0.2):
+    """Rows given as top-Kt lists, as a top-k stage would hand them on: target
+    ids int32 [B, Kd+1, Kt] (distinct per row, uniform over the vocabulary)
+    with logits fp32 sorted descending; draft lists [B, Kd, Kt] holding the
+    target row's ids, a fraction `swap` of them replaced by other ids, with
+    the target logits plus N(0, noise_std); drafts int32 [B, Kd] picked from
+    the draft lists by the Gumbel-max rule at `temperature`."""
+    g = rng(seed)
+    t_ids = np.empty((B, Kd + 1, Kt), np.int32)
+    t_vals = np.empty((B, Kd + 1, Kt), np.float32)
+    d_ids = np.empty((B, Kd, Kt), np.int32)
+    d_vals = np.empty((B, Kd, Kt), np.float32)
+    drafts = np.empty((B, Kd), np.int32)
+    for b in range(B):
+        for r in range(Kd + 1):
+            ids = g.choice(V, size=Kt, replace=False).astype(np.int32)
+            vals = np.sort(g.standard_normal(Kt).astype(np.float32) * np.float32(target_std))[::-1]
+            t_ids[b, r], t_vals[b, r] = ids, vals
+            if r < Kd:
+                di = ids.copy()
+                sw = g.random(Kt) < swap
+                if sw.any():
+                    pool = np.setdiff1d(np.arange(V, dtype=np.int32), ids)
+                    di[sw] = g.choice(pool, size=int(sw.sum()), replace=False)
+                dv = vals + g.standard_normal(Kt).astype(np.float32) * np.float32(noise_std)
+                d_ids[b, r], d_vals[b, r] = di, dv
+                gum = -np.log(-np.log(g.random(Kt)))
+                drafts[b, r] = di[int(np.argmax(dv.astype(np.float64) / temperature + gum))]
+    return t_ids, t_vals, d_ids, d_vals, drafts
+

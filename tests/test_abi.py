@@ -98,6 +98,28 @@ def test_accept_argument_checks_on_host(lib):
                                 0x200, 0x1000, 1 << 20, None) == 1
 
 
+def test_accept_rejection_topk_argument_checks_on_host(lib):
+    assert vw4.vw4_workspace_bytes(vw4.OP_REJECTION_TOPK, 256, 8, 64) > 0
+    assert vw4.vw4_workspace_bytes(vw4.OP_REJECTION_TOPK, 256, 8, 1025) == 0
+    prm = vw4.Sampling(0.6, 0.95, 0, 0.0)
+
+    def call(Kt=16, B=2, Kd=2, V=100, p=prm, ws=0x1000, ws_bytes=1 << 24, t_ids=0x100):
+        return lib.accept_rejection_topk(t_ids, 0x200, 0x300, 0x400, 0x500, B, Kd, Kt, V,
+                                         ctypes.byref(p), 0, 0, 0x600, 0x700, ws, ws_bytes, None)
+    assert call(Kt=0) == 1
+    assert call(B=0) == 1
+    assert call(Kd=9) == 1
+    assert call(V=0) == 1
+    assert call(t_ids=None) == 1
+    assert call(Kt=1025) == 2                                 # longer lists: unsupported
+    assert call(p=vw4.Sampling(0.0, 0.95, 0, 0.0)) == 2       # greedy: accept_greedy instead
+    assert call(p=vw4.Sampling(0.6, 0.95, -1, 0.0)) == 1
+    assert call(p=vw4.Sampling(0.6, 0.95, 0, 2.0)) == 1
+    assert call(ws=None) == 6
+    assert call(ws_bytes=64) == 6
+    assert call(ws=0x1001) == 3
+
+
 def test_verify_greedy_argument_checks_on_host(lib):
     W = _weight()
     # B * (Kd + 1) above 16, B < 1, Kd < 0, null tokens / lengths, null drafts with Kd > 0

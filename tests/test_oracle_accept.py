@@ -289,3 +289,55 @@ def test_first_token_marginal_with_top_k_and_min_p():
     assert np.array_equal(W0 > 0, p0 > 0)           # the same kept set as the float pipeline
     counts = np.bincount(tok[:, 0], minlength=V)
     assert _chi2_against(counts, p0) > 1e-4
+
+
+# ------------------------------------------------------------ top-k lists
+def _top_lists(rows, Kt, g):
+    """The top-Kt entries of each row in (logit desc, index asc) order, then
+    shuffled: ids int32, logits fp32 [B, R, Kt]."""
+    B, R, V = rows.shape
+    ids = np.empty((B, R, Kt), np.int32)
+    vals = np.empty((B, R, Kt), np.float32)
+    for b in range(B):
+        for r in range(R):
+            o = np.lexsort((np.arange(V), -rows[b, r].astype(np.float64)))[:Kt]
+            o = o[g.permutation(Kt)]
+            ids[b, r], vals[b, r] = o, rows[b, r, o]
+    return ids, vals
+
+
+@pytest.mark.parametrize("B,Kd,V,Kt,top_p,top_k,min_p", [
+    (12, 3, 200, 16, 0.95, 0, 0.0), (8, 2, 1000, 50, 0.9, 0, 0.05), (6, 4, 500, 64, 1.0, 20, 0.0),
+    (10, 1, 300, 1, 0.95, 0, 0.0), (7, 0, 400, 30, 0.8, 0, 0.1)])
+def test_top_k_lists_equal_the_dense_top_k_stage(B, Kd, V, Kt, top_p, top_k, min_p):
+    """Rows given as their top-Kt lists (any order) accept exactly as the
+    dense rows with the top-k stage at Kt (and any further top-k / min-p):
+    the scatter into -inf rows against the sampler's own top-k stage."""
+    g = np.random.default_rng(B * 31 + Kt)
+    target = (g.standard_normal((B, Kd + 1, V)) * 3).astype(np.float32)
+    draft = (target[:, :Kd] + g.standard_normal((B, Kd, V))).astype(np.float32)
+    kk = min(top_k, Kt) if top_k else Kt
+    drafts = oracle.sample_drafts(draft, 0.6, top_p, 5, 1 << 32, top_k=kk, min_p=min_p) if Kd \
+        else np.zeros((B, 0), np.int32)
+    t_ids, t_vals = _top_lists(target, Kt, g)
+    d_ids, d_vals = _top_lists(draft, Kt, g) if Kd else (None, None)
+    lt, ll, lb = oracle.accept_rejection_topk(t_ids, t_vals, d_ids, d_vals, drafts, V, 0.6, top_p,
+                                              5, 3, top_k=top_k, min_p=min_p)
+    dt, dl, db = oracle.accept_rejection(target, draft, drafts, 0.6, top_p, 5, 3, top_k=kk,
+                                         min_p=min_p)
+    assert np.array_equal(ll, dl) and np.array_equal(lt, dt) and lb == db
+
+
+def test_lists_to_rows_places_every_listed_logit():
+    ids = np.array([[[3, 0, 7], [9, 2, 5]]], np.int32)
+    vals = np.array([[[1.0, -2.0, 0.5], [4.0, np.nan, -np.inf]]], np.float32)
+    rows = oracle.lists_to_rows(ids, vals, 10)
+    assert rows.shape == (1, 2, 10)
+    assert rows[0, 0, 3] == 1.0 and rows[0, 0, 0] == -2.0 and rows[0, 0, 7] == 0.5
+    assert np.isnan(rows[0, 1, 2]) and rows[0, 1, 9] == 4.0
+    assert np.isneginf(rows[0, 1, 5])
+    assert np.isneginf(np.delete(rows[0, 0], [0, 3, 7])).all()
+    # ids outside [0, V) are dropped
+    rows = oracle.lists_to_rows(np.array([[[11, 1]]], np.int32), np.array([[[5.0, 6.0]]],
+                                                                          np.float32), 10)
+    assert rows[0, 0, 1] == 6.0 and np.isneginf(np.delete(rows[0, 0], [1])).all()
