@@ -1446,21 +1446,22 @@ __global__ void __launch_bounds__(kThreads, 2) seq_kernel(
 // vocabulary reads as -infinity.  The kept masses are those of the dense
 // pipeline on that row, so the committed ids equal the dense accept's on
 // rows holding the listed logits and -infinity elsewhere.
-constexpr int kListMax = 1024;     // longest list
-constexpr int kListThreads = 256;  // row kernel
-constexpr int kListPer = kListMax / kListThreads;
+constexpr int kListMax = 1024;  // longest list
 
+// Row kernel shapes: NT threads for lists of up to NMAX entries (NMAX / NT
+// sorted positions per thread in the prefix scan).  Short lists take small
+// blocks with small arrays, so that many rows run per SM.
+template <int NT, int NMAX>
 struct ListSmem {
-    unsigned long long key[kListMax];
-    unsigned long long W[kListMax];
-    int id[kListMax];
-    float l[kListMax];
+    unsigned long long key[NMAX];
+    unsigned long long W[NMAX];
+    int id[NMAX];
+    float l[NMAX];
     Red red;
     int nan0, cut_p, cut_mp;
 };
 
-// Sorts a[0 .. n) (n a power of two, at most kListMax) in descending order
-// across the block.
+// Sorts a[0 .. n) (n a power of two) in descending order across the block.
 __device__ void list_sort_desc(unsigned long long* a, int n) {
     for (int k = 2; k <= n; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
@@ -1500,12 +1501,16 @@ __device__ __forceinline__ unsigned long long block_incl_u64(unsigned long long 
 // One CTA per list row: rows (b, j) for j = 0..Kd are target rows, j =
 // Kd+1..2Kd draft rows.  Writes the row's entries sorted by id with their
 // kept masses (0 for the dropped ones) and the kept sum.
-__global__ void __launch_bounds__(kListThreads) list_row_kernel(
+template <int NT, int NMAX>
+__global__ void __launch_bounds__(NT) list_row_kernel(
     const int32_t* __restrict__ t_ids, const float* __restrict__ t_vals,
     const int32_t* __restrict__ d_ids, const float* __restrict__ d_vals, int Kd, int Kt, int V,
     float invT, unsigned long long P, int top_k, unsigned long long MP, int32_t* __restrict__ o_ids,
     unsigned long long* __restrict__ o_W, unsigned long long* __restrict__ o_S, uint32_t* status) {
-    __shared__ ListSmem sm;
+    constexpr int kListThreads = NT;
+    constexpr int kListPer = NMAX / NT;
+    static_assert(NMAX % NT == 0 && NT % 32 == 0, "list row kernel shape");
+    __shared__ ListSmem<NT, NMAX> sm;
     const int tid = threadIdx.x;
     const long long r = blockIdx.x;
     const int per_seq = 2 * Kd + 1;
@@ -1853,6 +1858,7 @@ cudaError_t launch_accept_rejection_topk(const int32_t* t_ids, const float* t_va
                                          int32_t* len, void* ws, size_t ws_bytes,
                                          uint32_t* status, cudaStream_t s) {
     if (Kt < 1 || Kt > kListMax) return cudaErrorNotSupported;
+    static_assert(kListMax == 1024, "the two row kernel shapes cover lists up to 1024");
     const long long rows = static_cast<long long>(B) * (2 * Kd + 1);
     if (rows > 0x7fffffffll) return cudaErrorNotSupported;
     if (rejection_topk_workspace_bytes(B, Kd, Kt) > ws_bytes) return cudaErrorInvalidValue;
@@ -1862,9 +1868,14 @@ cudaError_t launch_accept_rejection_topk(const int32_t* t_ids, const float* t_va
     unsigned long long* l_W = reinterpret_cast<unsigned long long*>(w);
     w += round256(static_cast<size_t>(rows) * Kt * 8);
     unsigned long long* l_S = reinterpret_cast<unsigned long long*>(w);
-    list_row_kernel<<<static_cast<unsigned>(rows), kListThreads, 0, s>>>(
-        t_ids, t_vals, d_ids, d_vals, Kd, Kt, V, invT, static_cast<unsigned long long>(P), top_k,
-        static_cast<unsigned long long>(MP), l_ids, l_W, l_S, status);
+    if (Kt <= 256)
+        list_row_kernel<64, 256><<<static_cast<unsigned>(rows), 64, 0, s>>>(
+            t_ids, t_vals, d_ids, d_vals, Kd, Kt, V, invT, static_cast<unsigned long long>(P),
+            top_k, static_cast<unsigned long long>(MP), l_ids, l_W, l_S, status);
+    else
+        list_row_kernel<256, 1024><<<static_cast<unsigned>(rows), 256, 0, s>>>(
+            t_ids, t_vals, d_ids, d_vals, Kd, Kt, V, invT, static_cast<unsigned long long>(P),
+            top_k, static_cast<unsigned long long>(MP), l_ids, l_W, l_S, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     list_seq_kernel<<<(B + kListSeqWarps - 1) / kListSeqWarps, kListSeqWarps * 32, 0, s>>>(
