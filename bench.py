@@ -331,21 +331,7 @@ def run_ours(args, rank, world, device):
                 "kernel": "vw4::gemm_w4_kernel<nvfp4> (with its activation-prep launch)",
                 "per_unit": "0.5625 B per weight (nibble + e4m3/16) + 2*M B per k of activations"}
 
-    # the draft-depth controller on the measured verify cost of each width
-    # (the layer step at M = 1, 2, 4, 8; linear in between), a synthetic
-    # acceptance of 0.8 at every position and, as an assumption, a draft
-    # costing a tenth of a one-row verify step per token
-    mus = {int(m): per_m["nvfp4"][m]["layer_us"] for m in per_m["nvfp4"]}
-    pts = sorted(mus)
-    verify_us = {w: float(np.interp(w, pts, [mus[p] for p in pts])) for w in range(1, 9)}
-    ctl = vw4.DepthController(k_max=7, decay=1.0, verify_us=verify_us,
-                              draft_us_per_token=0.1 * verify_us[1])
-    for i in range(8):      # counts giving (acc + 1) / (att + 2) ~ 0.8 at every position
-        ctl.state.att[i], ctl.state.acc[i] = 10000.0, 8000.0
-    rates = {k: round(ctl.expected(k)[0] / ctl.expected(k)[1] * 1e3, 3) for k in range(8)}
-    depth = {"acceptance": 0.8, "draft_us_per_token": round(0.1 * verify_us[1], 2),
-             "verify_us": {w: round(v, 2) for w, v in verify_us.items()},
-             "committed_tokens_per_ms": rates, "chosen_depth": ctl.choose()}
+    depth = depth_controller_summary(per_m)
 
     stream = torch.cuda.current_stream()
     accept = run_accept_timings(device, stream)
@@ -371,6 +357,27 @@ def run_ours(args, rank, world, device):
         "clocks": clk.summary(),
     }
     return result
+
+
+def depth_controller_summary(per_m):
+    """The draft-depth controller on the measured verify cost of each width
+    (the nvfp4 layer step at the measured M, linear in between), a synthetic
+    acceptance of 0.8 at every position and, as an assumption, a draft
+    costing a tenth of a one-row verify step per token."""
+    import speculative_decode_verification_w4_gb300 as vw4
+    mus = {int(m): per_m["nvfp4"][m]["layer_us"] for m in per_m["nvfp4"]}
+    pts = sorted(mus)
+    k_max = max(pts) - 1
+    verify_us = {w: float(np.interp(w, pts, [mus[p] for p in pts])) for w in range(1, k_max + 2)}
+    ctl = vw4.DepthController(k_max=k_max, decay=1.0, verify_us=verify_us,
+                              draft_us_per_token=0.1 * verify_us[1])
+    for i in range(k_max + 1):  # counts giving (acc + 1) / (att + 2) ~ 0.8 at every position
+        ctl.state.att[i], ctl.state.acc[i] = 10000.0, 8000.0
+    rates = {k: round(ctl.expected(k)[0] / ctl.expected(k)[1] * 1e3, 3)
+             for k in range(k_max + 1)}
+    return {"acceptance": 0.8, "draft_us_per_token": round(0.1 * verify_us[1], 2),
+            "verify_us": {w: round(v, 2) for w, v in verify_us.items()},
+            "committed_tokens_per_ms": rates, "chosen_depth": ctl.choose()}
 
 
 def run_accept_timings(device, stream):

@@ -361,11 +361,12 @@ VW4_API vw4_status vw4_own_exp(const float* x_dev, float* y_dev, int64_t n, void
  *
  * State (caller-owned, zero it or call vw4_depth_ctl_init):
  *   att[i], acc[i]  decayed counts of drafts attempted / accepted at position
- *                   i, given drafts 0..i-1 were accepted (i < 8);
- *   verify_us[w]    the cost of a verify pass over w = K + 1 rows (1..8);
+ *                   i, given drafts 0..i-1 were accepted (i < 16);
+ *   verify_us[w]    the cost of a verify pass over w = K + 1 rows (1..16);
  *   draft_us_fixed, draft_us_per_token   the cost of drafting K > 0 tokens,
  *                   fixed + K * per_token;
- *   k_max           the deepest draft considered (0..7: M = K + 1 <= 8);
+ *   k_max           the deepest draft considered (0..15: the verify GEMM
+ *                   takes M = K + 1 <= 16 rows);
  *   decay           weight kept by old observations at each new one (0..1].
  * The acceptance estimate of position i is (acc[i] + 1) / (att[i] + 2).  The
  * expected committed run of depth K is sum_{j=0..K} prod_{i<j} alpha_i (the
@@ -373,8 +374,8 @@ VW4_API vw4_status vw4_own_exp(const float* x_dev, float* y_dev, int64_t n, void
  * drafting cost (none at K = 0, plain decoding).
  */
 typedef struct vw4_depth_ctl {
-    double att[8], acc[8];
-    float verify_us[9];
+    double att[16], acc[16];
+    float verify_us[17];
     float draft_us_fixed, draft_us_per_token;
     int k_max;
     float decay;

@@ -60,8 +60,8 @@ class VW4Error(RuntimeError):
 
 class DepthCtl(ctypes.Structure):
     """vw4_depth_ctl (see vw4.h): the draft-depth controller's state."""
-    _fields_ = [("att", ctypes.c_double * 8), ("acc", ctypes.c_double * 8),
-                ("verify_us", ctypes.c_float * 9), ("draft_us_fixed", ctypes.c_float),
+    _fields_ = [("att", ctypes.c_double * 16), ("acc", ctypes.c_double * 16),
+                ("verify_us", ctypes.c_float * 17), ("draft_us_fixed", ctypes.c_float),
                 ("draft_us_per_token", ctypes.c_float), ("k_max", ctypes.c_int32),
                 ("decay", ctypes.c_float)]
 

@@ -17,8 +17,11 @@
 
 namespace {
 
+constexpr int kMaxDepth = 15;  // verify rows K + 1 <= 16, the verify GEMM's widest call
+constexpr int kPositions = kMaxDepth + 1;
+
 bool valid(const vw4_depth_ctl* c) {
-    if (c == nullptr || c->k_max < 0 || c->k_max > 7) return false;
+    if (c == nullptr || c->k_max < 0 || c->k_max > kMaxDepth) return false;
     if (!(c->decay > 0.0f && c->decay <= 1.0f)) return false;
     for (int w = 1; w <= c->k_max + 1; ++w)
         if (!(c->verify_us[w] > 0.0f) || !std::isfinite(c->verify_us[w])) return false;
@@ -33,10 +36,10 @@ double alpha(const vw4_depth_ctl* c, int i) { return (c->acc[i] + 1.0) / (c->att
 extern "C" {
 
 VW4_API vw4_status vw4_depth_ctl_init(vw4_depth_ctl* c, int k_max, float decay) {
-    if (c == nullptr || k_max < 0 || k_max > 7 || !(decay > 0.0f && decay <= 1.0f))
+    if (c == nullptr || k_max < 0 || k_max > kMaxDepth || !(decay > 0.0f && decay <= 1.0f))
         return VW4_ERR_INVALID_ARG;
-    for (int i = 0; i < 8; ++i) c->att[i] = c->acc[i] = 0.0;
-    for (int w = 0; w <= 8; ++w) c->verify_us[w] = 1.0f;
+    for (int i = 0; i < kPositions; ++i) c->att[i] = c->acc[i] = 0.0;
+    for (int w = 0; w <= kPositions; ++w) c->verify_us[w] = 1.0f;
     c->draft_us_fixed = 0.0f;
     c->draft_us_per_token = 0.0f;
     c->k_max = k_max;
@@ -47,7 +50,7 @@ VW4_API vw4_status vw4_depth_ctl_init(vw4_depth_ctl* c, int k_max, float decay) 
 VW4_API vw4_status vw4_depth_ctl_observe(vw4_depth_ctl* c, int depth, int accepted) {
     if (!valid(c) || depth < 0 || depth > c->k_max || accepted < 0 || accepted > depth)
         return VW4_ERR_INVALID_ARG;
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < kPositions; ++i) {
         c->att[i] *= c->decay;
         c->acc[i] *= c->decay;
     }

@@ -61,3 +61,16 @@ def test_step_bytes_counts_weights_scales_and_activations():
     w4 = sum(n * k * 9 // 16 for _, n, k in bench.STEP)
     assert w7 == w4
     assert bench.step_bytes(8, spec=bench.LAYER) - total == 8 * 5120 * 2 * 3
+
+
+def test_depth_controller_summary_over_sixteen_widths():
+    """The bench's controller summary from per-M step times (M = 1..16):
+    widths interpolated, depths 0..15 rated, the choice the best rate."""
+    lay = {"1": 57.2, "2": 57.5, "4": 57.5, "8": 57.6, "16": 73.4}
+    per_m = {"nvfp4": {m: {"layer_us": us} for m, us in lay.items()}}
+    d = bench.depth_controller_summary(per_m)
+    assert sorted(d["verify_us"]) == list(range(1, 17))
+    assert d["verify_us"][12] == pytest.approx(57.6 + (73.4 - 57.6) * 4 / 8, abs=0.01)
+    rates = d["committed_tokens_per_ms"]
+    assert sorted(rates) == list(range(16))
+    assert d["chosen_depth"] == max(rates, key=lambda k: (rates[k], -k))

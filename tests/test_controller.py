@@ -43,18 +43,19 @@ def test_decay_weights_old_observations_down():
     assert c.state.acc[0] == pytest.approx(0.5)
 
 
-@pytest.mark.parametrize("seed", range(5))
-def test_expected_and_choice_match_brute_force(seed):
+@pytest.mark.parametrize("seed,k_max", [(s, 7) for s in range(5)] + [(s, 15) for s in range(5, 8)])
+def test_expected_and_choice_match_brute_force(seed, k_max):
     g = np.random.default_rng(seed)
-    c = vw4.DepthController(k_max=7, decay=1.0, draft_us_fixed=float(g.uniform(0, 20)),
+    c = vw4.DepthController(k_max=k_max, decay=1.0, draft_us_fixed=float(g.uniform(0, 20)),
                             draft_us_per_token=float(g.uniform(0, 10)),
-                            verify_us={w: float(50 + 8 * w + g.uniform(0, 5)) for w in range(1, 9)})
+                            verify_us={w: float(50 + 8 * w + g.uniform(0, 5))
+                                       for w in range(1, k_max + 2)})
     for _ in range(200):
-        d = int(g.integers(0, 8))
+        d = int(g.integers(0, k_max + 1))
         c.observe(d, int(g.integers(0, d + 1)))
-    alphas = [(c.state.acc[i] + 1.0) / (c.state.att[i] + 2.0) for i in range(8)]
+    alphas = [(c.state.acc[i] + 1.0) / (c.state.att[i] + 2.0) for i in range(k_max + 1)]
     rates = []
-    for k in range(8):
+    for k in range(k_max + 1):
         t, us = c.expected(k)
         assert t == pytest.approx(expected_run(alphas, k), rel=1e-12)
         cost = c.state.verify_us[k + 1] + (c.state.draft_us_fixed +
@@ -70,6 +71,18 @@ def test_falls_back_to_plain_decoding_when_drafts_are_rejected():
     for _ in range(100):
         c.observe(3, 0)
     assert c.choose() == 0
+
+
+def test_drafts_past_eight_when_sixteen_row_verify_is_cheap():
+    """Verify widths up to 16 rows: with a flat verify cost and near-certain
+    acceptance the deepest depth, 15, wins."""
+    c = vw4.DepthController(k_max=15, decay=1.0, draft_us_per_token=1.0,
+                            verify_us={w: 100.0 for w in range(1, 17)})
+    for _ in range(200):
+        c.observe(15, 15)
+    assert c.choose() == 15
+    t, _ = c.expected(15)
+    assert 15.0 < t <= 16.0
 
 
 def test_drafts_deep_when_verify_width_is_cheap_and_acceptance_high():
@@ -142,7 +155,7 @@ def test_invalid_arguments():
     with pytest.raises(vw4.VW4Error):
         c.observe(2, 3)
     with pytest.raises(vw4.VW4Error):
-        vw4.DepthController(k_max=8)
+        vw4.DepthController(k_max=16)
     c.state.verify_us[2] = 0.0
     with pytest.raises(vw4.VW4Error):
         c.choose()
