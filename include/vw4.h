@@ -57,7 +57,7 @@ typedef enum { VW4_FMT_NVFP4 = 1, VW4_FMT_Q4_0 = 2 } vw4_fmt;
 typedef enum {
     VW4_OK = 0,
     VW4_ERR_INVALID_ARG = 1,   /* null pointer, size or enum out of range       */
-    VW4_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement   */
+    VW4_ERR_UNSUPPORTED = 2,   /* valid request the library does not implement  */
     VW4_ERR_ALIGN = 3,         /* a pointer or leading dimension is misaligned  */
     VW4_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed             */
     VW4_ERR_TIMEOUT = 5,       /* reported by vw4_get_device_status bits only   */
