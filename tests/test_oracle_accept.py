@@ -16,6 +16,7 @@ import pytest
 from scipy import stats
 
 import oracle
+import synth
 from conftest import golden_lines
 
 
@@ -341,3 +342,24 @@ def test_lists_to_rows_places_every_listed_logit():
     rows = oracle.lists_to_rows(np.array([[[11, 1]]], np.int32), np.array([[[5.0, 6.0]]],
                                                                           np.float32), 10)
     assert rows[0, 0, 1] == 6.0 and np.isneginf(np.delete(rows[0, 0], [1])).all()
+
+
+def test_topk_lists_case_follows_its_recipe():
+    """The seeded list generator: distinct in-range ids per row, target logits
+    sorted descending, drafts taken from their own draft lists, and the
+    draft lists sharing most of the target row's ids."""
+    B, Kd, Kt, V = 6, 3, 40, 500
+    t_ids, t_vals, d_ids, d_vals, drafts = synth.topk_lists_case(1, B, Kd, Kt, V)
+    assert t_ids.shape == (B, Kd + 1, Kt) and d_ids.shape == (B, Kd, Kt)
+    for ids in (t_ids, d_ids):
+        assert ids.min() >= 0 and ids.max() < V
+        for row in ids.reshape(-1, Kt):
+            assert np.unique(row).size == Kt
+    assert np.all(np.diff(t_vals, axis=-1) <= 0)
+    shared = [np.intersect1d(t_ids[b, i], d_ids[b, i]).size for b in range(B) for i in range(Kd)]
+    assert np.mean(shared) > 0.6 * Kt
+    for b in range(B):
+        for i in range(Kd):
+            assert drafts[b, i] in d_ids[b, i]
+    again = synth.topk_lists_case(1, B, Kd, Kt, V)
+    assert all(np.array_equal(a, c) for a, c in zip(again, (t_ids, t_vals, d_ids, d_vals, drafts)))
