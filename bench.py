@@ -734,8 +734,8 @@ def run_reference(args, rank, world):
 def run_case(case: str, device):
     """Profiling helper: a few calls of the GEMM on a fixed case, nothing timed
     or printed but a one-line summary.  'dense' = the 4 nvfp4 calls of the
-    packed layer step at M = 8 (3 warm-up passes, then 1); 'N,K,M' = one nvfp4
-    GEMM of that shape (3 warm-up calls, then 1); 'rejection:K' = the
+    packed layer step at M = 8 (3 warm-up passes, then 1); 'N,K,M[,q4_0]' = one
+    GEMM of that shape, nvfp4 unless q4_0 is named (3 warm-up calls, then 1); 'rejection:K' = the
     rejection accept of the stochastic sweep (B = 256, V = 151936, K drafts),
     4 calls."""
     import torch
@@ -762,16 +762,22 @@ def run_case(case: str, device):
         jobs = [(qd, sd, ts, acts[j], N) for j, (name, N, K, qd, sd, ts) in enumerate(layer)]
     else:
         import synth
-        N, K, M = (int(x) for x in case.split(","))
-        q, sc, ts = synth.linear(1, N, K, "nvfp4")
+        parts = case.split(",")
+        N, K, M = (int(x) for x in parts[:3])
+        fmt = parts[3] if len(parts) > 3 else "nvfp4"
+        q, sc, ts = synth.linear(1, N, K, fmt)
         bits = synth.activations(synth.rng(2), M, K)
         A = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(device)
-        jobs = [(torch.from_numpy(q).to(device), torch.from_numpy(sc).to(device), ts, A, N)]
+        sd = torch.from_numpy(sc if fmt == "nvfp4" else sc.view(np.uint16)).to(device)
+        if fmt != "nvfp4":
+            sd = sd.view(torch.float16)
+        jobs = [(torch.from_numpy(q).to(device), sd, ts, A, N)]
+    code = vw4.FMT_Q4_0 if case.endswith("q4_0") else vw4.FMT_NVFP4
     outs = [torch.empty((a.shape[0], N), dtype=torch.float32, device=device)
             for (_, _, _, a, N) in jobs]
     for _ in range(4):
         for (qd, sd, ts, a, N), o in zip(jobs, outs):
-            vw4.verify_gemm_w4(vw4.FMT_NVFP4, qd, sd, ts, a, out=o, workspace=ws)
+            vw4.verify_gemm_w4(code, qd, sd, ts, a, out=o, workspace=ws)
     torch.cuda.synchronize()
     print(f"case {case}: {len(jobs)} GEMM(s) x 4 calls, device status "
           f"{vw4.vw4_get_device_status()}", flush=True)
@@ -785,7 +791,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--case", default=None,
-                    help="profiling helper: 'dense', 'N,K,M' or 'rejection:K' (see run_case); "
+                    help="profiling helper: 'dense', 'N,K,M[,q4_0]' or 'rejection:K' (see run_case); "
                          "no JSON line")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -126,8 +126,24 @@ typedef struct vw4_sampling {
  *             aligned, reused freely between calls on the same stream.
  * Error behaviour: VW4_ERR_INVALID_ARG for null pointers, M outside 1..16,
  * N < 1, K not a positive multiple of the block, lda < K, ldo < N;
+ * VW4_ERR_UNSUPPORTED when K is a multiple of the block but not of 256 (the
+ * weights are streamed by TMA tensor copies in 256-wide k stages, which need
+ * row pitches of K/2 and K/16 bytes that are multiples of 16: every K of the
+ * dense-layer, LM-head and MoE configurations is a multiple of 256);
  * VW4_ERR_ALIGN for misaligned pointers or leading dimensions;
  * VW4_ERR_WORKSPACE when the workspace is too small.
+ *
+ * Precision.  Products of the unpacked weights (exact in fp16) with the
+ * activations are accumulated in fp32 on the tensor cores.  The activations
+ * enter as fp16 after an exact power-of-two scaling per verify row and
+ * 256-wide k stage, chosen so that the stage's largest magnitude amax lies in
+ * [2^14, 2^15).  An activation is carried exactly when it is zero or at least
+ * 2^-31 * amax in magnitude (every bf16 value down to that ratio fits fp16's
+ * range and 11-bit significand); a smaller one is rounded to a multiple of at
+ * most 2^-39 * amax.  So every output satisfies
+ *   |out - exact| <= 1e-3 * sum_k |a_k w_k| + 2^-39 * sum_k amax(k) * |w_k|,
+ * amax(k) the largest |a| of the row in the stage of k; the second term is
+ * zero unless a stage mixes activations more than 2^31 apart.
  */
 VW4_API vw4_status verify_gemm_w4(const vw4_weight* W, const void* A_dev, int M, int lda,
                                   float* out_dev, int ldo, int32_t* row_argmax_dev,
@@ -323,6 +339,44 @@ VW4_API vw4_status verify_gemm_w4_noalloc(const vw4_weight* W, const void* A_dev
                                           float* out_dev, int ldo, int32_t* row_argmax_dev,
                                           void* stream);
 
+/*
+ * One row record of accept_rejection, as its first kernel leaves it in the
+ * workspace.  It describes the row's distribution after top-k, temperature /
+ * softmax, top-p and min-p in the exact integer form above: with
+ * W_v = floor(exp_own((l_v - max) * (1/T)) * 2^40) the mass of entry v before
+ * any cut, entry v is kept iff it passes top-k (its logit key is above
+ * topk_key, or equal and v <= topk_idx) and W_v > tau, or W_v == tau and
+ * v <= cut; kept_sum is the sum of the kept masses.
+ */
+typedef struct vw4_row_record {
+    float max;              /* the row max (scanned from index 0 with ">")     */
+    int32_t cut;            /* largest kept index among the entries W == tau   */
+    uint64_t tau;           /* the smallest kept mass                           */
+    uint64_t kept_sum;      /* sum of the kept masses (S)                       */
+    uint32_t topk_key;      /* top-k cut key (0 when top-k is off)              */
+    int32_t topk_idx;       /* top-k cut index (INT32_MAX when top-k is off)    */
+} vw4_row_record;
+
+/*
+ * vw4_rejection_row_records -- test hook: the row records of an
+ * accept_rejection call.
+ *
+ * No counterpart in the source material: it exposes the per-row state of the
+ * accept step so that every row can be compared with an independent
+ * implementation, not only the ids the draws commit.
+ *
+ * workspace_dev / ws_bytes  the workspace of an accept_rejection call with
+ *             the same B, Kd and V, after that call (stream order).
+ * records_dev vw4_row_record [B * (2 Kd + 1)], device memory: the target rows
+ *             (b, i) for i = 0..Kd in order, then the draft rows (b, i) for
+ *             i < Kd.  Asynchronous on `stream` (a device-to-device copy).
+ * Errors: VW4_ERR_INVALID_ARG for null pointers or sizes out of range,
+ * VW4_ERR_WORKSPACE when ws_bytes is below what that call needed.
+ */
+VW4_API vw4_status vw4_rejection_row_records(const void* workspace_dev, size_t ws_bytes, int B,
+                                             int Kd, int V, vw4_row_record* records_dev,
+                                             void* stream);
+
 /* Workspace bytes needed by an operation:
  *   VW4_OP_GEMM:      (M, N, K)
  *   VW4_OP_MOE:       (M*topk, N, K)   -- pass the number of routed pairs first
@@ -359,7 +413,9 @@ VW4_API vw4_status vw4_own_exp(const float* x_dev, float* y_dev, int64_t n, void
  * at runtime from acceptance rates and verification pass times, falling back
  * when drafting does not pay).
  *
- * State (caller-owned, zero it or call vw4_depth_ctl_init):
+ * State (caller-owned; call vw4_depth_ctl_init before any other use: a
+ * zero-filled state is invalid -- decay 0 and verify costs of 0 are rejected,
+ * choose returns -1 and the others VW4_ERR_INVALID_ARG):
  *   att[i], acc[i]  decayed counts of drafts attempted / accepted at position
  *                   i, given drafts 0..i-1 were accepted (i < 16);
  *   verify_us[w]    the cost of a verify pass over w = K + 1 rows (1..16);
@@ -409,6 +465,15 @@ VW4_API int vw4_version(void);
  * kernels (default 2e9).  A wait that runs out sets VW4_DEV_WAIT_TIMEOUT and
  * the kernel returns early with its copies drained.  0 restores the default. */
 VW4_API void vw4_set_wait_limit_ns(uint64_t ns);
+
+/* Test hook: the next `calls` verify GEMM launches of this process (through
+ * verify_gemm_w4, verify_greedy_w4, verify_moe_w4 or the no-alloc variant)
+ * make their consumer warps wait, before their first stage, on a pipeline
+ * barrier that nothing ever completes, so that the bounded wait runs out: the
+ * launch sets VW4_DEV_WAIT_TIMEOUT, lets its copies in flight land and returns
+ * without writing its results.  0 cancels.  With vw4_set_wait_limit_ns it
+ * exercises the timeout path without faulting or hanging the GPU. */
+VW4_API void vw4_test_inject_stall(int calls);
 
 #ifdef __cplusplus
 }

@@ -46,7 +46,8 @@ EXPORTS = ("verify_gemm_w4", "verify_moe_w4", "accept_greedy", "accept_rejection
            "vw4_status_str", "vw4_last_error_string", "vw4_version", "vw4_set_wait_limit_ns",
            "vw4_own_exp", "verify_gemm_w4_noalloc", "verify_greedy_w4", "vw4_depth_ctl_init",
            "vw4_depth_ctl_observe", "vw4_depth_ctl_expected", "vw4_depth_ctl_choose",
-           "accept_rejection_topk")
+           "accept_rejection_topk", "vw4_rejection_row_records",
+           "vw4_test_inject_stall")
 
 
 class VW4Error(RuntimeError):
@@ -119,6 +120,8 @@ def load_library(path: str = LIB_PATH):
             "vw4_depth_ctl_choose": (I, [ctypes.POINTER(DepthCtl)]),
             "verify_greedy_w4": (I, [ctypes.POINTER(Weight), P, I, P, I, I, P, P, P, I, P,
                                      ctypes.c_size_t, P]),
+            "vw4_rejection_row_records": (I, [P, ctypes.c_size_t, I, I, I, P, P]),
+            "vw4_test_inject_stall": (None, [I]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -405,6 +408,25 @@ def accept_rejection_topk(target_ids: torch.Tensor, target_vals: torch.Tensor,
     return tokens, length
 
 
+# vw4_row_record (see vw4.h): 32 bytes per row
+ROW_RECORD_DTYPE = [("max", "<f4"), ("cut", "<i4"), ("tau", "<u8"), ("kept_sum", "<u8"),
+                    ("topk_key", "<u4"), ("topk_idx", "<i4")]
+
+
+def vw4_rejection_row_records(workspace, B: int, Kd: int, V: int, stream=None):
+    """The row records of the accept_rejection call that last used `workspace`
+    (a Workspace or a uint8 tensor) with the same B, Kd, V: a CUDA uint8
+    tensor [rows, 32]; view it on the host with ROW_RECORD_DTYPE.  Rows: the
+    target rows (b, i <= Kd) in order, then the draft rows (b, i < Kd)."""
+    buf = workspace.buf if isinstance(workspace, Workspace) else workspace
+    rows = B * (2 * Kd + 1)
+    rec = torch.empty((rows, 32), dtype=torch.uint8, device=buf.device)
+    _check(load_library().vw4_rejection_row_records(_ptr(buf), buf.numel(), B, Kd, V, _ptr(rec),
+                                                    _stream(stream)),
+           "vw4_rejection_row_records")
+    return rec
+
+
 def vw4_get_device_status(stream=None) -> int:
     bits = ctypes.c_uint32(0)
     _check(load_library().vw4_get_device_status(ctypes.byref(bits), _stream(stream)),
@@ -431,3 +453,9 @@ def vw4_own_exp(x: torch.Tensor, out: torch.Tensor | None = None, stream=None):
 
 def vw4_set_wait_limit_ns(ns: int):
     load_library().vw4_set_wait_limit_ns(int(ns))
+
+
+def vw4_test_inject_stall(calls: int):
+    """Test hook: the next `calls` GEMM launches wait on a barrier nothing
+    completes until their bounded wait runs out (see vw4.h)."""
+    load_library().vw4_test_inject_stall(int(calls))

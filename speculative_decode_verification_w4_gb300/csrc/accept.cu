@@ -144,13 +144,12 @@ cudaError_t launch_accept_greedy(const float* logits, const int32_t* drafts,
     if (am == nullptr) {
         const long long rows = static_cast<long long>(B) * (Kd + 1);
         const int vec = (V % 4 == 0 && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0) ? 1 : 0;
-        static bool attr_done = false;
-        if (!attr_done) {
-            cudaError_t e = cudaFuncSetAttribute(
-                row_argmax_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-            if (e != cudaSuccess) return e;
-            attr_done = true;
-        }
+        static std::atomic<unsigned long long> attr_once{0};
+        cudaError_t ea = set_attribute_per_device(attr_once, [] {
+            return cudaFuncSetAttribute(row_argmax_kernel,
+                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        });
+        if (ea != cudaSuccess) return ea;
         row_argmax_kernel<<<static_cast<unsigned>(rows * kArgCluster), kArgThreads, 0, s>>>(
             logits, V, vec, tokens);
         cudaError_t e = cudaGetLastError();

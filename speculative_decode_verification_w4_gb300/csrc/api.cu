@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -34,6 +35,14 @@ struct DeviceInfo {
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
 unsigned long long g_wait_ns = 2000000000ull;
+std::atomic<int> g_stall_calls{0};  // test hook: GEMM launches left to stall
+
+int take_stall() {
+    int n = g_stall_calls.load();
+    while (n > 0 && !g_stall_calls.compare_exchange_weak(n, n - 1)) {
+    }
+    return n > 0 ? 1 : 0;
+}
 thread_local std::string g_last_error;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -175,6 +184,8 @@ VW4_API void vw4_set_wait_limit_ns(uint64_t ns) {
     g_wait_ns = ns == 0 ? 2000000000ull : static_cast<unsigned long long>(ns);
 }
 
+VW4_API void vw4_test_inject_stall(int calls) { g_stall_calls.store(calls > 0 ? calls : 0); }
+
 VW4_API size_t vw4_workspace_bytes(int op, int a, int b, int c) {
     if (op == VW4_OP_GEMM) {
         const int M = a, N = b, K = c;
@@ -289,6 +300,7 @@ static vw4_status gemm_entry(const vw4_weight* W, const void* A_dev, int M, int 
     p.status = d->status;
     p.wait_ns = g_wait_ns;
     p.cluster = clustered ? 1 : 0;
+    p.stall_test = take_stall();
     if (greedy) {
         p.greedy_B = greedy->B;
         p.greedy_Kd = greedy->Kd;
@@ -392,6 +404,7 @@ VW4_API vw4_status verify_moe_w4(const vw4_weight* experts, int E, const void* A
     p.row_argmax = nullptr;
     p.status = d->status;
     p.wait_ns = g_wait_ns;
+    p.stall_test = take_stall();
     e = launch_gemm(experts->fmt, 8, tmW, tmS, p, static_cast<int>(G), 1, s);
     if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
     if (combine) {
@@ -500,6 +513,19 @@ VW4_API vw4_status accept_rejection_topk(const int32_t* target_ids_dev,
         d->status, static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return VW4_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return cuda_fail(e, "accept_rejection_topk launch");
+    return VW4_OK;
+}
+
+VW4_API vw4_status vw4_rejection_row_records(const void* workspace_dev, size_t ws_bytes, int B,
+                                             int Kd, int V, vw4_row_record* records_dev,
+                                             void* stream) {
+    if (!workspace_dev || !records_dev) return VW4_ERR_INVALID_ARG;
+    if (B < 1 || Kd < 0 || Kd > kMaxRows || V < 1 || V > (1 << 24)) return VW4_ERR_INVALID_ARG;
+    if (ws_bytes < rejection_workspace_bytes(B, Kd, V)) return VW4_ERR_WORKSPACE;
+    const long long rows = static_cast<long long>(B) * (2 * Kd + 1);
+    cudaError_t e = copy_rejection_row_records(workspace_dev, rows, records_dev,
+                                               static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "row record copy");
     return VW4_OK;
 }
 

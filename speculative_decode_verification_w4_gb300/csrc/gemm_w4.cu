@@ -643,7 +643,8 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Sh::kSmemBar);
     uint64_t* empty = full + Sh::kStages;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + Sh::kStages);
+    uint64_t* never = empty + Sh::kStages;  // completed by nothing (the stall test)
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(never + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // The next call's kernels may become resident now: they touch nothing
@@ -654,6 +655,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps);
         }
+        mbar_init(never, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -811,6 +813,12 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     // ---------------------------------------------------------- consumers
     {
     grid_dependency_wait();  // activations, scales of this call, tickets reset
+    if (p.stall_test && !mbar_wait_bounded(never, 0u, p.wait_ns, abort_flag)) {
+        if (lane == 0) atomicOr(p.status, kStatusTimeout);
+        *abort_flag = 1;
+        if (cluster_mode) goto combine;
+        return;
+    }
     const int g = lane >> 2, c = lane & 3;
     const int wrow = warp * kWarpRows;  // first tile row of this warp
     uint32_t it = 0;
@@ -1182,13 +1190,12 @@ template <int FMT, int NR>
 static cudaError_t launch_gemm_t(const CUtensorMap& tmW, const CUtensorMap& tmS,
                                  const GemmParams& p, int grid, int cluster, cudaStream_t s) {
     constexpr int kSmem = GemmShape<NR>::kSmem;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_w4_kernel<FMT, NR>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    static std::atomic<unsigned long long> attr_once{0};
+    cudaError_t ea = set_attribute_per_device(attr_once, [] {
+        return cudaFuncSetAttribute(gemm_w4_kernel<FMT, NR>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    });
+    if (ea != cudaSuccess) return ea;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kGemmThreads);

@@ -41,8 +41,10 @@
 // (to the workspace), finds the segment that holds the draw point by a block
 // scan of those sums and rescans that one segment.
 #include <cmath>
+#include <cstddef>
 
 #include "ptx.cuh"
+#include "vw4.h"
 #include "vw4_internal.cuh"
 
 namespace vw4 {
@@ -1841,6 +1843,24 @@ cudaError_t launch_accept_rejection(const float* target, const float* draft,
                                       static_cast<unsigned long long>(offset), n_target_rows,
                                       info, segmax, segsum, tokens, len, status);
     return cudaGetLastError();
+}
+
+// The records are vw4_row_record in the public header: the same fields at
+// the same offsets.
+static_assert(sizeof(RowInfo) == sizeof(vw4_row_record), "row record size");
+static_assert(offsetof(RowInfo, mx) == offsetof(vw4_row_record, max) &&
+                  offsetof(RowInfo, cut) == offsetof(vw4_row_record, cut) &&
+                  offsetof(RowInfo, tau) == offsetof(vw4_row_record, tau) &&
+                  offsetof(RowInfo, S) == offsetof(vw4_row_record, kept_sum) &&
+                  offsetof(RowInfo, tk_key) == offsetof(vw4_row_record, topk_key) &&
+                  offsetof(RowInfo, tk_idx) == offsetof(vw4_row_record, topk_idx),
+              "row record layout");
+
+cudaError_t copy_rejection_row_records(const void* ws, long long rows, void* out,
+                                       cudaStream_t s) {
+    // the records are the first part of the workspace (info_bytes)
+    return cudaMemcpyAsync(out, ws, static_cast<size_t>(rows) * sizeof(RowInfo),
+                           cudaMemcpyDeviceToDevice, s);
 }
 
 static size_t round256(size_t x) { return (x + 255) / 256 * 256; }

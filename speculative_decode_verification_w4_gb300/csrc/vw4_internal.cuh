@@ -4,10 +4,25 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
 namespace vw4 {
+
+// Kernel attributes set with cudaFuncSetAttribute apply to the current device
+// only: `once` keeps one bit per device (devices past 63 set it every time).
+inline cudaError_t set_attribute_per_device(std::atomic<unsigned long long>& once,
+                                            cudaError_t (*set)()) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
+    if (bit && (once.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = set();
+    if (e == cudaSuccess && bit) once.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 
 constexpr int kMaxRows = 8;        // rows of one mma n-tile; verify rows per MoE segment
 constexpr int kMaxVerifyRows = 16; // dense verify rows per call: two n-tiles
@@ -115,6 +130,9 @@ struct GemmParams {
     const int32_t* drafts;
     int32_t* tokens;
     int32_t* len;
+    // test hook: the consumers first wait on a barrier nothing completes, so
+    // that the bounded wait runs out (the timeout path, without a fault)
+    int stall_test;
 };
 
 // Lays the GEMM/MoE workspace out from `base` (nullptr: size only) for
@@ -150,6 +168,9 @@ cudaError_t launch_accept_rejection(const float* target, const float* draft,
                                     int32_t* len, void* ws, size_t ws_bytes, uint32_t* status,
                                     unsigned long long wait_ns, cudaStream_t s);
 
+// Copies the first `rows` row records of a rejection workspace (test hook).
+cudaError_t copy_rejection_row_records(const void* ws, long long rows, void* out,
+                                       cudaStream_t s);
 size_t rejection_topk_workspace_bytes(int B, int Kd, int Kt);
 cudaError_t launch_accept_rejection_topk(const int32_t* t_ids, const float* t_vals,
                                          const int32_t* d_ids, const float* d_vals,

@@ -159,3 +159,19 @@ def test_invalid_arguments():
     c.state.verify_us[2] = 0.0
     with pytest.raises(vw4.VW4Error):
         c.choose()
+
+
+def test_zero_filled_state_is_rejected_until_init():
+    """A zero-filled state is invalid (decay 0, verify costs 0), as the header
+    says: choose returns -1 and observe / expected fail; after
+    vw4_depth_ctl_init the same struct works."""
+    import ctypes
+    lib = vw4.load_library()
+    st = vw4.DepthCtl()          # ctypes zero-fills
+    assert lib.vw4_depth_ctl_choose(ctypes.byref(st)) == -1
+    assert lib.vw4_depth_ctl_observe(ctypes.byref(st), 0, 0) == 1
+    t, us = ctypes.c_double(), ctypes.c_double()
+    assert lib.vw4_depth_ctl_expected(ctypes.byref(st), 0, ctypes.byref(t), ctypes.byref(us)) == 1
+    assert lib.vw4_depth_ctl_init(ctypes.byref(st), 3, 1.0) == 0
+    assert lib.vw4_depth_ctl_choose(ctypes.byref(st)) in range(4)
+    assert lib.vw4_depth_ctl_observe(ctypes.byref(st), 2, 1) == 0

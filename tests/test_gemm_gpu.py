@@ -204,3 +204,56 @@ def test_argument_errors_are_synchronous():
         vw4.verify_gemm_w4(vw4.FMT_Q4_0, qd, sd, 2.0, Ad)  # Q4_0 needs tensor_scale 1
     assert e.value.code == 1
     assert vw4.vw4_get_device_status() == 0
+
+
+def _mixed_stage_case(tiny_exp):
+    """Rows whose first 256-wide k stage holds activations of 1 on the k's
+    where a chosen output column's weight is zero-coded and 2^tiny_exp * u
+    (u in [1, 2), random bf16 mantissas) elsewhere; the second stage is zero.
+    The large activations then add nothing to that column, whose sum|a*w|
+    comes from the tiny ones alone."""
+    N, K, M = 256, 512, 4
+    q, s, ts = synth.linear(31, N, K, "nvfp4")
+    w = oracle.dequant(oracle.FMT_NVFP4, N, K, q, s, ts)
+    g = synth.rng(32)
+    x = np.zeros((M, K), np.float32)
+    cols = []
+    for m in range(M):
+        n = (37 * m + 5) % N
+        cols.append(n)
+        zero = w[n, :256] == 0.0
+        assert zero.sum() >= 8 and (~zero).sum() >= 64
+        u = (1.0 + g.random(256)).astype(np.float32) * np.float32(2.0 ** tiny_exp)
+        sign = np.where(g.random(256) < 0.5, -1.0, 1.0).astype(np.float32)
+        x[m, :256] = np.where(zero, np.float32(1.0), u * sign)
+    return N, K, M, q, s, ts, w, synth.bf16_bits(x), np.array(cols)
+
+
+def test_mixed_magnitude_stage_inside_the_exact_range():
+    """Within one 256-wide k stage, activations down to 2^-31 of the stage's
+    largest magnitude are represented exactly (vw4.h, verify_gemm_w4
+    precision): the pass rule holds for the column the large activations do
+    not reach."""
+    N, K, M, q, s, ts, w, A, cols = _mixed_stage_case(-31)
+    gpu = gemm_gpu("nvfp4", q, s, ts, A).cpu().numpy()
+    ref, bnd = oracle.gemm_w4(oracle.FMT_NVFP4, N, K, q, s, ts, A)
+    assert_gemm_close(gpu, ref, bnd, "mixed magnitudes, exact range")
+    for m, n in enumerate(cols):
+        assert bnd[m, n] > 0.0 and abs(gpu[m, n] - ref[m, n]) <= 1e-3 * bnd[m, n]
+
+
+@pytest.mark.parametrize("tiny_exp", [-36, -40, -60])
+def test_mixed_magnitude_stage_below_the_exact_range(tiny_exp):
+    """Below 2^-31 of the stage's largest magnitude an activation is rounded
+    to a multiple of 2^-39 of it (or to zero): the error of every element
+    stays within 1e-3 * sum|a*w| + 2^-39 * sum_k amax_stage(k) * |w_k|, the
+    bound vw4.h states."""
+    N, K, M, q, s, ts, w, A, cols = _mixed_stage_case(tiny_exp)
+    gpu = gemm_gpu("nvfp4", q, s, ts, A).cpu().numpy()
+    ref, bnd = oracle.gemm_w4(oracle.FMT_NVFP4, N, K, q, s, ts, A)
+    a = np.array([[oracle.bf16(int(b)) for b in row] for row in A])
+    amax = np.abs(a).reshape(M, K // 256, 256).max(axis=2)          # [M, stages]
+    amax_k = np.repeat(amax, 256, axis=1)                            # [M, K]
+    extra = 2.0 ** -39 * (amax_k @ np.abs(w).T)                      # [M, N]
+    err = np.abs(gpu.astype(np.float64) - ref)
+    assert np.all(err <= 1e-3 * bnd + extra), float(np.max(err - 1e-3 * bnd - extra))

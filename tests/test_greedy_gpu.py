@@ -151,3 +151,44 @@ def test_verify_greedy_bad_draft_ids():
     assert vw4.vw4_get_device_status() & vw4.DEV_BAD_DRAFT_ID
     rt, rl, _ = oracle.accept_greedy(lg, drafts)
     assert np.array_equal(tok.cpu().numpy(), rt) and np.array_equal(ln.cpu().numpy(), rl)
+
+
+def test_verify_greedy_lm_head_full_size():
+    """LM-head verify + fused accept at its full size, through the timed path:
+    W 5376 -> 262144 nvfp4 N(0, 0.02), M = 8 bf16 hidden rows (B = 1, 7
+    drafts), drafts agreeing with the oracle's fp64 argmax with probability
+    0.8 (seeded).  verify_greedy_w4 runs the GEMM, the row argmax and the
+    greedy accept in one launch; the committed run must equal the oracle's
+    greedy accept over the GPU's own fp32 logits (which the same call writes),
+    every logit must be within 1e-3 * sum|a*w| of the oracle's fp64 value, and
+    the GPU argmax of each row must be the fp64 one unless the two lie within
+    the GEMM error bound of each other (a tie within tolerance)."""
+    N, K, B, Kd = 262144, 5376, 1, 7
+    M = B * (Kd + 1)
+    q, s, ts = synth.linear(2, N, K, "nvfp4")
+    A = synth.activations(synth.rng(2), M, K)
+    ref, bnd = oracle.gemm_w4(oracle.FMT_NVFP4, N, K, q, s, ts, A)   # fp64, every column
+    ref_am = np.array([int(np.argmax(ref[m])) for m in range(M)])
+    drafts = synth.greedy_drafts(synth.rng(333), ref_am[None, :Kd], N)
+    qd, sd = torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda()
+    Ad = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16).cuda()
+    d = torch.from_numpy(np.ascontiguousarray(drafts, np.int32)).cuda()
+    logits = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    tok, ln = vw4.verify_greedy_w4(vw4.FMT_NVFP4, qd, sd, ts, Ad, d, out=logits)
+    tok2, ln2 = vw4.verify_greedy_w4(vw4.FMT_NVFP4, qd, sd, ts, Ad, d)   # no logits written
+    torch.cuda.synchronize()
+    assert vw4.vw4_get_device_status() == 0
+    lg = logits.cpu().numpy()
+    tok, ln = tok.cpu().numpy(), ln.cpu().numpy()
+    rt, rl, _ = oracle.accept_greedy(lg.reshape(B, Kd + 1, N), drafts)
+    assert np.array_equal(tok, rt) and np.array_equal(ln, rl), (tok, rt, ln, rl)
+    assert np.array_equal(tok2.cpu().numpy(), rt) and np.array_equal(ln2.cpu().numpy(), rl)
+    err = np.abs(lg.astype(np.float64) - ref)
+    assert np.all(err <= 1e-3 * bnd), float(np.max(err / bnd))
+    for m in range(M):
+        g = oracle.argmax_f32(lg[m])
+        if g != ref_am[m]:
+            gap = ref[m, ref_am[m]] - ref[m, g]
+            assert gap <= 2e-3 * max(bnd[m, ref_am[m]], bnd[m, g]), (m, g, ref_am[m], gap)
+    # the accept agreed with at least the drafts that match the GPU argmax
+    assert 1 <= ln[0] <= Kd + 1

@@ -135,12 +135,15 @@ def test_bad_draft_ids_set_status():
 @pytest.mark.parametrize("Kd", [1, 2, 4, 8])
 def test_stochastic_sweep_full_size_sampled(Kd):
     """Vocab 151936, 256 sequences, fp32 N(0,3) target, draft = target + N(0,1),
-    T = 0.6, top_p = 0.95, Philox seed 4: all sequences on the GPU, a sample
-    of them through the oracle (same counter indices)."""
+    T = 0.6, top_p = 0.95, Philox seed 4: all sequences on the GPU, at least
+    32 of them through the oracle (same counter indices)."""
     B, V = 256, 151936
     target, draft, drafts = synth.stochastic_case(40 + Kd, B, Kd, V)
     tok, ln = gpu_accept(target, draft, drafts, 0.6, 0.95, 4, 0)
-    for b in (0, 1, 77, 128, 200, 255):
+    fixed = np.array([0, 1, 77, 128, 200, 255])
+    rest = np.setdiff1d(np.arange(B), fixed)
+    picks = np.sort(np.concatenate([fixed, synth.rng(900 + Kd).choice(rest, 26, replace=False)]))
+    for b in picks:
         rt, rl, _ = oracle.accept_rejection(target[b:b + 1], draft[b:b + 1], drafts[b:b + 1],
                                             0.6, 0.95, 4, 0, b_base=b)
         assert rl[0] == ln[b] and np.array_equal(rt[0], tok[b]), (b, rt, tok[b])
@@ -179,3 +182,36 @@ def test_top_k_cut_inside_ties(V):
                                             min_p=min_p)
         assert np.array_equal(ln, rl), (top_k, min_p, ln, rl)
         assert np.array_equal(tok, rt), (top_k, min_p)
+
+
+def test_row_records_match_oracle_every_row_full_size():
+    """The row kernel's record of every row of the K = 1 sweep (vocab 151936,
+    256 sequences: 768 target and draft rows), element by element against the
+    oracle: the row max, the kept sum S, and the kept set that (tau, cut)
+    describe -- exactly the entries the oracle's top-p cut keeps."""
+    B, Kd, V = 256, 1, 151936
+    target, draft, drafts = synth.stochastic_case(41, B, Kd, V)
+    ws = vw4.Workspace()
+    t = torch.from_numpy(target).cuda()
+    d = torch.from_numpy(draft).cuda()
+    x = torch.from_numpy(drafts).cuda()
+    vw4.accept_rejection(t, d, x, 0.6, 0.95, 4, 0, workspace=ws)
+    rec = vw4.vw4_rejection_row_records(ws, B, Kd, V).cpu().numpy()
+    rec = rec.reshape(-1).view(np.dtype(vw4.ROW_RECORD_DTYPE))
+    assert vw4.vw4_get_device_status() == 0
+    rows = [target[b, i] for b in range(B) for i in range(Kd + 1)] + \
+           [draft[b, i] for b in range(B) for i in range(Kd)]
+    assert len(rows) == len(rec)
+    idx = np.arange(V)
+    for r, row in enumerate(rows):
+        W, S = oracle.row_mass(row, 0.6, 0.95)
+        W_all, _ = oracle.row_mass(row, 0.6, 1.0)      # every mass before the cut
+        g = rec[r]
+        assert g["max"] == row.max(), (r, g["max"], row.max())
+        assert int(g["kept_sum"]) == S, (r, int(g["kept_sum"]), S)
+        assert g["topk_key"] == 0 and g["topk_idx"] == 0x7FFFFFFF
+        tau, cut = int(g["tau"]), int(g["cut"])
+        kept_gpu = (W_all > tau) | ((W_all == tau) & (idx <= cut))
+        kept_ref = W > 0
+        assert np.array_equal(kept_gpu, kept_ref), (r, tau, cut, np.flatnonzero(kept_gpu ^ kept_ref)[:5])
+        assert int(W_all[kept_gpu].sum()) == S

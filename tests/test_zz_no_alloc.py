@@ -54,6 +54,30 @@ def test_noalloc_matches_workspace_entry_point_twice(fmt, N, K, M):
         assert not np.isnan(got).any()
 
 
+def test_noalloc_fused_argmax_twice():
+    """The fused row argmax through the fixed scratch array (its per-row keys
+    and ticket live there): two calls in a row, M = 16 and N = 40000, each
+    argmax bit-exact against the argmax of the workspace entry point's own
+    output (ties to the lowest index)."""
+    N, K, M = 40000, 512, 16
+    q, s, ts = synth.linear(77, N, K, "nvfp4")
+    qd, sd = torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda()
+    W = vw4.make_weight(vw4.FMT_NVFP4, qd, sd, ts, N, K)
+    for call in range(2):
+        Ad = bf16_dev(synth.activations(synth.rng(60 + call), M, K))
+        ref_am = torch.full((M,), -1, dtype=torch.int32, device="cuda")
+        ref_out = vw4.verify_gemm_w4(vw4.FMT_NVFP4, qd, sd, ts, Ad, row_argmax=ref_am)
+        out = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        am = torch.full((M,), -1, dtype=torch.int32, device="cuda")
+        _call_noalloc(W, Ad, out, row_argmax=am)
+        torch.cuda.synchronize()
+        assert vw4.vw4_get_device_status() == 0
+        want = np.argmax(ref_out.cpu().numpy(), axis=1)
+        assert np.array_equal(am.cpu().numpy(), want), (call, am.cpu().numpy(), want)
+        assert torch.equal(am, ref_am)
+        assert torch.equal(out, ref_out)   # same kernel, same split: the same sums
+
+
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     lib = vw4.load_library()
     W = vw4.Weight(vw4.FMT_NVFP4, 2048, 1 << 20, 0, 0x1000, 0x2000, 1.0, 0.0)  # K = 1M: too big
