@@ -197,6 +197,10 @@ def run_ours(args, rank, world, device):
 
     torch.cuda.set_device(device)
     layers = {"nvfp4": make_layer("nvfp4", device), "q4_0": make_layer("q4_0", device)}
+    # a second copy of the nvfp4 layer: the headline alternates the two, so
+    # that 383 MB of weights (more than twice the 129 MB L2) pass per two steps
+    layer_b = [(name, N, K, qd.clone(), sd.clone(), ts) for (name, N, K, qd, sd, ts) in
+               layers["nvfp4"]]
     acts = {M: make_acts(M, device, seed=7 + M) for M in PER_M}
     outs = {M: [torch.empty((M, N), dtype=torch.float32, device=device) for _, N, _ in STEP]
             for M in PER_M}
@@ -205,8 +209,8 @@ def run_ours(args, rank, world, device):
                for _, N, K in STEP + LAYER))
     FMTS = {"nvfp4": vw4.FMT_NVFP4, "q4_0": vw4.FMT_Q4_0}
 
-    def one_step(fmt, M):
-        for j, (name, N, K, qd, sd, ts) in enumerate(layers[fmt]):
+    def one_step(fmt, M, layer=None):
+        for j, (name, N, K, qd, sd, ts) in enumerate(layer or layers[fmt]):
             vw4.verify_gemm_w4(FMTS[fmt], qd, sd, ts, acts[M][j], out=outs[M][j], workspace=ws)
 
     def capture(fn, warm=3):
@@ -223,17 +227,19 @@ def run_ours(args, rank, world, device):
         if world > 1:
             torch.distributed.barrier()
 
-    def time_graph(g, reps, warmup):
-        for _ in range(warmup):
-            g.replay()
+    def time_graph(g, reps, warmup, g_alt=None):
+        """ms for reps replays (alternating g and g_alt when given)."""
+        seq = [g, g_alt] if g_alt is not None else [g]
+        for i in range(warmup):
+            seq[i % len(seq)].replay()
         torch.cuda.synchronize()
         barrier()
         torch.cuda.synchronize()
         stream = torch.cuda.current_stream()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(reps):
-            g.replay()
+        for i in range(reps):
+            seq[i % len(seq)].replay()
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
@@ -261,12 +267,14 @@ def run_ours(args, rank, world, device):
         # headline: one step = the packed layer at M = 8 (a CUDA graph of the
         # four C-ABI calls, replayed K times back to back)
         g_head = capture(lambda: one_step("nvfp4", HEAD_M))
+        g_head_b = capture(lambda: one_step("nvfp4", HEAD_M, layer_b))
         soak_end = time.time() + 0.4
         while time.time() < soak_end:      # let the clock sampler see the load
-            for _ in range(20):
+            for _ in range(10):
                 g_head.replay()
+                g_head_b.replay()
             torch.cuda.synchronize()
-        ms = time_graph(g_head, steps, warmup)
+        ms = time_graph(g_head, steps, warmup, g_head_b)
         ms_max = reduce_max(ms, world)
         ms_per_step = ms_max / steps
         value = step_bytes(HEAD_M) * steps * world / (ms_max * 1e-3) / 1e9
@@ -310,6 +318,9 @@ def run_ours(args, rank, world, device):
         del lay7
         torch.cuda.empty_cache()
 
+    stream = torch.cuda.current_stream()
+    accept = run_accept_timings(device, stream)
+    heads = run_head_timings(device, stream)
     gate = {}
     for name in ("qkv", "o", "gate_up", "down"):
         t1 = per_m["nvfp4"]["1"]["call_us"][name]
@@ -319,6 +330,14 @@ def run_ours(args, rank, world, device):
         gate[name] = {"m8_over_m1": round(t8 / t1, 3), "m8_gbs": round(gbs, 1),
                       "frac_of_8tbs": round(gbs / SPEC_HBM_GBS, 3),
                       "frac_of_measured_copy": round(gbs / peak, 3)}
+
+    lm = heads.get("lmhead_per_m") if isinstance(heads, dict) else None
+    if lm:
+        t1, t8 = lm["1"]["us"], lm["8"]["us"]
+        gbs = lm["8"]["gbs"]
+        gate["lm_head"] = {"m8_over_m1": round(t8 / t1, 3), "m8_gbs": gbs,
+                           "frac_of_8tbs": round(gbs / SPEC_HBM_GBS, 3),
+                           "frac_of_measured_copy": round(gbs / peak, 3)}
 
     # roofline of the GEMM: algorithmic bytes of the step's calls at M = 8 over
     # their times, each call timed alone (graph replay, CUDA events)
@@ -333,9 +352,6 @@ def run_ours(args, rank, world, device):
 
     depth = depth_controller_summary(per_m)
 
-    stream = torch.cuda.current_stream()
-    accept = run_accept_timings(device, stream)
-    heads = run_head_timings(device, stream)
     e2e = run_e2e(vw4, layers["nvfp4"], device, stream, steps, warmup, world)
 
     result = {
@@ -346,8 +362,10 @@ def run_ours(args, rank, world, device):
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": HEAD_M, "fmt": "nvfp4",
                    "bytes_per_step": step_bytes(HEAD_M),
-                   "l2": "inputs larger than L2: 191.7 MB of weights+scales per step vs 129 MB L2",
-                   "timing": "CUDA graph of the step's 4 C-ABI calls, replayed back to back",
+                   "l2": "inputs larger than L2: 191.7 MB of weights+scales per step, two "
+                         "weight copies alternating (383 MB per two steps) vs 129 MB L2",
+                   "timing": "CUDA graphs of the step's 4 C-ABI calls on the two weight copies, "
+                             "replayed alternately back to back",
                    "parallelism": f"replicas x{world}"},
         "per_m": per_m, "unpacked_7_calls": unpacked, "gate": gate, "accept_us": accept,
         "depth_controller": depth,
@@ -585,7 +603,75 @@ def run_head_timings(device, stream):
     us = timed(head1, 10)
     out["lmhead_fused_greedy_m8"] = {"us": round(us, 2), "gbs": round(hb / (us * 1e-6) / 1e9, 1),
                                      "what": "verify_greedy_w4: one launch, no logits written"}
-    del heads, logits
+
+    # the LM head alone at each verify width (logits written, two weight
+    # copies alternating: 1.58 GB, far above L2)
+    lm_per_m = {}
+    Ahs = {M: torch.from_numpy(synth.activations(synth.rng(230 + M), M, K).view(np.int16)).view(
+        torch.bfloat16).to(device) for M in PER_M}
+    lgs = {M: torch.empty((M, V), dtype=torch.float32, device=device) for M in PER_M}
+    for M in PER_M:
+        def lm(c, M=M):
+            vw4.verify_gemm_w4(vw4.FMT_NVFP4, *heads[c], Ahs[M], out=lgs[M], workspace=ws,
+                               stream=stream)
+        us = timed(lm, 10)
+        b = weight_bytes(V, K) + M * K * 2
+        lm_per_m[str(M)] = {"us": round(us, 2), "gbs": round(b / (us * 1e-6) / 1e9, 1)}
+    out["lmhead_per_m"] = lm_per_m
+    del lgs
+
+    # the sampled accept fed by the LM-head GEMM (B = 1 sequence, 7 drafts,
+    # T = 0.6, top_p = 0.95): the verify GEMM's 8 rows, then the rejection
+    # accept against the 7 draft rows (made once, by the same head, as a
+    # drafter sharing it would).  Unfused: verify_gemm_w4 + accept_rejection;
+    # fused: verify_gemm_w4_blockmax (logits and the maximum of every 16) +
+    # accept_rejection_blockmax (no pass over the rows for their maxima).
+    Kd = 7
+    Ad7 = torch.from_numpy(synth.activations(synth.rng(240), Kd, K).view(np.int16)).view(
+        torch.bfloat16).to(device)
+    dlog, dbm = vw4.verify_gemm_w4_blockmax(vw4.FMT_NVFP4, *heads[0], Ad7, workspace=ws,
+                                            stream=stream)
+    torch.cuda.synchronize()
+    g7 = torch.Generator(device=device).manual_seed(5)
+    sd_drafts = torch.multinomial(torch.softmax(dlog / 0.6, dim=-1), 1, generator=g7).reshape(
+        1, Kd).to(torch.int32)
+    tlog = torch.empty((Kd + 1, V), dtype=torch.float32, device=device)
+    tbm = torch.empty((Kd + 1, (V + 15) // 16), dtype=torch.float32, device=device)
+    ws_acc = vw4.Workspace(device)
+    tok_s = torch.empty((1, Kd + 1), dtype=torch.int32, device=device)
+    len_s = torch.empty((1,), dtype=torch.int32, device=device)
+
+    def sampled(c):
+        vw4.verify_gemm_w4(vw4.FMT_NVFP4, *heads[c], Ah, out=tlog, workspace=ws, stream=stream)
+        vw4.accept_rejection(tlog.view(1, Kd + 1, V), dlog.view(1, Kd, V), sd_drafts, 0.6, 0.95, 4,
+                             c, tokens=tok_s, length=len_s, workspace=ws_acc, stream=stream)
+
+    def sampled_fused(c):
+        vw4.verify_gemm_w4_blockmax(vw4.FMT_NVFP4, *heads[c], Ah, out=tlog, block_max=tbm,
+                                    workspace=ws, stream=stream)
+        vw4.accept_rejection_blockmax(tlog.view(1, Kd + 1, V), tbm, dlog.view(1, Kd, V), dbm,
+                                      sd_drafts, 0.6, 0.95, 4, c, tokens=tok_s, length=len_s,
+                                      workspace=ws_acc, stream=stream)
+
+    def accept_only(c):
+        vw4.accept_rejection(tlog.view(1, Kd + 1, V), dlog.view(1, Kd, V), sd_drafts, 0.6, 0.95, 4,
+                             c, tokens=tok_s, length=len_s, workspace=ws_acc, stream=stream)
+
+    def accept_only_fused(c):
+        vw4.accept_rejection_blockmax(tlog.view(1, Kd + 1, V), tbm, dlog.view(1, Kd, V), dbm,
+                                      sd_drafts, 0.6, 0.95, 4, c, tokens=tok_s, length=len_s,
+                                      workspace=ws_acc, stream=stream)
+
+    us_u = timed(sampled, 10)
+    us_f = timed(sampled_fused, 10)
+    us_a = timed(accept_only, 10)
+    us_af = timed(accept_only_fused, 10)
+    out["lmhead_sampled_accept_m8"] = {
+        "unfused_us": round(us_u, 2), "fused_us": round(us_f, 2),
+        "accept_alone_us": round(us_a, 2), "accept_alone_fused_us": round(us_af, 2),
+        "what": "B=1, 7 drafts, V=262144, T=0.6, top_p=0.95: verify_gemm_w4 + accept_rejection "
+                "vs verify_gemm_w4_blockmax + accept_rejection_blockmax"}
+    del heads, logits, tlog, dlog
     torch.cuda.empty_cache()
     return out
 

@@ -10,6 +10,10 @@
  *    copied and nothing is freed.  The library never allocates device memory
  *    in a call: scratch comes from the caller's workspace (sized by
  *    vw4_workspace_bytes) or is not needed.
+ *  - A workspace needs no initialization: every call sets up what it reads
+ *    (the verify GEMM clears its own counters at the start of each launch),
+ *    so one workspace, sized for the largest use, may serve every entry
+ *    point, one call after another on the same stream.
  *  - `stream` is a cudaStream_t (0 = the legacy default stream).  Every call
  *    is asynchronous on it; no call synchronizes except vw4_get_device_status.
  *  - Argument errors are detected on the host, before anything is launched,
@@ -150,6 +154,31 @@ VW4_API vw4_status verify_gemm_w4(const vw4_weight* W, const void* A_dev, int M,
                                   void* workspace_dev, size_t ws_bytes, void* stream);
 
 /*
+ * verify_gemm_w4_blockmax -- verify_gemm_w4 that also hands the logits' block
+ * maxima to the sampled accept.
+ *
+ * Defined by: "Faster Gemma 4 on MLX with multi-token prediction" (drafting,
+ * sampling and verification run on the GPU as one pass, with no return to
+ * the CPU) and Ollama's mtp.go commit log paragraph "rework the MLX sampler"
+ * (the acceptance, residual and bonus draws reuse the target distribution):
+ * the verify GEMM already holds every logit of a row in registers, so it
+ * writes the row's maximum over every 16 consecutive outputs next to the
+ * logits, and accept_rejection_blockmax takes the row max and its segment
+ * maxima from them instead of reading the full rows for them.
+ *
+ * W, A_dev, M, lda, out_dev, ldo, workspace  as verify_gemm_w4 (out_dev is
+ *             required).
+ * block_max_dev  fp32 [M][ceil(N / 16)]: element (m, j) = the largest of
+ *             out[m][16 j .. min(16 j + 16, N)), NaN read as -infinity, +0
+ *             over -0.  4-byte aligned.
+ * Errors as verify_gemm_w4; VW4_ERR_INVALID_ARG when block_max_dev or out_dev
+ * is NULL.
+ */
+VW4_API vw4_status verify_gemm_w4_blockmax(const vw4_weight* W, const void* A_dev, int M,
+                                           int lda, float* out_dev, int ldo, float* block_max_dev,
+                                           void* workspace_dev, size_t ws_bytes, void* stream);
+
+/*
  * verify_greedy_w4 -- the verify GEMM, its row argmax and the greedy accept
  * in one launch.
  *
@@ -276,6 +305,35 @@ VW4_API vw4_status accept_rejection(const float* target_logits_dev, const float*
                                     const vw4_sampling* params, uint64_t seed, uint64_t offset,
                                     int32_t* tokens_dev, int32_t* len_dev, void* workspace_dev,
                                     size_t ws_bytes, void* stream);
+
+/*
+ * accept_rejection_blockmax -- accept_rejection fed by the verify GEMM's
+ * block maxima.
+ *
+ * Defined by: the passages of accept_rejection, with the fusion of
+ * verify_gemm_w4_blockmax ("Faster Gemma 4 on MLX with multi-token
+ * prediction": sampling and verification in one pass on the GPU).
+ *
+ * The arguments of accept_rejection, plus the block maxima of every logits
+ * row as verify_gemm_w4_blockmax writes them:
+ * target_bmax_dev  fp32 [B][Kd+1][ceil(V / 16)];
+ * draft_bmax_dev   fp32 [B][Kd][ceil(V / 16)] (NULL when Kd == 0).
+ * The first pass of the accept, which reads every logit for the row max and
+ * the maxima of its 128-entry segments, takes them from these arrays instead.
+ * The committed ids and lengths are those of accept_rejection on the same
+ * logits, for every row whose NaN entries (if any) lie elsewhere than at
+ * index 0.  Errors as accept_rejection; VW4_ERR_INVALID_ARG for a NULL
+ * block-max array that is needed.
+ */
+VW4_API vw4_status accept_rejection_blockmax(const float* target_logits_dev,
+                                             const float* target_bmax_dev,
+                                             const float* draft_logits_dev,
+                                             const float* draft_bmax_dev,
+                                             const int32_t* drafts_dev, int B, int Kd, int V,
+                                             const vw4_sampling* params, uint64_t seed,
+                                             uint64_t offset, int32_t* tokens_dev,
+                                             int32_t* len_dev, void* workspace_dev,
+                                             size_t ws_bytes, void* stream);
 
 /*
  * accept_rejection_topk -- accept_rejection over rows kept as top-k lists.

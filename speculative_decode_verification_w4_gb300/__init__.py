@@ -47,7 +47,7 @@ EXPORTS = ("verify_gemm_w4", "verify_moe_w4", "accept_greedy", "accept_rejection
            "vw4_own_exp", "verify_gemm_w4_noalloc", "verify_greedy_w4", "vw4_depth_ctl_init",
            "vw4_depth_ctl_observe", "vw4_depth_ctl_expected", "vw4_depth_ctl_choose",
            "accept_rejection_topk", "vw4_rejection_row_records",
-           "vw4_test_inject_stall")
+           "vw4_test_inject_stall", "verify_gemm_w4_blockmax", "accept_rejection_blockmax")
 
 
 class VW4Error(RuntimeError):
@@ -122,6 +122,10 @@ def load_library(path: str = LIB_PATH):
                                      ctypes.c_size_t, P]),
             "vw4_rejection_row_records": (I, [P, ctypes.c_size_t, I, I, I, P, P]),
             "vw4_test_inject_stall": (None, [I]),
+            "verify_gemm_w4_blockmax": (I, [ctypes.POINTER(Weight), P, I, I, P, I, P, P,
+                                            ctypes.c_size_t, P]),
+            "accept_rejection_blockmax": (I, [P, P, P, P, P, I, I, I, ctypes.POINTER(Sampling),
+                                              U64, U64, P, P, P, ctypes.c_size_t, P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -158,7 +162,9 @@ def vw4_workspace_bytes(op: int, a: int, b: int, c: int) -> int:
 
 
 class Workspace:
-    """A growable device scratch buffer (256-byte aligned torch allocation)."""
+    """A growable device scratch buffer (256-byte aligned torch allocation),
+    zero-filled when allocated as the library requires of a fresh workspace
+    (every call leaves it that way)."""
 
     def __init__(self, device=None):
         self.device = torch.device(device or "cuda")
@@ -166,7 +172,7 @@ class Workspace:
 
     def get(self, nbytes: int) -> torch.Tensor:
         if self.buf is None or self.buf.numel() < nbytes:
-            self.buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+            self.buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=self.device)
         return self.buf
 
 
@@ -211,6 +217,31 @@ def verify_gemm_w4(fmt: int, q: torch.Tensor, scales: torch.Tensor, tensor_scale
                                          ws.numel(), _stream(stream))
     _check(code, "verify_gemm_w4")
     return out
+
+
+def verify_gemm_w4_blockmax(fmt: int, q: torch.Tensor, scales: torch.Tensor,
+                            tensor_scale: float, A: torch.Tensor, out: torch.Tensor | None = None,
+                            block_max: torch.Tensor | None = None, workspace=None, stream=None):
+    """verify_gemm_w4 that also writes block_max fp32 [M, ceil(N/16)], the
+    largest of every 16 consecutive outputs of each row -> (out, block_max)."""
+    N, K = q.shape[0], q.shape[1] * 2
+    M = A.shape[0]
+    if A.dtype != torch.bfloat16:
+        raise ValueError("A must be bfloat16")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    nb = (N + 15) // 16
+    if block_max is None:
+        block_max = torch.empty((M, nb), dtype=torch.float32, device=A.device)
+    if block_max.stride(0) != nb or block_max.stride(1) != 1:
+        raise ValueError("block_max must be a contiguous [M, ceil(N/16)] tensor")
+    W = make_weight(fmt, q, scales, tensor_scale, N, K)
+    ws = _workspace(workspace, vw4_workspace_bytes(OP_GEMM, M, N, K), A.device)
+    code = load_library().verify_gemm_w4_blockmax(ctypes.byref(W), _ptr(A), M, A.stride(0),
+                                                  _ptr(out), out.stride(0), _ptr(block_max),
+                                                  _ptr(ws), ws.numel(), _stream(stream))
+    _check(code, "verify_gemm_w4_blockmax")
+    return out, block_max
 
 
 def verify_greedy_w4(fmt: int, q: torch.Tensor, scales: torch.Tensor, tensor_scale: float,
@@ -284,7 +315,7 @@ class PreparedGemm:
         self.N, self.K = q.shape[0], q.shape[1] * 2
         self.W = make_weight(fmt, q, scales, tensor_scale, self.N, self.K)
         need = vw4_workspace_bytes(OP_GEMM, M_max, self.N, self.K)
-        self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+        self.ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=q.device)
         self.ws_ptr, self.ws_bytes = self.ws.data_ptr(), self.ws.numel()
         self.stream = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
         self._fn = load_library().verify_gemm_w4
@@ -379,6 +410,33 @@ def accept_rejection(target_logits: torch.Tensor, draft_logits: torch.Tensor | N
                                            _ptr(tokens), _ptr(length), _ptr(ws), ws.numel(),
                                            _stream(stream))
     _check(code, "accept_rejection")
+    return tokens, length
+
+
+def accept_rejection_blockmax(target_logits: torch.Tensor, target_bmax: torch.Tensor,
+                              draft_logits: torch.Tensor | None, draft_bmax: torch.Tensor | None,
+                              drafts: torch.Tensor, temperature: float, top_p: float, seed: int,
+                              offset: int = 0, top_k: int = 0, min_p: float = 0.0, tokens=None,
+                              length=None, workspace=None, stream=None):
+    """accept_rejection with the block maxima of every logits row (as
+    verify_gemm_w4_blockmax writes them) -> (tokens [B, Kd+1], len [B])."""
+    B, R, V = target_logits.shape
+    Kd = R - 1
+    nb = (V + 15) // 16
+    if target_bmax.numel() != B * R * nb or (Kd and draft_bmax.numel() != B * Kd * nb):
+        raise ValueError("block maxima must be [B, rows, ceil(V/16)]")
+    dev = target_logits.device
+    if tokens is None:
+        tokens = torch.empty((B, Kd + 1), dtype=torch.int32, device=dev)
+    if length is None:
+        length = torch.empty((B,), dtype=torch.int32, device=dev)
+    prm = Sampling(float(temperature), float(top_p), int(top_k), float(min_p))
+    ws = _workspace(workspace, vw4_workspace_bytes(OP_REJECTION, B, Kd, V), dev)
+    code = load_library().accept_rejection_blockmax(
+        _ptr(target_logits), _ptr(target_bmax), _ptr(draft_logits), _ptr(draft_bmax),
+        _ptr(drafts), B, Kd, V, ctypes.byref(prm), int(seed), int(offset), _ptr(tokens),
+        _ptr(length), _ptr(ws), ws.numel(), _stream(stream))
+    _check(code, "accept_rejection_blockmax")
     return tokens, length
 
 

@@ -219,15 +219,16 @@ struct GreedyArgs {
 };
 
 static vw4_status gemm_entry(const vw4_weight* W, const void* A_dev, int M, int lda,
-                             float* out_dev, int ldo, int32_t* row_argmax_dev,
-                             const GreedyArgs* greedy, void* workspace_dev, size_t ws_bytes,
-                             void* stream) {
+                             float* out_dev, int ldo, int32_t* row_argmax_dev, float* bmax_dev,
+                             int ldb, const GreedyArgs* greedy, void* workspace_dev,
+                             size_t ws_bytes, void* stream) {
     vw4_status st = check_weight(W);
     if (st != VW4_OK) return st;
     if (!A_dev || (!out_dev && !greedy)) return VW4_ERR_INVALID_ARG;
     if (M < 1 || M > kMaxVerifyRows || lda < W->K || (out_dev && ldo < W->N))
         return VW4_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(A_dev) & 1u) || (reinterpret_cast<uintptr_t>(out_dev) & 3u))
+    if ((reinterpret_cast<uintptr_t>(A_dev) & 1u) || (reinterpret_cast<uintptr_t>(out_dev) & 3u) ||
+        (reinterpret_cast<uintptr_t>(bmax_dev) & 3u))
         return VW4_ERR_ALIGN;
     if (!workspace_dev) return VW4_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace_dev) & 255u) != 0) return VW4_ERR_ALIGN;
@@ -270,10 +271,11 @@ static vw4_status gemm_entry(const vw4_weight* W, const void* A_dev, int M, int 
         G = n_tiles * S;
     }
     if (G > U) G = U;
-    // Up to kMaxClusterSplit parts (and no fused argmax): the parts of a tile
-    // form one cluster and combine over distributed shared memory.
+    // Up to kMaxClusterSplit parts (and no fused reduction): the parts of a
+    // tile form one cluster and combine over distributed shared memory.
     const bool fused_argmax = row_argmax_dev != nullptr || greedy != nullptr;
-    const bool clustered = split > 1 && split <= kMaxClusterSplit && !fused_argmax;
+    const bool clustered =
+        split > 1 && split <= kMaxClusterSplit && !fused_argmax && bmax_dev == nullptr;
 
     cudaError_t e = launch_prep_act(static_cast<const uint16_t*>(A_dev), lda, K, W->fmt, M, 0, 1,
                                     1, ws, n_tiles * kConsumerWarps, s, nr);
@@ -297,6 +299,8 @@ static vw4_status gemm_entry(const vw4_weight* W, const void* A_dev, int M, int 
     p.am_key = ws.am_key;
     p.am_cnt = ws.am_cnt;
     p.row_argmax = row_argmax_dev;
+    p.bmax = bmax_dev;
+    p.ldb = ldb;
     p.status = d->status;
     p.wait_ns = g_wait_ns;
     p.cluster = clustered ? 1 : 0;
@@ -316,7 +320,16 @@ static vw4_status gemm_entry(const vw4_weight* W, const void* A_dev, int M, int 
 VW4_API vw4_status verify_gemm_w4(const vw4_weight* W, const void* A_dev, int M, int lda,
                                   float* out_dev, int ldo, int32_t* row_argmax_dev,
                                   void* workspace_dev, size_t ws_bytes, void* stream) {
-    return gemm_entry(W, A_dev, M, lda, out_dev, ldo, row_argmax_dev, nullptr, workspace_dev,
+    return gemm_entry(W, A_dev, M, lda, out_dev, ldo, row_argmax_dev, nullptr, 0, nullptr,
+                      workspace_dev, ws_bytes, stream);
+}
+
+VW4_API vw4_status verify_gemm_w4_blockmax(const vw4_weight* W, const void* A_dev, int M,
+                                           int lda, float* out_dev, int ldo, float* block_max_dev,
+                                           void* workspace_dev, size_t ws_bytes, void* stream) {
+    if (!block_max_dev || !out_dev || !W || W->N < 1) return VW4_ERR_INVALID_ARG;
+    return gemm_entry(W, A_dev, M, lda, out_dev, ldo, nullptr, block_max_dev,
+                      (W->N + kBlockMaxRows - 1) / kBlockMaxRows, nullptr, workspace_dev,
                       ws_bytes, stream);
 }
 
@@ -327,8 +340,8 @@ VW4_API vw4_status verify_greedy_w4(const vw4_weight* W, const void* A_dev, int 
     if (B < 1 || Kd < 0 || B * (Kd + 1) > kMaxVerifyRows) return VW4_ERR_INVALID_ARG;
     if (!tokens_dev || !len_dev || (Kd > 0 && !drafts_dev)) return VW4_ERR_INVALID_ARG;
     const GreedyArgs g{drafts_dev, B, Kd, tokens_dev, len_dev};
-    return gemm_entry(W, A_dev, B * (Kd + 1), lda, out_dev, ldo, nullptr, &g, workspace_dev,
-                      ws_bytes, stream);
+    return gemm_entry(W, A_dev, B * (Kd + 1), lda, out_dev, ldo, nullptr, nullptr, 0, &g,
+                      workspace_dev, ws_bytes, stream);
 }
 
 VW4_API vw4_status verify_moe_w4(const vw4_weight* experts, int E, const void* A_dev, int lda,
@@ -432,11 +445,12 @@ VW4_API vw4_status accept_greedy(const float* target_logits_dev, const int32_t* 
     return VW4_OK;
 }
 
-VW4_API vw4_status accept_rejection(const float* target_logits_dev, const float* draft_logits_dev,
-                                    const int32_t* drafts_dev, int B, int Kd, int V,
-                                    const vw4_sampling* params, uint64_t seed, uint64_t offset,
-                                    int32_t* tokens_dev, int32_t* len_dev, void* workspace_dev,
-                                    size_t ws_bytes, void* stream) {
+static vw4_status rejection_entry(const float* target_logits_dev, const float* target_bmax_dev,
+                                  const float* draft_logits_dev, const float* draft_bmax_dev,
+                                  const int32_t* drafts_dev, int B, int Kd, int V,
+                                  const vw4_sampling* params, uint64_t seed, uint64_t offset,
+                                  int32_t* tokens_dev, int32_t* len_dev, void* workspace_dev,
+                                  size_t ws_bytes, void* stream) {
     if (!params || !target_logits_dev || !tokens_dev || !len_dev) return VW4_ERR_INVALID_ARG;
     if (B < 1 || Kd < 0 || Kd > kMaxRows || V < 1 || V > (1 << 24)) return VW4_ERR_INVALID_ARG;
     if (Kd > 0 && (!drafts_dev || !draft_logits_dev)) return VW4_ERR_INVALID_ARG;
@@ -468,10 +482,36 @@ VW4_API vw4_status accept_rejection(const float* target_logits_dev, const float*
                                             V, invT, P, params->top_k, MP, seed, offset,
                                             tokens_dev, len_dev,
                                             workspace_dev, ws_bytes, d->status, g_wait_ns,
-                                            static_cast<cudaStream_t>(stream));
+                                            static_cast<cudaStream_t>(stream), target_bmax_dev,
+                                            Kd > 0 ? draft_bmax_dev : nullptr);
     if (e == cudaErrorNotSupported) return VW4_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return cuda_fail(e, "accept_rejection launch");
     return VW4_OK;
+}
+
+VW4_API vw4_status accept_rejection(const float* target_logits_dev, const float* draft_logits_dev,
+                                    const int32_t* drafts_dev, int B, int Kd, int V,
+                                    const vw4_sampling* params, uint64_t seed, uint64_t offset,
+                                    int32_t* tokens_dev, int32_t* len_dev, void* workspace_dev,
+                                    size_t ws_bytes, void* stream) {
+    return rejection_entry(target_logits_dev, nullptr, draft_logits_dev, nullptr, drafts_dev, B,
+                           Kd, V, params, seed, offset, tokens_dev, len_dev, workspace_dev,
+                           ws_bytes, stream);
+}
+
+VW4_API vw4_status accept_rejection_blockmax(const float* target_logits_dev,
+                                             const float* target_bmax_dev,
+                                             const float* draft_logits_dev,
+                                             const float* draft_bmax_dev,
+                                             const int32_t* drafts_dev, int B, int Kd, int V,
+                                             const vw4_sampling* params, uint64_t seed,
+                                             uint64_t offset, int32_t* tokens_dev,
+                                             int32_t* len_dev, void* workspace_dev,
+                                             size_t ws_bytes, void* stream) {
+    if (!target_bmax_dev || (Kd > 0 && !draft_bmax_dev)) return VW4_ERR_INVALID_ARG;
+    return rejection_entry(target_logits_dev, target_bmax_dev, draft_logits_dev, draft_bmax_dev,
+                           drafts_dev, B, Kd, V, params, seed, offset, tokens_dev, len_dev,
+                           workspace_dev, ws_bytes, stream);
 }
 
 VW4_API vw4_status accept_rejection_topk(const int32_t* target_ids_dev,

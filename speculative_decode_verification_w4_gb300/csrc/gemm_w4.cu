@@ -81,6 +81,14 @@ __device__ __forceinline__ float pow2f(int n) {  // exact 2^n, n in [-126, 127]
     return __uint_as_float(static_cast<uint32_t>(n + 127) << 23);
 }
 
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependents_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------- prep kernel
 // One warp per (segment, 256-wide k stage, verify row); each lane owns one
 // 16-byte chunk of the stage's fp16 block.  The row's values in the stage are
@@ -536,6 +544,13 @@ __device__ __forceinline__ unsigned long long am_key(float v, uint32_t idx) {
     return (static_cast<unsigned long long>(ord) << 32) | (0xFFFFFFFFu - idx);
 }
 
+// The value of the high half of a key: the value ordered by am_key (NaN
+// read as -inf, -0 as +0).
+__device__ __forceinline__ float key_value(unsigned long long k) {
+    const uint32_t ord = static_cast<uint32_t>(k >> 32);
+    return __uint_as_float((ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord);
+}
+
 __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
     uint32_t old;
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
@@ -622,14 +637,6 @@ __device__ void argmax_finish(const GemmParams& p, int lane) {
     }
 }
 
-__device__ __forceinline__ void grid_dependency_wait() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-__device__ __forceinline__ void grid_dependents_launch() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 // NR verify rows per activation block: 8 (one mma n-tile; dense or MoE) or
 // 16 (two n-tiles over the same unpacked weights; dense calls of 9..16 rows).
 template <int FMT, int NR>
@@ -666,8 +673,10 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     __syncthreads();
 
     const int T = p.T, n_tiles = p.n_tiles;
-    // Dense calls pass the one-segment shape directly; MoE calls read the
-    // router's table, which is complete before this grid's predecessor ran.
+    // Dense calls pass the one-segment shape directly.  MoE calls read the
+    // routing table that the activation prep (this grid's predecessor)
+    // writes: wait for that grid first.
+    if (p.dense_M == 0) grid_dependency_wait();
     const int n_seg = p.dense_M > 0 ? 1 : p.seg->n_seg;
     // Effective grid: never more CTAs than units, so every active CTA owns at
     // least one unit (the contributor arithmetic of split tiles relies on it).
@@ -933,10 +942,13 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         if (whole) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                // argmax keys of verify rows 8nt + 2c and 8nt + 2c + 1
+                // argmax keys of verify rows 8nt + 2c and 8nt + 2c + 1, per
+                // 16-row block and over the warp's 32 rows
                 unsigned long long k0 = 0ull, k1 = 0ull;
+                unsigned long long kr0[kRowBlocks], kr1[kRowBlocks];
 #pragma unroll
                 for (int rb = 0; rb < kRowBlocks; ++rb) {
+                    kr0[rb] = kr1[rb] = 0ull;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const int tok = 8 * nt + 2 * c + (q & 1);
@@ -946,8 +958,29 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                                 p.out[static_cast<size_t>(dest_of(tok)) * p.ldo + n] = v[rb][nt][q];
                             const unsigned long long k =
                                 am_key(v[rb][nt][q], static_cast<uint32_t>(n));
-                            if (q & 1) k1 = umax64(k1, k);
-                            else k0 = umax64(k0, k);
+                            if (q & 1) kr1[rb] = umax64(kr1[rb], k);
+                            else kr0[rb] = umax64(kr0[rb], k);
+                        }
+                    }
+                    k0 = umax64(k0, kr0[rb]);
+                    k1 = umax64(k1, kr1[rb]);
+                }
+                if (p.bmax != nullptr) {
+                    // the largest of each 16 outputs: one block per row block
+#pragma unroll
+                    for (int rb = 0; rb < kRowBlocks; ++rb) {
+#pragma unroll
+                        for (int o = 4; o < 32; o <<= 1) {
+                            kr0[rb] = umax64(kr0[rb], __shfl_xor_sync(0xffffffffu, kr0[rb], o));
+                            kr1[rb] = umax64(kr1[rb], __shfl_xor_sync(0xffffffffu, kr1[rb], o));
+                        }
+                        const int nb0 = n0 + wrow + rb * 16;
+                        const int t0 = 8 * nt + 2 * c;
+                        if (lane < 4 && nb0 < p.N) {  // lane c holds rows 2c, 2c + 1
+                            float* bm = p.bmax + nb0 / kBlockMaxRows;
+                            if (t0 < count) bm[static_cast<size_t>(t0) * p.ldb] = key_value(kr0[rb]);
+                            if (t0 + 1 < count)
+                                bm[static_cast<size_t>(t0 + 1) * p.ldb] = key_value(kr1[rb]);
                         }
                     }
                 }
@@ -1041,7 +1074,8 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                 }
             }
             const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
-            unsigned long long kb = 0ull;
+            // keys of the slice's first and second 16 rows
+            unsigned long long kb0 = 0ull, kb1 = 0ull;
             if (tok < count) {
                 float* orow =
                     p.out != nullptr ? p.out + static_cast<size_t>(dest_of(tok)) * p.ldo : nullptr;
@@ -1050,14 +1084,24 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                     const int n = n0 + rr + (j & 3) + ((j & 4) ? 16 : 0);
                     if (n < p.N) {
                         if (p.out != nullptr) orow[n] = sv[j];
-                        kb = umax64(kb, am_key(sv[j], static_cast<uint32_t>(n)));
+                        const unsigned long long k = am_key(sv[j], static_cast<uint32_t>(n));
+                        if (j & 4) kb1 = umax64(kb1, k);
+                        else kb0 = umax64(kb0, k);
                     }
                 }
             }
-            if (p.argmax_M > 0) {
-                kb = umax64(kb, __shfl_xor_sync(0xffffffffu, kb, 1));
-                kb = umax64(kb, __shfl_xor_sync(0xffffffffu, kb, 2));
-                am_run[nt] = umax64(am_run[nt], kb);  // lanes 4t .. 4t+3 hold row 8nt + t
+            if (p.argmax_M > 0 || p.bmax != nullptr) {
+                kb0 = umax64(kb0, __shfl_xor_sync(0xffffffffu, kb0, 1));
+                kb0 = umax64(kb0, __shfl_xor_sync(0xffffffffu, kb0, 2));
+                kb1 = umax64(kb1, __shfl_xor_sync(0xffffffffu, kb1, 1));
+                kb1 = umax64(kb1, __shfl_xor_sync(0xffffffffu, kb1, 2));
+                // lanes 4t .. 4t+3 hold row 8nt + t
+                am_run[nt] = umax64(am_run[nt], umax64(kb0, kb1));
+                if (p.bmax != nullptr && (lane & 3) == 0 && tok < count) {
+                    float* bm = p.bmax + static_cast<size_t>(tok) * p.ldb;
+                    if (n0 + wrow < p.N) bm[(n0 + wrow) / kBlockMaxRows] = key_value(kb0);
+                    if (n0 + wrow + 16 < p.N) bm[(n0 + wrow + 16) / kBlockMaxRows] = key_value(kb1);
+                }
             }
         }
     }

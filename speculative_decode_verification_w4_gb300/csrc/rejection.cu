@@ -467,6 +467,34 @@ __device__ __forceinline__ void x_window(unsigned long long wlo, unsigned long l
     xb = __logf(static_cast<float>(whi)) - ln2_40 + 1e-3f;
 }
 
+// Blocks of the maxima that a verify GEMM can hand over with its logits: the
+// largest of every 16 consecutive entries of a row (NaN read as -infinity).
+constexpr int kBlockLen = 16;
+static_assert(kSegLen % kBlockLen == 0, "a segment is whole blocks");
+
+// The row's max and segment maxima from its block maxima bm[ceil(V / 16)]
+// instead of the row itself: the same values as the max pass for any row
+// whose NaN entries (which weigh 0) lie elsewhere than index 0.
+__device__ float row_max_from_blocks(const float* __restrict__ bm, int V, float* seg,
+                                     RowSmem& sm) {
+    const int nb = (V + kBlockLen - 1) / kBlockLen;
+    float lmax = -INFINITY;
+    if (seg != nullptr) {
+        constexpr int kPer = kSegLen / kBlockLen;
+        const int nseg = n_segments(V);
+        for (int sg = threadIdx.x; sg < nseg; sg += kRowThreads) {
+            float m = -INFINITY;
+            const int b0 = sg * kPer, b1 = min(b0 + kPer, nb);
+            for (int bk = b0; bk < b1; ++bk) m = fmaxf(m, __ldg(bm + bk));
+            seg[sg] = m;
+            lmax = fmaxf(lmax, m);
+        }
+    } else {
+        for (int bk = threadIdx.x; bk < nb; bk += kRowThreads) lmax = fmaxf(lmax, __ldg(bm + bk));
+    }
+    return block_max(lmax, sm.red);
+}
+
 // The row's max (valid in every thread), and its segment maxima into seg
 // (vec rows), or null.
 __device__ float row_max(const float* __restrict__ row, int V, bool vec, float* seg, RowSmem& sm) {
@@ -1026,9 +1054,9 @@ __device__ RowInfo row_cut(const float* __restrict__ row, int V, bool vec, float
 // valid in every thread.  seg: this row's segment maxima (vec rows), or null.
 __device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, float invT,
                              unsigned long long P, int top_k, unsigned long long MP, float* seg,
-                             RowSmem& sm) {
+                             const float* bm, RowSmem& sm) {
     RowInfo info;
-    info.mx = row_max(row, V, vec, seg, sm);
+    info.mx = bm != nullptr ? row_max_from_blocks(bm, V, seg, sm) : row_max(row, V, vec, seg, sm);
     info.tk_key = 0u;
     info.tk_idx = 0x7fffffff;
     info.tau = 0ull;
@@ -1069,15 +1097,20 @@ __device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, flo
 __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(
     const float* __restrict__ target, const float* __restrict__ draft, long long n_target_rows,
     int V, int vec_ok, float invT, unsigned long long P, int top_k, unsigned long long MP,
-    RowInfo* __restrict__ info, float* __restrict__ segmax) {
+    RowInfo* __restrict__ info, float* __restrict__ segmax, const float* __restrict__ tbm,
+    const float* __restrict__ dbm) {
     extern __shared__ float4 dyn[];
     RowSmem& sm = *reinterpret_cast<RowSmem*>(dyn);
     const long long row = blockIdx.x;
     const float* src = row < n_target_rows
                            ? target + row * static_cast<long long>(V)
                            : draft + (row - n_target_rows) * static_cast<long long>(V);
+    // block maxima handed over by the GEMM that wrote the logits, if any
+    const long long nb = (V + kBlockLen - 1) / kBlockLen;
+    const float* bm = row < n_target_rows ? (tbm ? tbm + row * nb : nullptr)
+                                          : (dbm ? dbm + (row - n_target_rows) * nb : nullptr);
     float* seg = vec_ok ? segmax + row * static_cast<long long>(n_segments(V)) : nullptr;
-    const RowInfo r = row_stats(src, V, vec_ok != 0, invT, P, top_k, MP, seg, sm);
+    const RowInfo r = row_stats(src, V, vec_ok != 0, invT, P, top_k, MP, seg, bm, sm);
     if (threadIdx.x == 0) info[row] = r;
 }
 
@@ -1813,7 +1846,8 @@ cudaError_t launch_accept_rejection(const float* target, const float* draft,
                                     uint64_t P, int top_k, uint64_t MP, uint64_t seed,
                                     uint64_t offset, int32_t* tokens,
                                     int32_t* len, void* ws, size_t ws_bytes, uint32_t* status,
-                                    unsigned long long wait_ns, cudaStream_t s) {
+                                    unsigned long long wait_ns, cudaStream_t s,
+                                    const float* target_bmax, const float* draft_bmax) {
     const long long n_target_rows = static_cast<long long>(B) * (Kd + 1);
     const long long rows = n_target_rows + static_cast<long long>(B) * Kd;
     if (rows > 0x7fffffffll) return cudaErrorNotSupported;
@@ -1835,7 +1869,7 @@ cudaError_t launch_accept_rejection(const float* target, const float* draft,
     row_kernel<<<static_cast<unsigned>(rows), kRowThreads, smem, s>>>(
         target, draft, n_target_rows, V, vec_ok, invT, static_cast<unsigned long long>(P), top_k,
         static_cast<unsigned long long>(MP), info,
-        segmax);
+        segmax, target_bmax, draft_bmax);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     seq_kernel<<<B, kThreads, 0, s>>>(target, draft, drafts, Kd, V, vec_ok, invT,
@@ -1859,7 +1893,8 @@ static_assert(offsetof(RowInfo, mx) == offsetof(vw4_row_record, max) &&
 cudaError_t copy_rejection_row_records(const void* ws, long long rows, void* out,
                                        cudaStream_t s) {
     // the records are the first part of the workspace (info_bytes)
-    return cudaMemcpyAsync(out, ws, static_cast<size_t>(rows) * sizeof(RowInfo),
+    return cudaMemcpyAsync(out, ws,
+                           static_cast<size_t>(rows) * sizeof(RowInfo),
                            cudaMemcpyDeviceToDevice, s);
 }
 

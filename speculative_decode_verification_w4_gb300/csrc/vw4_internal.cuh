@@ -37,6 +37,7 @@ constexpr int kWarpRows = kTileRows / kConsumerWarps;  // 32
 constexpr int kRowBlocks = kWarpRows / 16;             // 16-row MMA blocks per warp
 constexpr int kGemmThreads = (kConsumerWarps + 1) * 32;
 constexpr int kGemmConsumers = kConsumerWarps * 32;
+constexpr int kBlockMaxRows = 16;  // the fused block maxima: one per 16 outputs
 static_assert(kRowBlocks == 2, "the split-tile finish assumes two row blocks per warp");
 constexpr int kWBytes = kTileRows * (kStageK / 2);     // 16384: packed nibbles
 // Scales travel in boxes of 128 rows x (16 * g) bytes that cover g = min(4, T)
@@ -117,9 +118,11 @@ struct GemmParams {
     unsigned long long* am_key;
     uint32_t* am_cnt;
     int32_t* row_argmax;
+    float* bmax;                  // optional [M][ldb]: the largest output of every 16
+    int ldb;
     uint32_t* status;
     unsigned long long wait_ns;
-    // cluster != 0 (tile-aligned split-K without the fused argmax): the split
+    // cluster != 0 (tile-aligned split-K without a fused reduction): the split
     // parts of a tile are launched as one cluster and combine their partial
     // tiles over distributed shared memory instead of tickets in L2.
     int cluster;
@@ -166,7 +169,9 @@ cudaError_t launch_accept_rejection(const float* target, const float* draft,
                                     uint64_t P, int top_k, uint64_t MP, uint64_t seed,
                                     uint64_t offset, int32_t* tokens,
                                     int32_t* len, void* ws, size_t ws_bytes, uint32_t* status,
-                                    unsigned long long wait_ns, cudaStream_t s);
+                                    unsigned long long wait_ns, cudaStream_t s,
+                                    const float* target_bmax = nullptr,
+                                    const float* draft_bmax = nullptr);
 
 // Copies the first `rows` row records of a rejection workspace (test hook).
 cudaError_t copy_rejection_row_records(const void* ws, long long rows, void* out,

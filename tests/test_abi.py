@@ -45,8 +45,10 @@ def test_workspace_sizes(lib):
     # 9..16 rows take 16-row activation blocks and partial tiles: more bytes
     w8 = vw4.vw4_workspace_bytes(vw4.OP_GEMM, 8, 262144, 5376)
     assert vw4.vw4_workspace_bytes(vw4.OP_GEMM, 9, 262144, 5376) > w8
-    assert vw4.vw4_workspace_bytes(vw4.OP_GEMM, 16, 262144, 5376) == \
-        vw4.vw4_workspace_bytes(vw4.OP_GEMM, 9, 262144, 5376)
+    # the rest grows only by the room to repack unaligned activation rows
+    w9 = vw4.vw4_workspace_bytes(vw4.OP_GEMM, 9, 262144, 5376)
+    w16 = vw4.vw4_workspace_bytes(vw4.OP_GEMM, 16, 262144, 5376)
+    assert w9 <= w16 <= w9 + 7 * 5376 * 2 + 256
     assert vw4.vw4_workspace_bytes(vw4.OP_GEMM, 17, 1024, 1024) == 0
     assert vw4.vw4_workspace_bytes(vw4.OP_GEMM, 4, 1024, 1000) == 0
     assert vw4.vw4_workspace_bytes(vw4.OP_MOE, 64, 1536, 2048) > 0
