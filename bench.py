@@ -823,7 +823,7 @@ def run_case(case: str, device):
     packed layer step at M = 8 (3 warm-up passes, then 1); 'N,K,M[,q4_0]' = one
     GEMM of that shape, nvfp4 unless q4_0 is named (3 warm-up calls, then 1); 'rejection:K' = the
     rejection accept of the stochastic sweep (B = 256, V = 151936, K drafts),
-    4 calls."""
+    4 calls; 'lists:K' = the accept over top-64 lists of those rows, 4 calls."""
     import torch
     import speculative_decode_verification_w4_gb300 as vw4
     torch.cuda.set_device(device)
@@ -838,6 +838,26 @@ def run_case(case: str, device):
         del probs
         for r in range(4):
             tok, ln = vw4.accept_rejection(tgt, drf, drafts, 0.6, 0.95, 4, r, workspace=ws)
+        torch.cuda.synchronize()
+        print(f"case {case}: 4 calls, mean run {ln.float().mean().item():.3f}, device status "
+              f"{vw4.vw4_get_device_status()}", flush=True)
+        return
+    if case.startswith("lists:"):  # the accept over top-64 lists of the sweep rows, K drafts
+        Kd, B, V, Kt = int(case.split(":")[1]), 256, 151936, 64
+        g = torch.Generator(device=device).manual_seed(4)
+        tgt = torch.randn((B, Kd + 1, V), generator=g, device=device) * 3.0
+        drf = tgt[:, :Kd] + torch.randn((B, Kd, V), generator=g, device=device)
+        tv, ti = torch.topk(tgt, Kt, dim=-1)
+        dv, di = torch.topk(drf, Kt, dim=-1)
+        ti, di = ti.to(torch.int32).contiguous(), di.to(torch.int32).contiguous()
+        tv, dv = tv.contiguous(), dv.contiguous()
+        del tgt, drf
+        pick = torch.multinomial(torch.softmax(dv.reshape(-1, Kt) / 0.6, dim=-1), 1,
+                                 generator=g).reshape(B, Kd, 1)
+        ldrafts = torch.gather(di, 2, pick).reshape(B, Kd).contiguous()
+        for r in range(4):
+            tok, ln = vw4.accept_rejection_topk(ti, tv, di, dv, ldrafts, V, 0.6, 0.95, 4, r,
+                                                workspace=ws)
         torch.cuda.synchronize()
         print(f"case {case}: 4 calls, mean run {ln.float().mean().item():.3f}, device status "
               f"{vw4.vw4_get_device_status()}", flush=True)
@@ -877,7 +897,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--case", default=None,
-                    help="profiling helper: 'dense', 'N,K,M[,q4_0]' or 'rejection:K' (see run_case); "
+                    help="profiling helper: 'dense', 'N,K,M[,q4_0]', 'rejection:K' or 'lists:K' (see run_case); "
                          "no JSON line")
     args = ap.parse_args()
     if args.warmup < 3:
