@@ -566,7 +566,31 @@ def run_head_timings(device, stream):
     moe_bytes = n_exp * (2 * f * d + d * f) * 9 // 16 + (M * d + M * topk * f) * 2
     out["moe_head_m8"] = {"us": round(us, 2), "distinct_experts": n_exp,
                           "gbs": round(moe_bytes / (us * 1e-6) / 1e9, 1)}
-    del gu, dn, pair, res, h
+    # the same head with 16 tokens (128 routed pairs)
+    M16 = 16
+    ids16, gates16 = synth.routing(302, M16, E, topk)
+    ids16_d = torch.from_numpy(np.ascontiguousarray(ids16, np.int32)).to(device)
+    gates16_d = torch.from_numpy(np.ascontiguousarray(gates16, np.float32)).to(device)
+    A16 = torch.from_numpy(synth.activations(synth.rng(303), M16, d).view(np.int16)).view(
+        torch.bfloat16).to(device)
+    pair16 = torch.empty((M16 * topk, 2 * f), dtype=torch.float32, device=device)
+    res16 = torch.empty((M16, d), dtype=torch.float32, device=device)
+    vw4.verify_moe_w4(vw4.FMT_NVFP4, *gu[0], E, A16, 0, ids16_d, gates16_d, 0, out=pair16,
+                      workspace=ws, stream=stream)
+    h16 = (torch.nn.functional.silu(pair16[:, :f]) * pair16[:, f:]).to(torch.bfloat16).contiguous()
+
+    def moe16(c):
+        vw4.verify_moe_w4(vw4.FMT_NVFP4, *gu[c], E, A16, 0, ids16_d, gates16_d, 0, out=pair16,
+                          workspace=ws, stream=stream)
+        vw4.verify_moe_w4(vw4.FMT_NVFP4, *dn[c], E, h16, 1, ids16_d, gates16_d, 1, out=res16,
+                          workspace=ws, stream=stream)
+
+    us = timed(moe16, 20)
+    n_exp16 = len(set(int(x) for x in ids16.reshape(-1)))
+    moe_bytes16 = n_exp16 * (2 * f * d + d * f) * 9 // 16 + (M16 * d + M16 * topk * f) * 2
+    out["moe_head_m16"] = {"us": round(us, 2), "distinct_experts": n_exp16,
+                           "gbs": round(moe_bytes16 / (us * 1e-6) / 1e9, 1)}
+    del gu, dn, pair, res, h, pair16, res16, h16
     torch.cuda.empty_cache()
 
     V, K = 262144, 5376

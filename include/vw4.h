@@ -226,7 +226,9 @@ VW4_API vw4_status verify_greedy_w4(const vw4_weight* W, const void* A_dev, int 
  *             M*topk pair rows, pair p = m*topk + j (rows_are_pairs == 1).
  * expert_ids_dev  int32 [M][topk] routed experts, distinct within a token.
  * gates_dev   fp32 [M][topk] (read only when combine == 1).
- * M           1..8 tokens; topk 1..8.
+ * M           1..16 tokens; topk 1..8 (at most 128 routed pairs).  The pairs
+ *             of an expert are gathered into segments of up to 8 rows, each
+ *             streaming the expert's weights once.
  * combine     0: out[p][n] for every pair p (out has M*topk rows);
  *             1: out[m][n] = sum_j gates[m][j] * pair(m, j)[n], j ascending.
  * Each touched expert streams its weights once for all its pair rows.

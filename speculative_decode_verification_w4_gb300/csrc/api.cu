@@ -353,7 +353,8 @@ VW4_API vw4_status verify_moe_w4(const vw4_weight* experts, int E, const void* A
     if (st != VW4_OK) return st;
     if (E < 1 || !A_dev || !expert_ids_dev || !out_dev) return VW4_ERR_INVALID_ARG;
     if (combine && !gates_dev) return VW4_ERR_INVALID_ARG;
-    if (M < 1 || M > kMaxRows || topk < 1 || topk > kMaxRows) return VW4_ERR_INVALID_ARG;
+    if (M < 1 || M > kMaxVerifyRows || topk < 1 || topk > kMaxRows || M * topk > kMaxSeg)
+        return VW4_ERR_INVALID_ARG;
     if ((rows_are_pairs != 0 && rows_are_pairs != 1) || (combine != 0 && combine != 1))
         return VW4_ERR_INVALID_ARG;
     const int N = experts->N, K = experts->K;

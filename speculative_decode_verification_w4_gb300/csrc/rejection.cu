@@ -58,7 +58,12 @@ constexpr int kThreads = 512;  // the sequence kernel
 constexpr int kWarps = kThreads / 32;
 constexpr int kLogBuckets = 16 + 37 * 8;  // exact 0..15, then 8 per binade up to 2^40
 constexpr int kLinBuckets = 256;
-constexpr int kCandTotal = 1024;   // crossing-bucket members a row may gather
+constexpr int kCandTotal = 1024;   // top-k candidates a row may gather
+// crossing-bucket members a row may gather before the radix fallback: the
+// flat distributions of wide vocabularies (an LM head's 262144 logits of
+// spread ~1.5 at T = 0.6) put a few thousand entries in the bucket where the
+// top-p cut falls
+constexpr int kCutCand = 4096;
 constexpr int kRankSortMax = 128;  // up to this many: sort by counting ranks
 constexpr unsigned long long kKeepAll = 1ull << 32;
 static_assert(kThreads >= kMaxRows + 1, "one thread per acceptance test");
@@ -357,8 +362,8 @@ struct RowSmem {
     unsigned long long mass[kLogBuckets];             // merged
     unsigned int cnt[kLinBuckets];                    // radix fallback: counts
     unsigned long long lmass[kLinBuckets];            //                 masses
-    unsigned long long cw[kCandTotal];                // crossing-bucket members
-    int ci[kCandTotal];
+    unsigned long long cw[kCutCand];                  // crossing-bucket members
+    int ci[kCutCand];
     unsigned int ncand;
     int beta, wbits, cut_found;
     unsigned long long above, lo, width, n_eq, count_eq;
@@ -702,6 +707,91 @@ __device__ void top_k_cut(const float* __restrict__ row, int V, bool vec, const 
     }
 }
 
+// The cut inside the crossing bucket from its gathered members sm.cw / sm.ci
+// (total <= kCutCand, in any order): sorted by (W desc, index asc), then the
+// running mass from `above_in` down the list; the first entry whose running
+// mass reaches TGT / 2^32 is the cut.  Sets info.tau, info.cut, info.S (valid
+// in every thread).
+__device__ void cut_from_candidates(RowSmem& sm, unsigned int total, unsigned long long above_in,
+                                    u128 TGT, RowInfo& info) {
+    const int tid = threadIdx.x;
+    if (total <= static_cast<unsigned int>(kRankSortMax)) {
+        // few: each candidate's place is the number that precede it
+        unsigned long long wt = 0ull;
+        int it = 0x7fffffff;
+        unsigned int place = 0;
+        if (static_cast<unsigned int>(tid) < total) {
+            wt = sm.cw[tid];
+            it = sm.ci[tid];
+            for (unsigned int u = 0; u < total; ++u) {
+                const unsigned long long wu = sm.cw[u];
+                const int iu = sm.ci[u];
+                place += (wu > wt || (wu == wt && iu < it)) ? 1u : 0u;
+            }
+        }
+        __syncthreads();
+        if (static_cast<unsigned int>(tid) < total) {
+            sm.cw[place] = wt;
+            sm.ci[place] = it;
+        }
+        __syncthreads();
+    } else {
+        // pad to a power of two, bitonic sort by (W desc, index asc)
+        unsigned int pw = 1;
+        while (pw < total) pw <<= 1;
+        for (unsigned int t = total + tid; t < pw; t += kRowThreads) {
+            sm.cw[t] = 0ull;
+            sm.ci[t] = 0x7fffffff;
+        }
+        __syncthreads();
+        for (unsigned int kk = 2; kk <= pw; kk <<= 1) {
+            for (unsigned int j = kk >> 1; j > 0; j >>= 1) {
+                for (unsigned int t = tid; t < pw; t += kRowThreads) {
+                    const unsigned int u = t ^ j;
+                    if (u > t) {
+                        const unsigned long long wa = sm.cw[t], wb = sm.cw[u];
+                        const int ia = sm.ci[t], ib = sm.ci[u];
+                        const bool a_first = wa > wb || (wa == wb && ia < ib);
+                        const bool up = (t & kk) == 0;
+                        if (up != a_first) {
+                            sm.cw[t] = wb;
+                            sm.cw[u] = wa;
+                            sm.ci[t] = ib;
+                            sm.ci[u] = ia;
+                        }
+                    }
+                }
+                __syncthreads();
+            }
+        }
+    }
+    // running mass down the sorted list; the first crossing is the cut
+    constexpr int kCutPer = kCutCand / kRowThreads;  // candidates per thread
+    const unsigned int t0 = kCutPer * tid;
+    u128 part = 0;
+    for (int j = 0; j < kCutPer; ++j)
+        if (t0 + j < total) part += sm.cw[t0 + j];
+    u128 tot;
+    const u128 ex = block_excl_u128(part, sm.red, tot);
+    const u128 above = above_in;
+    u128 run = above + ex;
+    for (int j = 0; j < kCutPer; ++j) {
+        if (t0 + j >= total) break;
+        const unsigned long long w = sm.cw[t0 + j];
+        const u128 nxt = run + w;
+        if ((nxt << 32) >= TGT && (run << 32) < TGT) {
+            sm.info.tau = w;
+            sm.info.cut = sm.ci[t0 + j];
+            sm.info.S = static_cast<unsigned long long>(nxt);
+        }
+        run = nxt;
+    }
+    __syncthreads();
+    info.tau = sm.info.tau;
+    info.cut = sm.info.cut;
+    info.S = sm.info.S;
+}
+
 // The row's (tau, cut, kept sum) after top-p, over the entries the top-k
 // stage of info keeps (n_keep of them); valid in every thread.
 __device__ RowInfo row_cut(const float* __restrict__ row, int V, bool vec, float invT,
@@ -861,7 +951,7 @@ __device__ RowInfo row_cut(const float* __restrict__ row, int V, bool vec, float
                 const float e = own_exp(x);
                 if (e >= b_lo && e < b_hi) {
                     const unsigned int slot = atomicAdd(&sm.ncand, 1u);
-                    if (slot < static_cast<unsigned int>(kCandTotal)) {
+                    if (slot < static_cast<unsigned int>(kCutCand)) {
                         sm.cw[slot] = mass_of(e);
                         sm.ci[slot] = k;
                     }
@@ -871,78 +961,8 @@ __device__ RowInfo row_cut(const float* __restrict__ row, int V, bool vec, float
     }
     __syncthreads();
     const unsigned int total = sm.ncand;
-    if (total <= static_cast<unsigned int>(kCandTotal)) {
-        if (total <= static_cast<unsigned int>(kRankSortMax)) {
-            // few: each candidate's place is the number that precede it
-            unsigned long long wt = 0ull;
-            int it = 0x7fffffff;
-            unsigned int place = 0;
-            if (static_cast<unsigned int>(tid) < total) {
-                wt = sm.cw[tid];
-                it = sm.ci[tid];
-                for (unsigned int u = 0; u < total; ++u) {
-                    const unsigned long long wu = sm.cw[u];
-                    const int iu = sm.ci[u];
-                    place += (wu > wt || (wu == wt && iu < it)) ? 1u : 0u;
-                }
-            }
-            __syncthreads();
-            if (static_cast<unsigned int>(tid) < total) {
-                sm.cw[place] = wt;
-                sm.ci[place] = it;
-            }
-            __syncthreads();
-        } else {
-            // pad to a power of two, bitonic sort by (W desc, index asc)
-            unsigned int pw = 1;
-            while (pw < total) pw <<= 1;
-            for (unsigned int t = total + tid; t < pw; t += kRowThreads) {
-                sm.cw[t] = 0ull;
-                sm.ci[t] = 0x7fffffff;
-            }
-            __syncthreads();
-            for (unsigned int kk = 2; kk <= pw; kk <<= 1) {
-                for (unsigned int j = kk >> 1; j > 0; j >>= 1) {
-                    for (unsigned int t = tid; t < pw; t += kRowThreads) {
-                        const unsigned int u = t ^ j;
-                        if (u > t) {
-                            const unsigned long long wa = sm.cw[t], wb = sm.cw[u];
-                            const int ia = sm.ci[t], ib = sm.ci[u];
-                            const bool a_first = wa > wb || (wa == wb && ia < ib);
-                            const bool up = (t & kk) == 0;
-                            if (up != a_first) {
-                                sm.cw[t] = wb;
-                                sm.cw[u] = wa;
-                                sm.ci[t] = ib;
-                                sm.ci[u] = ia;
-                            }
-                        }
-                    }
-                    __syncthreads();
-                }
-            }
-        }
-        // running mass down the sorted list; the first crossing is the cut
-        const unsigned int t0 = 2 * tid;
-        const unsigned long long w0 = t0 < total ? sm.cw[t0] : 0ull;
-        const unsigned long long w1 = t0 + 1 < total ? sm.cw[t0 + 1] : 0ull;
-        u128 tot;
-        const u128 ex = block_excl_u128(static_cast<u128>(w0) + w1, sm.red, tot);
-        const u128 above = sm.above;
-        const u128 c0s = above + ex + w0, c1s = c0s + w1;
-        if (t0 < total && (c0s << 32) >= TGT && ((above + ex) << 32) < TGT) {
-            sm.info.tau = w0;
-            sm.info.cut = sm.ci[t0];
-            sm.info.S = static_cast<unsigned long long>(c0s);
-        } else if (t0 + 1 < total && (c1s << 32) >= TGT && (c0s << 32) < TGT) {
-            sm.info.tau = w1;
-            sm.info.cut = sm.ci[t0 + 1];
-            sm.info.S = static_cast<unsigned long long>(c1s);
-        }
-        __syncthreads();
-        info.tau = sm.info.tau;
-        info.cut = sm.info.cut;
-        info.S = sm.info.S;
+    if (total <= static_cast<unsigned int>(kCutCand)) {
+        cut_from_candidates(sm, total, sm.above, TGT, info);
         return info;
     }
 
@@ -1114,6 +1134,365 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(
     if (threadIdx.x == 0) info[row] = r;
 }
 
+// ------------------------------------------------------- split rows
+// With few logits rows (a handful of sequences, e.g. one sequence of an
+// LM-head verify) one CTA per row leaves most SMs idle, and each CTA streams
+// its whole row several times.  Then every row is cut into C chunks of whole
+// 128-entry segments, one CTA per (row, chunk), and the row statistics are
+// taken in five launches: the chunk maxima; the chunks' integer mass sums and
+// mass histograms (exact integers, so their sums over the chunks are exact
+// and order-free); the crossing bucket of the top-p cut per row; the members
+// of that bucket gathered from every chunk; and the cut among them.  The
+// records are exactly those of the one-CTA row kernel (same masses, same
+// cut); a bucket with more than kCutCand members falls back to that kernel's
+// code for its row.
+constexpr int kSplitRowsMax = 152;   // more rows than this: one CTA per row
+constexpr int kSplitMinV = 16384;    // shorter rows: one CTA per row
+constexpr int kSplitSlots = 304;     // (row, chunk) CTAs per call
+
+struct SplitState {
+    int beta;                 // crossing bucket, or -1 when the record is final
+    int pad;
+    unsigned long long above; // kept mass above the bucket
+    unsigned long long S;     // the row's whole mass (top-p off: the kept sum)
+    unsigned long long pad2;
+};
+
+__host__ __device__ inline int split_chunks(long long rows) {
+    const long long c = kSplitSlots / (rows > 0 ? rows : 1);
+    return static_cast<int>(c < 2 ? 2 : (c > 64 ? 64 : c));
+}
+
+struct SplitWs {
+    float* chunkmax;               // [rows][C]
+    unsigned long long* pS;        // [rows][C]
+    unsigned long long* phist;     // [rows][C][kLogBuckets]
+    SplitState* state;             // [rows]
+    uint32_t* ncand;               // [rows]
+    unsigned long long* cw;        // [rows][kCutCand]
+    int* ci;                       // [rows][kCutCand]
+    ulonglong2* chunk_tot;         // [sequences][C] draw weight of each chunk (u128)
+    size_t bytes;
+};
+
+static size_t r256(size_t x) { return (x + 255) / 256 * 256; }
+
+static SplitWs split_layout(char* base, long long rows) {
+    SplitWs w{};
+    const int C = split_chunks(rows);
+    size_t off = 0;
+    auto take = [&](size_t b) {
+        char* p = base ? base + off : nullptr;
+        off += r256(b);
+        return p;
+    };
+    w.chunkmax = reinterpret_cast<float*>(take(rows * C * sizeof(float)));
+    w.pS = reinterpret_cast<unsigned long long*>(take(rows * C * 8));
+    w.phist = reinterpret_cast<unsigned long long*>(take(rows * C * kLogBuckets * 8));
+    w.state = reinterpret_cast<SplitState*>(take(rows * sizeof(SplitState)));
+    w.ncand = reinterpret_cast<uint32_t*>(take(rows * 4));
+    w.cw = reinterpret_cast<unsigned long long*>(take(rows * kCutCand * 8));
+    w.ci = reinterpret_cast<int*>(take(rows * kCutCand * 4));
+    w.chunk_tot = reinterpret_cast<ulonglong2*>(take(rows * 64 * sizeof(ulonglong2)));
+    w.bytes = off;
+    return w;
+}
+
+// Row r's logits: the target rows (b, i <= Kd) first, then the draft rows.
+__device__ __forceinline__ const float* split_row(const float* target, const float* draft,
+                                                  long long n_target_rows, long long r, int V) {
+    return r < n_target_rows ? target + r * static_cast<long long>(V)
+                             : draft + (r - n_target_rows) * static_cast<long long>(V);
+}
+
+// Segments [s0, s1) of chunk c of a row of nseg segments.
+__device__ __forceinline__ void split_span(int nseg, int C, int c, int& s0, int& s1) {
+    const int spc = (nseg + C - 1) / C;
+    s0 = c * spc;
+    s1 = min(s0 + spc, nseg);
+    if (s0 > nseg) s0 = nseg;
+}
+
+// 1. Chunk maxima and the maxima of the chunk's segments (the max pass of
+//    row_max, segment by segment: a warp takes a segment, a lane one float4
+//    group); with block maxima given, from those.
+__global__ void __launch_bounds__(kRowThreads) split_max_kernel(
+    const float* __restrict__ target, const float* __restrict__ draft, long long n_target_rows,
+    int V, int C, const float* __restrict__ tbm, const float* __restrict__ dbm,
+    float* __restrict__ segmax, float* __restrict__ chunkmax) {
+    __shared__ Red red;
+    const long long r = blockIdx.x / C;
+    const int c = blockIdx.x % C;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int nseg = n_segments(V), V4 = V >> 2;
+    int s0, s1;
+    split_span(nseg, C, c, s0, s1);
+    float* seg = segmax + r * nseg;
+    const long long nb = (V + kBlockLen - 1) / kBlockLen;
+    const float* bm = r < n_target_rows ? (tbm ? tbm + r * nb : nullptr)
+                                        : (dbm ? dbm + (r - n_target_rows) * nb : nullptr);
+    float lmax = -INFINITY;
+    if (bm != nullptr) {
+        constexpr int kPer = kSegLen / kBlockLen;
+        for (int sg = s0 + tid; sg < s1; sg += kRowThreads) {
+            float m = -INFINITY;
+            const int b1 = min((sg + 1) * kPer, static_cast<int>(nb));
+            for (int bk = sg * kPer; bk < b1; ++bk) m = fmaxf(m, __ldg(bm + bk));
+            seg[sg] = m;
+            lmax = fmaxf(lmax, m);
+        }
+    } else {
+        const float4* r4 = reinterpret_cast<const float4*>(split_row(target, draft, n_target_rows,
+                                                                     r, V));
+        const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        for (int sg0 = s0 + wid; sg0 < s1; sg0 += 4 * kRowWarps) {
+            float4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int sg = sg0 + j * kRowWarps, i = sg * 32 + lane;
+                v[j] = (sg < s1 && i < V4) ? __ldg(r4 + i) : ninf;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int sg = sg0 + j * kRowWarps;
+                if (sg >= s1) break;  // the same for the whole warp
+                const float m = fmaxf(fmaxf(v[j].x, v[j].y), fmaxf(v[j].z, v[j].w));
+                lmax = fmaxf(lmax, m);
+                const int key = __reduce_max_sync(0xffffffffu, float_key(m));
+                if (lane == 0) seg[sg] = __int_as_float(key ^ ((key >> 31) & 0x7fffffff));
+            }
+        }
+    }
+    const float m = block_max(lmax, red);
+    if (tid == 0) chunkmax[r * C + c] = m;
+}
+
+// 2. The chunk's mass sum and mass histogram: the integer masses W of
+//    row_cut's second pass, entry for entry the same operations; the sums are
+//    exact, so the row's are their sums over the chunks.
+__global__ void __launch_bounds__(kRowThreads, 2) split_mass_kernel(
+    const float* __restrict__ target, const float* __restrict__ draft, long long n_target_rows,
+    int V, int C, float invT, unsigned long long P, const float* __restrict__ chunkmax,
+    unsigned long long* __restrict__ pS, unsigned long long* __restrict__ phist) {
+    extern __shared__ float4 dyn[];
+    RowSmem& sm = *reinterpret_cast<RowSmem*>(dyn);
+    const long long r = blockIdx.x / C;
+    const int c = blockIdx.x % C;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int nseg = n_segments(V), V4 = V >> 2;
+    int s0, s1;
+    split_span(nseg, C, c, s0, s1);
+    float mx = -INFINITY;
+    for (int j = 0; j < C; ++j) mx = fmaxf(mx, __ldg(chunkmax + r * C + j));
+    const bool want_hist = P < kKeepAll;
+    const unsigned long long c0 =
+        want_hist ? ((kKeepAll - P) << 8) / static_cast<unsigned long long>(V) : 0ull;
+    const unsigned long long cmin = c0 > 1ull ? c0 : 1ull;
+    const float f_lo = want_hist ? __ull2float_rd(cmin) : INFINITY;
+    unsigned long long* hist = sm.whist[wid];
+    for (int t = lane; t < kLogBuckets; t += 32) hist[t] = 0ull;
+    __syncwarp();
+    uint32_t sum_hib = 0u, sum_lob = 0u, n_mine = 0u;
+    auto to_hist = [&](float f, uint32_t hib, uint32_t lob) {
+        const unsigned long long W =
+            (static_cast<unsigned long long>(hib - 0x4B000000u) << 20) | (lob - 0x4B000000u);
+        if (W >= cmin) atomic_add_u64_split(&hist[log_bucket_f(f)], W);
+    };
+    const float2 nmx = make_float2(-mx, -mx), it2 = make_float2(invT, invT);
+    const float2 k20 = make_float2(9.5367431640625e-07f, 9.5367431640625e-07f);
+    const float2 m20 = make_float2(-1048576.0f, -1048576.0f);
+    const float2 b23 = make_float2(8388608.0f, 8388608.0f), nb23 = make_float2(-8388608.0f, -8388608.0f);
+    auto pair = [&](float la, float lb) {
+        const float2 f = own_exp_2_40_x2(__fmul2_rn(__fadd2_rn(make_float2(la, lb), nmx), it2));
+        const float2 t1 = __fadd2_rd(__fmul2_rn(f, k20), b23);
+        const float2 t2 = __fadd2_rd(__ffma2_rn(__fadd2_rn(t1, nb23), m20, f), b23);
+        const uint32_t h0 = __float_as_uint(t1.x), h1 = __float_as_uint(t1.y);
+        const uint32_t l0 = __float_as_uint(t2.x), l1 = __float_as_uint(t2.y);
+        sum_hib += h0 + h1;
+        sum_lob += l0 + l1;
+        if (fmaxf(f.x, f.y) >= f_lo) {
+            if (f.x >= f_lo) to_hist(f.x, h0, l0);
+            if (f.y >= f_lo) to_hist(f.y, h1, l1);
+        }
+    };
+    const float4* r4 = reinterpret_cast<const float4*>(split_row(target, draft, n_target_rows, r, V));
+    for (int sg0 = s0 + wid; sg0 < s1; sg0 += 4 * kRowWarps) {
+        float4 v[4];
+        bool in[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int sg = sg0 + j * kRowWarps, i = sg * 32 + lane;
+            in[j] = sg < s1 && i < V4;
+            v[j] = in[j] ? __ldg(r4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (in[j]) {
+                pair(v[j].x, v[j].y);
+                pair(v[j].z, v[j].w);
+                n_mine += 4u;
+            }
+    }
+    const uint32_t bias = n_mine * 0x4B000000u;
+    const unsigned long long S = block_sum_u64(
+        (static_cast<unsigned long long>(sum_hib - bias) << 20) + (sum_lob - bias), sm.red);
+    __syncthreads();  // every warp's histogram is complete
+    unsigned long long* out = phist + (r * C + c) * kLogBuckets;
+    for (int t = tid; t < kLogBuckets; t += kRowThreads) {
+        unsigned long long m = 0ull;
+        for (int w = 0; w < kRowWarps; ++w) m += sm.whist[w][t];
+        out[t] = m;
+    }
+    if (tid == 0) pS[r * C + c] = S;
+}
+
+// 3. Per row: the mass S, the merged histogram and the bucket where the
+//    top-p cut falls, as row_cut finds them; a row whose record is already
+//    decided (top-p off, all masses 0, or the cut at the last entry) gets it.
+__global__ void __launch_bounds__(kRowThreads, 2) split_beta_kernel(
+    int V, int C, unsigned long long P, const float* __restrict__ chunkmax,
+    const unsigned long long* __restrict__ pS, const unsigned long long* __restrict__ phist,
+    RowInfo* __restrict__ info_out, SplitState* __restrict__ state, uint32_t* __restrict__ ncand) {
+    extern __shared__ float4 dyn[];
+    RowSmem& sm = *reinterpret_cast<RowSmem*>(dyn);
+    const long long r = blockIdx.x;
+    const int tid = threadIdx.x;
+    float mx = -INFINITY;
+    for (int j = 0; j < C; ++j) mx = fmaxf(mx, __ldg(chunkmax + r * C + j));
+    unsigned long long s = 0ull;
+    for (int j = tid; j < C; j += kRowThreads) s += pS[r * C + j];
+    const unsigned long long S = block_sum_u64(s, sm.red);
+    RowInfo info;
+    info.mx = mx;
+    info.tk_key = 0u;
+    info.tk_idx = 0x7fffffff;
+    info.tau = 0ull;
+    info.cut = V - 1;
+    info.S = S;
+    int beta = -1;
+    unsigned long long above = 0ull;
+    if (P < kKeepAll && S == 0ull) {
+        info.cut = 0;  // every W is 0: the prefix is the first entry, mass 0
+    } else if (P < kKeepAll) {
+        const u128 TGT = static_cast<u128>(P) * S;
+        const int tb = kLogBuckets - 1 - tid;
+        unsigned long long m = 0ull;
+        if (tb >= 1)
+            for (int j = 0; j < C; ++j) m += phist[(r * C + j) * kLogBuckets + tb];
+        u128 tot_unused;
+        const u128 incl = block_excl_u128(static_cast<u128>(m), sm.red, tot_unused) + m;
+        if (tid == 0) sm.beta = -1;
+        __syncthreads();
+        if (tb >= 1 && (incl << 32) >= TGT && ((incl - m) << 32) < TGT) {
+            sm.beta = tb;
+            sm.above = static_cast<unsigned long long>(incl - m);
+        }
+        __syncthreads();
+        beta = sm.beta;
+        above = sm.above;
+    }
+    if (tid == 0) {
+        SplitState st{};
+        st.beta = beta;
+        st.above = above;
+        st.S = S;
+        state[r] = st;
+        ncand[r] = 0u;
+        if (beta < 0) info_out[r] = info;
+    }
+}
+
+// 4. The members of the crossing bucket, from every chunk (the window pass
+//    of row_cut, over the chunk's segments whose max reaches the window).
+__global__ void __launch_bounds__(kRowThreads) split_gather_kernel(
+    const float* __restrict__ target, const float* __restrict__ draft, long long n_target_rows,
+    int V, int C, float invT, const float* __restrict__ segmax, const float* __restrict__ chunkmax,
+    const SplitState* __restrict__ state, uint32_t* __restrict__ ncand,
+    unsigned long long* __restrict__ cw, int* __restrict__ ci) {
+    const long long r = blockIdx.x / C;
+    const int c = blockIdx.x % C;
+    const int beta = state[r].beta;
+    if (beta < 0) return;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int nseg = n_segments(V), V4 = V >> 2;
+    int s0, s1;
+    split_span(nseg, C, c, s0, s1);
+    float mx = -INFINITY;
+    for (int j = 0; j < C; ++j) mx = fmaxf(mx, __ldg(chunkmax + r * C + j));
+    float b_lo, b_hi;
+    bucket_e_range(beta, b_lo, b_hi);
+    unsigned long long wlo, whi;
+    if (beta < 16) {
+        wlo = static_cast<unsigned long long>(beta);
+        whi = wlo + 1ull;
+    } else {
+        const int msb = 4 + (beta - 16) / 8, j = (beta - 16) % 8;
+        wlo = static_cast<unsigned long long>(8 + j) << (msb - 3);
+        whi = static_cast<unsigned long long>(9 + j) << (msb - 3);
+    }
+    float xa, xb;
+    x_window(wlo, whi, xa, xb);
+    const float* seg = segmax + r * nseg;
+    const float4* r4 = reinterpret_cast<const float4*>(split_row(target, draft, n_target_rows, r, V));
+    for (int sg = s0 + wid; sg < s1; sg += kRowWarps) {
+        if (scaled_x(__ldcg(seg + sg), mx, invT) < xa) continue;  // the same for the warp
+        const int i = sg * 32 + lane;
+        if (i >= V4) continue;
+        const float4 a = __ldg(r4 + i);
+        const float lv[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float x = scaled_x(lv[q], mx, invT);
+            if (x >= xa && x < xb) {
+                const float e = own_exp(x);
+                if (e >= b_lo && e < b_hi) {
+                    const unsigned int slot = atomicAdd(&ncand[r], 1u);
+                    if (slot < static_cast<unsigned int>(kCutCand)) {
+                        cw[r * kCutCand + slot] = mass_of(e);
+                        ci[r * kCutCand + slot] = 4 * i + q;
+                    }
+                }
+            }
+        }
+    }
+}
+
+// 5. Per row: the cut among the gathered members (or, for a bucket with more
+//    than kCutCand members, the one-CTA row statistics of that row).
+__global__ void __launch_bounds__(kRowThreads, 2) split_cut_kernel(
+    const float* __restrict__ target, const float* __restrict__ draft, long long n_target_rows,
+    int V, int C, float invT, unsigned long long P, float* __restrict__ segmax,
+    const float* __restrict__ chunkmax, const SplitState* __restrict__ state,
+    const uint32_t* __restrict__ ncand, const unsigned long long* __restrict__ cw,
+    const int* __restrict__ ci, RowInfo* __restrict__ info_out) {
+    extern __shared__ float4 dyn[];
+    RowSmem& sm = *reinterpret_cast<RowSmem*>(dyn);
+    const long long r = blockIdx.x;
+    const SplitState st = state[r];
+    if (st.beta < 0) return;
+    const int tid = threadIdx.x;
+    const unsigned int total = ncand[r];
+    RowInfo info;
+    if (total <= static_cast<unsigned int>(kCutCand)) {
+        float mx = -INFINITY;
+        for (int j = 0; j < C; ++j) mx = fmaxf(mx, __ldg(chunkmax + r * C + j));
+        for (unsigned int t = tid; t < total; t += kRowThreads) {
+            sm.cw[t] = cw[r * kCutCand + t];
+            sm.ci[t] = ci[r * kCutCand + t];
+        }
+        __syncthreads();
+        info.mx = mx;
+        info.tk_key = 0u;
+        info.tk_idx = 0x7fffffff;
+        const u128 TGT = static_cast<u128>(P) * st.S;
+        cut_from_candidates(sm, total, st.above, TGT, info);
+    } else {
+        const float* row = split_row(target, draft, n_target_rows, r, V);
+        info = row_stats(row, V, true, invT, P, 0, 0ull, segmax + r * n_segments(V), nullptr, sm);
+    }
+    if (tid == 0) info_out[r] = info;
+}
+
 // --------------------------------------------------------- sequence kernel
 // Weight of entry v in the draw: the kept target mass (p), or the residual
 // max(0, p_v * Sq - q_v * Sp).  Entries whose scaled logit is below xth have
@@ -1202,11 +1581,14 @@ __device__ __forceinline__ void atomic_add_u128(unsigned long long* a, u128 x) {
 // Level 1 of the draw: warp wid sums the weights of each segment of its run
 // of segments into ssum[] (zero for the segments that cannot weigh) and
 // returns the run's total (in lane 0).
+// (Segments [s_begin, s_end) of the row; the whole row by default.)
 __device__ __forceinline__ u128 segment_sums(const DrawRow& w, ulonglong2* ssum, WarpQueue& wq,
-                                             int wid, int lane) {
-    const int nseg = n_segments(w.V);
-    const int s_lo = static_cast<int>(static_cast<long long>(wid) * nseg / kWarps);
-    const int s_hi = static_cast<int>(static_cast<long long>(wid + 1) * nseg / kWarps);
+                                             int wid, int lane, int s_begin = 0,
+                                             int s_end = -1) {
+    if (s_end < 0) s_end = n_segments(w.V);
+    const long long span = s_end - s_begin;
+    const int s_lo = s_begin + static_cast<int>(static_cast<long long>(wid) * span / kWarps);
+    const int s_hi = s_begin + static_cast<int>(static_cast<long long>(wid + 1) * span / kWarps);
     u128 tot = 0;
     for (int s0 = s_lo; s0 < s_hi; s0 += 32) {
         const int s = s0 + lane;
@@ -1298,16 +1680,16 @@ __device__ __forceinline__ u128 segment_sums(const DrawRow& w, ulonglong2* ssum,
 // One CTA per sequence: acceptance tests in order, then one ordered draw and
 // the committed run.
 // (Two CTAs per SM: 256 sequences fit one wave.)
-__global__ void __launch_bounds__(kThreads, 2) seq_kernel(
-    const float* __restrict__ target, const float* __restrict__ draft,
-    const int32_t* __restrict__ drafts, int Kd, int V, int vec_ok, float invT,
-    unsigned long long seed, unsigned long long offset, long long n_target_rows,
-    const RowInfo* __restrict__ info, const float* __restrict__ segmax, ulonglong2* segsum,
-    int32_t* __restrict__ tokens, int32_t* __restrict__ len, uint32_t* status) {
-    __shared__ SeqSmem sm;
-    const int b = blockIdx.x;
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    // the Kd acceptance tests are independent: thread i takes draft i
+// The sequence's acceptance tests (thread i < Kd takes draft i, in
+// parallel) and the run they decide: sm.n_acc accepted drafts, the rows of
+// the draw (sm.rowp, and sm.rowq for a residual, -1 for the bonus) and its
+// 64-bit uniform sm.u64.  Every thread of the block calls it.
+__device__ void seq_decide(const float* __restrict__ target, const float* __restrict__ draft,
+                           const int32_t* __restrict__ drafts, int Kd, int V, float invT,
+                           unsigned long long seed, unsigned long long offset,
+                           long long n_target_rows, const RowInfo* __restrict__ info, int b,
+                           uint32_t* status, SeqSmem& sm) {
+    const int tid = threadIdx.x;
     if (tid <= Kd) {
         const int i = tid;
         uint32_t rr[4];
@@ -1351,6 +1733,14 @@ __global__ void __launch_bounds__(kThreads, 2) seq_kernel(
         sm.seg = -1;
     }
     __syncthreads();
+}
+
+// The row the draw weighs: the kept target masses p (the bonus), or the
+// residual max(0, p Sq - q Sp) at the first rejection.
+__device__ DrawRow seq_draw_row(const float* __restrict__ target, const float* __restrict__ draft,
+                                int V, int vec_ok, float invT, long long n_target_rows,
+                                const RowInfo* __restrict__ info,
+                                const float* __restrict__ segmax, const SeqSmem& sm) {
     const int rowp = sm.rowp, rowq = sm.rowq;
     const int nseg = n_segments(V);
     DrawRow w;
@@ -1365,23 +1755,36 @@ __global__ void __launch_bounds__(kThreads, 2) seq_kernel(
     w.invT = invT;
     w.V = V;
     w.vec = vec_ok != 0;
-    {
-        const unsigned long long tm = w.ip.tau > 1ull ? w.ip.tau : 1ull;
-        w.xth = static_cast<float>(log(static_cast<double>(tm)) - 40.0 * 0.69314718055994530942 -
-                                   1e-3);
-    }
-    ulonglong2* ssum = segsum + static_cast<long long>(b) * nseg;
+    const unsigned long long tm = w.ip.tau > 1ull ? w.ip.tau : 1ull;
+    w.xth = static_cast<float>(log(static_cast<double>(tm)) - 40.0 * 0.69314718055994530942 -
+                               1e-3);
+    return w;
+}
 
-    // level 1: the weight of every segment, and the total
-    u128 wt = segment_sums(w, ssum, sm.q[wid], wid, lane);
+// Sums the warps' level-1 totals (lane 0 of each) into one u128 in every
+// thread.
+__device__ __forceinline__ u128 seq_block_total(u128 wt, SeqSmem& sm) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     if (lane == 0) {
         sm.tot_lo[wid] = static_cast<unsigned long long>(wt);
         sm.tot_hi[wid] = static_cast<unsigned long long>(wt >> 64);
     }
     __syncthreads();
+    u128 R = 0;
+    for (int k = 0; k < kWarps; ++k) R += (static_cast<u128>(sm.tot_hi[k]) << 64) | sm.tot_lo[k];
+    __syncthreads();
+    return R;
+}
+
+// Given every segment's weight in ssum[] and their total R: the draw point,
+// the segment that holds it (a block scan), the entry inside it (warp 0
+// rescans the segment), and the committed run.
+__device__ void seq_finish(DrawRow& w, u128 R, ulonglong2* ssum, const int32_t* __restrict__ drafts,
+                           int Kd, int b, int32_t* __restrict__ tokens, int32_t* __restrict__ len,
+                           uint32_t* status, SeqSmem& sm) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int V = w.V, nseg = n_segments(V), rowq = sm.rowq;
     if (tid == 0) {
-        u128 R = 0;
-        for (int k = 0; k < kWarps; ++k) R += (static_cast<u128>(sm.tot_hi[k]) << 64) | sm.tot_lo[k];
         sm.sel = 0;
         if (rowq >= 0 && R == 0) {  // only reachable through an invalid draft id
             atomicOr(status, kStatusZeroResidual);
@@ -1473,6 +1876,69 @@ __global__ void __launch_bounds__(kThreads, 2) seq_kernel(
         tokens[static_cast<long long>(b) * (Kd + 1) + tid] = tk;
     }
     if (tid == 0) len[b] = sm.n_acc + 1;
+}
+
+__global__ void __launch_bounds__(kThreads, 2) seq_kernel(
+    const float* __restrict__ target, const float* __restrict__ draft,
+    const int32_t* __restrict__ drafts, int Kd, int V, int vec_ok, float invT,
+    unsigned long long seed, unsigned long long offset, long long n_target_rows,
+    const RowInfo* __restrict__ info, const float* __restrict__ segmax, ulonglong2* segsum,
+    int32_t* __restrict__ tokens, int32_t* __restrict__ len, uint32_t* status) {
+    __shared__ SeqSmem sm;
+    const int b = blockIdx.x;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    seq_decide(target, draft, drafts, Kd, V, invT, seed, offset, n_target_rows, info, b, status,
+               sm);
+    DrawRow w = seq_draw_row(target, draft, V, vec_ok, invT, n_target_rows, info, segmax, sm);
+    ulonglong2* ssum = segsum + static_cast<long long>(b) * n_segments(V);
+    // level 1: the weight of every segment, and the total
+    const u128 R = seq_block_total(segment_sums(w, ssum, sm.q[wid], wid, lane), sm);
+    seq_finish(w, R, ssum, drafts, Kd, b, tokens, len, status, sm);
+}
+
+// The draw of a split call: (sequence, chunk) CTAs weigh the chunk's
+// segments of the sequence's draw row (level 1) ...
+__global__ void __launch_bounds__(kThreads, 2) split_seq_sums_kernel(
+    const float* __restrict__ target, const float* __restrict__ draft,
+    const int32_t* __restrict__ drafts, int Kd, int V, int C, float invT,
+    unsigned long long seed, unsigned long long offset, long long n_target_rows,
+    const RowInfo* __restrict__ info, const float* __restrict__ segmax, ulonglong2* segsum,
+    ulonglong2* chunk_tot, uint32_t* status) {
+    __shared__ SeqSmem sm;
+    const int b = blockIdx.x / C, c = blockIdx.x % C;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    seq_decide(target, draft, drafts, Kd, V, invT, seed, offset, n_target_rows, info, b, status,
+               sm);
+    DrawRow w = seq_draw_row(target, draft, V, 1, invT, n_target_rows, info, segmax, sm);
+    int s0, s1;
+    split_span(n_segments(V), C, c, s0, s1);
+    ulonglong2* ssum = segsum + static_cast<long long>(b) * n_segments(V);
+    const u128 R = seq_block_total(segment_sums(w, ssum, sm.q[wid], wid, lane, s0, s1), sm);
+    if (threadIdx.x == 0)
+        chunk_tot[static_cast<long long>(b) * C + c] =
+            make_ulonglong2(static_cast<unsigned long long>(R), static_cast<unsigned long long>(R >> 64));
+}
+
+// ... then one CTA per sequence sums the chunk totals and finishes the draw.
+__global__ void __launch_bounds__(kThreads, 2) split_seq_finish_kernel(
+    const float* __restrict__ target, const float* __restrict__ draft,
+    const int32_t* __restrict__ drafts, int Kd, int V, int C, float invT,
+    unsigned long long seed, unsigned long long offset, long long n_target_rows,
+    const RowInfo* __restrict__ info, const float* __restrict__ segmax, ulonglong2* segsum,
+    const ulonglong2* __restrict__ chunk_tot, int32_t* __restrict__ tokens,
+    int32_t* __restrict__ len, uint32_t* status) {
+    __shared__ SeqSmem sm;
+    const int b = blockIdx.x;
+    seq_decide(target, draft, drafts, Kd, V, invT, seed, offset, n_target_rows, info, b, status,
+               sm);
+    DrawRow w = seq_draw_row(target, draft, V, 1, invT, n_target_rows, info, segmax, sm);
+    u128 R = 0;
+    for (int c = 0; c < C; ++c) {
+        const ulonglong2 x = chunk_tot[static_cast<long long>(b) * C + c];
+        R += (static_cast<u128>(x.y) << 64) | x.x;
+    }
+    seq_finish(w, R, segsum + static_cast<long long>(b) * n_segments(V), drafts, Kd, b, tokens,
+               len, status, sm);
 }
 
 // ------------------------------------------------------ top-k lists
@@ -1835,10 +2301,20 @@ static size_t segmax_bytes(size_t rows, int V) {
     return ((seg + 255) / 256) * 256;
 }
 
+// ... then, for few rows of a wide vocabulary, the split-row arrays.
+static size_t base_bytes(size_t rows, int B, int V) {
+    const size_t draw = static_cast<size_t>(B) * ((V + kSegLen - 1) / kSegLen) * 16;
+    return info_bytes(rows) + segmax_bytes(rows, V) + r256(draw);
+}
+
+static bool split_sized(long long rows, int V) { return rows <= kSplitRowsMax && V >= kSplitMinV; }
+
 size_t rejection_workspace_bytes(int B, int Kd, int V) {
     const size_t rows = static_cast<size_t>(B) * (2 * static_cast<size_t>(Kd) + 1);
-    const size_t draw = static_cast<size_t>(B) * ((V + kSegLen - 1) / kSegLen) * 16;
-    return info_bytes(rows) + segmax_bytes(rows, V) + draw;
+    size_t b = base_bytes(rows, B, V);
+    if (split_sized(static_cast<long long>(rows), V))
+        b += split_layout(nullptr, static_cast<long long>(rows)).bytes;
+    return b;
 }
 
 cudaError_t launch_accept_rejection(const float* target, const float* draft,
@@ -1866,10 +2342,50 @@ cudaError_t launch_accept_rejection(const float* target, const float* draft,
                         (reinterpret_cast<uintptr_t>(draft) & 15u) == 0)
                            ? 1
                            : 0;
-    row_kernel<<<static_cast<unsigned>(rows), kRowThreads, smem, s>>>(
-        target, draft, n_target_rows, V, vec_ok, invT, static_cast<unsigned long long>(P), top_k,
-        static_cast<unsigned long long>(MP), info,
-        segmax, target_bmax, draft_bmax);
+    // few rows of a wide vocabulary (and no top-k or min-p stage): each row
+    // in chunks over many CTAs
+    const bool split = split_sized(rows, V) && vec_ok && (top_k <= 0 || top_k >= V) && MP == 0;
+    if (split) {
+        const int C = split_chunks(rows);
+        const SplitWs sw = split_layout(static_cast<char*>(ws) + base_bytes(rows, B, V), rows);
+        const unsigned long long Pu = static_cast<unsigned long long>(P);
+        for (const void* k : {reinterpret_cast<const void*>(split_mass_kernel),
+                              reinterpret_cast<const void*>(split_beta_kernel),
+                              reinterpret_cast<const void*>(split_cut_kernel)}) {
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem));
+            if (e != cudaSuccess) return e;
+        }
+        const unsigned grid = static_cast<unsigned>(rows * C);
+        split_max_kernel<<<grid, kRowThreads, 0, s>>>(target, draft, n_target_rows, V, C,
+                                                      target_bmax, draft_bmax, segmax,
+                                                      sw.chunkmax);
+        split_mass_kernel<<<grid, kRowThreads, smem, s>>>(target, draft, n_target_rows, V, C,
+                                                          invT, Pu, sw.chunkmax, sw.pS, sw.phist);
+        split_beta_kernel<<<static_cast<unsigned>(rows), kRowThreads, smem, s>>>(
+            V, C, Pu, sw.chunkmax, sw.pS, sw.phist, info, sw.state, sw.ncand);
+        split_gather_kernel<<<grid, kRowThreads, 0, s>>>(target, draft, n_target_rows, V, C,
+                                                         invT, segmax, sw.chunkmax, sw.state,
+                                                         sw.ncand, sw.cw, sw.ci);
+        split_cut_kernel<<<static_cast<unsigned>(rows), kRowThreads, smem, s>>>(
+            target, draft, n_target_rows, V, C, invT, Pu, segmax, sw.chunkmax, sw.state,
+            sw.ncand, sw.cw, sw.ci, info);
+        // the draw: every sequence's draw row weighed in chunks, then finished
+        const int Cs = split_chunks(B);
+        split_seq_sums_kernel<<<static_cast<unsigned>(B * Cs), kThreads, 0, s>>>(
+            target, draft, drafts, Kd, V, Cs, invT, static_cast<unsigned long long>(seed),
+            static_cast<unsigned long long>(offset), n_target_rows, info, segmax, segsum,
+            sw.chunk_tot, status);
+        split_seq_finish_kernel<<<B, kThreads, 0, s>>>(
+            target, draft, drafts, Kd, V, Cs, invT, static_cast<unsigned long long>(seed),
+            static_cast<unsigned long long>(offset), n_target_rows, info, segmax, segsum,
+            sw.chunk_tot, tokens, len, status);
+        return cudaGetLastError();
+    } else {
+        row_kernel<<<static_cast<unsigned>(rows), kRowThreads, smem, s>>>(
+            target, draft, n_target_rows, V, vec_ok, invT, static_cast<unsigned long long>(P),
+            top_k, static_cast<unsigned long long>(MP), info, segmax, target_bmax, draft_bmax);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     seq_kernel<<<B, kThreads, 0, s>>>(target, draft, drafts, Kd, V, vec_ok, invT,

@@ -26,7 +26,7 @@ inline cudaError_t set_attribute_per_device(std::atomic<unsigned long long>& onc
 
 constexpr int kMaxRows = 8;        // rows of one mma n-tile; verify rows per MoE segment
 constexpr int kMaxVerifyRows = 16; // dense verify rows per call: two n-tiles
-constexpr int kMaxSeg = 64;        // routed (token, expert) pairs per call
+constexpr int kMaxSeg = 128;       // routed (token, expert) pairs per call: 16 tokens x top-8
 constexpr int kTileRows = 128;     // weight rows per tile
 constexpr int kStageK = 256;       // k elements per pipeline stage
 constexpr int kMinUnitsPerCta = 4; // tile-aligned split-K: at least this many stages per part

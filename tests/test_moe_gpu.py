@@ -2,7 +2,8 @@
 
 MoE head: 128 experts, top-8, d = 2048; each expert's gate and up projections
 (2048 -> 768 each) are stored stacked as one 1536-row matrix, the down
-projection is 768 -> 2048; nvfp4; M = 8 tokens with seeded top-8 routing.
+projection is 768 -> 2048; nvfp4; M = 8 tokens with seeded top-8 routing, and
+1-16 tokens (up to 128 routed pairs).
 The activation between the two GEMMs (silu(gate) * up, rounded to bf16) is
 computed by the test harness and fed to both sides.
 """
@@ -36,7 +37,7 @@ def moe_head():
     return E, d, f, gu, dn
 
 
-@pytest.mark.parametrize("M", [8, 1, 3])
+@pytest.mark.parametrize("M", [8, 1, 3, 16, 12, 9])
 def test_moe_head_full_config(moe_head, M):
     E, d, f, (qg, sg, tg), (qd, sd, tdn) = moe_head
     ids, gates = synth.routing(300 + M, M, E, 8)
@@ -80,3 +81,25 @@ def test_moe_same_expert_for_every_token_and_bad_ids():
     ref, bnd = oracle.moe_w4(oracle.FMT_NVFP4, E, N, K, q, s, ts, A, 0, ids, gates, M, topk, 0)
     assert_gemm_close(out, ref, bnd, "moe shared expert")
     assert np.all(out[5 * topk] == 0.0)
+
+
+def test_moe_sixteen_tokens_crowded_expert():
+    """16 tokens x top-8 = 128 pairs, a third of them on one expert: that
+    expert's pairs fill several 8-row segments (each streams its weights),
+    the rest spread over the others; the combine sums the gates in order."""
+    E, N, K, M, topk = 16, 384, 512, 16, 8
+    q, s, ts = synth.linear(230, E * N, K, "nvfp4")
+    g = synth.rng(231)
+    ids = np.stack([g.permutation(E)[:topk] for _ in range(M)]).astype(np.int32)
+    ids[:6, 0] = 5
+    ids[6:12, 2] = 5
+    for m in range(M):   # keep each token's experts distinct
+        row = list(dict.fromkeys(ids[m].tolist()))
+        rest = [e for e in g.permutation(E).tolist() if e not in row]
+        ids[m] = (row + rest)[:topk]
+    gates = g.random((M, topk)).astype(np.float32)
+    A = synth.activations(synth.rng(232), M * topk, K)
+    out = moe_gpu(q, s, ts, E, A, 1, ids, gates, 1)
+    ref, bnd = oracle.moe_w4(oracle.FMT_NVFP4, E, N, K, q, s, ts, A, 1, ids, gates, M, topk, 1)
+    assert_gemm_close(out, ref, bnd, "moe 16 tokens, crowded expert")
+    assert vw4.vw4_get_device_status() == 0

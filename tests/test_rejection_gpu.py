@@ -199,12 +199,20 @@ def test_row_records_match_oracle_every_row_full_size():
     rec = vw4.vw4_rejection_row_records(ws, B, Kd, V).cpu().numpy()
     rec = rec.reshape(-1).view(np.dtype(vw4.ROW_RECORD_DTYPE))
     assert vw4.vw4_get_device_status() == 0
+    check_records(rec, target, draft)
+
+
+def check_records(rec, target, draft, top_p=0.95):
+    """Each row record against the oracle's masses: the max, the kept sum S,
+    and the kept set that (tau, cut) describe."""
+    B, R, V = target.shape
+    Kd = R - 1
     rows = [target[b, i] for b in range(B) for i in range(Kd + 1)] + \
            [draft[b, i] for b in range(B) for i in range(Kd)]
     assert len(rows) == len(rec)
     idx = np.arange(V)
     for r, row in enumerate(rows):
-        W, S = oracle.row_mass(row, 0.6, 0.95)
+        W, S = oracle.row_mass(row, 0.6, top_p)
         W_all, _ = oracle.row_mass(row, 0.6, 1.0)      # every mass before the cut
         g = rec[r]
         assert g["max"] == row.max(), (r, g["max"], row.max())
@@ -215,3 +223,37 @@ def test_row_records_match_oracle_every_row_full_size():
         kept_ref = W > 0
         assert np.array_equal(kept_gpu, kept_ref), (r, tau, cut, np.flatnonzero(kept_gpu ^ kept_ref)[:5])
         assert int(W_all[kept_gpu].sum()) == S
+
+
+@pytest.mark.parametrize("case", ["lm_head_flat", "integer_logits", "few_rows_sharp"])
+def test_split_rows_match_oracle(case):
+    """Few logits rows of a wide vocabulary take the split-row path (each row
+    in chunks over many CTAs; sums and histograms of exact integer masses):
+    the records and the committed ids against the oracle.  lm_head_flat: one
+    sequence, 7 drafts, 262144 logits of spread 1.5 (thousands of entries in
+    the bucket where the top-p cut falls); integer_logits: whole-number logits,
+    so tens of thousands of entries tie in that bucket and the row falls back
+    to the one-CTA search; few_rows_sharp: the sweep's N(0, 3) logits for 3
+    sequences."""
+    g = synth.rng({"lm_head_flat": 61, "integer_logits": 62, "few_rows_sharp": 63}[case])
+    if case == "lm_head_flat":
+        B, Kd, V = 1, 7, 262144
+        target = synth.logits(g, (B, Kd + 1, V), 1.5)
+        draft = synth.logits(g, (B, Kd, V), 1.5)
+    elif case == "integer_logits":
+        B, Kd, V = 2, 2, 131072
+        target = np.round(synth.logits(g, (B, Kd + 1, V), 1.5)).astype(np.float32)
+        draft = np.round(synth.logits(g, (B, Kd, V), 1.5)).astype(np.float32)
+    else:
+        B, Kd, V = 3, 4, 151936
+        target, draft, _ = synth.stochastic_case(63, B, Kd, V)
+    drafts = oracle.sample_drafts(draft, 0.6, 0.95, 7, 1 << 32)
+    ws = vw4.Workspace()
+    tok, ln = vw4.accept_rejection(torch.from_numpy(target).cuda(), torch.from_numpy(draft).cuda(),
+                                   torch.from_numpy(drafts).cuda(), 0.6, 0.95, 7, 0, workspace=ws)
+    rec = vw4.vw4_rejection_row_records(ws, B, Kd, V).cpu().numpy()
+    torch.cuda.synchronize()
+    assert vw4.vw4_get_device_status() == 0
+    check_records(rec.reshape(-1).view(np.dtype(vw4.ROW_RECORD_DTYPE)), target, draft)
+    rt, rl, _ = oracle.accept_rejection(target, draft, drafts, 0.6, 0.95, 7, 0)
+    assert np.array_equal(ln.cpu().numpy(), rl) and np.array_equal(tok.cpu().numpy(), rt)
