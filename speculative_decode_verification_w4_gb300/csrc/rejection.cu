@@ -707,15 +707,117 @@ __device__ void top_k_cut(const float* __restrict__ row, int V, bool vec, const 
     }
 }
 
+// The integer masses of log bucket beta: [wlo, wlo + 2^wbits).
+__device__ __forceinline__ void bucket_w_range(int beta, unsigned long long& wlo, int& wbits) {
+    if (beta < 16) {
+        wlo = static_cast<unsigned long long>(beta);
+        wbits = 0;
+    } else {
+        const int msb = 4 + (beta - 16) / 8, j = (beta - 16) % 8;
+        wbits = msb - 3;
+        wlo = static_cast<unsigned long long>(8 + j) << wbits;
+    }
+}
+
+// The cut of cut_from_candidates without sorting the members: their masses
+// lie in [wlo, wlo + 2^wbits); each level histograms the members still in
+// play by the next 8 bits of the mass (counts and exact masses), and the
+// sub-bucket where the running mass from the top crosses the target narrows
+// the range, until one mass tau is left.  The cut is then the jneed-th member
+// of mass tau in index order (jneed the fewest such entries whose mass
+// reaches the target), found by a radix selection on the indices: the entry
+// the sorted scan stops at.
+__device__ void cut_by_radix(RowSmem& sm, unsigned int total, unsigned long long wlo, int wbits,
+                             unsigned long long above_in, u128 TGT, RowInfo& info) {
+    const int tid = threadIdx.x;
+    unsigned long long lo = wlo, above = above_in, n_eq = total;
+    int wb = wbits;
+    while (wb > 0) {
+        const int bits = wb < 8 ? wb : 8;
+        const int shift = wb - bits;
+        const unsigned long long hi = lo + (1ull << wb);
+        for (int t = tid; t < kLinBuckets; t += kRowThreads) {
+            sm.cnt[t] = 0u;
+            sm.lmass[t] = 0ull;
+        }
+        __syncthreads();
+        for (unsigned int t = tid; t < total; t += kRowThreads) {
+            const unsigned long long W = sm.cw[t];
+            if (W >= lo && W < hi) {
+                const int bk = static_cast<int>((W - lo) >> shift);
+                atomicAdd(&sm.cnt[bk], 1u);
+                atomic_add_u64_split(&sm.lmass[bk], W);
+            }
+        }
+        __syncthreads();
+        const int t = (1 << bits) - 1 - tid;  // thread tid holds sub-bucket t, masses descending
+        const unsigned long long mt = t >= 0 ? sm.lmass[t] : 0ull;
+        u128 tot2;
+        const u128 inc = block_excl_u128(static_cast<u128>(mt), sm.red, tot2) + mt;
+        if (t >= 0 && ((above + inc) << 32) >= TGT && ((above + inc - mt) << 32) < TGT) {
+            sm.lo = lo + (static_cast<unsigned long long>(t) << shift);
+            sm.above = static_cast<unsigned long long>(above + inc - mt);
+            sm.n_eq = sm.cnt[t];
+        }
+        __syncthreads();
+        lo = sm.lo;
+        above = sm.above;
+        n_eq = sm.n_eq;
+        wb = shift;
+        __syncthreads();
+    }
+    const unsigned long long tau = lo;
+    const u128 num = TGT - (static_cast<u128>(above) << 32);
+    const u128 den = static_cast<u128>(tau) << 32;
+    unsigned long long jneed = static_cast<unsigned long long>((num + den - 1) / den);
+    if (jneed > n_eq) jneed = n_eq;  // (not reached: the crossing lies in this mass)
+    // the jneed-th index among the members of mass tau: 8 bits a level
+    unsigned int prefix = 0u;
+    unsigned long long need = jneed;
+    for (int sh = 16; sh >= 0; sh -= 8) {
+        for (int t = tid; t < kLinBuckets; t += kRowThreads) sm.cnt[t] = 0u;
+        __syncthreads();
+        for (unsigned int t = tid; t < total; t += kRowThreads) {
+            const unsigned int ix = static_cast<unsigned int>(sm.ci[t]);
+            if (sm.cw[t] == tau && (ix >> (sh + 8)) == (prefix >> (sh + 8)))
+                atomicAdd(&sm.cnt[(ix >> sh) & 255u], 1u);
+        }
+        __syncthreads();
+        const unsigned long long ct = tid < kLinBuckets ? sm.cnt[tid] : 0u;  // ascending
+        u128 tot3;
+        const unsigned long long ex =
+            static_cast<unsigned long long>(block_excl_u128(static_cast<u128>(ct), sm.red, tot3));
+        if (tid < kLinBuckets && ex < need && need <= ex + ct) {
+            sm.cut_found = tid;
+            sm.count_eq = need - ex;
+        }
+        __syncthreads();
+        prefix |= static_cast<unsigned int>(sm.cut_found) << sh;
+        need = sm.count_eq;
+        __syncthreads();
+    }
+    info.tau = tau;
+    info.S = above + jneed * tau;
+    info.cut = static_cast<int>(prefix);
+}
+
 // The cut inside the crossing bucket from its gathered members sm.cw / sm.ci
 // (total <= kCutCand, in any order): sorted by (W desc, index asc), then the
 // running mass from `above_in` down the list; the first entry whose running
 // mass reaches TGT / 2^32 is the cut.  Sets info.tau, info.cut, info.S (valid
 // in every thread).
 __device__ void cut_from_candidates(RowSmem& sm, unsigned int total, unsigned long long above_in,
-                                    u128 TGT, RowInfo& info) {
+                                    u128 TGT, RowInfo& info, int beta) {
     const int tid = threadIdx.x;
-    if (total <= static_cast<unsigned int>(kRankSortMax)) {
+    if (total > static_cast<unsigned int>(kRankSortMax)) {
+        // many members: select the cut by radix instead of sorting them
+        unsigned long long wlo;
+        int wbits;
+        bucket_w_range(beta, wlo, wbits);
+        cut_by_radix(sm, total, wlo, wbits, above_in, TGT, info);
+        return;
+    }
+    {
         // few: each candidate's place is the number that precede it
         unsigned long long wt = 0ull;
         int it = 0x7fffffff;
@@ -735,35 +837,6 @@ __device__ void cut_from_candidates(RowSmem& sm, unsigned int total, unsigned lo
             sm.ci[place] = it;
         }
         __syncthreads();
-    } else {
-        // pad to a power of two, bitonic sort by (W desc, index asc)
-        unsigned int pw = 1;
-        while (pw < total) pw <<= 1;
-        for (unsigned int t = total + tid; t < pw; t += kRowThreads) {
-            sm.cw[t] = 0ull;
-            sm.ci[t] = 0x7fffffff;
-        }
-        __syncthreads();
-        for (unsigned int kk = 2; kk <= pw; kk <<= 1) {
-            for (unsigned int j = kk >> 1; j > 0; j >>= 1) {
-                for (unsigned int t = tid; t < pw; t += kRowThreads) {
-                    const unsigned int u = t ^ j;
-                    if (u > t) {
-                        const unsigned long long wa = sm.cw[t], wb = sm.cw[u];
-                        const int ia = sm.ci[t], ib = sm.ci[u];
-                        const bool a_first = wa > wb || (wa == wb && ia < ib);
-                        const bool up = (t & kk) == 0;
-                        if (up != a_first) {
-                            sm.cw[t] = wb;
-                            sm.cw[u] = wa;
-                            sm.ci[t] = ib;
-                            sm.ci[u] = ia;
-                        }
-                    }
-                }
-                __syncthreads();
-            }
-        }
     }
     // running mass down the sorted list; the first crossing is the cut
     constexpr int kCutPer = kCutCand / kRowThreads;  // candidates per thread
@@ -962,7 +1035,7 @@ __device__ RowInfo row_cut(const float* __restrict__ row, int V, bool vec, float
     __syncthreads();
     const unsigned int total = sm.ncand;
     if (total <= static_cast<unsigned int>(kCutCand)) {
-        cut_from_candidates(sm, total, sm.above, TGT, info);
+        cut_from_candidates(sm, total, sm.above, TGT, info, beta);
         return info;
     }
 
@@ -1434,22 +1507,33 @@ __global__ void __launch_bounds__(kRowThreads) split_gather_kernel(
     x_window(wlo, whi, xa, xb);
     const float* seg = segmax + r * nseg;
     const float4* r4 = reinterpret_cast<const float4*>(split_row(target, draft, n_target_rows, r, V));
-    for (int sg = s0 + wid; sg < s1; sg += kRowWarps) {
-        if (scaled_x(__ldcg(seg + sg), mx, invT) < xa) continue;  // the same for the warp
-        const int i = sg * 32 + lane;
-        if (i >= V4) continue;
-        const float4 a = __ldg(r4 + i);
-        const float lv[4] = {a.x, a.y, a.z, a.w};
+    // four segments of the warp at a time, their loads first (a segment whose
+    // max lies below the window holds no member)
+    for (int sg0 = s0 + wid; sg0 < s1; sg0 += 4 * kRowWarps) {
+        float4 v[4];
+        bool in[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float x = scaled_x(lv[q], mx, invT);
-            if (x >= xa && x < xb) {
-                const float e = own_exp(x);
-                if (e >= b_lo && e < b_hi) {
-                    const unsigned int slot = atomicAdd(&ncand[r], 1u);
-                    if (slot < static_cast<unsigned int>(kCutCand)) {
-                        cw[r * kCutCand + slot] = mass_of(e);
-                        ci[r * kCutCand + slot] = 4 * i + q;
+        for (int j = 0; j < 4; ++j) {
+            const int sg = sg0 + j * kRowWarps, i = sg * 32 + lane;
+            in[j] = sg < s1 && i < V4 && !(scaled_x(__ldcg(seg + sg), mx, invT) < xa);
+            v[j] = in[j] ? __ldg(r4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (!in[j]) continue;
+            const int i = (sg0 + j * kRowWarps) * 32 + lane;
+            const float lv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float x = scaled_x(lv[q], mx, invT);
+                if (x >= xa && x < xb) {
+                    const float e = own_exp(x);
+                    if (e >= b_lo && e < b_hi) {
+                        const unsigned int slot = atomicAdd(&ncand[r], 1u);
+                        if (slot < static_cast<unsigned int>(kCutCand)) {
+                            cw[r * kCutCand + slot] = mass_of(e);
+                            ci[r * kCutCand + slot] = 4 * i + q;
+                        }
                     }
                 }
             }
@@ -1485,7 +1569,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) split_cut_kernel(
         info.tk_key = 0u;
         info.tk_idx = 0x7fffffff;
         const u128 TGT = static_cast<u128>(P) * st.S;
-        cut_from_candidates(sm, total, st.above, TGT, info);
+        cut_from_candidates(sm, total, st.above, TGT, info, st.beta);
     } else {
         const float* row = split_row(target, draft, n_target_rows, r, V);
         info = row_stats(row, V, true, invT, P, 0, 0ull, segmax + r * n_segments(V), nullptr, sm);
