@@ -130,10 +130,13 @@ typedef struct vw4_sampling {
  *             aligned, reused freely between calls on the same stream.
  * Error behaviour: VW4_ERR_INVALID_ARG for null pointers, M outside 1..16,
  * N < 1, K not a positive multiple of the block, lda < K, ldo < N;
- * VW4_ERR_UNSUPPORTED when K is a multiple of the block but not of 256 (the
- * weights are streamed by TMA tensor copies in 256-wide k stages, which need
- * row pitches of K/2 and K/16 bytes that are multiples of 16: every K of the
- * dense-layer, LM-head and MoE configurations is a multiple of 256);
+ * K a multiple of the block but not of 256 is accepted on a slower path: the
+ * weights are streamed by TMA tensor copies in 256-wide k stages, whose row
+ * pitches (K/2 and K/16 bytes) must be multiples of 16, so such a call first
+ * copies the weights and scales, zero-padded to whole stages, into the
+ * workspace (vw4_workspace_bytes counts the room) and reads them twice;
+ * every K of the dense-layer, LM-head and MoE configurations is a multiple
+ * of 256;
  * VW4_ERR_ALIGN for misaligned pointers or leading dimensions;
  * VW4_ERR_WORKSPACE when the workspace is too small.
  *
@@ -232,7 +235,9 @@ VW4_API vw4_status verify_greedy_w4(const vw4_weight* W, const void* A_dev, int 
  * combine     0: out[p][n] for every pair p (out has M*topk rows);
  *             1: out[m][n] = sum_j gates[m][j] * pair(m, j)[n], j ascending.
  * Each touched expert streams its weights once for all its pair rows.
- * Error behaviour as verify_gemm_w4; an expert id outside [0, E) sets
+ * Error behaviour as verify_gemm_w4, except that K must be a multiple of 256
+ * (VW4_ERR_UNSUPPORTED otherwise: the experts are streamed in place); an
+ * expert id outside [0, E) sets
  * VW4_DEV_BAD_EXPERT_ID and that pair contributes zeros.
  */
 VW4_API vw4_status verify_moe_w4(const vw4_weight* experts, int E, const void* A_dev, int lda,

@@ -151,10 +151,11 @@ vw4_status check_weight(const vw4_weight* W) {
     if (W->fmt == VW4_FMT_Q4_0 && W->tensor_scale != 1.0f) return VW4_ERR_INVALID_ARG;
     if (!std::isfinite(W->tensor_scale)) return VW4_ERR_INVALID_ARG;
     if (!aligned16(W->q_dev) || !aligned16(W->scales_dev)) return VW4_ERR_ALIGN;
-    // the TMA path streams 256-wide k slices with 16-byte-multiple row pitches
-    if (W->K % kStageK != 0) return VW4_ERR_UNSUPPORTED;
     return VW4_OK;
 }
+
+// K rounded up to whole 256-wide stages (the TMA path's row pitches).
+int padded_k(int K) { return (K + kStageK - 1) / kStageK * kStageK; }
 
 }  // namespace
 }  // namespace vw4
@@ -189,8 +190,11 @@ VW4_API void vw4_test_inject_stall(int calls) { g_stall_calls.store(calls > 0 ? 
 VW4_API size_t vw4_workspace_bytes(int op, int a, int b, int c) {
     if (op == VW4_OP_GEMM) {
         const int M = a, N = b, K = c;
-        if (M < 1 || M > kMaxVerifyRows || N < 1 || K < kStageK || K % kStageK) return 0;
-        return gemm_workspace_layout(nullptr, 1, N, K, kMaxGrid, 0, gemm_rows_for(M)).bytes;
+        if (M < 1 || M > kMaxVerifyRows || N < 1 || K < 16 || K % 16) return 0;
+        // K not a multiple of 256: room for the weights padded to whole stages
+        const int Kp = padded_k(K);
+        return gemm_workspace_layout(nullptr, 1, N, Kp, kMaxGrid, 0, gemm_rows_for(M),
+                                     Kp != K ? N : 0).bytes;
     }
     if (op == VW4_OP_MOE) {
         const int P = a, N = b, K = c;
@@ -232,22 +236,34 @@ static vw4_status gemm_entry(const vw4_weight* W, const void* A_dev, int M, int 
         return VW4_ERR_ALIGN;
     if (!workspace_dev) return VW4_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace_dev) & 255u) != 0) return VW4_ERR_ALIGN;
-    const int N = W->N, K = W->K;
+    const int N = W->N, K_true = W->K;
+    // K not a multiple of 256: the weights are first copied, zero-padded, into
+    // the workspace, and the stages run over the padded K
+    const int K = padded_k(K_true);
+    const bool pad = K != K_true;
     // 1..8 rows: one mma n-tile; 9..16: two n-tiles over the same weights
     const int nr = gemm_rows_for(M);
-    GemmWorkspace ws = gemm_workspace_layout(workspace_dev, 1, N, K, kMaxGrid, 0, nr);
+    GemmWorkspace ws = gemm_workspace_layout(workspace_dev, 1, N, K, kMaxGrid, 0, nr, pad ? N : 0);
     if (ws.bytes > ws_bytes) return VW4_ERR_WORKSPACE;
     DeviceInfo* d = nullptr;
     st = device_info(&d);
     if (st != VW4_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
+    const void* q_src = W->q_dev;
+    const void* s_src = W->scales_dev;
+    if (pad) {
+        cudaError_t e = launch_pad_weights(W->q_dev, W->scales_dev, N, K_true, K, ws.wpad, ws.spad, s);
+        if (e != cudaSuccess) return cuda_fail(e, "pad_weights launch");
+        q_src = ws.wpad;
+        s_src = ws.spad;
+    }
     CUtensorMap tmW, tmS;
     const int sgroup = K / kStageK < kScaleGroup ? K / kStageK : kScaleGroup;
-    st = make_map(&tmW, W->q_dev, static_cast<uint64_t>(K) / 2, N, kStageK / 2, kTileRows,
+    st = make_map(&tmW, q_src, static_cast<uint64_t>(K) / 2, N, kStageK / 2, kTileRows,
                   CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != VW4_OK) return st;
-    st = make_map(&tmS, W->scales_dev, static_cast<uint64_t>(K) / 16, N, 16 * sgroup, kTileRows,
+    st = make_map(&tmS, s_src, static_cast<uint64_t>(K) / 16, N, 16 * sgroup, kTileRows,
                   CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != VW4_OK) return st;
 
@@ -278,7 +294,8 @@ static vw4_status gemm_entry(const vw4_weight* W, const void* A_dev, int M, int 
         split > 1 && split <= kMaxClusterSplit && !fused_argmax && bmax_dev == nullptr;
 
     cudaError_t e = launch_prep_act(static_cast<const uint16_t*>(A_dev), lda, K, W->fmt, M, 0, 1,
-                                    1, ws, n_tiles * kConsumerWarps, s, nr);
+                                    1, ws, n_tiles * kConsumerWarps, s, nr, nullptr, 0, nullptr,
+                                    nullptr, 0, 0, K_true);
     if (e != cudaSuccess) return cuda_fail(e, "prep_act launch");
     GemmParams p{};
     p.N = N;
@@ -351,6 +368,8 @@ VW4_API vw4_status verify_moe_w4(const vw4_weight* experts, int E, const void* A
                                  void* stream) {
     vw4_status st = check_weight(experts);
     if (st != VW4_OK) return st;
+    // the experts are streamed in place: their rows need whole 256-wide stages
+    if (experts->K % kStageK != 0) return VW4_ERR_UNSUPPORTED;
     if (E < 1 || !A_dev || !expert_ids_dev || !out_dev) return VW4_ERR_INVALID_ARG;
     if (combine && !gates_dev) return VW4_ERR_INVALID_ARG;
     if (M < 1 || M > kMaxVerifyRows || topk < 1 || topk > kMaxRows || M * topk > kMaxSeg)
@@ -619,10 +638,11 @@ extern "C" {
 VW4_API vw4_status verify_gemm_w4_noalloc(const vw4_weight* W, const void* A_dev, int M, int lda,
                                           float* out_dev, int ldo, int32_t* row_argmax_dev,
                                           void* stream) {
-    if (W && W->N >= 1 && W->K >= kStageK && W->K % kStageK == 0 && M >= 1 &&
-        M <= kMaxVerifyRows) {
-        const size_t need =
-            gemm_workspace_layout(nullptr, 1, W->N, W->K, kMaxGrid, 0, gemm_rows_for(M)).bytes;
+    if (W && W->N >= 1 && W->K >= 16 && W->K % 16 == 0 && M >= 1 && M <= kMaxVerifyRows) {
+        const int Kp = padded_k(W->K);
+        const size_t need = gemm_workspace_layout(nullptr, 1, W->N, Kp, kMaxGrid, 0,
+                                                  gemm_rows_for(M), Kp != W->K ? W->N : 0)
+                                .bytes;
         if (need > kNoAllocScratchBytes) {
             char buf[160];
             snprintf(buf, sizeof buf,

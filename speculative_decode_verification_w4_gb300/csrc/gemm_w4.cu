@@ -49,7 +49,7 @@ constexpr uint32_t kStatusBadExpert = 0x2u;
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 GemmWorkspace gemm_workspace_layout(void* base, int n_seg_max, int N, int K, int grid,
-                                    int pair_rows, int nr) {
+                                    int pair_rows, int nr, int pad_rows) {
     GemmWorkspace w{};
     char* b = static_cast<char*>(base);
     size_t off = 0;
@@ -68,8 +68,47 @@ GemmWorkspace gemm_workspace_layout(void* base, int n_seg_max, int N, int K, int
     w.am_cnt = static_cast<uint32_t*>(take(4));
     w.pair_out = pair_rows ? static_cast<float*>(take((size_t)pair_rows * N * sizeof(float)))
                            : nullptr;
+    w.wpad = pad_rows ? static_cast<uint8_t*>(take((size_t)pad_rows * (K / 2))) : nullptr;
+    w.spad = pad_rows ? static_cast<uint8_t*>(take((size_t)pad_rows * (K / 16))) : nullptr;
     w.bytes = off;
     return w;
+}
+
+// ------------------------------------------------------------ padded weights
+// A matrix whose K is a multiple of the block but not of 256 (row pitches of
+// K/2 and K/16 bytes that TMA cannot address) is copied into rows of Kp/2
+// nibble bytes and Kp/16 scale bytes (Kp = K rounded up to 256), zero past K:
+// zero nibbles and zero scales are weights of exactly 0 in both formats.
+// Both formats keep K/16 scale bytes per row (nvfp4: one E4M3 per 16; Q4_0:
+// one fp16 per 32).
+__global__ void pad_weights_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ sc,
+                                   int N, int K, int Kp, uint8_t* __restrict__ qo,
+                                   uint8_t* __restrict__ so) {
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    const long long t0 = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+    // nibbles in 8-byte units (K / 2 is a multiple of 8, rows start 8-byte aligned)
+    const int in8 = K / 16, out8 = Kp / 16;
+    const unsigned long long* q8 = reinterpret_cast<const unsigned long long*>(q);
+    unsigned long long* qo8 = reinterpret_cast<unsigned long long*>(qo);
+    for (long long i = t0; i < static_cast<long long>(N) * out8; i += stride) {
+        const long long row = i / out8;
+        const int j = static_cast<int>(i % out8);
+        qo8[i] = j < in8 ? q8[row * in8 + j] : 0ull;
+    }
+    // scales, byte by byte (K / 16 bytes a row, any alignment)
+    const int ins = K / 16, outs = Kp / 16;
+    for (long long i = t0; i < static_cast<long long>(N) * outs; i += stride) {
+        const long long row = i / outs;
+        const int j = static_cast<int>(i % outs);
+        so[i] = j < ins ? sc[row * ins + j] : static_cast<uint8_t>(0);
+    }
+}
+
+cudaError_t launch_pad_weights(const void* q, const void* sc, int N, int K, int Kp, uint8_t* qo,
+                               uint8_t* so, cudaStream_t s) {
+    pad_weights_kernel<<<1216, 256, 0, s>>>(static_cast<const uint8_t*>(q),
+                                             static_cast<const uint8_t*>(sc), N, K, Kp, qo, so);
+    return cudaGetLastError();
 }
 
 // ------------------------------------------------------------ small helpers
@@ -190,7 +229,8 @@ __device__ void route_pairs(const int32_t* __restrict__ ids, int P, int E, SegTa
 // rows (out_zero, when the pair rows are the output).
 // One warp per verify row: 256 threads (8 rows) or 512 (16 rows, dense only).
 __global__ void __launch_bounds__(512) prep_act_kernel(
-    const uint16_t* __restrict__ A, int lda, int vec_ok, int K, int fmt, int nr, int dense_M,
+    const uint16_t* __restrict__ A, int lda, int vec_ok, int K, int K_true, int fmt, int nr,
+    int dense_M,
     int rows_are_pairs, int topk, SegTable* seg, uint8_t* act, uint32_t* tile_cnt, int n_cnt,
     unsigned long long* am_key, uint32_t* am_cnt, const int32_t* __restrict__ ids, int P, int E,
     uint32_t* status, float* out_zero, int ldo, int N) {
@@ -264,7 +304,13 @@ __global__ void __launch_bounds__(512) prep_act_kernel(
     }
     const uint16_t* a = A + static_cast<size_t>(src_row) * lda + st * kStageK;
     float x[8];
-    if (fmt == 1) {
+    // past K_true (a K padded to whole stages) the activations are zero; a
+    // lane's 8 (nvfp4) or 32-block (Q4_0) elements lie wholly on one side
+    const int k_lane = st * kStageK + (fmt == 1 ? 8 * lane : 32 * (lane >> 2));
+    if (k_lane >= K_true) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+    } else if (fmt == 1) {
         load8_bf16(a + 8 * lane, vec_ok != 0, x);
     } else {
         const int beta = lane >> 2, c = lane & 3;
@@ -1209,7 +1255,7 @@ __global__ void q4_0_split_kernel(const uint8_t* __restrict__ blocks, int N, int
 cudaError_t launch_prep_act(const uint16_t* A, int lda, int K, int fmt, int dense_M,
                             int rows_are_pairs, int topk, int n_seg_grid, const GemmWorkspace& ws,
                             int n_counters, cudaStream_t s, int nr, const int32_t* ids, int E,
-                            uint32_t* status, float* out_zero, int ldo, int N) {
+                            uint32_t* status, float* out_zero, int ldo, int N, int K_true) {
     if ((nr != 8 && nr != 16) || (nr == 16 && dense_M <= 0)) return cudaErrorInvalidValue;
     const int T = K / kStageK;
     const int vec_ok = ((reinterpret_cast<uintptr_t>(A) & 15u) == 0 && lda % 8 == 0) ? 1 : 0;
@@ -1224,7 +1270,8 @@ cudaError_t launch_prep_act(const uint16_t* A, int lda, int K, int fmt, int dens
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prep_act_kernel, A, lda, vec_ok, K, fmt, nr, dense_M,
+    return cudaLaunchKernelEx(&cfg, prep_act_kernel, A, lda, vec_ok, K, K_true > 0 ? K_true : K,
+                              fmt, nr, dense_M,
                               rows_are_pairs, topk, ws.seg, ws.act, ws.tile_cnt, n_counters,
                               ws.am_key, ws.am_cnt, ids, dense_M > 0 ? 0 : n_seg_grid, E, status,
                               out_zero, ldo, N);

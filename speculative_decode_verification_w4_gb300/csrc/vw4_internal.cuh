@@ -99,6 +99,8 @@ struct GemmWorkspace {
     unsigned long long* am_key;  // [16] packed (value, ~index) running maxima
     uint32_t* am_cnt;            // [1] quarter-tile tickets of the argmax
     float* pair_out;             // [pairs][N] MoE pair rows before the combine
+    uint8_t* wpad;               // [N][Kp/2] nibbles padded to whole stages (K % 256 != 0)
+    uint8_t* spad;               // [N][Kp/16] their scales
     size_t bytes;
 };
 
@@ -140,8 +142,10 @@ struct GemmParams {
 
 // Lays the GEMM/MoE workspace out from `base` (nullptr: size only) for
 // blocks of nr (8 or 16) verify rows.
+// K: the stages' K (a multiple of 256); pad_rows > 0: room for a copy of
+// that many weight rows padded to K.
 GemmWorkspace gemm_workspace_layout(void* base, int n_seg_max, int N, int K, int grid,
-                                    int pair_rows, int nr);
+                                    int pair_rows, int nr, int pad_rows = 0);
 
 // Kernel launchers (gemm_w4.cu).  All asynchronous on `s`.
 // nr: rows per activation block (8, or 16 for a dense call of 9..16 rows)
@@ -149,7 +153,9 @@ cudaError_t launch_prep_act(const uint16_t* A, int lda, int K, int fmt, int dens
                             int rows_are_pairs, int topk, int n_seg_grid, const GemmWorkspace& ws,
                             int n_counters, cudaStream_t s, int nr, const int32_t* ids = nullptr,
                             int E = 0, uint32_t* status = nullptr, float* out_zero = nullptr,
-                            int ldo = 0, int N = 0);
+                            int ldo = 0, int N = 0, int K_true = 0);
+cudaError_t launch_pad_weights(const void* q, const void* sc, int N, int K, int Kp, uint8_t* qo,
+                               uint8_t* so, cudaStream_t s);
 cudaError_t launch_gemm(int fmt, int nr, const CUtensorMap& tmW, const CUtensorMap& tmS,
                         const GemmParams& p, int grid, int cluster, cudaStream_t s);
 cudaError_t launch_combine(const float* pair_out, const float* gates, const int32_t* ids,

@@ -76,7 +76,7 @@ def test_gemm_argument_checks_on_host(lib, kw, code):
 
 @pytest.mark.parametrize("W,code", [
     (_weight(fmt=3), 1), (_weight(K=24), 1), (_weight(fmt=2, ts=2.0), 1),
-    (_weight(q=0x1001), 3), (_weight(K=272), 2), (_weight(N=0), 1),
+    (_weight(q=0x1001), 3), (_weight(N=0), 1),
 ])
 def test_weight_checks_on_host(lib, W, code):
     r = lib.verify_gemm_w4(ctypes.byref(W), 0x3000, 2, 512, 0x4000, 128, None, 0x10000,
@@ -135,3 +135,18 @@ def test_verify_greedy_argument_checks_on_host(lib):
                                 0x10000, 1 << 30, None) == 1
     assert lib.verify_greedy_w4(ctypes.byref(W), 0x3000, 512, None, 1, 3, 0x200, 0x300, None, 0,
                                 0x10000, 1 << 30, None) == 1
+
+
+def test_ragged_k_sizes_and_moe_rule(lib):
+    """K a multiple of the block but not of 256: the dense GEMM sizes room for
+    the weights padded to whole stages; the MoE call (its experts streamed in
+    place) returns VW4_ERR_UNSUPPORTED on the host."""
+    w256 = vw4.vw4_workspace_bytes(vw4.OP_GEMM, 8, 1000, 256)
+    w272 = vw4.vw4_workspace_bytes(vw4.OP_GEMM, 8, 1000, 272)
+    assert w272 >= w256 + 1000 * (512 // 2) + 1000 * (512 // 16)
+    assert vw4.vw4_workspace_bytes(vw4.OP_GEMM, 8, 1000, 24) == 0
+    assert vw4.vw4_workspace_bytes(vw4.OP_MOE, 8, 1000, 272) == 0
+    W = _weight(K=272, N=64)
+    r = lib.verify_moe_w4(ctypes.byref(W), 4, 0x3000, 512, 0, 0x5000, 0x6000, 2, 2, 1, 0x4000,
+                          64, 0x10000, 1 << 30, None)
+    assert r == 2

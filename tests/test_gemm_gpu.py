@@ -257,3 +257,34 @@ def test_mixed_magnitude_stage_below_the_exact_range(tiny_exp):
     extra = 2.0 ** -39 * (amax_k @ np.abs(w).T)                      # [M, N]
     err = np.abs(gpu.astype(np.float64) - ref)
     assert np.all(err <= 1e-3 * bnd + extra), float(np.max(err - 1e-3 * bnd - extra))
+
+
+@pytest.mark.parametrize("fmt,K", [("nvfp4", 272), ("nvfp4", 1040), ("nvfp4", 5136),
+                                   ("q4_0", 288), ("q4_0", 1056), ("q4_0", 5152)])
+@pytest.mark.parametrize("N,M", [(300, 8), (5000, 1), (1000, 12)])
+def test_k_not_a_multiple_of_256(fmt, K, N, M):
+    """K a multiple of the format's block (16 nvfp4, 32 Q4_0) but not of 256:
+    the weights are padded to whole stages in the workspace, the activations
+    read as zero past K; element by element against the oracle."""
+    q, s, ts, A = _case(fmt, 3 * K + N + M, N, K, M)
+    gpu = gemm_gpu(fmt, q, s, ts, A).cpu().numpy()
+    ref, bnd = oracle.gemm_w4(ORACLE_FMT[fmt], N, K, q, s, ts, A)
+    assert_gemm_close(gpu, ref, bnd, f"{fmt} N={N} K={K} M={M}")
+
+
+def test_k_not_a_multiple_of_256_fused_argmax_and_greedy():
+    N, K, B, Kd = 20000, 1040, 1, 7
+    M = B * (Kd + 1)
+    q, s, ts, A = _case("nvfp4", 77, N, K, M)
+    qd, sd = upload_weight(q, s, "nvfp4")
+    Ad = bf16_dev(A)
+    am = torch.empty((M,), dtype=torch.int32, device="cuda")
+    logits = vw4.verify_gemm_w4(vw4.FMT_NVFP4, qd, sd, ts, Ad, row_argmax=am)
+    lg = logits.cpu().numpy()
+    assert np.array_equal(am.cpu().numpy(), lg.argmax(axis=1))
+    drafts = synth.greedy_drafts(synth.rng(78), am.cpu().numpy()[None, :Kd], N)
+    tok, ln = vw4.verify_greedy_w4(vw4.FMT_NVFP4, qd, sd, ts, Ad, torch.from_numpy(drafts).cuda())
+    torch.cuda.synchronize()
+    rt, rl, _ = oracle.accept_greedy(lg.reshape(B, Kd + 1, N), drafts)
+    assert np.array_equal(tok.cpu().numpy(), rt) and np.array_equal(ln.cpu().numpy(), rl)
+    assert vw4.vw4_get_device_status() == 0
