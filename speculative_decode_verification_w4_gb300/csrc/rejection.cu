@@ -354,6 +354,8 @@ __device__ __forceinline__ void atomic_add_u64_split(unsigned long long* a, unsi
 // members of the crossing bucket, in the segments that can hold them.
 constexpr int kRowThreads = 512;
 constexpr int kRowWarps = kRowThreads / 32;
+constexpr int kHistQ = 24;       // queue slots per lane (MassPass)
+constexpr int kHistGroup = 16;   // entries a lane may push between two checks
 static_assert(kRowThreads >= kLogBuckets, "one thread per log bucket in the suffix scan");
 
 struct RowSmem {
@@ -362,8 +364,13 @@ struct RowSmem {
     unsigned long long mass[kLogBuckets];             // merged
     unsigned int cnt[kLinBuckets];                    // radix fallback: counts
     unsigned long long lmass[kLinBuckets];            //                 masses
-    unsigned long long cw[kCutCand];                  // crossing-bucket members
-    int ci[kCutCand];
+    union {
+        struct {
+            unsigned long long cw[kCutCand];  // crossing-bucket members
+            int ci[kCutCand];
+        };
+        float hq[kRowWarps][kHistQ][32];  // the mass pass's histogram queues
+    };
     unsigned int ncand;
     int beta, wbits, cut_found;
     unsigned long long above, lo, width, n_eq, count_eq;
@@ -461,6 +468,81 @@ __device__ __forceinline__ uint32_t stream_count(int V, bool vec) {
     }
     return tid < V ? static_cast<uint32_t>((V - 1 - tid) / kRowThreads + 1) : 0u;
 }
+
+// The mass pass over a lane's entries, two at a time with packed fp32-pair
+// operations: the integer masses W = floor(own_exp(x) 2^40) summed exactly
+// (as the two 20-bit halves' 2^23-biased bit patterns, mod 2^32; the true
+// sums stay below 2^32), and every W >= cmin added to the warp's mass
+// histogram.  Only a few entries reach cmin, so a lane does not add them as
+// it meets them (the whole warp would step through the insertion for the one
+// lane that has one): it queues their f = own_exp(x) 2^40 in its own column of
+// a shared-memory queue, and the warp empties all its lanes' queues together
+// when one of them runs full, recomputing each W from f bit for bit.
+struct MassPass {
+    float2 nmx, it2;
+    float f_lo;               // f < f_lo proves W < cmin (cmin rounded down)
+    unsigned long long cmin;
+    unsigned long long* hist; // the warp's histogram [kLogBuckets]
+    float* q0;                // this lane's queue column: slot s at q0[32 s]
+    float* qp;                // next free slot
+    uint32_t sum_hib, sum_lob, n;
+
+    __device__ __forceinline__ void init(float mx, float invT, unsigned long long cmin_,
+                                         float f_lo_, unsigned long long* hist_, float* col) {
+        nmx = make_float2(-mx, -mx);
+        it2 = make_float2(invT, invT);
+        cmin = cmin_;
+        f_lo = f_lo_;
+        hist = hist_;
+        q0 = col;
+        qp = col;
+        sum_hib = sum_lob = n = 0u;
+    }
+    __device__ __forceinline__ void pair(float la, float lb) {
+        const float2 k20 = make_float2(9.5367431640625e-07f, 9.5367431640625e-07f);
+        const float2 m20 = make_float2(-1048576.0f, -1048576.0f);
+        const float2 b23 = make_float2(8388608.0f, 8388608.0f);
+        const float2 nb23 = make_float2(-8388608.0f, -8388608.0f);
+        const float2 f = own_exp_2_40_x2(__fmul2_rn(__fadd2_rn(make_float2(la, lb), nmx), it2));
+        const float2 t1 = __fadd2_rd(__fmul2_rn(f, k20), b23);
+        const float2 t2 = __fadd2_rd(__ffma2_rn(__fadd2_rn(t1, nb23), m20, f), b23);
+        sum_hib += __float_as_uint(t1.x) + __float_as_uint(t1.y);
+        sum_lob += __float_as_uint(t2.x) + __float_as_uint(t2.y);
+        n += 2u;
+        if (f.x >= f_lo) { *qp = f.x; qp += 32; }
+        if (f.y >= f_lo) { *qp = f.y; qp += 32; }
+    }
+    __device__ __forceinline__ void quad(const float4& v) {
+        pair(v.x, v.y);
+        pair(v.z, v.w);
+    }
+    // empties the warp's queues into the histogram (every lane calls it)
+    __device__ __forceinline__ void drain() {
+        const int mine = static_cast<int>((qp - q0) >> 5);
+        const int rounds = __reduce_max_sync(0xffffffffu, mine);
+        for (int r = 0; r < rounds; ++r) {
+            if (r < mine) {
+                const float f = q0[32 * r];
+                uint32_t hib, lob;
+                mass_bits(f, hib, lob);
+                const unsigned long long W =
+                    (static_cast<unsigned long long>(hib - 0x4B000000u) << 20) |
+                    (lob - 0x4B000000u);
+                if (W >= cmin) atomic_add_u64_split(&hist[log_bucket_f(f)], W);
+            }
+        }
+        qp = q0;
+    }
+    // after at most kHistGroup entries per lane since the last call
+    __device__ __forceinline__ void check() {
+        if (__any_sync(0xffffffffu, (qp - q0) > 32 * (kHistQ - kHistGroup))) drain();
+    }
+    // the lane's exact sum of W (its entries' halves, with the bias removed)
+    __device__ __forceinline__ unsigned long long sum() const {
+        const uint32_t bias = n * 0x4B000000u;
+        return (static_cast<unsigned long long>(sum_hib - bias) << 20) + (sum_lob - bias);
+    }
+};
 
 // The scaled-logit window [xa, xb) that holds every entry with wlo <= W <
 // whi (1 <= wlo): own_exp is monotone and within 2 ulp of exp, so a margin of
@@ -912,40 +994,40 @@ __device__ RowInfo row_cut(const float* __restrict__ row, int V, bool vec, float
                             if (f >= f_lo) to_hist(f, hib, lob);
                         });
     } else if (vec) {
-        // two entries per packed operation (mass_bits on pairs)
-        const float2 nmx = make_float2(-mx, -mx), it2 = make_float2(invT, invT);
-        const float2 k20 = make_float2(9.5367431640625e-07f, 9.5367431640625e-07f);
-        const float2 m20 = make_float2(-1048576.0f, -1048576.0f);
-        const float2 b23 = make_float2(8388608.0f, 8388608.0f), nb23 = make_float2(-8388608.0f, -8388608.0f);
-        auto pair = [&](float la, float lb) {
-            const float2 f = own_exp_2_40_x2(__fmul2_rn(__fadd2_rn(make_float2(la, lb), nmx), it2));
-            const float2 t1 = __fadd2_rd(__fmul2_rn(f, k20), b23);
-            const float2 t2 = __fadd2_rd(__ffma2_rn(__fadd2_rn(t1, nb23), m20, f), b23);
-            const uint32_t h0 = __float_as_uint(t1.x), h1 = __float_as_uint(t1.y);
-            const uint32_t l0 = __float_as_uint(t2.x), l1 = __float_as_uint(t2.y);
-            sum_hib += h0 + h1;
-            sum_lob += l0 + l1;
-            if (fmaxf(f.x, f.y) >= f_lo) {
-                if (f.x >= f_lo) to_hist(f.x, h0, l0);
-                if (f.y >= f_lo) to_hist(f.y, h1, l1);
-            }
-        };
-        // last groups first: they left L2 least long ago in the max pass
+        // two entries per packed operation; the histogram through the queues
+        // (they share the candidate arrays, which are unused until step 3)
+        __syncthreads();
+        MassPass mp;
+        mp.init(mx, invT, cmin, f_lo, hist, &sm.hq[wid][0][lane]);
+        // float4 group k of this thread is r4[k * kRowThreads + tid]; the last
+        // groups first: they left L2 least long ago in the max pass.  The
+        // loop runs over k, the same for every lane of a warp.
         const float4* r4 = reinterpret_cast<const float4*>(row);
         const int V4 = V >> 2;
         const int nk = (V4 + kRowThreads - 1) / kRowThreads;
-        int i = (nk - 1) * kRowThreads + tid;
-        if (i >= V4) i -= kRowThreads;
-        for (; i - 3 * kRowThreads >= 0; i -= 4 * kRowThreads) {
+        static_assert(kHistGroup >= 16, "four float4 groups between checks");
+        int k = nk - 1;
+        {
+            // the top group may be partial: entries past V4 are skipped
+            const int i = k * kRowThreads + tid;
+            if (i < V4) mp.quad(__ldg(r4 + i));
+            mp.check();
+            --k;
+        }
+        for (; k >= 3; k -= 4) {
+            const int i = k * kRowThreads + tid;
             const float4 a = __ldg(r4 + i), b = __ldg(r4 + i - kRowThreads),
                          c = __ldg(r4 + i - 2 * kRowThreads), d = __ldg(r4 + i - 3 * kRowThreads);
-            pair(a.x, a.y); pair(a.z, a.w); pair(b.x, b.y); pair(b.z, b.w);
-            pair(c.x, c.y); pair(c.z, c.w); pair(d.x, d.y); pair(d.z, d.w);
+            mp.quad(a); mp.quad(b); mp.quad(c); mp.quad(d);
+            mp.check();
         }
-        for (; i >= 0; i -= kRowThreads) {
-            const float4 a = __ldg(r4 + i);
-            pair(a.x, a.y); pair(a.z, a.w);
+        for (; k >= 0; --k) {
+            mp.quad(__ldg(r4 + k * kRowThreads + tid));
+            mp.check();
         }
+        mp.drain();
+        sum_hib = mp.sum_hib;
+        sum_lob = mp.sum_lob;
     } else {
         stream_row(row, V, vec, [&](int, float l) {
             const float f = own_exp_2_40(scaled_x(l, mx, invT));
@@ -1365,31 +1447,11 @@ __global__ void __launch_bounds__(kRowThreads, 2) split_mass_kernel(
     unsigned long long* hist = sm.whist[wid];
     for (int t = lane; t < kLogBuckets; t += 32) hist[t] = 0ull;
     __syncwarp();
-    uint32_t sum_hib = 0u, sum_lob = 0u, n_mine = 0u;
-    auto to_hist = [&](float f, uint32_t hib, uint32_t lob) {
-        const unsigned long long W =
-            (static_cast<unsigned long long>(hib - 0x4B000000u) << 20) | (lob - 0x4B000000u);
-        if (W >= cmin) atomic_add_u64_split(&hist[log_bucket_f(f)], W);
-    };
-    const float2 nmx = make_float2(-mx, -mx), it2 = make_float2(invT, invT);
-    const float2 k20 = make_float2(9.5367431640625e-07f, 9.5367431640625e-07f);
-    const float2 m20 = make_float2(-1048576.0f, -1048576.0f);
-    const float2 b23 = make_float2(8388608.0f, 8388608.0f), nb23 = make_float2(-8388608.0f, -8388608.0f);
-    auto pair = [&](float la, float lb) {
-        const float2 f = own_exp_2_40_x2(__fmul2_rn(__fadd2_rn(make_float2(la, lb), nmx), it2));
-        const float2 t1 = __fadd2_rd(__fmul2_rn(f, k20), b23);
-        const float2 t2 = __fadd2_rd(__ffma2_rn(__fadd2_rn(t1, nb23), m20, f), b23);
-        const uint32_t h0 = __float_as_uint(t1.x), h1 = __float_as_uint(t1.y);
-        const uint32_t l0 = __float_as_uint(t2.x), l1 = __float_as_uint(t2.y);
-        sum_hib += h0 + h1;
-        sum_lob += l0 + l1;
-        if (fmaxf(f.x, f.y) >= f_lo) {
-            if (f.x >= f_lo) to_hist(f.x, h0, l0);
-            if (f.y >= f_lo) to_hist(f.y, h1, l1);
-        }
-    };
+    MassPass mp;
+    mp.init(mx, invT, cmin, f_lo, hist, &sm.hq[wid][0][lane]);
     const float4* r4 = reinterpret_cast<const float4*>(split_row(target, draft, n_target_rows, r, V));
-    for (int sg0 = s0 + wid; sg0 < s1; sg0 += 4 * kRowWarps) {
+    static_assert(kHistGroup >= 16, "four float4 groups between checks");
+    for (int sg0 = s0 + wid; sg0 < s1; sg0 += 4 * kRowWarps) {  // the same for a warp's lanes
         float4 v[4];
         bool in[4];
 #pragma unroll
@@ -1400,15 +1462,11 @@ __global__ void __launch_bounds__(kRowThreads, 2) split_mass_kernel(
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            if (in[j]) {
-                pair(v[j].x, v[j].y);
-                pair(v[j].z, v[j].w);
-                n_mine += 4u;
-            }
+            if (in[j]) mp.quad(v[j]);
+        mp.check();
     }
-    const uint32_t bias = n_mine * 0x4B000000u;
-    const unsigned long long S = block_sum_u64(
-        (static_cast<unsigned long long>(sum_hib - bias) << 20) + (sum_lob - bias), sm.red);
+    mp.drain();
+    const unsigned long long S = block_sum_u64(mp.sum(), sm.red);
     __syncthreads();  // every warp's histogram is complete
     unsigned long long* out = phist + (r * C + c) * kLogBuckets;
     for (int t = tid; t < kLogBuckets; t += kRowThreads) {
