@@ -467,6 +467,15 @@ VW4_API vw4_status vw4_q4_0_from_blocks(const void* blocks_dev, int N, int K, vo
  * bit against an independent implementation.  Device pointers. */
 VW4_API vw4_status vw4_own_exp(const float* x_dev, float* y_dev, int64_t n, void* stream);
 
+/* The integer masses W[i] = floor(own_exp(x[i]) * 2^40) of scaled logits x,
+ * computed by the packed fp32-pair arithmetic the row statistics use (two
+ * entries per operation), exposed so that it can be checked against
+ * vw4_own_exp and an independent implementation.  x: float [n]; W: uint64 [n]
+ * (8-byte aligned).  Device pointers; asynchronous on `stream`.
+ * VW4_ERR_INVALID_ARG for null pointers or n < 0; VW4_ERR_ALIGN for W. */
+VW4_API vw4_status vw4_own_mass_pairs(const float* x_dev, uint64_t* W_dev, int64_t n,
+                                      void* stream);
+
 /*
  * Draft-depth controller (host only, no GPU work).
  *

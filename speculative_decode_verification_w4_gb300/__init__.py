@@ -44,7 +44,8 @@ STATUS_NAMES = {0: "VW4_OK", 1: "VW4_ERR_INVALID_ARG", 2: "VW4_ERR_UNSUPPORTED",
 EXPORTS = ("verify_gemm_w4", "verify_moe_w4", "accept_greedy", "accept_rejection",
            "vw4_workspace_bytes", "vw4_get_device_status", "vw4_q4_0_from_blocks",
            "vw4_status_str", "vw4_last_error_string", "vw4_version", "vw4_set_wait_limit_ns",
-           "vw4_own_exp", "verify_gemm_w4_noalloc", "verify_greedy_w4", "vw4_depth_ctl_init",
+           "vw4_own_exp", "vw4_own_mass_pairs", "verify_gemm_w4_noalloc", "verify_greedy_w4",
+           "vw4_depth_ctl_init",
            "vw4_depth_ctl_observe", "vw4_depth_ctl_expected", "vw4_depth_ctl_choose",
            "accept_rejection_topk", "vw4_rejection_row_records",
            "vw4_test_inject_stall", "verify_gemm_w4_blockmax", "accept_rejection_blockmax")
@@ -111,6 +112,7 @@ def load_library(path: str = LIB_PATH):
             "vw4_version": (I, []),
             "vw4_set_wait_limit_ns": (None, [U64]),
             "vw4_own_exp": (I, [P, P, ctypes.c_int64, P]),
+            "vw4_own_mass_pairs": (I, [P, P, ctypes.c_int64, P]),
             "verify_gemm_w4_noalloc": (I, [ctypes.POINTER(Weight), P, I, I, P, I, P, P]),
             "vw4_depth_ctl_init": (I, [ctypes.POINTER(DepthCtl), I, ctypes.c_float]),
             "vw4_depth_ctl_observe": (I, [ctypes.POINTER(DepthCtl), I, I]),
@@ -506,6 +508,16 @@ def vw4_own_exp(x: torch.Tensor, out: torch.Tensor | None = None, stream=None):
         out = torch.empty_like(x)
     _check(load_library().vw4_own_exp(_ptr(x), _ptr(out), x.numel(), _stream(stream)),
            "vw4_own_exp")
+    return out
+
+
+def vw4_own_mass_pairs(x: torch.Tensor, out: torch.Tensor | None = None, stream=None):
+    """The accept step's integer masses floor(own_exp(x) 2^40) by its packed
+    fp32-pair path, elementwise on a float32 CUDA tensor (int64 result)."""
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.int64, device=x.device)
+    _check(load_library().vw4_own_mass_pairs(_ptr(x), _ptr(out), x.numel(), _stream(stream)),
+           "vw4_own_mass_pairs")
     return out
 
 

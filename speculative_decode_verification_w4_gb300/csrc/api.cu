@@ -682,6 +682,17 @@ VW4_API vw4_status vw4_own_exp(const float* x_dev, float* y_dev, int64_t n, void
     return VW4_OK;
 }
 
+VW4_API vw4_status vw4_own_mass_pairs(const float* x_dev, uint64_t* W_dev, int64_t n,
+                                      void* stream) {
+    if (!x_dev || !W_dev || n < 0) return VW4_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(W_dev) & 7u) != 0) return VW4_ERR_ALIGN;
+    if (n == 0) return VW4_OK;
+    cudaError_t e = launch_own_mass_pairs(x_dev, reinterpret_cast<unsigned long long*>(W_dev), n,
+                                          static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "own_mass_pairs launch");
+    return VW4_OK;
+}
+
 VW4_API vw4_status vw4_q4_0_from_blocks(const void* blocks_dev, int N, int K, void* q_dev,
                                         void* d_dev, void* stream) {
     if (!blocks_dev || !q_dev || !d_dev || N < 1 || K < 32 || K % 32) return VW4_ERR_INVALID_ARG;

@@ -139,14 +139,16 @@ __device__ __forceinline__ float own_exp_2_40(float x) {
 
 // own_exp_2_40 of two scaled logits with packed fp32-pair operations: each
 // half is the same IEEE operation, rounding included, as in own_exp_2_40
-// (x - n c equals x + n (-c); rint(t) is read from t + 1.5 * 2^23, which
-// rounds to the nearest even integer just as rint does, |t| < 2^22).
+// (x - n c equals x + n (-c)).  n = rint(t) is taken per half with rintf: a
+// packed add and subtract of 1.5 * 2^23 was measured to round some exact
+// ties (t = -9.5) away from the even integer, which moves the reduction by
+// ln 2 and the result by an ulp.  n + 1.5 * 2^23 is then exact.
 __device__ __forceinline__ float2 own_exp_2_40_x2(float2 x) {
     x.x = fmaxf(x.x, -32.0f);
     x.y = fmaxf(x.y, -32.0f);
     const float2 t = __fmul2_rn(x, make_float2(1.44269504088896340736f, 1.44269504088896340736f));
-    const float2 m = __fadd2_rn(t, make_float2(12582912.0f, 12582912.0f));
-    const float2 n = __fadd2_rn(m, make_float2(-12582912.0f, -12582912.0f));
+    const float2 n = make_float2(rintf(t.x), rintf(t.y));
+    const float2 m = __fadd2_rn(n, make_float2(12582912.0f, 12582912.0f));
     float2 r = __ffma2_rn(n, make_float2(-0.693145751953125f, -0.693145751953125f), x);
     r = __ffma2_rn(n, make_float2(-1.42860682030941723212e-6f, -1.42860682030941723212e-6f), r);
     float2 p = make_float2(1.0f / 5040.0f, 1.0f / 5040.0f);
@@ -469,6 +471,17 @@ __device__ __forceinline__ uint32_t stream_count(int V, bool vec) {
     return tid < V ? static_cast<uint32_t>((V - 1 - tid) / kRowThreads + 1) : 0u;
 }
 
+// mass_bits of two entries with packed operations: the halves' bit patterns
+// are 2^23 + floor(f / 2^20) (t1) and 2^23 + floor(f mod 2^20) (t2).
+__device__ __forceinline__ void mass_bits_x2(float2 f, float2& t1, float2& t2) {
+    const float2 k20 = make_float2(9.5367431640625e-07f, 9.5367431640625e-07f);
+    const float2 m20 = make_float2(-1048576.0f, -1048576.0f);
+    const float2 b23 = make_float2(8388608.0f, 8388608.0f);
+    const float2 nb23 = make_float2(-8388608.0f, -8388608.0f);
+    t1 = __fadd2_rd(__fmul2_rn(f, k20), b23);
+    t2 = __fadd2_rd(__ffma2_rn(__fadd2_rn(t1, nb23), m20, f), b23);
+}
+
 // The mass pass over a lane's entries, two at a time with packed fp32-pair
 // operations: the integer masses W = floor(own_exp(x) 2^40) summed exactly
 // (as the two 20-bit halves' 2^23-biased bit patterns, mod 2^32; the true
@@ -499,13 +512,9 @@ struct MassPass {
         sum_hib = sum_lob = n = 0u;
     }
     __device__ __forceinline__ void pair(float la, float lb) {
-        const float2 k20 = make_float2(9.5367431640625e-07f, 9.5367431640625e-07f);
-        const float2 m20 = make_float2(-1048576.0f, -1048576.0f);
-        const float2 b23 = make_float2(8388608.0f, 8388608.0f);
-        const float2 nb23 = make_float2(-8388608.0f, -8388608.0f);
         const float2 f = own_exp_2_40_x2(__fmul2_rn(__fadd2_rn(make_float2(la, lb), nmx), it2));
-        const float2 t1 = __fadd2_rd(__fmul2_rn(f, k20), b23);
-        const float2 t2 = __fadd2_rd(__ffma2_rn(__fadd2_rn(t1, nb23), m20, f), b23);
+        float2 t1, t2;
+        mass_bits_x2(f, t1, t2);
         sum_hib += __float_as_uint(t1.x) + __float_as_uint(t1.y);
         sum_lob += __float_as_uint(t2.x) + __float_as_uint(t2.y);
         n += 2u;
@@ -2423,8 +2432,38 @@ __global__ void own_exp_kernel(const float* __restrict__ x, float* __restrict__ 
         y[i] = own_exp(x[i]);
 }
 
+// W = floor(own_exp(x) 2^40) of scaled logits x by the packed-pair path of
+// the mass passes (entries 2j and 2j + 1 in one pair; an odd tail paired
+// with -inf).
+__global__ void own_mass_pairs_kernel(const float* __restrict__ x,
+                                      unsigned long long* __restrict__ W, long long n) {
+    const long long np = (n + 1) / 2;
+    for (long long j = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; j < np;
+         j += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long i = 2 * j;
+        const bool two = i + 1 < n;
+        const float2 f = own_exp_2_40_x2(make_float2(x[i], two ? x[i + 1] : -INFINITY));
+        float2 t1, t2;
+        mass_bits_x2(f, t1, t2);
+        W[i] = (static_cast<unsigned long long>(__float_as_uint(t1.x) - 0x4B000000u) << 20) +
+               (__float_as_uint(t2.x) - 0x4B000000u);
+        if (two)
+            W[i + 1] = (static_cast<unsigned long long>(__float_as_uint(t1.y) - 0x4B000000u) << 20) +
+                       (__float_as_uint(t2.y) - 0x4B000000u);
+    }
+}
+
 
 }  // namespace
+
+cudaError_t launch_own_mass_pairs(const float* x, unsigned long long* W, long long n,
+                                  cudaStream_t s) {
+    long long blocks = ((n + 1) / 2 + 255) / 256;
+    if (blocks > 65536) blocks = 65536;
+    if (blocks < 1) blocks = 1;
+    own_mass_pairs_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(x, W, n);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_own_exp(const float* x, float* y, long long n, cudaStream_t s) {
     long long blocks = (n + 255) / 256;

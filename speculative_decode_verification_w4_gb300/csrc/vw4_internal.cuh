@@ -170,6 +170,8 @@ cudaError_t launch_accept_greedy(const float* logits, const int32_t* drafts,
                                  int32_t* len, uint32_t* status, cudaStream_t s);
 size_t rejection_workspace_bytes(int B, int Kd, int V);
 cudaError_t launch_own_exp(const float* x, float* y, long long n, cudaStream_t s);
+cudaError_t launch_own_mass_pairs(const float* x, unsigned long long* W, long long n,
+                                  cudaStream_t s);
 cudaError_t launch_accept_rejection(const float* target, const float* draft,
                                     const int32_t* drafts, int B, int Kd, int V, float invT,
                                     uint64_t P, int top_k, uint64_t MP, uint64_t seed,

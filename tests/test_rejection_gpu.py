@@ -39,6 +39,52 @@ def test_own_exp_bitwise_equal_to_oracle_over_all_inputs():
     assert np.array_equal(y.view(np.uint32), oracle.own_exp_array(sp).view(np.uint32))
 
 
+def tie_inputs():
+    """Every fp32 x in [-32, 0] whose product with log2(e) (fp32, rounded to
+    nearest) is an exact half-integer: the reduction's rint(t) is a tie."""
+    l2e = np.float32(1.44269504088896340736)
+    out = []
+    for h in range(-47, 1):
+        t = np.float32(h + 0.5)
+        x0 = np.float32(float(t) / float(l2e))
+        cand = [x0]
+        up, dn = x0, x0
+        for _ in range(16):
+            up = np.nextafter(up, np.float32(np.inf))
+            dn = np.nextafter(dn, np.float32(-np.inf))
+            cand += [up, dn]
+        out += [c for c in cand if np.float32(c * l2e) == t and -32.0 <= c <= 0.0]
+    return np.array(sorted(set(float(c) for c in out)), np.float32)
+
+
+def test_packed_masses_equal_scalar_path_over_all_inputs():
+    """The mass passes' packed fp32-pair arithmetic (two entries per
+    operation) gives W = floor(own_exp(x) 2^40) bit for bit: against the
+    scalar own_exp (pinned to the oracle over every input above) for every
+    fp32 x in [-32, 0], and against the oracle directly at every x whose
+    reduction t = x log2(e) is an exact tie, which rint takes to the even
+    integer (t = -9.5 went to -9 in an earlier packed form)."""
+    start, stop = 0x80000000, 0xC2000000 + 1  # -0.0 ... -32.0
+    chunk = 1 << 26
+    for lo in range(start, stop, chunk):
+        hi = min(stop, lo + chunk)
+        bits = (torch.arange(lo, hi, dtype=torch.int64, device="cuda") - (1 << 32)).to(torch.int32)
+        x = bits.view(torch.float32)
+        ref = torch.floor(vw4.vw4_own_exp(x).double() * 2.0 ** 40).to(torch.int64)
+        W = vw4.vw4_own_mass_pairs(x)
+        if not torch.equal(W, ref):
+            bad = torch.nonzero(W != ref)[:4, 0]
+            raise AssertionError((lo, x[bad].tolist(), W[bad].tolist(), ref[bad].tolist()))
+    ties = tie_inputs()
+    assert ties.size >= 40 and np.float32(-6.584897994995117) in ties
+    W = vw4.vw4_own_mass_pairs(torch.from_numpy(ties).cuda()).cpu().numpy()
+    ref = np.floor(oracle.own_exp_array(ties).astype(np.float64) * 2.0 ** 40).astype(np.int64)
+    assert np.array_equal(W, ref), ties[W != ref]
+    # an odd count: the last entry is paired with -inf
+    W3 = vw4.vw4_own_mass_pairs(torch.from_numpy(ties[:3].copy()).cuda()).cpu().numpy()
+    assert np.array_equal(W3, ref[:3])
+
+
 @pytest.mark.parametrize("B,Kd,V,top_p", [(16, 3, 16, 0.95), (64, 1, 1000, 0.95),
                                           (32, 4, 5000, 0.8), (8, 8, 20000, 0.95),
                                           (20, 2, 777, 1.0), (5, 0, 300, 0.95),
@@ -202,15 +248,50 @@ def test_row_records_match_oracle_every_row_full_size():
     check_records(rec, target, draft)
 
 
-def check_records(rec, target, draft, top_p=0.95):
+def log_bucket(W):
+    """The mass histogram's log bucket of each W >= 1: W itself below 16, then
+    8 buckets per binade (the 3 bits after the leading one)."""
+    W = np.asarray(W, np.uint64)
+    b = W.astype(np.int64)
+    big = W >= 16
+    _, e = np.frexp(W[big].astype(np.float64))     # exact: W < 2^53
+    msb = e.astype(np.int64) - 1
+    j = (W[big] >> (msb - 3).astype(np.uint64)) & np.uint64(7)
+    b[big] = 16 + (msb - 4) * 8 + j.astype(np.int64)
+    return b
+
+
+def cut_regime(W, W_all, chunks=1):
+    """How the row kernel finds a row's cut: 'rank' (at most 128 members in
+    the crossing bucket, sorted by counting), 'radix' (up to 4096 gathered,
+    selected by radix) or 'fallback' (a crowded bucket: the exact radix search
+    over further passes); with the number of the row's `chunks` equal runs of
+    whole 128-entry segments that hold members (a run may gather at most
+    4096 / chunks).  None when there is no cut to find."""
+    kept = W[W > 0]
+    if kept.size == 0 or kept.size == W.size:
+        return None
+    V = W.size
+    span = ((V + 127) // 128 + chunks - 1) // chunks * 128
+    beta = log_bucket(np.array([kept.min()], np.uint64))[0]
+    mem = np.flatnonzero((W_all >= 1) & (log_bucket(np.maximum(W_all, 1)) == beta))
+    per = np.bincount(mem // span, minlength=chunks)
+    if per.max() > 4096 // chunks or mem.size > 4096:
+        return ("fallback", int((per > 0).sum()))
+    return ("radix" if mem.size > 128 else "rank", int((per > 0).sum()))
+
+
+def check_records(rec, target, draft, top_p=0.95, chunks=None):
     """Each row record against the oracle's masses: the max, the kept sum S,
-    and the kept set that (tau, cut) describe."""
+    and the kept set that (tau, cut) describe.  With `chunks`, also returns
+    each row's cut_regime."""
     B, R, V = target.shape
     Kd = R - 1
     rows = [target[b, i] for b in range(B) for i in range(Kd + 1)] + \
            [draft[b, i] for b in range(B) for i in range(Kd)]
     assert len(rows) == len(rec)
     idx = np.arange(V)
+    regimes = []
     for r, row in enumerate(rows):
         W, S = oracle.row_mass(row, 0.6, top_p)
         W_all, _ = oracle.row_mass(row, 0.6, 1.0)      # every mass before the cut
@@ -219,10 +300,20 @@ def check_records(rec, target, draft, top_p=0.95):
         assert int(g["kept_sum"]) == S, (r, int(g["kept_sum"]), S)
         assert g["topk_key"] == 0 and g["topk_idx"] == 0x7FFFFFFF
         tau, cut = int(g["tau"]), int(g["cut"])
-        kept_gpu = (W_all > tau) | ((W_all == tau) & (idx <= cut))
+        # (entries of mass 0 weigh nothing, kept or not: tau = 0 keeps them)
+        kept_gpu = ((W_all > tau) | ((W_all == tau) & (idx <= cut))) & (W_all > 0)
         kept_ref = W > 0
         assert np.array_equal(kept_gpu, kept_ref), (r, tau, cut, np.flatnonzero(kept_gpu ^ kept_ref)[:5])
         assert int(W_all[kept_gpu].sum()) == S
+        if chunks:
+            regimes.append(cut_regime(W, W_all, chunks))
+    return regimes
+
+
+def test_log_bucket_edges():
+    """The test's bucket function: exact below 16, 8 per binade above."""
+    W = np.array([1, 15, 16, 17, 18, 19, 31, 32, 35, 36, 2**40 - 1, 2**40], np.uint64)
+    assert log_bucket(W).tolist() == [1, 15, 16, 16, 17, 17, 23, 24, 24, 25, 303, 304]
 
 
 @pytest.mark.parametrize("case", ["lm_head_flat", "integer_logits", "few_rows_sharp"])
@@ -256,4 +347,68 @@ def test_split_rows_match_oracle(case):
     assert vw4.vw4_get_device_status() == 0
     check_records(rec.reshape(-1).view(np.dtype(vw4.ROW_RECORD_DTYPE)), target, draft)
     rt, rl, _ = oracle.accept_rejection(target, draft, drafts, 0.6, 0.95, 7, 0)
+    assert np.array_equal(ln.cpu().numpy(), rl) and np.array_equal(tok.cpu().numpy(), rt)
+
+
+def _many_rows_case(case):
+    g = synth.rng({"sweep_ragged": 81, "flat_wide": 82, "integer_logits": 83,
+                   "degenerate": 84}[case])
+    B, Kd = 20, 4                       # 180 rows: one CTA each (more than the split path takes)
+    if case == "sweep_ragged":
+        V = 20004                       # V % 4 == 0; the last segment holds 36 entries
+        target, draft, _ = synth.stochastic_case(81, B, Kd, V)
+    elif case == "flat_wide":
+        V = 200000                      # flat rows: thousands in the crossing bucket
+        target = synth.logits(g, (B, Kd + 1, V), 1.0)
+        draft = synth.logits(g, (B, Kd, V), 1.0)
+    elif case == "integer_logits":
+        V = 65536
+        target = np.round(synth.logits(g, (B, Kd + 1, V), 1.5)).astype(np.float32)
+        draft = np.round(synth.logits(g, (B, Kd, V), 1.5)).astype(np.float32)
+    else:
+        V = 32768
+        target, draft, _ = synth.stochastic_case(84, B, Kd, V)
+        mask = g.random((B, Kd + 1, V)) < 0.3
+        target[mask] = -np.inf
+        draft[mask[:, :Kd]] = -np.inf
+        target[1, 0, :] = -np.inf       # fully masked: every W is 0
+        target[2, 1, :] = -np.inf
+        target[2, 1, V - 1] = 5.0       # one-hot at the last index
+        target[3, 0, 100] = np.inf      # +inf: every W is 0
+        target[4, 2, :] = 1.25          # constant row: every entry ties at the top
+        draft[5, 0, :] = -np.inf
+        draft[5, 0, 5] = 0.0
+    return B, Kd, V, target, draft
+
+
+@pytest.mark.parametrize("case,top_p", [("sweep_ragged", 0.95), ("sweep_ragged", 0.5),
+                                        ("sweep_ragged", 1.0), ("flat_wide", 0.95),
+                                        ("integer_logits", 0.95), ("degenerate", 0.95)])
+def test_many_rows_match_oracle(case, top_p):
+    """More rows than the split path takes (one CTA per row), every record and
+    the committed ids against the oracle.  The cases are chosen (and checked
+    here, from the oracle's masses) to reach every way the cut is found: few
+    crossing-bucket members sorted by rank, thousands selected by radix, and
+    crowded buckets searched over further passes; sweep_ragged has a partial
+    last segment (V = 20004), degenerate masked, one-hot, +inf and constant
+    rows; top_p 1 keeps every entry.  flat_wide's rows hold an x whose
+    reduction is an exact rint tie, which the packed mass pass once rounded
+    the wrong way (kept sums 128 low)."""
+    B, Kd, V, target, draft = _many_rows_case(case)
+    drafts = oracle.sample_drafts(draft, 0.6, top_p, 9, 1 << 32)
+    ws = vw4.Workspace()
+    tok, ln = vw4.accept_rejection(torch.from_numpy(target).cuda(), torch.from_numpy(draft).cuda(),
+                                   torch.from_numpy(drafts).cuda(), 0.6, top_p, 9, 0, workspace=ws)
+    rec = vw4.vw4_rejection_row_records(ws, B, Kd, V).cpu().numpy()
+    torch.cuda.synchronize()
+    st = vw4.vw4_get_device_status()
+    assert st & ~vw4.DEV_ZERO_RESIDUAL == 0, st   # (an empty residual in the degenerate rows)
+    regimes = check_records(rec.reshape(-1).view(np.dtype(vw4.ROW_RECORD_DTYPE)), target, draft,
+                            top_p, chunks=1)
+    kinds = {k for k, _ in filter(None, regimes)}
+    if top_p < 1.0:
+        want = {"sweep_ragged": {"rank"}, "flat_wide": {"radix", "fallback"},
+                "integer_logits": {"fallback"}, "degenerate": {"rank", "fallback"}}[case]
+        assert want <= kinds, (case, kinds)
+    rt, rl, _ = oracle.accept_rejection(target, draft, drafts, 0.6, top_p, 9, 0)
     assert np.array_equal(ln.cpu().numpy(), rl) and np.array_equal(tok.cpu().numpy(), rt)
