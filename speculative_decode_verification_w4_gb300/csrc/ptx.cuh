@@ -98,6 +98,11 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
     return p;
 }
 
+// Asks L2 to fetch the line holding p (no registers, no completion).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // ------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

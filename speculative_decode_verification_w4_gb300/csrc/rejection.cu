@@ -357,6 +357,7 @@ __device__ __forceinline__ void atomic_add_u64_split(unsigned long long* a, unsi
 constexpr int kRowThreads = 512;
 constexpr int kRowWarps = kRowThreads / 32;
 constexpr int kHistQ = 24;       // queue slots per lane (MassPass)
+constexpr int kSegCache = 2048;  // segment maxima kept in shared memory (V <= 262144)
 constexpr int kHistGroup = 16;   // entries a lane may push between two checks
 static_assert(kRowThreads >= kLogBuckets, "one thread per log bucket in the suffix scan");
 
@@ -377,6 +378,7 @@ struct RowSmem {
     int beta, wbits, cut_found;
     unsigned long long above, lo, width, n_eq, count_eq;
     RowInfo info;
+    float segc[kSegCache];  // the row's segment maxima, when it has at most kSegCache
 };
 
 // f(k, l) for every entry of the row, each thread taking entries in
@@ -421,10 +423,18 @@ __device__ __forceinline__ int float_key(float x) {
     return k ^ ((k >> 31) & 0x7fffffff);
 }
 
+// A segment max written by this CTA in its max pass: from its shared-memory
+// copy, or from the workspace through L2 (which the writes reached; L1 may
+// hold an older line).
+__device__ __forceinline__ float seg_load(const float* p) {
+    return __isShared(p) ? *p : __ldcg(p);
+}
+
 // f(k, l) for every entry of the segments whose max passes the window test
 // (vec rows with a segment table; otherwise every entry, as stream_row).
-// seg[] was written by this CTA in its max pass: read through L2.
-// (need(m): whether a segment whose largest logit is m can hold a wanted entry)
+// (need(m): whether a segment whose largest logit is m can hold a wanted
+// entry.)  A warp loads up to four of its wanted segments before it hands
+// any entry on.
 template <class N, class F>
 __device__ __forceinline__ void stream_segments(const float* __restrict__ row, int V, bool vec,
                                                 const float* seg, N&& need_of, F&& f) {
@@ -439,15 +449,28 @@ __device__ __forceinline__ void stream_segments(const float* __restrict__ row, i
         // lane j tests the segment of step k0 + j that this warp streams
         const int k = k0 + lane, sg = k * kRowWarps + wid;
         bool need = false;
-        if (k < nk && sg < nseg) need = need_of(__ldcg(seg + sg));
-        unsigned int m = __ballot_sync(0xffffffffu, need);
+        if (k < nk && sg < nseg) need = need_of(seg_load(seg + sg));
+        unsigned int m = __ballot_sync(0xffffffffu, need);  // the same in every lane
         while (m) {
-            const int j = __ffs(m) - 1;
-            m &= m - 1;
-            const int i = (k0 + j) * kRowThreads + tid;
-            if (i < V4) {
-                const float4 a = __ldg(r4 + i);
-                f(4 * i, a.x); f(4 * i + 1, a.y); f(4 * i + 2, a.z); f(4 * i + 3, a.w);
+            int ks[4];
+            float4 v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                ks[q] = -1;
+                if (m) {
+                    ks[q] = k0 + __ffs(m) - 1;
+                    m &= m - 1;
+                }
+                const int i = ks[q] * kRowThreads + tid;
+                v[q] = (ks[q] >= 0 && i < V4) ? __ldg(r4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int i = ks[q] * kRowThreads + tid;
+                if (ks[q] >= 0 && i < V4) {
+                    f(4 * i, v[q].x); f(4 * i + 1, v[q].y); f(4 * i + 2, v[q].z);
+                    f(4 * i + 3, v[q].w);
+                }
             }
         }
     }
@@ -583,6 +606,7 @@ __device__ float row_max_from_blocks(const float* __restrict__ bm, int V, float*
             const int b0 = sg * kPer, b1 = min(b0 + kPer, nb);
             for (int bk = b0; bk < b1; ++bk) m = fmaxf(m, __ldg(bm + bk));
             seg[sg] = m;
+            if (sg < kSegCache) sm.segc[sg] = m;
             lmax = fmaxf(lmax, m);
         }
     } else {
@@ -603,21 +627,25 @@ __device__ float row_max(const float* __restrict__ row, int V, bool vec, float* 
         const float4* r4 = reinterpret_cast<const float4*>(row);
         const int V4 = V >> 2, nk = (V4 + kRowThreads - 1) / kRowThreads, nseg = n_segments(V);
         const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        for (int k0 = 0; k0 < nk; k0 += 4) {
-            float4 v[4];
+        for (int k0 = 0; k0 < nk; k0 += 8) {  // eight loads in flight
+            float4 v[8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 8; ++j) {
                 const int i = (k0 + j) * kRowThreads + tid;
                 v[j] = (k0 + j < nk && i < V4) ? __ldg(r4 + i) : ninf;
             }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 8; ++j) {
                 if (k0 + j >= nk) break;  // the same for the whole warp
                 const float m = fmaxf(fmaxf(v[j].x, v[j].y), fmaxf(v[j].z, v[j].w));
                 lmax = fmaxf(lmax, m);
                 const int key = __reduce_max_sync(0xffffffffu, float_key(m));
                 const int sg = (k0 + j) * kRowWarps + wid;
-                if (lane == 0 && sg < nseg) seg[sg] = __int_as_float(key ^ ((key >> 31) & 0x7fffffff));
+                if (lane == 0 && sg < nseg) {
+                    const float sm_ = __int_as_float(key ^ ((key >> 31) & 0x7fffffff));
+                    seg[sg] = sm_;
+                    if (sg < kSegCache) sm.segc[sg] = sm_;
+                }
             }
         }
     } else {
@@ -643,7 +671,7 @@ __device__ bool top_k_cut_segments(const float* __restrict__ row, int V, const f
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     uint32_t* sk = reinterpret_cast<uint32_t*>(&sm.whist[0][0]);  // [kMaxSegs] maxima keys
     uint32_t* hist = sk + kMaxSegs;                                // [256]
-    for (int t = tid; t < nseg; t += kRowThreads) sk[t] = logit_key(__ldcg(seg + t));
+    for (int t = tid; t < nseg; t += kRowThreads) sk[t] = logit_key(seg_load(seg + t));
     uint32_t prefix = 0u;
     unsigned int need = static_cast<unsigned int>(top_k);
     for (int shift = 24; shift >= 16; shift -= 8) {
@@ -968,11 +996,28 @@ __device__ RowInfo row_cut(const float* __restrict__ row, int V, bool vec, float
     // 2. sum W, and the mass histogram of the entries with W >= c0 (each warp
     //    its own copy).  The entries below c <= (1 - P/2^32) S / V weigh less
     //    than (1 - P/2^32) S together, so they all lie in the dropped tail;
-    //    c0 uses 2^40 (the top entry's mass, a lower bound of S) in place of
-    //    S, so c0 <= c and the histogram holds every bucket the cut can be in.
+    //    c0 uses a lower bound Slb of S in place of S, so c0 <= c and the
+    //    histogram holds every bucket the cut can be in.  Slb is 2^40 (the top
+    //    entry's own mass), or, with the segment maxima at hand and no top-k
+    //    stage, the masses of the segment maxima (distinct entries) summed.
     const bool want_hist = P < kKeepAll;
-    const unsigned long long c0 =
-        want_hist ? ((kKeepAll - P) << 8) / static_cast<unsigned long long>(n_keep) : 0ull;
+    unsigned long long c0 = 0ull;
+    if (want_hist) {
+        unsigned long long Slb = 1ull << 40;
+        if (seg != nullptr && !topk) {
+            unsigned long long part = 0ull;
+            for (int j = tid; j < n_segments(V); j += kRowThreads) {
+                uint32_t hib, lob;
+                mass_bits(own_exp_2_40(scaled_x(seg_load(seg + j), mx, invT)), hib, lob);
+                part += (static_cast<unsigned long long>(hib - 0x4B000000u) << 20) +
+                        (lob - 0x4B000000u);
+            }
+            const unsigned long long sum = block_sum_u64(part, sm.red);
+            Slb = sum > Slb ? sum : Slb;  // (a non-finite max: every W is 0)
+        }
+        c0 = static_cast<unsigned long long>(static_cast<u128>(kKeepAll - P) * Slb /
+                                             (static_cast<u128>(n_keep) << 32));
+    }
     const unsigned long long cmin = c0 > 1ull ? c0 : 1ull;
     // f < f_lo proves W < cmin with one compare (f_lo is cmin rounded down)
     const float f_lo = want_hist ? __ull2float_rd(cmin) : INFINITY;
@@ -1025,6 +1070,12 @@ __device__ RowInfo row_cut(const float* __restrict__ row, int V, bool vec, float
         }
         for (; k >= 3; k -= 4) {
             const int i = k * kRowThreads + tid;
+            if (k >= 7) {  // the next four groups towards L2 while these are computed
+                prefetch_l2(r4 + i - 4 * kRowThreads);
+                prefetch_l2(r4 + i - 5 * kRowThreads);
+                prefetch_l2(r4 + i - 6 * kRowThreads);
+                prefetch_l2(r4 + i - 7 * kRowThreads);
+            }
             const float4 a = __ldg(r4 + i), b = __ldg(r4 + i - kRowThreads),
                          c = __ldg(r4 + i - 2 * kRowThreads), d = __ldg(r4 + i - 3 * kRowThreads);
             mp.quad(a); mp.quad(b); mp.quad(c); mp.quad(d);
@@ -1247,8 +1298,11 @@ __device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, flo
     info.cut = V - 1;
     info.S = 0ull;
     const bool topk = top_k > 0 && top_k < V;
-    if (topk) top_k_cut(row, V, vec, seg, top_k, sm, info.tk_key, info.tk_idx);
-    RowInfo r = row_cut(row, V, vec, invT, P, seg, info, topk ? top_k : V, sm);
+    // the later passes read the segment maxima from shared memory when the
+    // row has few enough segments (the max pass wrote both copies)
+    const float* segr = (seg != nullptr && n_segments(V) <= kSegCache) ? sm.segc : seg;
+    if (topk) top_k_cut(row, V, vec, segr, top_k, sm, info.tk_key, info.tk_idx);
+    RowInfo r = row_cut(row, V, vec, invT, P, segr, info, topk ? top_k : V, sm);
     // min-p: of what top-p keeps, only W * 2^32 >= MP * W_top, W_top = 2^40
     // (the max entry's own mass), i.e. W >= MP * 2^8.  Both keep a prefix of
     // the (W desc, index asc) order: when min-p's is the shorter, it is every
@@ -1260,7 +1314,7 @@ __device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, flo
             x_window(Wmin, Wmin + 1ull, xa, xb);
             const float mx = r.mx;
             unsigned long long part = 0ull;
-            stream_window(row, V, vec, seg, mx, invT, xa, [&](int k, float l) {
+            stream_window(row, V, vec, segr, mx, invT, xa, [&](int k, float l) {
                 const float x = scaled_x(l, mx, invT);
                 if (x >= xa && in_top_k(l, k, r)) {
                     const unsigned long long W = mass_of(own_exp(x));
