@@ -433,9 +433,9 @@ __device__ __forceinline__ float seg_load(const float* p) {
 // f(k, l) for every entry of the segments whose max passes the window test
 // (vec rows with a segment table; otherwise every entry, as stream_row).
 // (need(m): whether a segment whose largest logit is m can hold a wanted
-// entry.)  A warp loads up to four of its wanted segments before it hands
-// any entry on.
-template <class N, class F>
+// entry.)  A warp loads up to kDepth of its wanted segments before it hands
+// any entry on (1 where f is heavy: its inlined copies would crowd the loop).
+template <int kDepth = 4, class N, class F>
 __device__ __forceinline__ void stream_segments(const float* __restrict__ row, int V, bool vec,
                                                 const float* seg, N&& need_of, F&& f) {
     if (seg == nullptr) {
@@ -452,10 +452,10 @@ __device__ __forceinline__ void stream_segments(const float* __restrict__ row, i
         if (k < nk && sg < nseg) need = need_of(seg_load(seg + sg));
         unsigned int m = __ballot_sync(0xffffffffu, need);  // the same in every lane
         while (m) {
-            int ks[4];
-            float4 v[4];
+            int ks[kDepth];
+            float4 v[kDepth];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < kDepth; ++q) {
                 ks[q] = -1;
                 if (m) {
                     ks[q] = k0 + __ffs(m) - 1;
@@ -465,7 +465,7 @@ __device__ __forceinline__ void stream_segments(const float* __restrict__ row, i
                 v[q] = (ks[q] >= 0 && i < V4) ? __ldg(r4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < kDepth; ++q) {
                 const int i = ks[q] * kRowThreads + tid;
                 if (ks[q] >= 0 && i < V4) {
                     f(4 * i, v[q].x); f(4 * i + 1, v[q].y); f(4 * i + 2, v[q].z);
@@ -476,11 +476,11 @@ __device__ __forceinline__ void stream_segments(const float* __restrict__ row, i
     }
 }
 
-template <class F>
+template <int kDepth = 4, class F>
 __device__ __forceinline__ void stream_window(const float* __restrict__ row, int V, bool vec,
                                               const float* seg, float mx, float invT, float xa,
                                               F&& f) {
-    stream_segments(row, V, vec, seg,
+    stream_segments<kDepth>(row, V, vec, seg,
                     [&](float m) { return !(scaled_x(m, mx, invT) < xa); }, f);
 }
 
@@ -627,15 +627,15 @@ __device__ float row_max(const float* __restrict__ row, int V, bool vec, float* 
         const float4* r4 = reinterpret_cast<const float4*>(row);
         const int V4 = V >> 2, nk = (V4 + kRowThreads - 1) / kRowThreads, nseg = n_segments(V);
         const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        for (int k0 = 0; k0 < nk; k0 += 8) {  // eight loads in flight
-            float4 v[8];
+        for (int k0 = 0; k0 < nk; k0 += 4) {
+            float4 v[4];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 4; ++j) {
                 const int i = (k0 + j) * kRowThreads + tid;
                 v[j] = (k0 + j < nk && i < V4) ? __ldg(r4 + i) : ninf;
             }
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 4; ++j) {
                 if (k0 + j >= nk) break;  // the same for the whole warp
                 const float m = fmaxf(fmaxf(v[j].x, v[j].y), fmaxf(v[j].z, v[j].w));
                 lmax = fmaxf(lmax, m);
@@ -1035,7 +1035,7 @@ __device__ RowInfo row_cut(const float* __restrict__ row, int V, bool vec, float
     uint32_t n_mine = 0u;  // entries this thread summed (the top-k path)
     if (topk) {
         // only the top-k entries carry mass: the segments that can hold one
-        stream_segments(row, V, vec, seg,
+        stream_segments<1>(row, V, vec, seg,
                         [&](float m) { return logit_key(m) >= info.tk_key; },
                         [&](int k, float l) {
                             if (!in_top_k(l, k, info)) return;
@@ -1314,7 +1314,7 @@ __device__ RowInfo row_stats(const float* __restrict__ row, int V, bool vec, flo
             x_window(Wmin, Wmin + 1ull, xa, xb);
             const float mx = r.mx;
             unsigned long long part = 0ull;
-            stream_window(row, V, vec, segr, mx, invT, xa, [&](int k, float l) {
+            stream_window<1>(row, V, vec, segr, mx, invT, xa, [&](int k, float l) {
                 const float x = scaled_x(l, mx, invT);
                 if (x >= xa && in_top_k(l, k, r)) {
                     const unsigned long long W = mass_of(own_exp(x));
