@@ -2364,6 +2364,202 @@ __global__ void __launch_bounds__(NT) list_row_kernel(
     if (tid == 0) o_S[r] = S_kept;
 }
 
+// ------------------------------------------------ top-k lists, warp rows
+// Lists of at most 64 entries: one warp per list row, the same steps as
+// list_row_kernel with the row in registers -- lane l holds positions l and
+// l + 32 -- and every sort a bitonic network over the 64 positions whose
+// partners are exchanged by shuffles, so no step waits on a block barrier.
+constexpr int kListWarpMax = 64;
+constexpr int kListWarpRows = 4;  // rows (warps) per CTA
+
+__device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int o) {
+    return __shfl_xor_sync(0xffffffffu, v, o);
+}
+
+// Sorts the 64 keys a[r] at positions lane + 32 r in descending order.
+__device__ __forceinline__ void warp_sort64_desc(unsigned long long (&a)[2]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 2; k <= 64; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            if (j == 32) {  // (k = 64) partners in the same lane: the lower keeps the larger
+                const unsigned long long x = a[0], y = a[1];
+                a[0] = x > y ? x : y;
+                a[1] = x > y ? y : x;
+            } else {
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int p = lane + 32 * r;
+                    const unsigned long long y = shfl_xor_u64(a[r], j);
+                    // in a block sorted descending ((p & k) == 0) the lower
+                    // position keeps the larger key; in an ascending one the smaller
+                    const bool keep_max = ((p & j) == 0) == ((p & k) == 0);
+                    a[r] = keep_max ? (a[r] > y ? a[r] : y) : (a[r] < y ? a[r] : y);
+                }
+            }
+        }
+    }
+}
+
+// The key at sorted position p (the same p in every lane).
+__device__ __forceinline__ unsigned long long warp_at(const unsigned long long (&a)[2], int p) {
+    return __shfl_sync(0xffffffffu, p < 32 ? a[0] : a[1], p & 31);
+}
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += shfl_xor_u64(v, o);
+    return v;
+}
+
+__global__ void __launch_bounds__(kListWarpRows * 32) list_row_warp_kernel(
+    const int32_t* __restrict__ t_ids, const float* __restrict__ t_vals,
+    const int32_t* __restrict__ d_ids, const float* __restrict__ d_vals, int Kd, int Kt, int V,
+    long long rows, float invT, unsigned long long P, int top_k, unsigned long long MP,
+    int32_t* __restrict__ o_ids, unsigned long long* __restrict__ o_W,
+    unsigned long long* __restrict__ o_S, uint32_t* status) {
+    const int lane = threadIdx.x & 31;
+    const long long r = static_cast<long long>(blockIdx.x) * kListWarpRows + (threadIdx.x >> 5);
+    if (r >= rows) return;  // (whole warps)
+    const int per_seq = 2 * Kd + 1;
+    const long long b = r / per_seq;
+    const int j = static_cast<int>(r % per_seq);
+    const long long src = j <= Kd ? (b * (Kd + 1) + j) * Kt : (b * Kd + (j - Kd - 1)) * Kt;
+    const int32_t* ids = j <= Kd ? t_ids : d_ids;
+    const float* vals = j <= Kd ? t_vals : d_vals;
+
+    // (1) load; an id outside [0, V) is dropped (its logit read as -inf)
+    int id[2];
+    float l[2];
+    float m = -INFINITY;
+    bool bad = false, nan0 = false;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int t = lane + 32 * q;
+        id[q] = V + t;  // positions past Kt: never real, sort last
+        l[q] = -INFINITY;
+        if (t < Kt) {
+            int i = __ldg(ids + src + t);
+            float v = __ldg(vals + src + t);
+            if (i < 0 || i >= V) {
+                bad = true;
+                i = V + t;
+                v = -INFINITY;
+            }
+            if (i == 0 && v != v) nan0 = true;
+            m = fmaxf(m, v);  // NaN never raises the max
+            id[q] = i;
+            l[q] = v;
+        }
+    }
+    if (bad) atomicOr(status, kStatusBadListId);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    // the dense row's max: NaN when id 0 holds a NaN, else NaN is skipped
+    const float mx = __any_sync(0xffffffffu, nan0) ? __int_as_float(0x7fc00000) : m;
+
+    // (2) top-k: the first top_k entries in (logit desc, id asc) order
+    const bool tk_on = top_k > 0 && top_k < V && top_k < Kt;
+    unsigned long long tkey[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+        tkey[q] = lane + 32 * q < Kt ? (static_cast<unsigned long long>(logit_key(l[q])) << 32) |
+                                           (0xFFFFFFFFu - static_cast<uint32_t>(id[q]))
+                                     : 0ull;
+    unsigned long long tk_cut = 0ull;
+    if (tk_on) {
+        unsigned long long srt[2] = {tkey[0], tkey[1]};
+        warp_sort64_desc(srt);
+        tk_cut = warp_at(srt, top_k - 1);
+    }
+    // (3) masses
+    unsigned long long W[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const bool in = lane + 32 * q < Kt && (!tk_on || tkey[q] >= tk_cut);
+        W[q] = in ? mass_of(own_exp(scaled_x(l[q], mx, invT))) : 0ull;
+    }
+    const unsigned long long S = warp_sum_u64(W[0] + W[1]);
+
+    // (4) top-p and min-p: both keep a prefix of the (W desc, id asc) order
+    // (keys as in list_row_kernel)
+    auto wkey = [&](int q) -> unsigned long long {
+        if (lane + 32 * q >= Kt) return 0ull;
+        const unsigned long long w40 = W[q] >= (1ull << 40) ? (1ull << 40) - 1ull : W[q];
+        return (w40 << 24) | (0xFFFFFFull - (static_cast<uint32_t>(id[q]) & 0xFFFFFFu));
+    };
+    if (P < kKeepAll || MP > 0) {
+        unsigned long long srt[2] = {wkey(0), wkey(1)};
+        warp_sort64_desc(srt);
+        unsigned long long ws[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const unsigned long long w = srt[q] >> 24;
+            ws[q] = lane + 32 * q < Kt ? (w == (1ull << 40) - 1ull ? (1ull << 40) : w) : 0ull;
+        }
+        const unsigned long long w_top = __shfl_sync(0xffffffffu, ws[0], 0);
+        // inclusive prefix over the positions: lanes' first halves, then seconds
+        unsigned long long c0 = ws[0], c1 = ws[1];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y0 = __shfl_up_sync(0xffffffffu, c0, o);
+            const unsigned long long y1 = __shfl_up_sync(0xffffffffu, c1, o);
+            if (lane >= o) {
+                c0 += y0;
+                c1 += y1;
+            }
+        }
+        c1 += __shfl_sync(0xffffffffu, c0, 31);
+        const u128 target = static_cast<u128>(P) * S;
+        int keep = Kt;
+        const unsigned long long cum[2] = {c0, c1};
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const bool valid = lane + 32 * q < Kt;
+            // the shortest prefix reaching P; the first entry below min-p
+            const unsigned int hp = __ballot_sync(
+                0xffffffffu, valid && P < kKeepAll && (static_cast<u128>(cum[q]) << 32) >= target);
+            const unsigned int hm = __ballot_sync(
+                0xffffffffu,
+                valid && MP > 0 && (static_cast<u128>(ws[q]) << 32) < static_cast<u128>(MP) * w_top);
+            if (hp) keep = min(keep, 32 * q + __ffs(hp));
+            if (hm) keep = min(keep, 32 * q + __ffs(hm) - 1);
+        }
+        // the kept entries are the sorted positions below keep (keep >= 1
+        // unless min-p drops the top entry itself)
+        const unsigned long long kcut = keep > 0 ? warp_at(srt, keep - 1) : ~0ull;
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+            if (keep == 0 || wkey(q) < kcut) W[q] = 0ull;
+    }
+    const unsigned long long S_kept = warp_sum_u64(W[0] + W[1]);
+
+    // (5) the row sorted by id (ascending), with its kept masses
+    unsigned long long srt[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int t = lane + 32 * q;
+        srt[q] = t < Kt ? ((static_cast<unsigned long long>(0x7FFFFFFF - id[q]) << 32) |
+                           static_cast<uint32_t>(t))
+                        : 0ull;
+    }
+    warp_sort64_desc(srt);  // descending in 0x7FFFFFFF - id: ascending in id
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int p = lane + 32 * q;
+        const int t = static_cast<int>(srt[q] & 0xFFFFFFFFu);
+        // entry t's mass from the lane that holds it (every lane shuffles)
+        const unsigned long long w0 = __shfl_sync(0xffffffffu, W[0], t & 31);
+        const unsigned long long w1 = __shfl_sync(0xffffffffu, W[1], t & 31);
+        if (p < Kt) {
+            o_ids[r * Kt + p] = 0x7FFFFFFF - static_cast<int>(srt[q] >> 32);
+            o_W[r * Kt + p] = t < 32 ? w0 : w1;
+        }
+    }
+    if (lane == 0) o_S[r] = S_kept;
+}
+
 // The kept mass of id x in a row sorted by id (0 when absent).
 __device__ __forceinline__ unsigned long long list_mass(const int32_t* ids,
                                                         const unsigned long long* W, int Kt,
@@ -2392,29 +2588,40 @@ __global__ void __launch_bounds__(kListSeqWarps * 32) list_seq_kernel(
     if (b >= B) return;
     const long long per_seq = 2 * Kd + 1;
     auto row = [&](int j) { return static_cast<long long>(b) * per_seq + j; };  // list row
-    int n = 0;
+    // the acceptance tests, lane i taking position i (Kd < 32), all at once;
+    // the first rejection decides the run, and position n's uniform the draw
+    static_assert(kMaxRows < 32, "one lane per position");
     unsigned long long u64 = 0ull;
-    for (; n <= Kd; ++n) {
+    bool ok = true;
+    if (lane <= Kd) {
+        const int i = lane;
         uint32_t rr[4];
-        philox4x32_10(static_cast<uint32_t>(n), static_cast<uint32_t>(b),
+        philox4x32_10(static_cast<uint32_t>(i), static_cast<uint32_t>(b),
                       static_cast<uint32_t>(offset), static_cast<uint32_t>(offset >> 32),
                       static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32), rr);
         u64 = (static_cast<unsigned long long>(rr[2]) << 32) | rr[1];
-        if (n == Kd) break;  // every draft accepted: the bonus
-        const int32_t x = drafts[static_cast<long long>(b) * Kd + n];
-        bool ok = false;
-        if (x >= 0 && x < V) {
-            const long long rp = row(n), rq = row(Kd + 1 + n);
-            const unsigned long long Wp = list_mass(l_ids + rp * Kt, l_W + rp * Kt, Kt, x);
-            const unsigned long long Wq = list_mass(l_ids + rq * Kt, l_W + rq * Kt, Kt, x);
-            const unsigned long long U = rr[0] >> 8;
-            const u128 lhs = static_cast<u128>(U * Wq) * l_S[rp];
-            const u128 rhs = (static_cast<u128>(Wp) * l_S[rq]) << 24;
-            ok = lhs < rhs;
-        } else if (lane == 0) {
-            atomicOr(status, kStatusBadDraft);
+        if (i < Kd) {
+            const int32_t x = drafts[static_cast<long long>(b) * Kd + i];
+            ok = false;
+            if (x >= 0 && x < V) {
+                const long long rp = row(i), rq = row(Kd + 1 + i);
+                const unsigned long long Wp = list_mass(l_ids + rp * Kt, l_W + rp * Kt, Kt, x);
+                const unsigned long long Wq = list_mass(l_ids + rq * Kt, l_W + rq * Kt, Kt, x);
+                const unsigned long long U = rr[0] >> 8;
+                const u128 lhs = static_cast<u128>(U * Wq) * l_S[rp];
+                const u128 rhs = (static_cast<u128>(Wp) * l_S[rq]) << 24;
+                ok = lhs < rhs;
+            }
         }
-        if (!ok) break;
+    }
+    const unsigned int rej = __ballot_sync(0xffffffffu, lane < Kd && !ok);
+    const int n = rej ? __ffs(rej) - 1 : Kd;  // accepted drafts before the first rejection
+    u64 = __shfl_sync(0xffffffffu, u64, n);
+    // an invalid draft id counts as a rejection; flagged when it is reached
+    // (the tests after the first rejection are not part of the run)
+    if (lane == n && n < Kd) {
+        const int32_t x = drafts[static_cast<long long>(b) * Kd + n];
+        if (x < 0 || x >= V) atomicOr(status, kStatusBadDraft);
     }
     // the draw: over target list n in id order, weights the residual
     // max(0, Wp Sq - Wq Sp) at a rejection, else (the bonus, or an empty
@@ -2437,14 +2644,25 @@ __global__ void __launch_bounds__(kListSeqWarps * 32) list_seq_kernel(
         return x > y ? x - y : 0;
     };
     bool resid = rejected;
-    u128 mine = 0;
-    for (int p = a; p < e; ++p) mine += weight(p, resid);
+    // up to two positions a lane (lists of at most 64): both weights at once
+    // (their searches overlap), kept for the rescan below
+    u128 w2[2] = {0, 0};
+    auto weigh_all = [&]() -> u128 {
+        if (c <= 2) {
+            w2[0] = a < e ? weight(a, resid) : 0;
+            w2[1] = a + 1 < e ? weight(a + 1, resid) : 0;
+            return w2[0] + w2[1];
+        }
+        u128 m = 0;
+        for (int p = a; p < e; ++p) m += weight(p, resid);
+        return m;
+    };
+    u128 mine = weigh_all();
     u128 R = warp_sum_u128(mine);
     if (resid && R == 0) {  // only reachable through an invalid draft id
         if (lane == 0) atomicOr(status, kStatusZeroResidual);
         resid = false;
-        mine = 0;
-        for (int p = a; p < e; ++p) mine += weight(p, false);
+        mine = weigh_all();
         R = warp_sum_u128(mine);
     }
     int tok = V - 1;  // an empty row: as the dense draw
@@ -2462,7 +2680,7 @@ __global__ void __launch_bounds__(kListSeqWarps * 32) list_seq_kernel(
         if (lane == L) {
             u128 cum = incl - mine;
             for (int p = a; p < e; ++p) {
-                cum += weight(p, resid);
+                cum += c <= 2 ? (p == a ? w2[0] : w2[1]) : weight(p, resid);
                 if (cum > t) {
                     found = __ldg(pid + p);
                     break;
@@ -2674,7 +2892,13 @@ cudaError_t launch_accept_rejection_topk(const int32_t* t_ids, const float* t_va
     unsigned long long* l_W = reinterpret_cast<unsigned long long*>(w);
     w += round256(static_cast<size_t>(rows) * Kt * 8);
     unsigned long long* l_S = reinterpret_cast<unsigned long long*>(w);
-    if (Kt <= 256)
+    if (Kt <= kListWarpMax)
+        list_row_warp_kernel<<<static_cast<unsigned>((rows + kListWarpRows - 1) / kListWarpRows),
+                               kListWarpRows * 32, 0, s>>>(
+            t_ids, t_vals, d_ids, d_vals, Kd, Kt, V, rows, invT,
+            static_cast<unsigned long long>(P), top_k, static_cast<unsigned long long>(MP), l_ids,
+            l_W, l_S, status);
+    else if (Kt <= 256)
         list_row_kernel<64, 256><<<static_cast<unsigned>(rows), 64, 0, s>>>(
             t_ids, t_vals, d_ids, d_vals, Kd, Kt, V, invT, static_cast<unsigned long long>(P),
             top_k, static_cast<unsigned long long>(MP), l_ids, l_W, l_S, status);
