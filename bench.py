@@ -352,7 +352,7 @@ def run_ours(args, rank, world, device):
 
     depth = depth_controller_summary(per_m)
 
-    e2e = run_e2e(vw4, layers["nvfp4"], device, stream, steps, warmup, world)
+    e2e = run_e2e(vw4, layers["nvfp4"], layer_b, device, steps, warmup, world)
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
@@ -700,10 +700,16 @@ def run_head_timings(device, stream):
     return out
 
 
-def run_e2e(vw4, layer, device, stream, steps, warmup, world):
+def run_e2e(vw4, layer, layer_b, device, steps, warmup, world):
     """Same step through the public API with pinned host inputs and outputs:
-    every step copies the activation rows in and the fp32 results out."""
+    every step copies the activation rows in and the fp32 results out.  The
+    step is one CUDA graph, as an engine would issue it: the four input
+    copies on a copy stream, each GEMM waiting for its own input, and each
+    result's copy out on a second copy stream while the next GEMM runs.  As
+    in the headline, steps alternate two weight copies of the layer, so that
+    nothing is served from L2."""
     import torch
+    stream = torch.cuda.Stream(device)  # graphs are captured off the default stream
     M = HEAD_M
     g = np.random.default_rng(11)
     host_in = []
@@ -714,26 +720,54 @@ def run_e2e(vw4, layer, device, stream, steps, warmup, world):
     host_out = [torch.empty((M, N), dtype=torch.float32).pin_memory() for _, N, *_ in layer]
     dev_in = [h.to(device) for h in host_in]
     dev_out = [torch.empty((M, N), dtype=torch.float32, device=device) for _, N, *_ in layer]
-    gemms = [vw4.PreparedGemm(vw4.FMT_NVFP4, qd, sd, ts, M, stream=stream)
-             for (name, N, K, qd, sd, ts) in layer]
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    ev_in = [torch.cuda.Event() for _ in layer]
+    ev_out = [torch.cuda.Event() for _ in layer]
 
-    def step():
-        for j in range(len(layer)):
-            dev_in[j].copy_(host_in[j], non_blocking=True)
-            gemms[j](dev_in[j], dev_out[j])
-            host_out[j].copy_(dev_out[j], non_blocking=True)
+    def make_step(lay):
+        gemms = [vw4.PreparedGemm(vw4.FMT_NVFP4, qd, sd, ts, M, stream=stream)
+                 for (name, N, K, qd, sd, ts) in lay]
 
-    for _ in range(warmup):
-        step()
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
+        def step():
+            s_in.wait_stream(stream)
+            with torch.cuda.stream(s_in):
+                for j in range(len(lay)):
+                    dev_in[j].copy_(host_in[j], non_blocking=True)
+                    ev_in[j].record(s_in)
+            for j in range(len(lay)):
+                stream.wait_event(ev_in[j])
+                gemms[j](dev_in[j], dev_out[j])  # on `stream`
+                ev_out[j].record(stream)
+                s_out.wait_event(ev_out[j])
+                with torch.cuda.stream(s_out):
+                    host_out[j].copy_(dev_out[j], non_blocking=True)
+            stream.wait_stream(s_out)
+        return step
+
+    graphs = []
+    for lay in (layer, layer_b):
+        step = make_step(lay)
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                step()
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            step()
+        torch.cuda.synchronize()
+        graphs.append(gr)
+    with torch.cuda.stream(stream):  # replays run on the current stream: this one
+        for i in range(warmup):
+            graphs[i % 2].replay()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            graphs[i % 2].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
     ms = reduce_max(e0.elapsed_time(e1), world)
     h2d = sum(M * K * 2 for _, N, K in STEP)
     d2h = sum(M * N * 4 for _, N, K in STEP)
