@@ -2365,31 +2365,43 @@ __global__ void __launch_bounds__(NT) list_row_kernel(
 }
 
 // ------------------------------------------------ top-k lists, warp rows
-// Lists of at most 64 entries: one warp per list row, the same steps as
-// list_row_kernel with the row in registers -- lane l holds positions l and
-// l + 32 -- and every sort a bitonic network over the 64 positions whose
-// partners are exchanged by shuffles, so no step waits on a block barrier.
-constexpr int kListWarpMax = 64;
+// Lists of at most 256 entries: one warp per list row, the same steps as
+// list_row_kernel with the row in registers -- lane l holds positions
+// l + 32 r, r < R (R = 2, 4, 8 for up to 64, 128, 256 entries) -- and every
+// sort a bitonic network over the 32 R positions: partners less than 32
+// apart are exchanged by shuffles, the others are in the same lane.  No step
+// waits on a block barrier.
+constexpr int kListWarpMax = 256;
 constexpr int kListWarpRows = 4;  // rows (warps) per CTA
 
 __device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int o) {
     return __shfl_xor_sync(0xffffffffu, v, o);
 }
 
-// Sorts the 64 keys a[r] at positions lane + 32 r in descending order.
-__device__ __forceinline__ void warp_sort64_desc(unsigned long long (&a)[2]) {
+// Sorts the 32 R keys a[r] at positions lane + 32 r in descending order.
+template <int R>
+__device__ __forceinline__ void warp_sort_desc(unsigned long long (&a)[R]) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int k = 2; k <= 64; k <<= 1) {
+    for (int k = 2; k <= 32 * R; k <<= 1) {
 #pragma unroll
         for (int j = k >> 1; j > 0; j >>= 1) {
-            if (j == 32) {  // (k = 64) partners in the same lane: the lower keeps the larger
-                const unsigned long long x = a[0], y = a[1];
-                a[0] = x > y ? x : y;
-                a[1] = x > y ? y : x;
+            if (j >= 32) {
+                // partners in the same lane: registers r and r ^ (j / 32)
+                const int jr = j >> 5;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    if (r & jr) continue;  // (the pair is handled from its lower register)
+                    const int p = lane + 32 * r;
+                    const unsigned long long x = a[r], y = a[r | jr];
+                    const bool desc = (p & k) == 0;  // the lower position keeps the larger
+                    const bool swap = desc ? x < y : x > y;
+                    a[r] = swap ? y : x;
+                    a[r | jr] = swap ? x : y;
+                }
             } else {
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
+                for (int r = 0; r < R; ++r) {
                     const int p = lane + 32 * r;
                     const unsigned long long y = shfl_xor_u64(a[r], j);
                     // in a block sorted descending ((p & k) == 0) the lower
@@ -2402,9 +2414,20 @@ __device__ __forceinline__ void warp_sort64_desc(unsigned long long (&a)[2]) {
     }
 }
 
+// Register r of an array (r the same in every lane, or not: no local memory).
+template <int R, class T>
+__device__ __forceinline__ T reg_at(const T (&a)[R], int r) {
+    T v = a[0];
+#pragma unroll
+    for (int q = 1; q < R; ++q)
+        if (q == r) v = a[q];
+    return v;
+}
+
 // The key at sorted position p (the same p in every lane).
-__device__ __forceinline__ unsigned long long warp_at(const unsigned long long (&a)[2], int p) {
-    return __shfl_sync(0xffffffffu, p < 32 ? a[0] : a[1], p & 31);
+template <int R>
+__device__ __forceinline__ unsigned long long warp_at(const unsigned long long (&a)[R], int p) {
+    return __shfl_sync(0xffffffffu, reg_at<R>(a, p >> 5), p & 31);
 }
 
 __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
@@ -2413,6 +2436,7 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
     return v;
 }
 
+template <int R>
 __global__ void __launch_bounds__(kListWarpRows * 32) list_row_warp_kernel(
     const int32_t* __restrict__ t_ids, const float* __restrict__ t_vals,
     const int32_t* __restrict__ d_ids, const float* __restrict__ d_vals, int Kd, int Kt, int V,
@@ -2430,12 +2454,12 @@ __global__ void __launch_bounds__(kListWarpRows * 32) list_row_warp_kernel(
     const float* vals = j <= Kd ? t_vals : d_vals;
 
     // (1) load; an id outside [0, V) is dropped (its logit read as -inf)
-    int id[2];
-    float l[2];
+    int id[R];
+    float l[R];
     float m = -INFINITY;
     bool bad = false, nan0 = false;
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < R; ++q) {
         const int t = lane + 32 * q;
         id[q] = V + t;  // positions past Kt: never real, sort last
         l[q] = -INFINITY;
@@ -2461,26 +2485,30 @@ __global__ void __launch_bounds__(kListWarpRows * 32) list_row_warp_kernel(
 
     // (2) top-k: the first top_k entries in (logit desc, id asc) order
     const bool tk_on = top_k > 0 && top_k < V && top_k < Kt;
-    unsigned long long tkey[2];
+    unsigned long long tkey[R];
 #pragma unroll
-    for (int q = 0; q < 2; ++q)
+    for (int q = 0; q < R; ++q)
         tkey[q] = lane + 32 * q < Kt ? (static_cast<unsigned long long>(logit_key(l[q])) << 32) |
                                            (0xFFFFFFFFu - static_cast<uint32_t>(id[q]))
                                      : 0ull;
     unsigned long long tk_cut = 0ull;
     if (tk_on) {
-        unsigned long long srt[2] = {tkey[0], tkey[1]};
-        warp_sort64_desc(srt);
-        tk_cut = warp_at(srt, top_k - 1);
+        unsigned long long srt[R];
+#pragma unroll
+        for (int q = 0; q < R; ++q) srt[q] = tkey[q];
+        warp_sort_desc<R>(srt);
+        tk_cut = warp_at<R>(srt, top_k - 1);
     }
     // (3) masses
-    unsigned long long W[2];
+    unsigned long long W[R];
+    unsigned long long part = 0ull;
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < R; ++q) {
         const bool in = lane + 32 * q < Kt && (!tk_on || tkey[q] >= tk_cut);
         W[q] = in ? mass_of(own_exp(scaled_x(l[q], mx, invT))) : 0ull;
+        part += W[q];
     }
-    const unsigned long long S = warp_sum_u64(W[0] + W[1]);
+    const unsigned long long S = warp_sum_u64(part);
 
     // (4) top-p and min-p: both keep a prefix of the (W desc, id asc) order
     // (keys as in list_row_kernel)
@@ -2490,36 +2518,35 @@ __global__ void __launch_bounds__(kListWarpRows * 32) list_row_warp_kernel(
         return (w40 << 24) | (0xFFFFFFull - (static_cast<uint32_t>(id[q]) & 0xFFFFFFu));
     };
     if (P < kKeepAll || MP > 0) {
-        unsigned long long srt[2] = {wkey(0), wkey(1)};
-        warp_sort64_desc(srt);
-        unsigned long long ws[2];
+        unsigned long long srt[R];
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
+        for (int q = 0; q < R; ++q) srt[q] = wkey(q);
+        warp_sort_desc<R>(srt);
+        unsigned long long ws[R];
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
             const unsigned long long w = srt[q] >> 24;
             ws[q] = lane + 32 * q < Kt ? (w == (1ull << 40) - 1ull ? (1ull << 40) : w) : 0ull;
         }
         const unsigned long long w_top = __shfl_sync(0xffffffffu, ws[0], 0);
-        // inclusive prefix over the positions: lanes' first halves, then seconds
-        unsigned long long c0 = ws[0], c1 = ws[1];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const unsigned long long y0 = __shfl_up_sync(0xffffffffu, c0, o);
-            const unsigned long long y1 = __shfl_up_sync(0xffffffffu, c1, o);
-            if (lane >= o) {
-                c0 += y0;
-                c1 += y1;
-            }
-        }
-        c1 += __shfl_sync(0xffffffffu, c0, 31);
         const u128 target = static_cast<u128>(P) * S;
         int keep = Kt;
-        const unsigned long long cum[2] = {c0, c1};
+        unsigned long long base = 0ull;  // the mass of positions 0 .. 32 q - 1
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
+        for (int q = 0; q < R; ++q) {
+            // inclusive prefix over positions 32 q + 0 .. 31
+            unsigned long long cum = ws[q];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long y = __shfl_up_sync(0xffffffffu, cum, o);
+                if (lane >= o) cum += y;
+            }
+            cum += base;
+            base = __shfl_sync(0xffffffffu, cum, 31);
             const bool valid = lane + 32 * q < Kt;
             // the shortest prefix reaching P; the first entry below min-p
             const unsigned int hp = __ballot_sync(
-                0xffffffffu, valid && P < kKeepAll && (static_cast<u128>(cum[q]) << 32) >= target);
+                0xffffffffu, valid && P < kKeepAll && (static_cast<u128>(cum) << 32) >= target);
             const unsigned int hm = __ballot_sync(
                 0xffffffffu,
                 valid && MP > 0 && (static_cast<u128>(ws[q]) << 32) < static_cast<u128>(MP) * w_top);
@@ -2528,33 +2555,40 @@ __global__ void __launch_bounds__(kListWarpRows * 32) list_row_warp_kernel(
         }
         // the kept entries are the sorted positions below keep (keep >= 1
         // unless min-p drops the top entry itself)
-        const unsigned long long kcut = keep > 0 ? warp_at(srt, keep - 1) : ~0ull;
+        const unsigned long long kcut = keep > 0 ? warp_at<R>(srt, keep - 1) : ~0ull;
 #pragma unroll
-        for (int q = 0; q < 2; ++q)
+        for (int q = 0; q < R; ++q)
             if (keep == 0 || wkey(q) < kcut) W[q] = 0ull;
     }
-    const unsigned long long S_kept = warp_sum_u64(W[0] + W[1]);
+    unsigned long long kpart = 0ull;
+#pragma unroll
+    for (int q = 0; q < R; ++q) kpart += W[q];
+    const unsigned long long S_kept = warp_sum_u64(kpart);
 
     // (5) the row sorted by id (ascending), with its kept masses
-    unsigned long long srt[2];
+    unsigned long long srt[R];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < R; ++q) {
         const int t = lane + 32 * q;
         srt[q] = t < Kt ? ((static_cast<unsigned long long>(0x7FFFFFFF - id[q]) << 32) |
                            static_cast<uint32_t>(t))
                         : 0ull;
     }
-    warp_sort64_desc(srt);  // descending in 0x7FFFFFFF - id: ascending in id
+    warp_sort_desc<R>(srt);  // descending in 0x7FFFFFFF - id: ascending in id
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < R; ++q) {
         const int p = lane + 32 * q;
         const int t = static_cast<int>(srt[q] & 0xFFFFFFFFu);
         // entry t's mass from the lane that holds it (every lane shuffles)
-        const unsigned long long w0 = __shfl_sync(0xffffffffu, W[0], t & 31);
-        const unsigned long long w1 = __shfl_sync(0xffffffffu, W[1], t & 31);
+        unsigned long long wt = 0ull;
+#pragma unroll
+        for (int u = 0; u < R; ++u) {
+            const unsigned long long x = __shfl_sync(0xffffffffu, W[u], t & 31);
+            if (u == (t >> 5)) wt = x;
+        }
         if (p < Kt) {
             o_ids[r * Kt + p] = 0x7FFFFFFF - static_cast<int>(srt[q] >> 32);
-            o_W[r * Kt + p] = t < 32 ? w0 : w1;
+            o_W[r * Kt + p] = wt;
         }
     }
     if (lane == 0) o_S[r] = S_kept;
@@ -2882,7 +2916,7 @@ cudaError_t launch_accept_rejection_topk(const int32_t* t_ids, const float* t_va
                                          int32_t* len, void* ws, size_t ws_bytes,
                                          uint32_t* status, cudaStream_t s) {
     if (Kt < 1 || Kt > kListMax) return cudaErrorNotSupported;
-    static_assert(kListMax == 1024, "the two row kernel shapes cover lists up to 1024");
+    static_assert(kListMax == 1024, "the row kernel shapes cover lists up to 1024");
     const long long rows = static_cast<long long>(B) * (2 * Kd + 1);
     if (rows > 0x7fffffffll) return cudaErrorNotSupported;
     if (rejection_topk_workspace_bytes(B, Kd, Kt) > ws_bytes) return cudaErrorInvalidValue;
@@ -2892,20 +2926,26 @@ cudaError_t launch_accept_rejection_topk(const int32_t* t_ids, const float* t_va
     unsigned long long* l_W = reinterpret_cast<unsigned long long*>(w);
     w += round256(static_cast<size_t>(rows) * Kt * 8);
     unsigned long long* l_S = reinterpret_cast<unsigned long long*>(w);
-    if (Kt <= kListWarpMax)
-        list_row_warp_kernel<<<static_cast<unsigned>((rows + kListWarpRows - 1) / kListWarpRows),
-                               kListWarpRows * 32, 0, s>>>(
-            t_ids, t_vals, d_ids, d_vals, Kd, Kt, V, rows, invT,
-            static_cast<unsigned long long>(P), top_k, static_cast<unsigned long long>(MP), l_ids,
-            l_W, l_S, status);
-    else if (Kt <= 256)
-        list_row_kernel<64, 256><<<static_cast<unsigned>(rows), 64, 0, s>>>(
-            t_ids, t_vals, d_ids, d_vals, Kd, Kt, V, invT, static_cast<unsigned long long>(P),
-            top_k, static_cast<unsigned long long>(MP), l_ids, l_W, l_S, status);
+    const unsigned wgrid = static_cast<unsigned>((rows + kListWarpRows - 1) / kListWarpRows);
+    const unsigned long long Pu = static_cast<unsigned long long>(P);
+    const unsigned long long MPu = static_cast<unsigned long long>(MP);
+    static_assert(kListWarpMax == 256, "three warp shapes: 64, 128 and 256 entries");
+    if (Kt <= 64)
+        list_row_warp_kernel<2><<<wgrid, kListWarpRows * 32, 0, s>>>(
+            t_ids, t_vals, d_ids, d_vals, Kd, Kt, V, rows, invT, Pu, top_k, MPu, l_ids, l_W,
+            l_S, status);
+    else if (Kt <= 128)
+        list_row_warp_kernel<4><<<wgrid, kListWarpRows * 32, 0, s>>>(
+            t_ids, t_vals, d_ids, d_vals, Kd, Kt, V, rows, invT, Pu, top_k, MPu, l_ids, l_W,
+            l_S, status);
+    else if (Kt <= kListWarpMax)
+        list_row_warp_kernel<8><<<wgrid, kListWarpRows * 32, 0, s>>>(
+            t_ids, t_vals, d_ids, d_vals, Kd, Kt, V, rows, invT, Pu, top_k, MPu, l_ids, l_W,
+            l_S, status);
     else
         list_row_kernel<256, 1024><<<static_cast<unsigned>(rows), 256, 0, s>>>(
-            t_ids, t_vals, d_ids, d_vals, Kd, Kt, V, invT, static_cast<unsigned long long>(P),
-            top_k, static_cast<unsigned long long>(MP), l_ids, l_W, l_S, status);
+            t_ids, t_vals, d_ids, d_vals, Kd, Kt, V, invT, Pu, top_k, MPu, l_ids, l_W, l_S,
+            status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     list_seq_kernel<<<(B + kListSeqWarps - 1) / kListSeqWarps, kListSeqWarps * 32, 0, s>>>(
