@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(512) prep_act_kernel(
     int dense_M,
     int rows_are_pairs, int topk, SegTable* seg, uint8_t* act, uint32_t* tile_cnt, int n_cnt,
     unsigned long long* am_key, uint32_t* am_cnt, const int32_t* __restrict__ ids, int P, int E,
-    uint32_t* status, float* out_zero, int ldo, int N) {
+    uint32_t* status, float* out_zero, int ldo, int N, int stage_ctas) {
     __shared__ SegTable lt;
     __shared__ RouteScratch rs;
     // The GEMM may start streaming weights now; it waits for this grid before
@@ -242,8 +242,11 @@ __global__ void __launch_bounds__(512) prep_act_kernel(
     // still runs: nothing is read or written before that grid has finished.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // CTA (sgi, st0) converts stages st0, st0 + stage_ctas, ... of segment
+    // sgi: one CTA per stage for dense calls; for MoE calls a few per
+    // segment, so that each CTA's routing (below) serves several stages
     const int T = K / kStageK;
-    const int sgi = blockIdx.x / T, st = blockIdx.x % T;
+    const int sgi = blockIdx.x / stage_ctas, st0 = blockIdx.x % stage_ctas;
     const int r = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (blockIdx.x == 0) {
         for (int i = threadIdx.x; i < n_cnt; i += blockDim.x) tile_cnt[i] = 0u;
@@ -279,76 +282,78 @@ __global__ void __launch_bounds__(512) prep_act_kernel(
             src_row = rows_are_pairs ? pr : pr / topk;
         }
     }
-    uint8_t* blk = act + (static_cast<size_t>(sgi) * T + st) * act_stride(nr);
-    __half* dst = reinterpret_cast<__half*>(blk);
-    float* inv = reinterpret_cast<float*>(blk + act_bytes(nr));
-    // Where this lane's 16-byte chunk goes in the stage's [nr][256] block (16
-    // rows: two [8][256] halves, one per mma n-tile, laid out alike).  The
-    // order puts a consumer lane's B operands of consecutive MMAs in one chunk
-    // and the XOR keeps a quarter-warp's reads on distinct bank groups.
-    //  nvfp4: lane holds elements 8*lane .. 8*lane+7 (consumer lane c = lane/8
-    //         covers [64c, 64c+64) of the stage);
-    //  Q4_0:  lane = 4*beta + c holds elements 4c+{0,2,1,3} and 16+4c+{0,2,1,3}
-    //         of 32-element block beta.
-    int pos;
-    if (fmt == 1) {
-        const int c = lane >> 3, i = lane & 7;
-        pos = r * 256 + c * 64 + ((i ^ (((r & 1) << 2) | c)) << 3);
-    } else {
-        pos = r * 256 + ((lane ^ ((r & 1) << 2)) << 3);
-    }
-    if (r >= count) {
-        *reinterpret_cast<uint4*>(dst + pos) = make_uint4(0u, 0u, 0u, 0u);
-        if (lane == 0) inv[r] = 0.0f;
-        return;
-    }
-    const uint16_t* a = A + static_cast<size_t>(src_row) * lda + st * kStageK;
-    float x[8];
-    // past K_true (a K padded to whole stages) the activations are zero; a
-    // lane's 8 (nvfp4) or 32-block (Q4_0) elements lie wholly on one side
-    const int k_lane = st * kStageK + (fmt == 1 ? 8 * lane : 32 * (lane >> 2));
-    if (k_lane >= K_true) {
+    for (int st = st0; st < T; st += stage_ctas) {
+        uint8_t* blk = act + (static_cast<size_t>(sgi) * T + st) * act_stride(nr);
+        __half* dst = reinterpret_cast<__half*>(blk);
+        float* inv = reinterpret_cast<float*>(blk + act_bytes(nr));
+        // Where this lane's 16-byte chunk goes in the stage's [nr][256] block (16
+        // rows: two [8][256] halves, one per mma n-tile, laid out alike).  The
+        // order puts a consumer lane's B operands of consecutive MMAs in one chunk
+        // and the XOR keeps a quarter-warp's reads on distinct bank groups.
+        //  nvfp4: lane holds elements 8*lane .. 8*lane+7 (consumer lane c = lane/8
+        //         covers [64c, 64c+64) of the stage);
+        //  Q4_0:  lane = 4*beta + c holds elements 4c+{0,2,1,3} and 16+4c+{0,2,1,3}
+        //         of 32-element block beta.
+        int pos;
+        if (fmt == 1) {
+            const int c = lane >> 3, i = lane & 7;
+            pos = r * 256 + c * 64 + ((i ^ (((r & 1) << 2) | c)) << 3);
+        } else {
+            pos = r * 256 + ((lane ^ ((r & 1) << 2)) << 3);
+        }
+        if (r >= count) {
+            *reinterpret_cast<uint4*>(dst + pos) = make_uint4(0u, 0u, 0u, 0u);
+            if (lane == 0) inv[r] = 0.0f;
+            continue;
+        }
+        const uint16_t* a = A + static_cast<size_t>(src_row) * lda + st * kStageK;
+        float x[8];
+        // past K_true (a K padded to whole stages) the activations are zero; a
+        // lane's 8 (nvfp4) or 32-block (Q4_0) elements lie wholly on one side
+        const int k_lane = st * kStageK + (fmt == 1 ? 8 * lane : 32 * (lane >> 2));
+        if (k_lane >= K_true) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) x[j] = 0.0f;
-    } else if (fmt == 1) {
-        load8_bf16(a + 8 * lane, vec_ok != 0, x);
-    } else {
-        const int beta = lane >> 2, c = lane & 3;
-        float lo4[4], hi4[4];
-        load4_bf16(a + 32 * beta + 4 * c, vec_ok != 0, lo4);
-        load4_bf16(a + 32 * beta + 16 + 4 * c, vec_ok != 0, hi4);
-        x[0] = lo4[0]; x[1] = lo4[2]; x[2] = lo4[1]; x[3] = lo4[3];
-        x[4] = hi4[0]; x[5] = hi4[2]; x[6] = hi4[1]; x[7] = hi4[3];
-    }
-    float amax = 0.0f;
-    int bad = 0;
+            for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+        } else if (fmt == 1) {
+            load8_bf16(a + 8 * lane, vec_ok != 0, x);
+        } else {
+            const int beta = lane >> 2, c = lane & 3;
+            float lo4[4], hi4[4];
+            load4_bf16(a + 32 * beta + 4 * c, vec_ok != 0, lo4);
+            load4_bf16(a + 32 * beta + 16 + 4 * c, vec_ok != 0, hi4);
+            x[0] = lo4[0]; x[1] = lo4[2]; x[2] = lo4[1]; x[3] = lo4[3];
+            x[4] = hi4[0]; x[5] = hi4[2]; x[6] = hi4[1]; x[7] = hi4[3];
+        }
+        float amax = 0.0f;
+        int bad = 0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const float v = fabsf(x[j]);
-        if (!(v <= 3.4e38f)) bad = 1;
-        else amax = fmaxf(amax, v);
-    }
+        for (int j = 0; j < 8; ++j) {
+            const float v = fabsf(x[j]);
+            if (!(v <= 3.4e38f)) bad = 1;
+            else amax = fmaxf(amax, v);
+        }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        bad |= __shfl_xor_sync(0xffffffffu, bad, o);
-    }
-    int n = 0;
-    if (!bad && amax > 0.0f) {
-        int ex;
-        frexpf(amax, &ex);  // amax in [2^(ex-1), 2^ex)
-        n = 15 - ex;        // scaled max in [2^14, 2^15)
-        n = n < -125 ? -125 : (n > 125 ? 125 : n);
-    }
-    const float sc = pow2f(n);
-    uint32_t h[4];
+        for (int o = 16; o > 0; o >>= 1) {
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+        }
+        int n = 0;
+        if (!bad && amax > 0.0f) {
+            int ex;
+            frexpf(amax, &ex);  // amax in [2^(ex-1), 2^ex)
+            n = 15 - ex;        // scaled max in [2^14, 2^15)
+            n = n < -125 ? -125 : (n > 125 ? 125 : n);
+        }
+        const float sc = pow2f(n);
+        uint32_t h[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const __half2 v = __floats2half2_rn(x[2 * j] * sc, x[2 * j + 1] * sc);
-        h[j] = *reinterpret_cast<const uint32_t*>(&v);
+        for (int j = 0; j < 4; ++j) {
+            const __half2 v = __floats2half2_rn(x[2 * j] * sc, x[2 * j + 1] * sc);
+            h[j] = *reinterpret_cast<const uint32_t*>(&v);
+        }
+        *reinterpret_cast<uint4*>(dst + pos) = make_uint4(h[0], h[1], h[2], h[3]);
+        if (lane == 0) inv[r] = pow2f(-n);
     }
-    *reinterpret_cast<uint4*>(dst + pos) = make_uint4(h[0], h[1], h[2], h[3]);
-    if (lane == 0) inv[r] = pow2f(-n);
 }
 
 // ------------------------------------------------------------ GEMM pieces
@@ -1261,7 +1266,14 @@ cudaError_t launch_prep_act(const uint16_t* A, int lda, int K, int fmt, int dens
     const int vec_ok = ((reinterpret_cast<uintptr_t>(A) & 15u) == 0 && lda % 8 == 0) ? 1 : 0;
     // a programmatic dependent of whatever kernel precedes it on the stream
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(n_seg_grid * T);
+    // MoE: a few CTAs per segment, each computing the routing for several
+    // stages, about 256 CTAs in all (the routing is redundant per CTA)
+    int stage_ctas = T;
+    if (dense_M <= 0) {
+        stage_ctas = 256 / (n_seg_grid > 0 ? n_seg_grid : 1);
+        stage_ctas = stage_ctas < 1 ? 1 : (stage_ctas > T ? T : stage_ctas);
+    }
+    cfg.gridDim = dim3(n_seg_grid * stage_ctas);
     cfg.blockDim = dim3(32 * nr);  // one warp per verify row
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
@@ -1274,7 +1286,7 @@ cudaError_t launch_prep_act(const uint16_t* A, int lda, int K, int fmt, int dens
                               fmt, nr, dense_M,
                               rows_are_pairs, topk, ws.seg, ws.act, ws.tile_cnt, n_counters,
                               ws.am_key, ws.am_cnt, ids, dense_M > 0 ? 0 : n_seg_grid, E, status,
-                              out_zero, ldo, N);
+                              out_zero, ldo, N, stage_ctas);
 }
 
 template <int FMT, int NR>
