@@ -79,7 +79,7 @@ def kernel_source_hash() -> str:
 
 
 def measured_traffic():
-    """DRAM bytes (read + write) of the GEMM kernel per layer step (its 7
+    """DRAM bytes (read + write) of the GEMM kernel per layer step (its 4
     launches), from the committed ncu summary -- null when the kernel sources
     changed since those counters were taken."""
     try:
@@ -881,7 +881,9 @@ def run_case(case: str, device):
     packed layer step at M = 8 (3 warm-up passes, then 1); 'N,K,M[,q4_0]' = one
     GEMM of that shape, nvfp4 unless q4_0 is named (3 warm-up calls, then 1); 'rejection:K' = the
     rejection accept of the stochastic sweep (B = 256, V = 151936, K drafts),
-    4 calls; 'lists:K' = the accept over top-64 lists of those rows, 4 calls."""
+    4 calls; 'lists:K' = the accept over top-64 lists of those rows, 4 calls;
+    'moe:M' = the MoE head (gate/up, then down with the gate combine) at M
+    tokens, 4 calls."""
     import torch
     import speculative_decode_verification_w4_gb300 as vw4
     torch.cuda.set_device(device)
@@ -920,6 +922,31 @@ def run_case(case: str, device):
         print(f"case {case}: 4 calls, mean run {ln.float().mean().item():.3f}, device status "
               f"{vw4.vw4_get_device_status()}", flush=True)
         return
+    if case.startswith("moe:"):  # the MoE head (gate/up then down with the combine), M tokens
+        import synth
+        M = int(case.split(":")[1])
+        E, d, f, topk = 128, 2048, 768, 8
+        gu = [torch.from_numpy(x).to(device) if isinstance(x, np.ndarray) else x
+              for x in synth.linear(200, E * 2 * f, d, "nvfp4")]
+        dn = [torch.from_numpy(x).to(device) if isinstance(x, np.ndarray) else x
+              for x in synth.linear(210, E * d, f, "nvfp4")]
+        ids, gates = synth.routing(300 if M == 8 else 302, M, E, topk)
+        ids_d = torch.from_numpy(np.ascontiguousarray(ids, np.int32)).to(device)
+        gates_d = torch.from_numpy(np.ascontiguousarray(gates, np.float32)).to(device)
+        A = torch.from_numpy(synth.activations(synth.rng(301), M, d).view(np.int16)).view(
+            torch.bfloat16).to(device)
+        pair = torch.empty((M * topk, 2 * f), dtype=torch.float32, device=device)
+        res = torch.empty((M, d), dtype=torch.float32, device=device)
+        h = torch.zeros((M * topk, f), dtype=torch.bfloat16, device=device)
+        for _ in range(4):
+            vw4.verify_moe_w4(vw4.FMT_NVFP4, *gu, E, A, 0, ids_d, gates_d, 0, out=pair,
+                              workspace=ws)
+            vw4.verify_moe_w4(vw4.FMT_NVFP4, *dn, E, h, 1, ids_d, gates_d, 1, out=res,
+                              workspace=ws)
+        torch.cuda.synchronize()
+        print(f"case {case}: 4 head calls, device status {vw4.vw4_get_device_status()}",
+              flush=True)
+        return
     if case == "dense":
         layer = make_layer("nvfp4", device)
         acts = make_acts(HEAD_M, device, seed=7 + HEAD_M)
@@ -955,7 +982,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--case", default=None,
-                    help="profiling helper: 'dense', 'N,K,M[,q4_0]', 'rejection:K' or 'lists:K' (see run_case); "
+                    help="profiling helper: 'dense', 'N,K,M[,q4_0]', 'rejection:K', 'lists:K' or 'moe:M' (see run_case); "
                          "no JSON line")
     args = ap.parse_args()
     if args.warmup < 3:
