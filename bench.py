@@ -245,6 +245,26 @@ def run_ours(args, rank, world, device):
         barrier()
         return e0.elapsed_time(e1)
 
+    def time_steps(g_pair, g_one, n, warmup):
+        """ms for exactly n steps: n // 2 replays of the two-step graph, then
+        the one-step graph if n is odd (after ceil(warmup / 2) pair replays)."""
+        for _ in range((warmup + 1) // 2):
+            g_pair.replay()
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n // 2):
+            g_pair.replay()
+        if n % 2:
+            g_one.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        return e0.elapsed_time(e1)
+
     def time_alone(fmt, name, N, K, qd, sd, ts, A, out, steps):
         """One call timed alone: a graph of R calls on R different weight copies
         (more than 2x L2 of weights in flight, so nothing is served from L2)."""
@@ -264,17 +284,21 @@ def run_ours(args, rank, world, device):
     steps, warmup = args.steps, args.warmup
     peak, peak_kind = read_peaks()
     with ClockSampler(torch.cuda.current_device()) as clk:
-        # headline: one step = the packed layer at M = 8 (a CUDA graph of the
-        # four C-ABI calls, replayed K times back to back)
+        # headline: one step = the packed layer at M = 8 (the four C-ABI
+        # calls).  Consecutive steps alternate the two weight copies and are
+        # captured in pairs, one CUDA graph per pair, as an engine captures
+        # consecutive layers in one graph; an odd K ends on a one-step graph.
+        def two_steps():
+            one_step("nvfp4", HEAD_M)
+            one_step("nvfp4", HEAD_M, layer_b)
         g_head = capture(lambda: one_step("nvfp4", HEAD_M))
-        g_head_b = capture(lambda: one_step("nvfp4", HEAD_M, layer_b))
+        g_pair = capture(two_steps)
         soak_end = time.time() + 0.4
         while time.time() < soak_end:      # let the clock sampler see the load
             for _ in range(10):
-                g_head.replay()
-                g_head_b.replay()
+                g_pair.replay()
             torch.cuda.synchronize()
-        ms = time_graph(g_head, steps, warmup, g_head_b)
+        ms = time_steps(g_pair, g_head, steps, warmup)
         ms_max = reduce_max(ms, world)
         ms_per_step = ms_max / steps
         value = step_bytes(HEAD_M) * steps * world / (ms_max * 1e-3) / 1e9
@@ -364,8 +388,9 @@ def run_ours(args, rank, world, device):
                    "bytes_per_step": step_bytes(HEAD_M),
                    "l2": "inputs larger than L2: 191.7 MB of weights+scales per step, two "
                          "weight copies alternating (383 MB per two steps) vs 129 MB L2",
-                   "timing": "CUDA graphs of the step's 4 C-ABI calls on the two weight copies, "
-                             "replayed alternately back to back",
+                   "timing": "one CUDA graph per two consecutive steps (the 4 C-ABI calls on "
+                             "weight copy A, then on copy B), replayed back to back; an odd "
+                             "step count ends on a one-step graph",
                    "parallelism": f"replicas x{world}"},
         "per_m": per_m, "unpacked_7_calls": unpacked, "gate": gate, "accept_us": accept,
         "depth_controller": depth,
@@ -702,27 +727,37 @@ def run_head_timings(device, stream):
 
 def run_e2e(vw4, layer, layer_b, device, steps, warmup, world):
     """Same step through the public API with pinned host inputs and outputs:
-    every step copies the activation rows in and the fp32 results out.  The
-    step is one CUDA graph, as an engine would issue it: the four input
-    copies on a copy stream, each GEMM waiting for its own input, and each
-    result's copy out on a second copy stream while the next GEMM runs.  As
-    in the headline, steps alternate two weight copies of the layer, so that
-    nothing is served from L2."""
+    every step copies its four activation inputs in and its four fp32
+    results out.  As an engine would issue it, the step is part of a CUDA
+    graph: the inputs, which sit contiguous in one pinned buffer, come in
+    with one copy on a copy stream that the first GEMM waits for; the
+    results of the first three GEMMs (contiguous too) go out with one copy
+    on a second copy stream while the last GEMM runs, and the last result
+    with one copy after it.  As in the headline, consecutive steps alternate
+    two weight copies of the layer (so that nothing is served from L2) and
+    are captured two to a graph."""
     import torch
+    import synth
     stream = torch.cuda.Stream(device)  # graphs are captured off the default stream
     M = HEAD_M
     g = np.random.default_rng(11)
-    host_in = []
-    for _, N, K, *_ in layer:
-        import synth
+    Ks = [K for _, N, K, *_ in layer]
+    Ns = [N for _, N, *_ in layer]
+    in_off = np.cumsum([0] + [M * K for K in Ks]).tolist()
+    out_off = np.cumsum([0] + [M * N for N in Ns]).tolist()
+    host_in = torch.empty(in_off[-1], dtype=torch.bfloat16).pin_memory()
+    for j, K in enumerate(Ks):
         bits = synth.activations(g, M, K)
-        host_in.append(torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).pin_memory())
-    host_out = [torch.empty((M, N), dtype=torch.float32).pin_memory() for _, N, *_ in layer]
-    dev_in = [h.to(device) for h in host_in]
-    dev_out = [torch.empty((M, N), dtype=torch.float32, device=device) for _, N, *_ in layer]
+        host_in[in_off[j]:in_off[j + 1]].copy_(
+            torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).reshape(-1))
+    host_out = torch.empty(out_off[-1], dtype=torch.float32).pin_memory()
+    dev_in = torch.empty(in_off[-1], dtype=torch.bfloat16, device=device)
+    dev_out = torch.empty(out_off[-1], dtype=torch.float32, device=device)
+    d_in = [dev_in[in_off[j]:in_off[j + 1]].view(M, Ks[j]) for j in range(len(Ks))]
+    d_out = [dev_out[out_off[j]:out_off[j + 1]].view(M, Ns[j]) for j in range(len(Ns))]
+    last = len(Ns) - 1
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
-    ev_in = [torch.cuda.Event() for _ in layer]
-    ev_out = [torch.cuda.Event() for _ in layer]
+    ev_in, ev_head, ev_last = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
 
     def make_step(lay):
         gemms = [vw4.PreparedGemm(vw4.FMT_NVFP4, qd, sd, ts, M, stream=stream)
@@ -731,46 +766,58 @@ def run_e2e(vw4, layer, layer_b, device, steps, warmup, world):
         def step():
             s_in.wait_stream(stream)
             with torch.cuda.stream(s_in):
-                for j in range(len(lay)):
-                    dev_in[j].copy_(host_in[j], non_blocking=True)
-                    ev_in[j].record(s_in)
+                dev_in.copy_(host_in, non_blocking=True)
+                ev_in.record(s_in)
+            stream.wait_event(ev_in)
             for j in range(len(lay)):
-                stream.wait_event(ev_in[j])
-                gemms[j](dev_in[j], dev_out[j])  # on `stream`
-                ev_out[j].record(stream)
-                s_out.wait_event(ev_out[j])
-                with torch.cuda.stream(s_out):
-                    host_out[j].copy_(dev_out[j], non_blocking=True)
+                gemms[j](d_in[j], d_out[j])  # on `stream`
+                if j == last - 1:            # results 0 .. last-1 out, behind the last GEMM
+                    ev_head.record(stream)
+                    s_out.wait_event(ev_head)
+                    with torch.cuda.stream(s_out):
+                        host_out[:out_off[last]].copy_(dev_out[:out_off[last]],
+                                                       non_blocking=True)
+            ev_last.record(stream)
+            s_out.wait_event(ev_last)
+            with torch.cuda.stream(s_out):
+                host_out[out_off[last]:].copy_(dev_out[out_off[last]:], non_blocking=True)
             stream.wait_stream(s_out)
         return step
 
-    graphs = []
-    for lay in (layer, layer_b):
-        step = make_step(lay)
-        with torch.cuda.stream(stream):
-            for _ in range(warmup):
-                step()
-        torch.cuda.synchronize()
+    steps_ab = [make_step(layer), make_step(layer_b)]
+    with torch.cuda.stream(stream):
+        for i in range(max(warmup, 2)):
+            steps_ab[i % 2]()
+    torch.cuda.synchronize()
+
+    def capture(fn):
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gr, stream=stream):
-            step()
+            fn()
         torch.cuda.synchronize()
-        graphs.append(gr)
+        return gr
+
+    def two():
+        steps_ab[0]()
+        steps_ab[1]()
+    g_pair, g_one = capture(two), capture(steps_ab[0])
     with torch.cuda.stream(stream):  # replays run on the current stream: this one
-        for i in range(warmup):
-            graphs[i % 2].replay()
+        for _ in range((warmup + 1) // 2):
+            g_pair.replay()
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for i in range(steps):
-            graphs[i % 2].replay()
+        for _ in range(steps // 2):
+            g_pair.replay()
+        if steps % 2:
+            g_one.replay()
         e1.record(stream)
         torch.cuda.synchronize()
     ms = reduce_max(e0.elapsed_time(e1), world)
-    h2d = sum(M * K * 2 for _, N, K in STEP)
-    d2h = sum(M * N * 4 for _, N, K in STEP)
+    h2d = host_in.numel() * host_in.element_size()
+    d2h = host_out.numel() * host_out.element_size()
     value = step_bytes(M) * steps * world / (ms * 1e-3) / 1e9
     return {"value": round(value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h}
