@@ -74,6 +74,8 @@ typedef enum {
 #define VW4_DEV_WAIT_TIMEOUT   0x4u  /* a pipeline wait gave up; outputs are incomplete    */
 #define VW4_DEV_ZERO_RESIDUAL  0x8u  /* a forced rejection met p == q: drew from p instead */
 #define VW4_DEV_BAD_LIST_ID    0x10u /* a top-k list id outside [0, V): entry dropped      */
+#define VW4_DEV_BOUNDS         0x20u /* checks build only: an in-kernel bounds check failed;
+                                        the access was skipped (a library bug)            */
 
 /* A block-quantized weight matrix [N][K] (see the format notes above). */
 typedef struct vw4_weight {
@@ -534,6 +536,15 @@ VW4_API const char* vw4_last_error_string(void);
 
 /* Library version (major * 10000 + minor * 100 + patch). */
 VW4_API int vw4_version(void);
+
+/* How this copy of the library was built: VW4_BUILD_CHECKS is set in the
+ * checks build (compiled with -DVW4_CHECKS, libvw4_checks.so), whose kernels
+ * test the indexes that come from data -- the output row a MoE routing table
+ * names, the activation row a segment reads, the token ids an accept commits
+ * -- and report a failed test as VW4_DEV_BOUNDS instead of touching memory
+ * out of bounds.  Results are otherwise identical to the plain build. */
+#define VW4_BUILD_CHECKS 0x1
+VW4_API int vw4_build_flags(void);
 
 /* Test hook: upper bound, in nanoseconds, of every pipeline wait inside the
  * kernels (default 2e9).  A wait that runs out sets VW4_DEV_WAIT_TIMEOUT and

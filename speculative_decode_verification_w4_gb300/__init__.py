@@ -21,7 +21,11 @@ import threading
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libvw4.so")
+# the plain build; the checks build (in-kernel bounds checks, see vw4.h) sits
+# beside it.  VW4_LIB, when set, names the library that load_library() opens
+# by default (e.g. the checks build for a test run).
+LIB_CHECKS_PATH = os.path.join(_HERE, "libvw4_checks.so")
+LIB_PATH = os.environ.get("VW4_LIB") or os.path.join(_HERE, "libvw4.so")
 
 FMT_NVFP4 = 1
 FMT_Q4_0 = 2
@@ -35,6 +39,8 @@ DEV_BAD_EXPERT_ID = 0x2
 DEV_WAIT_TIMEOUT = 0x4
 DEV_ZERO_RESIDUAL = 0x8
 DEV_BAD_LIST_ID = 0x10
+DEV_BOUNDS = 0x20          # checks build only: an in-kernel bounds check failed
+BUILD_CHECKS = 0x1         # vw4_build_flags(): the checks build
 
 STATUS_NAMES = {0: "VW4_OK", 1: "VW4_ERR_INVALID_ARG", 2: "VW4_ERR_UNSUPPORTED",
                 3: "VW4_ERR_ALIGN", 4: "VW4_ERR_CUDA", 5: "VW4_ERR_TIMEOUT",
@@ -48,7 +54,8 @@ EXPORTS = ("verify_gemm_w4", "verify_moe_w4", "accept_greedy", "accept_rejection
            "vw4_depth_ctl_init",
            "vw4_depth_ctl_observe", "vw4_depth_ctl_expected", "vw4_depth_ctl_choose",
            "accept_rejection_topk", "vw4_rejection_row_records",
-           "vw4_test_inject_stall", "verify_gemm_w4_blockmax", "accept_rejection_blockmax")
+           "vw4_test_inject_stall", "verify_gemm_w4_blockmax", "accept_rejection_blockmax",
+           "vw4_build_flags")
 
 
 class VW4Error(RuntimeError):
@@ -91,7 +98,7 @@ def load_library(path: str = LIB_PATH):
         if _lib is not None:
             return _lib
         if not os.path.exists(path):
-            raise ImportError(f"libvw4.so not built at {path}: run "
+            raise ImportError(f"the vw4 library is not built at {path}: run "
                               "`python -m speculative_decode_verification_w4_gb300.build`")
         lib = ctypes.CDLL(path)
         P, I, U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64
@@ -110,6 +117,7 @@ def load_library(path: str = LIB_PATH):
             "vw4_status_str": (ctypes.c_char_p, [I]),
             "vw4_last_error_string": (ctypes.c_char_p, []),
             "vw4_version": (I, []),
+            "vw4_build_flags": (I, []),
             "vw4_set_wait_limit_ns": (None, [U64]),
             "vw4_own_exp": (I, [P, P, ctypes.c_int64, P]),
             "vw4_own_mass_pairs": (I, [P, P, ctypes.c_int64, P]),
@@ -519,6 +527,11 @@ def vw4_own_mass_pairs(x: torch.Tensor, out: torch.Tensor | None = None, stream=
     _check(load_library().vw4_own_mass_pairs(_ptr(x), _ptr(out), x.numel(), _stream(stream)),
            "vw4_own_mass_pairs")
     return out
+
+
+def vw4_build_flags() -> int:
+    """BUILD_CHECKS when the loaded library is the checks build."""
+    return int(load_library().vw4_build_flags())
 
 
 def vw4_set_wait_limit_ns(ns: int):

@@ -1,4 +1,6 @@
-"""Builds libvw4.so (the C-ABI CUDA library) in place for sm_103a.
+"""Builds libvw4.so (the C-ABI CUDA library) in place for sm_103a, and the
+checks build libvw4_checks.so (the same sources with -DVW4_CHECKS: in-kernel
+bounds checks that report through the device status word).
 
 Each translation unit is compiled by nvcc in parallel, then linked into one
 shared object next to this file.  Outputs are git-ignored.
@@ -17,6 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libvw4.so")
+BUILD_CHECKS = os.path.join(HERE, "_build_checks")
+LIB_CHECKS = os.path.join(HERE, "libvw4_checks.so")
 SOURCES = ["api.cu", "gemm_w4.cu", "accept.cu", "rejection.cu", "controller.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler",
@@ -37,16 +41,17 @@ def _stale(out: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra=None) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra=None, checks: bool = False) -> str:
+    build_dir, lib = (BUILD_CHECKS, LIB_CHECKS) if checks else (BUILD, LIB)
+    os.makedirs(build_dir, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     headers.append(os.path.join(INCLUDE, "vw4.h"))
     cc = nvcc()
-    extra = list(extra or [])
+    extra = list(extra or []) + (["-DVW4_CHECKS"] if checks else [])
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        o = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
         if force or _stale(o, [s] + headers):
             jobs.append([cc, *ARCH, *FLAGS, *extra, "-c", s, "-o", o])
     def run(cmd):
@@ -60,15 +65,22 @@ def build(force: bool = False, verbose: bool = False, extra=None) -> str:
         for msg in ex.map(run, jobs):
             if verbose and msg:
                 print(msg, file=sys.stderr)
-    objs = [os.path.join(BUILD, os.path.splitext(s)[0] + ".o") for s in SOURCES]
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    objs = [os.path.join(build_dir, os.path.splitext(s)[0] + ".o") for s in SOURCES]
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         run([cc, *ARCH, "-shared", "-o", tmp, *objs])
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
+
+
+def build_all(force: bool = False, verbose: bool = False):
+    """Both libraries, their translation units compiled side by side."""
+    with cf.ThreadPoolExecutor(max_workers=2) as ex:
+        libs = [ex.submit(build, force, verbose, None, c) for c in (False, True)]
+        return [f.result() for f in libs]
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose=True,
-          extra=["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else None)
-    print(LIB)
+    print(build(force="--force" in sys.argv, verbose=True,
+                extra=["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else None,
+                checks="--checks" in sys.argv))

@@ -127,6 +127,7 @@ __global__ void greedy_finish_kernel(const int32_t* __restrict__ drafts,
         if (x != g[i]) break;
         ++n;
     }
+    check(g[n] >= 0 && g[n] < V, status);  // the row argmax was found
     for (int i = 0; i <= Kd; ++i) {
         int32_t t = -1;
         if (i < n) t = drafts[static_cast<long long>(b) * Kd + i];

@@ -166,6 +166,8 @@ extern "C" {
 
 VW4_API int vw4_version(void) { return 100; }
 
+VW4_API int vw4_build_flags(void) { return kChecks ? VW4_BUILD_CHECKS : 0; }
+
 VW4_API const char* vw4_status_str(vw4_status s) {
     switch (s) {
         case VW4_OK: return "ok";
@@ -308,6 +310,7 @@ static vw4_status gemm_entry(const vw4_weight* W, const void* A_dev, int M, int 
     p.seg = ws.seg;
     p.act = ws.act;
     p.out = out_dev;
+    p.out_rows = M;
     p.ldo = ldo;
     p.dense_M = M;
     p.argmax_M = fused_argmax ? M : 0;
@@ -424,6 +427,7 @@ VW4_API vw4_status verify_moe_w4(const vw4_weight* experts, int E, const void* A
     p.seg = ws.seg;
     p.act = ws.act;
     p.out = combine ? ws.pair_out : out_dev;
+    p.out_rows = P;
     p.ldo = combine ? N : ldo;
     p.dense_M = 0;
     p.argmax_M = 0;

@@ -279,7 +279,8 @@ __global__ void __launch_bounds__(512) prep_act_kernel(
         count = lt.count[sgi];
         if (r < count) {
             const int pr = lt.dest[sgi][r];
-            src_row = rows_are_pairs ? pr : pr / topk;
+            if (check(pr >= 0 && pr < P, status)) src_row = rows_are_pairs ? pr : pr / topk;
+            else count = r;  // this row and the ones after it stay zero
         }
     }
     for (int st = st0; st < T; st += stage_ctas) {
@@ -680,6 +681,7 @@ __device__ void argmax_finish(const GemmParams& p, int lane) {
                 if (x != g[r0 + i]) break;
                 ++n;
             }
+            check(g[r0 + n] >= 0 && g[r0 + n] < p.N, p.status);  // the argmax was found
             for (int i = 0; i <= Kd; ++i)
                 p.tokens[r0 + i] = i < n ? d[i] : (i == n ? g[r0 + n] : -1);
             p.len[b] = n + 1;
@@ -1005,8 +1007,11 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                         const int tok = 8 * nt + 2 * c + (q & 1);
                         const int n = n0 + wrow + rb * 16 + g + ((q & 2) ? 8 : 0);
                         if (n < p.N) {
-                            if (tok < count && p.out != nullptr)
-                                p.out[static_cast<size_t>(dest_of(tok)) * p.ldo + n] = v[rb][nt][q];
+                            if (tok < count && p.out != nullptr) {
+                                const int dr = dest_of(tok);
+                                if (check(dr >= 0 && dr < p.out_rows, p.status))
+                                    p.out[static_cast<size_t>(dr) * p.ldo + n] = v[rb][nt][q];
+                            }
                             const unsigned long long k =
                                 am_key(v[rb][nt][q], static_cast<uint32_t>(n));
                             if (q & 1) kr1[rb] = umax64(kr1[rb], k);
@@ -1128,13 +1133,15 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             // keys of the slice's first and second 16 rows
             unsigned long long kb0 = 0ull, kb1 = 0ull;
             if (tok < count) {
-                float* orow =
-                    p.out != nullptr ? p.out + static_cast<size_t>(dest_of(tok)) * p.ldo : nullptr;
+                const int dr = dest_of(tok);
+                float* orow = p.out != nullptr && check(dr >= 0 && dr < p.out_rows, p.status)
+                                  ? p.out + static_cast<size_t>(dr) * p.ldo
+                                  : nullptr;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const int n = n0 + rr + (j & 3) + ((j & 4) ? 16 : 0);
                     if (n < p.N) {
-                        if (p.out != nullptr) orow[n] = sv[j];
+                        if (orow != nullptr) orow[n] = sv[j];
                         const unsigned long long k = am_key(sv[j], static_cast<uint32_t>(n));
                         if (j & 4) kb1 = umax64(kb1, k);
                         else kb0 = umax64(kb0, k);

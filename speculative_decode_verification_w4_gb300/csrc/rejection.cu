@@ -2070,7 +2070,10 @@ __device__ void seq_finish(DrawRow& w, u128 R, ulonglong2* ssum, const int32_t* 
                 tok = __shfl_sync(0xffffffffu, tok, L);
             }
         }
-        if (lane == 0) sm.token = tok >= 0 ? tok : V - 1;
+        if (lane == 0) {
+            if (tok >= 0) check(tok < V, status);  // the drawn entry lies in the row
+            sm.token = tok >= 0 ? tok : V - 1;
+        }
     }
     __syncthreads();
     if (tid <= Kd) {
@@ -2723,6 +2726,7 @@ __global__ void __launch_bounds__(kListSeqWarps * 32) list_seq_kernel(
         }
         tok = __shfl_sync(0xffffffffu, found, L);
     }
+    if (lane == 0) check(tok >= 0 && tok < V, status);  // the drawn id lies in the vocabulary
     for (int i = lane; i <= Kd; i += 32) {
         int32_t tk = -1;
         if (i < n) tk = drafts[static_cast<long long>(b) * Kd + i];

@@ -24,6 +24,24 @@ inline cudaError_t set_attribute_per_device(std::atomic<unsigned long long>& onc
     return e;
 }
 
+// In-kernel bounds checks, compiled in by -DVW4_CHECKS (the checks build):
+// check(ok, status) records a failed check in the device status word
+// (VW4_DEV_BOUNDS) and returns false, so that the caller skips the access.
+// In other builds it returns true and the test compiles away.
+constexpr uint32_t kStatusBounds = 0x20u;
+#ifdef VW4_CHECKS
+constexpr bool kChecks = true;
+#else
+constexpr bool kChecks = false;
+#endif
+__device__ __forceinline__ bool check(bool ok, uint32_t* status) {
+    if (kChecks && !ok) {
+        atomicOr(status, kStatusBounds);
+        return false;
+    }
+    return true;
+}
+
 constexpr int kMaxRows = 8;        // rows of one mma n-tile; verify rows per MoE segment
 constexpr int kMaxVerifyRows = 16; // dense verify rows per call: two n-tiles
 constexpr int kMaxSeg = 128;       // routed (token, expert) pairs per call: 16 tokens x top-8
@@ -113,6 +131,7 @@ struct GemmParams {
     const uint8_t* act;
     float* out;
     int ldo;
+    int out_rows;                 // rows of out: the verify rows, or the routed pairs
     int dense_M;                  // > 0: one dense segment of dense_M rows (no table reads)
     int argmax_M;                 // 0 = no fused argmax
     float* partials;

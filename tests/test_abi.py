@@ -34,6 +34,21 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(raw, name), name
 
 
+def test_checks_build_exports_every_declared_symbol_and_says_so(lib):
+    """The checks build (-DVW4_CHECKS: in-kernel bounds checks) compiles for
+    sm_103a, exports every declared symbol, and reports its flag; the plain
+    build reports none."""
+    path = vbuild.build(checks=True)
+    raw = ctypes.CDLL(path)
+    for name in declared_symbols():
+        assert hasattr(raw, name), name
+    raw.vw4_build_flags.restype = ctypes.c_int
+    assert raw.vw4_build_flags() == vw4.BUILD_CHECKS
+    plain = ctypes.CDLL(vbuild.LIB)
+    plain.vw4_build_flags.restype = ctypes.c_int
+    assert plain.vw4_build_flags() == 0
+
+
 def test_status_strings(lib):
     assert lib.vw4_status_str(0) == b"ok"
     assert lib.vw4_status_str(6) == b"workspace too small"
