@@ -930,7 +930,8 @@ def run_case(case: str, device):
     rejection accept of the stochastic sweep (B = 256, V = 151936, K drafts),
     4 calls; 'lists:K' = the accept over top-64 lists of those rows, 4 calls;
     'moe:M' = the MoE head (gate/up, then down with the gate combine) at M
-    tokens, 4 calls."""
+    tokens, 4 calls; 'sampled:K' = one sequence's rejection accept with K
+    drafts over 262144-entry rows of the LM head's logit spread, 4 calls."""
     import torch
     import speculative_decode_verification_w4_gb300 as vw4
     torch.cuda.set_device(device)
@@ -967,6 +968,20 @@ def run_case(case: str, device):
                                                 workspace=ws)
         torch.cuda.synchronize()
         print(f"case {case}: 4 calls, mean run {ln.float().mean().item():.3f}, device status "
+              f"{vw4.vw4_get_device_status()}", flush=True)
+        return
+    if case.startswith("sampled:"):  # one sequence's rejection accept at the LM head's width
+        Kd, V = int(case.split(":")[1]), 262144
+        g = torch.Generator(device=device).manual_seed(5)
+        # logits of the LM head's spread: N(0, 0.02^2 * 5376) per entry
+        tgt = torch.randn((1, Kd + 1, V), generator=g, device=device) * 1.466
+        drf = torch.randn((1, Kd, V), generator=g, device=device) * 1.466
+        drafts = torch.multinomial(torch.softmax(drf.reshape(-1, V) / 0.6, dim=-1), 1,
+                                   generator=g).reshape(1, Kd).to(torch.int32)
+        for r in range(4):
+            tok, ln = vw4.accept_rejection(tgt, drf, drafts, 0.6, 0.95, 4, r, workspace=ws)
+        torch.cuda.synchronize()
+        print(f"case {case}: 4 calls, run {ln.item()}, device status "
               f"{vw4.vw4_get_device_status()}", flush=True)
         return
     if case.startswith("moe:"):  # the MoE head (gate/up then down with the combine), M tokens
@@ -1029,7 +1044,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--case", default=None,
-                    help="profiling helper: 'dense', 'N,K,M[,q4_0]', 'rejection:K', 'lists:K' or 'moe:M' (see run_case); "
+                    help="profiling helper: 'dense', 'N,K,M[,q4_0]', 'rejection:K', 'lists:K', 'moe:M' or 'sampled:K' (see run_case); "
                          "no JSON line")
     args = ap.parse_args()
     if args.warmup < 3:

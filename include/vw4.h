@@ -74,8 +74,9 @@ typedef enum {
 #define VW4_DEV_WAIT_TIMEOUT   0x4u  /* a pipeline wait gave up; outputs are incomplete    */
 #define VW4_DEV_ZERO_RESIDUAL  0x8u  /* a forced rejection met p == q: drew from p instead */
 #define VW4_DEV_BAD_LIST_ID    0x10u /* a top-k list id outside [0, V): entry dropped      */
-#define VW4_DEV_BOUNDS         0x20u /* checks build only: an in-kernel bounds check failed;
-                                        the access was skipped (a library bug)            */
+#define VW4_DEV_BOUNDS         0x20u /* checks build only: an index that came from data was
+                                        out of range (a library bug): a memory access it
+                                        addressed was skipped; a token id is still written */
 
 /* A block-quantized weight matrix [N][K] (see the format notes above). */
 typedef struct vw4_weight {
@@ -541,8 +542,9 @@ VW4_API int vw4_version(void);
  * checks build (compiled with -DVW4_CHECKS, libvw4_checks.so), whose kernels
  * test the indexes that come from data -- the output row a MoE routing table
  * names, the activation row a segment reads, the token ids an accept commits
- * -- and report a failed test as VW4_DEV_BOUNDS instead of touching memory
- * out of bounds.  Results are otherwise identical to the plain build. */
+ * -- and report a failed test as VW4_DEV_BOUNDS: an out-of-range row is not
+ * touched, an out-of-range token id is flagged.  Results are otherwise
+ * identical to the plain build. */
 #define VW4_BUILD_CHECKS 0x1
 VW4_API int vw4_build_flags(void);
 
