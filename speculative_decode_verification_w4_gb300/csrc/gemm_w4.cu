@@ -388,10 +388,22 @@ __device__ __forceinline__ void cvt_e4m3x4(uint32_t w, uint32_t& lo, uint32_t& h
         : "r"(w));
 }
 
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
+__device__ __forceinline__ __half2 as_half2(uint32_t u) {
+    __half2 h;
+    memcpy(&h, &u, 4);
+    return h;
+}
+__device__ __forceinline__ uint32_t as_u32(__half2 h) {
+    uint32_t u;
+    memcpy(&u, &h, 4);
+    return u;
+}
+// a * s, s one block scale in both halves.  Written as an f16x2 multiply by
+// a half broadcast (not a byte-permuted register) so that the broadcast
+// becomes the multiply's operand selection: 16 fewer instructions a warp and
+// stage, and 1-3 % off the call time.
+__device__ __forceinline__ uint32_t hmul2_bcast(uint32_t a, __half2 s) {
+    return as_u32(__hmul2(as_half2(a), s));
 }
 __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
     uint32_t d;
@@ -493,10 +505,9 @@ __device__ __forceinline__ void compute_nvfp4(const ActRegs (&a)[NT], const WReg
     uint32_t sa0, sb0, sa1, sb1;
     cvt_e4m3x4(r.s0, sa0, sb0);
     cvt_e4m3x4(r.s1, sa1, sb1);
-    const uint32_t sc0[4] = {__byte_perm(sa0, sa0, 0x1010), __byte_perm(sa0, sa0, 0x3232),
-                             __byte_perm(sb0, sb0, 0x1010), __byte_perm(sb0, sb0, 0x3232)};
-    const uint32_t sc1[4] = {__byte_perm(sa1, sa1, 0x1010), __byte_perm(sa1, sa1, 0x3232),
-                             __byte_perm(sb1, sb1, 0x1010), __byte_perm(sb1, sb1, 0x3232)};
+    const __half2 A0 = as_half2(sa0), B0 = as_half2(sb0), A1 = as_half2(sa1), B1 = as_half2(sb1);
+    const __half2 sc0[4] = {__low2half2(A0), __high2half2(A0), __low2half2(B0), __high2half2(B0)};
+    const __half2 sc1[4] = {__low2half2(A1), __high2half2(A1), __low2half2(B1), __high2half2(B1)};
     const uint32_t wr0[8] = {r.w00.x, r.w00.y, r.w00.z, r.w00.w, r.w01.x, r.w01.y, r.w01.z, r.w01.w};
     const uint32_t wr1[8] = {r.w10.x, r.w10.y, r.w10.z, r.w10.w, r.w11.x, r.w11.y, r.w11.z, r.w11.w};
 #pragma unroll
@@ -504,11 +515,11 @@ __device__ __forceinline__ void compute_nvfp4(const ActRegs (&a)[NT], const WReg
         uint32_t h0, h1, h2, h3, q0, q1, q2, q3;
         cvt_e2m1x8(wr0[wi], h0, h1, h2, h3);
         cvt_e2m1x8(wr1[wi], q0, q1, q2, q3);
-        const uint32_t s0 = sc0[wi >> 1], s1 = sc1[wi >> 1];
-        const uint32_t e0 = hmul2(h0, s0), e1 = hmul2(q0, s1), e2 = hmul2(h1, s0),
-                       e3 = hmul2(q1, s1);
-        const uint32_t o0 = hmul2(h2, s0), o1 = hmul2(q2, s1), o2 = hmul2(h3, s0),
-                       o3 = hmul2(q3, s1);
+        const __half2 s0 = sc0[wi >> 1], s1 = sc1[wi >> 1];
+        const uint32_t e0 = hmul2_bcast(h0, s0), e1 = hmul2_bcast(q0, s1),
+                       e2 = hmul2_bcast(h1, s0), e3 = hmul2_bcast(q1, s1);
+        const uint32_t o0 = hmul2_bcast(h2, s0), o1 = hmul2_bcast(q2, s1),
+                       o2 = hmul2_bcast(h3, s0), o3 = hmul2_bcast(q3, s1);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const uint4& b = a[nt].bf[wi];
