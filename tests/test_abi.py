@@ -49,6 +49,25 @@ def test_checks_build_exports_every_declared_symbol_and_says_so(lib):
     assert plain.vw4_build_flags() == 0
 
 
+def test_vw4_lib_selects_the_library_the_binding_opens(lib):
+    """VW4_LIB names the library load_library() opens by default: the checks
+    build when it points there, the plain build otherwise (host calls only)."""
+    import subprocess
+    import sys
+    checks = vbuild.build(checks=True)
+    code = ("import speculative_decode_verification_w4_gb300 as v; "
+            "print(v.LIB_PATH, v.vw4_build_flags())")
+    env = {k: val for k, val in os.environ.items() if k != "VW4_LIB"}
+    plain = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env,
+                           capture_output=True, text=True, timeout=300)
+    assert plain.returncode == 0, plain.stderr[-2000:]
+    assert plain.stdout.split() == [vbuild.LIB, "0"], plain.stdout
+    chk = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=dict(env, VW4_LIB=checks),
+                         capture_output=True, text=True, timeout=300)
+    assert chk.returncode == 0, chk.stderr[-2000:]
+    assert chk.stdout.split() == [checks, str(vw4.BUILD_CHECKS)], chk.stdout
+
+
 def test_status_strings(lib):
     assert lib.vw4_status_str(0) == b"ok"
     assert lib.vw4_status_str(6) == b"workspace too small"
